@@ -1,0 +1,300 @@
+"""fp64 CPU oracle of the top-1 Switch MoE layer forward pass.
+
+TEST INFRASTRUCTURE.  Only tests/, __graft_entry__.smoke() and bench.py's CPU
+baseline (and its --impl reference arm) may import or run this module.  The
+CUDA library never imports it, and it imports nothing from the library: the two
+share no code.  It is deliberately plain and slow: NumPy in float64, one
+library matmul per linear map, and pure-Python loops where the pages define a
+step as a sequential count.
+
+Pages cited (title, then the section / equation / table):
+  [042]  "042 · Switch Transformer：每个词只选一个专家" (wq-win.github.io)
+  [card] "Switch Transformers: Scaling to Trillion Parameter Models with Simple
+         and Efficient Sparsity - 中文验证版" (ai-papers.xuzou.cn)
+  [moe]  "混合专家" (world.lapla.si/zh/moe)
+  [070]  "开源 AI 论文复现实验与代码解读 · 070" on MoE routing load collapse
+         (zffjzz.top)
+
+Readings taken where the pages leave a step open (each is listed in the design doc):
+  * argmax is taken over the logits z (softmax is monotone); ties go to the
+    lowest expert index, the NumPy rule [070, 核心思想与公式].
+  * capacity C = ceil(c*T/E), with c*T/E snapped to an integer when it is within
+    1e-9 of one, so that 1.1*100/10 gives 11 [070, 核心思想与公式; 042, §一].
+  * f counts choices BEFORE capacity truncation [070, 核心思想与公式].
+  * alpha sits inside the loss: L = alpha*E*sum_i f_i P_i [042, §二]; the
+    unweighted E*sum f P is returned too.
+  * with several routing groups, each group has its own capacity, slots and
+    statistics, and the aux loss is the mean over groups [070, 评测协议].
+  * the dispatched buffer packs each expert's kept tokens group by group, in
+    sequence order: row = (kept tokens of that expert in earlier groups) + slot.
+  * y excludes the residual; a dropped token's expert output is exactly 0
+    [042, §一; 070, 核心思想与公式 (the m_t mask)].
+
+Every function here is pinned by tests/test_oracle_pins.py against values the
+pages print, closed forms, a dense one-hot einsum formulation [card, 方法适配]
+and brute force on tiny inputs.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+
+def capacity(capacity_factor: float, T: int, E: int, override: int = 0) -> int:
+    """Expert capacity per routing group.
+
+    [042, §一]: C is about (T/E)*c; [070, 核心思想与公式] fixes the rounding
+    as C = ceil(c*T/E).  `override` > 0 replaces the rule (used to pin the
+    [28,12,12,12] -> [8,8,8,8] truncation example).
+    """
+    if override > 0:
+        return int(override)
+    if T <= 0 or E <= 0:
+        return 0
+    v = float(capacity_factor) * T / E
+    r = round(v)
+    if abs(v - r) <= 1e-9:
+        return int(r)
+    return int(math.ceil(v))
+
+
+def router_logits(x: np.ndarray, Wr: np.ndarray, br: Optional[np.ndarray] = None) -> np.ndarray:
+    """z_t = W_r x_t (+ b_r), in float64 from the exact input values.
+
+    [042, §一]: p(x) = softmax(W_r x); [070, 核心思想与公式]: Z = X W with W
+    of shape [d, E]; here W_r is stored [E, d], so Z = X W_r^T.  The router
+    input is cast up before the product [card, 方法适配 (selective precision)].
+    """
+    z = np.asarray(x, dtype=np.float64) @ np.asarray(Wr, dtype=np.float64).T
+    if br is not None:
+        z = z + np.asarray(br, dtype=np.float64)[None, :]
+    return z
+
+
+def softmax(z: np.ndarray) -> np.ndarray:
+    """Row softmax of the router logits, computed as exp(z - max z) / sum."""
+    m = z.max(axis=-1, keepdims=True)
+    e = np.exp(z - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def top1(z: np.ndarray) -> np.ndarray:
+    """e*(x) = argmax_e, first maximal index on ties [042, §一; 070, 核心思想与公式]."""
+    return np.argmax(z, axis=-1).astype(np.int64)
+
+
+def assign_slots(a: Sequence[int], E: int, C: int):
+    """Slot of each token inside its expert, in sequence order, and the capacity mask.
+
+    [070, 官方代码阅读路线]: positions come from a cumulative count along the
+    sequence, not from an ordering by probability.  Token t's slot is the number
+    of earlier tokens of the same group that chose the same expert; the token is
+    kept when slot < C [042, §一 (overflow tokens skip the expert)].
+
+    Returns slot [T], keep [T] (bool), raw [E] (choices before truncation) and
+    accepted [E] = min(raw, C).
+    """
+    counts = [0] * E
+    T = len(a)
+    slot = np.empty(T, dtype=np.int64)
+    for t in range(T):
+        e = int(a[t])
+        slot[t] = counts[e]
+        counts[e] += 1
+    raw = np.asarray(counts, dtype=np.int64)
+    keep = slot < C
+    accepted = np.minimum(raw, C)
+    return slot, keep, raw, accepted
+
+
+def load_balance(a: np.ndarray, p: np.ndarray, E: int, alpha: float):
+    """f_i, P_i and the auxiliary loss of one routing group.
+
+    [042, §二]: L_aux = alpha * E * sum_e f_e P_e with f_e = (1/T) sum_x 1[e*(x)=e]
+    and P_e = (1/T) sum_x p_e(x).  f uses the hard choices before capacity
+    truncation [070, 核心思想与公式].
+    Returns f [E], P [E], the unweighted term E*sum f P, and alpha times it.
+    """
+    T = len(a)
+    f = np.bincount(np.asarray(a, dtype=np.int64), minlength=E).astype(np.float64) / T
+    P = p.mean(axis=0)
+    unweighted = E * float(np.sum(f * P))
+    return f, P, unweighted, alpha * unweighted
+
+
+@dataclasses.dataclass
+class Route:
+    C: int
+    logits: np.ndarray       # [N, E] float64 (or the substituted logits)
+    probs: np.ndarray        # [N, E]
+    expert: np.ndarray       # [N] raw choice, also for dropped tokens
+    gate: np.ndarray         # [N] p_{t, expert_t}
+    slot: np.ndarray         # [N]
+    keep: np.ndarray         # [N] bool
+    row: np.ndarray          # [N] row in the expert's block of xe, -1 if dropped
+    raw: np.ndarray          # [G, E]
+    accepted: np.ndarray     # [G, E]
+    f: np.ndarray            # [G, E]
+    P: np.ndarray            # [G, E]
+    balance: np.ndarray      # [G] unweighted E * sum f P
+    aux_per_group: np.ndarray  # [G] alpha * balance
+    aux_loss: float          # mean over groups
+    expert_rows: np.ndarray  # [E] kept tokens per expert, all groups
+
+    @property
+    def overflow(self) -> int:
+        return int((~self.keep).sum())
+
+
+def route(x, Wr, br, G: int, T: int, E: int, capacity_factor: float, alpha: float = 1e-2,
+          capacity_override: int = 0, logits_override: Optional[dict] = None) -> Route:
+    """Router, top-1 choice, slots, capacity mask and load statistics per group.
+
+    Steps in the order of the pipeline in [042, §三]: router probabilities in
+    float (here float64), one expert per token, load statistics and aux loss,
+    then capacity truncation.  `logits_override` maps a group index to a [T, E]
+    array of logits to use for that group instead of the float64 ones (used
+    when the GPU's float32 logits sit within 1e-6 of a tie).
+    """
+    x = np.asarray(x)
+    N = G * T
+    assert x.shape[0] == N
+    C = capacity(capacity_factor, T, E, capacity_override)
+    z = router_logits(x, Wr, br)
+    if logits_override:
+        z = z.copy()
+        for g, zg in logits_override.items():
+            z[g * T:(g + 1) * T] = np.asarray(zg, dtype=np.float64)
+    p = softmax(z) if N > 0 else np.zeros((0, E))
+    a = top1(z) if N > 0 else np.zeros(0, dtype=np.int64)
+    gate = p[np.arange(N), a] if N > 0 else np.zeros(0)
+
+    slot = np.empty(N, dtype=np.int64)
+    keep = np.empty(N, dtype=bool)
+    raw = np.zeros((G, E), dtype=np.int64)
+    accepted = np.zeros((G, E), dtype=np.int64)
+    f = np.zeros((G, E))
+    P = np.zeros((G, E))
+    balance = np.zeros(G)
+    aux = np.zeros(G)
+    for g in range(G):
+        sl = slice(g * T, (g + 1) * T)
+        slot[sl], keep[sl], raw[g], accepted[g] = assign_slots(a[sl], E, C)
+        if T > 0:
+            f[g], P[g], balance[g], aux[g] = load_balance(a[sl], p[sl], E, alpha)
+
+    # Row of each kept token in its expert's block: kept tokens of the same
+    # expert in earlier groups come first, then this group's slot.
+    row = np.full(N, -1, dtype=np.int64)
+    before = np.zeros(E, dtype=np.int64)
+    for g in range(G):
+        for t in range(g * T, (g + 1) * T):
+            if keep[t]:
+                row[t] = before[a[t]] + slot[t]
+        before += accepted[g]
+    return Route(C=C, logits=z, probs=p, expert=a, gate=gate, slot=slot, keep=keep, row=row,
+                 raw=raw, accepted=accepted, f=f, P=P, balance=balance, aux_per_group=aux,
+                 aux_loss=float(aux.mean()) if G > 0 else 0.0, expert_rows=accepted.sum(axis=0))
+
+
+def dispatch(x, r: Route, E: int, G: int) -> np.ndarray:
+    """Gather kept tokens into the per-expert buffer xe [E, G*C, d] (float64).
+
+    [042, §三] builds dispatch tensors after capacity truncation; [card,
+    方法适配] writes the dispatch as a one-hot tensor over (tokens, experts,
+    capacity), so unused slots hold zeros.  Here each expert's block holds its
+    kept tokens group by group in sequence order (see module header).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[1]
+    xe = np.zeros((E, G * r.C, d))
+    for t in range(x.shape[0]):
+        if r.keep[t]:
+            xe[r.expert[t], r.row[t]] = x[t]
+    return xe
+
+
+def expert_ffn(xrows, W1, b1, W2, b2) -> np.ndarray:
+    """One expert's FFN on rows: ReLU(x W1^T + b1) W2^T + b2, float64.
+
+    [moe, 专家里面是什么]: an expert is an ordinary feed-forward block, d ->
+    d_ff with negatives set to 0, then back to d; its parameter count
+    (48*32+32+32*48+48 = 3,152) shows both layers carry a bias.
+    W1 is stored [d_ff, d] and W2 [d, d_ff].
+    """
+    xr = np.asarray(xrows, dtype=np.float64)
+    h = xr @ np.asarray(W1, dtype=np.float64).T
+    if b1 is not None:
+        h = h + np.asarray(b1, dtype=np.float64)[None, :]
+    h = np.maximum(h, 0.0)
+    o = h @ np.asarray(W2, dtype=np.float64).T
+    if b2 is not None:
+        o = o + np.asarray(b2, dtype=np.float64)[None, :]
+    return o
+
+
+def expert_outputs(x, r: Route, W1, b1, W2, b2, tokens: Optional[Sequence[int]] = None) -> dict:
+    """Ungated expert output o_t = f_{e*(t)}(x_t) for kept tokens (or the given subset)."""
+    x = np.asarray(x)
+    idx = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    idx = idx[r.keep[idx]]
+    out = {}
+    for e in np.unique(r.expert[idx]):
+        sel = idx[r.expert[idx] == e]
+        o = expert_ffn(x[sel], W1[e], None if b1 is None else b1[e],
+                       W2[e], None if b2 is None else b2[e])
+        for i, t in enumerate(sel):
+            out[int(t)] = o[i]
+    return out
+
+
+def combine(r: Route, outputs: dict, tokens: Sequence[int], d: int) -> np.ndarray:
+    """y_t = p_{e*}(x_t) * f_{e*}(x_t) for kept tokens, 0 for dropped ones.
+
+    [042, §一]: y = p_{e*(x)}(x) f_{e*(x)}(x); the selected gate multiplies the
+    expert output un-renormalised ([042] "只执行一个专家时检查路由是否被错误归一化":
+    a gate of 0.7 stays 0.7).  Dropped tokens get zero expert output and carry
+    on through the residual, which is outside y [042, §一].
+    """
+    y = np.zeros((len(tokens), d))
+    for i, t in enumerate(tokens):
+        if r.keep[t]:
+            y[i] = r.gate[t] * outputs[int(t)]
+    return y
+
+
+def forward(x, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor: float,
+            alpha: float = 1e-2, capacity_override: int = 0,
+            tokens: Optional[Sequence[int]] = None, logits_override: Optional[dict] = None):
+    """The whole layer: route, then expert FFN and combine on `tokens` (default: all).
+
+    Returns (route, y[tokens], ungated expert outputs by token).
+    """
+    r = route(x, Wr, br, G, T, E, capacity_factor, alpha, capacity_override, logits_override)
+    N = G * T
+    toks = np.arange(N) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    outs = expert_outputs(x, r, W1, b1, W2, b2, toks)
+    y = combine(r, outs, toks, np.asarray(x).shape[1])
+    return r, y, outs
+
+
+def ties_within(z: np.ndarray, eps: float) -> np.ndarray:
+    """Per token: True when the two largest logits differ by at most eps."""
+    if z.shape[1] < 2:
+        return np.zeros(z.shape[0], dtype=bool)
+    top2 = np.partition(z, -2, axis=1)[:, -2:]
+    return (top2[:, 1] - top2[:, 0]) <= eps
+
+
+def groups_with_near_ties(z_list: List[np.ndarray], G: int, T: int, eps: float = 1e-6) -> List[int]:
+    """Groups in which any token's top-two logits (in any of the given logit
+    arrays) lie within eps; such groups are routed from the GPU's own logits."""
+    out = []
+    for g in range(G):
+        sl = slice(g * T, (g + 1) * T)
+        if any(ties_within(np.asarray(z, dtype=np.float64)[sl], eps).any() for z in z_list):
+            out.append(g)
+    return out
