@@ -1,0 +1,367 @@
+"""Benchmark of the top-1 Switch MoE layer forward pass on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one switch_forward (router, top-1, slots, capacity mask, statistics,
+aux loss, dispatch, expert FFN, combine) over one batch of synthetic tokens
+already resident in HBM.  The default workload is the Switch-Base-shaped layer
+(d_model 768, d_ff 3072, 128 experts, capacity factor 1.0, one routing group of
+8192 tokens = 16 sequences x 512).  Prints one JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle on this host instead (a bounded
+sample of the same workload), and prints the same line with "impl": "reference".
+Under torchrun every rank processes its own batch (weak scaling: routing groups
+are independent); ranks share nothing on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gen import WORKLOADS, make_inputs, workload_seed  # noqa: E402
+
+METRIC = "Switch top-1 MoE layer fwd tokens/s on 1 B300; % TC peak; dispatch HBM GB/s"
+DEFAULT_WORKLOAD = "switch-base-e128"
+L2_FLUSH_BYTES = 256 << 20  # > 126 MB L2
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks during the timed region
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        top = max(sm)
+        loaded = [s for s in sm if s >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- algorithmic work per launch
+def algorithmic(shape, expert_rows: np.ndarray, N: int):
+    """Bytes / FLOPs each stage must move or do (kept rows only, experts with tokens only)."""
+    d, F, E = shape.d_model, shape.d_ff, shape.E
+    es = 4 if shape.dtype == "f32" else 2
+    K = int(expert_rows.sum())
+    used = int((expert_rows > 0).sum())
+    R = expert_rows.size and None
+    w_bytes = used * F * d * es
+    out = {
+        "kept_rows": K,
+        "experts_used": used,
+        # route: read x and W_r, write 13 B of per-token records + [E] stats
+        "route_bytes": N * d * es + E * d * 4 + N * 13,
+        # dispatch: read kept rows, write every row of the expert blocks (kept + zeroed)
+        "dispatch_bytes": K * d * es,
+        "ffn1_bytes": w_bytes + K * d * es + K * F * es,
+        "ffn2_bytes": w_bytes + K * F * es + K * d * es,
+        "ffn1_flops": 2.0 * K * d * F,
+        "ffn2_flops": 2.0 * K * d * F,
+        # combine: read kept rows of ye, write all N rows of y
+        "combine_bytes": K * d * es + N * d * es,
+        "router_flops": 2.0 * N * d * E,
+    }
+    return out
+
+
+def traffic_from_profiles(kernel: str):
+    """DRAM bytes per launch recorded by an ncu capture (profiles/ncu_traffic.json),
+    or None when the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)[kernel]
+        src = os.path.join(ROOT, "sparse_mixture_experts_slots_b300", "csrc", rec["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if h != rec["source_sha256_16"]:
+            return None
+        return rec
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+def oracle_sample(shape, inp, n_ffn_tokens: int):
+    """Time the fp64 oracle: routing of the whole batch + the expert FFN of a
+    sample of kept tokens, scaled to the batch.  Returns (tokens/s, detail)."""
+    from oracle import switch_oracle as so
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = os.cpu_count()
+    x = inp["x"].float().cpu().numpy().astype(np.float64)
+    Wr = inp["Wr"].cpu().numpy().astype(np.float64)
+    br = None if inp["br"] is None else inp["br"].cpu().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    r = so.route(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor)
+    t_route = time.perf_counter() - t0
+    kept = np.flatnonzero(r.keep)
+    rng = np.random.default_rng(0)
+    sample = np.sort(rng.choice(kept, size=min(n_ffn_tokens, kept.size), replace=False))
+    experts = np.unique(r.expert[sample])
+    W1 = {int(e): inp["W1"][int(e)].float().cpu().numpy().astype(np.float64) for e in experts}
+    W2 = {int(e): inp["W2"][int(e)].float().cpu().numpy().astype(np.float64) for e in experts}
+    t0 = time.perf_counter()
+    for e in experts:
+        ts = sample[r.expert[sample] == e]
+        o = so.expert_ffn(x[ts], W1[int(e)], None, W2[int(e)], None)
+        _ = r.gate[ts, None] * o
+    t_ffn = time.perf_counter() - t0
+    t_total = t_route + t_ffn * kept.size / max(1, sample.size)
+    return shape.N / t_total, {
+        "cores": threads,
+        "sample": (f"routing of all {shape.N} tokens + expert FFN/combine of {sample.size} of {kept.size} kept "
+                   f"tokens, FFN time scaled by {kept.size}/{sample.size}"),
+        "t_route_s": t_route, "t_ffn_sample_s": t_ffn}
+
+
+def run_reference(args, shape):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = make_inputs(shape, workload_seed(args.workload), "cpu")
+    vals = []
+    detail = {}
+    for i in range(args.warmup + args.steps):
+        v, detail = oracle_sample(shape, inp, args.ref_ffn_tokens)
+        if i >= args.warmup:
+            vals.append(v)
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * shape.N / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(shape, args),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": detail["cores"], "kind": "oracle",
+                         "sample": detail["sample"]},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(shape, args):
+    return {"workload": shape.name, "G": shape.G, "T": shape.T, "d_model": shape.d_model, "d_ff": shape.d_ff,
+            "E": shape.E, "capacity_factor": shape.capacity_factor, "top_k": 1,
+            "global_batch_tokens": shape.N * args.gpus, "parallelism": f"replicas{args.gpus}",
+            "l2": "flushed (256 MB write) before every timed step; expert weights (>1 GB) exceed L2 anyway"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, shape):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from sparse_mixture_experts_slots_b300 import SwitchMoE
+
+    seed = workload_seed(args.workload)
+    inp = make_inputs(shape, seed, dev)
+    if world > 1:  # each rank routes its own batch; the expert weights are replicated
+        inp["x"] = make_inputs(shape, seed + 7919 * rank, dev, with_experts=False)["x"]
+    dt = torch.float32 if shape.dtype == "f32" else torch.bfloat16
+    layer = SwitchMoE(shape.G, shape.T, shape.d_model, shape.d_ff, shape.E, shape.capacity_factor, dtype=dt,
+                      profile=True, device=dev)
+    r = layer.alloc_route()
+    y = torch.empty(shape.N, shape.d_model, dtype=dt, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        layer.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], r=r, y=y,
+                      stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    layer.sync_status(stream)
+    torch.cuda.synchronize(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    stage_sum = np.zeros(5)
+    launches = 0
+    clocks = ClockSampler(dev.index)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        launches += layer.last_launch_count()
+        stage_sum += np.array(layer.stage_ms())  # synchronises on the step's last event
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = float(sum(step_ms))
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    layer.sync_status(stream)
+
+    # ---------------- end to end through the public API: pinned host x in, y + aux loss out
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty(shape.N, shape.d_model, dtype=dt).pin_memory()
+    aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1.0)
+        if i >= args.warmup:
+            e2e_ev[i - args.warmup][0].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev, inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], r=r, y=y,
+                      stream=stream)
+        y_host.copy_(y, non_blocking=True)
+        aux_host.copy_(r.aux_loss, non_blocking=True)
+        if i >= args.warmup:
+            e2e_ev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    # ---------------- roofline of the dominant kernel
+    hbm, tc_burst, tc_sust, peak_src = peaks()
+    rows = r.expert_rows.cpu().numpy()
+    work = algorithmic(shape, rows, shape.N)
+    stage_avg = stage_sum / args.steps  # ms: route, dispatch, ffn1, ffn2, combine
+    names = ["route", "dispatch", "ffn1", "ffn2", "combine"]
+    stage_bytes = [work["route_bytes"], work["dispatch_bytes"], work["ffn1_bytes"], work["ffn2_bytes"],
+                   work["combine_bytes"]]
+    dom = int(np.argmax(stage_avg[2:4])) + 2  # the FFN kernels dominate the step
+    dom_name = names[dom]
+    achieved = stage_bytes[dom] / (stage_avg[dom] * 1e-3) / 1e9
+    kern = "grouped_linear_tc_kernel" if shape.dtype == "bf16" else "grouped_linear_simt_kernel"
+    traffic = traffic_from_profiles(f"{kern}:{dom_name}:{shape.name}")
+    ffn_flops = work["ffn1_flops"] + work["ffn2_flops"]
+    ffn_ms = stage_avg[2] + stage_avg[3]
+    value = shape.N * world * args.steps / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if shape.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": config_of(shape, argparse.Namespace(gpus=world)),
+        "roofline": {"bound": "hbm", "kernel": f"{kern} ({dom_name})", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs",
+                     "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+                     "algorithmic_bytes_per_launch": stage_bytes[dom]},
+        "stages_ms": {n: float(v) for n, v in zip(names, stage_avg)},
+        "stage_gbs": {n: float(b / (t * 1e-3) / 1e9) for n, b, t in zip(names, stage_bytes, stage_avg)},
+        "ffn_tc_frac": {"achieved_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12, "peak_tflops": tc_burst,
+                        "frac": ffn_flops / (ffn_ms * 1e-3) / 1e12 / tc_burst,
+                        "note": f"kept-row FLOPs 4*K*d*d_ff over both FFN kernels; {peak_src} bf16 burst"},
+        "dispatch_hbm_gbs": float(work["dispatch_bytes"] / (stage_avg[1] * 1e-3) / 1e9),
+        "kept_rows": work["kept_rows"], "dropped": int(shape.N - work["kept_rows"]),
+        "e2e": {"value": shape.N * world * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
+                "d2h_bytes_per_step": int(y_host.numel() * y_host.element_size() + 4)},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        v, det = oracle_sample(shape, inp, args.ref_ffn_tokens)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": det["cores"], "kind": "oracle",
+                                "sample": det["sample"]}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--ref-ffn-tokens", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    shape = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, shape)
+    return run_gpu(args, shape)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

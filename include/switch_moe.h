@@ -1,0 +1,194 @@
+/*
+ * switch_moe.h -- C ABI of the B300 (sm_103a) top-1 Switch MoE layer forward pass.
+ *
+ * The layer (pages cited by title, then section / equation):
+ *   "042 · Switch Transformer：每个词只选一个专家" (wq-win.github.io), section 一:
+ *       p(x) = softmax(W_r x), e*(x) = argmax_e p_e(x), y = p_{e*}(x) f_{e*}(x),
+ *       capacity about (T/E) c, overflow tokens skip the expert and ride the residual;
+ *   same page, section 二: L_aux = alpha E sum_e f_e P_e;
+ *   same page, section 三: the pipeline (float32 router -> top-1 -> aux loss ->
+ *       capacity truncation -> low-precision dispatch -> expert FFN -> gated combine),
+ *       with "token representations, expert set, capacity factor, balance weight" in
+ *       and "layer output and per-expert load statistics" out;
+ *   "开源 AI 论文复现实验与代码解读 · 070" (zffjzz.top), section 核心思想与公式:
+ *       Z = XW, f before truncation, P mean probability, C = ceil(cT/E), NumPy tie rule;
+ *       section 官方代码阅读路线: slots by cumulative count in sequence order;
+ *   "Switch Transformers ... - 中文验证版" (ai-papers.xuzou.cn), section 方法适配:
+ *       float32 router inside, bfloat16 dispatch/combine;
+ *   "混合专家" (world.lapla.si/zh/moe), section 专家里面是什么: d -> d_ff ReLU -> d with biases.
+ *
+ * Conventions for every call below
+ *   - Ownership: the caller owns every pointer it passes (device memory unless
+ *     a name ends in _host).  The handle owns only its internal workspace, which
+ *     switch_create allocates and switch_destroy frees.  Nothing passed in is freed.
+ *   - Execution: all calls except switch_get_stats, switch_sync_status and
+ *     switch_stage_ms are asynchronous on the given stream.  Calls on one handle
+ *     share its workspace: calls on one handle that overlap on the GPU race, so
+ *     issue them on one stream (or serialise the streams).
+ *   - Errors: argument errors return at once (nothing is enqueued).  A kernel
+ *     that finds an impossible state (a bounded wait that ran out, a debug bounds
+ *     hit) sets a flag in the workspace; switch_get_stats / switch_sync_status
+ *     report it.  Kernels never trap.
+ *   - Layouts: row-major, dense.  N = G*T tokens, group-major ("16 sequences x 512"
+ *     flattens sequence-major inside a group).  "act" = the config's dtype
+ *     (float32 or bfloat16) for activations, expert weights and expert biases.
+ *     The router weights and bias are always float32.
+ *   - Alignment: every pointer must be 16-byte aligned; d_model * sizeof(act)
+ *     and d_ff * sizeof(act) must be multiples of 16 bytes.
+ */
+#ifndef SWITCH_MOE_H
+#define SWITCH_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SWITCH_API __attribute__((visibility("default")))
+#else
+#define SWITCH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SWITCH_OK = 0,
+  SWITCH_ERR_INVALID_ARG = 1,     /* bad pointer, size, alignment or config */
+  SWITCH_ERR_UNSUPPORTED = 2,     /* valid but outside what this build implements */
+  SWITCH_ERR_CUDA = 3,            /* a CUDA runtime call failed */
+  SWITCH_ERR_DEVICE_TIMEOUT = 4,  /* a kernel's bounded wait ran out (flag set on device) */
+  SWITCH_ERR_OOM = 5,             /* workspace allocation failed */
+  SWITCH_ERR_DEVICE_BOUNDS = 6    /* a debug bounds check fired on the device */
+} switch_status;
+
+typedef enum { SWITCH_F32 = 0, SWITCH_BF16 = 1 } switch_dtype;
+
+/* switch_config.flags */
+#define SWITCH_FLAG_WRITE_PROBS   0x1u  /* route writes probs[N*E] (verification only) */
+#define SWITCH_FLAG_WRITE_LOGITS  0x2u  /* route writes logits[N*E] (verification only) */
+#define SWITCH_FLAG_DEBUG_BOUNDS  0x4u  /* kernels check slot/row/expert ranges */
+#define SWITCH_FLAG_PROFILE       0x8u  /* switch_forward records per-stage CUDA events */
+
+typedef struct {
+  int G;                   /* routing groups; capacity and statistics are per group */
+  int T;                   /* tokens per group */
+  int d_model;             /* d */
+  int d_ff;                /* expert hidden width */
+  int E;                   /* experts, 1..2048 */
+  double capacity_factor;  /* c; C = ceil(c*T/E), c*T/E snapped to an integer within 1e-9 */
+  int capacity_override;   /* > 0: use this C instead */
+  float alpha;             /* aux-loss weight (0.01 on the 042 page, section 二) */
+  switch_dtype dtype;      /* act dtype */
+  unsigned flags;          /* SWITCH_FLAG_* */
+} switch_config;
+
+typedef struct switch_layer* switch_handle;
+
+/* Device buffers that switch_route fills (caller-owned).  Sizes in elements. */
+typedef struct {
+  int32_t* expert;          /* [N]   e*(x_t): the raw choice, also for dropped tokens   */
+  int32_t* slot;            /* [N]   earlier tokens of the group that chose the same expert */
+  uint8_t* keep;            /* [N]   1 when slot < C                                    */
+  float* gate;              /* [N]   p_{t, expert_t}, never renormalised                */
+  int32_t* row;             /* [N]   row of the token in its expert's block of xe, -1 if dropped */
+  int32_t* raw_count;       /* [G*E] choices per expert before truncation               */
+  int32_t* accepted_count;  /* [G*E] min(raw, C)                                        */
+  float* P;                 /* [G*E] mean router probability per expert                 */
+  float* balance;           /* [G]   unweighted E * sum_e f_e P_e                       */
+  float* aux_loss_per_group;/* [G]   alpha * balance                                    */
+  float* aux_loss;          /* [1]   mean over groups                                   */
+  int32_t* expert_rows;     /* [E]   sum over groups of accepted_count (rows of xe used) */
+  float* probs;             /* [N*E] or NULL; written when SWITCH_FLAG_WRITE_PROBS      */
+  float* logits;            /* [N*E] or NULL; written when SWITCH_FLAG_WRITE_LOGITS     */
+} switch_route_out;
+
+/* Capacity C for cfg (host only, no GPU needed); -1 when cfg is invalid. */
+SWITCH_API int64_t switch_capacity(const switch_config* cfg);
+
+/* Rows per expert block of the dispatched buffer: G*C.  -1 when cfg is invalid. */
+SWITCH_API int64_t switch_expert_block_rows(const switch_config* cfg);
+
+SWITCH_API const char* switch_status_string(switch_status s);
+
+/* Validate cfg, allocate the workspace on the current CUDA device, return a handle. */
+SWITCH_API switch_status switch_create(const switch_config* cfg, switch_handle* out);
+SWITCH_API switch_status switch_destroy(switch_handle h);
+
+/*
+ * Router + top-1 + slots + capacity mask + load statistics + aux loss.
+ *   x   [N, d] act;  Wr [E, d] float32;  br [E] float32 or NULL (zero).
+ * Logits are float32 (x cast up, then dot products with float32 accumulation);
+ * ties go to the lowest expert index.  Writes every non-NULL field of *out
+ * except probs/logits, which need their flags.  All fields other than
+ * probs and logits are required.
+ */
+SWITCH_API switch_status switch_route(switch_handle h, const void* x, const float* Wr, const float* br,
+                           const switch_route_out* out, void* stream);
+
+/*
+ * Dispatch gather: xe[e, row_t, :] = x_t for every kept token t with expert e;
+ * every other row of xe is zero.  xe is [E, G*C, d] act: expert e's block holds
+ * its kept tokens group by group in sequence order.
+ */
+SWITCH_API switch_status switch_dispatch(switch_handle h, const void* x, const switch_route_out* r,
+                              void* xe, void* stream);
+
+/*
+ * Expert FFN on each expert's first expert_rows[e] rows of xe:
+ *   ye[e, i, :] = ReLU(xe[e, i, :] W1[e]^T + b1[e]) W2[e]^T + b2[e]
+ * W1 [E, d_ff, d], b1 [E, d_ff] or NULL, W2 [E, d, d_ff], b2 [E, d] or NULL (act).
+ * bfloat16: products on the tensor cores with float32 accumulation; the hidden
+ * activation is rounded to bfloat16, and so is ye.  Rows of ye past
+ * expert_rows[e] are left unspecified.
+ */
+SWITCH_API switch_status switch_expert_ffn(switch_handle h, const void* xe, const void* W1, const void* b1,
+                                const void* W2, const void* b2, const int32_t* expert_rows,
+                                void* ye, void* stream);
+
+/*
+ * Combine: y_t = gate_t * ye[expert_t, row_t, :] for kept tokens, 0 for dropped
+ * ones, plus x_residual_t when x_residual is not NULL.  The gate is used as is
+ * (no renormalisation).  y [N, d] act.
+ */
+SWITCH_API switch_status switch_combine(switch_handle h, const void* ye, const switch_route_out* r,
+                             const void* x_residual, void* y, void* stream);
+
+/*
+ * The whole layer: route, dispatch, expert FFN, combine, on one stream.
+ * Same arguments and results as the four calls above; the dispatched buffer,
+ * the hidden activations and the expert outputs live in the workspace.
+ * x_residual may be NULL.
+ */
+SWITCH_API switch_status switch_forward(switch_handle h, const void* x, const float* Wr, const float* br,
+                             const void* W1, const void* b1, const void* W2, const void* b2,
+                             const switch_route_out* r, const void* x_residual, void* y,
+                             void* stream);
+
+/*
+ * Synchronise `stream`, then copy the aux loss, the [G*E] raw and accepted counts
+ * and the number of dropped tokens of the route results `r` to the host
+ * (any _host pointer may be NULL).  Returns the device error flag's status
+ * (SWITCH_ERR_DEVICE_TIMEOUT / SWITCH_ERR_DEVICE_BOUNDS) if set, and clears it.
+ */
+SWITCH_API switch_status switch_get_stats(switch_handle h, const switch_route_out* r, void* stream,
+                               float* aux_loss_host, int32_t* raw_host,
+                               int32_t* accepted_host, int64_t* dropped_host);
+
+/* Synchronise `stream` and return the device error flag's status (then clear it). */
+SWITCH_API switch_status switch_sync_status(switch_handle h, void* stream);
+
+/*
+ * With SWITCH_FLAG_PROFILE: synchronise and return the elapsed milliseconds of
+ * each stage of the last switch_forward: ms[0] route, ms[1] dispatch,
+ * ms[2] FFN first layer, ms[3] FFN second layer, ms[4] combine.  n >= 5.
+ */
+SWITCH_API switch_status switch_stage_ms(switch_handle h, float* ms, int n);
+
+/* Number of kernels the last switch_forward on this handle launched. */
+SWITCH_API int switch_last_launch_count(switch_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SWITCH_MOE_H */

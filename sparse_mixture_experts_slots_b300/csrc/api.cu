@@ -1,0 +1,351 @@
+// C ABI of the Switch MoE layer: argument checks, workspace, stage launches.
+// The operations are specified in include/switch_moe.h.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/switch_moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace smoe;
+
+struct switch_layer {
+  switch_config cfg;
+  int N, C, Ceff, R, nT;
+  int es;  // bytes per act element
+  int device;
+  uint8_t* ws;
+  size_t ws_bytes;
+  uint32_t* err;
+  float* logits;
+  int32_t* tile_hist;
+  float* tile_P;
+  int32_t* tile_base;
+  int32_t* group_off;
+  int32_t* tok_of_row;
+  void* xe;
+  void* hbuf;
+  void* ye;
+  cudaEvent_t ev[6];
+  bool have_events;
+  int last_launches;
+};
+
+namespace {
+
+constexpr int MAX_E = 2048;
+
+int64_t capacity_of(const switch_config* c) {
+  if (c->capacity_override > 0) return c->capacity_override;
+  if (c->T <= 0) return 0;
+  const double v = c->capacity_factor * (double)c->T / (double)c->E;
+  const double r = nearbyint(v);
+  if (fabs(v - r) <= 1e-9) return (int64_t)r;
+  return (int64_t)ceil(v);
+}
+
+bool config_ok(const switch_config* c) {
+  if (!c) return false;
+  if (c->G < 1 || c->T < 0 || c->d_model < 1 || c->d_ff < 1 || c->E < 1 || c->E > MAX_E) return false;
+  if (c->dtype != SWITCH_F32 && c->dtype != SWITCH_BF16) return false;
+  if (c->capacity_override < 0) return false;
+  if (c->capacity_override == 0 && !(c->capacity_factor > 0.0 && c->capacity_factor < 1e6)) return false;
+  const int es = c->dtype == SWITCH_F32 ? 4 : 2;
+  if ((c->d_model * es) % 16 != 0 || (c->d_ff * es) % 16 != 0) return false;
+  const int64_t N = (int64_t)c->G * c->T;
+  if (N > (int64_t)1 << 30) return false;
+  if (N * c->E > (int64_t)1 << 36) return false;
+  const int64_t C = capacity_of(c);
+  const int64_t Ceff = C < c->T ? C : c->T;
+  if ((int64_t)c->G * Ceff * c->E > (int64_t)1 << 30) return false;
+  // grid limits: routing groups on grid.y, token tiles of 64 rows of one expert block on grid.y
+  if (c->G > 65535 || (int64_t)c->G * Ceff > (int64_t)65535 * 64 || N > (int64_t)65535 * 64) return false;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool route_out_ok(const switch_route_out* r) {
+  return r && r->expert && r->slot && r->keep && r->gate && r->row && r->raw_count && r->accepted_count && r->P &&
+         r->balance && r->aux_loss_per_group && r->aux_loss && r->expert_rows;
+}
+
+switch_status launched(int n, switch_layer* h) {
+  if (n < 0) return SWITCH_ERR_CUDA;
+  h->last_launches += n;
+  return SWITCH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t switch_capacity(const switch_config* cfg) { return config_ok(cfg) ? capacity_of(cfg) : -1; }
+
+int64_t switch_expert_block_rows(const switch_config* cfg) {
+  if (!config_ok(cfg)) return -1;
+  const int64_t C = capacity_of(cfg);
+  return (int64_t)cfg->G * (C < cfg->T ? C : cfg->T);
+}
+
+const char* switch_status_string(switch_status s) {
+  switch (s) {
+    case SWITCH_OK: return "ok";
+    case SWITCH_ERR_INVALID_ARG: return "invalid argument";
+    case SWITCH_ERR_UNSUPPORTED: return "unsupported";
+    case SWITCH_ERR_CUDA: return "CUDA error";
+    case SWITCH_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case SWITCH_ERR_OOM: return "out of device memory";
+    case SWITCH_ERR_DEVICE_BOUNDS: return "device bounds check failed";
+  }
+  return "unknown status";
+}
+
+switch_status switch_create(const switch_config* cfg, switch_handle* out) {
+  if (!out) return SWITCH_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!config_ok(cfg)) return SWITCH_ERR_INVALID_ARG;
+  switch_layer* h = new (std::nothrow) switch_layer();
+  if (!h) return SWITCH_ERR_OOM;
+  h->cfg = *cfg;
+  h->N = cfg->G * cfg->T;
+  h->C = (int)capacity_of(cfg);
+  h->Ceff = h->C < cfg->T ? h->C : cfg->T;
+  h->R = cfg->G * h->Ceff;
+  h->nT = (cfg->T + ROUTE_TILE - 1) / ROUTE_TILE;
+  h->es = cfg->dtype == SWITCH_F32 ? 4 : 2;
+  if (cudaGetDevice(&h->device) != cudaSuccess) {
+    delete h;
+    return SWITCH_ERR_CUDA;
+  }
+  const size_t E = cfg->E, G = cfg->G, N = h->N, R = h->R, nT = h->nT;
+  const size_t d = cfg->d_model, F = cfg->d_ff;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 256);
+    return o;
+  };
+  const size_t o_err = take(sizeof(uint32_t) * 4);
+  const size_t o_logits = take(N * E * sizeof(float));
+  const size_t o_hist = take(G * nT * E * sizeof(int32_t));
+  const size_t o_tP = take(G * nT * E * sizeof(float));
+  const size_t o_base = take(G * nT * E * sizeof(int32_t));
+  const size_t o_goff = take(G * E * sizeof(int32_t));
+  const size_t o_tor = take(E * R * sizeof(int32_t));
+  const size_t o_xe = take(E * R * d * h->es);
+  const size_t o_h = take(E * R * F * h->es);
+  const size_t o_ye = take(E * R * d * h->es);
+  h->ws_bytes = off;
+  if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return SWITCH_ERR_OOM;
+  }
+  h->err = reinterpret_cast<uint32_t*>(h->ws + o_err);
+  h->logits = reinterpret_cast<float*>(h->ws + o_logits);
+  h->tile_hist = reinterpret_cast<int32_t*>(h->ws + o_hist);
+  h->tile_P = reinterpret_cast<float*>(h->ws + o_tP);
+  h->tile_base = reinterpret_cast<int32_t*>(h->ws + o_base);
+  h->group_off = reinterpret_cast<int32_t*>(h->ws + o_goff);
+  h->tok_of_row = reinterpret_cast<int32_t*>(h->ws + o_tor);
+  h->xe = h->ws + o_xe;
+  h->hbuf = h->ws + o_h;
+  h->ye = h->ws + o_ye;
+  if (cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return SWITCH_ERR_CUDA;
+  }
+  h->have_events = true;
+  for (int i = 0; i < 6; ++i)
+    if (cudaEventCreate(&h->ev[i]) != cudaSuccess) h->have_events = false;
+  *out = h;
+  return SWITCH_OK;
+}
+
+switch_status switch_destroy(switch_handle h) {
+  if (!h) return SWITCH_ERR_INVALID_ARG;
+  if (h->have_events)
+    for (int i = 0; i < 6; ++i) cudaEventDestroy(h->ev[i]);
+  const cudaError_t e = cudaFree(h->ws);
+  delete h;
+  return e == cudaSuccess ? SWITCH_OK : SWITCH_ERR_CUDA;
+}
+
+switch_status switch_route(switch_handle h, const void* x, const float* Wr, const float* br,
+                           const switch_route_out* out, void* stream) {
+  if (!h || !Wr || !route_out_ok(out)) return SWITCH_ERR_INVALID_ARG;
+  if (h->N > 0 && !x) return SWITCH_ERR_INVALID_ARG;
+  if (x && !aligned16(x)) return SWITCH_ERR_INVALID_ARG;
+  const switch_config& c = h->cfg;
+  const bool want_logits = (c.flags & SWITCH_FLAG_WRITE_LOGITS) && out->logits;
+  const bool want_probs = (c.flags & SWITCH_FLAG_WRITE_PROBS) && out->probs;
+  RouteArgs a;
+  a.x = x;
+  a.Wr = Wr;
+  a.br = br;
+  a.G = c.G;
+  a.T = c.T;
+  a.d = c.d_model;
+  a.E = c.E;
+  a.C = h->C;
+  a.R = h->R;
+  a.x_bf16 = c.dtype == SWITCH_BF16;
+  a.alpha = c.alpha;
+  a.debug = (c.flags & SWITCH_FLAG_DEBUG_BOUNDS) != 0;
+  a.logits = want_logits ? out->logits : h->logits;
+  a.tile_hist = h->tile_hist;
+  a.tile_P = h->tile_P;
+  a.tile_base = h->tile_base;
+  a.group_off = h->group_off;
+  a.tok_of_row = h->tok_of_row;
+  a.err = h->err;
+  a.expert = out->expert;
+  a.slot = out->slot;
+  a.keep = out->keep;
+  a.gate = out->gate;
+  a.row = out->row;
+  a.raw = out->raw_count;
+  a.accepted = out->accepted_count;
+  a.P = out->P;
+  a.balance = out->balance;
+  a.aux_g = out->aux_loss_per_group;
+  a.aux = out->aux_loss;
+  a.expert_rows = out->expert_rows;
+  a.probs = want_probs ? out->probs : nullptr;
+  return launched(launch_route(a, (cudaStream_t)stream), h);
+}
+
+switch_status switch_dispatch(switch_handle h, const void* x, const switch_route_out* r, void* xe, void* stream) {
+  if (!h || !route_out_ok(r) || !xe || !aligned16(xe)) return SWITCH_ERR_INVALID_ARG;
+  if (h->N > 0 && (!x || !aligned16(x))) return SWITCH_ERR_INVALID_ARG;
+  return launched(launch_dispatch(x, xe, r->expert, r->row, r->expert_rows, h->N, h->cfg.E, h->R,
+                                  h->cfg.d_model * h->es, (cudaStream_t)stream),
+                  h);
+}
+
+static switch_status run_ffn(switch_handle h, const void* xe, const void* W1, const void* b1, const void* W2,
+                             const void* b2, const int32_t* rows, void* ye, cudaStream_t s, int ev_mid) {
+  const switch_config& c = h->cfg;
+  const int E = c.E, R = h->R, d = c.d_model, F = c.d_ff;
+  const bool bf16 = c.dtype == SWITCH_BF16;
+  const bool tc = bf16 && tc_shape_ok(F, d) && tc_shape_ok(d, F);
+  int n;
+  n = tc ? launch_grouped_linear_tc(xe, W1, b1, h->hbuf, rows, E, R, F, d, true, h->err, s)
+         : launch_grouped_linear_simt(xe, W1, b1, h->hbuf, rows, E, R, F, d, true, bf16, s);
+  if (n < 0) return SWITCH_ERR_CUDA;
+  h->last_launches += n;
+  if (ev_mid >= 0) cudaEventRecord(h->ev[ev_mid], s);
+  n = tc ? launch_grouped_linear_tc(h->hbuf, W2, b2, ye, rows, E, R, d, F, false, h->err, s)
+         : launch_grouped_linear_simt(h->hbuf, W2, b2, ye, rows, E, R, d, F, false, bf16, s);
+  if (n < 0) return SWITCH_ERR_CUDA;
+  h->last_launches += n;
+  return SWITCH_OK;
+}
+
+switch_status switch_expert_ffn(switch_handle h, const void* xe, const void* W1, const void* b1, const void* W2,
+                                const void* b2, const int32_t* expert_rows, void* ye, void* stream) {
+  if (!h || !xe || !W1 || !W2 || !expert_rows || !ye) return SWITCH_ERR_INVALID_ARG;
+  if (!aligned16(xe) || !aligned16(W1) || !aligned16(W2) || !aligned16(ye)) return SWITCH_ERR_INVALID_ARG;
+  return run_ffn(h, xe, W1, b1, W2, b2, expert_rows, ye, (cudaStream_t)stream, -1);
+}
+
+switch_status switch_combine(switch_handle h, const void* ye, const switch_route_out* r, const void* x_residual,
+                             void* y, void* stream) {
+  if (!h || !route_out_ok(r) || !ye || !y || !aligned16(ye) || !aligned16(y)) return SWITCH_ERR_INVALID_ARG;
+  if (x_residual && !aligned16(x_residual)) return SWITCH_ERR_INVALID_ARG;
+  return launched(launch_combine(ye, r->expert, r->row, r->gate, x_residual, y, h->N, h->cfg.d_model, h->R,
+                                 h->cfg.dtype == SWITCH_BF16, (cudaStream_t)stream),
+                  h);
+}
+
+switch_status switch_forward(switch_handle h, const void* x, const float* Wr, const float* br, const void* W1,
+                             const void* b1, const void* W2, const void* b2, const switch_route_out* r,
+                             const void* x_residual, void* y, void* stream) {
+  if (!h || !W1 || !W2 || !y || !aligned16(y) || !aligned16(W1) || !aligned16(W2)) return SWITCH_ERR_INVALID_ARG;
+  if (x_residual && !aligned16(x_residual)) return SWITCH_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool prof = (h->cfg.flags & SWITCH_FLAG_PROFILE) && h->have_events;
+  h->last_launches = 0;
+  if (prof) cudaEventRecord(h->ev[0], s);
+  switch_status st = switch_route(h, x, Wr, br, r, stream);
+  if (st != SWITCH_OK) return st;
+  if (prof) cudaEventRecord(h->ev[1], s);
+  st = switch_dispatch(h, x, r, h->xe, stream);
+  if (st != SWITCH_OK) return st;
+  if (prof) cudaEventRecord(h->ev[2], s);
+  st = run_ffn(h, h->xe, W1, b1, W2, b2, r->expert_rows, h->ye, s, prof ? 3 : -1);
+  if (st != SWITCH_OK) return st;
+  if (prof) cudaEventRecord(h->ev[4], s);
+  st = switch_combine(h, h->ye, r, x_residual, y, stream);
+  if (st != SWITCH_OK) return st;
+  if (prof) cudaEventRecord(h->ev[5], s);
+  return SWITCH_OK;
+}
+
+static switch_status read_error_word(switch_handle h, cudaStream_t s) {
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, h->err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SWITCH_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SWITCH_ERR_CUDA;
+  if (word) {
+    if (cudaMemsetAsync(h->err, 0, sizeof(uint32_t), s) != cudaSuccess) return SWITCH_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SWITCH_ERR_CUDA;
+    return (word & ERR_TIMEOUT) ? SWITCH_ERR_DEVICE_TIMEOUT : SWITCH_ERR_DEVICE_BOUNDS;
+  }
+  return SWITCH_OK;
+}
+
+switch_status switch_get_stats(switch_handle h, const switch_route_out* r, void* stream, float* aux_loss_host,
+                               int32_t* raw_host, int32_t* accepted_host, int64_t* dropped_host) {
+  if (!h || !route_out_ok(r)) return SWITCH_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t GE = (size_t)h->cfg.G * h->cfg.E;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SWITCH_ERR_CUDA;
+  if (aux_loss_host && cudaMemcpy(aux_loss_host, r->aux_loss, sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SWITCH_ERR_CUDA;
+  if (raw_host && cudaMemcpy(raw_host, r->raw_count, GE * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SWITCH_ERR_CUDA;
+  int32_t* acc = accepted_host;
+  int32_t* tmp = nullptr;
+  if (!acc && dropped_host) {
+    tmp = (int32_t*)malloc(GE * sizeof(int32_t));
+    if (!tmp) return SWITCH_ERR_OOM;
+    acc = tmp;
+  }
+  if (acc && cudaMemcpy(acc, r->accepted_count, GE * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    free(tmp);
+    return SWITCH_ERR_CUDA;
+  }
+  if (dropped_host) {
+    int64_t kept = 0;
+    for (size_t i = 0; i < GE; ++i) kept += acc[i];
+    *dropped_host = (int64_t)h->N - kept;
+  }
+  free(tmp);
+  return read_error_word(h, s);
+}
+
+switch_status switch_sync_status(switch_handle h, void* stream) {
+  if (!h) return SWITCH_ERR_INVALID_ARG;
+  return read_error_word(h, (cudaStream_t)stream);
+}
+
+switch_status switch_stage_ms(switch_handle h, float* ms, int n) {
+  if (!h || !ms || n < 5) return SWITCH_ERR_INVALID_ARG;
+  if (!(h->cfg.flags & SWITCH_FLAG_PROFILE) || !h->have_events) return SWITCH_ERR_UNSUPPORTED;
+  if (cudaEventSynchronize(h->ev[5]) != cudaSuccess) return SWITCH_ERR_CUDA;
+  for (int i = 0; i < 5; ++i)
+    if (cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1]) != cudaSuccess) return SWITCH_ERR_CUDA;
+  return SWITCH_OK;
+}
+
+int switch_last_launch_count(switch_handle h) { return h ? h->last_launches : -1; }
+
+}  // extern "C"

@@ -1,0 +1,140 @@
+// Dispatch gather and combine scatter (sm_103a), 16-byte vectors, one warp per row.
+//
+// Dispatch: kept tokens are copied into their expert's block of xe; the rest of
+// the block is zero, as the one-hot dispatch tensor of the Switch Transformers
+// card (ai-papers.xuzou.cn, 方法适配) would give.
+// Combine: y_t = p_{e*}(x_t) * f_{e*}(x_t) for kept tokens and 0 for dropped ones
+// ("042 · Switch Transformer：每个词只选一个专家", section 一; the gate is not
+// renormalised, section 只执行一个专家时检查路由是否被错误归一化).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace smoe {
+
+constexpr int DC_WARPS = 8;
+
+// Warps [0, N) copy token rows to their slots; warps [N, N + E*R) zero the rows
+// past each expert's count.  Both reads and writes are whole 16-byte-vector rows.
+__global__ void __launch_bounds__(DC_WARPS * 32) dispatch_kernel(const uint4* __restrict__ x, uint4* __restrict__ xe,
+                                                                 const int32_t* __restrict__ expert,
+                                                                 const int32_t* __restrict__ row,
+                                                                 const int32_t* __restrict__ expert_rows, int N,
+                                                                 int E, int R, int vecs) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const long long w = (long long)blockIdx.x * DC_WARPS + warp;
+  if (w < N) {
+    const int r = row[w];
+    if (r < 0) return;
+    const uint4* src = x + w * vecs;
+    uint4* dst = xe + ((long long)expert[w] * R + r) * vecs;
+    for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
+    return;
+  }
+  const long long dr = w - N;
+  if (dr >= (long long)E * R) return;
+  const int e = (int)(dr / R), r = (int)(dr % R);
+  if (r < expert_rows[e]) return;
+  uint4* dst = xe + dr * vecs;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int v = lane; v < vecs; v += 32) dst[v] = zero;
+}
+
+int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_t* row, const int32_t* expert_rows,
+                    int N, int E, int R, int row_bytes, cudaStream_t s) {
+  const long long warps = (long long)N + (long long)E * R;
+  if (warps == 0 || (long long)E * R == 0) return 0;
+  const unsigned blocks = (unsigned)((warps + DC_WARPS - 1) / DC_WARPS);
+  dispatch_kernel<<<blocks, DC_WARPS * 32, 0, s>>>((const uint4*)x, (uint4*)xe, expert, row, expert_rows, N, E, R,
+                                                   row_bytes / 16);
+  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+// ---------------------------------------------------------------- combine
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p = __bfloat1622float2(h[i]);
+    f[2 * i] = p.x;
+    f[2 * i + 1] = p.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(DC_WARPS * 32) combine_kernel(const uint4* __restrict__ ye,
+                                                                const int32_t* __restrict__ expert,
+                                                                const int32_t* __restrict__ row,
+                                                                const float* __restrict__ gate,
+                                                                const uint4* __restrict__ resid, uint4* __restrict__ y,
+                                                                int N, int R, int vecs) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const long long t = (long long)blockIdx.x * DC_WARPS + warp;
+  if (t >= N) return;
+  const int r = row[t];
+  const uint4* src = nullptr;
+  float g = 0.f;
+  if (r >= 0) {
+    src = ye + ((long long)expert[t] * R + r) * vecs;
+    g = gate[t];
+  }
+  uint4* dst = y + t * vecs;
+  const uint4* res = resid ? resid + t * vecs : nullptr;
+  for (int v = lane; v < vecs; v += 32) {
+    constexpr int W = BF16 ? 8 : 4;
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (src) {
+      const uint4 in = __ldg(src + v);
+      if (BF16) {
+        unpack8(in, o);
+      } else {
+        const float* f = reinterpret_cast<const float*>(&in);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = f[i];
+      }
+#pragma unroll
+      for (int i = 0; i < W; ++i) o[i] *= g;
+    }
+    if (res) {
+      const uint4 rv = __ldg(res + v);
+      if (BF16) {
+        float rf[8];
+        unpack8(rv, rf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] += rf[i];
+      } else {
+        const float* f = reinterpret_cast<const float*>(&rv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] += f[i];
+      }
+    }
+    if (BF16) {
+      dst[v] = pack8(o);
+    } else {
+      dst[v] = make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                          __float_as_uint(o[3]));
+    }
+  }
+}
+
+int launch_combine(const void* ye, const int32_t* expert, const int32_t* row, const float* gate, const void* resid,
+                   void* y, int N, int d, int R, bool bf16, cudaStream_t s) {
+  if (N == 0) return 0;
+  const int vecs = d * (bf16 ? 2 : 4) / 16;
+  const unsigned blocks = (unsigned)((N + DC_WARPS - 1) / DC_WARPS);
+  if (bf16)
+    combine_kernel<true><<<blocks, DC_WARPS * 32, 0, s>>>((const uint4*)ye, expert, row, gate, (const uint4*)resid,
+                                                          (uint4*)y, N, R, vecs);
+  else
+    combine_kernel<false><<<blocks, DC_WARPS * 32, 0, s>>>((const uint4*)ye, expert, row, gate,
+                                                           (const uint4*)resid, (uint4*)y, N, R, vecs);
+  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+}  // namespace smoe

@@ -1,0 +1,63 @@
+// Internal launchers of the Switch MoE kernels (host side).  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace smoe {
+
+// Tokens per routing tile (softmax/top-1 CTA and slot-scan warp).
+constexpr int ROUTE_TILE = 128;
+
+struct RouteArgs {
+  // inputs
+  const void* x;       // [N, d] act
+  const float* Wr;     // [E, d]
+  const float* br;     // [E] or null
+  int G, T, d, E, C, R;
+  bool x_bf16;
+  float alpha;
+  bool debug;
+  // workspace
+  float* logits;       // [N, E] (the caller's buffer when it asked for logits)
+  int32_t* tile_hist;  // [G, nT, E]
+  float* tile_P;       // [G, nT, E]
+  int32_t* tile_base;  // [G, nT, E]
+  int32_t* group_off;  // [G, E]
+  int32_t* tok_of_row; // [E * R]
+  uint32_t* err;
+  // outputs
+  int32_t* expert; int32_t* slot; uint8_t* keep; float* gate; int32_t* row;
+  int32_t* raw; int32_t* accepted; float* P; float* balance; float* aux_g; float* aux;
+  int32_t* expert_rows;
+  float* probs;        // or null
+};
+
+// Router GEMM, softmax/top-1, per-tile statistics, scan, finalize, slots.
+// Returns the number of kernels launched (or -1 on a launch error).
+int launch_route(const RouteArgs& a, cudaStream_t s);
+
+// xe[expert[t]*R + row[t]] = x[t] for kept tokens (row[t] >= 0); rows r >= expert_rows[e]
+// of every expert block are zeroed.
+int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_t* row,
+                    const int32_t* expert_rows, int N, int E, int R, int row_bytes, cudaStream_t s);
+
+// y[t] = (row[t] >= 0 ? gate[t] * ye[expert[t]*R + row[t]] : 0) (+ resid[t]).
+int launch_combine(const void* ye, const int32_t* expert, const int32_t* row, const float* gate,
+                   const void* resid, void* y, int N, int d, int R, bool bf16, cudaStream_t s);
+
+// out[e*R + n, m] = act(sum_k in[e*R + n, k] * W[e, m, k] + bias[e, m]) for n < expert_rows[e].
+// CUDA-core kernel for float32 and for shapes the tensor-core kernel does not take.
+int launch_grouped_linear_simt(const void* in, const void* W, const void* bias, void* out,
+                               const int32_t* expert_rows, int E, int R, int M, int K, bool relu,
+                               bool bf16, cudaStream_t s);
+
+// Same contraction on tcgen05 tensor cores (bf16 in, f32 accumulate, bf16 out).
+// Needs M % 128 == 0 and K % 64 == 0.  Returns launches, or -1 on error.
+bool tc_shape_ok(int M, int K);
+int launch_grouped_linear_tc(const void* in, const void* W, const void* bias, void* out,
+                             const int32_t* expert_rows, int E, int R, int M, int K, bool relu,
+                             uint32_t* err, cudaStream_t s);
+
+}  // namespace smoe
