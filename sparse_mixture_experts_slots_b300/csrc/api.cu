@@ -70,9 +70,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool route_out_ok(const switch_route_out* r) {
-  return r && r->expert && r->slot && r->keep && r->gate && r->row && r->raw_count && r->accepted_count && r->P &&
-         r->balance && r->aux_loss_per_group && r->aux_loss && r->expert_rows;
+// Per-token arrays may be NULL only when there are no tokens.
+bool route_out_ok(const switch_route_out* r, int64_t N) {
+  if (!r) return false;
+  if (N > 0 && !(r->expert && r->slot && r->keep && r->gate && r->row)) return false;
+  return r->raw_count && r->accepted_count && r->P && r->balance && r->aux_loss_per_group && r->aux_loss &&
+         r->expert_rows;
 }
 
 switch_status launched(int n, switch_layer* h) {
@@ -180,7 +183,7 @@ switch_status switch_destroy(switch_handle h) {
 
 switch_status switch_route(switch_handle h, const void* x, const float* Wr, const float* br,
                            const switch_route_out* out, void* stream) {
-  if (!h || !Wr || !route_out_ok(out)) return SWITCH_ERR_INVALID_ARG;
+  if (!h || !Wr || !route_out_ok(out, h ? h->N : 0)) return SWITCH_ERR_INVALID_ARG;
   if (h->N > 0 && !x) return SWITCH_ERR_INVALID_ARG;
   if (x && !aligned16(x)) return SWITCH_ERR_INVALID_ARG;
   const switch_config& c = h->cfg;
@@ -223,7 +226,7 @@ switch_status switch_route(switch_handle h, const void* x, const float* Wr, cons
 }
 
 switch_status switch_dispatch(switch_handle h, const void* x, const switch_route_out* r, void* xe, void* stream) {
-  if (!h || !route_out_ok(r) || !xe || !aligned16(xe)) return SWITCH_ERR_INVALID_ARG;
+  if (!h || !route_out_ok(r, h->N) || (h->R > 0 && !xe) || !aligned16(xe)) return SWITCH_ERR_INVALID_ARG;
   if (h->N > 0 && (!x || !aligned16(x))) return SWITCH_ERR_INVALID_ARG;
   return launched(launch_dispatch(x, xe, r->expert, r->row, r->expert_rows, h->N, h->cfg.E, h->R,
                                   h->cfg.d_model * h->es, (cudaStream_t)stream),
@@ -251,14 +254,16 @@ static switch_status run_ffn(switch_handle h, const void* xe, const void* W1, co
 
 switch_status switch_expert_ffn(switch_handle h, const void* xe, const void* W1, const void* b1, const void* W2,
                                 const void* b2, const int32_t* expert_rows, void* ye, void* stream) {
-  if (!h || !xe || !W1 || !W2 || !expert_rows || !ye) return SWITCH_ERR_INVALID_ARG;
+  if (!h || !W1 || !W2 || !expert_rows) return SWITCH_ERR_INVALID_ARG;
+  if (h->R > 0 && (!xe || !ye)) return SWITCH_ERR_INVALID_ARG;
   if (!aligned16(xe) || !aligned16(W1) || !aligned16(W2) || !aligned16(ye)) return SWITCH_ERR_INVALID_ARG;
   return run_ffn(h, xe, W1, b1, W2, b2, expert_rows, ye, (cudaStream_t)stream, -1);
 }
 
 switch_status switch_combine(switch_handle h, const void* ye, const switch_route_out* r, const void* x_residual,
                              void* y, void* stream) {
-  if (!h || !route_out_ok(r) || !ye || !y || !aligned16(ye) || !aligned16(y)) return SWITCH_ERR_INVALID_ARG;
+  if (!h || !route_out_ok(r, h->N) || (h->R > 0 && !ye) || (h->N > 0 && !y) || !aligned16(ye) || !aligned16(y))
+    return SWITCH_ERR_INVALID_ARG;
   if (x_residual && !aligned16(x_residual)) return SWITCH_ERR_INVALID_ARG;
   return launched(launch_combine(ye, r->expert, r->row, r->gate, x_residual, y, h->N, h->cfg.d_model, h->R,
                                  h->cfg.dtype == SWITCH_BF16, (cudaStream_t)stream),
@@ -268,7 +273,7 @@ switch_status switch_combine(switch_handle h, const void* ye, const switch_route
 switch_status switch_forward(switch_handle h, const void* x, const float* Wr, const float* br, const void* W1,
                              const void* b1, const void* W2, const void* b2, const switch_route_out* r,
                              const void* x_residual, void* y, void* stream) {
-  if (!h || !W1 || !W2 || !y || !aligned16(y) || !aligned16(W1) || !aligned16(W2)) return SWITCH_ERR_INVALID_ARG;
+  if (!h || !W1 || !W2 || (h->N > 0 && !y) || !aligned16(y) || !aligned16(W1) || !aligned16(W2)) return SWITCH_ERR_INVALID_ARG;
   if (x_residual && !aligned16(x_residual)) return SWITCH_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const bool prof = (h->cfg.flags & SWITCH_FLAG_PROFILE) && h->have_events;
@@ -304,7 +309,7 @@ static switch_status read_error_word(switch_handle h, cudaStream_t s) {
 
 switch_status switch_get_stats(switch_handle h, const switch_route_out* r, void* stream, float* aux_loss_host,
                                int32_t* raw_host, int32_t* accepted_host, int64_t* dropped_host) {
-  if (!h || !route_out_ok(r)) return SWITCH_ERR_INVALID_ARG;
+  if (!h || !route_out_ok(r, h->N)) return SWITCH_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const size_t GE = (size_t)h->cfg.G * h->cfg.E;
   if (cudaStreamSynchronize(s) != cudaSuccess) return SWITCH_ERR_CUDA;
