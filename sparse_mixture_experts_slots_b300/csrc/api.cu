@@ -26,6 +26,9 @@ struct switch_layer {
   int32_t* tile_base;
   int32_t* group_off;
   int32_t* tok_of_row;
+  void* wsplit;
+  float* scan_partial;
+  uint32_t* scan_counter;
   void* xe;
   void* hbuf;
   void* ye;
@@ -134,8 +137,11 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
     off = round_up(off + bytes, 256);
     return o;
   };
-  const size_t o_err = take(sizeof(uint32_t) * 4);
-  const size_t o_logits = take(N * E * sizeof(float));
+  const size_t o_err = take(sizeof(uint32_t) * 4);  // [0] error word, [1] scan counter
+  // float32 logits are materialised only by the CUDA-core router (float32 activations)
+  const size_t o_logits = take(cfg->dtype == SWITCH_F32 ? N * E * sizeof(float) : 0);
+  const size_t o_wsplit = take(cfg->dtype == SWITCH_BF16 ? 3 * E * d * 2 : 0);
+  const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
   const size_t o_hist = take(G * nT * E * sizeof(int32_t));
   const size_t o_tP = take(G * nT * E * sizeof(float));
   const size_t o_base = take(G * nT * E * sizeof(int32_t));
@@ -157,6 +163,9 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->tile_base = reinterpret_cast<int32_t*>(h->ws + o_base);
   h->group_off = reinterpret_cast<int32_t*>(h->ws + o_goff);
   h->tok_of_row = reinterpret_cast<int32_t*>(h->ws + o_tor);
+  h->wsplit = h->ws + o_wsplit;
+  h->scan_partial = reinterpret_cast<float*>(h->ws + o_part);
+  h->scan_counter = h->err + 1;
   h->xe = h->ws + o_xe;
   h->hbuf = h->ws + o_h;
   h->ye = h->ws + o_ye;
@@ -181,47 +190,59 @@ switch_status switch_destroy(switch_handle h) {
   return e == cudaSuccess ? SWITCH_OK : SWITCH_ERR_CUDA;
 }
 
-switch_status switch_route(switch_handle h, const void* x, const float* Wr, const float* br,
-                           const switch_route_out* out, void* stream) {
+static switch_status route_args(switch_handle h, const void* x, const float* Wr, const float* br,
+                                const switch_route_out* out, RouteArgs* a) {
   if (!h || !Wr || !route_out_ok(out, h ? h->N : 0)) return SWITCH_ERR_INVALID_ARG;
   if (h->N > 0 && !x) return SWITCH_ERR_INVALID_ARG;
   if (x && !aligned16(x)) return SWITCH_ERR_INVALID_ARG;
   const switch_config& c = h->cfg;
   const bool want_logits = (c.flags & SWITCH_FLAG_WRITE_LOGITS) && out->logits;
   const bool want_probs = (c.flags & SWITCH_FLAG_WRITE_PROBS) && out->probs;
+  a->x = x;
+  a->Wr = Wr;
+  a->br = br;
+  a->G = c.G;
+  a->T = c.T;
+  a->d = c.d_model;
+  a->E = c.E;
+  a->C = h->C;
+  a->R = h->R;
+  a->x_bf16 = c.dtype == SWITCH_BF16;
+  a->alpha = c.alpha;
+  a->debug = (c.flags & SWITCH_FLAG_DEBUG_BOUNDS) != 0;
+  a->slots = true;
+  a->logits = want_logits ? out->logits : h->logits;
+  a->logits_out = want_logits ? out->logits : nullptr;
+  a->wsplit = h->wsplit;
+  a->tile_hist = h->tile_hist;
+  a->tile_P = h->tile_P;
+  a->tile_base = h->tile_base;
+  a->group_off = h->group_off;
+  a->tok_of_row = h->tok_of_row;
+  a->scan_partial = h->scan_partial;
+  a->scan_counter = h->scan_counter;
+  a->err = h->err;
+  a->expert = out->expert;
+  a->slot = out->slot;
+  a->keep = out->keep;
+  a->gate = out->gate;
+  a->row = out->row;
+  a->raw = out->raw_count;
+  a->accepted = out->accepted_count;
+  a->P = out->P;
+  a->balance = out->balance;
+  a->aux_g = out->aux_loss_per_group;
+  a->aux = out->aux_loss;
+  a->expert_rows = out->expert_rows;
+  a->probs = want_probs ? out->probs : nullptr;
+  return SWITCH_OK;
+}
+
+switch_status switch_route(switch_handle h, const void* x, const float* Wr, const float* br,
+                           const switch_route_out* out, void* stream) {
   RouteArgs a;
-  a.x = x;
-  a.Wr = Wr;
-  a.br = br;
-  a.G = c.G;
-  a.T = c.T;
-  a.d = c.d_model;
-  a.E = c.E;
-  a.C = h->C;
-  a.R = h->R;
-  a.x_bf16 = c.dtype == SWITCH_BF16;
-  a.alpha = c.alpha;
-  a.debug = (c.flags & SWITCH_FLAG_DEBUG_BOUNDS) != 0;
-  a.logits = want_logits ? out->logits : h->logits;
-  a.tile_hist = h->tile_hist;
-  a.tile_P = h->tile_P;
-  a.tile_base = h->tile_base;
-  a.group_off = h->group_off;
-  a.tok_of_row = h->tok_of_row;
-  a.err = h->err;
-  a.expert = out->expert;
-  a.slot = out->slot;
-  a.keep = out->keep;
-  a.gate = out->gate;
-  a.row = out->row;
-  a.raw = out->raw_count;
-  a.accepted = out->accepted_count;
-  a.P = out->P;
-  a.balance = out->balance;
-  a.aux_g = out->aux_loss_per_group;
-  a.aux = out->aux_loss;
-  a.expert_rows = out->expert_rows;
-  a.probs = want_probs ? out->probs : nullptr;
+  const switch_status st = route_args(h, x, Wr, br, out, &a);
+  if (st != SWITCH_OK) return st;
   return launched(launch_route(a, (cudaStream_t)stream), h);
 }
 
@@ -279,10 +300,14 @@ switch_status switch_forward(switch_handle h, const void* x, const float* Wr, co
   const bool prof = (h->cfg.flags & SWITCH_FLAG_PROFILE) && h->have_events;
   h->last_launches = 0;
   if (prof) cudaEventRecord(h->ev[0], s);
-  switch_status st = switch_route(h, x, Wr, br, r, stream);
+  RouteArgs a;
+  switch_status st = route_args(h, x, Wr, br, r, &a);
+  if (st != SWITCH_OK) return st;
+  a.slots = false;  // the dispatch pass below turns ranks into slots
+  st = launched(launch_route(a, s), h);
   if (st != SWITCH_OK) return st;
   if (prof) cudaEventRecord(h->ev[1], s);
-  st = switch_dispatch(h, x, r, h->xe, stream);
+  st = launched(launch_dispatch_slots(x, h->xe, a, s), h);
   if (st != SWITCH_OK) return st;
   if (prof) cudaEventRecord(h->ev[2], s);
   st = run_ffn(h, h->xe, W1, b1, W2, b2, r->expert_rows, h->ye, s, prof ? 3 : -1);

@@ -49,6 +49,77 @@ int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_
   return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
+// Forward path: the slots of the routing step and the dispatch copy in one pass.
+// Warp w < N: lane 0 turns the token's in-tile rank (held in slot[]) into its slot,
+// keep flag and row (as route_slots_kernel does), then the warp copies the row.
+// Warps past N zero the rows past each expert's count.
+__global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
+    const uint4* __restrict__ x, uint4* __restrict__ xe, const int32_t* __restrict__ expert,
+    const int32_t* __restrict__ tile_base, const int32_t* __restrict__ group_off,
+    const int32_t* __restrict__ expert_rows, int32_t* __restrict__ slot, uint8_t* __restrict__ keep,
+    int32_t* __restrict__ row, int32_t* __restrict__ tok_of_row, long long N, int T, int E, int nT, int C, int R,
+    int vecs, bool debug, uint32_t* err) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const long long w = (long long)blockIdx.x * DC_WARPS + warp;
+  if (w < N) {
+    int r = -1, e = 0;
+    if (lane == 0) {
+      const int g = (int)(w / T);
+      const int ti = (int)(w - (long long)g * T);
+      e = expert[w];
+      if (e < 0 || e >= E) {
+        raise_error(err, ERR_BOUNDS);
+        e = 0;
+        slot[w] = 0;
+        keep[w] = 0;
+      } else {
+        const int s = tile_base[((size_t)g * nT + ti / ROUTE_TILE) * E + e] + slot[w];
+        const bool k = s < C;
+        slot[w] = s;
+        if (k) {
+          r = group_off[(size_t)g * E + e] + s;
+          if (r < 0 || r >= R) {
+            if (debug) raise_error(err, ERR_BOUNDS);
+            r = -1;
+          } else {
+            tok_of_row[(size_t)e * R + r] = (int32_t)w;
+          }
+        }
+        keep[w] = r >= 0 ? 1 : 0;
+      }
+      row[w] = r;
+    }
+    r = __shfl_sync(0xffffffffu, r, 0);
+    e = __shfl_sync(0xffffffffu, e, 0);
+    if (r < 0) return;
+    const uint4* src = x + w * vecs;
+    uint4* dst = xe + ((long long)e * R + r) * vecs;
+    for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
+    return;
+  }
+  const long long dr = w - N;
+  if (dr >= (long long)E * R) return;
+  const int e = (int)(dr / R), r = (int)(dr % R);
+  if (r < expert_rows[e]) return;
+  uint4* dst = xe + dr * vecs;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int v = lane; v < vecs; v += 32) dst[v] = zero;
+}
+
+int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, cudaStream_t s) {
+  const long long N = (long long)a.G * a.T;
+  const long long warps = N + (long long)a.E * a.R;
+  if (warps == 0) return 0;
+  const int nT = (a.T + ROUTE_TILE - 1) / ROUTE_TILE;
+  const int vecs = a.d * (a.x_bf16 ? 2 : 4) / 16;
+  const unsigned blocks = (unsigned)((warps + DC_WARPS - 1) / DC_WARPS);
+  dispatch_slots_kernel<<<blocks, DC_WARPS * 32, 0, s>>>((const uint4*)x, (uint4*)xe, a.expert, a.tile_base,
+                                                         a.group_off, a.expert_rows, a.slot, a.keep, a.row,
+                                                         a.tok_of_row, N, a.T, a.E, nT, a.C, a.R, vecs, a.debug,
+                                                         a.err);
+  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
 // ---------------------------------------------------------------- combine
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);

@@ -177,8 +177,7 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [rows, cols] (cols contiguous); box = box_rows x 64 columns, 128-byte swizzle.
-static bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -216,8 +215,8 @@ int launch_grouped_linear_tc(const void* in, const void* W, const void* bias, vo
   if (!tc_shape_ok(M, K)) return -1;
   const int BN = R <= 32 ? 32 : R <= 64 ? 64 : R <= 128 ? 128 : 256;
   CUtensorMap tmW, tmX;
-  if (!encode_2d(&tmW, W, (uint64_t)E * M, (uint64_t)K, TC_BM)) return -1;
-  if (!encode_2d(&tmX, in, (uint64_t)E * R, (uint64_t)K, (uint32_t)BN)) return -1;
+  if (!encode_bf16_2d(&tmW, W, (uint64_t)E * M, (uint64_t)K, TC_BM)) return -1;
+  if (!encode_bf16_2d(&tmX, in, (uint64_t)E * R, (uint64_t)K, (uint32_t)BN)) return -1;
 #define SMOE_TC(BNV, ST)                                                                                      \
   return relu ? launch_tc<BNV, ST, true>(tmW, tmX, bias, out, expert_rows, E, R, M, K, err, s)               \
               : launch_tc<BNV, ST, false>(tmW, tmX, bias, out, expert_rows, E, R, M, K, err, s)

@@ -19,13 +19,18 @@ struct RouteArgs {
   bool x_bf16;
   float alpha;
   bool debug;
+  bool slots;          // false: leave rank in slot[] (a fused dispatch finishes the slots)
   // workspace
-  float* logits;       // [N, E] (the caller's buffer when it asked for logits)
+  float* logits;       // [N, E] float32 logits of the CUDA-core router (workspace or the caller's)
+  float* logits_out;   // [N, E] or null: logits the caller asked for
+  void* wsplit;        // [3, E, d] bf16: W_r split into hi, mid, lo (tensor-core router)
   int32_t* tile_hist;  // [G, nT, E]
   float* tile_P;       // [G, nT, E]
   int32_t* tile_base;  // [G, nT, E]
   int32_t* group_off;  // [G, E]
   int32_t* tok_of_row; // [E * R]
+  float* scan_partial; // [G, ceil(E / 32)]
+  uint32_t* scan_counter;  // one word, zero between launches
   uint32_t* err;
   // outputs
   int32_t* expert; int32_t* slot; uint8_t* keep; float* gate; int32_t* row;
@@ -34,9 +39,25 @@ struct RouteArgs {
   float* probs;        // or null
 };
 
-// Router GEMM, softmax/top-1, per-tile statistics, scan, finalize, slots.
+// Blocks of the cross-tile scan (one per 32 experts); scan_partial holds G * this many floats.
+inline int route_scan_blocks(int E) { return (E + 31) / 32; }
+
+// Router (tensor cores for bf16 x, CUDA cores for float32 x), softmax/top-1, per-tile
+// statistics, cross-tile scan + finalize, slots (when a.slots).
 // Returns the number of kernels launched (or -1 on a launch error).
 int launch_route(const RouteArgs& a, cudaStream_t s);
+
+// Tensor-core router: W_r split + one fused GEMM/softmax/top-1/statistics kernel.
+// Writes expert, gate, the in-tile rank (into `rank`), tile_hist, tile_P and, when
+// asked, logits_out / probs.  Returns launches or -1.
+int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s);
+int router_tc_experts_per_cta(int E);
+
+// 2-D bf16 tensor map [rows, cols] (cols contiguous), box box_rows x 64 columns, 128-byte swizzle.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// Slots from in-tile ranks, then the dispatch copy: one warp per token.
+int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, cudaStream_t s);
 
 // xe[expert[t]*R + row[t]] = x[t] for kept tokens (row[t] >= 0); rows r >= expert_rows[e]
 // of every expert block are zeroed.

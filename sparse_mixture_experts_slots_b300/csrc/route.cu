@@ -3,17 +3,21 @@
 // Stages, following the pipeline of "042 · Switch Transformer：每个词只选一个专家",
 // section 三 (float32 router -> one expert per token -> load statistics and aux
 // loss -> capacity truncation):
-//   1. router_logits:   z = x W_r^T + b_r in float32 (x cast up; selective precision,
-//                        Switch Transformers card on ai-papers.xuzou.cn, 方法适配).
-//   2. route_softmax:   per token max/argmax (ties -> lowest index), softmax sum, gate;
-//                        per 128-token tile: expert histogram and probability sums.
-//   3. route_scan:      per (group, expert): exclusive prefix of tile histograms,
-//                        raw and accepted counts, mean probability P.
-//   4. route_finalize:  per group balance E * sum f P and aux loss; expert row offsets.
-//   5. route_slots:     per tile, one warp walks its tokens in sequence order and
-//                        gives each its slot = earlier tokens of the group with the
-//                        same expert ("开源 AI 论文复现实验与代码解读 · 070",
-//                        官方代码阅读路线: cumulative count along the sequence).
+//   1. router:   z = x W_r^T + b_r in float32 (x cast up; selective precision,
+//                Switch Transformers card on ai-papers.xuzou.cn, 方法适配), softmax,
+//                top-1 (ties -> lowest index), gate, and per 128-token tile the expert
+//                histogram, the probability sums and each token's rank among the
+//                tile's earlier tokens with the same expert.  bf16 activations use the
+//                tensor-core kernel in route_tc.cu; float32 activations use the
+//                CUDA-core kernels below (router_logits + route_softmax).
+//   2. route_scan: per (group, expert) exclusive prefix of the tile histograms, raw
+//                and accepted counts, mean probability P, expert row offsets; the last
+//                block computes each group's balance E * sum f P, its aux loss and
+//                the mean over groups.
+//   3. slots:    slot = (tokens of the group's earlier tiles with the same expert)
+//                + rank, i.e. the cumulative count along the sequence
+//                ("开源 AI 论文复现实验与代码解读 · 070", 官方代码阅读路线);
+//                keep = slot < C; row in the expert's block of the dispatched buffer.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -68,13 +72,15 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const T* __restrict_
   }
 }
 
-// ---------------------------------------------------------------- 2. softmax / top-1 per tile
-// grid (nT, G), 256 threads.  Dynamic smem: hist[E] ints.
+// ---------------------------------------------------------------- 2. softmax / top-1 per tile (float32 path)
+// grid (nT, G), 256 threads.  Dynamic smem: hist[E] ints.  Writes the in-tile rank to rank[].
 __global__ void __launch_bounds__(256) route_softmax_kernel(
     const float* __restrict__ z, int T, int E, int nT, int32_t* __restrict__ expert, float* __restrict__ gate,
-    int32_t* __restrict__ tile_hist, float* __restrict__ tile_P, float* __restrict__ probs) {
+    int32_t* __restrict__ rank, int32_t* __restrict__ tile_hist, float* __restrict__ tile_P,
+    float* __restrict__ probs, uint32_t* err) {
   extern __shared__ int32_t hist[];
   __shared__ float m_s[ROUTE_TILE], s_s[ROUTE_TILE];
+  __shared__ int a_s[ROUTE_TILE];
   const int g = blockIdx.y, tile = blockIdx.x;
   const int t0 = tile * ROUTE_TILE;
   const int len = min(ROUTE_TILE, T - t0);
@@ -92,18 +98,30 @@ __global__ void __launch_bounds__(256) route_softmax_kernel(
       if (v > best) { best = v; bi = e; }   // strict: first (lowest) index among equals
     }
     warp_argmax(best, bi);
+    if (bi < 0 || bi >= E) {  // non-finite logits only
+      if (lane == 0) raise_error(err, ERR_BOUNDS);
+      bi = 0;
+    }
     float s = 0.f;
     for (int e = lane; e < E; e += 32) s += expf(zr[e] - best);
     s = warp_sum(s);
     if (lane == 0) {
       m_s[i] = best;
       s_s[i] = s;
+      a_s[i] = bi;
       expert[tok0 + i] = bi;
       gate[tok0 + i] = 1.0f / s;   // exp(z_top - max) / s with z_top = max
       atomicAdd(&hist[bi], 1);
     }
   }
   __syncthreads();
+
+  // rank among the tile's earlier tokens with the same expert
+  for (int i = threadIdx.x; i < len; i += blockDim.x) {
+    int r = 0;
+    for (int j = 0; j < i; ++j) r += a_s[j] == a_s[i];
+    rank[tok0 + i] = r;
+  }
 
   // Column pass: probability sums per expert over the tile (fixed token order).
   const size_t tbase = ((size_t)g * nT + tile) * E;
@@ -119,138 +137,156 @@ __global__ void __launch_bounds__(256) route_softmax_kernel(
   }
 }
 
-// ---------------------------------------------------------------- 3. per (group, expert) scan over tiles
-__global__ void route_scan_kernel(const int32_t* __restrict__ tile_hist, const float* __restrict__ tile_P,
-                                  int32_t* __restrict__ tile_base, int32_t* __restrict__ raw,
-                                  int32_t* __restrict__ accepted, float* __restrict__ P, int T, int E, int nT,
-                                  int C) {
-  const int g = blockIdx.y;
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= E) return;
-  int base = 0;
-  float psum = 0.f;
-  for (int j = 0; j < nT; ++j) {
-    const size_t i = ((size_t)g * nT + j) * E + e;
-    tile_base[i] = base;
-    base += tile_hist[i];
-    psum += tile_P[i];
-  }
-  raw[(size_t)g * E + e] = base;
-  accepted[(size_t)g * E + e] = min(base, C);
-  P[(size_t)g * E + e] = T > 0 ? psum / (float)T : 0.f;
-}
+// ---------------------------------------------------------------- 3. cross-tile scan + finalize
+// One block per 32 experts (lane <-> expert); the warps split each group's tiles.
+constexpr int SCAN_WARPS = 16;
 
-// ---------------------------------------------------------------- 4. finalize (one CTA)
-__global__ void __launch_bounds__(1024) route_finalize_kernel(
-    const int32_t* __restrict__ raw, const int32_t* __restrict__ accepted, const float* __restrict__ P, int G,
-    int T, int E, float alpha, float* __restrict__ balance, float* __restrict__ aux_g, float* __restrict__ aux,
-    int32_t* __restrict__ group_off, int32_t* __restrict__ expert_rows) {
-  __shared__ float red[1024];
-  float total = 0.f;
-  for (int g = 0; g < G; ++g) {
-    float part = 0.f;
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-      part += (float)raw[(size_t)g * E + e] * P[(size_t)g * E + e];
-    red[threadIdx.x] = part;
-    __syncthreads();
-    for (int w = blockDim.x / 2; w > 0; w >>= 1) {
-      if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-      __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-      // E * sum_e f_e P_e with f_e = raw_e / T
-      const float b = T > 0 ? (float)E * (red[0] / (float)T) : 0.f;
-      balance[g] = b;
-      aux_g[g] = alpha * b;
-      total += alpha * b;
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) aux[0] = G > 0 ? total / (float)G : 0.f;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int g = 0; g < G; ++g) {
-      group_off[(size_t)g * E + e] = run;
-      run += accepted[(size_t)g * E + e];
-    }
-    expert_rows[e] = run;
-  }
-}
-
-// ---------------------------------------------------------------- 5. slots, one warp per tile
-constexpr int SLOT_WARPS = 4;
-
-__global__ void __launch_bounds__(SLOT_WARPS * 32) route_slots_kernel(
-    const int32_t* __restrict__ expert, const int32_t* __restrict__ tile_base, const int32_t* __restrict__ group_off,
-    int T, int E, int nT, int C, int R, int32_t* __restrict__ slot, uint8_t* __restrict__ keep,
-    int32_t* __restrict__ row, int32_t* __restrict__ tok_of_row, bool debug, uint32_t* err) {
-  extern __shared__ int32_t cnt_all[];
+__global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
+    const int32_t* __restrict__ tile_hist, const float* __restrict__ tile_P, int G, int T, int E, int nT, int C,
+    float alpha, int32_t* __restrict__ tile_base, int32_t* __restrict__ raw, int32_t* __restrict__ accepted,
+    float* __restrict__ P, int32_t* __restrict__ group_off, int32_t* __restrict__ expert_rows,
+    float* __restrict__ balance, float* __restrict__ aux_g, float* __restrict__ aux, float* __restrict__ partial,
+    uint32_t* __restrict__ counter) {
+  __shared__ int sh_h[SCAN_WARPS][32];
+  __shared__ float sh_p[SCAN_WARPS][32];
+  __shared__ int is_last;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int g = blockIdx.y;
-  const int tile = blockIdx.x * SLOT_WARPS + warp;
-  if (tile >= nT) return;  // whole warp leaves; no block-wide barrier below
-  int32_t* cnt = cnt_all + (size_t)warp * E;
-  const size_t tb = ((size_t)g * nT + tile) * E;
-  for (int e = lane; e < E; e += 32) cnt[e] = tile_base[tb + e];
-  __syncwarp();
-  const unsigned lt_mask = (1u << lane) - 1u;
-  const int t_end = min(T, (tile + 1) * ROUTE_TILE);
-  for (int t0 = tile * ROUTE_TILE; t0 < t_end; t0 += 32) {
-    const int t = t0 + lane;
-    const bool valid = t < t_end;
-    const size_t tok = (size_t)g * T + t;
-    int e = valid ? expert[tok] : -1 - lane;  // invalid lanes get keys of their own
-    if (debug && valid && (e < 0 || e >= E)) { raise_error(err, ERR_BOUNDS); e = -1 - lane; }
-    const bool live = e >= 0;
-    const unsigned same = __match_any_sync(0xffffffffu, e);
-    const int base = live ? cnt[e] : 0;
-    __syncwarp();
-    if (live && lane == __ffs(same) - 1) cnt[e] = base + __popc(same);
-    __syncwarp();
-    if (valid) {
-      const int s = base + __popc(same & lt_mask);
-      const bool k = live && s < C;
-      slot[tok] = s;
-      keep[tok] = k ? 1 : 0;
-      int r = -1;
-      if (k) {
-        r = group_off[(size_t)g * E + e] + s;
-        if (debug && (r < 0 || r >= R)) { raise_error(err, ERR_BOUNDS); r = -1; }
-        else tok_of_row[(size_t)e * R + r] = (int32_t)tok;
+  const int e = blockIdx.x * 32 + lane;
+  const bool ev = e < E;
+  const int chunk = (nT + SCAN_WARPS - 1) / SCAN_WARPS;
+  const int j0 = min(nT, warp * chunk), j1 = min(nT, j0 + chunk);
+  int rows_run = 0;
+  for (int g = 0; g < G; ++g) {
+    int hs = 0;
+    float ps = 0.f;
+    if (ev)
+      for (int j = j0; j < j1; ++j) {
+        const size_t idx = ((size_t)g * nT + j) * E + e;
+        hs += tile_hist[idx];
+        ps += tile_P[idx];
       }
-      row[tok] = r;
+    sh_h[warp][lane] = hs;
+    sh_p[warp][lane] = ps;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += sh_h[w][lane];
+    if (ev)
+      for (int j = j0; j < j1; ++j) {
+        const size_t idx = ((size_t)g * nT + j) * E + e;
+        tile_base[idx] = base;
+        base += tile_hist[idx];
+      }
+    if (warp == 0) {
+      int tot = 0;
+      float psum = 0.f;
+      for (int w = 0; w < SCAN_WARPS; ++w) {
+        tot += sh_h[w][lane];
+        psum += sh_p[w][lane];
+      }
+      float contrib = 0.f;
+      if (ev) {
+        const size_t ge = (size_t)g * E + e;
+        const int acc = min(tot, C);
+        const float Pv = T > 0 ? psum / (float)T : 0.f;
+        raw[ge] = tot;
+        accepted[ge] = acc;
+        P[ge] = Pv;
+        group_off[ge] = rows_run;
+        rows_run += acc;
+        contrib = (float)tot * Pv;
+      }
+      contrib = warp_sum(contrib);
+      if (lane == 0) partial[(size_t)g * gridDim.x + blockIdx.x] = contrib;
+    }
+    __syncthreads();
+  }
+  if (warp == 0 && ev) expert_rows[e] = rows_run;
+
+  // The last block to finish sums the per-block partials (fixed order) per group.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    float sum = 0.f;
+    for (int b = 0; b < (int)gridDim.x; ++b) sum += __ldcg(&partial[(size_t)g * gridDim.x + b]);
+    // E * sum_e f_e P_e with f_e = raw_e / T
+    const float bal = T > 0 ? (float)E * (sum / (float)T) : 0.f;
+    balance[g] = bal;
+    aux_g[g] = alpha * bal;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float total = 0.f;
+    for (int g = 0; g < G; ++g) total += aux_g[g];
+    aux[0] = G > 0 ? total / (float)G : 0.f;
+    *counter = 0u;
+  }
+}
+
+// ---------------------------------------------------------------- 4. slots, one thread per token
+__global__ void __launch_bounds__(256) route_slots_kernel(
+    const int32_t* __restrict__ expert, const int32_t* __restrict__ tile_base, const int32_t* __restrict__ group_off,
+    long long N, int T, int E, int nT, int C, int R, int32_t* __restrict__ slot, uint8_t* __restrict__ keep,
+    int32_t* __restrict__ row, int32_t* __restrict__ tok_of_row, bool debug, uint32_t* err) {
+  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (t >= N) return;
+  const int g = (int)(t / T);
+  const int ti = (int)(t - (long long)g * T);
+  const int e = expert[t];
+  if (e < 0 || e >= E) {  // the router never writes one; keep every access in bounds regardless
+    raise_error(err, ERR_BOUNDS);
+    slot[t] = 0;
+    keep[t] = 0;
+    row[t] = -1;
+    return;
+  }
+  const int s = tile_base[((size_t)g * nT + ti / ROUTE_TILE) * E + e] + slot[t];  // slot[] holds the rank
+  const bool k = s < C;
+  slot[t] = s;
+  keep[t] = k ? 1 : 0;
+  int r = -1;
+  if (k) {
+    r = group_off[(size_t)g * E + e] + s;
+    if (r < 0 || r >= R) {
+      if (debug) raise_error(err, ERR_BOUNDS);
+      r = -1;
+      keep[t] = 0;
+    } else {
+      tok_of_row[(size_t)e * R + r] = (int32_t)t;
     }
   }
+  row[t] = r;
 }
 
 // ---------------------------------------------------------------- launcher
 int launch_route(const RouteArgs& a, cudaStream_t s) {
-  const int N = a.G * a.T;
+  const long long N = (long long)a.G * a.T;
   const int nT = (a.T + ROUTE_TILE - 1) / ROUTE_TILE;
   int launches = 0;
   if (N > 0) {
-    dim3 grid((a.E + RL_BN - 1) / RL_BN, (N + RL_BM - 1) / RL_BM);
-    if (a.x_bf16)
-      router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)a.x, a.Wr, a.br, a.logits,
-                                                               N, a.d, a.E);
-    else
-      router_logits_kernel<float><<<grid, 256, 0, s>>>((const float*)a.x, a.Wr, a.br, a.logits, N, a.d, a.E);
-    ++launches;
-    route_softmax_kernel<<<dim3(nT, a.G), 256, a.E * sizeof(int32_t), s>>>(
-        a.logits, a.T, a.E, nT, a.expert, a.gate, a.tile_hist, a.tile_P, a.probs);
-    ++launches;
+    if (a.x_bf16) {
+      const int n = launch_router_tc(a, a.slot, s);
+      if (n < 0) return -1;
+      launches += n;
+    } else {
+      dim3 grid((a.E + RL_BN - 1) / RL_BN, (unsigned)((N + RL_BM - 1) / RL_BM));
+      router_logits_kernel<float><<<grid, 256, 0, s>>>((const float*)a.x, a.Wr, a.br, a.logits, (int)N, a.d, a.E);
+      route_softmax_kernel<<<dim3(nT, a.G), 256, a.E * sizeof(int32_t), s>>>(
+          a.logits, a.T, a.E, nT, a.expert, a.gate, a.slot, a.tile_hist, a.tile_P, a.probs, a.err);
+      launches += 2;
+    }
   }
-  route_scan_kernel<<<dim3((a.E + 255) / 256, a.G), 256, 0, s>>>(a.tile_hist, a.tile_P, a.tile_base, a.raw,
-                                                                 a.accepted, a.P, a.T, a.E, nT, a.C);
+  route_scan_kernel<<<route_scan_blocks(a.E), SCAN_WARPS * 32, 0, s>>>(
+      a.tile_hist, a.tile_P, a.G, a.T, a.E, nT, a.C, a.alpha, a.tile_base, a.raw, a.accepted, a.P, a.group_off,
+      a.expert_rows, a.balance, a.aux_g, a.aux, a.scan_partial, a.scan_counter);
   ++launches;
-  route_finalize_kernel<<<1, 1024, 0, s>>>(a.raw, a.accepted, a.P, a.G, a.T, a.E, a.alpha, a.balance, a.aux_g,
-                                           a.aux, a.group_off, a.expert_rows);
-  ++launches;
-  if (N > 0) {
-    route_slots_kernel<<<dim3((nT + SLOT_WARPS - 1) / SLOT_WARPS, a.G), SLOT_WARPS * 32,
-                         SLOT_WARPS * a.E * sizeof(int32_t), s>>>(a.expert, a.tile_base, a.group_off, a.T, a.E,
-                                                                  nT, a.C, a.R, a.slot, a.keep, a.row,
-                                                                  a.tok_of_row, a.debug, a.err);
+  if (N > 0 && a.slots) {
+    route_slots_kernel<<<(unsigned)((N + 255) / 256), 256, 0, s>>>(a.expert, a.tile_base, a.group_off, N, a.T, a.E,
+                                                                   nT, a.C, a.R, a.slot, a.keep, a.row,
+                                                                   a.tok_of_row, a.debug, a.err);
     ++launches;
   }
   if (cudaGetLastError() != cudaSuccess) return -1;
