@@ -140,7 +140,7 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_err = take(sizeof(uint32_t) * 4);  // [0] error word, [1] scan counter
   // float32 logits are materialised only by the CUDA-core router (float32 activations)
   const size_t o_logits = take(cfg->dtype == SWITCH_F32 ? N * E * sizeof(float) : 0);
-  const size_t o_wsplit = take(cfg->dtype == SWITCH_BF16 ? 3 * E * d * 2 : 0);
+  const size_t o_wsplit = take(cfg->dtype == SWITCH_BF16 ? router_tc_wsplit_bytes(cfg->E, cfg->d_model) : 0);
   const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
   const size_t o_hist = take(G * nT * E * sizeof(int32_t));
   const size_t o_tP = take(G * nT * E * sizeof(float));

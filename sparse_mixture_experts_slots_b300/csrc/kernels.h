@@ -52,6 +52,12 @@ int launch_route(const RouteArgs& a, cudaStream_t s);
 // asked, logits_out / probs.  Returns launches or -1.
 int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s);
 int router_tc_experts_per_cta(int E);
+int router_tc_mma_n(int EC);
+// Bytes of the split W_r workspace ([Q][hi, mid, lo][EC][d] bf16) for E experts of width d.
+size_t router_tc_wsplit_bytes(int E, int d);
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
 
 // 2-D bf16 tensor map [rows, cols] (cols contiguous), box box_rows x 64 columns, 128-byte swizzle.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);

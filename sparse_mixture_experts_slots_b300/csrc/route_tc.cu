@@ -6,21 +6,25 @@
 // is exact in bfloat16; W_r is float32 and is split into three bfloat16 pieces
 // hi + mid + lo whose sum equals w to within 2^-24 |w| (each piece holds the
 // next 8 bits of the significand).  Then
-//     z = x . hi + x . (mid + lo)
+//     z = x . hi + (x . mid + x . lo)
 // with every bf16 x bf16 product exact and accumulated in float32 by the tensor
-// cores: two TMEM accumulators (hi and the correction) so the small terms do not
-// share an accumulator with the large ones; they are added in the epilogue.
+// cores, each piece in its own TMEM accumulator so the small terms never share an
+// accumulator with the large ones; the pieces are added in the epilogue.
 //
 // One CTA (or a cluster of Q CTAs, each with EC experts) takes a tile of 128
 // tokens of one routing group:
-//   warp 0, one lane : TMA producer (x tiles in one ring, W_r pieces in another)
-//   warp 1, one lane : MMA issuer (M = 128 tokens, N = EC experts, K = 16 per op)
-//   4 warps          : epilogue; thread i owns token i (TMEM lane i):
-//     pass 1  logits z (+ bias), local max / argmax (ties -> lowest index), local sum
+//   warp 0, one lane : TMA producer; one stage = the x tile and the slice's three
+//                      W pieces for 64 or 128 columns of K, behind one barrier
+//   warp 1, one lane : MMA issuer (M = 128 tokens, N = 3 EC rows of pieces, K = 16)
+//   16 warps         : epilogue; warp w reads TMEM lane quadrant w % 4 (32 tokens)
+//                      and column group w / 4 (a quarter of the CTA's experts):
+//     pass 1  logits z (+ bias) into registers, max / argmax (ties -> lowest index),
+//             combined over the column groups through shared memory
+//     pass 1b exp(z - max) in registers (ex2 of the log2e-scaled difference), sums
 //     exchange of (max, sum, argmax) between the Q CTAs through distributed shared memory
-//     pass 2  p = exp(z - max) / sum; column sums over the tile's tokens (warp
-//             reduce-scatter), expert histogram of the tile, rank of each token
-//             among the tile's earlier tokens with the same expert.
+//     pass 2  p = exp(z - max) * exp(max - Max) / Sum; column sums over the tile's
+//             tokens (warp reduce-scatter), expert histogram of the tile, rank of
+//             each token among the tile's earlier tokens with the same expert.
 // Outputs per token: expert (raw choice), gate = p_{expert}, rank in tile; per
 // (group, tile, expert): token count and probability sum.  The cross-tile scan
 // that turns ranks into slots runs in route.cu.
@@ -33,56 +37,106 @@ namespace smoe {
 
 constexpr int RT_BM = ROUTE_TILE;  // 128 tokens per tile
 constexpr int RT_BK = 64;          // 64 bf16 = one 128-byte swizzle row
+constexpr int RT_THREADS = 512;    // 16 warps: 4 TMEM lane quadrants x 4 column groups
+constexpr float LOG2E = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- W_r -> hi, mid, lo
-__global__ void router_split_kernel(const float* __restrict__ Wr, __nv_bfloat16* __restrict__ ws, long long n) {
+// Layout of the pieces: [Q slices][hi, mid, lo][EC experts][d], experts past E zero, so
+// one TMA box (and one MMA) covers all three pieces of a slice's experts.
+__global__ void router_split_kernel(const float* __restrict__ Wr, __nv_bfloat16* __restrict__ ws, int E, int d,
+                                    int EC, long long n /* Q * EC * d */) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
-    const float w = Wr[i];
+    const long long row = i / d;  // q * EC + el = expert index
+    const int k = (int)(i - row * d);
+    const int q = (int)(row / EC), el = (int)(row - (long long)q * EC);
+    const float w = row < E ? Wr[row * d + k] : 0.f;
     const __nv_bfloat16 hi = __float2bfloat16_rn(w);
     const float r1 = w - __bfloat162float(hi);  // exact: fits in the 24-bit significand
     const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
     const float r2 = r1 - __bfloat162float(mid);  // exact
-    ws[i] = hi;
-    ws[n + i] = mid;
-    ws[2 * n + i] = __float2bfloat16_rn(r2);
+    const size_t base = ((size_t)q * 3 * EC + el) * d + k;
+    ws[base] = hi;
+    ws[base + (size_t)EC * d] = mid;
+    ws[base + (size_t)2 * EC * d] = __float2bfloat16_rn(r2);
   }
 }
 
-// ---------------------------------------------------------------- shared memory layout
+// ---------------------------------------------------------------- tiling
+// Per 64-column atom of K, a stage holds the x tile (128 tokens) and the 3 * EC rows of
+// W pieces of the CTA's slice, in WBOXES boxes of MMA_N rows; MMA m takes box m.
+// Accumulators in TMEM: one block of EC columns per piece (hi, mid, lo); with EC = 256
+// the 512 columns hold hi and (mid + lo).
 template <int EC>
-struct RtCfg {
-  static constexpr int XS = EC >= 128 ? 2 : 3;  // x-tile ring depth
-  static constexpr int WS = EC >= 128 ? 4 : 6;  // W-piece ring depth
-  static constexpr int X_BYTES = RT_BM * RT_BK * 2;
-  static constexpr int W_BYTES = EC * RT_BK * 2;
-  static constexpr int RING_BYTES = XS * X_BYTES + WS * W_BYTES;
-  static constexpr uint32_t TMEM_COLS = 2 * EC < 32 ? 32 : 2 * EC;  // hi + correction accumulators
-  static_assert(EC % 16 == 0 && EC >= 16 && EC <= 256, "tcgen05 M=128 takes N = 16..256 in steps of 16");
-  static_assert((EC & (EC - 1)) == 0, "EC is a power of two (TMEM allocation)");
-  static_assert(X_BYTES % 1024 == 0 && W_BYTES % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+struct RtGeom {
+  static constexpr int WROWS = 3 * EC;
+  static constexpr int MMA_N = EC == 256 ? 256 : (WROWS <= 256 ? WROWS : 192);
+  static constexpr int WBOXES = WROWS / MMA_N;
+  static constexpr int ACC_BLOCKS = EC == 256 ? 2 : 3;
+  static constexpr uint32_t TMEM_COLS = ACC_BLOCKS * EC <= 32 ? 32 : ACC_BLOCKS * EC <= 64 ? 64
+                                       : ACC_BLOCKS * EC <= 128 ? 128 : ACC_BLOCKS * EC <= 256 ? 256 : 512;
+  // first TMEM column written by MMA m
+  static __device__ __forceinline__ uint32_t dcol(int m) { return EC == 256 ? (m == 0 ? 0u : 256u) : (uint32_t)(m * MMA_N); }
+  static_assert(WROWS % MMA_N == 0 && MMA_N % 16 == 0 && MMA_N <= 256, "tcgen05 M=128 takes N = 16..256, step 16");
+  static_assert((MMA_N * 128) % 1024 == 0, "every W box starts on a swizzle atom");
 };
 
-template <int EC>
-struct RtShared {
-  uint64_t xfull[RtCfg<EC>::XS], xempty[RtCfg<EC>::XS];
-  uint64_t wfull[RtCfg<EC>::WS], wempty[RtCfg<EC>::WS];
+// DEEP: one CTA per SM with ~170-220 KB of loads in flight (a grid that fits in one
+// wave); !DEEP: two CTAs per SM (each <= 113 KB, <= 256 TMEM columns), so one CTA's
+// epilogue overlaps the other's main loop on larger grids.  Each stage is one barrier
+// phase: per-phase cost, not bytes, limits a CTA's TMA stream, so stages are large.
+template <int EC, bool DEEP>
+struct RtCfg {
+  using G = RtGeom<EC>;
+  static constexpr int NA = (EC <= 16 || (EC <= 64 && DEEP)) ? 2 : 1;  // 64-column atoms per stage
+  static constexpr int X_ATOM = RT_BM * RT_BK * 2;                    // 16 KB
+  static constexpr int W_ATOM = G::WROWS * RT_BK * 2;
+  static constexpr int STAGE_BYTES = NA * (X_ATOM + W_ATOM);
+  static constexpr int RING_BUDGET = DEEP ? 224 * 1024 : 110 * 1024;
+  static constexpr int STAGES = RING_BUDGET / STAGE_BYTES < 4 ? RING_BUDGET / STAGE_BYTES : 4;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static_assert(STAGES >= 2, "double buffering at least");
+  static_assert(DEEP || G::TMEM_COLS <= 256, "two CTAs per SM share the 512 TMEM columns");
+};
+
+template <int EC, bool DEEP>
+struct RtBars {
+  uint64_t full[RtCfg<EC, DEEP>::STAGES], empty[RtCfg<EC, DEEP>::STAGES];
   uint64_t accb;
   uint32_t tmem_slot;
   volatile int abort_flag;
-  float m[RT_BM];     // local (this CTA's experts) max logit per token
-  float s[RT_BM];     // local sum of exp(z - m)
-  int a[RT_BM];       // local argmax
-  int texp[RT_BM];    // final expert per token (-1 past the group's end)
-  float colsum[4][EC];
+};
+
+// Epilogue scratch; it reuses the ring's shared memory once every MMA has completed.
+template <int EC>
+struct RtScratch {
+  float red_m[4][RT_BM];  // per column group: max logit of each token
+  int red_a[4][RT_BM];    // per column group: argmax
+  float red_s[4][RT_BM];  // per column group: sum of exp(z - m)
+  float m[RT_BM];         // this CTA's experts: max logit per token (read by cluster peers)
+  float s[RT_BM];         // this CTA's experts: sum of exp(z - m)
+  int a[RT_BM];           // this CTA's experts: argmax
+  float Mall[RT_BM];      // all experts: max logit per token
+  float Sall[RT_BM];      // all experts: sum of exp(z - Mall)
+  int texp[RT_BM];        // final expert per token (-1 past the group's end)
+  float colsum[4][EC];    // per lane quadrant: probability sums of the columns
   int hist[EC];
   float bias[EC];
 };
 
-template <int EC>
+template <int EC, bool DEEP>
 constexpr int rt_smem_bytes() {
-  return RtCfg<EC>::RING_BYTES + (int)sizeof(RtShared<EC>) + 1024;
+  return RtCfg<EC, DEEP>::RING_BYTES + (int)sizeof(RtBars<EC, DEEP>) + 1024;
 }
+static_assert(sizeof(RtScratch<256>) <= RtCfg<256, true>::RING_BYTES, "scratch fits in the ring");
+static_assert(sizeof(RtScratch<16>) <= RtCfg<16, false>::RING_BYTES, "scratch fits in the ring");
+static_assert(rt_smem_bytes<256, true>() <= 227 * 1024 && rt_smem_bytes<128, true>() <= 227 * 1024 &&
+                  rt_smem_bytes<64, true>() <= 227 * 1024 && rt_smem_bytes<32, true>() <= 227 * 1024 &&
+                  rt_smem_bytes<16, true>() <= 227 * 1024,
+              "deep ring fits in one SM's shared memory");
+static_assert(rt_smem_bytes<64, false>() <= 113 * 1024 && rt_smem_bytes<32, false>() <= 113 * 1024 &&
+                  rt_smem_bytes<16, false>() <= 113 * 1024,
+              "shallow ring lets two CTAs share an SM");
 
 // Sum of v over the 32 lanes for 16 columns at once (reduce-scatter).  On return,
 // lane L holds the warp's total of column (L >> 1) & 15 (lanes L and L^1 agree).
@@ -115,19 +169,19 @@ __device__ __forceinline__ float warp_colsum16(const float (&p)[16], int lane) {
 
 // ---------------------------------------------------------------- the router kernel
 // grid (Q * nT, G); clusters of Q CTAs along x when Q > 1.
-template <int EC>
-__global__ void __launch_bounds__(128, 1)
+template <int EC, bool DEEP>
+__global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const float* __restrict__ br, int T, int E, int d, int nT, int Q,
                      int32_t* __restrict__ expert, float* __restrict__ gate, int32_t* __restrict__ rank,
                      int32_t* __restrict__ tile_hist, float* __restrict__ tile_P, float* __restrict__ logits,
                      float* __restrict__ probs, uint32_t* err) {
-  using Cf = RtCfg<EC>;
+  using Cf = RtCfg<EC, DEEP>;
+  using Gm = RtGeom<EC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sX = smem;
-  uint8_t* sW = smem + Cf::XS * Cf::X_BYTES;
-  RtShared<EC>& sh = *reinterpret_cast<RtShared<EC>*>(smem + Cf::RING_BYTES);
+  RtBars<EC, DEEP>& bar = *reinterpret_cast<RtBars<EC, DEEP>*>(smem + Cf::RING_BYTES);
+  RtScratch<EC>& sh = *reinterpret_cast<RtScratch<EC>*>(smem);  // valid after the main loop
 
   const int q = Q > 1 ? (int)cluster_ctarank() : 0;
   const int tile = blockIdx.x / Q;
@@ -136,198 +190,227 @@ __global__ void __launch_bounds__(128, 1)
   const int t0 = tile * RT_BM;
   const long long tok0 = (long long)g * T + t0;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int KB = (d + RT_BK - 1) / RT_BK;
+  const int NST = (d + Cf::NA * RT_BK - 1) / (Cf::NA * RT_BK);  // stages along K
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Cf::XS; ++i) {
-      mbar_init(&sh.xfull[i], 1);
-      mbar_init(&sh.xempty[i], 1);
+    for (int i = 0; i < Cf::STAGES; ++i) {
+      mbar_init(&bar.full[i], 1);
+      mbar_init(&bar.empty[i], 1);
     }
-    for (int i = 0; i < Cf::WS; ++i) {
-      mbar_init(&sh.wfull[i], 1);
-      mbar_init(&sh.wempty[i], 1);
-    }
-    mbar_init(&sh.accb, 1);
-    sh.abort_flag = 0;
+    mbar_init(&bar.accb, 1);
+    bar.abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
   }
-  for (int c = threadIdx.x; c < EC; c += blockDim.x) {
-    const int e = e0 + c;
-    sh.bias[c] = (br && e < E) ? br[e] : 0.f;
-    sh.hist[c] = 0;
-  }
   if (warp == 1) {
-    tmem_alloc(&sh.tmem_slot, Cf::TMEM_COLS);
+    tmem_alloc(&bar.tmem_slot, Gm::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = sh.tmem_slot;
+  const uint32_t tmem = bar.tmem_slot;
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
-    int xi = 0, wi = 0;  // loads issued into each ring
+    int issued = 0;
     bool ok = true;
-    for (int kb = 0; kb < KB && ok; ++kb) {
-      const int xs = kb % Cf::XS;
-      if (kb >= Cf::XS && !mbar_wait(&sh.xempty[xs], ((kb / Cf::XS) - 1) & 1)) { ok = false; break; }
-      if (sh.abort_flag) { ok = false; break; }
-      mbar_arrive_expect_tx(&sh.xfull[xs], Cf::X_BYTES);
-      tma_load_2d(sX + xs * Cf::X_BYTES, &tmX, &sh.xfull[xs], kb * RT_BK, (int)tok0);
-      xi = kb + 1;
-      for (int s = 0; s < 3; ++s) {
-        const int j = kb * 3 + s, ws = j % Cf::WS;
-        if (j >= Cf::WS && !mbar_wait(&sh.wempty[ws], ((j / Cf::WS) - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(&sh.wfull[ws], Cf::W_BYTES);
-        tma_load_2d(sW + ws * Cf::W_BYTES, &tmW, &sh.wfull[ws], kb * RT_BK, s * E + e0);
-        wi = j + 1;
+    for (int st = 0; st < NST; ++st) {
+      const int slot = st % Cf::STAGES;
+      if (st >= Cf::STAGES && !mbar_wait(&bar.empty[slot], ((st / Cf::STAGES) - 1) & 1)) { ok = false; break; }
+      if (bar.abort_flag) { ok = false; break; }
+      const int na = min(Cf::NA, (d - st * Cf::NA * RT_BK + RT_BK - 1) / RT_BK);  // atoms inside d
+      mbar_arrive_expect_tx(&bar.full[slot], (uint32_t)(na * (Cf::X_ATOM + Cf::W_ATOM)));
+      uint8_t* stage = smem + slot * Cf::STAGE_BYTES;
+      for (int at = 0; at < na; ++at) {
+        const int kx = (st * Cf::NA + at) * RT_BK;
+        tma_load_2d(stage + at * Cf::X_ATOM, &tmX, &bar.full[slot], kx, (int)tok0);
+        for (int b = 0; b < Gm::WBOXES; ++b)
+          tma_load_2d(stage + Cf::NA * Cf::X_ATOM + at * Cf::W_ATOM + b * Gm::MMA_N * 128, &tmW, &bar.full[slot], kx,
+                      q * Gm::WROWS + b * Gm::MMA_N);
       }
+      issued = st + 1;
     }
     if (!ok) {
       raise_error(err, ERR_TIMEOUT);
-      sh.abort_flag = 1;
+      bar.abort_flag = 1;
     }
     // Drain: every copy started here has landed before the CTA can leave.
-    for (int i = xi > Cf::XS ? xi - Cf::XS : 0; i < xi; ++i)
-      if (!mbar_wait(&sh.xfull[i % Cf::XS], (i / Cf::XS) & 1)) raise_error(err, ERR_TIMEOUT);
-    for (int i = wi > Cf::WS ? wi - Cf::WS : 0; i < wi; ++i)
-      if (!mbar_wait(&sh.wfull[i % Cf::WS], (i / Cf::WS) & 1)) raise_error(err, ERR_TIMEOUT);
+    for (int i = issued > Cf::STAGES ? issued - Cf::STAGES : 0; i < issued; ++i)
+      if (!mbar_wait(&bar.full[i % Cf::STAGES], (i / Cf::STAGES) & 1)) raise_error(err, ERR_TIMEOUT);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(RT_BM, EC);
+    constexpr uint32_t idesc = idesc_bf16_f32(RT_BM, Gm::MMA_N);
     bool ok = true;
-    for (int kb = 0; kb < KB && ok; ++kb) {
-      const int xs = kb % Cf::XS;
-      if (!mbar_wait(&sh.xfull[xs], (kb / Cf::XS) & 1)) { ok = false; break; }
-      for (int s = 0; s < 3; ++s) {
-        const int j = kb * 3 + s, ws = j % Cf::WS;
-        if (!mbar_wait(&sh.wfull[ws], (j / Cf::WS) & 1)) { ok = false; break; }
-        if (sh.abort_flag) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(sX + xs * Cf::X_BYTES);
-        const uint32_t b0 = smem_u32(sW + ws * Cf::W_BYTES);
-        const uint32_t acc = s == 0 ? tmem : tmem + EC;
+    for (int st = 0; st < NST && ok; ++st) {
+      const int slot = st % Cf::STAGES;
+      if (!mbar_wait(&bar.full[slot], (st / Cf::STAGES) & 1)) { ok = false; break; }
+      if (bar.abort_flag) { ok = false; break; }
+      tc_fence_after();
+      const int na = min(Cf::NA, (d - st * Cf::NA * RT_BK + RT_BK - 1) / RT_BK);
+      const uint32_t stage = smem_u32(smem + slot * Cf::STAGE_BYTES);
+      for (int at = 0; at < na; ++at) {
+        const uint32_t xa = stage + at * Cf::X_ATOM;
+        const uint32_t wa = stage + Cf::NA * Cf::X_ATOM + at * Cf::W_ATOM;
 #pragma unroll
-        for (int k = 0; k < RT_BK / 16; ++k)
-          tc_mma_bf16(acc, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32), idesc,
-                      (kb > 0 || k > 0 || s == 2) ? 1u : 0u);
-        tc_commit(&sh.wempty[ws]);
+        for (int kk = 0; kk < RT_BK / 16; ++kk)
+#pragma unroll
+          for (int mm = 0; mm < Gm::WBOXES; ++mm) {
+            const bool first = st == 0 && at == 0 && kk == 0 && !(EC == 256 && mm == 2);
+            tc_mma_bf16(tmem + Gm::dcol(mm), sw128_kmajor_desc(xa + kk * 32),
+                        sw128_kmajor_desc(wa + mm * Gm::MMA_N * 128 + kk * 32), idesc, first ? 0u : 1u);
+          }
       }
-      if (ok) tc_commit(&sh.xempty[xs]);
+      tc_commit(&bar.empty[slot]);
     }
     if (!ok) {
       raise_error(err, ERR_TIMEOUT);
-      sh.abort_flag = 1;
+      bar.abort_flag = 1;
     }
-    tc_commit(&sh.accb);  // arrives once every MMA issued above has completed
+    tc_commit(&bar.accb);  // arrives once every MMA issued above has completed
   }
   __syncwarp();
 
   // ---------------- epilogue
-  if (!mbar_wait(&sh.accb, 0)) {
+  if (!mbar_wait(&bar.accb, 0)) {
     raise_error(err, ERR_TIMEOUT);
-    sh.abort_flag = 1;
+    bar.abort_flag = 1;
   }
   tc_fence_after();
+  __syncthreads();  // every MMA has read its operands: the ring is scratch from here on
+  const bool run = bar.abort_flag == 0;
+  for (int c = threadIdx.x; c < EC; c += blockDim.x) {
+    const int e = e0 + c;
+    sh.bias[c] = (br && e < E) ? br[e] : 0.f;
+    sh.hist[c] = 0;
+  }
   __syncthreads();
-  const bool run = sh.abort_flag == 0;
 
-  const int i = warp * 32 + lane;
+  // Warp w reads TMEM lane quadrant lq = w % 4 (tokens 32 lq .. 32 lq + 31) and column
+  // group cg = w / 4 (CPW consecutive experts); NCG groups cover the CTA's EC experts.
+  constexpr int NCG = EC >= 64 ? 4 : EC / 16;
+  constexpr int CPW = EC / NCG;
+  const int lq = warp & 3, cg = warp >> 2;
+  const bool has_cols = cg < NCG;
+  const int cbeg = cg * CPW;
+  const int i = lq * 32 + lane;
   const bool valid = t0 + i < T;
   const long long tok = tok0 + i;
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t trow = tmem + ((uint32_t)(lq * 32) << 16);
 
-  // pass 1: local max / argmax (increasing e, strict >: the lowest index wins a tie), local sum
-  float m = -INFINITY, ssum = 0.f;
+  // pass 1: logits z (+ bias) into registers; max / argmax over this warp's columns
+  // (increasing e with strict >, so the lowest index wins a tie)
+  float v[CPW];
+  float m = -INFINITY;
   int a = INT_MAX;
-  if (run) {
-#pragma unroll 1
-    for (int c0 = 0; c0 < EC; c0 += 16) {
-      uint32_t h[16], r[16];
-      tmem_ld16(trow + c0, h);
-      tmem_ld16(trow + EC + c0, r);
+  if (run && has_cols) {
+#pragma unroll
+    for (int ch = 0; ch < CPW / 16; ++ch) {
+      const uint32_t col = (uint32_t)(cbeg + ch * 16);
+      uint32_t h[16], r1[16], r2[16];
+      tmem_ld16(trow + col, h);
+      tmem_ld16(trow + EC + col, r1);
+      if (Gm::ACC_BLOCKS == 3) tmem_ld16(trow + 2 * EC + col, r2);
       tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int e = e0 + c0 + j;
-        if (e < E) {
-          const float z = (__uint_as_float(h[j]) + __uint_as_float(r[j])) + sh.bias[c0 + j];
-          if (z > m) { m = z; a = e; }
-          if (logits && valid) logits[tok * E + e] = z;
+        const int c = cbeg + ch * 16 + j;
+        const float corr = Gm::ACC_BLOCKS == 3 ? __uint_as_float(r1[j]) + __uint_as_float(r2[j])
+                                                : __uint_as_float(r1[j]);
+        const float z = (__uint_as_float(h[j]) + corr) + sh.bias[c];
+        v[ch * 16 + j] = z;
+        if (e0 + c < E) {
+          if (z > m) { m = z; a = e0 + c; }
+          if (logits && valid) logits[tok * E + e0 + c] = z;
         }
       }
     }
-#pragma unroll 1
-    for (int c0 = 0; c0 < EC; c0 += 16) {
-      uint32_t h[16], r[16];
-      tmem_ld16(trow + c0, h);
-      tmem_ld16(trow + EC + c0, r);
-      tmem_ld_wait();
+  }
+  if (has_cols) {
+    sh.red_m[cg][i] = m;
+    sh.red_a[cg][i] = a;
+  }
+  __syncthreads();
+  float mc = -INFINITY;  // max over this CTA's experts
+  int ac = INT_MAX;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int e = e0 + c0 + j;
-        if (e < E) ssum += expf((__uint_as_float(h[j]) + __uint_as_float(r[j])) + sh.bias[c0 + j] - m);
-      }
+  for (int k = 0; k < NCG; ++k)
+    if (sh.red_m[k][i] > mc) { mc = sh.red_m[k][i]; ac = sh.red_a[k][i]; }
+
+  // pass 1b: exp(z - mc) in registers, partial sums
+  float ps = 0.f;
+  if (run && has_cols) {
+    const float mcs = mc * LOG2E;
+#pragma unroll
+    for (int k = 0; k < CPW; ++k) {
+      const float ex = (e0 + cbeg + k < E) ? ex2_approx(fmaf(v[k], LOG2E, -mcs)) : 0.f;
+      v[k] = ex;
+      ps += ex;
     }
   }
-  sh.m[i] = m;
-  sh.s[i] = ssum;
-  sh.a[i] = a;
+  if (has_cols) sh.red_s[cg][i] = ps;
+  __syncthreads();
+  if (cg == 0) {
+    float sc = 0.f;
+#pragma unroll
+    for (int k = 0; k < NCG; ++k) sc += sh.red_s[k][i];
+    sh.m[i] = mc;
+    sh.s[i] = sc;
+    sh.a[i] = ac;
+  }
 
   // exchange between the cluster's CTAs (expert slices in rank order)
   if (Q > 1) cluster_sync();
-  float M = m, S = ssum;
-  int A = a;
-  if (Q > 1) {
-    M = -INFINITY;
-    A = INT_MAX;
-    for (int rk = 0; rk < Q; ++rk) {
-      const float mr = dsmem_ld_f32(dsmem_addr(&sh.m[i], rk));
-      if (mr > M) {
-        M = mr;
-        A = dsmem_ld_s32(dsmem_addr(&sh.a[i], rk));
+  else __syncthreads();
+  if (cg == 0) {
+    float M = sh.m[i], S = sh.s[i];
+    int A = sh.a[i];
+    if (Q > 1) {
+      M = -INFINITY;
+      A = INT_MAX;
+      for (int rk = 0; rk < Q; ++rk) {
+        const float mr = dsmem_ld_f32(dsmem_addr(&sh.m[i], rk));
+        if (mr > M) {
+          M = mr;
+          A = dsmem_ld_s32(dsmem_addr(&sh.a[i], rk));
+        }
+      }
+      S = 0.f;
+      for (int rk = 0; rk < Q; ++rk) {
+        const float mr = dsmem_ld_f32(dsmem_addr(&sh.m[i], rk));
+        const float sr = dsmem_ld_f32(dsmem_addr(&sh.s[i], rk));
+        if (sr > 0.f) S += sr * expf(mr - M);
       }
     }
-    S = 0.f;
-    for (int rk = 0; rk < Q; ++rk) {
-      const float mr = dsmem_ld_f32(dsmem_addr(&sh.m[i], rk));
-      const float sr = dsmem_ld_f32(dsmem_addr(&sh.s[i], rk));
-      if (sr > 0.f) S += sr * expf(mr - M);
+    if (A < 0 || A >= E) {  // only non-finite logits (or an aborted tile) get here
+      if (run && valid) raise_error(err, ERR_BOUNDS);
+      A = 0;
     }
+    sh.Mall[i] = M;
+    sh.Sall[i] = S;
+    sh.texp[i] = valid ? A : -1;
   }
-  if (A < 0 || A >= E) {  // only non-finite logits (or an aborted tile) get here
-    if (run && valid) raise_error(err, ERR_BOUNDS);
-    A = 0;
-  }
-  sh.texp[i] = valid ? A : -1;
+  __syncthreads();
 
-  // pass 2: probabilities and their column sums over the tile
-#pragma unroll 1
-  for (int c0 = 0; c0 < EC; c0 += 16) {
-    float p[16];
-    if (run) {
-      uint32_t h[16], r[16];
-      tmem_ld16(trow + c0, h);
-      tmem_ld16(trow + EC + c0, r);
-      tmem_ld_wait();
+  // pass 2: p = exp(z - mc) * exp(mc - M) / S; column sums over the tile's tokens
+  const float scale = (run && valid) ? expf(mc - sh.Mall[i]) / sh.Sall[i] : 0.f;
+  if (has_cols) {
+#pragma unroll
+    for (int ch = 0; ch < CPW / 16; ++ch) {
+      float p[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int e = e0 + c0 + j;
-        const float z = (__uint_as_float(h[j]) + __uint_as_float(r[j])) + sh.bias[c0 + j];
-        p[j] = (valid && e < E) ? expf(z - M) / S : 0.f;
-        if (probs && valid && e < E) probs[tok * E + e] = p[j];
+        const int c = cbeg + ch * 16 + j;
+        p[j] = v[ch * 16 + j] * scale;  // 0 past E (v = 0) and for invalid tokens (scale = 0)
+        if (probs && valid && run && e0 + c < E) probs[tok * E + e0 + c] = p[j];
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) p[j] = 0.f;
+      const float cs = warp_colsum16(p, lane);
+      if ((lane & 1) == 0) sh.colsum[lq][cbeg + ch * 16 + (lane >> 1)] = cs;
     }
-    const float cs = warp_colsum16(p, lane);
-    if ((lane & 1) == 0) sh.colsum[warp][c0 + (lane >> 1)] = cs;
   }
-  if (valid && A >= e0 && A < e0 + EC) atomicAdd(&sh.hist[A - e0], 1);
+  const int A = sh.texp[i];
+  if (cg == 0 && A >= e0 && A < e0 + EC) atomicAdd(&sh.hist[A - e0], 1);
   __syncthreads();
 
   const size_t tbase = ((size_t)g * nT + tile) * E;
@@ -338,35 +421,35 @@ __global__ void __launch_bounds__(128, 1)
       tile_hist[tbase + e] = sh.hist[c];
     }
   }
-  if (q == 0) {
+  if (q == 0 && cg == 0) {
     // rank among the tile's earlier tokens with the same expert
     const int key = valid ? A : -1 - lane;
     const unsigned same = __match_any_sync(0xffffffffu, key);
     int rk = __popc(same & ((1u << lane) - 1u));
-    for (int j = 0; j < warp * 32; ++j) rk += sh.texp[j] == A;
+    for (int j = 0; j < lq * 32; ++j) rk += sh.texp[j] == A;
     if (valid) {
       expert[tok] = A;
-      gate[tok] = 1.0f / S;  // exp(z_A - M) / S with z_A = M; never renormalised
+      gate[tok] = 1.0f / sh.Sall[i];  // exp(z_A - M) / S with z_A = M; never renormalised
       rank[tok] = rk;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, Cf::TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem, Gm::TMEM_COLS);
   if (Q > 1) cluster_sync();  // peers are done reading this CTA's m / s / a
 }
 
 // ---------------------------------------------------------------- host side
-template <int EC>
+template <int EC, bool DEEP>
 static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteArgs& a, int nT, int Q,
                      int32_t* rank, cudaStream_t s) {
-  auto kern = router_tc_kernel<EC>;
-  constexpr int smem = rt_smem_bytes<EC>();
+  auto kern = router_tc_kernel<EC, DEEP>;
+  constexpr int smem = rt_smem_bytes<EC, DEEP>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(Q * nT), (unsigned)a.G, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.blockDim = dim3(RT_THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -391,6 +474,14 @@ int router_tc_experts_per_cta(int E) {
   return ec > want ? ec : want;
 }
 
+int router_tc_mma_n(int EC) { return EC == 256 ? 256 : (3 * EC <= 256 ? 3 * EC : 192); }
+
+size_t router_tc_wsplit_bytes(int E, int d) {
+  const int EC = router_tc_experts_per_cta(E);
+  const size_t Q = (size_t)((E + EC - 1) / EC);
+  return Q * EC * 3 * (size_t)d * 2;
+}
+
 int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
   const long long N = (long long)a.G * a.T;
   if (N == 0) return 0;
@@ -398,21 +489,27 @@ int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
   const int EC = router_tc_experts_per_cta(a.E);
   const int Q = (a.E + EC - 1) / EC;
   if (EC > 256 || Q > 8) return -1;
-  const long long n = (long long)a.E * a.d;
+  const long long n = (long long)Q * EC * a.d;
   const unsigned sb = (unsigned)((n + 255) / 256 < 148 * 16 ? (n + 255) / 256 : 148 * 16);
-  router_split_kernel<<<sb, 256, 0, s>>>(a.Wr, (__nv_bfloat16*)a.wsplit, n);
+  router_split_kernel<<<sb, 256, 0, s>>>(a.Wr, (__nv_bfloat16*)a.wsplit, a.E, a.d, EC, n);
   if (cudaGetLastError() != cudaSuccess) return -1;
   CUtensorMap tmX, tmW;
   if (!encode_bf16_2d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM)) return -1;
-  if (!encode_bf16_2d(&tmW, a.wsplit, (uint64_t)3 * a.E, (uint64_t)a.d, (uint32_t)EC)) return -1;
+  if (!encode_bf16_2d(&tmW, a.wsplit, (uint64_t)3 * Q * EC, (uint64_t)a.d, (uint32_t)router_tc_mma_n(EC))) return -1;
+  // One wave on this device's SMs -> the deep ring; EC = 256 always takes it (one CTA per SM).
+  const long long ctas = (long long)Q * nT * a.G;
+  const bool deep = EC >= 128 || ctas <= (long long)device_sm_count();
   int n2;
+#define SMOE_RT(ECV)                                                                        \
+  n2 = deep ? launch_rt<ECV, true>(tmX, tmW, a, nT, Q, rank, s) : launch_rt<ECV, false>(tmX, tmW, a, nT, Q, rank, s)
   switch (EC) {
-    case 16: n2 = launch_rt<16>(tmX, tmW, a, nT, Q, rank, s); break;
-    case 32: n2 = launch_rt<32>(tmX, tmW, a, nT, Q, rank, s); break;
-    case 64: n2 = launch_rt<64>(tmX, tmW, a, nT, Q, rank, s); break;
-    case 128: n2 = launch_rt<128>(tmX, tmW, a, nT, Q, rank, s); break;
-    default: n2 = launch_rt<256>(tmX, tmW, a, nT, Q, rank, s); break;
+    case 16: SMOE_RT(16); break;
+    case 32: SMOE_RT(32); break;
+    case 64: SMOE_RT(64); break;
+    case 128: n2 = launch_rt<128, true>(tmX, tmW, a, nT, Q, rank, s); break;
+    default: n2 = launch_rt<256, true>(tmX, tmW, a, nT, Q, rank, s); break;
   }
+#undef SMOE_RT
   return n2 < 0 ? -1 : 2;
 }
 
