@@ -27,6 +27,8 @@ struct switch_layer {
   int32_t* group_off;
   int32_t* tok_of_row;
   void* wsplit;
+  uint32_t* ffn_counters;
+  int ffn_counter_words;
   float* scan_partial;
   uint32_t* scan_counter;
   void* xe;
@@ -142,6 +144,8 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_logits = take(cfg->dtype == SWITCH_F32 ? N * E * sizeof(float) : 0);
   const size_t o_wsplit = take(cfg->dtype == SWITCH_BF16 ? router_tc_wsplit_bytes(cfg->E, cfg->d_model) : 0);
   const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
+  const size_t ffn_words = ffn_counter_words(cfg->E, (int)R);
+  const size_t o_fcnt = take(ffn_words * sizeof(uint32_t));
   const size_t o_hist = take(G * nT * E * sizeof(int32_t));
   const size_t o_tP = take(G * nT * E * sizeof(float));
   const size_t o_base = take(G * nT * E * sizeof(int32_t));
@@ -165,6 +169,8 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->tok_of_row = reinterpret_cast<int32_t*>(h->ws + o_tor);
   h->wsplit = h->ws + o_wsplit;
   h->scan_partial = reinterpret_cast<float*>(h->ws + o_part);
+  h->ffn_counters = reinterpret_cast<uint32_t*>(h->ws + o_fcnt);
+  h->ffn_counter_words = (int)ffn_words;
   h->scan_counter = h->err + 1;
   h->xe = h->ws + o_xe;
   h->hbuf = h->ws + o_h;
@@ -254,20 +260,53 @@ switch_status switch_dispatch(switch_handle h, const void* x, const switch_route
                   h);
 }
 
-static switch_status run_ffn(switch_handle h, const void* xe, const void* W1, const void* b1, const void* W2,
-                             const void* b2, const int32_t* rows, void* ye, cudaStream_t s, int ev_mid) {
+static bool use_tc_ffn(const switch_layer* h) {
+  const switch_config& c = h->cfg;
+  return c.dtype == SWITCH_BF16 && tc_shape_ok(c.d_ff, c.d_model) && tc_shape_ok(c.d_model, c.d_ff);
+}
+
+// Both FFN layers on the tensor cores (one persistent kernel).  combine: write y in
+// token order (gate * expert output, + x_residual) instead of ye.
+static switch_status run_ffn_tc(switch_handle h, const void* xe, const void* W1, const void* b1, const void* W2,
+                                const void* b2, const int32_t* rows, void* out, bool combine,
+                                const switch_route_out* r, const void* resid, cudaStream_t s) {
+  const switch_config& c = h->cfg;
+  FfnLaunch L;
+  L.xe = xe;
+  L.W1 = W1;
+  L.b1 = b1;
+  L.W2 = W2;
+  L.b2 = b2;
+  L.h = h->hbuf;
+  L.out = out;
+  L.expert_rows = rows;
+  L.combine = combine;
+  L.tok_of_row = h->tok_of_row;
+  L.gate = r ? r->gate : nullptr;
+  L.resid = resid;
+  L.counters = h->ffn_counters;
+  L.err = h->err;
+  L.E = c.E;
+  L.R = h->R;
+  L.d = c.d_model;
+  L.F = c.d_ff;
+  const int n = launch_ffn_tc(L, s);
+  if (n < 0) return SWITCH_ERR_CUDA;
+  h->last_launches += n;
+  return SWITCH_OK;
+}
+
+// Both FFN layers on CUDA cores (float32, or widths the tensor-core tiles do not take).
+static switch_status run_ffn_simt(switch_handle h, const void* xe, const void* W1, const void* b1, const void* W2,
+                                  const void* b2, const int32_t* rows, void* ye, cudaStream_t s, int ev_mid) {
   const switch_config& c = h->cfg;
   const int E = c.E, R = h->R, d = c.d_model, F = c.d_ff;
   const bool bf16 = c.dtype == SWITCH_BF16;
-  const bool tc = bf16 && tc_shape_ok(F, d) && tc_shape_ok(d, F);
-  int n;
-  n = tc ? launch_grouped_linear_tc(xe, W1, b1, h->hbuf, rows, E, R, F, d, true, h->err, s)
-         : launch_grouped_linear_simt(xe, W1, b1, h->hbuf, rows, E, R, F, d, true, bf16, s);
+  int n = launch_grouped_linear_simt(xe, W1, b1, h->hbuf, rows, E, R, F, d, true, bf16, s);
   if (n < 0) return SWITCH_ERR_CUDA;
   h->last_launches += n;
   if (ev_mid >= 0) cudaEventRecord(h->ev[ev_mid], s);
-  n = tc ? launch_grouped_linear_tc(h->hbuf, W2, b2, ye, rows, E, R, d, F, false, h->err, s)
-         : launch_grouped_linear_simt(h->hbuf, W2, b2, ye, rows, E, R, d, F, false, bf16, s);
+  n = launch_grouped_linear_simt(h->hbuf, W2, b2, ye, rows, E, R, d, F, false, bf16, s);
   if (n < 0) return SWITCH_ERR_CUDA;
   h->last_launches += n;
   return SWITCH_OK;
@@ -278,7 +317,14 @@ switch_status switch_expert_ffn(switch_handle h, const void* xe, const void* W1,
   if (!h || !W1 || !W2 || !expert_rows) return SWITCH_ERR_INVALID_ARG;
   if (h->R > 0 && (!xe || !ye)) return SWITCH_ERR_INVALID_ARG;
   if (!aligned16(xe) || !aligned16(W1) || !aligned16(W2) || !aligned16(ye)) return SWITCH_ERR_INVALID_ARG;
-  return run_ffn(h, xe, W1, b1, W2, b2, expert_rows, ye, (cudaStream_t)stream, -1);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (use_tc_ffn(h)) {
+    if (h->R == 0) return SWITCH_OK;
+    if (cudaMemsetAsync(h->ffn_counters, 0, (size_t)h->ffn_counter_words * sizeof(uint32_t), s) != cudaSuccess)
+      return SWITCH_ERR_CUDA;
+    return run_ffn_tc(h, xe, W1, b1, W2, b2, expert_rows, ye, false, nullptr, nullptr, s);
+  }
+  return run_ffn_simt(h, xe, W1, b1, W2, b2, expert_rows, ye, s, -1);
 }
 
 switch_status switch_combine(switch_handle h, const void* ye, const switch_route_out* r, const void* x_residual,
@@ -307,14 +353,30 @@ switch_status switch_forward(switch_handle h, const void* x, const float* Wr, co
   st = launched(launch_route(a, s), h);
   if (st != SWITCH_OK) return st;
   if (prof) cudaEventRecord(h->ev[1], s);
-  st = launched(launch_dispatch_slots(x, h->xe, a, s), h);
+  const bool tc = use_tc_ffn(h);
+  // With the tensor-core FFN the combine happens in its epilogue: the dispatch pass
+  // writes the dropped tokens' rows of y and clears the FFN's scheduler counters.
+  st = launched(launch_dispatch_slots(x, h->xe, a, tc ? y : nullptr, tc ? x_residual : nullptr,
+                                      tc ? h->ffn_counters : nullptr, tc ? h->ffn_counter_words : 0, s),
+                h);
   if (st != SWITCH_OK) return st;
   if (prof) cudaEventRecord(h->ev[2], s);
-  st = run_ffn(h, h->xe, W1, b1, W2, b2, r->expert_rows, h->ye, s, prof ? 3 : -1);
-  if (st != SWITCH_OK) return st;
-  if (prof) cudaEventRecord(h->ev[4], s);
-  st = switch_combine(h, h->ye, r, x_residual, y, stream);
-  if (st != SWITCH_OK) return st;
+  if (tc) {
+    if (h->R > 0) {
+      st = run_ffn_tc(h, h->xe, W1, b1, W2, b2, r->expert_rows, y, true, r, x_residual, s);
+      if (st != SWITCH_OK) return st;
+    }
+    if (prof) {
+      cudaEventRecord(h->ev[3], s);
+      cudaEventRecord(h->ev[4], s);
+    }
+  } else {
+    st = run_ffn_simt(h, h->xe, W1, b1, W2, b2, r->expert_rows, h->ye, s, prof ? 3 : -1);
+    if (st != SWITCH_OK) return st;
+    if (prof) cudaEventRecord(h->ev[4], s);
+    st = switch_combine(h, h->ye, r, x_residual, y, stream);
+    if (st != SWITCH_OK) return st;
+  }
   if (prof) cudaEventRecord(h->ev[5], s);
   return SWITCH_OK;
 }

@@ -58,9 +58,12 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
     const int32_t* __restrict__ tile_base, const int32_t* __restrict__ group_off,
     const int32_t* __restrict__ expert_rows, int32_t* __restrict__ slot, uint8_t* __restrict__ keep,
     int32_t* __restrict__ row, int32_t* __restrict__ tok_of_row, long long N, int T, int E, int nT, int C, int R,
-    int vecs, bool debug, uint32_t* err) {
+    int vecs, bool debug, uint32_t* err, uint4* __restrict__ y, const uint4* __restrict__ resid,
+    uint32_t* __restrict__ zero_ptr, int zero_words) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const long long w = (long long)blockIdx.x * DC_WARPS + warp;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero_ptr[i] = 0u;
   if (w < N) {
     int r = -1, e = 0;
     if (lane == 0) {
@@ -91,7 +94,13 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
     }
     r = __shfl_sync(0xffffffffu, r, 0);
     e = __shfl_sync(0xffffffffu, e, 0);
-    if (r < 0) return;
+    if (r < 0) {
+      if (y) {  // a dropped token skips the expert: y is the residual alone, or zero
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        for (int v = lane; v < vecs; v += 32) y[w * vecs + v] = resid ? __ldg(resid + w * vecs + v) : zero;
+      }
+      return;
+    }
     const uint4* src = x + w * vecs;
     uint4* dst = xe + ((long long)e * R + r) * vecs;
     for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
@@ -106,17 +115,19 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
   for (int v = lane; v < vecs; v += 32) dst[v] = zero;
 }
 
-int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, cudaStream_t s) {
+int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, void* y, const void* resid,
+                          uint32_t* zero_ptr, int zero_words, cudaStream_t s) {
   const long long N = (long long)a.G * a.T;
-  const long long warps = N + (long long)a.E * a.R;
-  if (warps == 0) return 0;
+  long long warps = N + (long long)a.E * a.R;
+  if (warps == 0 && zero_words == 0) return 0;
+  if (warps == 0) warps = 1;  // one block still clears the words
   const int nT = (a.T + ROUTE_TILE - 1) / ROUTE_TILE;
   const int vecs = a.d * (a.x_bf16 ? 2 : 4) / 16;
   const unsigned blocks = (unsigned)((warps + DC_WARPS - 1) / DC_WARPS);
   dispatch_slots_kernel<<<blocks, DC_WARPS * 32, 0, s>>>((const uint4*)x, (uint4*)xe, a.expert, a.tile_base,
                                                          a.group_off, a.expert_rows, a.slot, a.keep, a.row,
                                                          a.tok_of_row, N, a.T, a.E, nT, a.C, a.R, vecs, a.debug,
-                                                         a.err);
+                                                         a.err, (uint4*)y, (const uint4*)resid, zero_ptr, zero_words);
   return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

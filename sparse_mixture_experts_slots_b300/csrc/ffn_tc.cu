@@ -1,23 +1,33 @@
-// Grouped expert linear layer on 5th-generation tensor cores (tcgen05, sm_103a).
+// Expert FFN of the Switch layer on 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// One CTA computes a 128 x BN tile of   out^T[m, n] = sum_k W[e, m, k] * in[e*R + n, k]
-// ("swap AB": the expert's weight rows fill the 128-row MMA; the expert's tokens,
-// often only a few dozen, are the N side).  The expert FFN of the Switch layer
-// is d -> d_ff, ReLU, d_ff -> d with biases ("混合专家", world.lapla.si/zh/moe,
-// section 专家里面是什么); bf16 operands with f32 accumulation follow the
-// bfloat16 expert computation of the Switch Transformers card (ai-papers.xuzou.cn,
-// 方法适配), where only the router runs in float32.
+// The expert FFN is d -> d_ff, ReLU, d_ff -> d with biases ("混合专家",
+// world.lapla.si/zh/moe, section 专家里面是什么); bf16 operands with float32
+// accumulation follow the bfloat16 expert computation of the Switch Transformers
+// card (ai-papers.xuzou.cn, 方法适配), where only the router runs in float32.
+// With the combine fused in, the second layer's epilogue writes
+//     y_t = gate_t * FFN(x_t) (+ x_t)
+// straight to token order ("042 · Switch Transformer：每个词只选一个专家", section 一;
+// the gate is used as is, never renormalised).
 //
-// Pipeline per CTA (128 threads):
-//   warp 0, one lane : TMA producer. Loads 128x64 bf16 tiles of W and BNx64 tiles
-//                      of the activations (128-byte swizzle) into a STAGES-deep ring.
-//   warp 1, one lane : MMA issuer. 4 x tcgen05.mma (K = 16 each) per stage into a
-//                      128-lane x BN-column f32 accumulator in TMEM; tcgen05.commit
-//                      frees the stage.
-//   warps 0-3        : epilogue. tcgen05.ld of their 32 TMEM lanes, + bias,
-//                      optional ReLU, bf16, store to out[e*R + n, m].
-// Every mbarrier wait is bounded; on timeout the CTA sets the error flag, drains
-// its own TMA copies and MMAs (bounded again), frees TMEM and returns.
+// One persistent kernel runs both layers of every expert.  A tile is
+//     out^T[m, n] = sum_k W[e, m, k] * in[e*R + n, k],  m in a 128-row block, n in a BN-row chunk
+// ("swap AB": the expert's weight rows fill the 128-row MMA, its tokens are the N side).
+// Layer-1 tiles (W1, input xe) write h; layer-2 tiles (W2, input h) write ye, or y
+// when the combine is fused.  Tiles are handed out by an atomic ticket in an order
+// that interleaves the layers: layer-1 tiles of expert s, then layer-2 tiles of
+// expert s - LOOK, so h is read back while it is still in L2; a layer-2 tile waits
+// (bounded) until all layer-1 tiles of its expert and chunk have been stored.
+//
+// Per CTA (one per SM, 192 threads):
+//   warp 0, one lane : scheduler + TMA producer.  Takes tickets, publishes each tile in a
+//                      small shared-memory queue, streams its W and activation tiles
+//                      (128-byte swizzle) into a ring of stages (one barrier each).
+//   warp 1, one lane : MMA issuer.  tcgen05.mma (M = 128, N = BN, K = 16) into one of two
+//                      TMEM accumulators, so the epilogue of a tile overlaps the next.
+//   warps 2-5        : epilogue.  tcgen05.ld, + bias, ReLU (layer 1), bf16, store;
+//                      layer 1 then publishes its chunk to the layer-2 tiles.
+// Every wait is bounded; on timeout the CTA sets the error flag, stops taking tiles,
+// drains its own copies and MMAs, frees TMEM and returns.
 #include <mutex>
 
 #include "common.cuh"
@@ -25,137 +35,346 @@
 
 namespace smoe {
 
-constexpr int TC_BM = 128;
-constexpr int TC_BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int FF_BM = 128;
+constexpr int FF_BK = 64;          // 64 bf16 = 128 bytes = one swizzle atom
+constexpr int FF_ATOM_A = FF_BM * FF_BK * 2;
+constexpr int FF_THREADS = 192;
+constexpr int FF_SCHED = 4;        // tile queue depth
+constexpr int FF_MAX_STAGES = 8;
+constexpr int FF_RING = 200 * 1024;
 
-template <int BN, int STAGES>
-struct TcLayout {
-  static constexpr int A_BYTES = TC_BM * TC_BK * 2;
-  static constexpr int B_BYTES = BN * TC_BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;  // barriers + 1024-byte alignment slack
-  static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;    // power of two >= 32
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0, 16..256");
-  static_assert((BN & (BN - 1)) == 0, "BN is a power of two here (TMEM allocation)");
+struct FfnParams {
+  const __nv_bfloat16* b1;       // [E, F] or null
+  const __nv_bfloat16* b2;       // [E, d] or null
+  __nv_bfloat16* h;              // [E * R, F]
+  __nv_bfloat16* out;            // ye [E * R, d], or y [N, d] with the combine
+  const int32_t* expert_rows;    // [E]
+  const int32_t* tok_of_row;     // [E * R] (combine)
+  const float* gate;             // [N] (combine)
+  const __nv_bfloat16* resid;    // [N, d] or null (combine)
+  uint32_t* next_tile;           // zero at launch
+  uint32_t* done1;               // [E * NCH], zero at launch
+  uint32_t* err;
+  int E, R, d, F, BN, NCH, LOOK, NA, STAGES, stage_bytes, combine, w_evict_first;
 };
 
-template <int BN, int STAGES, bool RELU>
-__global__ void __launch_bounds__(128, 1)
-    grouped_linear_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                             const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ out,
-                             const int32_t* __restrict__ expert_rows, int R, int M, int K, uint32_t* err) {
-  using L = TcLayout<BN, STAGES>;
+struct FfTile {
+  int layer, e, mt, nc;
+};
+
+// Ticket -> tile.  Per expert: S1 = NCH * F/128 layer-1 tiles, S2 = NCH * d/128 layer-2
+// tiles (m-block major, chunk minor).  Order: layer 1 of experts 0..L-1; then, for
+// s = L..E-1, layer 1 of s followed by layer 2 of s - L; then layer 2 of the last L.
+// Returns false past the last tile.
+__device__ __forceinline__ bool ff_decode(uint32_t t, const FfnParams& p, FfTile& tl) {
+  const uint32_t S1 = (uint32_t)p.NCH * (uint32_t)(p.F / FF_BM);
+  const uint32_t S2 = (uint32_t)p.NCH * (uint32_t)(p.d / FF_BM);
+  const uint32_t L = (uint32_t)min(p.LOOK, p.E);
+  const uint32_t E = (uint32_t)p.E;
+  uint32_t r;
+  if (t < L * S1) {
+    tl.layer = 0;
+    tl.e = (int)(t / S1);
+    r = t % S1;
+  } else if ((t -= L * S1) < (E - L) * (S1 + S2)) {
+    const uint32_t step = L + t / (S1 + S2);
+    r = t % (S1 + S2);
+    if (r < S1) {
+      tl.layer = 0;
+      tl.e = (int)step;
+    } else {
+      tl.layer = 1;
+      tl.e = (int)(step - L);
+      r -= S1;
+    }
+  } else if ((t -= (E - L) * (S1 + S2)) < L * S2) {
+    tl.layer = 1;
+    tl.e = (int)(E - L + t / S2);
+    r = t % S2;
+  } else {
+    return false;
+  }
+  tl.mt = (int)(r / (uint32_t)p.NCH);
+  tl.nc = (int)(r % (uint32_t)p.NCH);
+  return true;
+}
+
+struct FfShared {
+  uint64_t full[FF_MAX_STAGES], empty[FF_MAX_STAGES];
+  uint64_t sfull[FF_SCHED], sempty[FF_SCHED];
+  uint64_t afull[2], aempty[2];
+  int4 sched[FF_SCHED];
+  int4 ep_tile;       // epilogue: the leader's tile, broadcast by a named barrier
+  uint32_t tmem_slot;
+  volatile int abort_flag;
+  int ep_ok;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void epi_sync() {  // named barrier over the 4 epilogue warps
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(FF_THREADS, 1)
+    ffn_persistent_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
+                          const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
+                          const __grid_constant__ FfnParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * L::A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFFSET);
-  uint64_t* empty = full + STAGES;
-  uint64_t* accb = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int e = blockIdx.z;
-  const int m0 = blockIdx.x * TC_BM;
-  const int n0 = blockIdx.y * BN;
-  const int rows = expert_rows[e];
-  if (n0 >= rows) return;  // CTA-uniform, before any barrier or TMEM use
-
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FfShared& sh = *reinterpret_cast<FfShared*>(ring + FF_RING);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int KB = K / TC_BK;
+  const int BN = p.BN, NA = p.NA, STAGES = p.STAGES;
+  const uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], 1);
     }
-    mbar_init(accb, 1);
-    *abort_flag = 0;
+    for (int i = 0; i < FF_SCHED; ++i) {
+      mbar_init(&sh.sfull[i], 1);
+      mbar_init(&sh.sempty[i], 2);  // the MMA issuer and the epilogue
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.afull[i], 1);
+      mbar_init(&sh.aempty[i], 1);
+    }
+    sh.abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmW1);
     prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW2);
+    prefetch_tmap(&tmH);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_alloc(&sh.tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = sh.tmem_slot;
+  const int MT1 = p.F / FF_BM;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
-    const uint64_t w_policy = policy_evict_first();  // each weight tile is read by one CTA per n-tile
-    int issued = 0;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % STAGES;
-      if (kb >= STAGES && !mbar_wait(&empty[s], ((kb / STAGES) - 1) & 1)) {
-        raise_error(err, ERR_TIMEOUT);
-        *abort_flag = 1;
+    // ---------------- scheduler + TMA producer
+    const uint64_t w_policy = policy_evict_first();  // used when a weight tile is read once
+    uint32_t gst = 0;  // stages issued
+    int sidx = 0;      // queue entries published
+    while (true) {
+      if (sh.abort_flag) break;
+      FfTile tl;
+      const uint32_t t = atomicAdd(p.next_tile, 1u);
+      const bool has = ff_decode(t, p, tl);
+      if (has && tl.nc * BN >= p.expert_rows[tl.e]) continue;  // empty chunk
+      const int qs = sidx % FF_SCHED;
+      if (sidx >= FF_SCHED && !mbar_wait(&sh.sempty[qs], ((sidx / FF_SCHED) - 1) & 1)) {
+        raise_error(p.err, ERR_TIMEOUT);
+        sh.abort_flag = 1;
         break;
       }
-      if (*abort_flag) break;
-      mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
-      tma_load_2d_hint(sA + s * L::A_BYTES, &tmW, &full[s], kb * TC_BK, e * M + m0, w_policy);
-      tma_load_2d(sB + s * L::B_BYTES, &tmX, &full[s], kb * TC_BK, e * R + n0);
-      issued = kb + 1;
+      sh.sched[qs] = has ? make_int4(tl.layer, tl.e, tl.mt, tl.nc) : make_int4(-1, 0, 0, 0);
+      mbar_arrive(&sh.sfull[qs]);
+      ++sidx;
+      if (!has) break;
+      const bool l1 = tl.layer == 0;
+      if (!l1) {
+        // layer 2 reads h of (e, chunk): wait until every layer-1 tile of it is stored
+        const uint32_t* cnt = p.done1 + (size_t)tl.e * p.NCH + tl.nc;
+        if (ld_acquire_gpu(cnt) < (uint32_t)MT1) {
+          const long long t0 = clock64();
+          while (ld_acquire_gpu(cnt) < (uint32_t)MT1) {
+            if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+              raise_error(p.err, ERR_TIMEOUT);
+              break;
+            }
+          }
+        }
+        fence_proxy_async_global();  // order the acquire before the TMA reads of h
+      }
+      const CUtensorMap* tmA = l1 ? &tmW1 : &tmW2;
+      const CUtensorMap* tmB = l1 ? &tmX : &tmH;
+      const int K = l1 ? p.d : p.F;
+      const int M = l1 ? p.F : p.d;
+      const int arow = tl.e * M + tl.mt * FF_BM;
+      const int brow = tl.e * p.R + tl.nc * BN;
+      const int atoms = K / FF_BK;
+      bool ok = true;
+      for (int a0 = 0; a0 < atoms; a0 += NA) {
+        const int slot = (int)(gst % (uint32_t)STAGES);
+        if (gst >= (uint32_t)STAGES && !mbar_wait(&sh.empty[slot], ((gst / STAGES) - 1) & 1)) { ok = false; break; }
+        const int na = min(NA, atoms - a0);
+        mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)(na * (FF_ATOM_A + BN * FF_BK * 2)));
+        uint8_t* stage = ring + (size_t)slot * p.stage_bytes;
+        for (int at = 0; at < na; ++at) {
+          const int kx = (a0 + at) * FF_BK;
+          if (p.w_evict_first)
+            tma_load_2d_hint(stage + at * FF_ATOM_A, tmA, &sh.full[slot], kx, arow, w_policy);
+          else
+            tma_load_2d(stage + at * FF_ATOM_A, tmA, &sh.full[slot], kx, arow);
+          tma_load_2d(stage + NA * FF_ATOM_A + at * BN * FF_BK * 2, tmB, &sh.full[slot], kx, brow);
+        }
+        ++gst;
+      }
+      if (!ok) {
+        raise_error(p.err, ERR_TIMEOUT);
+        sh.abort_flag = 1;
+        break;
+      }
     }
-    // Drain: every copy this thread started has landed before the CTA may exit.
-    for (int kb = issued > STAGES ? issued - STAGES : 0; kb < issued; ++kb)
-      if (!mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1)) raise_error(err, ERR_TIMEOUT);
+    // Drain: every copy started here has landed before the CTA can leave.
+    for (uint32_t i = gst > (uint32_t)STAGES ? gst - STAGES : 0; i < gst; ++i)
+      if (!mbar_wait(&sh.full[i % STAGES], (i / STAGES) & 1)) raise_error(p.err, ERR_TIMEOUT);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % STAGES;
-      if (!mbar_wait(&full[s], (kb / STAGES) & 1)) {
-        raise_error(err, ERR_TIMEOUT);
-        *abort_flag = 1;
+    const uint32_t idesc = idesc_bf16_f32(FF_BM, BN);
+    uint32_t gst = 0;
+    int sidx = 0, lt = 0;
+    while (true) {
+      const int qs = sidx % FF_SCHED;
+      if (!mbar_wait(&sh.sfull[qs], (sidx / FF_SCHED) & 1)) {
+        raise_error(p.err, ERR_TIMEOUT);
+        sh.abort_flag = 1;
         break;
       }
-      if (*abort_flag) break;
+      const int4 tv = sh.sched[qs];
+      if (tv.x < 0) break;
+      const int buf = lt & 1;
+      if (lt >= 2 && !mbar_wait(&sh.aempty[buf], ((lt / 2) - 1) & 1)) {
+        raise_error(p.err, ERR_TIMEOUT);
+        sh.abort_flag = 1;
+        break;
+      }
       tc_fence_after();
-      const uint32_t a0 = smem_u32(sA + s * L::A_BYTES);
-      const uint32_t b0 = smem_u32(sB + s * L::B_BYTES);
+      const int atoms = (tv.x == 0 ? p.d : p.F) / FF_BK;
+      const uint32_t acc = tmem + (uint32_t)(buf * BN);
+      bool ok = true;
+      for (int a0 = 0; a0 < atoms; a0 += NA) {
+        const int slot = (int)(gst % (uint32_t)STAGES);
+        if (!mbar_wait(&sh.full[slot], (gst / STAGES) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const int na = min(NA, atoms - a0);
+        const uint32_t st = smem_u32(ring + (size_t)slot * p.stage_bytes);
+        for (int at = 0; at < na; ++at) {
+          const uint32_t a_s = st + at * FF_ATOM_A;
+          const uint32_t b_s = st + NA * FF_ATOM_A + at * BN * FF_BK * 2;
 #pragma unroll
-      for (int k = 0; k < TC_BK / 16; ++k)  // 16 bf16 = 32 bytes per MMA step inside the swizzle row
-        tc_mma_bf16(tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32), idesc,
-                    (kb > 0 || k > 0) ? 1u : 0u);
-      tc_commit(&empty[s]);
+          for (int kk = 0; kk < FF_BK / 16; ++kk)
+            tc_mma_bf16(acc, sw128_kmajor_desc(a_s + kk * 32), sw128_kmajor_desc(b_s + kk * 32), idesc,
+                        (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&sh.empty[slot]);
+        ++gst;
+      }
+      tc_commit(&sh.afull[buf]);  // the accumulator is complete once these MMAs are
+      if (!ok) {
+        raise_error(p.err, ERR_TIMEOUT);
+        sh.abort_flag = 1;
+        break;
+      }
+      mbar_arrive(&sh.sempty[qs]);
+      ++lt;
+      ++sidx;
     }
-    tc_commit(accb);  // arrives when every MMA issued above has completed
-  }
-  __syncwarp();
-
-  // ---------------- epilogue (all 4 warps; warp w owns TMEM lanes 32w..32w+31)
-  const bool acc_ok = mbar_wait(accb, 0);
-  if (!acc_ok) raise_error(err, ERR_TIMEOUT);
-  tc_fence_after();
-  if (acc_ok && !*abort_flag) {
-    const int m = m0 + warp * 32 + lane;
-    const float bv = bias ? __bfloat162float(bias[(size_t)e * M + m]) : 0.f;
-    __nv_bfloat16* orow = out + (size_t)e * R * M + m;
+  } else if (warp >= 2) {
+    // ---------------- epilogue (warps 2-5; TMEM lane quadrant = warp % 4)
+    const int quad = warp & 3;
+    const bool leader = threadIdx.x == 64;
+    int sidx = 0, lt = 0;
+    while (true) {
+      const int qs = sidx % FF_SCHED;
+      const int buf = lt & 1;
+      if (leader) {
+        int ok = mbar_wait(&sh.sfull[qs], (sidx / FF_SCHED) & 1) ? 1 : 0;
+        const int4 tv = sh.sched[qs];
+        if (ok && tv.x >= 0 && !mbar_wait(&sh.afull[buf], (lt / 2) & 1)) ok = 0;
+        if (!ok) {
+          raise_error(p.err, ERR_TIMEOUT);
+          sh.abort_flag = 1;
+        }
+        sh.ep_ok = ok;
+        sh.ep_tile = tv;
+      }
+      epi_sync();
+      const int4 tv = sh.ep_tile;
+      const int ok = sh.ep_ok;
+      epi_sync();  // everyone has read the broadcast before the leader can overwrite it
+      if (!ok || tv.x < 0) break;
+      tc_fence_after();
+      const bool l1 = tv.x == 0;
+      const int e = tv.y, mt = tv.z, nc = tv.w;
+      const int rows = p.expert_rows[e];
+      const int n0 = nc * BN;
+      const int nv = min(BN, rows - n0);
+      const int M = l1 ? p.F : p.d;
+      const int m = mt * FF_BM + quad * 32 + lane;
+      const __nv_bfloat16* bias = l1 ? p.b1 : p.b2;
+      const float bv = bias ? __bfloat162float(bias[(size_t)e * M + m]) : 0.f;
+      const uint32_t taddr = tmem + (uint32_t)(buf * BN) + ((uint32_t)(quad * 32) << 16);
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      uint32_t r[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, r);
-      tmem_ld_wait();
+      for (int c0 = 0; c0 < nv; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr + (uint32_t)c0, r);
+        tmem_ld_wait();
+        if (l1) {
+          __nv_bfloat16* dst = p.h + ((size_t)e * p.R + n0 + c0) * p.F + m;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int n = n0 + c0 + j;
-        if (n < rows) {
-          float v = __uint_as_float(r[j]) + bv;
-          if (RELU) v = fmaxf(v, 0.f);
-          orow[(size_t)n * M] = __float2bfloat16_rn(v);
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < nv) dst[(size_t)j * p.F] = __float2bfloat16_rn(fmaxf(__uint_as_float(r[j]) + bv, 0.f));
+        } else if (!p.combine) {
+          __nv_bfloat16* dst = p.out + ((size_t)e * p.R + n0 + c0) * p.d + m;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < nv) dst[(size_t)j * p.d] = __float2bfloat16_rn(__uint_as_float(r[j]) + bv);
+        } else {
+          // lane j < 16 fetches the token and gate of column c0 + j, then broadcasts them
+          int tk = 0;
+          float gt = 0.f;
+          if (lane < 16 && c0 + lane < nv) {
+            tk = p.tok_of_row[(size_t)e * p.R + n0 + c0 + lane];
+            gt = p.gate[tk];
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tj = __shfl_sync(0xffffffffu, tk, j);
+            const float gj = __shfl_sync(0xffffffffu, gt, j);
+            if (c0 + j < nv) {
+              const float ye = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[j]) + bv));
+              float o = gj * ye;
+              if (p.resid) o += __bfloat162float(p.resid[(size_t)tj * p.d + m]);
+              p.out[(size_t)tj * p.d + m] = __float2bfloat16_rn(o);
+            }
+          }
         }
       }
+      tc_fence_before();
+      epi_sync();  // every thread's TMEM reads and stores of this tile are done
+      if (leader) {
+        mbar_arrive(&sh.aempty[buf]);
+        if (l1) {
+          __threadfence();  // the chunk's h stores (ordered by the barrier) before the count
+          atomicAdd(p.done1 + (size_t)e * p.NCH + nc, 1u);
+        }
+        mbar_arrive(&sh.sempty[qs]);
+      }
+      ++lt;
+      ++sidx;
     }
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, L::TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- host side
@@ -193,51 +412,79 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)TC_BK, box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)FF_BK, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool tc_shape_ok(int M, int K) { return M > 0 && K > 0 && M % TC_BM == 0 && K % TC_BK == 0; }
+bool tc_shape_ok(int M, int K) { return M > 0 && K > 0 && M % FF_BM == 0 && K % FF_BK == 0; }
 
-template <int BN, int STAGES, bool RELU>
-static int launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const void* bias, void* out,
-                     const int32_t* expert_rows, int E, int R, int M, int K, uint32_t* err, cudaStream_t s) {
-  using L = TcLayout<BN, STAGES>;
-  auto kern = grouped_linear_tc_kernel<BN, STAGES, RELU>;
-  static bool attr_set = false;  // per instantiation; the attribute is per device function
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
-  dim3 grid(M / TC_BM, (R + BN - 1) / BN, E);
-  kern<<<grid, 128, L::SMEM_BYTES, s>>>(tmW, tmX, (const __nv_bfloat16*)bias, (__nv_bfloat16*)out, expert_rows, R,
-                                        M, K, err);
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+FfnTiling ffn_tiling(int R) {
+  FfnTiling t;
+  t.NCH = R <= 256 ? 1 : (R + 255) / 256;
+  const int rows = (R + t.NCH - 1) / t.NCH;
+  t.BN = rows <= 16 ? 16 : (rows + 15) / 16 * 16;
+  const int stage_atom = FF_ATOM_A + t.BN * FF_BK * 2;
+  t.NA = stage_atom <= 24 * 1024 ? 2 : 1;
+  t.stage_bytes = t.NA * stage_atom;
+  t.STAGES = FF_RING / t.stage_bytes < FF_MAX_STAGES ? FF_RING / t.stage_bytes : FF_MAX_STAGES;
+  return t;
 }
 
-int launch_grouped_linear_tc(const void* in, const void* W, const void* bias, void* out,
-                             const int32_t* expert_rows, int E, int R, int M, int K, bool relu, uint32_t* err,
-                             cudaStream_t s) {
-  if (E == 0 || R == 0) return 0;
-  if (!tc_shape_ok(M, K)) return -1;
-  const int BN = R <= 32 ? 32 : R <= 64 ? 64 : R <= 128 ? 128 : 256;
-  CUtensorMap tmW, tmX;
-  if (!encode_bf16_2d(&tmW, W, (uint64_t)E * M, (uint64_t)K, TC_BM)) return -1;
-  if (!encode_bf16_2d(&tmX, in, (uint64_t)E * R, (uint64_t)K, (uint32_t)BN)) return -1;
-#define SMOE_TC(BNV, ST)                                                                                      \
-  return relu ? launch_tc<BNV, ST, true>(tmW, tmX, bias, out, expert_rows, E, R, M, K, err, s)               \
-              : launch_tc<BNV, ST, false>(tmW, tmX, bias, out, expert_rows, E, R, M, K, err, s)
-  switch (BN) {
-    case 32: SMOE_TC(32, 5);
-    case 64: SMOE_TC(64, 4);
-    case 128: SMOE_TC(128, 3);
-    default: SMOE_TC(256, 4);
-  }
-#undef SMOE_TC
+size_t ffn_counter_words(int E, int R) { return 1 + (size_t)E * ffn_tiling(R).NCH; }
+
+int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s) {
+  if (L.E == 0 || L.R == 0) return 0;
+  if (!tc_shape_ok(L.F, L.d) || !tc_shape_ok(L.d, L.F)) return -1;
+  const FfnTiling t = ffn_tiling(L.R);
+  if (t.STAGES < 2 || t.BN > 256) return -1;
+  CUtensorMap tmW1, tmX, tmW2, tmH;
+  if (!encode_bf16_2d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM)) return -1;
+  if (!encode_bf16_2d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)t.BN)) return -1;
+  if (!encode_bf16_2d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM)) return -1;
+  if (!encode_bf16_2d(&tmH, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)t.BN)) return -1;
+  FfnParams p;
+  p.b1 = (const __nv_bfloat16*)L.b1;
+  p.b2 = (const __nv_bfloat16*)L.b2;
+  p.h = (__nv_bfloat16*)L.h;
+  p.out = (__nv_bfloat16*)L.out;
+  p.expert_rows = L.expert_rows;
+  p.tok_of_row = L.tok_of_row;
+  p.gate = L.gate;
+  p.resid = (const __nv_bfloat16*)L.resid;
+  p.next_tile = L.counters;
+  p.done1 = L.counters + 1;
+  p.err = L.err;
+  p.E = L.E;
+  p.R = L.R;
+  p.d = L.d;
+  p.F = L.F;
+  p.BN = t.BN;
+  p.NCH = t.NCH;
+  p.LOOK = 8;
+  p.NA = t.NA;
+  p.STAGES = t.STAGES;
+  p.stage_bytes = t.stage_bytes;
+  p.combine = L.combine ? 1 : 0;
+  p.w_evict_first = t.NCH == 1 ? 1 : 0;  // several chunks re-read a weight tile
+  const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
+  if (cudaFuncSetAttribute(ffn_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -1;
+  const long long tiles = (long long)L.E * t.NCH * (L.F / FF_BM + L.d / FF_BM);
+  if (tiles >= (1ll << 31) || (long long)L.E * L.R >= (1ll << 31) || (long long)L.E * L.F >= (1ll << 31) ||
+      (long long)L.E * L.d >= (1ll << 31))
+    return -1;  // tickets and TMA row coordinates are 32-bit
+  const int ctas = (int)(tiles < device_sm_count() ? tiles : device_sm_count());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(FF_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.numAttrs = 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, ffn_persistent_kernel, tmW1, tmX, tmW2, tmH, p);
+  return e == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace smoe

@@ -62,8 +62,11 @@ int device_sm_count();
 // 2-D bf16 tensor map [rows, cols] (cols contiguous), box box_rows x 64 columns, 128-byte swizzle.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
-// Slots from in-tile ranks, then the dispatch copy: one warp per token.
-int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, cudaStream_t s);
+// Slots from in-tile ranks, then the dispatch copy: one warp per token.  When y is
+// not null (combine fused into the FFN), dropped tokens' rows of y get their final
+// value here (x_residual or zero), and `zero` words at zero_ptr are cleared.
+int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, void* y, const void* resid,
+                          uint32_t* zero_ptr, int zero_words, cudaStream_t s);
 
 // xe[expert[t]*R + row[t]] = x[t] for kept tokens (row[t] >= 0); rows r >= expert_rows[e]
 // of every expert block are zeroed.
@@ -80,11 +83,35 @@ int launch_grouped_linear_simt(const void* in, const void* W, const void* bias, 
                                const int32_t* expert_rows, int E, int R, int M, int K, bool relu,
                                bool bf16, cudaStream_t s);
 
-// Same contraction on tcgen05 tensor cores (bf16 in, f32 accumulate, bf16 out).
-// Needs M % 128 == 0 and K % 64 == 0.  Returns launches, or -1 on error.
+// Expert FFN (both layers of every expert) in one persistent tensor-core kernel.
+struct FfnTiling {
+  int BN;           // token rows per tile (MMA N), multiple of 16
+  int NCH;          // chunks of BN rows per expert block
+  int NA;           // 64-column atoms per pipeline stage
+  int stage_bytes;
+  int STAGES;
+};
+FfnTiling ffn_tiling(int R);
+// 32-bit words of scheduler state the kernel needs zeroed at launch.
+size_t ffn_counter_words(int E, int R);
+
+struct FfnLaunch {
+  const void* xe;            // [E * R, d] bf16
+  const void* W1; const void* b1;  // [E, F, d], [E, F] or null
+  const void* W2; const void* b2;  // [E, d, F], [E, d] or null
+  void* h;                   // [E * R, F] bf16 scratch
+  void* out;                 // ye [E * R, d], or y [N, d] when combine
+  const int32_t* expert_rows;
+  bool combine;
+  const int32_t* tok_of_row; // [E * R] (combine)
+  const float* gate;         // [N] (combine)
+  const void* resid;         // [N, d] or null (combine)
+  uint32_t* counters;        // ffn_counter_words(E, R) words, zero at launch
+  uint32_t* err;
+  int E, R, d, F;
+};
+// Needs d % 128 == 0 and F % 128 == 0 (tc_shape_ok both ways).  Returns launches or -1.
 bool tc_shape_ok(int M, int K);
-int launch_grouped_linear_tc(const void* in, const void* W, const void* bias, void* out,
-                             const int32_t* expert_rows, int E, int R, int M, int K, bool relu,
-                             uint32_t* err, cudaStream_t s);
+int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s);
 
 }  // namespace smoe
