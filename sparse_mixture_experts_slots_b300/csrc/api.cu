@@ -144,7 +144,7 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_logits = take(cfg->dtype == SWITCH_F32 ? N * E * sizeof(float) : 0);
   const size_t o_wsplit = take(cfg->dtype == SWITCH_BF16 ? router_tc_wsplit_bytes(cfg->E, cfg->d_model) : 0);
   const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
-  const size_t ffn_words = ffn_counter_words(cfg->E, (int)R);
+  const size_t ffn_words = ffn_counter_words(cfg->E, (int)R, cfg->d_model, cfg->d_ff);
   const size_t o_fcnt = take(ffn_words * sizeof(uint32_t));
   const size_t o_hist = take(G * nT * E * sizeof(int32_t));
   const size_t o_tP = take(G * nT * E * sizeof(float));

@@ -56,6 +56,12 @@ int router_tc_mma_n(int EC);
 // Bytes of the split W_r workspace ([Q][hi, mid, lo][EC][d] bf16) for E experts of width d.
 size_t router_tc_wsplit_bytes(int E, int d);
 
+// 3-D view [cols / 64 atoms][rows][64] of a row-major bf16 matrix (cols % 64 == 0); a box of
+// box_atoms consecutive 64-column atoms of box_rows rows lands as box_atoms swizzled
+// [box_rows x 128 B] blocks, one after another.
+bool encode_bf16_3d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t box_atoms);
+
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 
@@ -86,14 +92,15 @@ int launch_grouped_linear_simt(const void* in, const void* W, const void* bias, 
 // Expert FFN (both layers of every expert) in one persistent tensor-core kernel.
 struct FfnTiling {
   int BN;           // token rows per tile (MMA N), multiple of 16
+  int MB;           // 128-row weight blocks per tile (1 or 2)
   int NCH;          // chunks of BN rows per expert block
   int NA;           // 64-column atoms per pipeline stage
   int stage_bytes;
   int STAGES;
 };
-FfnTiling ffn_tiling(int R);
+FfnTiling ffn_tiling(int R, int d, int F);
 // 32-bit words of scheduler state the kernel needs zeroed at launch.
-size_t ffn_counter_words(int E, int R);
+size_t ffn_counter_words(int E, int R, int d, int F);
 
 struct FfnLaunch {
   const void* xe;            // [E * R, d] bf16

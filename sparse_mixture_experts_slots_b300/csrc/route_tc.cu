@@ -97,6 +97,7 @@ struct RtCfg {
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
   static_assert(STAGES >= 2, "double buffering at least");
   static_assert(DEEP || G::TMEM_COLS <= 256, "two CTAs per SM share the 512 TMEM columns");
+  static_assert(NA == 1 || G::WBOXES == 1, "a 3-D W box spans atoms only when one box covers the pieces");
 };
 
 template <int EC, bool DEEP>
@@ -172,7 +173,7 @@ __device__ __forceinline__ float warp_colsum16(const float (&p)[16], int lane) {
 template <int EC, bool DEEP>
 __global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                     const float* __restrict__ br, int T, int E, int d, int nT, int Q,
+                     const float* __restrict__ br, int T, int E, int d, int nT, int Q, int use3d,
                      int32_t* __restrict__ expert, float* __restrict__ gate, int32_t* __restrict__ rank,
                      int32_t* __restrict__ tile_hist, float* __restrict__ tile_P, float* __restrict__ logits,
                      float* __restrict__ probs, uint32_t* err) {
@@ -220,15 +221,24 @@ __global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
       const int slot = st % Cf::STAGES;
       if (st >= Cf::STAGES && !mbar_wait(&bar.empty[slot], ((st / Cf::STAGES) - 1) & 1)) { ok = false; break; }
       if (bar.abort_flag) { ok = false; break; }
-      const int na = min(Cf::NA, (d - st * Cf::NA * RT_BK + RT_BK - 1) / RT_BK);  // atoms inside d
-      mbar_arrive_expect_tx(&bar.full[slot], (uint32_t)(na * (Cf::X_ATOM + Cf::W_ATOM)));
       uint8_t* stage = smem + slot * Cf::STAGE_BYTES;
-      for (int at = 0; at < na; ++at) {
-        const int kx = (st * Cf::NA + at) * RT_BK;
-        tma_load_2d(stage + at * Cf::X_ATOM, &tmX, &bar.full[slot], kx, (int)tok0);
-        for (int b = 0; b < Gm::WBOXES; ++b)
-          tma_load_2d(stage + Cf::NA * Cf::X_ATOM + at * Cf::W_ATOM + b * Gm::MMA_N * 128, &tmW, &bar.full[slot], kx,
-                      q * Gm::WROWS + b * Gm::MMA_N);
+      if (use3d) {
+        // one 3-D box per operand covers the stage's NA atoms (past d: zeros, not used)
+        mbar_arrive_expect_tx(&bar.full[slot], (uint32_t)Cf::STAGE_BYTES);
+        tma_load_3d(stage, &tmX, &bar.full[slot], 0, (int)tok0, st * Cf::NA);
+        for (int b = 0; b < Gm::WBOXES; ++b)  // WBOXES > 1 only with NA = 1
+          tma_load_3d(stage + Cf::NA * Cf::X_ATOM + b * Gm::MMA_N * 128, &tmW, &bar.full[slot], 0,
+                      q * Gm::WROWS + b * Gm::MMA_N, st * Cf::NA);
+      } else {
+        const int na = min(Cf::NA, (d - st * Cf::NA * RT_BK + RT_BK - 1) / RT_BK);  // atoms inside d
+        mbar_arrive_expect_tx(&bar.full[slot], (uint32_t)(na * (Cf::X_ATOM + Cf::W_ATOM)));
+        for (int at = 0; at < na; ++at) {
+          const int kx = (st * Cf::NA + at) * RT_BK;
+          tma_load_2d(stage + at * Cf::X_ATOM, &tmX, &bar.full[slot], kx, (int)tok0);
+          for (int b = 0; b < Gm::WBOXES; ++b)
+            tma_load_2d(stage + Cf::NA * Cf::X_ATOM + at * Cf::W_ATOM + b * Gm::MMA_N * 128, &tmW, &bar.full[slot],
+                        kx, q * Gm::WROWS + b * Gm::MMA_N);
+        }
       }
       issued = st + 1;
     }
@@ -442,7 +452,7 @@ __global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
 
 // ---------------------------------------------------------------- host side
 template <int EC, bool DEEP>
-static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteArgs& a, int nT, int Q,
+static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteArgs& a, int nT, int Q, int use3d,
                      int32_t* rank, cudaStream_t s) {
   auto kern = router_tc_kernel<EC, DEEP>;
   constexpr int smem = rt_smem_bytes<EC, DEEP>();
@@ -459,7 +469,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const Route
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = Q > 1 ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, a.expert, a.gate,
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, use3d, a.expert, a.gate,
                                            rank, a.tile_hist, a.tile_P, a.logits_out, a.probs, a.err);
   return e == cudaSuccess ? 1 : -1;
 }
@@ -493,21 +503,32 @@ int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
   const unsigned sb = (unsigned)((n + 255) / 256 < 148 * 16 ? (n + 255) / 256 : 148 * 16);
   router_split_kernel<<<sb, 256, 0, s>>>(a.Wr, (__nv_bfloat16*)a.wsplit, a.E, a.d, EC, n);
   if (cudaGetLastError() != cudaSuccess) return -1;
-  CUtensorMap tmX, tmW;
-  if (!encode_bf16_2d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM)) return -1;
-  if (!encode_bf16_2d(&tmW, a.wsplit, (uint64_t)3 * Q * EC, (uint64_t)a.d, (uint32_t)router_tc_mma_n(EC))) return -1;
-  // One wave on this device's SMs -> the deep ring; EC = 256 always takes it (one CTA per SM).
+  // One wave on this device's SMs -> the deep ring; EC >= 128 always takes it (512 TMEM columns).
   const long long ctas = (long long)Q * nT * a.G;
   const bool deep = EC >= 128 || ctas <= (long long)device_sm_count();
+  const int NA = (EC <= 16 || (EC <= 64 && deep)) ? 2 : 1;  // RtCfg<EC, deep>::NA
+  const int use3d = a.d % RT_BK == 0 ? 1 : 0;
+  CUtensorMap tmX, tmW;
+  if (use3d) {
+    if (!encode_bf16_3d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM, (uint32_t)NA)) return -1;
+    if (!encode_bf16_3d(&tmW, a.wsplit, (uint64_t)3 * Q * EC, (uint64_t)a.d, (uint32_t)router_tc_mma_n(EC),
+                        (uint32_t)NA))
+      return -1;
+  } else {
+    if (!encode_bf16_2d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM)) return -1;
+    if (!encode_bf16_2d(&tmW, a.wsplit, (uint64_t)3 * Q * EC, (uint64_t)a.d, (uint32_t)router_tc_mma_n(EC)))
+      return -1;
+  }
   int n2;
-#define SMOE_RT(ECV)                                                                        \
-  n2 = deep ? launch_rt<ECV, true>(tmX, tmW, a, nT, Q, rank, s) : launch_rt<ECV, false>(tmX, tmW, a, nT, Q, rank, s)
+#define SMOE_RT(ECV)                                                                                        \
+  n2 = deep ? launch_rt<ECV, true>(tmX, tmW, a, nT, Q, use3d, rank, s)                                      \
+            : launch_rt<ECV, false>(tmX, tmW, a, nT, Q, use3d, rank, s)
   switch (EC) {
     case 16: SMOE_RT(16); break;
     case 32: SMOE_RT(32); break;
     case 64: SMOE_RT(64); break;
-    case 128: n2 = launch_rt<128, true>(tmX, tmW, a, nT, Q, rank, s); break;
-    default: n2 = launch_rt<256, true>(tmX, tmW, a, nT, Q, rank, s); break;
+    case 128: n2 = launch_rt<128, true>(tmX, tmW, a, nT, Q, use3d, rank, s); break;
+    default: n2 = launch_rt<256, true>(tmX, tmW, a, nT, Q, use3d, rank, s); break;
   }
 #undef SMOE_RT
   return n2 < 0 ? -1 : 2;
