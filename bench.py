@@ -100,24 +100,21 @@ def algorithmic(shape, expert_rows: np.ndarray, N: int):
     es = 4 if shape.dtype == "f32" else 2
     K = int(expert_rows.sum())
     used = int((expert_rows > 0).sum())
-    R = expert_rows.size and None
-    w_bytes = used * F * d * es
-    out = {
+    w_bytes = 2 * used * F * d * es
+    return {
         "kept_rows": K,
         "experts_used": used,
         # route: read x and W_r, write 13 B of per-token records + [E] stats
         "route_bytes": N * d * es + E * d * 4 + N * 13,
-        # dispatch: read kept rows, write every row of the expert blocks (kept + zeroed)
-        "dispatch_bytes": K * d * es,
-        "ffn1_bytes": w_bytes + K * d * es + K * F * es,
-        "ffn2_bytes": w_bytes + K * F * es + K * d * es,
-        "ffn1_flops": 2.0 * K * d * F,
-        "ffn2_flops": 2.0 * K * d * F,
-        # combine: read kept rows of ye, write all N rows of y
-        "combine_bytes": K * d * es + N * d * es,
+        # dispatch: read kept rows, write them to the expert blocks
+        "dispatch_bytes": 2 * K * d * es,
+        # expert FFN with the combine fused in: weights of the used experts, the dispatched
+        # rows in, y rows out (h stays on chip / in L2); all N rows of y are written, the
+        # dropped ones by the dispatch pass
+        "ffn_bytes": w_bytes + K * d * es + K * d * es,
+        "ffn_flops": 4.0 * K * d * F,
         "router_flops": 2.0 * N * d * E,
     }
-    return out
 
 
 def traffic_from_profiles(kernel: str):
@@ -226,37 +223,36 @@ def run_gpu(args, shape):
     if world > 1:  # each rank routes its own batch; the expert weights are replicated
         inp["x"] = make_inputs(shape, seed + 7919 * rank, dev, with_experts=False)["x"]
     dt = torch.float32 if shape.dtype == "f32" else torch.bfloat16
-    layer = SwitchMoE(shape.G, shape.T, shape.d_model, shape.d_ff, shape.E, shape.capacity_factor, dtype=dt,
-                      profile=True, device=dev)
+    mk = lambda prof: SwitchMoE(shape.G, shape.T, shape.d_model, shape.d_ff, shape.E, shape.capacity_factor,
+                                dtype=dt, profile=prof, device=dev)
+    layer = mk(False)
     r = layer.alloc_route()
     y = torch.empty(shape.N, shape.d_model, dtype=dt, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        layer.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], r=r, y=y,
-                      stream=stream)
+    def step(lay):
+        lay.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], r=r, y=y,
+                    stream=stream)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        step()
+        step(layer)
     layer.sync_status(stream)
     torch.cuda.synchronize(dev)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    stage_sum = np.zeros(5)
     launches = 0
     clocks = ClockSampler(dev.index)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush.fill_(float(i))  # > L2, outside the step's events
         ev[i][0].record(stream)
-        step()
+        step(layer)
         ev[i][1].record(stream)
         launches += layer.last_launch_count()
-        stage_sum += np.array(layer.stage_ms())  # synchronises on the step's last event
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
@@ -268,6 +264,21 @@ def run_gpu(args, shape):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     layer.sync_status(stream)
+
+    # ---------------- per-stage times: a profiled pass of the same workload (CUDA events
+    # recorded on this stream between the stages; no programmatic overlap across them)
+    prof_layer = mk(True)
+    n_prof = max(3, min(args.steps, 50))
+    stage_sum = np.zeros(5)
+    for i in range(args.warmup + n_prof):
+        flush.fill_(1.0)
+        step(prof_layer)
+        st = np.array(prof_layer.stage_ms())
+        if i >= args.warmup:
+            stage_sum += st
+    prof_layer.sync_status(stream)
+    stage_avg = stage_sum / n_prof  # ms: route, dispatch, ffn (+combine), ffn2, combine
+    del prof_layer
 
     # ---------------- end to end through the public API: pinned host x in, y + aux loss out
     x_host = inp["x"].cpu().pin_memory()
@@ -298,36 +309,35 @@ def run_gpu(args, shape):
             dist.destroy_process_group()
         return 0
 
-    # ---------------- roofline of the dominant kernel
+    # ---------------- roofline of the dominant kernel (the expert FFN)
     hbm, tc_burst, tc_sust, peak_src = peaks()
     rows = r.expert_rows.cpu().numpy()
     work = algorithmic(shape, rows, shape.N)
-    stage_avg = stage_sum / args.steps  # ms: route, dispatch, ffn1, ffn2, combine
-    names = ["route", "dispatch", "ffn1", "ffn2", "combine"]
-    stage_bytes = [work["route_bytes"], work["dispatch_bytes"], work["ffn1_bytes"], work["ffn2_bytes"],
-                   work["combine_bytes"]]
-    dom = int(np.argmax(stage_avg[2:4])) + 2  # the FFN kernels dominate the step
-    dom_name = names[dom]
-    achieved = stage_bytes[dom] / (stage_avg[dom] * 1e-3) / 1e9
-    kern = "grouped_linear_tc_kernel" if shape.dtype == "bf16" else "grouped_linear_simt_kernel"
-    traffic = traffic_from_profiles(f"{kern}:{dom_name}:{shape.name}")
-    ffn_flops = work["ffn1_flops"] + work["ffn2_flops"]
-    ffn_ms = stage_avg[2] + stage_avg[3]
+    tc_path = shape.dtype == "bf16" and shape.d_model % 128 == 0 and shape.d_ff % 128 == 0
+    ffn_ms = stage_avg[2] + stage_avg[3] + (stage_avg[4] if not tc_path else 0.0)
+    kern = "ffn_persistent_kernel" if tc_path else "grouped_linear_simt_kernel"
+    achieved = work["ffn_bytes"] / (ffn_ms * 1e-3) / 1e9
+    traffic = traffic_from_profiles(f"{kern}:{shape.name}")
     value = shape.N * world * args.steps / (total_ms * 1e-3)
+    names = ["route", "dispatch", "ffn", "ffn_layer2", "combine"]
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if shape.dtype == "bf16" else "f32", "data": "synthetic",
         "config": config_of(shape, argparse.Namespace(gpus=world)),
-        "roofline": {"bound": "hbm", "kernel": f"{kern} ({dom_name})", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs",
+        "roofline": {"bound": "hbm", "kernel": kern, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
                      "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
-                     "algorithmic_bytes_per_launch": stage_bytes[dom]},
+                     "algorithmic_bytes_per_launch": work["ffn_bytes"],
+                     "kernel_ms": ffn_ms,
+                     "timing": "CUDA events around the kernel on its stream, profiled pass of the same workload"},
         "stages_ms": {n: float(v) for n, v in zip(names, stage_avg)},
-        "stage_gbs": {n: float(b / (t * 1e-3) / 1e9) for n, b, t in zip(names, stage_bytes, stage_avg)},
-        "ffn_tc_frac": {"achieved_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12, "peak_tflops": tc_burst,
-                        "frac": ffn_flops / (ffn_ms * 1e-3) / 1e12 / tc_burst,
-                        "note": f"kept-row FLOPs 4*K*d*d_ff over both FFN kernels; {peak_src} bf16 burst"},
+        "stage_gbs": {"route": work["route_bytes"] / (stage_avg[0] * 1e-3) / 1e9,
+                      "dispatch": work["dispatch_bytes"] / (stage_avg[1] * 1e-3) / 1e9,
+                      "ffn": achieved},
+        "ffn_tc_frac": {"achieved_tflops": work["ffn_flops"] / (ffn_ms * 1e-3) / 1e12, "peak_tflops": tc_burst,
+                        "frac": work["ffn_flops"] / (ffn_ms * 1e-3) / 1e12 / tc_burst,
+                        "note": f"kept-row FLOPs 4*K*d*d_ff; {peak_src} bf16 burst; the FFN is weight-bandwidth bound"},
         "dispatch_hbm_gbs": float(work["dispatch_bytes"] / (stage_avg[1] * 1e-3) / 1e9),
         "kept_rows": work["kept_rows"], "dropped": int(shape.N - work["kept_rows"]),
         "e2e": {"value": shape.N * world * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",

@@ -269,7 +269,7 @@ static bool use_tc_ffn(const switch_layer* h) {
 // token order (gate * expert output, + x_residual) instead of ye.
 static switch_status run_ffn_tc(switch_handle h, const void* xe, const void* W1, const void* b1, const void* W2,
                                 const void* b2, const int32_t* rows, void* out, bool combine,
-                                const switch_route_out* r, const void* resid, cudaStream_t s) {
+                                const switch_route_out* r, const void* resid, cudaStream_t s, bool pdl) {
   const switch_config& c = h->cfg;
   FfnLaunch L;
   L.xe = xe;
@@ -290,7 +290,7 @@ static switch_status run_ffn_tc(switch_handle h, const void* xe, const void* W1,
   L.R = h->R;
   L.d = c.d_model;
   L.F = c.d_ff;
-  const int n = launch_ffn_tc(L, s);
+  const int n = launch_ffn_tc(L, s, pdl);
   if (n < 0) return SWITCH_ERR_CUDA;
   h->last_launches += n;
   return SWITCH_OK;
@@ -298,15 +298,16 @@ static switch_status run_ffn_tc(switch_handle h, const void* xe, const void* W1,
 
 // Both FFN layers on CUDA cores (float32, or widths the tensor-core tiles do not take).
 static switch_status run_ffn_simt(switch_handle h, const void* xe, const void* W1, const void* b1, const void* W2,
-                                  const void* b2, const int32_t* rows, void* ye, cudaStream_t s, int ev_mid) {
+                                  const void* b2, const int32_t* rows, void* ye, cudaStream_t s, int ev_mid,
+                                  bool pdl) {
   const switch_config& c = h->cfg;
   const int E = c.E, R = h->R, d = c.d_model, F = c.d_ff;
   const bool bf16 = c.dtype == SWITCH_BF16;
-  int n = launch_grouped_linear_simt(xe, W1, b1, h->hbuf, rows, E, R, F, d, true, bf16, s);
+  int n = launch_grouped_linear_simt(xe, W1, b1, h->hbuf, rows, E, R, F, d, true, bf16, s, pdl);
   if (n < 0) return SWITCH_ERR_CUDA;
   h->last_launches += n;
   if (ev_mid >= 0) cudaEventRecord(h->ev[ev_mid], s);
-  n = launch_grouped_linear_simt(h->hbuf, W2, b2, ye, rows, E, R, d, F, false, bf16, s);
+  n = launch_grouped_linear_simt(h->hbuf, W2, b2, ye, rows, E, R, d, F, false, bf16, s, ev_mid < 0);
   if (n < 0) return SWITCH_ERR_CUDA;
   h->last_launches += n;
   return SWITCH_OK;
@@ -322,19 +323,24 @@ switch_status switch_expert_ffn(switch_handle h, const void* xe, const void* W1,
     if (h->R == 0) return SWITCH_OK;
     if (cudaMemsetAsync(h->ffn_counters, 0, (size_t)h->ffn_counter_words * sizeof(uint32_t), s) != cudaSuccess)
       return SWITCH_ERR_CUDA;
-    return run_ffn_tc(h, xe, W1, b1, W2, b2, expert_rows, ye, false, nullptr, nullptr, s);
+    return run_ffn_tc(h, xe, W1, b1, W2, b2, expert_rows, ye, false, nullptr, nullptr, s, false);
   }
-  return run_ffn_simt(h, xe, W1, b1, W2, b2, expert_rows, ye, s, -1);
+  return run_ffn_simt(h, xe, W1, b1, W2, b2, expert_rows, ye, s, -1, false);
 }
 
-switch_status switch_combine(switch_handle h, const void* ye, const switch_route_out* r, const void* x_residual,
-                             void* y, void* stream) {
+static switch_status combine_impl(switch_handle h, const void* ye, const switch_route_out* r, const void* x_residual,
+                                  void* y, cudaStream_t s, bool pdl) {
   if (!h || !route_out_ok(r, h->N) || (h->R > 0 && !ye) || (h->N > 0 && !y) || !aligned16(ye) || !aligned16(y))
     return SWITCH_ERR_INVALID_ARG;
   if (x_residual && !aligned16(x_residual)) return SWITCH_ERR_INVALID_ARG;
   return launched(launch_combine(ye, r->expert, r->row, r->gate, x_residual, y, h->N, h->cfg.d_model, h->R,
-                                 h->cfg.dtype == SWITCH_BF16, (cudaStream_t)stream),
+                                 h->cfg.dtype == SWITCH_BF16, s, pdl),
                   h);
+}
+
+switch_status switch_combine(switch_handle h, const void* ye, const switch_route_out* r, const void* x_residual,
+                             void* y, void* stream) {
+  return combine_impl(h, ye, r, x_residual, y, (cudaStream_t)stream, false);
 }
 
 switch_status switch_forward(switch_handle h, const void* x, const float* Wr, const float* br, const void* W1,
@@ -346,6 +352,9 @@ switch_status switch_forward(switch_handle h, const void* x, const float* Wr, co
   const bool prof = (h->cfg.flags & SWITCH_FLAG_PROFILE) && h->have_events;
   h->last_launches = 0;
   if (prof) cudaEventRecord(h->ev[0], s);
+  // Consecutive kernels of the call start as programmatic dependents of their
+  // predecessor (their prologues overlap its tail); with per-stage events in between
+  // (SWITCH_FLAG_PROFILE) every launch is an ordinary one.
   RouteArgs a;
   switch_status st = route_args(h, x, Wr, br, r, &a);
   if (st != SWITCH_OK) return st;
@@ -357,13 +366,13 @@ switch_status switch_forward(switch_handle h, const void* x, const float* Wr, co
   // With the tensor-core FFN the combine happens in its epilogue: the dispatch pass
   // writes the dropped tokens' rows of y and clears the FFN's scheduler counters.
   st = launched(launch_dispatch_slots(x, h->xe, a, tc ? y : nullptr, tc ? x_residual : nullptr,
-                                      tc ? h->ffn_counters : nullptr, tc ? h->ffn_counter_words : 0, s),
+                                      tc ? h->ffn_counters : nullptr, tc ? h->ffn_counter_words : 0, s, !prof),
                 h);
   if (st != SWITCH_OK) return st;
   if (prof) cudaEventRecord(h->ev[2], s);
   if (tc) {
     if (h->R > 0) {
-      st = run_ffn_tc(h, h->xe, W1, b1, W2, b2, r->expert_rows, y, true, r, x_residual, s);
+      st = run_ffn_tc(h, h->xe, W1, b1, W2, b2, r->expert_rows, y, true, r, x_residual, s, !prof);
       if (st != SWITCH_OK) return st;
     }
     if (prof) {
@@ -371,10 +380,10 @@ switch_status switch_forward(switch_handle h, const void* x, const float* Wr, co
       cudaEventRecord(h->ev[4], s);
     }
   } else {
-    st = run_ffn_simt(h, h->xe, W1, b1, W2, b2, r->expert_rows, h->ye, s, prof ? 3 : -1);
+    st = run_ffn_simt(h, h->xe, W1, b1, W2, b2, r->expert_rows, h->ye, s, prof ? 3 : -1, !prof);
     if (st != SWITCH_OK) return st;
     if (prof) cudaEventRecord(h->ev[4], s);
-    st = switch_combine(h, h->ye, r, x_residual, y, stream);
+    st = combine_impl(h, h->ye, r, x_residual, y, s, !prof);
     if (st != SWITCH_OK) return st;
   }
   if (prof) cudaEventRecord(h->ev[5], s);

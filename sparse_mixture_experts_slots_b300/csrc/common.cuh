@@ -21,6 +21,13 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the grid this one depends on (launched before it in the stream) has
+// completed and its writes are visible.  Returns at once for a normal launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid in the stream start its prologue while this one runs.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------- element access
 template <typename T> struct act_traits;
 template <> struct act_traits<float> {

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_kernel(const uint4* __
                                                                  const int32_t* __restrict__ row,
                                                                  const int32_t* __restrict__ expert_rows, int N,
                                                                  int E, int R, int vecs) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const long long w = (long long)blockIdx.x * DC_WARPS + warp;
   if (w < N) {
@@ -44,9 +46,10 @@ int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_
   const long long warps = (long long)N + (long long)E * R;
   if (warps == 0 || (long long)E * R == 0) return 0;
   const unsigned blocks = (unsigned)((warps + DC_WARPS - 1) / DC_WARPS);
-  dispatch_kernel<<<blocks, DC_WARPS * 32, 0, s>>>((const uint4*)x, (uint4*)xe, expert, row, expert_rows, N, E, R,
-                                                   row_bytes / 16);
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+  return launch_k(dispatch_kernel, dim3(blocks), dim3(DC_WARPS * 32), 0, s, false, 1, (const uint4*)x, (uint4*)xe,
+                  expert, row, expert_rows, N, E, R, row_bytes / 16) == cudaSuccess
+             ? 1
+             : -1;
 }
 
 // Forward path: the slots of the routing step and the dispatch copy in one pass.
@@ -60,6 +63,8 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
     int32_t* __restrict__ row, int32_t* __restrict__ tok_of_row, long long N, int T, int E, int nT, int C, int R,
     int vecs, bool debug, uint32_t* err, uint4* __restrict__ y, const uint4* __restrict__ resid,
     uint32_t* __restrict__ zero_ptr, int zero_words) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const long long w = (long long)blockIdx.x * DC_WARPS + warp;
   if (blockIdx.x == 0)
@@ -116,7 +121,7 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
 }
 
 int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, void* y, const void* resid,
-                          uint32_t* zero_ptr, int zero_words, cudaStream_t s) {
+                          uint32_t* zero_ptr, int zero_words, cudaStream_t s, bool pdl) {
   const long long N = (long long)a.G * a.T;
   long long warps = N + (long long)a.E * a.R;
   if (warps == 0 && zero_words == 0) return 0;
@@ -124,11 +129,12 @@ int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, void* y, 
   const int nT = (a.T + ROUTE_TILE - 1) / ROUTE_TILE;
   const int vecs = a.d * (a.x_bf16 ? 2 : 4) / 16;
   const unsigned blocks = (unsigned)((warps + DC_WARPS - 1) / DC_WARPS);
-  dispatch_slots_kernel<<<blocks, DC_WARPS * 32, 0, s>>>((const uint4*)x, (uint4*)xe, a.expert, a.tile_base,
-                                                         a.group_off, a.expert_rows, a.slot, a.keep, a.row,
-                                                         a.tok_of_row, N, a.T, a.E, nT, a.C, a.R, vecs, a.debug,
-                                                         a.err, (uint4*)y, (const uint4*)resid, zero_ptr, zero_words);
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+  return launch_k(dispatch_slots_kernel, dim3(blocks), dim3(DC_WARPS * 32), 0, s, pdl, 1, (const uint4*)x, (uint4*)xe,
+                  a.expert, a.tile_base, a.group_off, a.expert_rows, a.slot, a.keep, a.row, a.tok_of_row, N, a.T, a.E,
+                  nT, a.C, a.R, vecs, a.debug, a.err, (uint4*)y, (const uint4*)resid, zero_ptr, zero_words) ==
+                 cudaSuccess
+             ? 1
+             : -1;
 }
 
 // ---------------------------------------------------------------- combine
@@ -156,6 +162,8 @@ __global__ void __launch_bounds__(DC_WARPS * 32) combine_kernel(const uint4* __r
                                                                 const float* __restrict__ gate,
                                                                 const uint4* __restrict__ resid, uint4* __restrict__ y,
                                                                 int N, int R, int vecs) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const long long t = (long long)blockIdx.x * DC_WARPS + warp;
   if (t >= N) return;
@@ -206,17 +214,16 @@ __global__ void __launch_bounds__(DC_WARPS * 32) combine_kernel(const uint4* __r
 }
 
 int launch_combine(const void* ye, const int32_t* expert, const int32_t* row, const float* gate, const void* resid,
-                   void* y, int N, int d, int R, bool bf16, cudaStream_t s) {
+                   void* y, int N, int d, int R, bool bf16, cudaStream_t s, bool pdl) {
   if (N == 0) return 0;
   const int vecs = d * (bf16 ? 2 : 4) / 16;
   const unsigned blocks = (unsigned)((N + DC_WARPS - 1) / DC_WARPS);
-  if (bf16)
-    combine_kernel<true><<<blocks, DC_WARPS * 32, 0, s>>>((const uint4*)ye, expert, row, gate, (const uint4*)resid,
-                                                          (uint4*)y, N, R, vecs);
-  else
-    combine_kernel<false><<<blocks, DC_WARPS * 32, 0, s>>>((const uint4*)ye, expert, row, gate,
-                                                           (const uint4*)resid, (uint4*)y, N, R, vecs);
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+  const cudaError_t e =
+      bf16 ? launch_k(combine_kernel<true>, dim3(blocks), dim3(DC_WARPS * 32), 0, s, pdl, 1, (const uint4*)ye, expert,
+                      row, gate, (const uint4*)resid, (uint4*)y, N, R, vecs)
+           : launch_k(combine_kernel<false>, dim3(blocks), dim3(DC_WARPS * 32), 0, s, pdl, 1, (const uint4*)ye, expert,
+                      row, gate, (const uint4*)resid, (uint4*)y, N, R, vecs);
+  return e == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace smoe

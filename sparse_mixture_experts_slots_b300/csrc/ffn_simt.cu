@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(256) grouped_linear_simt_kernel(const T* __res
                                                                   const T* __restrict__ bias, T* __restrict__ out,
                                                                   const int32_t* __restrict__ expert_rows, int R,
                                                                   int M, int K) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float as[GL_BK][GL_BN + 4];
   __shared__ float bs[GL_BK][GL_BM + 4];
   const int e = blockIdx.z;
@@ -67,19 +69,20 @@ __global__ void __launch_bounds__(256) grouped_linear_simt_kernel(const T* __res
 
 int launch_grouped_linear_simt(const void* in, const void* W, const void* bias, void* out,
                                const int32_t* expert_rows, int E, int R, int M, int K, bool relu, bool bf16,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool pdl) {
   if (E == 0 || R == 0) return 0;
   dim3 grid((M + GL_BM - 1) / GL_BM, (R + GL_BN - 1) / GL_BN, E);
-#define SMOE_GL(T, RL)                                                                                      \
-  grouped_linear_simt_kernel<T, RL><<<grid, 256, 0, s>>>((const T*)in, (const T*)W, (const T*)bias, (T*)out, \
-                                                         expert_rows, R, M, K)
+  cudaError_t e;
+#define SMOE_GL(T, RL)                                                                                           \
+  e = launch_k(grouped_linear_simt_kernel<T, RL>, grid, dim3(256), 0, s, pdl, 1, (const T*)in, (const T*)W,     \
+               (const T*)bias, (T*)out, expert_rows, R, M, K)
   if (bf16) {
     if (relu) SMOE_GL(__nv_bfloat16, true); else SMOE_GL(__nv_bfloat16, false);
   } else {
     if (relu) SMOE_GL(float, true); else SMOE_GL(float, false);
   }
 #undef SMOE_GL
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+  return e == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace smoe

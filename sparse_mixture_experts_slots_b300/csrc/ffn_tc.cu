@@ -10,7 +10,7 @@
 // the gate is used as is, never renormalised).
 //
 // One persistent kernel runs both layers of every expert.  A tile is
-//     out^T[m, n] = sum_k W[e, m, k] * in[e*R + n, k],  m in a 128- or 256-row block, n in a BN-row chunk
+//     out^T[m, n] = sum_k W[e, m, k] * in[e*R + n, k],  m in a 128-row block, n in a BN-row chunk
 // ("swap AB": the expert's weight rows fill the 128-row MMA, its tokens are the N side).
 // Layer-1 tiles (W1, input xe) write h; layer-2 tiles (W2, input h) write ye, or y
 // when the combine is fused.  Tiles are handed out by an atomic ticket in an order
@@ -18,14 +18,13 @@
 // expert s - LOOK (a lead of about 8 tiles per CTA), so h is read back from L2; a layer-2 tile waits
 // (bounded) until all layer-1 tiles of its expert and chunk have been stored.
 //
-// Per CTA (one per SM, 320 threads):
+// Per CTA (one per SM, 192 threads):
 //   warp 0, one lane : scheduler + TMA producer.  Takes tickets, publishes each tile in a
 //                      small shared-memory queue, streams its W and activation tiles
 //                      (128-byte swizzle) into a ring of stages (one barrier each).
-//   warp 1, one lane : MMA issuer.  tcgen05.mma (M = 128, N = BN, K = 16; one per 128-row
-//                      block, both blocks reading the same activation tile) into one of
-//                      two TMEM accumulator sets, so the epilogue of a tile overlaps the next.
-//   warps 2-9        : epilogue.  tcgen05.ld, + bias, ReLU (layer 1), bf16, store;
+//   warp 1, one lane : MMA issuer.  tcgen05.mma (M = 128, N = BN, K = 16) into one of two
+//                      TMEM accumulators, so the epilogue of a tile overlaps the next.
+//   warps 2-5        : epilogue.  tcgen05.ld, + bias, ReLU (layer 1), bf16, store;
 //                      layer 1 then publishes its chunk to the layer-2 tiles.
 // Every wait is bounded; on timeout the CTA sets the error flag, stops taking tiles,
 // drains its own copies and MMAs, frees TMEM and returns.
@@ -39,7 +38,7 @@ namespace smoe {
 constexpr int FF_BM = 128;
 constexpr int FF_BK = 64;          // 64 bf16 = 128 bytes = one swizzle atom
 constexpr int FF_ATOM_A = FF_BM * FF_BK * 2;
-constexpr int FF_THREADS = 320;  // producer warp, MMA warp, 8 epilogue warps
+constexpr int FF_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
 constexpr int FF_SCHED = 4;        // tile queue depth
 constexpr int FF_MAX_STAGES = 8;
 constexpr int FF_RING = 200 * 1024;
@@ -57,20 +56,19 @@ struct FfnParams {
   uint32_t* done1;               // [E * NCH], zero at launch
   uint32_t* err;
   int E, R, d, F, BN, NCH, LOOK, NA, STAGES, stage_bytes, combine, w_evict_first;
-  int MB;                        // 128-row weight blocks per tile (1 or 2)
 };
 
 struct FfTile {
   int layer, e, mt, nc;
 };
 
-// Ticket -> tile.  Per expert: S1 = NCH * F/(128 MB) layer-1 tiles, S2 = NCH * d/(128 MB)
-// layer-2 tiles (m-block major, chunk minor).  Order: layer 1 of experts 0..L-1; then, for
+// Ticket -> tile.  Per expert: S1 = NCH * F/128 layer-1 tiles, S2 = NCH * d/128 layer-2
+// tiles (m-block major, chunk minor).  Order: layer 1 of experts 0..L-1; then, for
 // s = L..E-1, layer 1 of s followed by layer 2 of s - L; then layer 2 of the last L.
 // Returns false past the last tile.
 __device__ __forceinline__ bool ff_decode(uint32_t t, const FfnParams& p, FfTile& tl) {
-  const uint32_t S1 = (uint32_t)p.NCH * (uint32_t)(p.F / (FF_BM * p.MB));
-  const uint32_t S2 = (uint32_t)p.NCH * (uint32_t)(p.d / (FF_BM * p.MB));
+  const uint32_t S1 = (uint32_t)p.NCH * (uint32_t)(p.F / FF_BM);
+  const uint32_t S2 = (uint32_t)p.NCH * (uint32_t)(p.d / FF_BM);
   const uint32_t L = (uint32_t)min(p.LOOK, p.E);
   const uint32_t E = (uint32_t)p.E;
   uint32_t r;
@@ -115,8 +113,8 @@ struct FfShared {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void epi_sync() {  // named barrier over the 8 epilogue warps
-  asm volatile("bar.sync 1, 256;" ::: "memory");
+__device__ __forceinline__ void epi_sync() {  // named barrier over the 4 epilogue warps
+  asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
@@ -136,9 +134,7 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
   FfShared& sh = *reinterpret_cast<FfShared*>(ring + FF_RING);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int BN = p.BN, NA = p.NA, STAGES = p.STAGES;
-  const int MB = p.MB;
-  const int ACC = MB * BN;  // TMEM columns of one accumulator set (MB blocks of BN)
-  const uint32_t TMEM_COLS = 2 * ACC <= 32 ? 32 : 2 * ACC <= 64 ? 64 : 2 * ACC <= 128 ? 128 : 2 * ACC <= 256 ? 256 : 512;
+  const uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -168,7 +164,9 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_slot;
-  const int MT1 = p.F / (FF_BM * MB);
+  const int MT1 = p.F / FF_BM;
+  griddep_launch_dependents();  // after the TMEM allocation: a dependent grid cannot starve it
+  griddep_wait();               // the dispatched rows, row counts and cleared counters
 
   if (warp == 0 && lane == 0) {
     // ---------------- scheduler + TMA producer
@@ -210,7 +208,7 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
       const CUtensorMap* tmB = l1 ? &tmX : &tmH;
       const int K = l1 ? p.d : p.F;
       const int M = l1 ? p.F : p.d;
-      const int arow = tl.e * M + tl.mt * FF_BM * MB;
+      const int arow = tl.e * M + tl.mt * FF_BM;
       const int brow = tl.e * p.R + tl.nc * BN;
       const int atoms = K / FF_BK;
       bool ok = true;
@@ -225,7 +223,7 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
           tma_load_3d_hint(stage, tmA, &sh.full[slot], 0, arow, a0, w_policy);
         else
           tma_load_3d(stage, tmA, &sh.full[slot], 0, arow, a0);
-        tma_load_3d(stage + NA * MB * FF_ATOM_A, tmB, &sh.full[slot], 0, brow, a0);
+        tma_load_3d(stage + NA * FF_ATOM_A, tmB, &sh.full[slot], 0, brow, a0);
         ++gst;
       }
       if (!ok) {
@@ -259,7 +257,7 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
       }
       tc_fence_after();
       const int atoms = (tv.x == 0 ? p.d : p.F) / FF_BK;
-      const uint32_t acc = tmem + (uint32_t)(buf * ACC);
+      const uint32_t acc = tmem + (uint32_t)(buf * BN);
       bool ok = true;
       for (int a0 = 0; a0 < atoms; a0 += NA) {
         const int slot = (int)(gst % (uint32_t)STAGES);
@@ -268,13 +266,12 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
         const int na = min(NA, atoms - a0);
         const uint32_t st = smem_u32(ring + (size_t)slot * p.stage_bytes);
         for (int at = 0; at < na; ++at) {
-          const uint32_t a_s = st + at * MB * FF_ATOM_A;  // atom: MB blocks of 128 rows x 128 B
-          const uint32_t b_s = st + NA * MB * FF_ATOM_A + at * BN * FF_BK * 2;
+          const uint32_t a_s = st + at * FF_ATOM_A;
+          const uint32_t b_s = st + NA * FF_ATOM_A + at * BN * FF_BK * 2;
 #pragma unroll
           for (int kk = 0; kk < FF_BK / 16; ++kk)
-            for (int hb = 0; hb < MB; ++hb)
-              tc_mma_bf16(acc + (uint32_t)(hb * BN), sw128_kmajor_desc(a_s + hb * FF_ATOM_A + kk * 32),
-                          sw128_kmajor_desc(b_s + kk * 32), idesc, (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16(acc, sw128_kmajor_desc(a_s + kk * 32), sw128_kmajor_desc(b_s + kk * 32), idesc,
+                        (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&sh.empty[slot]);
         ++gst;
@@ -290,9 +287,8 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
       ++sidx;
     }
   } else if (warp >= 2) {
-    // ---------------- epilogue (warps 2-9; TMEM lane quadrant = warp % 4, block hb = (warp - 2) / 4)
+    // ---------------- epilogue (warps 2-5; TMEM lane quadrant = warp % 4)
     const int quad = warp & 3;
-    const int hb = (warp - 2) >> 2;
     const bool leader = threadIdx.x == 64;
     int sidx = 0, lt = 0;
     while (true) {
@@ -321,13 +317,12 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
       const int n0 = nc * BN;
       const int nv = min(BN, rows - n0);
       const int M = l1 ? p.F : p.d;
-      const bool active = hb < MB;  // with one block the second four warps only keep step
-      const int m = (mt * MB + (active ? hb : 0)) * FF_BM + quad * 32 + lane;
+      const int m = mt * FF_BM + quad * 32 + lane;
       const __nv_bfloat16* bias = l1 ? p.b1 : p.b2;
       const float bv = bias ? __bfloat162float(bias[(size_t)e * M + m]) : 0.f;
-      const uint32_t taddr = tmem + (uint32_t)(buf * ACC + (active ? hb : 0) * BN) + ((uint32_t)(quad * 32) << 16);
+      const uint32_t taddr = tmem + (uint32_t)(buf * BN) + ((uint32_t)(quad * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < (active ? nv : 0); c0 += 16) {
+      for (int c0 = 0; c0 < nv; c0 += 16) {
         uint32_t r[16];
         tmem_ld16(taddr + (uint32_t)c0, r);
         tmem_ld_wait();
@@ -444,13 +439,9 @@ FfnTiling ffn_tiling(int R, int d, int F) {
   t.NCH = R <= 256 ? 1 : (R + 255) / 256;
   const int rows = (R + t.NCH - 1) / t.NCH;
   t.BN = rows <= 16 ? 16 : (rows + 15) / 16 * 16;
-  // Tiles of two 128-row weight blocks sharing one activation tile (MB = 2) halve the
-  // activation re-reads, but on Switch-Base shapes they measured slower: their layer-2
-  // tiles stream ~1.6 MB each and lengthen the kernel's tail.  One block per tile.
-  t.MB = 1;
   (void)d;
   (void)F;
-  const int stage_atom = t.MB * FF_ATOM_A + t.BN * FF_BK * 2;
+  const int stage_atom = FF_ATOM_A + t.BN * FF_BK * 2;
   t.NA = stage_atom <= 48 * 1024 ? 2 : 1;  // 256 contiguous bytes per row when it fits
   t.stage_bytes = t.NA * stage_atom;
   t.STAGES = FF_RING / t.stage_bytes < FF_MAX_STAGES ? FF_RING / t.stage_bytes : FF_MAX_STAGES;
@@ -464,15 +455,15 @@ FfnTiling ffn_tiling(int R, int d, int F) {
 
 size_t ffn_counter_words(int E, int R, int d, int F) { return 1 + (size_t)E * ffn_tiling(R, d, F).NCH; }
 
-int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s) {
+int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   if (L.E == 0 || L.R == 0) return 0;
   if (!tc_shape_ok(L.F, L.d) || !tc_shape_ok(L.d, L.F)) return -1;
   const FfnTiling t = ffn_tiling(L.R, L.d, L.F);
   if (t.STAGES < 2 || t.BN > 256) return -1;
   CUtensorMap tmW1, tmX, tmW2, tmH;
-  if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
+  if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM, (uint32_t)t.NA)) return -1;
   if (!encode_bf16_3d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
-  if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
+  if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM, (uint32_t)t.NA)) return -1;
   if (!encode_bf16_3d(&tmH, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
   FfnParams p;
   p.b1 = (const __nv_bfloat16*)L.b1;
@@ -492,11 +483,10 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s) {
   p.F = L.F;
   p.BN = t.BN;
   p.NCH = t.NCH;
-  p.MB = t.MB;
   // Layer-2 tiles of an expert are handed out LOOK experts after its layer-1 tiles: a
   // lead of about 8 tiles per CTA, so a layer-1 tile (up to ~3 tiles of queue latency
   // behind a CTA's earlier tiles) is normally stored before anyone needs it.
-  const int per_expert = t.NCH * (L.F / (FF_BM * t.MB) + L.d / (FF_BM * t.MB));
+  const int per_expert = t.NCH * (L.F / FF_BM + L.d / FF_BM);
   const int ctas_max = device_sm_count();
   p.LOOK = (8 * ctas_max + per_expert - 1) / per_expert;
   if (p.LOOK > L.E) p.LOOK = L.E;
@@ -509,18 +499,13 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s) {
   const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
   if (cudaFuncSetAttribute(ffn_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return -1;
-  const long long tiles = (long long)L.E * t.NCH * (L.F / (FF_BM * t.MB) + L.d / (FF_BM * t.MB));
+  const long long tiles = (long long)L.E * t.NCH * (L.F / FF_BM + L.d / FF_BM);
   if (tiles >= (1ll << 31) || (long long)L.E * L.R >= (1ll << 31) || (long long)L.E * L.F >= (1ll << 31) ||
       (long long)L.E * L.d >= (1ll << 31))
     return -1;  // tickets and TMA row coordinates are 32-bit
   const int ctas = (int)(tiles < device_sm_count() ? tiles : device_sm_count());
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
-  cfg.blockDim = dim3(FF_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.numAttrs = 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, ffn_persistent_kernel, tmW1, tmX, tmW2, tmH, p);
+  const cudaError_t e = launch_k(ffn_persistent_kernel, dim3((unsigned)ctas), dim3(FF_THREADS), (size_t)smem, s, pdl,
+                                 1, tmW1, tmX, tmW2, tmH, p);
   return e == cudaSuccess ? 1 : -1;
 }
 

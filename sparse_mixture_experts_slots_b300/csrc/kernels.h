@@ -7,6 +7,36 @@
 
 namespace smoe {
 
+// Launch `kern` on stream s.  pdl: the kernel may start while the previous kernel of the
+// stream finishes (it must call griddep_wait() before touching that kernel's results);
+// cluster_x > 1: thread-block clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Tokens per routing tile (softmax/top-1 CTA and slot-scan warp).
 constexpr int ROUTE_TILE = 128;
 
@@ -72,7 +102,7 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 // not null (combine fused into the FFN), dropped tokens' rows of y get their final
 // value here (x_residual or zero), and `zero` words at zero_ptr are cleared.
 int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, void* y, const void* resid,
-                          uint32_t* zero_ptr, int zero_words, cudaStream_t s);
+                          uint32_t* zero_ptr, int zero_words, cudaStream_t s, bool pdl);
 
 // xe[expert[t]*R + row[t]] = x[t] for kept tokens (row[t] >= 0); rows r >= expert_rows[e]
 // of every expert block are zeroed.
@@ -81,18 +111,17 @@ int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_
 
 // y[t] = (row[t] >= 0 ? gate[t] * ye[expert[t]*R + row[t]] : 0) (+ resid[t]).
 int launch_combine(const void* ye, const int32_t* expert, const int32_t* row, const float* gate,
-                   const void* resid, void* y, int N, int d, int R, bool bf16, cudaStream_t s);
+                   const void* resid, void* y, int N, int d, int R, bool bf16, cudaStream_t s, bool pdl);
 
 // out[e*R + n, m] = act(sum_k in[e*R + n, k] * W[e, m, k] + bias[e, m]) for n < expert_rows[e].
 // CUDA-core kernel for float32 and for shapes the tensor-core kernel does not take.
 int launch_grouped_linear_simt(const void* in, const void* W, const void* bias, void* out,
                                const int32_t* expert_rows, int E, int R, int M, int K, bool relu,
-                               bool bf16, cudaStream_t s);
+                               bool bf16, cudaStream_t s, bool pdl);
 
 // Expert FFN (both layers of every expert) in one persistent tensor-core kernel.
 struct FfnTiling {
   int BN;           // token rows per tile (MMA N), multiple of 16
-  int MB;           // 128-row weight blocks per tile (1 or 2)
   int NCH;          // chunks of BN rows per expert block
   int NA;           // 64-column atoms per pipeline stage
   int stage_bytes;
@@ -119,6 +148,6 @@ struct FfnLaunch {
 };
 // Needs d % 128 == 0 and F % 128 == 0 (tc_shape_ok both ways).  Returns launches or -1.
 bool tc_shape_ok(int M, int K);
-int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s);
+int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl);
 
 }  // namespace smoe

@@ -30,6 +30,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) router_logits_kernel(const T* __restrict__ x, const float* __restrict__ Wr,
                                                             const float* __restrict__ br, float* __restrict__ z,
                                                             int N, int d, int E) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float xs[RL_BK][RL_BM + 4];
   __shared__ float ws[RL_BK][RL_BN + 4];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -78,6 +80,8 @@ __global__ void __launch_bounds__(256) route_softmax_kernel(
     const float* __restrict__ z, int T, int E, int nT, int32_t* __restrict__ expert, float* __restrict__ gate,
     int32_t* __restrict__ rank, int32_t* __restrict__ tile_hist, float* __restrict__ tile_P,
     float* __restrict__ probs, uint32_t* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ int32_t hist[];
   __shared__ float m_s[ROUTE_TILE], s_s[ROUTE_TILE];
   __shared__ int a_s[ROUTE_TILE];
@@ -147,6 +151,8 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
     float* __restrict__ P, int32_t* __restrict__ group_off, int32_t* __restrict__ expert_rows,
     float* __restrict__ balance, float* __restrict__ aux_g, float* __restrict__ aux, float* __restrict__ partial,
     uint32_t* __restrict__ counter) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ int sh_h[SCAN_WARPS][32];
   __shared__ float sh_p[SCAN_WARPS][32];
   __shared__ int is_last;
@@ -231,6 +237,8 @@ __global__ void __launch_bounds__(256) route_slots_kernel(
     const int32_t* __restrict__ expert, const int32_t* __restrict__ tile_base, const int32_t* __restrict__ group_off,
     long long N, int T, int E, int nT, int C, int R, int32_t* __restrict__ slot, uint8_t* __restrict__ keep,
     int32_t* __restrict__ row, int32_t* __restrict__ tok_of_row, bool debug, uint32_t* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (t >= N) return;
   const int g = (int)(t / T);
@@ -273,20 +281,26 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
       launches += n;
     } else {
       dim3 grid((a.E + RL_BN - 1) / RL_BN, (unsigned)((N + RL_BM - 1) / RL_BM));
-      router_logits_kernel<float><<<grid, 256, 0, s>>>((const float*)a.x, a.Wr, a.br, a.logits, (int)N, a.d, a.E);
-      route_softmax_kernel<<<dim3(nT, a.G), 256, a.E * sizeof(int32_t), s>>>(
-          a.logits, a.T, a.E, nT, a.expert, a.gate, a.slot, a.tile_hist, a.tile_P, a.probs, a.err);
+      if (launch_k(router_logits_kernel<float>, grid, dim3(256), 0, s, false, 1, (const float*)a.x, a.Wr, a.br,
+                   a.logits, (int)N, a.d, a.E) != cudaSuccess ||
+          launch_k(route_softmax_kernel, dim3(nT, a.G), dim3(256), a.E * sizeof(int32_t), s, true, 1, a.logits, a.T,
+                   a.E, nT, a.expert, a.gate, a.slot, a.tile_hist, a.tile_P, a.probs, a.err) != cudaSuccess)
+        return -1;
       launches += 2;
     }
   }
-  route_scan_kernel<<<route_scan_blocks(a.E), SCAN_WARPS * 32, 0, s>>>(
-      a.tile_hist, a.tile_P, a.G, a.T, a.E, nT, a.C, a.alpha, a.tile_base, a.raw, a.accepted, a.P, a.group_off,
-      a.expert_rows, a.balance, a.aux_g, a.aux, a.scan_partial, a.scan_counter);
+  // The scan follows the router kernel of this call (programmatic launch); with no
+  // tokens it is the first kernel of the call.
+  if (launch_k(route_scan_kernel, dim3(route_scan_blocks(a.E)), dim3(SCAN_WARPS * 32), 0, s, N > 0, 1, a.tile_hist,
+               a.tile_P, a.G, a.T, a.E, nT, a.C, a.alpha, a.tile_base, a.raw, a.accepted, a.P, a.group_off,
+               a.expert_rows, a.balance, a.aux_g, a.aux, a.scan_partial, a.scan_counter) != cudaSuccess)
+    return -1;
   ++launches;
   if (N > 0 && a.slots) {
-    route_slots_kernel<<<(unsigned)((N + 255) / 256), 256, 0, s>>>(a.expert, a.tile_base, a.group_off, N, a.T, a.E,
-                                                                   nT, a.C, a.R, a.slot, a.keep, a.row,
-                                                                   a.tok_of_row, a.debug, a.err);
+    if (launch_k(route_slots_kernel, dim3((unsigned)((N + 255) / 256)), dim3(256), 0, s, true, 1, a.expert,
+                 a.tile_base, a.group_off, N, a.T, a.E, nT, a.C, a.R, a.slot, a.keep, a.row, a.tok_of_row, a.debug,
+                 a.err) != cudaSuccess)
+      return -1;
     ++launches;
   }
   if (cudaGetLastError() != cudaSuccess) return -1;

@@ -45,6 +45,8 @@ constexpr float LOG2E = 1.4426950408889634f;
 // one TMA box (and one MMA) covers all three pieces of a slice's experts.
 __global__ void router_split_kernel(const float* __restrict__ Wr, __nv_bfloat16* __restrict__ ws, int E, int d,
                                     int EC, long long n /* Q * EC * d */) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const long long row = i / d;  // q * EC + el = expert index
@@ -212,11 +214,13 @@ __global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar.tmem_slot;
+  griddep_launch_dependents();  // after the TMEM allocation: a dependent grid cannot starve it
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
     int issued = 0;
     bool ok = true;
+    griddep_wait();  // the W_r pieces come from the previous kernel
     for (int st = 0; st < NST; ++st) {
       const int slot = st % Cf::STAGES;
       if (st >= Cf::STAGES && !mbar_wait(&bar.empty[slot], ((st / Cf::STAGES) - 1) & 1)) { ok = false; break; }
@@ -457,20 +461,9 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const Route
   auto kern = router_tc_kernel<EC, DEEP>;
   constexpr int smem = rt_smem_bytes<EC, DEEP>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(Q * nT), (unsigned)a.G, 1);
-  cfg.blockDim = dim3(RT_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)Q;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = Q > 1 ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, use3d, a.expert, a.gate,
-                                           rank, a.tile_hist, a.tile_P, a.logits_out, a.probs, a.err);
+  const cudaError_t e = launch_k(kern, dim3((unsigned)(Q * nT), (unsigned)a.G, 1), dim3(RT_THREADS, 1, 1), smem, s,
+                                 /*pdl=*/true, (unsigned)Q, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, use3d, a.expert,
+                                 a.gate, rank, a.tile_hist, a.tile_P, a.logits_out, a.probs, a.err);
   return e == cudaSuccess ? 1 : -1;
 }
 
@@ -501,8 +494,9 @@ int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
   if (EC > 256 || Q > 8) return -1;
   const long long n = (long long)Q * EC * a.d;
   const unsigned sb = (unsigned)((n + 255) / 256 < 148 * 16 ? (n + 255) / 256 : 148 * 16);
-  router_split_kernel<<<sb, 256, 0, s>>>(a.Wr, (__nv_bfloat16*)a.wsplit, a.E, a.d, EC, n);
-  if (cudaGetLastError() != cudaSuccess) return -1;
+  if (launch_k(router_split_kernel, dim3(sb), dim3(256), 0, s, false, 1, a.Wr, (__nv_bfloat16*)a.wsplit, a.E, a.d, EC,
+               n) != cudaSuccess)
+    return -1;
   // One wave on this device's SMs -> the deep ring; EC >= 128 always takes it (512 TMEM columns).
   const long long ctas = (long long)Q * nT * a.G;
   const bool deep = EC >= 128 || ctas <= (long long)device_sm_count();

@@ -55,7 +55,7 @@ SMALL = {
     "override": (LayerShape("override", 1, 64, 128, 128, 4, 1.0, capacity_override=8), {}),
     "capacity-over-T": (LayerShape("capacity-over-T", 2, 64, 128, 128, 4, 8.0), {}),
     "many-experts": (LayerShape("many-experts", 1, 700, 128, 128, 300, 1.0), {}),
-    # d and d_ff multiples of 256: FFN tiles of two 128-row weight blocks sharing one activation tile
+    # d and d_ff multiples of 256, several 128-row weight blocks per expert in both layers
     "tc-two-blocks": (LayerShape("tc-two-blocks", 2, 300, 256, 512, 6, 1.0), dict(expert_bias_std=0.05)),
     # d = 192: three 64-column atoms, so the router's last two-atom stage has a zero-filled half
     "odd-atoms": (LayerShape("odd-atoms", 2, 260, 192, 256, 12, 1.0), dict(router_bias_std=0.1)),
