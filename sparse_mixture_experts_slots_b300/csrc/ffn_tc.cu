@@ -263,14 +263,20 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
         const int slot = (int)(gst % (uint32_t)STAGES);
         if (!mbar_wait(&sh.full[slot], (gst / STAGES) & 1)) { ok = false; break; }
         tc_fence_after();
-        const int na = min(NA, atoms - a0);
+        // Descriptors of the stage's first A and B atoms; later K-steps and atoms add their
+        // offset (16-byte units) to the start-address field, which cannot carry out of its
+        // 14 bits inside the 227 KB shared window.
         const uint32_t st = smem_u32(ring + (size_t)slot * p.stage_bytes);
-        for (int at = 0; at < na; ++at) {
-          const uint32_t a_s = st + at * FF_ATOM_A;
-          const uint32_t b_s = st + NA * FF_ATOM_A + at * BN * FF_BK * 2;
+        const uint64_t da = sw128_kmajor_desc(st);
+        const uint64_t db = sw128_kmajor_desc(st + NA * FF_ATOM_A);
+        const uint32_t b_atom16 = (uint32_t)(BN * FF_BK * 2) >> 4;
+#pragma unroll
+        for (int at = 0; at < 2; ++at) {
+          if (at >= NA || a0 + at >= atoms) break;
 #pragma unroll
           for (int kk = 0; kk < FF_BK / 16; ++kk)
-            tc_mma_bf16(acc, sw128_kmajor_desc(a_s + kk * 32), sw128_kmajor_desc(b_s + kk * 32), idesc,
+            tc_mma_bf16(acc, da + (uint64_t)((at * FF_ATOM_A + kk * 32) >> 4),
+                        db + (uint64_t)(at * b_atom16 + ((kk * 32) >> 4)), idesc,
                         (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&sh.empty[slot]);
@@ -442,7 +448,7 @@ FfnTiling ffn_tiling(int R, int d, int F) {
   (void)d;
   (void)F;
   const int stage_atom = FF_ATOM_A + t.BN * FF_BK * 2;
-  t.NA = stage_atom <= 48 * 1024 ? 2 : 1;  // 256 contiguous bytes per row when it fits
+  t.NA = stage_atom <= 48 * 1024 ? 2 : 1;  // 256 contiguous bytes per row when it fits (NA <= 2)
   t.stage_bytes = t.NA * stage_atom;
   t.STAGES = FF_RING / t.stage_bytes < FF_MAX_STAGES ? FF_RING / t.stage_bytes : FF_MAX_STAGES;
   if (t.STAGES < 3 && t.NA == 2) {  // keep at least three stages in flight
