@@ -53,9 +53,13 @@ int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_
 }
 
 // Forward path: the slots of the routing step and the dispatch copy in one pass.
-// Warp w < N: lane 0 turns the token's in-tile rank (held in slot[]) into its slot,
-// keep flag and row (as route_slots_kernel does), then the warp copies the row.
-// Warps past N zero the rows past each expert's count.
+// Warp w < N takes token w: every lane first loads its part of the row (that read does not
+// depend on routing), while lane 0 turns the token's in-tile rank (held in slot[]) into its
+// slot, keep flag and row (as route_slots_kernel does); then the row goes to its expert
+// block, or, for a dropped token with the combine fused into the FFN, y gets the residual
+// (or zero).  Warps past N zero the rows past each expert's count.
+constexpr int DS_VMAX = 4;  // 16-byte vectors per lane held in registers (rows <= 2 KB)
+
 __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
     const uint4* __restrict__ x, uint4* __restrict__ xe, const int32_t* __restrict__ expert,
     const int32_t* __restrict__ tile_base, const int32_t* __restrict__ group_off,
@@ -70,10 +74,19 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero_ptr[i] = 0u;
   if (w < N) {
+    const uint4* src = x + w * vecs;
+    const bool in_regs = vecs <= 32 * DS_VMAX;
+    uint4 v[DS_VMAX];
+    if (in_regs) {
+#pragma unroll
+      for (int k = 0; k < DS_VMAX; ++k)
+        if (lane + 32 * k < vecs) v[k] = __ldg(src + lane + 32 * k);
+    }
     int r = -1, e = 0;
     if (lane == 0) {
       const int g = (int)(w / T);
       const int ti = (int)(w - (long long)g * T);
+      const int rank = slot[w];
       e = expert[w];
       if (e < 0 || e >= E) {
         raise_error(err, ERR_BOUNDS);
@@ -81,11 +94,11 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
         slot[w] = 0;
         keep[w] = 0;
       } else {
-        const int s = tile_base[((size_t)g * nT + ti / ROUTE_TILE) * E + e] + slot[w];
-        const bool k = s < C;
+        const int s = tile_base[((size_t)g * nT + ti / ROUTE_TILE) * E + e] + rank;
+        const int goff = group_off[(size_t)g * E + e];
         slot[w] = s;
-        if (k) {
-          r = group_off[(size_t)g * E + e] + s;
+        if (s < C) {
+          r = goff + s;
           if (r < 0 || r >= R) {
             if (debug) raise_error(err, ERR_BOUNDS);
             r = -1;
@@ -102,13 +115,18 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
     if (r < 0) {
       if (y) {  // a dropped token skips the expert: y is the residual alone, or zero
         const uint4 zero = make_uint4(0, 0, 0, 0);
-        for (int v = lane; v < vecs; v += 32) y[w * vecs + v] = resid ? __ldg(resid + w * vecs + v) : zero;
+        for (int k = lane; k < vecs; k += 32) y[w * vecs + k] = resid ? __ldg(resid + w * vecs + k) : zero;
       }
       return;
     }
-    const uint4* src = x + w * vecs;
     uint4* dst = xe + ((long long)e * R + r) * vecs;
-    for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
+    if (in_regs) {
+#pragma unroll
+      for (int k = 0; k < DS_VMAX; ++k)
+        if (lane + 32 * k < vecs) dst[lane + 32 * k] = v[k];
+    } else {
+      for (int k = lane; k < vecs; k += 32) dst[k] = __ldg(src + k);
+    }
     return;
   }
   const long long dr = w - N;
@@ -117,7 +135,7 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
   if (r < expert_rows[e]) return;
   uint4* dst = xe + dr * vecs;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int v = lane; v < vecs; v += 32) dst[v] = zero;
+  for (int k = lane; k < vecs; k += 32) dst[k] = zero;
 }
 
 int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, void* y, const void* resid,
