@@ -188,6 +188,34 @@ SWITCH_API switch_status switch_stage_ms(switch_handle h, float* ms, int n);
 /* Number of kernels the last switch_forward on this handle launched. */
 SWITCH_API int switch_last_launch_count(switch_handle h);
 
+/*
+ * switch_route without a handle, for callers that cannot allocate device memory once
+ * they are running: code inside a CUDA graph that is already instantiated, a real-time
+ * loop or driver where cudaMalloc could block or fail, an allocator-less embedding.
+ * (No page of the method has a counterpart: it is a packaging choice of this library.)
+ *
+ * Same arguments and outputs as switch_route, with the config in place of a handle.
+ * The routing kernels' scratch (split router weights, per-tile statistics, scan state,
+ * error word) is one fixed 32 MiB device array inside the library, which every GPU that
+ * loads the library holds until the process exits.  Nothing is allocated: no cudaMalloc,
+ * no cudaFree, no allocating library call; the call enqueues one cudaMemsetAsync of 16
+ * bytes (clearing the error word and a counter) and the routing kernels on `stream`.
+ *   - The first call on a device looks up the array's device address on that device
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call on a device shares the array and leaves its contents behind: two calls
+ *     whose kernels overlap on the GPU (different streams, or concurrent graphs) race and
+ *     give wrong results.  Serialise them.
+ *   - A configuration whose scratch needs more than 32 MiB returns SWITCH_ERR_UNSUPPORTED.
+ *     The scratch is about 12 G ceil(T/128) E + 6 E d + 4 E G C bytes with bfloat16
+ *     activations (all five named workloads fit; 65536 tokens x 2048 experts needs 22 MiB),
+ *     plus 4 G T E bytes of logits with float32 activations.  Invalid arguments return
+ *     SWITCH_ERR_INVALID_ARG.
+ *   - Device-side flags (a bounded wait that ran out, non-finite logits) stay in the array
+ *     and are not reported; use switch_route on a handle when they are needed.
+ */
+SWITCH_API switch_status switch_route_static(const switch_config* cfg, const void* x, const float* Wr,
+                                  const float* br, const switch_route_out* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

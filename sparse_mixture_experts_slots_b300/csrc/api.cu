@@ -4,6 +4,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 
 #include "../../include/switch_moe.h"
@@ -450,3 +451,117 @@ switch_status switch_stage_ms(switch_handle h, float* ms, int n) {
 int switch_last_launch_count(switch_handle h) { return h ? h->last_launches : -1; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- routing without a handle
+// switch_route_static keeps everything the routing kernels need between them (the split
+// router weights, per-tile statistics, scan state, the error word) in this one fixed
+// device array instead of a workspace from switch_create.  Every GPU that loads the
+// library holds it until the process exits.
+namespace {
+
+constexpr size_t STATIC_ROUTE_SCRATCH_BYTES = (size_t)32 << 20;  // 32 MiB
+__device__ __align__(256) uint8_t g_static_route_scratch[STATIC_ROUTE_SCRATCH_BYTES];
+
+constexpr int STATIC_MAX_DEVICES = 64;
+std::mutex g_static_mu;
+void* g_static_addr[STATIC_MAX_DEVICES];  // device address of the array, per device
+
+// Device address of the array on the current device (looked up once per device; the
+// name is only a host-side stand-in and must never be handed to a kernel).
+void* static_route_scratch(int dev) {
+  if (dev < 0 || dev >= STATIC_MAX_DEVICES) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_route_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_static_addr[dev] = p;
+  }
+  return g_static_addr[dev];
+}
+
+}  // namespace
+
+extern "C" switch_status switch_route_static(const switch_config* cfg, const void* x, const float* Wr,
+                                             const float* br, const switch_route_out* out, void* stream) {
+  if (!config_ok(cfg) || !Wr) return SWITCH_ERR_INVALID_ARG;
+  const int N = cfg->G * cfg->T;
+  if (!route_out_ok(out, N)) return SWITCH_ERR_INVALID_ARG;
+  if (N > 0 && !x) return SWITCH_ERR_INVALID_ARG;
+  if (x && !aligned16(x)) return SWITCH_ERR_INVALID_ARG;
+  const int C = (int)capacity_of(cfg);
+  const int Ceff = C < cfg->T ? C : cfg->T;
+  const int R = cfg->G * Ceff;
+  const int nT = (cfg->T + ROUTE_TILE - 1) / ROUTE_TILE;
+  const size_t E = cfg->E, G = cfg->G, d = cfg->d_model;
+  const bool bf16 = cfg->dtype == SWITCH_BF16;
+  // layout of the scratch, as in a handle's workspace (route part only)
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 256);
+    return o;
+  };
+  const size_t o_err = take(sizeof(uint32_t) * 4);  // [0] error word, [1] scan counter
+  const size_t o_logits = take(bf16 ? 0 : (size_t)N * E * sizeof(float));
+  const size_t o_wsplit = take(bf16 ? router_tc_wsplit_bytes(cfg->E, cfg->d_model) : 0);
+  const size_t o_hist = take(G * nT * E * sizeof(int32_t));
+  const size_t o_tP = take(G * nT * E * sizeof(float));
+  const size_t o_base = take(G * nT * E * sizeof(int32_t));
+  const size_t o_goff = take(G * E * sizeof(int32_t));
+  const size_t o_tor = take(E * (size_t)R * sizeof(int32_t));
+  const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
+  if (off > STATIC_ROUTE_SCRATCH_BYTES) return SWITCH_ERR_UNSUPPORTED;  // needs more than 32 MiB
+  (void)d;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWITCH_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(static_route_scratch(dev));
+  if (!ws) return SWITCH_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  // the error word and the scan's block counter must start at zero; everything else is
+  // written by the kernels before it is read
+  if (cudaMemsetAsync(ws + o_err, 0, sizeof(uint32_t) * 4, s) != cudaSuccess) return SWITCH_ERR_CUDA;
+  const bool want_logits = (cfg->flags & SWITCH_FLAG_WRITE_LOGITS) && out->logits;
+  const bool want_probs = (cfg->flags & SWITCH_FLAG_WRITE_PROBS) && out->probs;
+  RouteArgs a;
+  a.x = x;
+  a.Wr = Wr;
+  a.br = br;
+  a.G = cfg->G;
+  a.T = cfg->T;
+  a.d = cfg->d_model;
+  a.E = cfg->E;
+  a.C = C;
+  a.R = R;
+  a.x_bf16 = bf16;
+  a.alpha = cfg->alpha;
+  a.debug = (cfg->flags & SWITCH_FLAG_DEBUG_BOUNDS) != 0;
+  a.slots = true;
+  a.logits = want_logits ? out->logits : reinterpret_cast<float*>(ws + o_logits);
+  a.logits_out = want_logits ? out->logits : nullptr;
+  a.wsplit = ws + o_wsplit;
+  a.tile_hist = reinterpret_cast<int32_t*>(ws + o_hist);
+  a.tile_P = reinterpret_cast<float*>(ws + o_tP);
+  a.tile_base = reinterpret_cast<int32_t*>(ws + o_base);
+  a.group_off = reinterpret_cast<int32_t*>(ws + o_goff);
+  a.tok_of_row = reinterpret_cast<int32_t*>(ws + o_tor);
+  a.scan_partial = reinterpret_cast<float*>(ws + o_part);
+  a.scan_counter = reinterpret_cast<uint32_t*>(ws + o_err) + 1;
+  a.err = reinterpret_cast<uint32_t*>(ws + o_err);
+  a.expert = out->expert;
+  a.slot = out->slot;
+  a.keep = out->keep;
+  a.gate = out->gate;
+  a.row = out->row;
+  a.raw = out->raw_count;
+  a.accepted = out->accepted_count;
+  a.P = out->P;
+  a.balance = out->balance;
+  a.aux_g = out->aux_loss_per_group;
+  a.aux = out->aux_loss;
+  a.expert_rows = out->expert_rows;
+  a.probs = want_probs ? out->probs : nullptr;
+  return launch_route(a, s) < 0 ? SWITCH_ERR_CUDA : SWITCH_OK;
+}
