@@ -118,19 +118,22 @@ def algorithmic(shape, expert_rows: np.ndarray, N: int):
 
 
 def traffic_from_profiles(kernel: str):
-    """DRAM bytes per launch recorded by an ncu capture (profiles/ncu_traffic.json),
-    or None when the kernel source changed since the capture."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    """DRAM bytes per launch recorded by an ncu capture (profiles/ncu_traffic.txt), or None
+    when the kernel's source file changed since the capture (the counters no longer apply)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     try:
-        with open(path) as fh:
-            rec = json.load(fh)[kernel]
-        src = os.path.join(ROOT, "sparse_mixture_experts_slots_b300", "csrc", rec["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if h != rec["source_sha256_16"]:
-            return None
-        return rec
+        for line in open(path, encoding="utf-8"):
+            parts = line.split()
+            if not parts or parts[0].startswith("#") or parts[0] != kernel:
+                continue
+            src = os.path.join(ROOT, "sparse_mixture_experts_slots_b300", "csrc", parts[1])
+            h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            if h != parts[2]:
+                return None
+            return {"dram_bytes_per_launch": int(parts[3])}
     except Exception:
         return None
+    return None
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
@@ -271,7 +274,8 @@ def run_gpu(args, shape):
     n_prof = max(3, min(args.steps, 50))
     stage_sum = np.zeros(5)
     for i in range(args.warmup + n_prof):
-        flush.fill_(1.0)
+        for _ in range(4):  # ~1 GB of writes: the host enqueues the whole step while they run,
+            flush.fill_(1.0)  # so no launch latency lands between the stage events
         step(prof_layer)
         st = np.array(prof_layer.stage_ms())
         if i >= args.warmup:

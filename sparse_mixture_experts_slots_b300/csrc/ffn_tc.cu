@@ -38,7 +38,8 @@ namespace smoe {
 constexpr int FF_BM = 128;
 constexpr int FF_BK = 64;          // 64 bf16 = 128 bytes = one swizzle atom
 constexpr int FF_ATOM_A = FF_BM * FF_BK * 2;
-constexpr int FF_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
+// 64 + 128 MB threads: producer warp, MMA warp, 4 epilogue warps per 128-row weight block
+template <int MB> constexpr int ff_threads() { return 64 + 128 * MB; }
 constexpr int FF_SCHED = 4;        // tile queue depth
 constexpr int FF_MAX_STAGES = 8;
 constexpr int FF_RING = 200 * 1024;
@@ -56,19 +57,20 @@ struct FfnParams {
   uint32_t* done1;               // [E * NCH], zero at launch
   uint32_t* err;
   int E, R, d, F, BN, NCH, LOOK, NA, STAGES, stage_bytes, combine, w_evict_first;
+  int MB;                        // 128-row weight blocks per tile (the kernel's template value)
 };
 
 struct FfTile {
   int layer, e, mt, nc;
 };
 
-// Ticket -> tile.  Per expert: S1 = NCH * F/128 layer-1 tiles, S2 = NCH * d/128 layer-2
-// tiles (m-block major, chunk minor).  Order: layer 1 of experts 0..L-1; then, for
+// Ticket -> tile.  Per expert: S1 = NCH * F/(128 MB) layer-1 tiles, S2 = NCH * d/(128 MB)
+// layer-2 tiles (m-block major, chunk minor).  Order: layer 1 of experts 0..L-1; then, for
 // s = L..E-1, layer 1 of s followed by layer 2 of s - L; then layer 2 of the last L.
 // Returns false past the last tile.
 __device__ __forceinline__ bool ff_decode(uint32_t t, const FfnParams& p, FfTile& tl) {
-  const uint32_t S1 = (uint32_t)p.NCH * (uint32_t)(p.F / FF_BM);
-  const uint32_t S2 = (uint32_t)p.NCH * (uint32_t)(p.d / FF_BM);
+  const uint32_t S1 = (uint32_t)p.NCH * (uint32_t)(p.F / (FF_BM * p.MB));
+  const uint32_t S2 = (uint32_t)p.NCH * (uint32_t)(p.d / (FF_BM * p.MB));
   const uint32_t L = (uint32_t)min(p.LOOK, p.E);
   const uint32_t E = (uint32_t)p.E;
   uint32_t r;
@@ -113,8 +115,9 @@ struct FfShared {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void epi_sync() {  // named barrier over the 4 epilogue warps
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+template <int MB>
+__device__ __forceinline__ void epi_sync() {  // named barrier over the epilogue warps
+  asm volatile("bar.sync 1, %0;" ::"n"(128 * MB) : "memory");
 }
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
@@ -125,7 +128,11 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(FF_THREADS, 1)
+// MB: 128-row weight blocks per tile, all reading one activation tile (compile-time, so the
+// MMA issue loop stays fully unrolled).  NBUF: TMEM accumulator sets (2: the epilogue of
+// a tile overlaps the next tile's MMAs; 1 when two sets do not fit in 512 columns).
+template <int MB, int NBUF>
+__global__ void __launch_bounds__(ff_threads<MB>(), 1)
     ffn_persistent_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
                           const __grid_constant__ FfnParams p) {
@@ -134,7 +141,9 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
   FfShared& sh = *reinterpret_cast<FfShared*>(ring + FF_RING);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int BN = p.BN, NA = p.NA, STAGES = p.STAGES;
-  const uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+  const int ACC = MB * BN;  // TMEM columns of one accumulator set
+  const int cols = NBUF * ACC;
+  const uint32_t TMEM_COLS = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -164,7 +173,7 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_slot;
-  const int MT1 = p.F / FF_BM;
+  const int MT1 = p.F / (FF_BM * MB);
   griddep_launch_dependents();  // after the TMEM allocation: a dependent grid cannot starve it
   griddep_wait();               // the dispatched rows, row counts and cleared counters
 
@@ -208,7 +217,7 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
       const CUtensorMap* tmB = l1 ? &tmX : &tmH;
       const int K = l1 ? p.d : p.F;
       const int M = l1 ? p.F : p.d;
-      const int arow = tl.e * M + tl.mt * FF_BM;
+      const int arow = tl.e * M + tl.mt * FF_BM * MB;
       const int brow = tl.e * p.R + tl.nc * BN;
       const int atoms = K / FF_BK;
       bool ok = true;
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
           tma_load_3d_hint(stage, tmA, &sh.full[slot], 0, arow, a0, w_policy);
         else
           tma_load_3d(stage, tmA, &sh.full[slot], 0, arow, a0);
-        tma_load_3d(stage + NA * FF_ATOM_A, tmB, &sh.full[slot], 0, brow, a0);
+        tma_load_3d(stage + NA * MB * FF_ATOM_A, tmB, &sh.full[slot], 0, brow, a0);
         ++gst;
       }
       if (!ok) {
@@ -249,15 +258,15 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
       }
       const int4 tv = sh.sched[qs];
       if (tv.x < 0) break;
-      const int buf = lt & 1;
-      if (lt >= 2 && !mbar_wait(&sh.aempty[buf], ((lt / 2) - 1) & 1)) {
+      const int buf = lt % NBUF;
+      if (lt >= NBUF && !mbar_wait(&sh.aempty[buf], ((lt / NBUF) - 1) & 1)) {
         raise_error(p.err, ERR_TIMEOUT);
         sh.abort_flag = 1;
         break;
       }
       tc_fence_after();
       const int atoms = (tv.x == 0 ? p.d : p.F) / FF_BK;
-      const uint32_t acc = tmem + (uint32_t)(buf * BN);
+      const uint32_t acc = tmem + (uint32_t)(buf * ACC);
       bool ok = true;
       for (int a0 = 0; a0 < atoms; a0 += NA) {
         const int slot = (int)(gst % (uint32_t)STAGES);
@@ -268,16 +277,19 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
         // 14 bits inside the 227 KB shared window.
         const uint32_t st = smem_u32(ring + (size_t)slot * p.stage_bytes);
         const uint64_t da = sw128_kmajor_desc(st);
-        const uint64_t db = sw128_kmajor_desc(st + NA * FF_ATOM_A);
+        const uint64_t db = sw128_kmajor_desc(st + NA * MB * FF_ATOM_A);
         const uint32_t b_atom16 = (uint32_t)(BN * FF_BK * 2) >> 4;
 #pragma unroll
         for (int at = 0; at < 2; ++at) {
           if (at >= NA || a0 + at >= atoms) break;
 #pragma unroll
           for (int kk = 0; kk < FF_BK / 16; ++kk)
-            tc_mma_bf16(acc, da + (uint64_t)((at * FF_ATOM_A + kk * 32) >> 4),
-                        db + (uint64_t)(at * b_atom16 + ((kk * 32) >> 4)), idesc,
-                        (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int hb = 0; hb < MB; ++hb)  // weight block hb: rows 128 hb .. of the atom
+              tc_mma_bf16(acc + (uint32_t)(hb * BN),
+                          da + (uint64_t)(((at * MB + hb) * FF_ATOM_A + kk * 32) >> 4),
+                          db + (uint64_t)(at * b_atom16 + ((kk * 32) >> 4)), idesc,
+                          (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&sh.empty[slot]);
         ++gst;
@@ -293,17 +305,19 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
       ++sidx;
     }
   } else if (warp >= 2) {
-    // ---------------- epilogue (warps 2-5; TMEM lane quadrant = warp % 4)
+    // ---------------- epilogue (warps 2 .. 1 + 4 MB; TMEM lane quadrant = warp % 4,
+    // weight block hb = (warp - 2) / 4)
     const int quad = warp & 3;
+    const int hb = (warp - 2) >> 2;
     const bool leader = threadIdx.x == 64;
     int sidx = 0, lt = 0;
     while (true) {
       const int qs = sidx % FF_SCHED;
-      const int buf = lt & 1;
+      const int buf = lt % NBUF;
       if (leader) {
         int ok = mbar_wait(&sh.sfull[qs], (sidx / FF_SCHED) & 1) ? 1 : 0;
         const int4 tv = sh.sched[qs];
-        if (ok && tv.x >= 0 && !mbar_wait(&sh.afull[buf], (lt / 2) & 1)) ok = 0;
+        if (ok && tv.x >= 0 && !mbar_wait(&sh.afull[buf], (lt / NBUF) & 1)) ok = 0;
         if (!ok) {
           raise_error(p.err, ERR_TIMEOUT);
           sh.abort_flag = 1;
@@ -311,10 +325,10 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
         sh.ep_ok = ok;
         sh.ep_tile = tv;
       }
-      epi_sync();
+      epi_sync<MB>();
       const int4 tv = sh.ep_tile;
       const int ok = sh.ep_ok;
-      epi_sync();  // everyone has read the broadcast before the leader can overwrite it
+      epi_sync<MB>();  // everyone has read the broadcast before the leader can overwrite it
       if (!ok || tv.x < 0) break;
       tc_fence_after();
       const bool l1 = tv.x == 0;
@@ -323,10 +337,10 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
       const int n0 = nc * BN;
       const int nv = min(BN, rows - n0);
       const int M = l1 ? p.F : p.d;
-      const int m = mt * FF_BM + quad * 32 + lane;
+      const int m = (mt * MB + hb) * FF_BM + quad * 32 + lane;
       const __nv_bfloat16* bias = l1 ? p.b1 : p.b2;
       const float bv = bias ? __bfloat162float(bias[(size_t)e * M + m]) : 0.f;
-      const uint32_t taddr = tmem + (uint32_t)(buf * BN) + ((uint32_t)(quad * 32) << 16);
+      const uint32_t taddr = tmem + (uint32_t)(buf * ACC + hb * BN) + ((uint32_t)(quad * 32) << 16);
 #pragma unroll 1
       for (int c0 = 0; c0 < nv; c0 += 16) {
         uint32_t r[16];
@@ -364,7 +378,7 @@ __global__ void __launch_bounds__(FF_THREADS, 1)
         }
       }
       tc_fence_before();
-      epi_sync();  // every thread's TMEM reads and stores of this tile are done
+      epi_sync<MB>();  // every thread's TMEM reads and stores of this tile are done
       if (leader) {
         mbar_arrive(&sh.aempty[buf]);
         if (l1) {
@@ -445,9 +459,12 @@ FfnTiling ffn_tiling(int R, int d, int F) {
   t.NCH = R <= 256 ? 1 : (R + 255) / 256;
   const int rows = (R + t.NCH - 1) / t.NCH;
   t.BN = rows <= 16 ? 16 : (rows + 15) / 16 * 16;
-  (void)d;
-  (void)F;
-  const int stage_atom = FF_ATOM_A + t.BN * FF_BK * 2;
+  // Large token tiles (BN >= 128) are read once for two 128-row weight blocks: TMA ingest
+  // per SM (~100 GB/s) is what bounds those layers, and this halves the token re-reads.
+  // Small ones keep one block per tile (shorter layer-2 tiles, shorter tail).
+  t.MB = (t.BN >= 128 && d % 256 == 0 && F % 256 == 0) ? 2 : 1;
+  t.NBUF = 2 * t.MB * t.BN <= 512 ? 2 : 1;
+  const int stage_atom = t.MB * FF_ATOM_A + t.BN * FF_BK * 2;
   t.NA = stage_atom <= 48 * 1024 ? 2 : 1;  // 256 contiguous bytes per row when it fits (NA <= 2)
   t.stage_bytes = t.NA * stage_atom;
   t.STAGES = FF_RING / t.stage_bytes < FF_MAX_STAGES ? FF_RING / t.stage_bytes : FF_MAX_STAGES;
@@ -467,9 +484,9 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   const FfnTiling t = ffn_tiling(L.R, L.d, L.F);
   if (t.STAGES < 2 || t.BN > 256) return -1;
   CUtensorMap tmW1, tmX, tmW2, tmH;
-  if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM, (uint32_t)t.NA)) return -1;
+  if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
   if (!encode_bf16_3d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
-  if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM, (uint32_t)t.NA)) return -1;
+  if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
   if (!encode_bf16_3d(&tmH, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
   FfnParams p;
   p.b1 = (const __nv_bfloat16*)L.b1;
@@ -489,10 +506,11 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.F = L.F;
   p.BN = t.BN;
   p.NCH = t.NCH;
+  p.MB = t.MB;
   // Layer-2 tiles of an expert are handed out LOOK experts after its layer-1 tiles: a
   // lead of about 8 tiles per CTA, so a layer-1 tile (up to ~3 tiles of queue latency
   // behind a CTA's earlier tiles) is normally stored before anyone needs it.
-  const int per_expert = t.NCH * (L.F / FF_BM + L.d / FF_BM);
+  const int per_expert = t.NCH * (L.F / (FF_BM * t.MB) + L.d / (FF_BM * t.MB));
   const int ctas_max = device_sm_count();
   p.LOOK = (8 * ctas_max + per_expert - 1) / per_expert;
   if (p.LOOK > L.E) p.LOOK = L.E;
@@ -503,15 +521,26 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.combine = L.combine ? 1 : 0;
   p.w_evict_first = t.NCH == 1 ? 1 : 0;  // several chunks re-read a weight tile
   const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
-  if (cudaFuncSetAttribute(ffn_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return -1;
-  const long long tiles = (long long)L.E * t.NCH * (L.F / FF_BM + L.d / FF_BM);
+  const long long tiles = (long long)L.E * t.NCH * (L.F / (FF_BM * t.MB) + L.d / (FF_BM * t.MB));
   if (tiles >= (1ll << 31) || (long long)L.E * L.R >= (1ll << 31) || (long long)L.E * L.F >= (1ll << 31) ||
       (long long)L.E * L.d >= (1ll << 31))
     return -1;  // tickets and TMA row coordinates are 32-bit
   const int ctas = (int)(tiles < device_sm_count() ? tiles : device_sm_count());
-  const cudaError_t e = launch_k(ffn_persistent_kernel, dim3((unsigned)ctas), dim3(FF_THREADS), (size_t)smem, s, pdl,
-                                 1, tmW1, tmX, tmW2, tmH, p);
+  cudaError_t e;
+#define SMOE_FFN(MBV, NBV)                                                                                         \
+  do {                                                                                                             \
+    auto kern = ffn_persistent_kernel<MBV, NBV>;                                                                   \
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1; \
+    e = launch_k(kern, dim3((unsigned)ctas), dim3(ff_threads<MBV>()), (size_t)smem, s, pdl, 1, tmW1, tmX, tmW2, tmH, \
+                 p);                                                                                               \
+  } while (0)
+  if (t.MB == 1)
+    SMOE_FFN(1, 2);
+  else if (t.NBUF == 2)
+    SMOE_FFN(2, 2);
+  else
+    SMOE_FFN(2, 1);
+#undef SMOE_FFN
   return e == cudaSuccess ? 1 : -1;
 }
 

@@ -122,6 +122,8 @@ int launch_grouped_linear_simt(const void* in, const void* W, const void* bias, 
 // Expert FFN (both layers of every expert) in one persistent tensor-core kernel.
 struct FfnTiling {
   int BN;           // token rows per tile (MMA N), multiple of 16
+  int MB;           // 128-row weight blocks per tile (1 or 2)
+  int NBUF;         // TMEM accumulator sets (2: double-buffered)
   int NCH;          // chunks of BN rows per expert block
   int NA;           // 64-column atoms per pipeline stage
   int stage_bytes;

@@ -55,8 +55,10 @@ SMALL = {
     "override": (LayerShape("override", 1, 64, 128, 128, 4, 1.0, capacity_override=8), {}),
     "capacity-over-T": (LayerShape("capacity-over-T", 2, 64, 128, 128, 4, 8.0), {}),
     "many-experts": (LayerShape("many-experts", 1, 700, 128, 128, 300, 1.0), {}),
-    # d and d_ff multiples of 256, several 128-row weight blocks per expert in both layers
-    "tc-two-blocks": (LayerShape("tc-two-blocks", 2, 300, 256, 512, 6, 1.0), dict(expert_bias_std=0.05)),
+    # token tiles of >= 128 rows with d, d_ff multiples of 256: FFN tiles of two 128-row weight
+    # blocks sharing the token tile; 150 rows -> one TMEM accumulator set, 128 -> two
+    "tc-two-blocks": (LayerShape("tc-two-blocks", 1, 600, 256, 512, 4, 1.0), dict(expert_bias_std=0.05)),
+    "tc-two-blocks-db": (LayerShape("tc-two-blocks-db", 1, 512, 256, 512, 4, 1.0), dict(router_bias_std=0.1)),
     # d = 192: three 64-column atoms, so the router's last two-atom stage has a zero-filled half
     "odd-atoms": (LayerShape("odd-atoms", 2, 260, 192, 256, 12, 1.0), dict(router_bias_std=0.1)),
 }
