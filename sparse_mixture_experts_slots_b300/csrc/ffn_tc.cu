@@ -107,6 +107,7 @@ struct FfShared {
   uint64_t afull[2], aempty[2];
   int4 sched[FF_SCHED];
   int4 ep_tile;       // epilogue: the leader's tile, broadcast by a named barrier
+  __nv_bfloat16 xpose[8][16][32];  // per epilogue warp: 16 tokens x 32 features, for 16-byte stores
   uint32_t tmem_slot;
   volatile int abort_flag;
   int ep_ok;
@@ -341,40 +342,72 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       const __nv_bfloat16* bias = l1 ? p.b1 : p.b2;
       const float bv = bias ? __bfloat162float(bias[(size_t)e * M + m]) : 0.f;
       const uint32_t taddr = tmem + (uint32_t)(buf * ACC + hb * BN) + ((uint32_t)(quad * 32) << 16);
+      // 64 columns per round: up to four TMEM loads in flight before one wait (a wait per
+      // 16 columns left the MMA waiting on the epilogue with a single accumulator set)
 #pragma unroll 1
-      for (int c0 = 0; c0 < nv; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(taddr + (uint32_t)c0, r);
+      for (int c0 = 0; c0 < nv; c0 += 64) {
+        uint32_t r[4][16];
+        const int nch = min(4, (nv - c0 + 15) / 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < nch) tmem_ld16(taddr + (uint32_t)(c0 + 16 * q), r[q]);
         tmem_ld_wait();
-        if (l1) {
-          __nv_bfloat16* dst = p.h + ((size_t)e * p.R + n0 + c0) * p.F + m;
+        // Each 16-column chunk goes through shared memory: lane f writes feature f of the 16
+        // tokens, then every lane stores two 16-byte pieces (8 features of one token).
+        __nv_bfloat16 (*xp)[32] = sh.xpose[warp - 2];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < nv) dst[(size_t)j * p.F] = __float2bfloat16_rn(fmaxf(__uint_as_float(r[j]) + bv, 0.f));
-        } else if (!p.combine) {
-          __nv_bfloat16* dst = p.out + ((size_t)e * p.R + n0 + c0) * p.d + m;
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < nv) dst[(size_t)j * p.d] = __float2bfloat16_rn(__uint_as_float(r[j]) + bv);
-        } else {
-          // lane j < 16 fetches the token and gate of column c0 + j, then broadcasts them
-          int tk = 0;
-          float gt = 0.f;
-          if (lane < 16 && c0 + lane < nv) {
-            tk = p.tok_of_row[(size_t)e * p.R + n0 + c0 + lane];
-            gt = p.gate[tk];
-          }
+        for (int q = 0; q < 4; ++q) {
+          if (q >= nch) break;
+          const int cb = c0 + 16 * q;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int tj = __shfl_sync(0xffffffffu, tk, j);
-            const float gj = __shfl_sync(0xffffffffu, gt, j);
-            if (c0 + j < nv) {
-              const float ye = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[j]) + bv));
-              float o = gj * ye;
-              if (p.resid) o += __bfloat162float(p.resid[(size_t)tj * p.d + m]);
-              p.out[(size_t)tj * p.d + m] = __float2bfloat16_rn(o);
+            const float v = __uint_as_float(r[q][j]) + bv;
+            xp[j][lane] = __float2bfloat16_rn(l1 ? fmaxf(v, 0.f) : v);  // h, or ye rounded to bf16
+          }
+          __syncwarp();
+          const int mb = (mt * MB + hb) * FF_BM + quad * 32;  // first feature of this warp
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int piece = lane + 32 * half;  // 64 pieces of 16 bytes: token piece / 4, features 8 (piece % 4)
+            const int j = piece >> 2, f8 = (piece & 3) * 8;
+            if (cb + j < nv) {
+              const uint4 val = *reinterpret_cast<const uint4*>(&xp[j][f8]);
+              const size_t row = (size_t)e * p.R + n0 + cb + j;
+              if (l1) {
+                *reinterpret_cast<uint4*>(p.h + row * p.F + mb + f8) = val;
+              } else if (!p.combine) {
+                *reinterpret_cast<uint4*>(p.out + row * p.d + mb + f8) = val;
+              } else {
+                // y_t = gate_t * ye (+ x_t): the token and gate of this row, the residual as a vector
+                const int tk = p.tok_of_row[row];
+                const float g = p.gate[tk];
+                const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&val);
+                float o[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float2 f = __bfloat1622float2(yv[k]);
+                  o[2 * k] = g * f.x;
+                  o[2 * k + 1] = g * f.y;
+                }
+                if (p.resid) {
+                  const uint4 rv = __ldg(reinterpret_cast<const uint4*>(p.resid + (size_t)tk * p.d + mb + f8));
+                  const __nv_bfloat162* rr = reinterpret_cast<const __nv_bfloat162*>(&rv);
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    const float2 f = __bfloat1622float2(rr[k]);
+                    o[2 * k] += f.x;
+                    o[2 * k + 1] += f.y;
+                  }
+                }
+                uint4 ov;
+                __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(&ov);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) op[k] = __floats2bfloat162_rn(o[2 * k], o[2 * k + 1]);
+                *reinterpret_cast<uint4*>(p.out + (size_t)tk * p.d + mb + f8) = ov;
+              }
             }
           }
+          __syncwarp();  // the chunk's reads of xp are done before the next chunk writes it
         }
       }
       tc_fence_before();
