@@ -108,6 +108,8 @@ struct FfShared {
   int4 sched[FF_SCHED];
   int4 ep_tile;       // epilogue: the leader's tile, broadcast by a named barrier
   __nv_bfloat16 xpose[8][16][32];  // per epilogue warp: 16 tokens x 32 features, for 16-byte stores
+  int tok[256];       // combine: token of each column of the current layer-2 tile
+  float gate[256];    // and its gate
   uint32_t tmem_slot;
   volatile int abort_flag;
   int ep_ok;
@@ -342,6 +344,15 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       const __nv_bfloat16* bias = l1 ? p.b1 : p.b2;
       const float bv = bias ? __bfloat162float(bias[(size_t)e * M + m]) : 0.f;
       const uint32_t taddr = tmem + (uint32_t)(buf * ACC + hb * BN) + ((uint32_t)(quad * 32) << 16);
+      const bool comb = !l1 && p.combine;
+      if (comb) {  // the tile's tokens and gates, fetched once (two dependent loads per column)
+        for (int j = threadIdx.x - 64; j < nv; j += 128 * MB) {
+          const int tk = p.tok_of_row[(size_t)e * p.R + n0 + j];
+          sh.tok[j] = tk;
+          sh.gate[j] = p.gate[tk];
+        }
+        epi_sync<MB>();
+      }
       // 64 columns per round: up to four TMEM loads in flight before one wait (a wait per
       // 16 columns left the MMA waiting on the epilogue with a single accumulator set)
 #pragma unroll 1
@@ -379,8 +390,8 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
                 *reinterpret_cast<uint4*>(p.out + row * p.d + mb + f8) = val;
               } else {
                 // y_t = gate_t * ye (+ x_t): the token and gate of this row, the residual as a vector
-                const int tk = p.tok_of_row[row];
-                const float g = p.gate[tk];
+                const int tk = sh.tok[cb + j];
+                const float g = sh.gate[cb + j];
                 const __nv_bfloat162* yv = reinterpret_cast<const __nv_bfloat162*>(&val);
                 float o[8];
 #pragma unroll
