@@ -18,14 +18,16 @@
 // expert s - LOOK (a lead of about 8 tiles per CTA), so h is read back from L2; a layer-2 tile waits
 // (bounded) until all layer-1 tiles of its expert and chunk have been stored.
 //
-// Per CTA (one per SM, 192 threads):
+// Per CTA (one per SM, 64 + 256 MB threads):
 //   warp 0, one lane : scheduler + TMA producer.  Takes tickets, publishes each tile in a
 //                      small shared-memory queue, streams its W and activation tiles
 //                      (128-byte swizzle) into a ring of stages (one barrier each).
-//   warp 1, one lane : MMA issuer.  tcgen05.mma (M = 128, N = BN, K = 16) into one of two
-//                      TMEM accumulators, so the epilogue of a tile overlaps the next.
-//   warps 2-5        : epilogue.  tcgen05.ld, + bias, ReLU (layer 1), bf16, store;
-//                      layer 1 then publishes its chunk to the layer-2 tiles.
+//   warp 1, one lane : MMA issuer.  tcgen05.mma (M = 128 per weight block, N = BN, K = 16)
+//                      into one of NBUF TMEM accumulator sets.
+//   warps 2 ..       : epilogue, two warps per (weight block, TMEM lane quadrant), each
+//                      taking alternate 32-column slices.  tcgen05.ld, + bias, ReLU
+//                      (layer 1), bf16, store; layer 1 then publishes its chunk to the
+//                      layer-2 tiles.
 // Every wait is bounded; on timeout the CTA sets the error flag, stops taking tiles,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <mutex>
@@ -38,9 +40,11 @@ namespace smoe {
 constexpr int FF_BM = 128;
 constexpr int FF_BK = 64;          // 64 bf16 = 128 bytes = one swizzle atom
 constexpr int FF_ATOM_A = FF_BM * FF_BK * 2;
-// 64 + 128 MB threads: producer warp, MMA warp, 4 epilogue warps per 128-row weight block
-template <int MB> constexpr int ff_threads() { return 64 + 128 * MB; }
+// 64 + 256 MB threads: producer warp, MMA warp, 8 epilogue warps per 128-row weight block
+constexpr int FF_EPW = 2;  // epilogue warps per (weight block, TMEM lane quadrant)
+template <int MB> constexpr int ff_threads() { return 64 + 128 * FF_EPW * MB; }
 constexpr int FF_SCHED = 4;        // tile queue depth
+constexpr int FF_PB = 64;          // rows of the activation boxes used for partly filled chunks
 constexpr int FF_MAX_STAGES = 8;
 constexpr int FF_RING = 200 * 1024;
 
@@ -106,21 +110,25 @@ struct FfShared {
   uint64_t sfull[FF_SCHED], sempty[FF_SCHED];
   uint64_t afull[2], aempty[2];
   int4 sched[FF_SCHED];
+  int sched_nv[FF_SCHED];  // rows of the tile's token chunk that hold tokens (1 .. BN)
   int4 ep_tile;       // epilogue: the leader's tile, broadcast by a named barrier
-  __nv_bfloat16 xpose[8][16][32];  // per epilogue warp: 16 tokens x 32 features, for 16-byte stores
+  int ep_nv;
+  // per epilogue warp: 16 tokens x 32 features, read back as 16-byte vectors
+  alignas(16) __nv_bfloat16 xpose[8 * FF_EPW][16][32];
   int tok[256];       // combine: token of each column of the current layer-2 tile
   float gate[256];    // and its gate
   uint32_t tmem_slot;
   volatile int abort_flag;
   int ep_ok;
 };
+static_assert(offsetof(FfShared, xpose) % 16 == 0, "16-byte vector reads of the transpose buffer");
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 template <int MB>
 __device__ __forceinline__ void epi_sync() {  // named barrier over the epilogue warps
-  asm volatile("bar.sync 1, %0;" ::"n"(128 * MB) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(128 * FF_EPW * MB) : "memory");
 }
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
@@ -138,6 +146,7 @@ template <int MB, int NBUF>
 __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     ffn_persistent_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
+                          const __grid_constant__ CUtensorMap tmXp, const __grid_constant__ CUtensorMap tmHp,
                           const __grid_constant__ FfnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -167,6 +176,8 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW2);
     prefetch_tmap(&tmH);
+    prefetch_tmap(&tmXp);
+    prefetch_tmap(&tmHp);
   }
   if (warp == 1) {
     tmem_alloc(&sh.tmem_slot, TMEM_COLS);
@@ -190,7 +201,8 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       FfTile tl;
       const uint32_t t = atomicAdd(p.next_tile, 1u);
       const bool has = ff_decode(t, p, tl);
-      if (has && tl.nc * BN >= p.expert_rows[tl.e]) continue;  // empty chunk
+      const int nv = has ? min(BN, p.expert_rows[tl.e] - tl.nc * BN) : 0;
+      if (has && nv <= 0) continue;  // empty chunk
       const int qs = sidx % FF_SCHED;
       if (sidx >= FF_SCHED && !mbar_wait(&sh.sempty[qs], ((sidx / FF_SCHED) - 1) & 1)) {
         raise_error(p.err, ERR_TIMEOUT);
@@ -198,6 +210,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         break;
       }
       sh.sched[qs] = has ? make_int4(tl.layer, tl.e, tl.mt, tl.nc) : make_int4(-1, 0, 0, 0);
+      sh.sched_nv[qs] = nv;
       mbar_arrive(&sh.sfull[qs]);
       ++sidx;
       if (!has) break;
@@ -218,6 +231,12 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       }
       const CUtensorMap* tmA = l1 ? &tmW1 : &tmW2;
       const CUtensorMap* tmB = l1 ? &tmX : &tmH;
+      const CUtensorMap* tmBp = l1 ? &tmXp : &tmHp;
+      // A chunk filled to at most BN - 64 rows loads its activations as 64-row boxes, only
+      // as many as cover its rows (nbox = 0: one box of BN rows)
+      const int nt = (nv + 15) & ~15;
+      const int nbox = (BN > FF_PB && nt <= BN - FF_PB) ? (nt + FF_PB - 1) / FF_PB : 0;
+      const uint32_t tx = nbox ? (uint32_t)(NA * MB * FF_ATOM_A + NA * nbox * FF_PB * FF_BK * 2) : (uint32_t)p.stage_bytes;
       const int K = l1 ? p.d : p.F;
       const int M = l1 ? p.F : p.d;
       const int arow = tl.e * M + tl.mt * FF_BM * MB;
@@ -229,13 +248,21 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         if (gst >= (uint32_t)STAGES && !mbar_wait(&sh.empty[slot], ((gst / STAGES) - 1) & 1)) { ok = false; break; }
         // One 3-D box per operand: NA consecutive 64-column atoms of 128 (or BN) rows, each
         // atom a swizzled [rows x 128 B] block; atoms past K read as zero (never used).
-        mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)p.stage_bytes);
+        mbar_arrive_expect_tx(&sh.full[slot], tx);
         uint8_t* stage = ring + (size_t)slot * p.stage_bytes;
         if (p.w_evict_first)
           tma_load_3d_hint(stage, tmA, &sh.full[slot], 0, arow, a0, w_policy);
         else
           tma_load_3d(stage, tmA, &sh.full[slot], 0, arow, a0);
-        tma_load_3d(stage + NA * MB * FF_ATOM_A, tmB, &sh.full[slot], 0, brow, a0);
+        uint8_t* sb = stage + NA * MB * FF_ATOM_A;
+        if (nbox == 0) {
+          tma_load_3d(sb, tmB, &sh.full[slot], 0, brow, a0);
+        } else {
+          for (int at = 0; at < NA; ++at)  // atom at keeps its [BN x 128 B] place in the stage
+            for (int i = 0; i < nbox; ++i)
+              tma_load_3d(sb + (size_t)(at * BN + i * FF_PB) * (FF_BK * 2), tmBp, &sh.full[slot], 0,
+                          brow + i * FF_PB, a0 + at);
+        }
         ++gst;
       }
       if (!ok) {
@@ -249,7 +276,6 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       if (!mbar_wait(&sh.full[i % STAGES], (i / STAGES) & 1)) raise_error(p.err, ERR_TIMEOUT);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(FF_BM, BN);
     uint32_t gst = 0;
     int sidx = 0, lt = 0;
     while (true) {
@@ -261,6 +287,8 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       }
       const int4 tv = sh.sched[qs];
       if (tv.x < 0) break;
+      // N = the chunk's filled rows rounded up to 16: MMA time and operand reads scale with N
+      const uint32_t idesc = idesc_bf16_f32(FF_BM, (sh.sched_nv[qs] + 15) & ~15);
       const int buf = lt % NBUF;
       if (lt >= NBUF && !mbar_wait(&sh.aempty[buf], ((lt / NBUF) - 1) & 1)) {
         raise_error(p.err, ERR_TIMEOUT);
@@ -308,10 +336,11 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       ++sidx;
     }
   } else if (warp >= 2) {
-    // ---------------- epilogue (warps 2 .. 1 + 4 MB; TMEM lane quadrant = warp % 4,
-    // weight block hb = (warp - 2) / 4)
+    // ---------------- epilogue (warps 2 .. 1 + 8 MB; TMEM lane quadrant = warp % 4,
+    // weight block hb = (warp - 2) / 8, column slice part = ((warp - 2) / 4) % 2)
     const int quad = warp & 3;
-    const int hb = (warp - 2) >> 2;
+    const int hb = (warp - 2) >> 3;
+    const int part = ((warp - 2) >> 2) & 1;
     const bool leader = threadIdx.x == 64;
     int sidx = 0, lt = 0;
     while (true) {
@@ -327,18 +356,18 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         }
         sh.ep_ok = ok;
         sh.ep_tile = tv;
+        sh.ep_nv = sh.sched_nv[qs];
       }
       epi_sync<MB>();
       const int4 tv = sh.ep_tile;
       const int ok = sh.ep_ok;
+      const int nv = sh.ep_nv;
       epi_sync<MB>();  // everyone has read the broadcast before the leader can overwrite it
       if (!ok || tv.x < 0) break;
       tc_fence_after();
       const bool l1 = tv.x == 0;
       const int e = tv.y, mt = tv.z, nc = tv.w;
-      const int rows = p.expert_rows[e];
       const int n0 = nc * BN;
-      const int nv = min(BN, rows - n0);
       const int M = l1 ? p.F : p.d;
       const int m = (mt * MB + hb) * FF_BM + quad * 32 + lane;
       const __nv_bfloat16* bias = l1 ? p.b1 : p.b2;
@@ -346,28 +375,28 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       const uint32_t taddr = tmem + (uint32_t)(buf * ACC + hb * BN) + ((uint32_t)(quad * 32) << 16);
       const bool comb = !l1 && p.combine;
       if (comb) {  // the tile's tokens and gates, fetched once (two dependent loads per column)
-        for (int j = threadIdx.x - 64; j < nv; j += 128 * MB) {
+        for (int j = threadIdx.x - 64; j < nv; j += 128 * FF_EPW * MB) {
           const int tk = p.tok_of_row[(size_t)e * p.R + n0 + j];
           sh.tok[j] = tk;
           sh.gate[j] = p.gate[tk];
         }
         epi_sync<MB>();
       }
-      // 64 columns per round: up to four TMEM loads in flight before one wait (a wait per
-      // 16 columns left the MMA waiting on the epilogue with a single accumulator set)
+      // The two warps of a quadrant take alternate 32-column slices; both TMEM loads of a
+      // slice are in flight before one wait.
 #pragma unroll 1
-      for (int c0 = 0; c0 < nv; c0 += 64) {
-        uint32_t r[4][16];
-        const int nch = min(4, (nv - c0 + 15) / 16);
+      for (int c0 = 32 * part; c0 < nv; c0 += 64) {
+        uint32_t r[2][16];
+        const int nch = min(2, (nv - c0 + 15) / 16);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 2; ++q)
           if (q < nch) tmem_ld16(taddr + (uint32_t)(c0 + 16 * q), r[q]);
         tmem_ld_wait();
         // Each 16-column chunk goes through shared memory: lane f writes feature f of the 16
         // tokens, then every lane stores two 16-byte pieces (8 features of one token).
         __nv_bfloat16 (*xp)[32] = sh.xpose[warp - 2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
           if (q >= nch) break;
           const int cb = c0 + 16 * q;
 #pragma unroll
@@ -500,9 +529,10 @@ bool tc_shape_ok(int M, int K) { return M > 0 && K > 0 && M % FF_BM == 0 && K % 
 
 FfnTiling ffn_tiling(int R, int d, int F) {
   FfnTiling t;
+  // Chunks of 256 rows (one MMA of N = 256): an expert whose tokens fit one chunk streams
+  // its weights once, and a partly filled last chunk loads only the rows it holds.
   t.NCH = R <= 256 ? 1 : (R + 255) / 256;
-  const int rows = (R + t.NCH - 1) / t.NCH;
-  t.BN = rows <= 16 ? 16 : (rows + 15) / 16 * 16;
+  t.BN = R > 256 ? 256 : (R <= 16 ? 16 : (R + 15) / 16 * 16);
   // Large token tiles (BN >= 128) are read once for two 128-row weight blocks: TMA ingest
   // per SM (~100 GB/s) is what bounds those layers, and this halves the token re-reads.
   // Small ones keep one block per tile (shorter layer-2 tiles, shorter tail).
@@ -527,11 +557,18 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   if (!tc_shape_ok(L.F, L.d) || !tc_shape_ok(L.d, L.F)) return -1;
   const FfnTiling t = ffn_tiling(L.R, L.d, L.F);
   if (t.STAGES < 2 || t.BN > 256) return -1;
-  CUtensorMap tmW1, tmX, tmW2, tmH;
+  CUtensorMap tmW1, tmX, tmW2, tmH, tmXp, tmHp;
   if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
   if (!encode_bf16_3d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
   if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
   if (!encode_bf16_3d(&tmH, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
+  if (t.BN > FF_PB) {  // one atom per box: the boxes of a partly filled chunk
+    if (!encode_bf16_3d(&tmXp, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)FF_PB, 1u)) return -1;
+    if (!encode_bf16_3d(&tmHp, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)FF_PB, 1u)) return -1;
+  } else {
+    tmXp = tmX;
+    tmHp = tmH;
+  }
   FfnParams p;
   p.b1 = (const __nv_bfloat16*)L.b1;
   p.b2 = (const __nv_bfloat16*)L.b2;
@@ -576,7 +613,7 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
     auto kern = ffn_persistent_kernel<MBV, NBV>;                                                                   \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1; \
     e = launch_k(kern, dim3((unsigned)ctas), dim3(ff_threads<MBV>()), (size_t)smem, s, pdl, 1, tmW1, tmX, tmW2, tmH, \
-                 p);                                                                                               \
+                 tmXp, tmHp, p);                                                                                               \
   } while (0)
   if (t.MB == 1)
     SMOE_FFN(1, 2);

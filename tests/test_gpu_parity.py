@@ -42,7 +42,8 @@ SMALL = {
     # tensor-core FFN path (d, d_ff multiples of 128); 3 routing tiles per group, ragged tail
     "tc-ragged": (LayerShape("tc-ragged", 2, 300, 256, 384, 8, 1.0), dict(expert_bias_std=0.05,
                                                                           router_bias_std=0.1)),
-    # expert blocks of 313 rows: two 256-row N tiles, the second ragged
+    # expert blocks of 313 rows: two 256-row token chunks, the second partly filled (loaded as
+    # 64-row boxes, two atoms per stage)
     "tc-long-expert": (LayerShape("tc-long-expert", 1, 1000, 128, 256, 4, 1.25), {}),
     # CUDA-core FFN path for widths the tensor-core tiles do not take
     "simt-bf16": (LayerShape("simt-bf16", 3, 129, 72, 40, 5, 0.8), dict(expert_bias_std=0.05)),
@@ -59,6 +60,10 @@ SMALL = {
     # blocks sharing the token tile; 150 rows -> one TMEM accumulator set, 128 -> two
     "tc-two-blocks": (LayerShape("tc-two-blocks", 1, 600, 256, 512, 4, 1.0), dict(expert_bias_std=0.05)),
     "tc-two-blocks-db": (LayerShape("tc-two-blocks-db", 1, 512, 256, 512, 4, 1.0), dict(router_bias_std=0.1)),
+    # 350-row expert blocks with two weight blocks per tile and uneven loads: experts that fit
+    # one 256-row chunk, and second chunks of one or two 64-row boxes
+    "tc-chunks-256": (LayerShape("tc-chunks-256", 2, 700, 256, 512, 4, 1.0),
+                      dict(expert_bias_std=0.05, router_bias_std=0.3)),
     # d = 192: three 64-column atoms, so the router's last two-atom stage has a zero-filled half
     "odd-atoms": (LayerShape("odd-atoms", 2, 260, 192, 256, 12, 1.0), dict(router_bias_std=0.1)),
 }
