@@ -113,7 +113,8 @@ struct FfShared {
   int sched_nv[FF_SCHED];  // rows of the tile's token chunk that hold tokens (1 .. BN)
   int4 ep_tile;       // epilogue: the leader's tile, broadcast by a named barrier
   int ep_nv;
-  // per epilogue warp: 16 tokens x 32 features, read back as 16-byte vectors
+  // per epilogue warp: 16 tokens x 32 features (as 8 token pairs x 32 features, 32-bit
+  // words), read back as 16-byte vectors
   alignas(16) __nv_bfloat16 xpose[8 * FF_EPW][16][32];
   int tok[256];       // combine: token of each column of the current layer-2 tile
   float gate[256];    // and its gate
@@ -392,26 +393,43 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         for (int q = 0; q < 2; ++q)
           if (q < nch) tmem_ld16(taddr + (uint32_t)(c0 + 16 * q), r[q]);
         tmem_ld_wait();
-        // Each 16-column chunk goes through shared memory: lane f writes feature f of the 16
-        // tokens, then every lane stores two 16-byte pieces (8 features of one token).
-        __nv_bfloat16 (*xp)[32] = sh.xpose[warp - 2];
+        // Each 16-column chunk goes through shared memory as 8 token pairs x 32 features, one
+        // 32-bit word (both tokens of a pair) per lane and pair; each lane then reads the 8
+        // features of one pair and one feature group (two 16-byte loads, the halves swapped on
+        // odd pairs so a quarter-warp covers all banks) and splits the two tokens by byte
+        // permutes into two 16-byte stores.
+        uint32_t* xw = reinterpret_cast<uint32_t*>(&sh.xpose[warp - 2][0][0]);
+        const int ip = lane >> 2, f8 = (lane & 3) * 8;
+        const int sw = (ip & 1) * 4;
+        const int mb = (mt * MB + hb) * FF_BM + quad * 32;  // first feature of this warp
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           if (q >= nch) break;
           const int cb = c0 + 16 * q;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float v = __uint_as_float(r[q][j]) + bv;
-            xp[j][lane] = __float2bfloat16_rn(l1 ? fmaxf(v, 0.f) : v);  // h, or ye rounded to bf16
+          for (int i = 0; i < 8; ++i) {
+            float v0 = __uint_as_float(r[q][2 * i]) + bv, v1 = __uint_as_float(r[q][2 * i + 1]) + bv;
+            if (l1) {
+              v0 = fmaxf(v0, 0.f);
+              v1 = fmaxf(v1, 0.f);
+            }
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(v0, v1);  // h, or ye rounded to bf16
+            xw[i * 32 + lane] = *reinterpret_cast<const uint32_t*>(&pr);
           }
           __syncwarp();
-          const int mb = (mt * MB + hb) * FF_BM + quad * 32;  // first feature of this warp
+          const uint4 w0 = *reinterpret_cast<const uint4*>(xw + ip * 32 + f8 + sw);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(xw + ip * 32 + f8 + 4 - sw);
+          const uint4 lo = sw ? w1 : w0, hi = sw ? w0 : w1;  // features f8 .. +3, f8 + 4 .. +7
+          uint4 tv2[2];
+          tv2[0] = make_uint4(__byte_perm(lo.x, lo.y, 0x5410), __byte_perm(lo.z, lo.w, 0x5410),
+                              __byte_perm(hi.x, hi.y, 0x5410), __byte_perm(hi.z, hi.w, 0x5410));
+          tv2[1] = make_uint4(__byte_perm(lo.x, lo.y, 0x7632), __byte_perm(lo.z, lo.w, 0x7632),
+                              __byte_perm(hi.x, hi.y, 0x7632), __byte_perm(hi.z, hi.w, 0x7632));
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int piece = lane + 32 * half;  // 64 pieces of 16 bytes: token piece / 4, features 8 (piece % 4)
-            const int j = piece >> 2, f8 = (piece & 3) * 8;
+          for (int t2 = 0; t2 < 2; ++t2) {
+            const int j = 2 * ip + t2;
             if (cb + j < nv) {
-              const uint4 val = *reinterpret_cast<const uint4*>(&xp[j][f8]);
+              const uint4 val = tv2[t2];
               const size_t row = (size_t)e * p.R + n0 + cb + j;
               if (l1) {
                 *reinterpret_cast<uint4*>(p.h + row * p.F + mb + f8) = val;
@@ -447,7 +465,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
               }
             }
           }
-          __syncwarp();  // the chunk's reads of xp are done before the next chunk writes it
+          __syncwarp();  // the chunk's reads of xw are done before the next chunk writes it
         }
       }
       tc_fence_before();
