@@ -121,6 +121,7 @@ struct FfShared {
   uint32_t tmem_slot;
   volatile int abort_flag;
   int ep_ok;
+  int ep_acc_ok;
 };
 static_assert(offsetof(FfShared, xpose) % 16 == 0, "16-byte vector reads of the transpose buffer");
 
@@ -347,25 +348,24 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     while (true) {
       const int qs = sidx % FF_SCHED;
       const int buf = lt % NBUF;
+      // The leader takes the tile from the queue and broadcasts it; everyone then starts the
+      // tile's bias load (and, for the combine, gathers its tokens and gates) while the
+      // leader waits for the accumulator.  Readers of a broadcast are done with it before
+      // the end-of-tile barrier, so the leader never overwrites it early.
       if (leader) {
-        int ok = mbar_wait(&sh.sfull[qs], (sidx / FF_SCHED) & 1) ? 1 : 0;
-        const int4 tv = sh.sched[qs];
-        if (ok && tv.x >= 0 && !mbar_wait(&sh.afull[buf], (lt / NBUF) & 1)) ok = 0;
+        const int ok = mbar_wait(&sh.sfull[qs], (sidx / FF_SCHED) & 1) ? 1 : 0;
         if (!ok) {
           raise_error(p.err, ERR_TIMEOUT);
           sh.abort_flag = 1;
         }
         sh.ep_ok = ok;
-        sh.ep_tile = tv;
+        sh.ep_tile = sh.sched[qs];
         sh.ep_nv = sh.sched_nv[qs];
       }
       epi_sync<MB>();
       const int4 tv = sh.ep_tile;
-      const int ok = sh.ep_ok;
       const int nv = sh.ep_nv;
-      epi_sync<MB>();  // everyone has read the broadcast before the leader can overwrite it
-      if (!ok || tv.x < 0) break;
-      tc_fence_after();
+      if (!sh.ep_ok || tv.x < 0) break;
       const bool l1 = tv.x == 0;
       const int e = tv.y, mt = tv.z, nc = tv.w;
       const int n0 = nc * BN;
@@ -374,15 +374,24 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       const __nv_bfloat16* bias = l1 ? p.b1 : p.b2;
       const float bv = bias ? __bfloat162float(bias[(size_t)e * M + m]) : 0.f;
       const uint32_t taddr = tmem + (uint32_t)(buf * ACC + hb * BN) + ((uint32_t)(quad * 32) << 16);
-      const bool comb = !l1 && p.combine;
-      if (comb) {  // the tile's tokens and gates, fetched once (two dependent loads per column)
+      if (!l1 && p.combine) {  // the tile's tokens and gates (two dependent loads per column)
         for (int j = threadIdx.x - 64; j < nv; j += 128 * FF_EPW * MB) {
           const int tk = p.tok_of_row[(size_t)e * p.R + n0 + j];
           sh.tok[j] = tk;
           sh.gate[j] = p.gate[tk];
         }
-        epi_sync<MB>();
       }
+      if (leader) {
+        const int ok = mbar_wait(&sh.afull[buf], (lt / NBUF) & 1) ? 1 : 0;
+        if (!ok) {
+          raise_error(p.err, ERR_TIMEOUT);
+          sh.abort_flag = 1;
+        }
+        sh.ep_acc_ok = ok;
+      }
+      epi_sync<MB>();  // the accumulator is complete; the combine's tokens and gates are in place
+      if (!sh.ep_acc_ok) break;
+      tc_fence_after();
       // The two warps of a quadrant take alternate 32-column slices; both TMEM loads of a
       // slice are in flight before one wait.
 #pragma unroll 1
