@@ -166,6 +166,37 @@ SWITCH_API switch_status switch_forward(switch_handle h, const void* x, const fl
                              void* stream);
 
 /*
+ * The whole layer (as switch_forward) with the activations in HOST memory:
+ * x_host [N, d] act is copied to the device, the layer runs, and y [N, d] act
+ * and the aux loss are copied back to y_host and aux_loss_host (may be NULL).
+ * Weights and the route results r are device buffers, as in switch_forward;
+ * residual != 0 adds the layer input x to y.  Page-locked host buffers
+ * (cudaHostAlloc / cudaHostRegister) let the copies run asynchronously;
+ * pageable ones work, but their copies block the calling thread.
+ *
+ * Streams: the copy in runs on a copy stream of the handle and is NOT ordered
+ * after earlier work on `stream` (it only reads x_host, which the caller has
+ * filled); the layer runs on `stream`; the copy out runs on a second copy
+ * stream of the handle.  The handle keeps two staging slots that alternate
+ * between calls, so one call's copies overlap the previous or next call's
+ * layer.  Completion:
+ *   done_event == NULL: `stream` waits for the copy out, so the results are in
+ *     place once `stream` has reached the end of this call;
+ *   done_event != NULL (a cudaEvent_t the caller created): it is recorded after
+ *     the copy out and `stream` does not wait; the results are in place once
+ *     the event has completed.
+ * The first call allocates the staging buffers (4 * N * d act elements) and
+ * creates the copy streams, so it is not for use under stream capture.
+ * Returns SWITCH_ERR_INVALID_ARG for NULL x_host / y_host with N > 0, else as
+ * switch_forward.  The pages' layer is device-resident; moving activations
+ * between host and device has no counterpart there.
+ */
+SWITCH_API switch_status switch_forward_host(switch_handle h, const void* x_host, const float* Wr,
+                                  const float* br, const void* W1, const void* b1, const void* W2,
+                                  const void* b2, const switch_route_out* r, int residual,
+                                  void* y_host, float* aux_loss_host, void* done_event, void* stream);
+
+/*
  * Synchronise `stream`, then copy the aux loss, the [G*E] raw and accepted counts
  * and the number of dropped tokens of the route results `r` to the host
  * (any _host pointer may be NULL).  Returns the device error flag's status

@@ -56,6 +56,9 @@ SIGNATURES = {
     "switch_combine": (c_int, [c_void_p, c_void_p, POINTER(SwitchRouteOut), c_void_p, c_void_p, c_void_p]),
     "switch_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, POINTER(SwitchRouteOut), c_void_p, c_void_p, c_void_p]),
+    "switch_forward_host": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, POINTER(SwitchRouteOut), c_int, c_void_p, c_void_p, c_void_p,
+                                    c_void_p]),
     "switch_get_stats": (c_int, [c_void_p, POINTER(SwitchRouteOut), c_void_p, POINTER(c_float),
                                  POINTER(c_int32), POINTER(c_int32), POINTER(c_int64)]),
     "switch_sync_status": (c_int, [c_void_p, c_void_p]),

@@ -13,6 +13,19 @@
 
 using namespace smoe;
 
+// Resources of switch_forward_host, created by its first call: a copy-in and a copy-out
+// stream, two staging slots (x, y, aux loss) that alternate between calls, and the events
+// that keep a slot from being reused while a copy or the layer still reads it.
+struct HostPath {
+  cudaStream_t cin, cout;
+  cudaEvent_t in_done[2], fwd_done[2], out_done[2];
+  uint8_t* stage;     // x[2], y[2] (act_bytes each, 256-aligned), aux[2] (256 B each)
+  size_t act_bytes, slot_stride;
+  unsigned calls;
+  int n_events;       // events created (for cleanup)
+  bool ok;
+};
+
 struct switch_layer {
   switch_config cfg;
   int N, C, Ceff, R, nT;
@@ -38,6 +51,7 @@ struct switch_layer {
   cudaEvent_t ev[6];
   bool have_events;
   int last_launches;
+  HostPath* hp;
 };
 
 namespace {
@@ -188,8 +202,21 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   return SWITCH_OK;
 }
 
+static void host_path_free(HostPath* p) {
+  if (!p) return;
+  if (p->cin) cudaStreamSynchronize(p->cin);
+  if (p->cout) cudaStreamSynchronize(p->cout);
+  cudaEvent_t* evs[3] = {p->in_done, p->fwd_done, p->out_done};
+  for (int i = 0; i < p->n_events; ++i) cudaEventDestroy(evs[i / 2][i % 2]);
+  if (p->cin) cudaStreamDestroy(p->cin);
+  if (p->cout) cudaStreamDestroy(p->cout);
+  if (p->stage) cudaFree(p->stage);
+  delete p;
+}
+
 switch_status switch_destroy(switch_handle h) {
   if (!h) return SWITCH_ERR_INVALID_ARG;
+  host_path_free(h->hp);
   if (h->have_events)
     for (int i = 0; i < 6; ++i) cudaEventDestroy(h->ev[i]);
   const cudaError_t e = cudaFree(h->ws);
@@ -388,6 +415,74 @@ switch_status switch_forward(switch_handle h, const void* x, const float* Wr, co
     if (st != SWITCH_OK) return st;
   }
   if (prof) cudaEventRecord(h->ev[5], s);
+  return SWITCH_OK;
+}
+
+static switch_status host_path_init(switch_handle h) {
+  if (h->hp) return h->hp->ok ? SWITCH_OK : SWITCH_ERR_CUDA;
+  HostPath* p = new (std::nothrow) HostPath();
+  if (!p) return SWITCH_ERR_OOM;
+  h->hp = p;
+  p->act_bytes = (size_t)h->N * h->cfg.d_model * h->es;
+  p->slot_stride = round_up(p->act_bytes, 256);
+  if (cudaStreamCreateWithFlags(&p->cin, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&p->cout, cudaStreamNonBlocking) != cudaSuccess)
+    return SWITCH_ERR_CUDA;
+  cudaEvent_t* evs[3] = {p->in_done, p->fwd_done, p->out_done};
+  for (int i = 0; i < 6; ++i) {
+    if (cudaEventCreateWithFlags(&evs[i / 2][i % 2], cudaEventDisableTiming) != cudaSuccess) return SWITCH_ERR_CUDA;
+    p->n_events = i + 1;
+  }
+  if (cudaMalloc(&p->stage, 4 * p->slot_stride + 2 * 256) != cudaSuccess) {
+    cudaGetLastError();
+    p->stage = nullptr;
+    return SWITCH_ERR_OOM;
+  }
+  p->ok = true;
+  return SWITCH_OK;
+}
+
+switch_status switch_forward_host(switch_handle h, const void* x_host, const float* Wr, const float* br,
+                                  const void* W1, const void* b1, const void* W2, const void* b2,
+                                  const switch_route_out* r, int residual, void* y_host, float* aux_loss_host,
+                                  void* done_event, void* stream) {
+  if (!h || !r || (h->N > 0 && (!x_host || !y_host))) return SWITCH_ERR_INVALID_ARG;
+  switch_status st = host_path_init(h);
+  if (st != SWITCH_OK) return st;
+  HostPath* p = h->hp;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int k = (int)(p->calls & 1u);
+  uint8_t* xs = p->stage + (size_t)k * p->slot_stride;
+  uint8_t* ys = p->stage + (size_t)(2 + k) * p->slot_stride;
+  float* as = reinterpret_cast<float*>(p->stage + 4 * p->slot_stride + (size_t)k * 256);
+  const bool reuse = p->calls >= 2;  // slot k was used by the call before the previous one
+  // copy in: after the layer of that call has read x from slot k
+  if (reuse && cudaStreamWaitEvent(p->cin, p->fwd_done[k], 0) != cudaSuccess) return SWITCH_ERR_CUDA;
+  if (p->act_bytes && cudaMemcpyAsync(xs, x_host, p->act_bytes, cudaMemcpyHostToDevice, p->cin) != cudaSuccess)
+    return SWITCH_ERR_CUDA;
+  if (cudaEventRecord(p->in_done[k], p->cin) != cudaSuccess) return SWITCH_ERR_CUDA;
+  // the layer: after its input has landed and the copy out of that call has read y
+  if (cudaStreamWaitEvent(s, p->in_done[k], 0) != cudaSuccess) return SWITCH_ERR_CUDA;
+  if (reuse && cudaStreamWaitEvent(s, p->out_done[k], 0) != cudaSuccess) return SWITCH_ERR_CUDA;
+  ++p->calls;
+  st = switch_forward(h, xs, Wr, br, W1, b1, W2, b2, r, residual ? xs : nullptr, ys, stream);
+  if (st != SWITCH_OK) return st;
+  if (cudaMemcpyAsync(as, r->aux_loss, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+      cudaEventRecord(p->fwd_done[k], s) != cudaSuccess)
+    return SWITCH_ERR_CUDA;
+  // copy out
+  if (cudaStreamWaitEvent(p->cout, p->fwd_done[k], 0) != cudaSuccess) return SWITCH_ERR_CUDA;
+  if (p->act_bytes && cudaMemcpyAsync(y_host, ys, p->act_bytes, cudaMemcpyDeviceToHost, p->cout) != cudaSuccess)
+    return SWITCH_ERR_CUDA;
+  if (aux_loss_host &&
+      cudaMemcpyAsync(aux_loss_host, as, sizeof(float), cudaMemcpyDeviceToHost, p->cout) != cudaSuccess)
+    return SWITCH_ERR_CUDA;
+  if (cudaEventRecord(p->out_done[k], p->cout) != cudaSuccess) return SWITCH_ERR_CUDA;
+  if (done_event) {
+    if (cudaEventRecord((cudaEvent_t)done_event, p->cout) != cudaSuccess) return SWITCH_ERR_CUDA;
+  } else if (cudaStreamWaitEvent(s, p->out_done[k], 0) != cudaSuccess) {
+    return SWITCH_ERR_CUDA;
+  }
   return SWITCH_OK;
 }
 

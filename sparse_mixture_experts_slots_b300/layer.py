@@ -146,6 +146,29 @@ class SwitchMoE:
               "switch_forward")
         return y, r
 
+    def forward_host(self, x_host, Wr, br, W1, b1, W2, b2, y_host, aux_host=None, residual: bool = False,
+                     r: Optional[RouteResult] = None, done=None, stream=None) -> RouteResult:
+        """The whole layer on host activations: x_host, y_host [N, d] CPU tensors (page-locked
+        for asynchronous copies), aux_host a float32 CPU tensor of one element or None.
+        done: a torch.cuda.Event recorded after the copy out (the stream then does not wait
+        for it); without one the stream waits for the copy out.  Returns the route results."""
+        r = r or self.alloc_route()
+        if x_host.device.type != "cpu" or y_host.device.type != "cpu":
+            raise ValueError("forward_host takes CPU tensors for x_host and y_host")
+        if aux_host is not None and (aux_host.device.type != "cpu" or aux_host.dtype != torch.float32):
+            raise ValueError("aux_host must be a float32 CPU tensor")
+        ev = None
+        if done is not None:
+            if not done.cuda_event:  # torch creates its events on first record
+                done.record(torch.cuda.current_stream(self.device))
+            ev = ctypes.c_void_p(done.cuda_event)
+        cs = r.c_struct()
+        check(self.lib.switch_forward_host(self._h, _ptr(x_host), _ptr(Wr), _ptr(br), _ptr(W1), _ptr(b1), _ptr(W2),
+                                           _ptr(b2), ctypes.byref(cs), 1 if residual else 0, _ptr(y_host),
+                                           _ptr(aux_host), ev, _stream(stream)),
+              "switch_forward_host")
+        return r
+
     # ------------------------------------------------------------------ host-side reads
     def get_stats(self, r: RouteResult, stream=None) -> dict:
         GE = self.G * self.E
