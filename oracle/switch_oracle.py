@@ -29,6 +29,9 @@ Readings taken where the pages leave a step open (each is listed in the design doc):
     sequence order: row = (kept tokens of that expert in earlier groups) + slot.
   * y excludes the residual; a dropped token's expert output is exactly 0
     [042, §一; 070, 核心思想与公式 (the m_t mask)].
+  * the router z-loss is reported unweighted, per group over that group's T
+    tokens, and its mean over groups, like the balance term [070, 核心思想与公式
+    (ST-MoE's z-loss) and 最小实验 (both reported without their weights)].
 
 Every function here is pinned by tests/test_oracle_pins.py against values the
 pages print, closed forms, a dense one-hot einsum formulation [card, 方法适配]
@@ -125,6 +128,21 @@ def load_balance(a: np.ndarray, p: np.ndarray, E: int, alpha: float):
     return f, P, unweighted, alpha * unweighted
 
 
+def z_loss(z: np.ndarray) -> float:
+    """Router z-loss of one routing group: L_z = (1/T) sum_t (log sum_i exp z_ti)^2.
+
+    [070, 核心思想与公式]: ST-MoE's router z-loss on the score matrix Z (the logits
+    before the softmax); it penalises the log normaliser of each token's scores.
+    The log-sum-exp is evaluated as m + log sum_i exp(z_ti - m), m = max_i z_ti,
+    which is the same number without overflow.
+    """
+    if z.shape[0] == 0:
+        return 0.0
+    m = z.max(axis=-1)
+    lse = m + np.log(np.exp(z - m[:, None]).sum(axis=-1))
+    return float(np.mean(lse * lse))
+
+
 @dataclasses.dataclass
 class Route:
     C: int
@@ -143,6 +161,8 @@ class Route:
     aux_per_group: np.ndarray  # [G] alpha * balance
     aux_loss: float          # mean over groups
     expert_rows: np.ndarray  # [E] kept tokens per expert, all groups
+    z_per_group: np.ndarray = None  # [G] router z-loss of each group (unweighted)
+    z_loss: float = 0.0             # mean over groups
 
     @property
     def overflow(self) -> int:
@@ -180,11 +200,13 @@ def route(x, Wr, br, G: int, T: int, E: int, capacity_factor: float, alpha: floa
     P = np.zeros((G, E))
     balance = np.zeros(G)
     aux = np.zeros(G)
+    zg = np.zeros(G)
     for g in range(G):
         sl = slice(g * T, (g + 1) * T)
         slot[sl], keep[sl], raw[g], accepted[g] = assign_slots(a[sl], E, C)
         if T > 0:
             f[g], P[g], balance[g], aux[g] = load_balance(a[sl], p[sl], E, alpha)
+            zg[g] = z_loss(z[sl])
 
     # Row of each kept token in its expert's block: kept tokens of the same
     # expert in earlier groups come first, then this group's slot.
@@ -197,7 +219,8 @@ def route(x, Wr, br, G: int, T: int, E: int, capacity_factor: float, alpha: floa
         before += accepted[g]
     return Route(C=C, logits=z, probs=p, expert=a, gate=gate, slot=slot, keep=keep, row=row,
                  raw=raw, accepted=accepted, f=f, P=P, balance=balance, aux_per_group=aux,
-                 aux_loss=float(aux.mean()) if G > 0 else 0.0, expert_rows=accepted.sum(axis=0))
+                 aux_loss=float(aux.mean()) if G > 0 else 0.0, expert_rows=accepted.sum(axis=0),
+                 z_per_group=zg, z_loss=float(zg.mean()) if G > 0 else 0.0)
 
 
 def dispatch(x, r: Route, E: int, G: int) -> np.ndarray:

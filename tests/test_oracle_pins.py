@@ -364,3 +364,55 @@ def test_logits_override_reroutes_group():
     assert (r.expert[T:] == 2).all()
     r0 = so.route(x, Wr, None, G, T, E, 1.0)
     np.testing.assert_array_equal(r.expert[:T], r0.expert[:T])
+
+
+# ----------------------------------------------------------------------------- router z-loss
+
+def test_z_loss_equal_scores_closed_form():
+    # every score of a token equal to s_t: log sum_i e^{s_t} = s_t + ln E exactly
+    for E in (1, 2, 7, 128, 2048):
+        T = 5
+        x = np.array([[0.0], [1.5], [-2.0], [0.25], [3.0]])
+        Wr = np.ones((E, 1))
+        r = so.route(x, Wr, None, 1, T, E, 1.0)
+        want = float(np.mean((x[:, 0] + math.log(E)) ** 2))
+        assert abs(r.z_loss - want) <= 1e-12 * max(1.0, want)
+        # all-zero scores: (ln E)^2
+        r0 = so.route(np.zeros((T, 1)), Wr, None, 1, T, E, 1.0)
+        assert abs(r0.z_loss - math.log(E) ** 2) <= 1e-12 * max(1.0, math.log(E) ** 2)
+
+
+def test_z_loss_dominant_score():
+    # one score L far above the rest (zeros): log sum = L + log(1 + (E-1) e^-L) -> L^2 to 1e-12
+    E, L = 64, 60.0
+    br = np.zeros(E)
+    br[5] = L
+    r = so.route(np.zeros((3, 1)), np.zeros((E, 1)), br, 1, 3, E, 1.0)
+    assert abs(r.z_loss - L * L) <= 1e-12 * L * L
+
+
+def test_z_loss_changes_under_shift_but_routing_does_not(golden):
+    g = golden("z_loss_shift.json")
+    c = g["shift"]
+    rng = np.random.default_rng(5)
+    T, E, d = 40, 8, 6
+    x = rng.standard_normal((T, d))
+    Wr = rng.standard_normal((E, d)) * 0.3
+    br = rng.standard_normal(E) * 0.1
+    r0, r1, r2 = (so.route(x, Wr, br + k * c, 1, T, E, 1.0) for k in (0, 1, 2))
+    assert (r1.expert == r0.expert).all() and (r1.slot == r0.slot).all()
+    assert abs(r1.z_loss - r0.z_loss) > 1.0
+    # (log sum exp(z + c))^2 = (lse + c)^2: quadratic in c with unit leading coefficient,
+    # so the second difference over steps of c is exactly 2 c^2
+    second = r2.z_loss - 2.0 * r1.z_loss + r0.z_loss
+    assert abs(second - 2.0 * c * c) <= 1e-9 * c * c
+
+
+def test_z_loss_is_per_group_then_mean():
+    # two groups, every score of a token equal to x_t: group g's loss is mean_t (x_t + ln E)^2
+    E, T = 4, 3
+    x = np.array([[0.0], [0.0], [0.0], [2.0], [2.0], [2.0]])
+    r = so.route(x, np.ones((E, 1)), None, 2, T, E, 1.0)
+    lnE = math.log(E)
+    np.testing.assert_allclose(r.z_per_group, [lnE ** 2, (2.0 + lnE) ** 2], rtol=1e-13)
+    assert abs(r.z_loss - 0.5 * (lnE ** 2 + (2.0 + lnE) ** 2)) <= 1e-13 * r.z_loss
