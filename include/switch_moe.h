@@ -101,6 +101,11 @@ typedef struct {
   int32_t* expert_rows;     /* [E]   sum over groups of accepted_count (rows of xe used) */
   float* probs;             /* [N*E] or NULL; written when SWITCH_FLAG_WRITE_PROBS      */
   float* logits;            /* [N*E] or NULL; written when SWITCH_FLAG_WRITE_LOGITS     */
+  /* Router z-loss (ST-MoE, as restated on the 070 page, section 核心思想与公式):
+   * L_z = (1/T) sum_t (log sum_e exp z_te)^2 over a group's T tokens, unweighted.
+   * Either pointer may be NULL (not written). */
+  float* z_loss_per_group;  /* [G]   L_z of each routing group                            */
+  float* z_loss;            /* [1]   mean over groups                                     */
 } switch_route_out;
 
 /* Capacity C for cfg (host only, no GPU needed); -1 when cfg is invalid. */
@@ -237,7 +242,7 @@ SWITCH_API int switch_last_launch_count(switch_handle h);
  *     whose kernels overlap on the GPU (different streams, or concurrent graphs) race and
  *     give wrong results.  Serialise them.
  *   - A configuration whose scratch needs more than 32 MiB returns SWITCH_ERR_UNSUPPORTED.
- *     The scratch is about 12 G ceil(T/128) E + 6 E d + 4 E G C bytes with bfloat16
+ *     The scratch is about (12 E + 4) G ceil(T/128) + 6 E d + 4 E G C bytes with bfloat16
  *     activations (all five named workloads fit; 65536 tokens x 2048 experts needs 22 MiB),
  *     plus 4 G T E bytes of logits with float32 activations.  Invalid arguments return
  *     SWITCH_ERR_INVALID_ARG.

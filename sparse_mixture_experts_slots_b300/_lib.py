@@ -35,7 +35,7 @@ class SwitchConfig(ctypes.Structure):
 
 
 ROUTE_FIELDS = ["expert", "slot", "keep", "gate", "row", "raw_count", "accepted_count", "P", "balance",
-                "aux_loss_per_group", "aux_loss", "expert_rows", "probs", "logits"]
+                "aux_loss_per_group", "aux_loss", "expert_rows", "probs", "logits", "z_loss_per_group", "z_loss"]
 
 
 class SwitchRouteOut(ctypes.Structure):

@@ -37,6 +37,7 @@ struct switch_layer {
   float* logits;
   int32_t* tile_hist;
   float* tile_P;
+  float* tile_Z;
   int32_t* tile_base;
   int32_t* group_off;
   int32_t* tok_of_row;
@@ -163,6 +164,7 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_fcnt = take(ffn_words * sizeof(uint32_t));
   const size_t o_hist = take(G * nT * E * sizeof(int32_t));
   const size_t o_tP = take(G * nT * E * sizeof(float));
+  const size_t o_tZ = take(G * nT * sizeof(float));
   const size_t o_base = take(G * nT * E * sizeof(int32_t));
   const size_t o_goff = take(G * E * sizeof(int32_t));
   const size_t o_tor = take(E * R * sizeof(int32_t));
@@ -179,6 +181,7 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->logits = reinterpret_cast<float*>(h->ws + o_logits);
   h->tile_hist = reinterpret_cast<int32_t*>(h->ws + o_hist);
   h->tile_P = reinterpret_cast<float*>(h->ws + o_tP);
+  h->tile_Z = reinterpret_cast<float*>(h->ws + o_tZ);
   h->tile_base = reinterpret_cast<int32_t*>(h->ws + o_base);
   h->group_off = reinterpret_cast<int32_t*>(h->ws + o_goff);
   h->tok_of_row = reinterpret_cast<int32_t*>(h->ws + o_tor);
@@ -250,6 +253,7 @@ static switch_status route_args(switch_handle h, const void* x, const float* Wr,
   a->wsplit = h->wsplit;
   a->tile_hist = h->tile_hist;
   a->tile_P = h->tile_P;
+  a->tile_Z = h->tile_Z;
   a->tile_base = h->tile_base;
   a->group_off = h->group_off;
   a->tok_of_row = h->tok_of_row;
@@ -269,6 +273,8 @@ static switch_status route_args(switch_handle h, const void* x, const float* Wr,
   a->aux = out->aux_loss;
   a->expert_rows = out->expert_rows;
   a->probs = want_probs ? out->probs : nullptr;
+  a->z_g = out->z_loss_per_group;
+  a->z = out->z_loss;
   return SWITCH_OK;
 }
 
@@ -604,6 +610,7 @@ extern "C" switch_status switch_route_static(const switch_config* cfg, const voi
   const size_t o_wsplit = take(bf16 ? router_tc_wsplit_bytes(cfg->E, cfg->d_model) : 0);
   const size_t o_hist = take(G * nT * E * sizeof(int32_t));
   const size_t o_tP = take(G * nT * E * sizeof(float));
+  const size_t o_tZ = take(G * nT * sizeof(float));
   const size_t o_base = take(G * nT * E * sizeof(int32_t));
   const size_t o_goff = take(G * E * sizeof(int32_t));
   const size_t o_tor = take(E * (size_t)R * sizeof(int32_t));
@@ -639,6 +646,7 @@ extern "C" switch_status switch_route_static(const switch_config* cfg, const voi
   a.wsplit = ws + o_wsplit;
   a.tile_hist = reinterpret_cast<int32_t*>(ws + o_hist);
   a.tile_P = reinterpret_cast<float*>(ws + o_tP);
+  a.tile_Z = reinterpret_cast<float*>(ws + o_tZ);
   a.tile_base = reinterpret_cast<int32_t*>(ws + o_base);
   a.group_off = reinterpret_cast<int32_t*>(ws + o_goff);
   a.tok_of_row = reinterpret_cast<int32_t*>(ws + o_tor);
@@ -658,5 +666,7 @@ extern "C" switch_status switch_route_static(const switch_config* cfg, const voi
   a.aux = out->aux_loss;
   a.expert_rows = out->expert_rows;
   a.probs = want_probs ? out->probs : nullptr;
+  a.z_g = out->z_loss_per_group;
+  a.z = out->z_loss;
   return launch_route(a, s) < 0 ? SWITCH_ERR_CUDA : SWITCH_OK;
 }

@@ -50,6 +50,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // Max of (value, -index) pairs: larger value wins, equal values go to the lower index.
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 #pragma unroll

@@ -56,6 +56,7 @@ struct RouteArgs {
   void* wsplit;        // [3, E, d] bf16: W_r split into hi, mid, lo (tensor-core router)
   int32_t* tile_hist;  // [G, nT, E]
   float* tile_P;       // [G, nT, E]
+  float* tile_Z;       // [G, nT]: sum over the tile's tokens of (log sum_e exp z)^2
   int32_t* tile_base;  // [G, nT, E]
   int32_t* group_off;  // [G, E]
   int32_t* tok_of_row; // [E * R]
@@ -67,10 +68,12 @@ struct RouteArgs {
   int32_t* raw; int32_t* accepted; float* P; float* balance; float* aux_g; float* aux;
   int32_t* expert_rows;
   float* probs;        // or null
+  float* z_g;          // [G] router z-loss per group, or null
+  float* z;            // [1] its mean over groups, or null
 };
 
 // Blocks of the cross-tile scan (one per 32 experts); scan_partial holds G * this many floats.
-inline int route_scan_blocks(int E) { return (E + 31) / 32; }
+__host__ __device__ inline int route_scan_blocks(int E) { return (E + 31) / 32; }
 
 // Router (tensor cores for bf16 x, CUDA cores for float32 x), softmax/top-1, per-tile
 // statistics, cross-tile scan + finalize, slots (when a.slots).

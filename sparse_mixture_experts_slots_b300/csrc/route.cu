@@ -79,11 +79,11 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const T* __restrict_
 __global__ void __launch_bounds__(256) route_softmax_kernel(
     const float* __restrict__ z, int T, int E, int nT, int32_t* __restrict__ expert, float* __restrict__ gate,
     int32_t* __restrict__ rank, int32_t* __restrict__ tile_hist, float* __restrict__ tile_P,
-    float* __restrict__ probs, uint32_t* err) {
+    float* __restrict__ tile_Z, float* __restrict__ probs, uint32_t* err) {
   griddep_wait();
   griddep_launch_dependents();
   extern __shared__ int32_t hist[];
-  __shared__ float m_s[ROUTE_TILE], s_s[ROUTE_TILE];
+  __shared__ float m_s[ROUTE_TILE], s_s[ROUTE_TILE], zz_s[ROUTE_TILE];
   __shared__ int a_s[ROUTE_TILE];
   const int g = blockIdx.y, tile = blockIdx.x;
   const int t0 = tile * ROUTE_TILE;
@@ -113,12 +113,22 @@ __global__ void __launch_bounds__(256) route_softmax_kernel(
       m_s[i] = best;
       s_s[i] = s;
       a_s[i] = bi;
+      const float lse = best + logf(s);  // log sum_e exp z_e, for the router z-loss
+      zz_s[i] = lse * lse;
       expert[tok0 + i] = bi;
       gate[tok0 + i] = 1.0f / s;   // exp(z_top - max) / s with z_top = max
       atomicAdd(&hist[bi], 1);
     }
   }
   __syncthreads();
+
+  // the tile's sum of (log sum exp z)^2, in a fixed order
+  if (warp == 0) {
+    float zs = 0.f;
+    for (int i = lane; i < len; i += 32) zs += zz_s[i];
+    zs = warp_sum(zs);
+    if (lane == 0) tile_Z[(size_t)g * nT + tile] = zs;
+  }
 
   // rank among the tile's earlier tokens with the same expert
   for (int i = threadIdx.x; i < len; i += blockDim.x) {
@@ -142,21 +152,45 @@ __global__ void __launch_bounds__(256) route_softmax_kernel(
 }
 
 // ---------------------------------------------------------------- 3. cross-tile scan + finalize
-// One block per 32 experts (lane <-> expert); the warps split each group's tiles.
+// One block per 32 experts (lane <-> expert); the warps split each group's tiles.  When the
+// router z-loss is asked for, one more block reduces the tiles' sums of (log sum exp z)^2
+// per group, alongside the scan (nothing later in the layer waits for it).
 constexpr int SCAN_WARPS = 16;
 
 __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
-    const int32_t* __restrict__ tile_hist, const float* __restrict__ tile_P, int G, int T, int E, int nT, int C,
-    float alpha, int32_t* __restrict__ tile_base, int32_t* __restrict__ raw, int32_t* __restrict__ accepted,
-    float* __restrict__ P, int32_t* __restrict__ group_off, int32_t* __restrict__ expert_rows,
-    float* __restrict__ balance, float* __restrict__ aux_g, float* __restrict__ aux, float* __restrict__ partial,
+    const int32_t* __restrict__ tile_hist, const float* __restrict__ tile_P, const float* __restrict__ tile_Z,
+    int G, int T, int E, int nT, int C, float alpha, int32_t* __restrict__ tile_base, int32_t* __restrict__ raw,
+    int32_t* __restrict__ accepted, float* __restrict__ P, int32_t* __restrict__ group_off,
+    int32_t* __restrict__ expert_rows, float* __restrict__ balance, float* __restrict__ aux_g,
+    float* __restrict__ aux, float* __restrict__ z_g, float* __restrict__ z, float* __restrict__ partial,
     uint32_t* __restrict__ counter) {
   griddep_wait();
   griddep_launch_dependents();
   __shared__ int sh_h[SCAN_WARPS][32];
   __shared__ float sh_p[SCAN_WARPS][32];
+  __shared__ double sh_z[SCAN_WARPS];
   __shared__ int is_last;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nblk = route_scan_blocks(E);
+  if ((int)blockIdx.x >= nblk) {  // router z-loss: a warp per group, then the mean over groups
+    double wsum = 0.0;
+    for (int g = warp; g < G; g += SCAN_WARPS) {
+      double zs = 0.0;
+      for (int j = lane; j < nT; j += 32) zs += (double)tile_Z[(size_t)g * nT + j];
+      zs = warp_sum_d(zs);
+      const float zg = T > 0 ? (float)(zs / (double)T) : 0.f;
+      if (lane == 0 && z_g) z_g[g] = zg;
+      wsum += (double)zg;
+    }
+    if (lane == 0) sh_z[warp] = wsum;
+    __syncthreads();
+    if (threadIdx.x == 0 && z) {
+      double zt = 0.0;
+      for (int w = 0; w < SCAN_WARPS; ++w) zt += sh_z[w];
+      z[0] = G > 0 ? (float)(zt / (double)G) : 0.f;
+    }
+    return;
+  }
   const int e = blockIdx.x * 32 + lane;
   const bool ev = e < E;
   const int chunk = (nT + SCAN_WARPS - 1) / SCAN_WARPS;
@@ -202,7 +236,7 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
         contrib = (float)tot * Pv;
       }
       contrib = warp_sum(contrib);
-      if (lane == 0) partial[(size_t)g * gridDim.x + blockIdx.x] = contrib;
+      if (lane == 0) partial[(size_t)g * nblk + blockIdx.x] = contrib;
     }
     __syncthreads();
   }
@@ -211,13 +245,13 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
   // The last block to finish sums the per-block partials (fixed order) per group.
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == (unsigned)nblk - 1;
   __syncthreads();
   if (!is_last) return;
   __threadfence();
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     float sum = 0.f;
-    for (int b = 0; b < (int)gridDim.x; ++b) sum += __ldcg(&partial[(size_t)g * gridDim.x + b]);
+    for (int b = 0; b < nblk; ++b) sum += __ldcg(&partial[(size_t)g * nblk + b]);
     // E * sum_e f_e P_e with f_e = raw_e / T
     const float bal = T > 0 ? (float)E * (sum / (float)T) : 0.f;
     balance[g] = bal;
@@ -284,16 +318,18 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
       if (launch_k(router_logits_kernel<float>, grid, dim3(256), 0, s, false, 1, (const float*)a.x, a.Wr, a.br,
                    a.logits, (int)N, a.d, a.E) != cudaSuccess ||
           launch_k(route_softmax_kernel, dim3(nT, a.G), dim3(256), a.E * sizeof(int32_t), s, true, 1, a.logits, a.T,
-                   a.E, nT, a.expert, a.gate, a.slot, a.tile_hist, a.tile_P, a.probs, a.err) != cudaSuccess)
+                   a.E, nT, a.expert, a.gate, a.slot, a.tile_hist, a.tile_P, a.tile_Z, a.probs, a.err) != cudaSuccess)
         return -1;
       launches += 2;
     }
   }
   // The scan follows the router kernel of this call (programmatic launch); with no
   // tokens it is the first kernel of the call.
-  if (launch_k(route_scan_kernel, dim3(route_scan_blocks(a.E)), dim3(SCAN_WARPS * 32), 0, s, N > 0, 1, a.tile_hist,
-               a.tile_P, a.G, a.T, a.E, nT, a.C, a.alpha, a.tile_base, a.raw, a.accepted, a.P, a.group_off,
-               a.expert_rows, a.balance, a.aux_g, a.aux, a.scan_partial, a.scan_counter) != cudaSuccess)
+  const int scan_grid = route_scan_blocks(a.E) + ((a.z_g || a.z) ? 1 : 0);
+  if (launch_k(route_scan_kernel, dim3(scan_grid), dim3(SCAN_WARPS * 32), 0, s, N > 0, 1, a.tile_hist,
+               a.tile_P, (const float*)a.tile_Z, a.G, a.T, a.E, nT, a.C, a.alpha, a.tile_base, a.raw, a.accepted,
+               a.P, a.group_off, a.expert_rows, a.balance, a.aux_g, a.aux, a.z_g, a.z, a.scan_partial,
+               a.scan_counter) != cudaSuccess)
     return -1;
   ++launches;
   if (N > 0 && a.slots) {

@@ -122,6 +122,7 @@ struct RtScratch {
   float Mall[RT_BM];      // all experts: max logit per token
   float Sall[RT_BM];      // all experts: sum of exp(z - Mall)
   int texp[RT_BM];        // final expert per token (-1 past the group's end)
+  float zz[RT_BM];        // (log sum_e exp z)^2 per token (0 past the group's end)
   float colsum[4][EC];    // per lane quadrant: probability sums of the columns
   int hist[EC];
   float bias[EC];
@@ -177,8 +178,8 @@ __global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const float* __restrict__ br, int T, int E, int d, int nT, int Q, int use3d,
                      int32_t* __restrict__ expert, float* __restrict__ gate, int32_t* __restrict__ rank,
-                     int32_t* __restrict__ tile_hist, float* __restrict__ tile_P, float* __restrict__ logits,
-                     float* __restrict__ probs, uint32_t* err) {
+                     int32_t* __restrict__ tile_hist, float* __restrict__ tile_P, float* __restrict__ tile_Z,
+                     float* __restrict__ logits, float* __restrict__ probs, uint32_t* err) {
   using Cf = RtCfg<EC, DEEP>;
   using Gm = RtGeom<EC>;
   extern __shared__ uint8_t smem_raw[];
@@ -404,6 +405,8 @@ __global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
     sh.Mall[i] = M;
     sh.Sall[i] = S;
     sh.texp[i] = valid ? A : -1;
+    const float lse = M + logf(S);  // log sum_e exp z_e over all E experts (router z-loss)
+    sh.zz[i] = (run && valid) ? lse * lse : 0.f;
   }
   __syncthreads();
 
@@ -428,6 +431,11 @@ __global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
   __syncthreads();
 
   const size_t tbase = ((size_t)g * nT + tile) * E;
+  if (q == 0 && warp == 0) {  // the tile's sum of (log sum exp z)^2, fixed order
+    float zs = (sh.zz[lane] + sh.zz[lane + 32]) + (sh.zz[lane + 64] + sh.zz[lane + 96]);
+    zs = warp_sum(zs);
+    if (lane == 0) tile_Z[(size_t)g * nT + tile] = zs;
+  }
   for (int c = threadIdx.x; c < EC; c += blockDim.x) {
     const int e = e0 + c;
     if (e < E) {
@@ -463,7 +471,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const Route
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
   const cudaError_t e = launch_k(kern, dim3((unsigned)(Q * nT), (unsigned)a.G, 1), dim3(RT_THREADS, 1, 1), smem, s,
                                  /*pdl=*/true, (unsigned)Q, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, use3d, a.expert,
-                                 a.gate, rank, a.tile_hist, a.tile_P, a.logits_out, a.probs, a.err);
+                                 a.gate, rank, a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs, a.err);
   return e == cudaSuccess ? 1 : -1;
 }
 

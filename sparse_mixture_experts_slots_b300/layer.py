@@ -42,6 +42,8 @@ class RouteResult:
     expert_rows: torch.Tensor     # [E] int32
     probs: Optional[torch.Tensor] = None   # [N, E] float32
     logits: Optional[torch.Tensor] = None  # [N, E] float32
+    z_loss_per_group: Optional[torch.Tensor] = None  # [G] float32, router z-loss (unweighted)
+    z_loss: Optional[torch.Tensor] = None            # [1] float32, mean over groups
 
     def c_struct(self) -> SwitchRouteOut:
         return SwitchRouteOut(*[_ptr(getattr(self, n)) for n in _lib.ROUTE_FIELDS])
@@ -100,7 +102,8 @@ class SwitchMoE:
             aux_loss_per_group=torch.empty(G, dtype=f32, device=dev), aux_loss=torch.empty(1, dtype=f32, device=dev),
             expert_rows=torch.empty(E, dtype=i32, device=dev),
             probs=torch.empty(N, E, dtype=f32, device=dev) if self.write_probs else None,
-            logits=torch.empty(N, E, dtype=f32, device=dev) if self.write_logits else None)
+            logits=torch.empty(N, E, dtype=f32, device=dev) if self.write_logits else None,
+            z_loss_per_group=torch.empty(G, dtype=f32, device=dev), z_loss=torch.empty(1, dtype=f32, device=dev))
 
     def alloc_expert_buffer(self, width: Optional[int] = None) -> torch.Tensor:
         return torch.empty(self.E, self.block_rows, width or self.d_model, dtype=self.dtype, device=self.device)

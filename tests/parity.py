@@ -2,7 +2,7 @@
 
 Comparison rules:
   * expert, slot, keep, row, raw/accepted counts, expert rows: bit-exact;
-  * gate, probabilities, P, balance and aux loss: |a - b| <= 1e-5 * |b|;
+  * gate, probabilities, P, balance, aux loss and router z-loss: |a - b| <= 1e-5 * |b|;
   * dispatched rows: bit-exact copies of x; rows past an expert's count are zero;
   * y: |y - y_ref| <= 1e-2 + 1e-2 |y_ref| elementwise, plus per kept token
     ||y_t - y_ref,t|| <= 1e-2 ||y_ref,t|| (the elementwise bound alone would pass an
@@ -78,10 +78,15 @@ def compare_route(g, ref: so.Route, shape):
         rel_close(to_np(g.balance), ref.balance, what="balance")
         rel_close(to_np(g.aux_loss_per_group), ref.aux_per_group, what="aux per group")
         rel_close(to_np(g.aux_loss)[0], ref.aux_loss, what="aux loss")
+        if g.z_loss is not None:
+            rel_close(to_np(g.z_loss_per_group), ref.z_per_group, what="z-loss per group")
+            rel_close(to_np(g.z_loss)[0], ref.z_loss, what="z-loss")
         if g.probs is not None:
             rel_close(to_np(g.probs), ref.probs, what="probs")
     else:
         assert (to_np(g.P) == 0).all() and (to_np(g.aux_loss) == 0).all()
+        if g.z_loss is not None:
+            assert (to_np(g.z_loss) == 0).all()
 
 
 def check_dispatch(xe: torch.Tensor, x: torch.Tensor, ref: so.Route):

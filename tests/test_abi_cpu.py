@@ -51,7 +51,13 @@ def test_struct_layout():
     from sparse_mixture_experts_slots_b300._lib import SwitchConfig, SwitchRouteOut
     assert ctypes.sizeof(SwitchConfig) == 48
     assert SwitchConfig.capacity_factor.offset == 24
-    assert ctypes.sizeof(SwitchRouteOut) == 14 * 8
+    # the binding's fields are the header struct's pointer fields, in the same order
+    text = open(HEADER, encoding="utf-8").read()
+    body = re.search(r"typedef struct \{((?:(?!typedef).)*?)\} switch_route_out;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    header_fields = re.findall(r"\*\s*(\w+)\s*;", body)
+    assert [n for n, _ in SwitchRouteOut._fields_] == header_fields
+    assert ctypes.sizeof(SwitchRouteOut) == len(header_fields) * 8
 
 
 def test_capacity_matches_oracle_rule(lib):
