@@ -32,6 +32,11 @@ Readings taken where the pages leave a step open (each is listed in the design doc):
   * the router z-loss is reported unweighted, per group over that group's T
     tokens, and its mean over groups, like the balance term [070, 核心思想与公式
     (ST-MoE's z-loss) and 最小实验 (both reported without their weights)].
+  * top-2 (route_top2): the two highest scores (ties to the lower index), gates =
+    softmax over those two scores [moe, 路由器只开两条线]; capacity ceil(2cT/E),
+    twice top-1's [card, 方法适配: top-1 about halves the capacity need]; second
+    choices take slots after the expert's kept first choices, in sequence order;
+    f counts first choices; a dropped choice's weight is not moved to the other.
 
 Every function here is pinned by tests/test_oracle_pins.py against values the
 pages print, closed forms, a dense one-hot einsum formulation [card, 方法适配]
@@ -320,4 +325,149 @@ def groups_with_near_ties(z_list: List[np.ndarray], G: int, T: int, eps: float =
         sl = slice(g * T, (g + 1) * T)
         if any(ties_within(np.asarray(z, dtype=np.float64)[sl], eps).any() for z in z_list):
             out.append(g)
+    return out
+
+
+# ----------------------------------------------------------------------------- top-2 variant
+
+@dataclasses.dataclass
+class Route2:
+    C: int
+    logits: np.ndarray      # [N, E]
+    probs: np.ndarray       # [N, E] full softmax (for P)
+    expert: np.ndarray      # [N] first choice
+    expert2: np.ndarray     # [N] second choice
+    gate: np.ndarray        # [N] weight of the first choice (softmax over the two scores)
+    gate2: np.ndarray       # [N] weight of the second choice; gate + gate2 = 1
+    slot: np.ndarray        # [N]
+    slot2: np.ndarray       # [N] counted after the expert's kept first choices
+    keep: np.ndarray        # [N] bool
+    keep2: np.ndarray       # [N] bool
+    row: np.ndarray         # [N] row in the expert block, -1 if dropped
+    row2: np.ndarray        # [N]
+    raw: np.ndarray         # [G, E] first choices
+    raw2: np.ndarray        # [G, E] second choices
+    accepted: np.ndarray    # [G, E] kept first choices
+    accepted2: np.ndarray   # [G, E] kept second choices
+    f: np.ndarray           # [G, E] first-choice fractions
+    P: np.ndarray           # [G, E]
+    balance: np.ndarray     # [G]
+    aux_per_group: np.ndarray
+    aux_loss: float
+    z_per_group: np.ndarray
+    z_loss: float
+    expert_rows: np.ndarray  # [E] kept first + second choices, all groups
+
+
+def top2(z: np.ndarray):
+    """First and second choice: the highest score, then the highest of the others; ties go
+    to the lower expert index [moe, 路由器只开两条线 (keep the k highest scores)]."""
+    a1 = np.argmax(z, axis=-1).astype(np.int64)
+    zz = z.copy()
+    zz[np.arange(z.shape[0]), a1] = -np.inf
+    a2 = np.argmax(zz, axis=-1).astype(np.int64)
+    return a1, a2
+
+
+def route_top2(x, Wr, br, G: int, T: int, E: int, capacity_factor: float, alpha: float = 1e-2,
+               capacity_override: int = 0, logits_override: Optional[dict] = None) -> Route2:
+    """Top-2 routing per group: choices, gates, slots, capacity mask and statistics.
+
+    Gates: softmax over the two kept scores, so they add to 1 [moe, 路由器只开两条线].
+    Capacity: ceil(2 c T / E), twice the top-1 capacity [card, 方法适配].  Slots: the
+    first choices of the group in sequence order, then its second choices in sequence
+    order, each expert's second choices numbered after its kept first choices.
+    """
+    assert E >= 2
+    x = np.asarray(x)
+    N = G * T
+    C = capacity(2.0 * capacity_factor, T, E, capacity_override)
+    z = router_logits(x, Wr, br)
+    if logits_override:
+        z = z.copy()
+        for g, zg in logits_override.items():
+            z[g * T:(g + 1) * T] = np.asarray(zg, dtype=np.float64)
+    p = softmax(z) if N > 0 else np.zeros((0, E))
+    a1, a2 = top2(z) if N > 0 else (np.zeros(0, np.int64), np.zeros(0, np.int64))
+    z1 = z[np.arange(N), a1] if N > 0 else np.zeros(0)
+    z2 = z[np.arange(N), a2] if N > 0 else np.zeros(0)
+    gate = 1.0 / (1.0 + np.exp(z2 - z1))       # exp(z1) / (exp(z1) + exp(z2))
+    gate2 = 1.0 / (1.0 + np.exp(z1 - z2))
+
+    slot = np.empty(N, dtype=np.int64)
+    slot2 = np.empty(N, dtype=np.int64)
+    keep = np.empty(N, dtype=bool)
+    keep2 = np.empty(N, dtype=bool)
+    raw = np.zeros((G, E), dtype=np.int64)
+    raw2 = np.zeros((G, E), dtype=np.int64)
+    accepted = np.zeros((G, E), dtype=np.int64)
+    accepted2 = np.zeros((G, E), dtype=np.int64)
+    f = np.zeros((G, E))
+    P = np.zeros((G, E))
+    balance = np.zeros(G)
+    aux = np.zeros(G)
+    zg = np.zeros(G)
+    for g in range(G):
+        sl = slice(g * T, (g + 1) * T)
+        slot[sl], keep[sl], raw[g], accepted[g] = assign_slots(a1[sl], E, C)
+        # second choices: numbered per expert in sequence order, after the kept first choices
+        s2, _, raw2[g], _ = assign_slots(a2[sl], E, C)
+        slot2[sl] = s2 + accepted[g][a2[sl]]
+        keep2[sl] = slot2[sl] < C
+        accepted2[g] = np.minimum(raw2[g], np.maximum(C - accepted[g], 0))
+        if T > 0:
+            f[g], P[g], balance[g], aux[g] = load_balance(a1[sl], p[sl], E, alpha)
+            zg[g] = z_loss(z[sl])
+
+    row = np.full(N, -1, dtype=np.int64)
+    row2 = np.full(N, -1, dtype=np.int64)
+    before = np.zeros(E, dtype=np.int64)
+    for g in range(G):
+        for t in range(g * T, (g + 1) * T):
+            if keep[t]:
+                row[t] = before[a1[t]] + slot[t]
+            if keep2[t]:
+                row2[t] = before[a2[t]] + slot2[t]
+        before += accepted[g] + accepted2[g]
+    return Route2(C=C, logits=z, probs=p, expert=a1, expert2=a2, gate=gate, gate2=gate2, slot=slot, slot2=slot2,
+                  keep=keep, keep2=keep2, row=row, row2=row2, raw=raw, raw2=raw2, accepted=accepted,
+                  accepted2=accepted2, f=f, P=P, balance=balance, aux_per_group=aux,
+                  aux_loss=float(aux.mean()) if G > 0 else 0.0, z_per_group=zg,
+                  z_loss=float(zg.mean()) if G > 0 else 0.0,
+                  expert_rows=(accepted + accepted2).sum(axis=0))
+
+
+def combine_top2(r: Route2, outputs: dict, tokens: Sequence[int], d: int) -> np.ndarray:
+    """y_t = sum over the token's kept choices of gate_k * FFN_{e_k}(x_t)
+    [moe, 路由器只开两条线: the two results are added with their weights]; 0 when both
+    choices are dropped.  `outputs` maps (token, expert) to that expert's output row."""
+    y = np.zeros((len(tokens), d))
+    for i, t in enumerate(tokens):
+        if r.keep[t]:
+            y[i] += r.gate[t] * outputs[(t, int(r.expert[t]))]
+        if r.keep2[t]:
+            y[i] += r.gate2[t] * outputs[(t, int(r.expert2[t]))]
+    return y
+
+
+def forward_top2(x, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor: float,
+                 tokens: Optional[Sequence[int]] = None, alpha: float = 1e-2, capacity_override: int = 0):
+    """The top-2 layer on `tokens` (all when None): returns (y rows, Route2)."""
+    r = route_top2(x, Wr, br, G, T, E, capacity_factor, alpha, capacity_override)
+    tokens = list(range(G * T)) if tokens is None else list(tokens)
+    return combine_top2(r, expert_outputs_top2(x, r, W1, b1, W2, b2, tokens), tokens, np.asarray(x).shape[1]), r
+
+
+def expert_outputs_top2(x, r: Route2, W1, b1, W2, b2, tokens: Optional[Sequence[int]] = None) -> dict:
+    """Ungated outputs FFN_e(x_t) for every kept (token, choice): {(t, e): row}."""
+    x = np.asarray(x)
+    idx = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    out = {}
+    for ex, kp in ((r.expert, r.keep), (r.expert2, r.keep2)):
+        sel_all = idx[kp[idx]]
+        for e in np.unique(ex[sel_all]):
+            sel = sel_all[ex[sel_all] == e]
+            o = expert_ffn(x[sel], W1[e], None if b1 is None else b1[e], W2[e], None if b2 is None else b2[e])
+            for i, t in enumerate(sel):
+                out[(int(t), int(e))] = o[i]
     return out

@@ -416,3 +416,115 @@ def test_z_loss_is_per_group_then_mean():
     lnE = math.log(E)
     np.testing.assert_allclose(r.z_per_group, [lnE ** 2, (2.0 + lnE) ** 2], rtol=1e-13)
     assert abs(r.z_loss - 0.5 * (lnE ** 2 + (2.0 + lnE) ** 2)) <= 1e-13 * r.z_loss
+
+
+# ----------------------------------------------------------------------------- top-2 variant
+
+def queue_top2_slots(a1, a2, E, C):
+    """Second formulation of the top-2 slot rule: one queue of (token, choice) requests, all
+    first choices in sequence order, then all second choices in sequence order; each expert
+    accepts requests while it has fewer than C."""
+    T = len(a1)
+    taken = [0] * E
+    slot = {}  # (token, choice) -> slot of an accepted request; None when refused
+    for choice, a in ((0, a1), (1, a2)):
+        for t in range(T):
+            e = int(a[t])
+            if taken[e] < C:
+                slot[(t, choice)] = taken[e]
+                taken[e] += 1
+            else:
+                slot[(t, choice)] = None
+    return slot
+
+
+def test_top2_gates_page_rule(golden):
+    g = golden("top2_gates.json")
+    E, d, T = g["E"], g["d"], 40
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((T, d))
+    Wr = rng.standard_normal((E, d)) * math.sqrt(0.1 / d)
+    r = so.route_top2(x, Wr, None, 1, T, E, 1.0)
+    np.testing.assert_allclose(r.gate + r.gate2, g["weights_sum"], rtol=0, atol=1e-15)
+    for t in range(T):
+        z1, z2 = r.logits[t, r.expert[t]], r.logits[t, r.expert2[t]]
+        assert z1 >= z2 and r.expert[t] != r.expert2[t]
+        # softmax over the two kept scores: the first weight is the logistic of their gap
+        assert abs(r.gate[t] - 1.0 / (1.0 + math.exp(-(z1 - z2)))) < 1e-15
+        # and the two are the largest scores of the row
+        assert (np.sort(r.logits[t])[-2:] == np.sort([z1, z2])).all()
+
+
+def test_top2_two_experts_and_ties():
+    # E = 2: both experts chosen; equal scores: experts 0 then 1, weights 1/2 each
+    x = np.array([[0.7], [-1.2], [0.0]])
+    Wr = np.array([[1.0], [0.0]])
+    r = so.route_top2(x, Wr, None, 1, 3, 2, 1.0)
+    assert r.expert.tolist() == [0, 1, 0] and r.expert2.tolist() == [1, 0, 1]
+    assert abs(r.gate[2] - 0.5) < 1e-15 and abs(r.gate2[2] - 0.5) < 1e-15
+    r4 = so.route_top2(np.zeros((5, 1)), np.ones((4, 1)), None, 1, 5, 4, 1.0)
+    assert (r4.expert == 0).all() and (r4.expert2 == 1).all()
+
+
+def test_top2_capacity_is_twice_top1():
+    for (c, T, E) in [(1.0, 64, 4), (1.25, 4096, 64), (1.0, 8192, 128), (1.0, 32, 16)]:
+        assert so.capacity(2 * c, T, E) == 2 * so.capacity(c, T, E)  # c T / E integral here
+    r = so.route_top2(np.zeros((64, 1)), np.ones((4, 1)), None, 1, 64, 4, 1.0)
+    assert r.C == 32
+
+
+def test_top2_slots_match_queue_rule():
+    rng = np.random.default_rng(9)
+    for (G, T, E, c) in [(1, 30, 4, 0.5), (3, 17, 5, 1.0), (2, 40, 3, 0.25)]:
+        x = rng.standard_normal((G * T, 3))
+        Wr = rng.standard_normal((E, 3))
+        br = np.array([0.8] + [0.0] * (E - 1))  # crowd expert 0
+        r = so.route_top2(x, Wr, br, G, T, E, c)
+        before = np.zeros(E, dtype=np.int64)
+        for g in range(G):
+            sl = slice(g * T, (g + 1) * T)
+            q = queue_top2_slots(r.expert[sl], r.expert2[sl], E, r.C)
+            for t in range(T):
+                tt = g * T + t
+                for (sl_, kp, rw, ex, ch) in ((r.slot, r.keep, r.row, r.expert, 0),
+                                              (r.slot2, r.keep2, r.row2, r.expert2, 1)):
+                    qs = q[(t, ch)]
+                    assert bool(kp[tt]) == (qs is not None)
+                    if qs is None:
+                        assert sl_[tt] >= r.C and rw[tt] == -1
+                    else:
+                        assert sl_[tt] == qs and rw[tt] == before[ex[tt]] + qs
+            kept = np.bincount(r.expert[sl][r.keep[sl]], minlength=E) + \
+                np.bincount(r.expert2[sl][r.keep2[sl]], minlength=E)
+            assert (kept <= r.C).all()
+            assert (kept == r.accepted[g] + r.accepted2[g]).all()
+            before += kept
+        assert (r.expert_rows == before).all()
+        # f counts first choices only, over all T tokens
+        np.testing.assert_allclose(r.f.sum(axis=1), 1.0, rtol=1e-15)
+
+
+def test_top2_without_drops_is_the_dense_weighted_pair():
+    # enough capacity for every request: y_t = w1 FFN_e1(x_t) + w2 FFN_e2(x_t), computed here
+    # densely (every expert on every token) with the pair found by a stable sort
+    rng = np.random.default_rng(4)
+    G, T, E, d, F = 2, 9, 5, 6, 7
+    x = rng.standard_normal((G * T, d))
+    Wr = rng.standard_normal((E, d))
+    W1 = rng.standard_normal((E, F, d)) * 0.3
+    b1 = rng.standard_normal((E, F)) * 0.1
+    W2 = rng.standard_normal((E, d, F)) * 0.3
+    b2 = rng.standard_normal((E, d)) * 0.1
+    y, r = so.forward_top2(x, Wr, None, W1, b1, W2, b2, G, T, E, 1.0, capacity_override=2 * T)
+    assert r.keep.all() and r.keep2.all()
+    z = x @ Wr.T
+    h = np.maximum(np.einsum("nd,efd->nef", x, W1) + b1[None], 0.0)
+    o = np.einsum("nef,edf->ned", h, W2) + b2[None]
+    order = np.argsort(-z, axis=1, kind="stable")
+    want = np.zeros((G * T, d))
+    for t in range(G * T):
+        e1, e2 = order[t, 0], order[t, 1]
+        w = np.exp(z[t, [e1, e2]] - z[t, e1])
+        w = w / w.sum()
+        want[t] = w[0] * o[t, e1] + w[1] * o[t, e2]
+    np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-12)
