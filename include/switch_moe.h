@@ -69,6 +69,13 @@ typedef enum { SWITCH_F32 = 0, SWITCH_BF16 = 1 } switch_dtype;
 #define SWITCH_FLAG_WRITE_LOGITS  0x2u  /* route writes logits[N*E] (verification only) */
 #define SWITCH_FLAG_DEBUG_BOUNDS  0x4u  /* kernels check slot/row/expert ranges */
 #define SWITCH_FLAG_PROFILE       0x8u  /* switch_forward records per-stage CUDA events */
+/* Top-2 routing (the variant on the 混合专家 page, section 路由器只开两条线): each token
+ * goes to the experts of its two highest logits (ties to the lower index) with weights =
+ * softmax over those two logits (they add to 1); capacity C = ceil(2 c T / E), twice the
+ * top-1 capacity; a token's second choice takes a slot after its expert's kept first
+ * choices of the group, in sequence order; f (and raw_count / accepted_count) count first
+ * choices; a dropped choice's weight is not moved to the other.  Needs E >= 2. */
+#define SWITCH_FLAG_TOP2          0x10u
 
 typedef struct {
   int G;                   /* routing groups; capacity and statistics are per group */
@@ -98,7 +105,8 @@ typedef struct {
   float* balance;           /* [G]   unweighted E * sum_e f_e P_e                       */
   float* aux_loss_per_group;/* [G]   alpha * balance                                    */
   float* aux_loss;          /* [1]   mean over groups                                   */
-  int32_t* expert_rows;     /* [E]   sum over groups of accepted_count (rows of xe used) */
+  int32_t* expert_rows;     /* [E]   sum over groups of accepted_count (+ accepted2_count
+                                     with SWITCH_FLAG_TOP2): rows of xe used              */
   float* probs;             /* [N*E] or NULL; written when SWITCH_FLAG_WRITE_PROBS      */
   float* logits;            /* [N*E] or NULL; written when SWITCH_FLAG_WRITE_LOGITS     */
   /* Router z-loss (ST-MoE, as restated on the 070 page, section 核心思想与公式):
@@ -106,6 +114,14 @@ typedef struct {
    * Either pointer may be NULL (not written). */
   float* z_loss_per_group;  /* [G]   L_z of each routing group                            */
   float* z_loss;            /* [1]   mean over groups                                     */
+  /* Second choices (SWITCH_FLAG_TOP2 only, required then; ignored otherwise). */
+  int32_t* expert2;         /* [N]   second choice                                        */
+  int32_t* slot2;           /* [N]   kept first choices of that expert + earlier second choices */
+  uint8_t* keep2;           /* [N]   1 when slot2 < C                                     */
+  float* gate2;             /* [N]   its weight; gate + gate2 = 1 (gate is the first's)   */
+  int32_t* row2;            /* [N]   row in the expert's block of xe, -1 if dropped       */
+  int32_t* raw2_count;      /* [G*E] second choices per expert                            */
+  int32_t* accepted2_count; /* [G*E] kept second choices per expert                       */
 } switch_route_out;
 
 /* Capacity C for cfg (host only, no GPU needed); -1 when cfg is invalid. */
@@ -126,14 +142,16 @@ SWITCH_API switch_status switch_destroy(switch_handle h);
  * Logits are float32 (x cast up, then dot products with float32 accumulation);
  * ties go to the lowest expert index.  Writes every non-NULL field of *out
  * except probs/logits, which need their flags.  All fields other than
- * probs and logits are required.
+ * probs, logits and the z-loss are required, and with SWITCH_FLAG_TOP2 the
+ * second-choice fields too.
  */
 SWITCH_API switch_status switch_route(switch_handle h, const void* x, const float* Wr, const float* br,
                            const switch_route_out* out, void* stream);
 
 /*
- * Dispatch gather: xe[e, row_t, :] = x_t for every kept token t with expert e;
- * every other row of xe is zero.  xe is [E, G*C, d] act: expert e's block holds
+ * Dispatch gather: xe[e, row_t, :] = x_t for every kept token t with expert e
+ * (with SWITCH_FLAG_TOP2 also xe[expert2_t, row2_t, :] = x_t for kept second
+ * choices); every other row of xe is zero.  xe is [E, G*C, d] act: expert e's block holds
  * its kept tokens group by group in sequence order.
  */
 SWITCH_API switch_status switch_dispatch(switch_handle h, const void* x, const switch_route_out* r,
@@ -153,7 +171,8 @@ SWITCH_API switch_status switch_expert_ffn(switch_handle h, const void* xe, cons
 
 /*
  * Combine: y_t = gate_t * ye[expert_t, row_t, :] for kept tokens, 0 for dropped
- * ones, plus x_residual_t when x_residual is not NULL.  The gate is used as is
+ * ones (with SWITCH_FLAG_TOP2 plus gate2_t * ye[expert2_t, row2_t, :] for a kept
+ * second choice), plus x_residual_t when x_residual is not NULL.  The gate is used as is
  * (no renormalisation).  y [N, d] act.
  */
 SWITCH_API switch_status switch_combine(switch_handle h, const void* ye, const switch_route_out* r,
@@ -248,6 +267,8 @@ SWITCH_API int switch_last_launch_count(switch_handle h);
  *     SWITCH_ERR_INVALID_ARG.
  *   - Device-side flags (a bounded wait that ran out, non-finite logits) stay in the array
  *     and are not reported; use switch_route on a handle when they are needed.
+ *   - SWITCH_FLAG_TOP2 returns SWITCH_ERR_UNSUPPORTED (top-2 routing uses a logits buffer
+ *     that only a handle's workspace holds).
  */
 SWITCH_API switch_status switch_route_static(const switch_config* cfg, const void* x, const float* Wr,
                                   const float* br, const switch_route_out* out, void* stream);

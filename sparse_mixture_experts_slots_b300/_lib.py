@@ -26,6 +26,7 @@ FLAG_WRITE_PROBS = 0x1
 FLAG_WRITE_LOGITS = 0x2
 FLAG_DEBUG_BOUNDS = 0x4
 FLAG_PROFILE = 0x8
+FLAG_TOP2 = 0x10
 
 
 class SwitchConfig(ctypes.Structure):
@@ -35,7 +36,8 @@ class SwitchConfig(ctypes.Structure):
 
 
 ROUTE_FIELDS = ["expert", "slot", "keep", "gate", "row", "raw_count", "accepted_count", "P", "balance",
-                "aux_loss_per_group", "aux_loss", "expert_rows", "probs", "logits", "z_loss_per_group", "z_loss"]
+                "aux_loss_per_group", "aux_loss", "expert_rows", "probs", "logits", "z_loss_per_group", "z_loss",
+                "expert2", "slot2", "keep2", "gate2", "row2", "raw2_count", "accepted2_count"]
 
 
 class SwitchRouteOut(ctypes.Structure):

@@ -39,6 +39,8 @@ struct switch_layer {
   float* tile_P;
   float* tile_Z;
   int32_t* tile_base;
+  int32_t* tile_hist2;  // top-2 only
+  int32_t* tile_base2;
   int32_t* group_off;
   int32_t* tok_of_row;
   void* wsplit;
@@ -59,10 +61,13 @@ namespace {
 
 constexpr int MAX_E = 2048;
 
+bool top2_of(const switch_config* c) { return (c->flags & SWITCH_FLAG_TOP2) != 0; }
+
 int64_t capacity_of(const switch_config* c) {
   if (c->capacity_override > 0) return c->capacity_override;
   if (c->T <= 0) return 0;
-  const double v = c->capacity_factor * (double)c->T / (double)c->E;
+  // top-2: twice top-1's capacity (each token makes two requests)
+  const double v = (top2_of(c) ? 2.0 : 1.0) * c->capacity_factor * (double)c->T / (double)c->E;
   const double r = nearbyint(v);
   if (fabs(v - r) <= 1e-9) return (int64_t)r;
   return (int64_t)ceil(v);
@@ -71,6 +76,7 @@ int64_t capacity_of(const switch_config* c) {
 bool config_ok(const switch_config* c) {
   if (!c) return false;
   if (c->G < 1 || c->T < 0 || c->d_model < 1 || c->d_ff < 1 || c->E < 1 || c->E > MAX_E) return false;
+  if (top2_of(c) && c->E < 2) return false;
   if (c->dtype != SWITCH_F32 && c->dtype != SWITCH_BF16) return false;
   if (c->capacity_override < 0) return false;
   if (c->capacity_override == 0 && !(c->capacity_factor > 0.0 && c->capacity_factor < 1e6)) return false;
@@ -92,9 +98,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Per-token arrays may be NULL only when there are no tokens.
-bool route_out_ok(const switch_route_out* r, int64_t N) {
+bool route_out_ok(const switch_route_out* r, int64_t N, bool top2 = false) {
   if (!r) return false;
   if (N > 0 && !(r->expert && r->slot && r->keep && r->gate && r->row)) return false;
+  if (top2 && N > 0 && !(r->expert2 && r->slot2 && r->keep2 && r->gate2 && r->row2)) return false;
+  if (top2 && !(r->raw2_count && r->accepted2_count)) return false;
   return r->raw_count && r->accepted_count && r->P && r->balance && r->aux_loss_per_group && r->aux_loss &&
          r->expert_rows;
 }
@@ -157,7 +165,8 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   };
   const size_t o_err = take(sizeof(uint32_t) * 4);  // [0] error word, [1] scan counter
   // float32 logits are materialised only by the CUDA-core router (float32 activations)
-  const size_t o_logits = take(cfg->dtype == SWITCH_F32 ? N * E * sizeof(float) : 0);
+  const bool two = top2_of(cfg);
+  const size_t o_logits = take(cfg->dtype == SWITCH_F32 || two ? N * E * sizeof(float) : 0);
   const size_t o_wsplit = take(cfg->dtype == SWITCH_BF16 ? router_tc_wsplit_bytes(cfg->E, cfg->d_model) : 0);
   const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
   const size_t ffn_words = ffn_counter_words(cfg->E, (int)R, cfg->d_model, cfg->d_ff);
@@ -166,6 +175,8 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_tP = take(G * nT * E * sizeof(float));
   const size_t o_tZ = take(G * nT * sizeof(float));
   const size_t o_base = take(G * nT * E * sizeof(int32_t));
+  const size_t o_hist2 = take(two ? G * nT * E * sizeof(int32_t) : 0);
+  const size_t o_base2 = take(two ? G * nT * E * sizeof(int32_t) : 0);
   const size_t o_goff = take(G * E * sizeof(int32_t));
   const size_t o_tor = take(E * R * sizeof(int32_t));
   const size_t o_xe = take(E * R * d * h->es);
@@ -182,6 +193,8 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->tile_hist = reinterpret_cast<int32_t*>(h->ws + o_hist);
   h->tile_P = reinterpret_cast<float*>(h->ws + o_tP);
   h->tile_Z = reinterpret_cast<float*>(h->ws + o_tZ);
+  h->tile_hist2 = reinterpret_cast<int32_t*>(h->ws + o_hist2);
+  h->tile_base2 = reinterpret_cast<int32_t*>(h->ws + o_base2);
   h->tile_base = reinterpret_cast<int32_t*>(h->ws + o_base);
   h->group_off = reinterpret_cast<int32_t*>(h->ws + o_goff);
   h->tok_of_row = reinterpret_cast<int32_t*>(h->ws + o_tor);
@@ -229,7 +242,7 @@ switch_status switch_destroy(switch_handle h) {
 
 static switch_status route_args(switch_handle h, const void* x, const float* Wr, const float* br,
                                 const switch_route_out* out, RouteArgs* a) {
-  if (!h || !Wr || !route_out_ok(out, h ? h->N : 0)) return SWITCH_ERR_INVALID_ARG;
+  if (!h || !Wr || !route_out_ok(out, h ? h->N : 0, h && top2_of(&h->cfg))) return SWITCH_ERR_INVALID_ARG;
   if (h->N > 0 && !x) return SWITCH_ERR_INVALID_ARG;
   if (x && !aligned16(x)) return SWITCH_ERR_INVALID_ARG;
   const switch_config& c = h->cfg;
@@ -275,22 +288,37 @@ static switch_status route_args(switch_handle h, const void* x, const float* Wr,
   a->probs = want_probs ? out->probs : nullptr;
   a->z_g = out->z_loss_per_group;
   a->z = out->z_loss;
+  a->top2 = top2_of(&c);
+  if (a->top2) {
+    a->expert2 = out->expert2;
+    a->slot2 = out->slot2;
+    a->keep2 = out->keep2;
+    a->gate2 = out->gate2;
+    a->row2 = out->row2;
+    a->raw2 = out->raw2_count;
+    a->accepted2 = out->accepted2_count;
+    a->tile_hist2 = h->tile_hist2;
+    a->tile_base2 = h->tile_base2;
+  }
   return SWITCH_OK;
 }
 
 switch_status switch_route(switch_handle h, const void* x, const float* Wr, const float* br,
                            const switch_route_out* out, void* stream) {
-  RouteArgs a;
+  RouteArgs a{};
   const switch_status st = route_args(h, x, Wr, br, out, &a);
   if (st != SWITCH_OK) return st;
   return launched(launch_route(a, (cudaStream_t)stream), h);
 }
 
 switch_status switch_dispatch(switch_handle h, const void* x, const switch_route_out* r, void* xe, void* stream) {
-  if (!h || !route_out_ok(r, h->N) || (h->R > 0 && !xe) || !aligned16(xe)) return SWITCH_ERR_INVALID_ARG;
+  if (!h || !route_out_ok(r, h->N, top2_of(&h->cfg)) || (h->R > 0 && !xe) || !aligned16(xe))
+    return SWITCH_ERR_INVALID_ARG;
   if (h->N > 0 && (!x || !aligned16(x))) return SWITCH_ERR_INVALID_ARG;
-  return launched(launch_dispatch(x, xe, r->expert, r->row, r->expert_rows, h->N, h->cfg.E, h->R,
-                                  h->cfg.d_model * h->es, (cudaStream_t)stream),
+  const bool two = top2_of(&h->cfg);
+  return launched(launch_dispatch(x, xe, r->expert, r->row, two ? r->expert2 : nullptr, two ? r->row2 : nullptr,
+                                  r->expert_rows, h->N, h->cfg.E, h->R, h->cfg.d_model * h->es,
+                                  (cudaStream_t)stream),
                   h);
 }
 
@@ -364,11 +392,14 @@ switch_status switch_expert_ffn(switch_handle h, const void* xe, const void* W1,
 
 static switch_status combine_impl(switch_handle h, const void* ye, const switch_route_out* r, const void* x_residual,
                                   void* y, cudaStream_t s, bool pdl) {
-  if (!h || !route_out_ok(r, h->N) || (h->R > 0 && !ye) || (h->N > 0 && !y) || !aligned16(ye) || !aligned16(y))
+  const bool two = h && top2_of(&h->cfg);
+  if (!h || !route_out_ok(r, h->N, two) || (h->R > 0 && !ye) || (h->N > 0 && !y) || !aligned16(ye) ||
+      !aligned16(y))
     return SWITCH_ERR_INVALID_ARG;
   if (x_residual && !aligned16(x_residual)) return SWITCH_ERR_INVALID_ARG;
-  return launched(launch_combine(ye, r->expert, r->row, r->gate, x_residual, y, h->N, h->cfg.d_model, h->R,
-                                 h->cfg.dtype == SWITCH_BF16, s, pdl),
+  return launched(launch_combine(ye, r->expert, r->row, r->gate, two ? r->expert2 : nullptr,
+                                 two ? r->row2 : nullptr, two ? r->gate2 : nullptr, x_residual, y, h->N,
+                                 h->cfg.d_model, h->R, h->cfg.dtype == SWITCH_BF16, s, pdl),
                   h);
 }
 
@@ -389,9 +420,38 @@ switch_status switch_forward(switch_handle h, const void* x, const float* Wr, co
   // Consecutive kernels of the call start as programmatic dependents of their
   // predecessor (their prologues overlap its tail); with per-stage events in between
   // (SWITCH_FLAG_PROFILE) every launch is an ordinary one.
-  RouteArgs a;
+  RouteArgs a{};
   switch_status st = route_args(h, x, Wr, br, r, &a);
   if (st != SWITCH_OK) return st;
+  if (a.top2) {
+    // top-2: routing with its slots, one dispatch pass for both choices, the FFN into ye,
+    // and a combine that adds the two weighted outputs per token
+    st = launched(launch_route(a, s), h);
+    if (st != SWITCH_OK) return st;
+    if (prof) cudaEventRecord(h->ev[1], s);
+    st = launched(launch_dispatch(x, h->xe, r->expert, r->row, r->expert2, r->row2, r->expert_rows, h->N,
+                                  h->cfg.E, h->R, h->cfg.d_model * h->es, s),
+                  h);
+    if (st != SWITCH_OK) return st;
+    if (prof) cudaEventRecord(h->ev[2], s);
+    if (use_tc_ffn(h)) {
+      if (h->R > 0) {
+        if (cudaMemsetAsync(h->ffn_counters, 0, (size_t)h->ffn_counter_words * sizeof(uint32_t), s) != cudaSuccess)
+          return SWITCH_ERR_CUDA;
+        st = run_ffn_tc(h, h->xe, W1, b1, W2, b2, r->expert_rows, h->ye, false, nullptr, nullptr, s, false);
+        if (st != SWITCH_OK) return st;
+      }
+      if (prof) cudaEventRecord(h->ev[3], s);
+    } else {
+      st = run_ffn_simt(h, h->xe, W1, b1, W2, b2, r->expert_rows, h->ye, s, prof ? 3 : -1, !prof);
+      if (st != SWITCH_OK) return st;
+    }
+    if (prof) cudaEventRecord(h->ev[4], s);
+    st = combine_impl(h, h->ye, r, x_residual, y, s, false);
+    if (st != SWITCH_OK) return st;
+    if (prof) cudaEventRecord(h->ev[5], s);
+    return SWITCH_OK;
+  }
   a.slots = false;  // the dispatch pass below turns ranks into slots
   st = launched(launch_route(a, s), h);
   if (st != SWITCH_OK) return st;
@@ -588,6 +648,7 @@ void* static_route_scratch(int dev) {
 extern "C" switch_status switch_route_static(const switch_config* cfg, const void* x, const float* Wr,
                                              const float* br, const switch_route_out* out, void* stream) {
   if (!config_ok(cfg) || !Wr) return SWITCH_ERR_INVALID_ARG;
+  if (top2_of(cfg)) return SWITCH_ERR_UNSUPPORTED;  // top-2 routing needs a handle's logits buffer
   const int N = cfg->G * cfg->T;
   if (!route_out_ok(out, N)) return SWITCH_ERR_INVALID_ARG;
   if (N > 0 && !x) return SWITCH_ERR_INVALID_ARG;
@@ -627,7 +688,7 @@ extern "C" switch_status switch_route_static(const switch_config* cfg, const voi
   if (cudaMemsetAsync(ws + o_err, 0, sizeof(uint32_t) * 4, s) != cudaSuccess) return SWITCH_ERR_CUDA;
   const bool want_logits = (cfg->flags & SWITCH_FLAG_WRITE_LOGITS) && out->logits;
   const bool want_probs = (cfg->flags & SWITCH_FLAG_WRITE_PROBS) && out->probs;
-  RouteArgs a;
+  RouteArgs a{};
   a.x = x;
   a.Wr = Wr;
   a.br = br;

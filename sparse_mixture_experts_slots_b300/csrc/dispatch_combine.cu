@@ -15,9 +15,13 @@ constexpr int DC_WARPS = 8;
 
 // Warps [0, N) copy token rows to their slots; warps [N, N + E*R) zero the rows
 // past each expert's count.  Both reads and writes are whole 16-byte-vector rows.
+// expert2 / row2 (top-2 routing, else null): the token's second choice, copied from the
+// same read of its row.
 __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_kernel(const uint4* __restrict__ x, uint4* __restrict__ xe,
                                                                  const int32_t* __restrict__ expert,
                                                                  const int32_t* __restrict__ row,
+                                                                 const int32_t* __restrict__ expert2,
+                                                                 const int32_t* __restrict__ row2,
                                                                  const int32_t* __restrict__ expert_rows, int N,
                                                                  int E, int R, int vecs) {
   griddep_wait();
@@ -26,10 +30,16 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_kernel(const uint4* __
   const long long w = (long long)blockIdx.x * DC_WARPS + warp;
   if (w < N) {
     const int r = row[w];
-    if (r < 0) return;
+    const int r2 = row2 ? row2[w] : -1;
+    if (r < 0 && r2 < 0) return;
     const uint4* src = x + w * vecs;
-    uint4* dst = xe + ((long long)expert[w] * R + r) * vecs;
-    for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
+    uint4* dst = r >= 0 ? xe + ((long long)expert[w] * R + r) * vecs : nullptr;
+    uint4* dst2 = r2 >= 0 ? xe + ((long long)expert2[w] * R + r2) * vecs : nullptr;
+    for (int v = lane; v < vecs; v += 32) {
+      const uint4 val = __ldg(src + v);
+      if (dst) dst[v] = val;
+      if (dst2) dst2[v] = val;
+    }
     return;
   }
   const long long dr = w - N;
@@ -41,13 +51,13 @@ __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_kernel(const uint4* __
   for (int v = lane; v < vecs; v += 32) dst[v] = zero;
 }
 
-int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_t* row, const int32_t* expert_rows,
-                    int N, int E, int R, int row_bytes, cudaStream_t s) {
+int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_t* row, const int32_t* expert2,
+                    const int32_t* row2, const int32_t* expert_rows, int N, int E, int R, int row_bytes, cudaStream_t s) {
   const long long warps = (long long)N + (long long)E * R;
   if (warps == 0 || (long long)E * R == 0) return 0;
   const unsigned blocks = (unsigned)((warps + DC_WARPS - 1) / DC_WARPS);
   return launch_k(dispatch_kernel, dim3(blocks), dim3(DC_WARPS * 32), 0, s, false, 1, (const uint4*)x, (uint4*)xe,
-                  expert, row, expert_rows, N, E, R, row_bytes / 16) == cudaSuccess
+                  expert, row, expert2, row2, expert_rows, N, E, R, row_bytes / 16) == cudaSuccess
              ? 1
              : -1;
 }
@@ -173,11 +183,16 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return v;
 }
 
+// expert2 / row2 / gate2 (top-2 routing, else null): y_t also gets gate2_t * ye of the
+// token's second choice when that choice was kept.
 template <bool BF16>
 __global__ void __launch_bounds__(DC_WARPS * 32) combine_kernel(const uint4* __restrict__ ye,
                                                                 const int32_t* __restrict__ expert,
                                                                 const int32_t* __restrict__ row,
                                                                 const float* __restrict__ gate,
+                                                                const int32_t* __restrict__ expert2,
+                                                                const int32_t* __restrict__ row2,
+                                                                const float* __restrict__ gate2,
                                                                 const uint4* __restrict__ resid, uint4* __restrict__ y,
                                                                 int N, int R, int vecs) {
   griddep_wait();
@@ -191,6 +206,13 @@ __global__ void __launch_bounds__(DC_WARPS * 32) combine_kernel(const uint4* __r
   if (r >= 0) {
     src = ye + ((long long)expert[t] * R + r) * vecs;
     g = gate[t];
+  }
+  const int r2 = row2 ? row2[t] : -1;
+  const uint4* src2 = nullptr;
+  float g2 = 0.f;
+  if (r2 >= 0) {
+    src2 = ye + ((long long)expert2[t] * R + r2) * vecs;
+    g2 = gate2[t];
   }
   uint4* dst = y + t * vecs;
   const uint4* res = resid ? resid + t * vecs : nullptr;
@@ -208,6 +230,19 @@ __global__ void __launch_bounds__(DC_WARPS * 32) combine_kernel(const uint4* __r
       }
 #pragma unroll
       for (int i = 0; i < W; ++i) o[i] *= g;
+    }
+    if (src2) {
+      float o2[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const uint4 in = __ldg(src2 + v);
+      if (BF16) {
+        unpack8(in, o2);
+      } else {
+        const float* f = reinterpret_cast<const float*>(&in);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o2[i] = f[i];
+      }
+#pragma unroll
+      for (int i = 0; i < W; ++i) o[i] = fmaf(g2, o2[i], o[i]);
     }
     if (res) {
       const uint4 rv = __ldg(res + v);
@@ -231,16 +266,17 @@ __global__ void __launch_bounds__(DC_WARPS * 32) combine_kernel(const uint4* __r
   }
 }
 
-int launch_combine(const void* ye, const int32_t* expert, const int32_t* row, const float* gate, const void* resid,
+int launch_combine(const void* ye, const int32_t* expert, const int32_t* row, const float* gate,
+                   const int32_t* expert2, const int32_t* row2, const float* gate2, const void* resid,
                    void* y, int N, int d, int R, bool bf16, cudaStream_t s, bool pdl) {
   if (N == 0) return 0;
   const int vecs = d * (bf16 ? 2 : 4) / 16;
   const unsigned blocks = (unsigned)((N + DC_WARPS - 1) / DC_WARPS);
   const cudaError_t e =
       bf16 ? launch_k(combine_kernel<true>, dim3(blocks), dim3(DC_WARPS * 32), 0, s, pdl, 1, (const uint4*)ye, expert,
-                      row, gate, (const uint4*)resid, (uint4*)y, N, R, vecs)
+                      row, gate, expert2, row2, gate2, (const uint4*)resid, (uint4*)y, N, R, vecs)
            : launch_k(combine_kernel<false>, dim3(blocks), dim3(DC_WARPS * 32), 0, s, pdl, 1, (const uint4*)ye, expert,
-                      row, gate, (const uint4*)resid, (uint4*)y, N, R, vecs);
+                      row, gate, expert2, row2, gate2, (const uint4*)resid, (uint4*)y, N, R, vecs);
   return e == cudaSuccess ? 1 : -1;
 }
 

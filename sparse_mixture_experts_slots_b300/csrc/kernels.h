@@ -70,6 +70,12 @@ struct RouteArgs {
   float* probs;        // or null
   float* z_g;          // [G] router z-loss per group, or null
   float* z;            // [1] its mean over groups, or null
+  // top-2 routing (top2): second choices and their per-tile counts / prefixes
+  bool top2;
+  int32_t* expert2; int32_t* slot2; uint8_t* keep2; float* gate2; int32_t* row2;
+  int32_t* raw2; int32_t* accepted2;
+  int32_t* tile_hist2; // [G, nT, E]
+  int32_t* tile_base2; // [G, nT, E]
 };
 
 // Blocks of the cross-tile scan (one per 32 experts); scan_partial holds G * this many floats.
@@ -107,14 +113,18 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, void* y, const void* resid,
                           uint32_t* zero_ptr, int zero_words, cudaStream_t s, bool pdl);
 
-// xe[expert[t]*R + row[t]] = x[t] for kept tokens (row[t] >= 0); rows r >= expert_rows[e]
-// of every expert block are zeroed.
-int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_t* row,
-                    const int32_t* expert_rows, int N, int E, int R, int row_bytes, cudaStream_t s);
+// xe[expert[t]*R + row[t]] = x[t] for kept tokens (row[t] >= 0), and likewise for the
+// second choice (expert2/row2, top-2 routing; null otherwise); rows r >= expert_rows[e] of
+// every expert block are zeroed.
+int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_t* row, const int32_t* expert2,
+                    const int32_t* row2, const int32_t* expert_rows, int N, int E, int R, int row_bytes,
+                    cudaStream_t s);
 
-// y[t] = (row[t] >= 0 ? gate[t] * ye[expert[t]*R + row[t]] : 0) (+ resid[t]).
+// y[t] = (row[t] >= 0 ? gate[t] * ye[expert[t]*R + row[t]] : 0)
+//        (+ row2[t] >= 0 ? gate2[t] * ye[expert2[t]*R + row2[t]] : 0, top-2) (+ resid[t]).
 int launch_combine(const void* ye, const int32_t* expert, const int32_t* row, const float* gate,
-                   const void* resid, void* y, int N, int d, int R, bool bf16, cudaStream_t s, bool pdl);
+                   const int32_t* expert2, const int32_t* row2, const float* gate2, const void* resid,
+                   void* y, int N, int d, int R, bool bf16, cudaStream_t s, bool pdl);
 
 // out[e*R + n, m] = act(sum_k in[e*R + n, k] * W[e, m, k] + bias[e, m]) for n < expert_rows[e].
 // CUDA-core kernel for float32 and for shapes the tensor-core kernel does not take.

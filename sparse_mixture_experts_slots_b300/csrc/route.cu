@@ -151,6 +151,114 @@ __global__ void __launch_bounds__(256) route_softmax_kernel(
   }
 }
 
+// ---------------------------------------------------------------- 2b. top-2 per tile (from float32 logits)
+// grid (nT, G), 256 threads; dynamic smem: hist[E], hist2[E] ints.  Per token: the two
+// highest logits (ties to the lower index), their weights = softmax over the two, the
+// full softmax's column sums (P), (log sum exp z)^2, and the in-tile ranks of both
+// choices among the tile's first / second choices (into rank[] / rank2[]).
+__device__ __forceinline__ bool top_before(float v, int i, float w, int j) {
+  return v > w || (v == w && i < j);  // (v, i) ranks before (w, j)
+}
+
+__global__ void __launch_bounds__(256) route_top2_kernel(
+    const float* __restrict__ z, int T, int E, int nT, int32_t* __restrict__ expert, int32_t* __restrict__ expert2,
+    float* __restrict__ gate, float* __restrict__ gate2, int32_t* __restrict__ rank, int32_t* __restrict__ rank2,
+    int32_t* __restrict__ tile_hist, int32_t* __restrict__ tile_hist2, float* __restrict__ tile_P,
+    float* __restrict__ tile_Z, float* __restrict__ probs, uint32_t* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ int32_t hist[];  // [2E]: first choices, then second choices
+  int32_t* hist2 = hist + E;
+  __shared__ float m_s[ROUTE_TILE], s_s[ROUTE_TILE], zz_s[ROUTE_TILE];
+  __shared__ int a_s[ROUTE_TILE], a2_s[ROUTE_TILE];
+  const int g = blockIdx.y, tile = blockIdx.x;
+  const int t0 = tile * ROUTE_TILE;
+  const int len = min(ROUTE_TILE, T - t0);
+  const size_t tok0 = (size_t)g * T + t0;
+  for (int e = threadIdx.x; e < 2 * E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
+  for (int i = warp; i < len; i += nwarps) {
+    const float* zr = z + (tok0 + i) * E;
+    float m1 = -INFINITY, m2 = -INFINITY;
+    int i1 = 0x7fffffff, i2 = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {  // increasing e: strict > keeps the lower index
+      const float v = zr[e];
+      if (v > m1) {
+        m2 = m1; i2 = i1; m1 = v; i1 = e;
+      } else if (v > m2) {
+        m2 = v; i2 = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {  // merge the lanes' pairs (indices are distinct)
+      const float p1 = __shfl_xor_sync(0xffffffffu, m1, o), p2 = __shfl_xor_sync(0xffffffffu, m2, o);
+      const int j1 = __shfl_xor_sync(0xffffffffu, i1, o), j2 = __shfl_xor_sync(0xffffffffu, i2, o);
+      if (top_before(p1, j1, m1, i1)) {
+        if (!top_before(m1, i1, p2, j2)) { m2 = p2; i2 = j2; } else { m2 = m1; i2 = i1; }
+        m1 = p1; i1 = j1;
+      } else if (top_before(p1, j1, m2, i2)) {
+        m2 = p1; i2 = j1;
+      }
+    }
+    if (i1 < 0 || i1 >= E || i2 < 0 || i2 >= E || i1 == i2) {  // non-finite logits only
+      if (lane == 0) raise_error(err, ERR_BOUNDS);
+      i1 = 0;
+      i2 = 1;
+      m1 = zr[0];
+      m2 = zr[1];
+    }
+    float s = 0.f;
+    for (int e = lane; e < E; e += 32) s += expf(zr[e] - m1);
+    s = warp_sum(s);
+    if (lane == 0) {
+      m_s[i] = m1;
+      s_s[i] = s;
+      a_s[i] = i1;
+      a2_s[i] = i2;
+      const float u = expf(m2 - m1);  // the pair's softmax: 1 / (1 + u) and u / (1 + u)
+      expert[tok0 + i] = i1;
+      expert2[tok0 + i] = i2;
+      gate[tok0 + i] = 1.0f / (1.0f + u);
+      gate2[tok0 + i] = u / (1.0f + u);
+      const float lse = m1 + logf(s);
+      zz_s[i] = lse * lse;
+      atomicAdd(&hist[i1], 1);
+      atomicAdd(&hist2[i2], 1);
+    }
+  }
+  __syncthreads();
+
+  if (warp == 0) {  // the tile's sum of (log sum exp z)^2, in a fixed order
+    float zs = 0.f;
+    for (int i = lane; i < len; i += 32) zs += zz_s[i];
+    zs = warp_sum(zs);
+    if (lane == 0) tile_Z[(size_t)g * nT + tile] = zs;
+  }
+  for (int i = threadIdx.x; i < len; i += blockDim.x) {
+    int r = 0, r2 = 0;
+    for (int j = 0; j < i; ++j) {
+      r += a_s[j] == a_s[i];
+      r2 += a2_s[j] == a2_s[i];
+    }
+    rank[tok0 + i] = r;
+    rank2[tok0 + i] = r2;
+  }
+  const size_t tbase = ((size_t)g * nT + tile) * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float acc = 0.f;
+    for (int i = 0; i < len; ++i) {
+      const float p = expf(z[(tok0 + i) * E + e] - m_s[i]) / s_s[i];
+      acc += p;
+      if (probs) probs[(tok0 + i) * E + e] = p;
+    }
+    tile_P[tbase + e] = acc;
+    tile_hist[tbase + e] = hist[e];
+    tile_hist2[tbase + e] = hist2[e];
+  }
+}
+
 // ---------------------------------------------------------------- 3. cross-tile scan + finalize
 // One block per 32 experts (lane <-> expert); the warps split each group's tiles.  When the
 // router z-loss is asked for, one more block reduces the tiles' sums of (log sum exp z)^2
@@ -159,14 +267,16 @@ constexpr int SCAN_WARPS = 16;
 
 __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
     const int32_t* __restrict__ tile_hist, const float* __restrict__ tile_P, const float* __restrict__ tile_Z,
-    int G, int T, int E, int nT, int C, float alpha, int32_t* __restrict__ tile_base, int32_t* __restrict__ raw,
-    int32_t* __restrict__ accepted, float* __restrict__ P, int32_t* __restrict__ group_off,
+    const int32_t* __restrict__ tile_hist2, int G, int T, int E, int nT, int C, float alpha,
+    int32_t* __restrict__ tile_base, int32_t* __restrict__ tile_base2, int32_t* __restrict__ raw,
+    int32_t* __restrict__ accepted, int32_t* __restrict__ raw2, int32_t* __restrict__ accepted2,
+    float* __restrict__ P, int32_t* __restrict__ group_off,
     int32_t* __restrict__ expert_rows, float* __restrict__ balance, float* __restrict__ aux_g,
     float* __restrict__ aux, float* __restrict__ z_g, float* __restrict__ z, float* __restrict__ partial,
     uint32_t* __restrict__ counter) {
   griddep_wait();
   griddep_launch_dependents();
-  __shared__ int sh_h[SCAN_WARPS][32];
+  __shared__ int sh_h[SCAN_WARPS][32], sh_h2[SCAN_WARPS][32];
   __shared__ float sh_p[SCAN_WARPS][32];
   __shared__ double sh_z[SCAN_WARPS];
   __shared__ int is_last;
@@ -205,22 +315,35 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
         hs += tile_hist[idx];
         ps += tile_P[idx];
       }
+    // top-2: second choices, counted and prefixed the same way
+    int hs2 = 0;
+    if (tile_hist2 && ev)
+      for (int j = j0; j < j1; ++j) hs2 += tile_hist2[((size_t)g * nT + j) * E + e];
     sh_h[warp][lane] = hs;
+    sh_h2[warp][lane] = hs2;
     sh_p[warp][lane] = ps;
     __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += sh_h[w][lane];
+    int base = 0, base2 = 0;
+    for (int w = 0; w < warp; ++w) {
+      base += sh_h[w][lane];
+      base2 += sh_h2[w][lane];
+    }
     if (ev)
       for (int j = j0; j < j1; ++j) {
         const size_t idx = ((size_t)g * nT + j) * E + e;
         tile_base[idx] = base;
         base += tile_hist[idx];
+        if (tile_hist2) {
+          tile_base2[idx] = base2;
+          base2 += tile_hist2[idx];
+        }
       }
     if (warp == 0) {
-      int tot = 0;
+      int tot = 0, tot2 = 0;
       float psum = 0.f;
       for (int w = 0; w < SCAN_WARPS; ++w) {
         tot += sh_h[w][lane];
+        tot2 += sh_h2[w][lane];
         psum += sh_p[w][lane];
       }
       float contrib = 0.f;
@@ -233,6 +356,12 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
         P[ge] = Pv;
         group_off[ge] = rows_run;
         rows_run += acc;
+        if (tile_hist2) {  // second choices fill what the kept first choices leave
+          const int acc2 = min(tot2, max(C - acc, 0));
+          raw2[ge] = tot2;
+          accepted2[ge] = acc2;
+          rows_run += acc2;
+        }
         contrib = (float)tot * Pv;
       }
       contrib = warp_sum(contrib);
@@ -303,12 +432,81 @@ __global__ void __launch_bounds__(256) route_slots_kernel(
   row[t] = r;
 }
 
+// top-2: slots of both choices.  A first choice is numbered among the group's first
+// choices of its expert; a second choice after that expert's kept first choices, among
+// the group's second choices.  Rows: group_off + slot (kept first choices, then kept
+// second choices, in each expert's block of the group).
+__global__ void __launch_bounds__(256) route_slots_top2_kernel(
+    const int32_t* __restrict__ expert, const int32_t* __restrict__ expert2, const int32_t* __restrict__ tile_base,
+    const int32_t* __restrict__ tile_base2, const int32_t* __restrict__ group_off,
+    const int32_t* __restrict__ accepted, long long N, int T, int E, int nT, int C, int R,
+    int32_t* __restrict__ slot, int32_t* __restrict__ slot2, uint8_t* __restrict__ keep, uint8_t* __restrict__ keep2,
+    int32_t* __restrict__ row, int32_t* __restrict__ row2, int32_t* __restrict__ tok_of_row, bool debug,
+    uint32_t* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (t >= N) return;
+  const int g = (int)(t / T);
+  const int ti = (int)(t - (long long)g * T);
+  const size_t tb = ((size_t)g * nT + ti / ROUTE_TILE) * E;
+  for (int k = 0; k < 2; ++k) {
+    const int e = k ? expert2[t] : expert[t];
+    int32_t* sl = k ? slot2 : slot;
+    uint8_t* kp = k ? keep2 : keep;
+    int32_t* rw = k ? row2 : row;
+    if (e < 0 || e >= E) {  // the router never writes one; keep every access in bounds regardless
+      raise_error(err, ERR_BOUNDS);
+      sl[t] = 0;
+      kp[t] = 0;
+      rw[t] = -1;
+      continue;
+    }
+    const int s = k ? accepted[(size_t)g * E + e] + tile_base2[tb + e] + sl[t] : tile_base[tb + e] + sl[t];
+    const bool kept = s < C;
+    int r = -1;
+    if (kept) {
+      r = group_off[(size_t)g * E + e] + s;
+      if (r < 0 || r >= R) {
+        if (debug) raise_error(err, ERR_BOUNDS);
+        r = -1;
+      } else {
+        tok_of_row[(size_t)e * R + r] = (int32_t)t;
+      }
+    }
+    sl[t] = s;
+    kp[t] = r >= 0 ? 1 : 0;
+    rw[t] = r;
+  }
+}
+
 // ---------------------------------------------------------------- launcher
 int launch_route(const RouteArgs& a, cudaStream_t s) {
   const long long N = (long long)a.G * a.T;
   const int nT = (a.T + ROUTE_TILE - 1) / ROUTE_TILE;
   int launches = 0;
-  if (N > 0) {
+  if (N > 0 && a.top2) {
+    // top-2: float32 logits from the router (tensor cores for bf16 x: its own top-1
+    // outputs are overwritten below), then the per-tile top-2 pass
+    if (a.x_bf16) {
+      RouteArgs b = a;
+      b.logits_out = a.logits;
+      const int n = launch_router_tc(b, a.slot, s);
+      if (n < 0) return -1;
+      launches += n;
+    } else {
+      dim3 grid((a.E + RL_BN - 1) / RL_BN, (unsigned)((N + RL_BM - 1) / RL_BM));
+      if (launch_k(router_logits_kernel<float>, grid, dim3(256), 0, s, false, 1, (const float*)a.x, a.Wr, a.br,
+                   a.logits, (int)N, a.d, a.E) != cudaSuccess)
+        return -1;
+      ++launches;
+    }
+    if (launch_k(route_top2_kernel, dim3(nT, a.G), dim3(256), 2 * a.E * sizeof(int32_t), s, true, 1,
+                 (const float*)a.logits, a.T, a.E, nT, a.expert, a.expert2, a.gate, a.gate2, a.slot, a.slot2,
+                 a.tile_hist, a.tile_hist2, a.tile_P, a.tile_Z, a.probs, a.err) != cudaSuccess)
+      return -1;
+    ++launches;
+  } else if (N > 0) {
     if (a.x_bf16) {
       const int n = launch_router_tc(a, a.slot, s);
       if (n < 0) return -1;
@@ -327,12 +525,19 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   // tokens it is the first kernel of the call.
   const int scan_grid = route_scan_blocks(a.E) + ((a.z_g || a.z) ? 1 : 0);
   if (launch_k(route_scan_kernel, dim3(scan_grid), dim3(SCAN_WARPS * 32), 0, s, N > 0, 1, a.tile_hist,
-               a.tile_P, (const float*)a.tile_Z, a.G, a.T, a.E, nT, a.C, a.alpha, a.tile_base, a.raw, a.accepted,
-               a.P, a.group_off, a.expert_rows, a.balance, a.aux_g, a.aux, a.z_g, a.z, a.scan_partial,
-               a.scan_counter) != cudaSuccess)
+               a.tile_P, (const float*)a.tile_Z, a.top2 ? (const int32_t*)a.tile_hist2 : nullptr, a.G, a.T, a.E, nT,
+               a.C, a.alpha, a.tile_base, a.top2 ? a.tile_base2 : nullptr, a.raw, a.accepted,
+               a.top2 ? a.raw2 : nullptr, a.top2 ? a.accepted2 : nullptr, a.P, a.group_off, a.expert_rows,
+               a.balance, a.aux_g, a.aux, a.z_g, a.z, a.scan_partial, a.scan_counter) != cudaSuccess)
     return -1;
   ++launches;
-  if (N > 0 && a.slots) {
+  if (N > 0 && a.top2) {
+    if (launch_k(route_slots_top2_kernel, dim3((unsigned)((N + 255) / 256)), dim3(256), 0, s, true, 1, a.expert,
+                 a.expert2, a.tile_base, a.tile_base2, a.group_off, a.accepted, N, a.T, a.E, nT, a.C, a.R, a.slot,
+                 a.slot2, a.keep, a.keep2, a.row, a.row2, a.tok_of_row, a.debug, a.err) != cudaSuccess)
+      return -1;
+    ++launches;
+  } else if (N > 0 && a.slots) {
     if (launch_k(route_slots_kernel, dim3((unsigned)((N + 255) / 256)), dim3(256), 0, s, true, 1, a.expert,
                  a.tile_base, a.group_off, N, a.T, a.E, nT, a.C, a.R, a.slot, a.keep, a.row, a.tok_of_row, a.debug,
                  a.err) != cudaSuccess)

@@ -44,6 +44,14 @@ class RouteResult:
     logits: Optional[torch.Tensor] = None  # [N, E] float32
     z_loss_per_group: Optional[torch.Tensor] = None  # [G] float32, router z-loss (unweighted)
     z_loss: Optional[torch.Tensor] = None            # [1] float32, mean over groups
+    # top-2 routing only: the second choices
+    expert2: Optional[torch.Tensor] = None           # [N] int32
+    slot2: Optional[torch.Tensor] = None             # [N] int32
+    keep2: Optional[torch.Tensor] = None             # [N] uint8
+    gate2: Optional[torch.Tensor] = None             # [N] float32
+    row2: Optional[torch.Tensor] = None              # [N] int32
+    raw2_count: Optional[torch.Tensor] = None        # [G, E] int32
+    accepted2_count: Optional[torch.Tensor] = None   # [G, E] int32
 
     def c_struct(self) -> SwitchRouteOut:
         return SwitchRouteOut(*[_ptr(getattr(self, n)) for n in _lib.ROUTE_FIELDS])
@@ -55,14 +63,18 @@ class SwitchMoE:
     def __init__(self, G: int, T: int, d_model: int, d_ff: int, E: int, capacity_factor: float = 1.0, *,
                  dtype: torch.dtype = torch.bfloat16, alpha: float = 0.01, capacity_override: int = 0,
                  write_probs: bool = False, write_logits: bool = False, debug_bounds: bool = False,
-                 profile: bool = False, device=None):
+                 profile: bool = False, top_k: int = 1, device=None):
         self.lib = _lib.load()
         if dtype not in (torch.bfloat16, torch.float32):
             raise ValueError("dtype must be torch.bfloat16 or torch.float32")
         self.dtype = dtype
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         flags = ((_lib.FLAG_WRITE_PROBS if write_probs else 0) | (_lib.FLAG_WRITE_LOGITS if write_logits else 0)
-                 | (_lib.FLAG_DEBUG_BOUNDS if debug_bounds else 0) | (_lib.FLAG_PROFILE if profile else 0))
+                 | (_lib.FLAG_DEBUG_BOUNDS if debug_bounds else 0) | (_lib.FLAG_PROFILE if profile else 0)
+                 | (_lib.FLAG_TOP2 if top_k == 2 else 0))
+        if top_k not in (1, 2):
+            raise ValueError("top_k must be 1 or 2")
+        self.top_k = top_k
         self.cfg = SwitchConfig(G, T, d_model, d_ff, E, float(capacity_factor), int(capacity_override),
                                 float(alpha), _lib.SWITCH_BF16 if dtype == torch.bfloat16 else _lib.SWITCH_F32,
                                 flags)
@@ -103,7 +115,12 @@ class SwitchMoE:
             expert_rows=torch.empty(E, dtype=i32, device=dev),
             probs=torch.empty(N, E, dtype=f32, device=dev) if self.write_probs else None,
             logits=torch.empty(N, E, dtype=f32, device=dev) if self.write_logits else None,
-            z_loss_per_group=torch.empty(G, dtype=f32, device=dev), z_loss=torch.empty(1, dtype=f32, device=dev))
+            z_loss_per_group=torch.empty(G, dtype=f32, device=dev), z_loss=torch.empty(1, dtype=f32, device=dev),
+            **({} if self.top_k == 1 else dict(
+                expert2=torch.empty(N, dtype=i32, device=dev), slot2=torch.empty(N, dtype=i32, device=dev),
+                keep2=torch.empty(N, dtype=torch.uint8, device=dev), gate2=torch.empty(N, dtype=f32, device=dev),
+                row2=torch.empty(N, dtype=i32, device=dev), raw2_count=torch.empty(G, E, dtype=i32, device=dev),
+                accepted2_count=torch.empty(G, E, dtype=i32, device=dev))))
 
     def alloc_expert_buffer(self, width: Optional[int] = None) -> torch.Tensor:
         return torch.empty(self.E, self.block_rows, width or self.d_model, dtype=self.dtype, device=self.device)

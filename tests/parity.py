@@ -159,3 +159,89 @@ def check_y(y: torch.Tensor, ref: so.Route, outs: dict, tokens: np.ndarray, resi
             err = np.linalg.norm(got - dref)
             assert err <= ROW_REL_L2 * np.linalg.norm(dref) + 1e-30, \
                 f"token {t}: y rel L2 {err / np.linalg.norm(dref):.3e}"
+
+
+# ----------------------------------------------------------------------------- top-2 routing
+
+def top3_near_ties(z: np.ndarray, eps: float) -> np.ndarray:
+    """Tokens whose first/second or second/third highest logits lie within eps: rounding
+    can swap the two choices' order or change the second choice there."""
+    s = -np.sort(-z, axis=1)
+    gap = s[:, 0] - s[:, 1]
+    if z.shape[1] >= 3:
+        gap = np.minimum(gap, s[:, 1] - s[:, 2])
+    return gap < eps
+
+
+def oracle_route_top2(inp, shape, gpu_logits: np.ndarray):
+    """Oracle top-2 routing; groups with a near tie among a token's top three logits (GPU or
+    oracle) are routed from the GPU's own float32 logits."""
+    x = to_np(inp["x"])
+    Wr = to_np(inp["Wr"])
+    br = to_np(inp["br"]) if inp["br"] is not None else None
+    r = so.route_top2(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor,
+                      capacity_override=shape.capacity_override)
+    subst = []
+    if shape.N > 0:
+        near = top3_near_ties(gpu_logits, TIE_EPS) | top3_near_ties(r.logits, TIE_EPS)
+        subst = sorted({int(t) // shape.T for t in np.flatnonzero(near)})
+        if subst:
+            over = {g: gpu_logits[g * shape.T:(g + 1) * shape.T] for g in subst}
+            r = so.route_top2(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor,
+                              capacity_override=shape.capacity_override, logits_override=over)
+    return r, subst
+
+
+def compare_route_top2(g, ref: so.Route2, shape):
+    G, E = shape.G, shape.E
+    for name, want in (("expert", ref.expert), ("expert2", ref.expert2), ("slot", ref.slot), ("slot2", ref.slot2),
+                       ("row", ref.row), ("row2", ref.row2)):
+        assert np.array_equal(to_np(getattr(g, name)).astype(np.int64), want), name
+    assert np.array_equal(to_np(g.keep).astype(bool), ref.keep), "keep"
+    assert np.array_equal(to_np(g.keep2).astype(bool), ref.keep2), "keep2"
+    for name, want in (("raw_count", ref.raw), ("accepted_count", ref.accepted), ("raw2_count", ref.raw2),
+                       ("accepted2_count", ref.accepted2)):
+        assert np.array_equal(to_np(getattr(g, name)).reshape(G, E).astype(np.int64), want), name
+    assert np.array_equal(to_np(g.expert_rows).astype(np.int64), ref.expert_rows), "expert rows"
+    if shape.N > 0:
+        rel_close(to_np(g.gate), ref.gate, what="gate")
+        rel_close(to_np(g.gate2), ref.gate2, what="gate2")
+        rel_close(to_np(g.P).reshape(G, E), ref.P, what="P")
+        rel_close(to_np(g.balance), ref.balance, what="balance")
+        rel_close(to_np(g.aux_loss)[0], ref.aux_loss, what="aux loss")
+        rel_close(to_np(g.z_loss_per_group), ref.z_per_group, what="z-loss per group")
+
+
+def check_dispatch_top2(xe: torch.Tensor, x: torch.Tensor, ref: so.Route2):
+    for ex, kp, rw in ((ref.expert, ref.keep, ref.row), (ref.expert2, ref.keep2, ref.row2)):
+        kept = np.flatnonzero(kp)
+        if kept.size:
+            e = torch.as_tensor(ex[kept], device=xe.device)
+            r = torch.as_tensor(rw[kept], device=xe.device)
+            assert torch.equal(xe[e, r], x[torch.as_tensor(kept, device=xe.device)]), "dispatched rows differ from x"
+    rows = torch.as_tensor(ref.expert_rows, device=xe.device)
+    idx = torch.arange(xe.shape[1], device=xe.device)[None, :]
+    assert (xe[idx >= rows[:, None]] == 0).all(), "rows past the expert count are not zero"
+
+
+def check_y_top2(y: torch.Tensor, ref: so.Route2, inp, tokens: np.ndarray, resid: torch.Tensor | None = None):
+    """y against the oracle's weighted pair of fp64 expert outputs (the elementwise bound, and
+    a per-token relative L2 bound where some choice was kept and there is no residual)."""
+    xs = {k: (to_np(v) if v is not None else None) for k, v in inp.items() if k in ("W1", "b1", "W2", "b2")}
+    outs = so.expert_outputs_top2(to_np(inp["x"]), ref, xs["W1"], xs["b1"], xs["W2"], xs["b2"], tokens)
+    yref_all = so.combine_top2(ref, outs, tokens, y.shape[1])
+    yt = to_np(y[torch.as_tensor(tokens, device=y.device)])
+    base = to_np(resid[torch.as_tensor(tokens, device=y.device)]) if resid is not None else None
+    for i, t in enumerate(tokens):
+        yref = yref_all[i] + (base[i] if base is not None else 0.0)
+        got = yt[i]
+        any_kept = ref.keep[t] or ref.keep2[t]
+        if not any_kept and resid is None:
+            assert (got == 0).all(), f"token {t} with both choices dropped has non-zero output"
+            continue
+        bad = np.abs(got - yref) > Y_ATOL + Y_RTOL * np.abs(yref)
+        assert not bad.any(), f"token {t}: y outside |y-y_ref| <= 1e-2 + 1e-2|y_ref|"
+        if any_kept and resid is None:
+            err = np.linalg.norm(got - yref)
+            assert err <= ROW_REL_L2 * np.linalg.norm(yref) + 1e-30, \
+                f"token {t}: y rel L2 {err / np.linalg.norm(yref):.3e}"

@@ -110,3 +110,12 @@ def test_status_strings(lib):
     from sparse_mixture_experts_slots_b300 import SwitchError
     e = SwitchError(1, "x")
     assert "invalid argument" in str(e)
+
+
+def test_top2_capacity_and_config(lib):
+    from sparse_mixture_experts_slots_b300._lib import FLAG_TOP2, SwitchConfig
+    for (c, T, E) in [(1.0, 64, 4), (1.25, 4096, 64), (1.1, 100, 10), (0.5, 7, 3)]:
+        cfg = SwitchConfig(1, T, 128, 256, E, c, 0, 0.01, 1, FLAG_TOP2)
+        assert lib.switch_capacity(ctypes.byref(cfg)) == so.capacity(2 * c, T, E)
+    one = SwitchConfig(1, 64, 128, 256, 1, 1.0, 0, 0.01, 1, FLAG_TOP2)  # top-2 needs two experts
+    assert lib.switch_capacity(ctypes.byref(one)) == -1

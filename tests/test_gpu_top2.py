@@ -1,0 +1,87 @@
+"""GPU parity of the top-2 variant (SWITCH_FLAG_TOP2) against the fp64 oracle's route_top2.
+
+Both choices, their weights, slots (second choices after the expert's kept first choices),
+keep flags, rows, counts and statistics; the dispatched rows of both choices; y = the
+weighted pair of expert outputs.  Shapes take both FFN paths, ragged tiles, several groups,
+crowded experts (second choices dropped) and the 混合专家 page's 16-expert, 48-wide router.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from gen import LayerShape, WORKLOADS, make_inputs, workload_seed
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+CASES = {
+    "top2-tc": (LayerShape("top2-tc", 2, 300, 256, 384, 8, 1.0), dict(expert_bias_std=0.05, router_bias_std=0.1)),
+    # the page's demo router: 16 experts over 48 inputs, two chosen (float32, CUDA-core FFN)
+    "top2-page-fp32": (dataclasses.replace(WORKLOADS["tiny-e16-fp32"], name="top2-page-fp32", T=200, G=2),
+                       dict(expert_bias_std=0.05)),
+    # a strong bias on expert 0: many first and second choices dropped
+    "top2-crowded": (LayerShape("top2-crowded", 1, 500, 128, 256, 6, 0.5), dict(router_bias_std=0.8)),
+    "top2-many-experts": (LayerShape("top2-many-experts", 1, 700, 128, 128, 300, 1.0), {}),
+    # two 128-row weight blocks per FFN tile, 256-row token chunks
+    "top2-two-blocks": (LayerShape("top2-two-blocks", 1, 600, 256, 512, 4, 1.0), dict(expert_bias_std=0.05)),
+}
+
+
+def _run(shape, inp, resid=False):
+    layer = P.make_layer(shape, top_k=2, write_logits=True, debug_bounds=True)
+    r = layer.route(inp["x"], inp["Wr"], inp["br"])
+    xe = layer.dispatch(inp["x"], r)
+    ye = layer.expert_ffn(xe, inp["W1"], inp["b1"], inp["W2"], inp["b2"], r.expert_rows)
+    y = layer.combine(ye, r, inp["x"] if resid else None)
+    y2, r2 = layer.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"],
+                           inp["x"] if resid else None)
+    layer.sync_status()
+    torch.cuda.synchronize()
+    return layer, r, xe, y, y2, r2
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_top2_against_oracle(name):
+    shape, kw = CASES[name]
+    inp = make_inputs(shape, 7, "cuda", **kw)
+    layer, r, xe, y, y2, r2 = _run(shape, inp)
+    assert layer.C == P.so.capacity(2 * shape.capacity_factor, shape.T, shape.E)
+    ref, subst = P.oracle_route_top2(inp, shape, P.to_np(r.logits))
+    P.compare_route_top2(r, ref, shape)
+    P.compare_route_top2(r2, ref, shape)
+    P.check_dispatch_top2(xe, inp["x"], ref)
+    P.check_y_top2(y, ref, inp, np.arange(shape.N))
+    assert torch.equal(y, y2), "forward differs from the stage-by-stage calls"
+    if name == "top2-crowded":
+        assert (~ref.keep2).sum() > 0 and (~ref.keep).sum() > 0
+
+
+def test_top2_residual():
+    shape, kw = CASES["top2-tc"]
+    inp = make_inputs(shape, 13, "cuda", **kw)
+    layer, r, xe, y, y2, r2 = _run(shape, inp, resid=True)
+    ref, _ = P.oracle_route_top2(inp, shape, P.to_np(r.logits))
+    P.check_y_top2(y, ref, inp, np.arange(shape.N), resid=inp["x"])
+    assert torch.equal(y, y2)
+
+
+def test_top2_switch_base_full_size():
+    name = "switch-base-e128"
+    shape = WORKLOADS[name]
+    inp = make_inputs(shape, workload_seed(name), "cuda")
+    layer = P.make_layer(shape, top_k=2, write_logits=True)
+    y, r = layer.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"])
+    layer.sync_status()
+    ref, _ = P.oracle_route_top2(inp, shape, P.to_np(r.logits))
+    P.compare_route_top2(r, ref, shape)
+    tokens = np.sort(np.random.default_rng(1).choice(shape.N, 192, replace=False))
+    P.check_y_top2(y, ref, inp, tokens)
