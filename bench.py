@@ -137,9 +137,10 @@ def traffic_from_profiles(kernel: str):
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
-def oracle_sample(shape, inp, n_ffn_tokens: int):
+def oracle_sample(shape, inp, n_ffn_tokens: int, top_k: int = 1):
     """Time the fp64 oracle: routing of the whole batch + the expert FFN of a
-    sample of kept tokens, scaled to the batch.  Returns (tokens/s, detail)."""
+    sample of kept tokens (kept (token, choice) requests with top-2), scaled to the
+    batch.  Returns (tokens/s, detail)."""
     from oracle import switch_oracle as so
     try:
         from threadpoolctl import threadpool_info
@@ -150,25 +151,35 @@ def oracle_sample(shape, inp, n_ffn_tokens: int):
     Wr = inp["Wr"].cpu().numpy().astype(np.float64)
     br = None if inp["br"] is None else inp["br"].cpu().numpy().astype(np.float64)
     t0 = time.perf_counter()
-    r = so.route(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor)
+    if top_k == 2:
+        r = so.route_top2(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor)
+        req_e = np.concatenate([r.expert[r.keep], r.expert2[r.keep2]])  # kept (token, choice) requests
+        req_t = np.concatenate([np.flatnonzero(r.keep), np.flatnonzero(r.keep2)])
+        req_g = np.concatenate([r.gate[r.keep], r.gate2[r.keep2]])
+    else:
+        r = so.route(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor)
+        req_t = np.flatnonzero(r.keep)
+        req_e = r.expert[req_t]
+        req_g = r.gate[req_t]
     t_route = time.perf_counter() - t0
-    kept = np.flatnonzero(r.keep)
     rng = np.random.default_rng(0)
-    sample = np.sort(rng.choice(kept, size=min(n_ffn_tokens, kept.size), replace=False))
-    experts = np.unique(r.expert[sample])
+    pick = np.sort(rng.choice(req_t.size, size=min(n_ffn_tokens, req_t.size), replace=False))
+    kept = req_t  # the requests the FFN serves
+    sample = pick
+    experts = np.unique(req_e[pick])
     W1 = {int(e): inp["W1"][int(e)].float().cpu().numpy().astype(np.float64) for e in experts}
     W2 = {int(e): inp["W2"][int(e)].float().cpu().numpy().astype(np.float64) for e in experts}
     t0 = time.perf_counter()
     for e in experts:
-        ts = sample[r.expert[sample] == e]
-        o = so.expert_ffn(x[ts], W1[int(e)], None, W2[int(e)], None)
-        _ = r.gate[ts, None] * o
+        sel = pick[req_e[pick] == e]
+        o = so.expert_ffn(x[req_t[sel]], W1[int(e)], None, W2[int(e)], None)
+        _ = req_g[sel, None] * o
     t_ffn = time.perf_counter() - t0
     t_total = t_route + t_ffn * kept.size / max(1, sample.size)
     return shape.N / t_total, {
         "cores": threads,
         "sample": (f"routing of all {shape.N} tokens + expert FFN/combine of {sample.size} of {kept.size} kept "
-                   f"tokens, FFN time scaled by {kept.size}/{sample.size}"),
+                   f"{'requests' if top_k == 2 else 'tokens'}, FFN time scaled by {kept.size}/{sample.size}"),
         "t_route_s": t_route, "t_ffn_sample_s": t_ffn}
 
 
@@ -180,7 +191,7 @@ def run_reference(args, shape):
     vals = []
     detail = {}
     for i in range(args.warmup + args.steps):
-        v, detail = oracle_sample(shape, inp, args.ref_ffn_tokens)
+        v, detail = oracle_sample(shape, inp, args.ref_ffn_tokens, args.top_k)
         if i >= args.warmup:
             vals.append(v)
     value = float(np.mean(vals))
@@ -199,7 +210,7 @@ def run_reference(args, shape):
 
 def config_of(shape, args):
     return {"workload": shape.name, "G": shape.G, "T": shape.T, "d_model": shape.d_model, "d_ff": shape.d_ff,
-            "E": shape.E, "capacity_factor": shape.capacity_factor, "top_k": 1,
+            "E": shape.E, "capacity_factor": shape.capacity_factor, "top_k": getattr(args, "top_k", 1),
             "global_batch_tokens": shape.N * args.gpus, "parallelism": f"replicas{args.gpus}",
             "l2": "flushed (256 MB write) before every timed step; expert weights (>1 GB) exceed L2 anyway"}
 
@@ -227,7 +238,7 @@ def run_gpu(args, shape):
         inp["x"] = make_inputs(shape, seed + 7919 * rank, dev, with_experts=False)["x"]
     dt = torch.float32 if shape.dtype == "f32" else torch.bfloat16
     mk = lambda prof: SwitchMoE(shape.G, shape.T, shape.d_model, shape.d_ff, shape.E, shape.capacity_factor,
-                                dtype=dt, profile=prof, device=dev)
+                                dtype=dt, profile=prof, top_k=args.top_k, device=dev)
     layer = mk(False)
     r = layer.alloc_route()
     y = torch.empty(shape.N, shape.d_model, dtype=dt, device=dev)
@@ -337,7 +348,7 @@ def run_gpu(args, shape):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if shape.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": config_of(shape, argparse.Namespace(gpus=world)),
+        "config": config_of(shape, argparse.Namespace(gpus=world, top_k=args.top_k)),
         "roofline": ({"bound": "tensor", "kernel": kern, "achieved": tflops, "peak": tc_burst, "unit": "TFLOP/s",
                       "frac": tflops / tc_burst, "peak_source": f"{peak_src} bf16_tflops (cuBLAS bf16 GEMM, burst)",
                       "frac_of_sustained": tflops / tc_sust, "algorithmic_flops_per_launch": work["ffn_flops"]}
@@ -369,7 +380,7 @@ def run_gpu(args, shape):
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world == 1:
-        v, det = oracle_sample(shape, inp, args.ref_ffn_tokens)
+        v, det = oracle_sample(shape, inp, args.ref_ffn_tokens, args.top_k)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": det["cores"], "kind": "oracle",
                                 "sample": det["sample"]}
     print(json.dumps(line), flush=True)
@@ -387,6 +398,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--ref-ffn-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--top-k", type=int, default=1, choices=[1, 2],
+                    help="2: the top-2 variant (weights = softmax over the two highest scores)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     shape = WORKLOADS[args.workload]
