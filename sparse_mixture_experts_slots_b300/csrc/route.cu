@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(256) route_softmax_kernel(
 }
 
 // ---------------------------------------------------------------- 2b. top-2 per tile (from float32 logits)
-// grid (nT, G), 256 threads; dynamic smem: hist[E], hist2[E] ints.  Per token: the two
+// grid (nT, G), 512 threads; dynamic smem: hist[E], hist2[E] ints, then the column pass's
+// partial sums [ceil(512 / E)][E] floats.  Per token: the two
 // highest logits (ties to the lower index), their weights = softmax over the two, the
 // full softmax's column sums (P), (log sum exp z)^2, and the in-tile ranks of both
 // choices among the tile's first / second choices (into rank[] / rank2[]).
@@ -160,7 +161,9 @@ __device__ __forceinline__ bool top_before(float v, int i, float w, int j) {
   return v > w || (v == w && i < j);  // (v, i) ranks before (w, j)
 }
 
-__global__ void __launch_bounds__(256) route_top2_kernel(
+constexpr int TOP2_THREADS = 512;
+
+__global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
     const float* __restrict__ z, int T, int E, int nT, int32_t* __restrict__ expert, int32_t* __restrict__ expert2,
     float* __restrict__ gate, float* __restrict__ gate2, int32_t* __restrict__ rank, int32_t* __restrict__ rank2,
     int32_t* __restrict__ tile_hist, int32_t* __restrict__ tile_hist2, float* __restrict__ tile_P,
@@ -245,14 +248,26 @@ __global__ void __launch_bounds__(256) route_top2_kernel(
     rank[tok0 + i] = r;
     rank2[tok0 + i] = r2;
   }
+  // Column pass: (expert, token chunk) per thread, chunk sums combined in a fixed order.
   const size_t tbase = ((size_t)g * nT + tile) * E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  float* part = reinterpret_cast<float*>(hist + 2 * E);
+  const int nch = E >= (int)blockDim.x ? 1 : (int)blockDim.x / E;
+  const int clen = (len + nch - 1) / nch;
+  for (int k = threadIdx.x; k < E * nch; k += blockDim.x) {
+    const int e = k % E, c = k / E;
     float acc = 0.f;
-    for (int i = 0; i < len; ++i) {
+    const int i1 = min(len, (c + 1) * clen);
+    for (int i = c * clen; i < i1; ++i) {
       const float p = expf(z[(tok0 + i) * E + e] - m_s[i]) / s_s[i];
       acc += p;
       if (probs) probs[(tok0 + i) * E + e] = p;
     }
+    part[c * E + e] = acc;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float acc = 0.f;
+    for (int c = 0; c < nch; ++c) acc += part[c * E + e];
     tile_P[tbase + e] = acc;
     tile_hist[tbase + e] = hist[e];
     tile_hist2[tbase + e] = hist2[e];
@@ -501,7 +516,9 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
         return -1;
       ++launches;
     }
-    if (launch_k(route_top2_kernel, dim3(nT, a.G), dim3(256), 2 * a.E * sizeof(int32_t), s, true, 1,
+    const int nch = a.E >= TOP2_THREADS ? 1 : TOP2_THREADS / a.E;
+    if (launch_k(route_top2_kernel, dim3(nT, a.G), dim3(TOP2_THREADS),
+                 2 * a.E * sizeof(int32_t) + (size_t)nch * a.E * sizeof(float), s, true, 1,
                  (const float*)a.logits, a.T, a.E, nT, a.expert, a.expert2, a.gate, a.gate2, a.slot, a.slot2,
                  a.tile_hist, a.tile_hist2, a.tile_P, a.tile_Z, a.probs, a.err) != cudaSuccess)
       return -1;

@@ -337,7 +337,21 @@ __global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
         v[ch * 16 + j] = z;
         if (e0 + c < E) {
           if (z > m) { m = z; a = e0 + c; }
-          if (logits && valid) logits[tok * E + e0 + c] = z;
+        }
+      }
+      if (logits && valid) {  // the chunk's 16 logits of this token: 16-byte stores when aligned
+        const int c0 = e0 + cbeg + ch * 16;
+        float* dst = logits + tok * E + c0;
+        if ((E & 3) == 0 && c0 + 16 <= E) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<float4*>(dst + 4 * q4) =
+                make_float4(v[ch * 16 + 4 * q4], v[ch * 16 + 4 * q4 + 1], v[ch * 16 + 4 * q4 + 2],
+                            v[ch * 16 + 4 * q4 + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < E) dst[j] = v[ch * 16 + j];
         }
       }
     }
