@@ -471,3 +471,71 @@ def expert_outputs_top2(x, r: Route2, W1, b1, W2, b2, tokens: Optional[Sequence[
             for i, t in enumerate(sel):
                 out[(int(t), int(e))] = o[i]
     return out
+
+
+# ----------------------------------------------------------------------------- backward (top-1)
+
+def backward(x, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor: float, dy,
+             w_aux: float = 0.0, w_z: float = 0.0, alpha: float = 1e-2, capacity_override: int = 0,
+             residual: bool = False) -> dict:
+    """Gradients of L = sum(dy * y) + w_aux * aux_loss + w_z * z_loss for the top-1 layer.
+
+    The choice, the slots and the capacity mask are held fixed (they are piecewise
+    constant): the router gets its gradient through the selected expert's probability g_t =
+    p_{t,e*} [card, 方法适配: the gate probability keeps the router differentiable] and
+    through P in the aux loss, not through the hard counts f [070, 核心思想与公式]; the
+    z-loss adds d(lse_t^2)/dz = 2 lse_t p_t [070, 核心思想与公式].  With several groups the
+    aux and z losses are means over groups.  Returns float64 arrays: dx [N, d], dWr [E, d],
+    dbr [E], dW1 [E, F, d], db1 [E, F], dW2 [E, d, F], db2 [E, d].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    Wr = np.asarray(Wr, dtype=np.float64)
+    W1 = np.asarray(W1, dtype=np.float64)
+    W2 = np.asarray(W2, dtype=np.float64)
+    N, d = x.shape
+    F = W1.shape[1]
+    r = route(x, Wr, br, G, T, E, capacity_factor, alpha, capacity_override)
+    p = r.probs
+    dx = dy.copy() if residual else np.zeros_like(x)
+    dW1 = np.zeros_like(W1)
+    dW2 = np.zeros_like(W2)
+    db1 = np.zeros((E, F))
+    db2 = np.zeros((E, d))
+    dg = np.zeros(N)
+    # experts: y_t = g_t * (ReLU(x_t W1^T + b1) W2^T + b2) for kept tokens
+    for e in range(E):
+        ts = np.flatnonzero(r.keep & (r.expert == e))
+        if ts.size == 0:
+            continue
+        xe = x[ts]
+        hpre = xe @ W1[e].T + (0.0 if b1 is None else np.asarray(b1, np.float64)[e])
+        h = np.maximum(hpre, 0.0)
+        o = h @ W2[e].T + (0.0 if b2 is None else np.asarray(b2, np.float64)[e])
+        dg[ts] = np.sum(dy[ts] * o, axis=1)
+        do = r.gate[ts, None] * dy[ts]                 # dL/d(expert output)
+        dW2[e] = do.T @ h
+        db2[e] = do.sum(axis=0)
+        dh = (do @ W2[e]) * (hpre > 0)
+        dW1[e] = dh.T @ xe
+        db1[e] = dh.sum(axis=0)
+        dx[ts] += dh @ W1[e]
+    # router: dL/dp, then the softmax Jacobian, plus the z-loss term on the logits
+    dp = np.zeros_like(p)
+    dp[np.arange(N), r.expert] = dg
+    dz = np.zeros_like(p)
+    for g in range(G):
+        sl = slice(g * T, (g + 1) * T)
+        if T == 0:
+            continue
+        dp[sl] += (w_aux * alpha * E / (G * T)) * r.f[g][None, :]
+        ps = p[sl]
+        dz[sl] = ps * (dp[sl] - np.sum(ps * dp[sl], axis=1, keepdims=True))
+        zg = r.logits[sl]
+        m = zg.max(axis=1, keepdims=True)
+        lse = m + np.log(np.exp(zg - m).sum(axis=1, keepdims=True))
+        dz[sl] += (w_z * 2.0 / (G * T)) * lse * ps
+    dWr = dz.T @ x
+    dbr = dz.sum(axis=0)
+    dx += dz @ Wr
+    return dict(dx=dx, dWr=dWr, dbr=dbr, dW1=dW1, db1=db1, dW2=dW2, db2=db2, route=r)

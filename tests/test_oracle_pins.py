@@ -528,3 +528,76 @@ def test_top2_without_drops_is_the_dense_weighted_pair():
         w = w / w.sum()
         want[t] = w[0] * o[t, e1] + w[1] * o[t, e2]
     np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- backward
+
+def _loss(x, Wr, br, W1, b1, W2, b2, G, T, E, c, dy, w_aux, w_z, residual, fixed):
+    """L = sum(dy * y) + w_aux aux + w_z z for the given parameters, from the oracle's
+    forward pieces; `fixed` (expert, keep) must not change under the perturbation."""
+    r = so.route(x, Wr, br, G, T, E, c)
+    assert (r.expert == fixed[0]).all() and (r.keep == fixed[1]).all(), "a choice flipped"
+    outs = so.expert_outputs(x, r, W1, b1, W2, b2)
+    y = so.combine(r, outs, range(G * T), x.shape[1])
+    if residual:
+        y = y + x
+    return float(np.sum(dy * y)) + w_aux * r.aux_loss + w_z * r.z_loss
+
+
+@pytest.mark.parametrize("G,T,E,c,residual", [(1, 7, 3, 1.0, False), (2, 6, 4, 0.75, True)])
+def test_backward_matches_central_differences(G, T, E, c, residual):
+    # the pages' check: central differences over every parameter, routing unchanged by the step
+    rng = np.random.default_rng(17)
+    d, F = 4, 5
+    x = rng.standard_normal((G * T, d))
+    Wr = rng.standard_normal((E, d))
+    br = rng.standard_normal(E) * 0.3
+    W1 = rng.standard_normal((E, F, d))
+    b1 = rng.standard_normal((E, F)) * 0.3
+    W2 = rng.standard_normal((E, d, F))
+    b2 = rng.standard_normal((E, d)) * 0.3
+    dy = rng.standard_normal((G * T, d))
+    w_aux, w_z = 0.7, 0.3
+    grads = so.backward(x, Wr, br, W1, b1, W2, b2, G, T, E, c, dy, w_aux, w_z, residual=residual)
+    r = grads["route"]
+    assert (~r.keep).any() or c >= 1.0
+    fixed = (r.expert.copy(), r.keep.copy())
+    params = dict(x=x, Wr=Wr, br=br, W1=W1, b1=b1, W2=W2, b2=b2)
+    eps = 1e-6
+    worst = 0.0
+    for name, arr in params.items():
+        num = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            old = arr[i]
+            arr[i] = old + eps
+            lp = _loss(**params, G=G, T=T, E=E, c=c, dy=dy, w_aux=w_aux, w_z=w_z, residual=residual, fixed=fixed)
+            arr[i] = old - eps
+            lm = _loss(**params, G=G, T=T, E=E, c=c, dy=dy, w_aux=w_aux, w_z=w_z, residual=residual, fixed=fixed)
+            arr[i] = old
+            num[i] = (lp - lm) / (2 * eps)
+        ana = grads["d" + name]
+        err = np.max(np.abs(ana - num))
+        worst = max(worst, err)
+        assert err < 1e-6 * max(1.0, np.max(np.abs(num))), f"d{name}: max |analytic - central difference| {err:.3e}"
+    assert worst < 1e-6
+
+
+def test_backward_gate_path_only_reaches_the_chosen_expert():
+    # with w_aux = w_z = 0 the router gradient of a token is p_t * (e_a - p_t) * dg_t: rows sum to 0
+    rng = np.random.default_rng(2)
+    T, E, d, F = 9, 4, 3, 2
+    x = rng.standard_normal((T, d))
+    Wr = rng.standard_normal((E, d))
+    W1 = rng.standard_normal((E, F, d))
+    W2 = rng.standard_normal((E, d, F))
+    dy = rng.standard_normal((T, d))
+    g = so.backward(x, Wr, None, W1, None, W2, None, 1, T, E, 1.0, dy)
+    # softmax Jacobian rows sum to zero, so dbr sums to zero
+    assert abs(g["dbr"].sum()) < 1e-12
+    # experts nobody kept get no weight gradient
+    r = g["route"]
+    for e in range(E):
+        if not (r.keep & (r.expert == e)).any():
+            assert (g["dW1"][e] == 0).all() and (g["dW2"][e] == 0).all()
