@@ -76,6 +76,11 @@ typedef enum { SWITCH_F32 = 0, SWITCH_BF16 = 1 } switch_dtype;
  * choices of the group, in sequence order; f (and raw_count / accepted_count) count first
  * choices; a dropped choice's weight is not moved to the other.  Needs E >= 2. */
 #define SWITCH_FLAG_TOP2          0x10u
+/* Training: switch_forward keeps the dispatched rows, the hidden activations, the
+ * expert outputs and the router logits in the workspace (unfused FFN and combine) for
+ * switch_backward; the workspace grows by float32 gradient scratch (2 E G C d + E G C d_ff
+ * + N + N E floats). */
+#define SWITCH_FLAG_TRAINING      0x20u
 
 typedef struct {
   int G;                   /* routing groups; capacity and statistics are per group */
@@ -219,6 +224,26 @@ SWITCH_API switch_status switch_forward_host(switch_handle h, const void* x_host
                                   const float* br, const void* W1, const void* b1, const void* W2,
                                   const void* b2, const switch_route_out* r, int residual,
                                   void* y_host, float* aux_loss_host, void* done_event, void* stream);
+
+/*
+ * Backward of the top-1 layer (SWITCH_FLAG_TRAINING; top-2 returns
+ * SWITCH_ERR_UNSUPPORTED): float32 gradients of
+ *   L = sum(dy * y) + w_aux * aux_loss + w_z * z_loss
+ * for the inputs of the last switch_forward on this handle, whose route results `r`
+ * (and the workspace's saved activations) it reads.  The choices, slots and capacity
+ * mask are held fixed; the router's gradient flows through the chosen expert's gate
+ * probability (Switch Transformers card, section 方法适配) and through P in the aux loss,
+ * not through the hard counts f (070 page, section 核心思想与公式); the z-loss through the
+ * log-sum-exp.  residual != 0: y included x (dx gets dy too).
+ *   x [N, d] act, Wr [E, d] f32, W1 [E, d_ff, d], W2 [E, d, d_ff] act, dy [N, d] act.
+ *   Outputs (float32, caller-owned): dx [N, d], dWr [E, d], dbr [E], dW1 [E, d_ff, d],
+ *   db1 [E, d_ff], dW2 [E, d, d_ff], db2 [E, d]; dbr, db1, db2 may be NULL.
+ * The matrix products run on CUDA cores (float32 accumulation).
+ */
+SWITCH_API switch_status switch_backward(switch_handle h, const void* x, const float* Wr, const void* W1,
+                              const void* W2, const switch_route_out* r, const void* dy, float w_aux,
+                              float w_z, int residual, float* dx, float* dWr, float* dbr, float* dW1,
+                              float* db1, float* dW2, float* db2, void* stream);
 
 /*
  * Synchronise `stream`, then copy the aux loss, the [G*E] raw and accepted counts

@@ -477,7 +477,7 @@ def expert_outputs_top2(x, r: Route2, W1, b1, W2, b2, tokens: Optional[Sequence[
 
 def backward(x, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor: float, dy,
              w_aux: float = 0.0, w_z: float = 0.0, alpha: float = 1e-2, capacity_override: int = 0,
-             residual: bool = False) -> dict:
+             residual: bool = False, logits_override: Optional[dict] = None) -> dict:
     """Gradients of L = sum(dy * y) + w_aux * aux_loss + w_z * z_loss for the top-1 layer.
 
     The choice, the slots and the capacity mask are held fixed (they are piecewise
@@ -495,7 +495,7 @@ def backward(x, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor:
     W2 = np.asarray(W2, dtype=np.float64)
     N, d = x.shape
     F = W1.shape[1]
-    r = route(x, Wr, br, G, T, E, capacity_factor, alpha, capacity_override)
+    r = route(x, Wr, br, G, T, E, capacity_factor, alpha, capacity_override, logits_override)
     p = r.probs
     dx = dy.copy() if residual else np.zeros_like(x)
     dW1 = np.zeros_like(W1)

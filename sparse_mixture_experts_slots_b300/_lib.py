@@ -27,6 +27,7 @@ FLAG_WRITE_LOGITS = 0x2
 FLAG_DEBUG_BOUNDS = 0x4
 FLAG_PROFILE = 0x8
 FLAG_TOP2 = 0x10
+FLAG_TRAINING = 0x20
 
 
 class SwitchConfig(ctypes.Structure):
@@ -58,6 +59,9 @@ SIGNATURES = {
     "switch_combine": (c_int, [c_void_p, c_void_p, POINTER(SwitchRouteOut), c_void_p, c_void_p, c_void_p]),
     "switch_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, POINTER(SwitchRouteOut), c_void_p, c_void_p, c_void_p]),
+    "switch_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(SwitchRouteOut), c_void_p,
+                                ctypes.c_float, ctypes.c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_void_p, c_void_p, c_void_p, c_void_p]),
     "switch_forward_host": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, POINTER(SwitchRouteOut), c_int, c_void_p, c_void_p, c_void_p,
                                     c_void_p]),

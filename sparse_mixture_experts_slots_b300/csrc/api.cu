@@ -51,6 +51,12 @@ struct switch_layer {
   void* xe;
   void* hbuf;
   void* ye;
+  // backward scratch (SWITCH_FLAG_TRAINING): float32
+  float* bw_dye;  // [E, R, d]
+  float* bw_dh;   // [E, R, F]
+  float* bw_dxe;  // [E, R, d]
+  float* bw_dg;   // [N]
+  float* bw_dz;   // [N, E]
   cudaEvent_t ev[6];
   bool have_events;
   int last_launches;
@@ -62,6 +68,7 @@ namespace {
 constexpr int MAX_E = 2048;
 
 bool top2_of(const switch_config* c) { return (c->flags & SWITCH_FLAG_TOP2) != 0; }
+bool training_of(const switch_config* c) { return (c->flags & SWITCH_FLAG_TRAINING) != 0; }
 
 int64_t capacity_of(const switch_config* c) {
   if (c->capacity_override > 0) return c->capacity_override;
@@ -166,7 +173,8 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_err = take(sizeof(uint32_t) * 4);  // [0] error word, [1] scan counter
   // float32 logits are materialised only by the CUDA-core router (float32 activations)
   const bool two = top2_of(cfg);
-  const size_t o_logits = take(cfg->dtype == SWITCH_F32 || two ? N * E * sizeof(float) : 0);
+  const bool train = training_of(cfg);
+  const size_t o_logits = take(cfg->dtype == SWITCH_F32 || two || train ? N * E * sizeof(float) : 0);
   const size_t o_wsplit = take(cfg->dtype == SWITCH_BF16 ? router_tc_wsplit_bytes(cfg->E, cfg->d_model) : 0);
   const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
   const size_t ffn_words = ffn_counter_words(cfg->E, (int)R, cfg->d_model, cfg->d_ff);
@@ -182,6 +190,11 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_xe = take(E * R * d * h->es);
   const size_t o_h = take(E * R * F * h->es);
   const size_t o_ye = take(E * R * d * h->es);
+  const size_t o_bdye = take(train ? E * R * d * sizeof(float) : 0);
+  const size_t o_bdh = take(train ? E * R * F * sizeof(float) : 0);
+  const size_t o_bdxe = take(train ? E * R * d * sizeof(float) : 0);
+  const size_t o_bdg = take(train ? N * sizeof(float) : 0);
+  const size_t o_bdz = take(train ? N * E * sizeof(float) : 0);
   h->ws_bytes = off;
   if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -206,6 +219,11 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->xe = h->ws + o_xe;
   h->hbuf = h->ws + o_h;
   h->ye = h->ws + o_ye;
+  h->bw_dye = reinterpret_cast<float*>(h->ws + o_bdye);
+  h->bw_dh = reinterpret_cast<float*>(h->ws + o_bdh);
+  h->bw_dxe = reinterpret_cast<float*>(h->ws + o_bdxe);
+  h->bw_dg = reinterpret_cast<float*>(h->ws + o_bdg);
+  h->bw_dz = reinterpret_cast<float*>(h->ws + o_bdz);
   if (cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess) {
     cudaFree(h->ws);
     delete h;
@@ -262,7 +280,8 @@ static switch_status route_args(switch_handle h, const void* x, const float* Wr,
   a->debug = (c.flags & SWITCH_FLAG_DEBUG_BOUNDS) != 0;
   a->slots = true;
   a->logits = want_logits ? out->logits : h->logits;
-  a->logits_out = want_logits ? out->logits : nullptr;
+  // training: the backward needs the logits, so the tensor-core router writes them too
+  a->logits_out = want_logits ? out->logits : (training_of(&c) ? h->logits : nullptr);
   a->wsplit = h->wsplit;
   a->tile_hist = h->tile_hist;
   a->tile_P = h->tile_P;
@@ -423,14 +442,18 @@ switch_status switch_forward(switch_handle h, const void* x, const float* Wr, co
   RouteArgs a{};
   switch_status st = route_args(h, x, Wr, br, r, &a);
   if (st != SWITCH_OK) return st;
-  if (a.top2) {
+  if (a.top2 || training_of(&h->cfg)) {
     // top-2: routing with its slots, one dispatch pass for both choices, the FFN into ye,
-    // and a combine that adds the two weighted outputs per token
+    // and a combine that adds the two weighted outputs per token.  Training (top-1 or
+    // top-2) takes the same unfused path, so xe, h and ye stay in the workspace for the
+    // backward.
+    a.slots = true;
     st = launched(launch_route(a, s), h);
     if (st != SWITCH_OK) return st;
     if (prof) cudaEventRecord(h->ev[1], s);
-    st = launched(launch_dispatch(x, h->xe, r->expert, r->row, r->expert2, r->row2, r->expert_rows, h->N,
-                                  h->cfg.E, h->R, h->cfg.d_model * h->es, s),
+    st = launched(launch_dispatch(x, h->xe, r->expert, r->row, a.top2 ? r->expert2 : nullptr,
+                                  a.top2 ? r->row2 : nullptr, r->expert_rows, h->N, h->cfg.E, h->R,
+                                  h->cfg.d_model * h->es, s),
                   h);
     if (st != SWITCH_OK) return st;
     if (prof) cudaEventRecord(h->ev[2], s);
@@ -550,6 +573,57 @@ switch_status switch_forward_host(switch_handle h, const void* x_host, const flo
     return SWITCH_ERR_CUDA;
   }
   return SWITCH_OK;
+}
+
+switch_status switch_backward(switch_handle h, const void* x, const float* Wr, const void* W1, const void* W2,
+                              const switch_route_out* r, const void* dy, float w_aux, float w_z, int residual,
+                              float* dx, float* dWr, float* dbr, float* dW1, float* db1, float* dW2, float* db2,
+                              void* stream) {
+  if (!h || !Wr || !W1 || !W2 || !dWr || !dW1 || !dW2) return SWITCH_ERR_INVALID_ARG;
+  if (!training_of(&h->cfg) || top2_of(&h->cfg)) return SWITCH_ERR_UNSUPPORTED;
+  if (!route_out_ok(r, h->N)) return SWITCH_ERR_INVALID_ARG;
+  if (h->N > 0 && (!x || !dy || !dx)) return SWITCH_ERR_INVALID_ARG;
+  const switch_config& c = h->cfg;
+  BackwardArgs a{};
+  a.G = c.G;
+  a.T = c.T;
+  a.E = c.E;
+  a.R = h->R;
+  a.d = c.d_model;
+  a.F = c.d_ff;
+  a.bf16 = c.dtype == SWITCH_BF16;
+  a.alpha = c.alpha;
+  a.w_aux = w_aux;
+  a.w_z = w_z;
+  a.residual = residual != 0;
+  a.x = x;
+  a.dy = dy;
+  a.Wr = Wr;
+  a.W1 = W1;
+  a.W2 = W2;
+  a.xe = h->xe;
+  a.h = h->hbuf;
+  a.ye = h->ye;
+  a.logits = ((c.flags & SWITCH_FLAG_WRITE_LOGITS) && r->logits) ? r->logits : h->logits;
+  a.expert = r->expert;
+  a.row = r->row;
+  a.gate = r->gate;
+  a.raw = r->raw_count;
+  a.expert_rows = r->expert_rows;
+  a.dx = dx;
+  a.dWr = dWr;
+  a.dbr = dbr;
+  a.dW1 = dW1;
+  a.db1 = db1;
+  a.dW2 = dW2;
+  a.db2 = db2;
+  a.dye = h->bw_dye;
+  a.dh = h->bw_dh;
+  a.dxe = h->bw_dxe;
+  a.dg = h->bw_dg;
+  a.dz = h->bw_dz;
+  h->last_launches = 0;
+  return launched(launch_backward(a, (cudaStream_t)stream), h);
 }
 
 static switch_status read_error_word(switch_handle h, cudaStream_t s) {

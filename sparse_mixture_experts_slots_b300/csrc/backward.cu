@@ -1,0 +1,321 @@
+// Backward of the top-1 layer: gradients of L = sum(dy * y) + w_aux * aux + w_z * z_loss
+// with the choices, slots and capacity mask of the forward held fixed.
+//
+//   combine:  dye[e, r] = g_t * dy_t for the kept token t in row r of expert e, and
+//             dg_t = <dy_t, ye[e, r]> (the gate's gradient; 0 for dropped tokens)
+//   experts:  dh = (dye W2_e) * [h > 0];  dW2_e = dye^T h;  db2_e = sum_r dye
+//             dxe = dh W1_e;  dW1_e = dh^T xe;  db1_e = sum_r dh
+//   router:   dp_te = [e = e*_t] dg_t + w_aux alpha E f_ge / (G T)   (through P, not f)
+//             dz_t = p_t * (dp_t - <p_t, dp_t>) + w_z 2 lse_t / (G T) * p_t
+//             dWr = dz^T x;  dbr = sum_t dz_t;  dx = dz Wr + dxe[e*_t, row_t] (+ dy)
+// The gate keeps the router differentiable (Switch Transformers card, section 方法适配);
+// the aux loss's gradient flows through P and not through the hard counts f, and the z-loss
+// through the log-sum-exp (070 page, section 核心思想与公式).
+//
+// The matrix products run in one batched kernel with arbitrary strides on both operands
+// and per-batch limits on M, N or K (an expert's row count), float32 accumulation on CUDA
+// cores.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace smoe {
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// ---------------------------------------------------------------- batched strided GEMM
+// C_b(i, j) = sum_k A_b(i, k) B_b(j, k) for i < M_b, j < N_b, k < K_b, where X_b(u, v) =
+// X[b sXb + u sXu + v sXv] and M_b = min(M, limM[b]) (likewise N, K) when a limit array is
+// given.  EPI 1: C *= (mask_b(i, j) > 0), the mask in float32 or bfloat16.  ACC: C += .
+constexpr int BG_T = 64, BG_K = 16;
+
+template <typename TA, typename TB, typename TM, int EPI, bool ACC>
+__global__ void __launch_bounds__(256) bgemm_kernel(const TA* __restrict__ A, const TB* __restrict__ B,
+                                                    float* __restrict__ C, const TM* __restrict__ mask,
+                                                    BgemmArgs g) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float As[BG_K][BG_T + 4], Bs[BG_K][BG_T + 4];
+  const int b = blockIdx.z;
+  const int Mb = g.limM ? min(g.M, g.limM[b]) : g.M;
+  const int Nb = g.limN ? min(g.N, g.limN[b]) : g.N;
+  const int Kb = g.limK ? min(g.K, g.limK[b]) : g.K;
+  const int i0 = blockIdx.y * BG_T, j0 = blockIdx.x * BG_T;
+  if (i0 >= Mb || j0 >= Nb) return;
+  const TA* Ab = A + (long long)b * g.sAb;
+  const TB* Bb = B + (long long)b * g.sBb;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < Kb; k0 += BG_K) {
+    // 64 x 16 elements of each operand per step: 4 per thread
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int idx = threadIdx.x + 256 * q;
+      const int kk = idx / BG_T, u = idx % BG_T;
+      const int k = k0 + kk;
+      const int i = i0 + u, j = j0 + u;
+      As[kk][u] = (i < Mb && k < Kb) ? to_f<TA>(Ab[(long long)i * g.sAi + (long long)k * g.sAk]) : 0.f;
+      Bs[kk][u] = (j < Nb && k < Kb) ? to_f<TB>(Bb[(long long)j * g.sBj + (long long)k * g.sBk]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BG_K; ++kk) {
+      float a[4], bv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        a[q] = As[kk][ty + 16 * q];
+        bv[q] = Bs[kk][tx + 16 * q];
+      }
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(a[p], bv[q], acc[p][q]);
+    }
+    __syncthreads();
+  }
+  float* Cb = C + (long long)b * g.sCb;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int i = i0 + ty + 16 * p;
+    if (i >= Mb) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + tx + 16 * q;
+      if (j >= Nb) continue;
+      float v = acc[p][q];
+      if (EPI == 1) {
+        const TM mv = mask[(long long)b * g.sMb + (long long)i * g.sMi + (long long)j * g.sMj];
+        v = to_f<TM>(mv) > 0.f ? v : 0.f;
+      }
+      float* dst = Cb + (long long)i * g.sCi + (long long)j * g.sCj;
+      *dst = ACC ? *dst + v : v;
+    }
+  }
+}
+
+template <typename TA, typename TB, typename TM, int EPI, bool ACC>
+static int launch_bg(const TA* A, const TB* B, float* C, const TM* mask, const BgemmArgs& g, int batches,
+                     cudaStream_t s) {
+  if (g.M <= 0 || g.N <= 0 || batches <= 0) return 0;
+  const dim3 grid((unsigned)((g.N + BG_T - 1) / BG_T), (unsigned)((g.M + BG_T - 1) / BG_T), (unsigned)batches);
+  return launch_k(bgemm_kernel<TA, TB, TM, EPI, ACC>, grid, dim3(256), 0, s, false, 1, A, B, C, mask, g) ==
+                 cudaSuccess
+             ? 1
+             : -1;
+}
+
+// ---------------------------------------------------------------- combine backward
+// Warp per token: dye row = g dy (float32), dg = <dy, ye row>.
+template <typename T>
+__global__ void __launch_bounds__(256) combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ ye,
+                                                          const int32_t* __restrict__ expert,
+                                                          const int32_t* __restrict__ row,
+                                                          const float* __restrict__ gate, float* __restrict__ dye,
+                                                          float* __restrict__ dg, long long N, int d, int R) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long t = (long long)blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (t >= N) return;
+  const int r = row[t];
+  if (r < 0) {
+    if (lane == 0) dg[t] = 0.f;
+    return;
+  }
+  const long long base = ((long long)expert[t] * R + r) * d;
+  const float g = gate[t];
+  float s = 0.f;
+  for (int c = lane; c < d; c += 32) {
+    const float v = to_f<T>(dy[t * d + c]);
+    dye[base + c] = g * v;
+    s = fmaf(v, to_f<T>(ye[base + c]), s);
+  }
+  s = warp_sum(s);
+  if (lane == 0) dg[t] = s;
+}
+
+// ---------------------------------------------------------------- column sums over an expert's rows
+// out[e, c] = sum_{r < rows[e]} in[e, r, c] (fixed order), thread per (e, c).
+__global__ void __launch_bounds__(256) colsum_rows_kernel(const float* __restrict__ in, const int32_t* __restrict__ rows,
+                                                          float* __restrict__ out, int E, int R, int W) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= (long long)E * W) return;
+  const int e = (int)(k / W), c = (int)(k % W);
+  const int n = rows ? min(R, rows[e]) : R;
+  float s = 0.f;
+  for (int r = 0; r < n; ++r) s += in[((long long)e * R + r) * W + c];
+  out[k] = s;
+}
+
+// ---------------------------------------------------------------- router backward
+// Warp per token: p from the logits, dp = onehot(e*) dg + w_aux alpha E f / (G T), the
+// softmax Jacobian, plus the z-loss term; writes dz [N, E].
+__global__ void __launch_bounds__(256) router_bwd_kernel(const float* __restrict__ z, const int32_t* __restrict__ expert,
+                                                         const float* __restrict__ dg, const int32_t* __restrict__ raw,
+                                                         float* __restrict__ dz, long long N, int T, int E, int G,
+                                                         float aux_coef, float z_coef) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long t = (long long)blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (t >= N) return;
+  const float* zr = z + t * E;
+  const int g = (int)(t / T);
+  float m = -INFINITY;
+  for (int e = lane; e < E; e += 32) m = fmaxf(m, zr[e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+  for (int e = lane; e < E; e += 32) s += expf(zr[e] - m);
+  s = warp_sum(s);
+  const float lse = m + logf(s);
+  const int a = expert[t];
+  const float dgt = dg[t];
+  const int32_t* rg = raw + (long long)g * E;
+  // <p, dp>
+  float pdp = 0.f;
+  for (int e = lane; e < E; e += 32) {
+    const float p = expf(zr[e] - m) / s;
+    const float dp = (e == a ? dgt : 0.f) + aux_coef * (float)rg[e];
+    pdp = fmaf(p, dp, pdp);
+  }
+  pdp = warp_sum(pdp);
+  for (int e = lane; e < E; e += 32) {
+    const float p = expf(zr[e] - m) / s;
+    const float dp = (e == a ? dgt : 0.f) + aux_coef * (float)rg[e];
+    dz[t * E + e] = p * (dp - pdp) + z_coef * lse * p;
+  }
+}
+
+// ---------------------------------------------------------------- dx assembly
+// dx_t += dxe[e*_t, row_t] (kept tokens) (+ dy_t with the residual)
+template <typename T>
+__global__ void __launch_bounds__(256) dx_assemble_kernel(float* __restrict__ dx, const float* __restrict__ dxe,
+                                                          const T* __restrict__ dy, const int32_t* __restrict__ expert,
+                                                          const int32_t* __restrict__ row, long long N, int d, int R,
+                                                          int residual) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long t = (long long)blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (t >= N) return;
+  const int r = row[t];
+  const float* src = r >= 0 ? dxe + ((long long)expert[t] * R + r) * d : nullptr;
+  for (int c = lane; c < d; c += 32) {
+    float v = dx[t * d + c];
+    if (src) v += src[c];
+    if (residual) v += to_f<T>(dy[t * d + c]);
+    dx[t * d + c] = v;
+  }
+}
+
+// ---------------------------------------------------------------- launcher
+template <typename T>
+static int run_backward(const BackwardArgs& a, cudaStream_t s) {
+  const long long N = (long long)a.G * a.T;
+  const int E = a.E, R = a.R, d = a.d, F = a.F;
+  int n = 0, k;
+  const T* x = static_cast<const T*>(a.x);
+  const T* dy = static_cast<const T*>(a.dy);
+  const T* W1 = static_cast<const T*>(a.W1);
+  const T* W2 = static_cast<const T*>(a.W2);
+  const T* xe = static_cast<const T*>(a.xe);
+  const T* hb = static_cast<const T*>(a.h);
+  const T* ye = static_cast<const T*>(a.ye);
+#define BW_STEP(expr) \
+  do {                \
+    k = (expr);       \
+    if (k < 0) return -1; \
+    n += k;           \
+  } while (0)
+  if (N > 0)
+    BW_STEP(launch_k(combine_bwd_kernel<T>, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1, dy, ye,
+                     a.expert, a.row, a.gate, a.dye, a.dg, N, d, R) == cudaSuccess ? 1 : -1);
+  // dh = (dye W2_e) * [h > 0]: i = row (<= rows_e), j = f, k = c
+  {
+    BgemmArgs g{};
+    g.M = R; g.N = F; g.K = d; g.limM = a.expert_rows;
+    g.sAb = (long long)R * d; g.sAi = d; g.sAk = 1;                // dye [E, R, d]
+    g.sBb = (long long)d * F; g.sBj = 1; g.sBk = F;                // W2 [E, d, F]: B(j = f, k = c) = W2[c, f]
+    g.sCb = (long long)R * F; g.sCi = F; g.sCj = 1;                // dh [E, R, F]
+    g.sMb = (long long)R * F; g.sMi = F; g.sMj = 1;                // h
+    BW_STEP((launch_bg<float, T, T, 1, false>(a.dye, W2, a.dh, hb, g, E, s)));
+  }
+  // dW2_e = dye^T h: i = c (d), j = f, k = row (< rows_e)
+  {
+    BgemmArgs g{};
+    g.M = d; g.N = F; g.K = R; g.limK = a.expert_rows;
+    g.sAb = (long long)R * d; g.sAi = 1; g.sAk = d;
+    g.sBb = (long long)R * F; g.sBj = 1; g.sBk = F;
+    g.sCb = (long long)d * F; g.sCi = F; g.sCj = 1;
+    BW_STEP((launch_bg<float, T, float, 0, false>(a.dye, hb, a.dW2, nullptr, g, E, s)));
+  }
+  // dxe = dh W1_e: i = row, j = c, k = f
+  {
+    BgemmArgs g{};
+    g.M = R; g.N = d; g.K = F; g.limM = a.expert_rows;
+    g.sAb = (long long)R * F; g.sAi = F; g.sAk = 1;
+    g.sBb = (long long)F * d; g.sBj = 1; g.sBk = d;                // W1 [E, F, d]: B(j = c, k = f) = W1[f, c]
+    g.sCb = (long long)R * d; g.sCi = d; g.sCj = 1;
+    BW_STEP((launch_bg<float, T, float, 0, false>(a.dh, W1, a.dxe, nullptr, g, E, s)));
+  }
+  // dW1_e = dh^T xe: i = f, j = c, k = row
+  {
+    BgemmArgs g{};
+    g.M = F; g.N = d; g.K = R; g.limK = a.expert_rows;
+    g.sAb = (long long)R * F; g.sAi = 1; g.sAk = F;
+    g.sBb = (long long)R * d; g.sBj = 1; g.sBk = d;
+    g.sCb = (long long)F * d; g.sCi = d; g.sCj = 1;
+    BW_STEP((launch_bg<float, T, float, 0, false>(a.dh, xe, a.dW1, nullptr, g, E, s)));
+  }
+  // bias gradients
+  if (a.db2)
+    BW_STEP(launch_k(colsum_rows_kernel, dim3((unsigned)(((long long)E * d + 255) / 256)), dim3(256), 0, s, false, 1,
+                     (const float*)a.dye, a.expert_rows, a.db2, E, R, d) == cudaSuccess ? 1 : -1);
+  if (a.db1)
+    BW_STEP(launch_k(colsum_rows_kernel, dim3((unsigned)(((long long)E * F + 255) / 256)), dim3(256), 0, s, false, 1,
+                     (const float*)a.dh, a.expert_rows, a.db1, E, R, F) == cudaSuccess ? 1 : -1);
+  if (N > 0) {
+    const float aux_coef = a.w_aux * a.alpha * (float)E / ((float)a.G * (float)a.T * (float)a.T);  // f = raw / T
+    const float z_coef = a.w_z * 2.f / ((float)a.G * (float)a.T);
+    BW_STEP(launch_k(router_bwd_kernel, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1, a.logits, a.expert,
+                     (const float*)a.dg, a.raw, a.dz, N, a.T, E, a.G, aux_coef, z_coef) == cudaSuccess ? 1 : -1);
+    // dWr = dz^T x: i = e, j = c, k = t
+    {
+      BgemmArgs g{};
+      g.M = E; g.N = d; g.K = (int)N;
+      g.sAi = 1; g.sAk = E;
+      g.sBj = 1; g.sBk = d;
+      g.sCi = d; g.sCj = 1;
+      BW_STEP((launch_bg<float, T, float, 0, false>(a.dz, x, a.dWr, nullptr, g, 1, s)));
+    }
+    if (a.dbr)
+      BW_STEP(launch_k(colsum_rows_kernel, dim3((unsigned)((E + 255) / 256)), dim3(256), 0, s, false, 1,
+                       (const float*)a.dz, (const int32_t*)nullptr, a.dbr, 1, (int)N, E) == cudaSuccess ? 1 : -1);
+    // dx = dz Wr: i = t, j = c, k = e
+    {
+      BgemmArgs g{};
+      g.M = (int)N; g.N = d; g.K = E;
+      g.sAi = E; g.sAk = 1;
+      g.sBj = 1; g.sBk = d;
+      g.sCi = d; g.sCj = 1;
+      BW_STEP((launch_bg<float, float, float, 0, false>(a.dz, a.Wr, a.dx, nullptr, g, 1, s)));
+    }
+    BW_STEP(launch_k(dx_assemble_kernel<T>, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1, a.dx,
+                     (const float*)a.dxe, dy, a.expert, a.row, N, d, R, a.residual ? 1 : 0) == cudaSuccess ? 1 : -1);
+  }
+#undef BW_STEP
+  return n;
+}
+
+int launch_backward(const BackwardArgs& a, cudaStream_t s) {
+  return a.bf16 ? run_backward<__nv_bfloat16>(a, s) : run_backward<float>(a, s);
+}
+
+}  // namespace smoe

@@ -78,6 +78,33 @@ struct RouteArgs {
   int32_t* tile_base2; // [G, nT, E]
 };
 
+// Batched strided product C_b(i, j) = sum_k A_b(i, k) B_b(j, k) (see backward.cu).
+struct BgemmArgs {
+  int M, N, K;
+  const int32_t* limM; const int32_t* limN; const int32_t* limK;  // per-batch limits or null
+  long long sAb, sAi, sAk, sBb, sBj, sBk, sCb, sCi, sCj, sMb, sMi, sMj;
+};
+
+// Backward of the top-1 layer (backward.cu); float32 gradients.
+struct BackwardArgs {
+  int G, T, E, R, d, F;
+  bool bf16;           // activations and expert weights bfloat16 (else float32)
+  float alpha, w_aux, w_z;
+  bool residual;
+  // forward inputs and saved activations
+  const void* x; const void* dy; const float* Wr; const void* W1; const void* W2;
+  const void* xe; const void* h; const void* ye;  // [E, R, d], [E, R, F], [E, R, d]
+  const float* logits;                             // [N, E]
+  const int32_t* expert; const int32_t* row; const float* gate;
+  const int32_t* raw;                              // [G, E] choices before truncation
+  const int32_t* expert_rows;                      // [E]
+  // outputs (db1, db2, dbr may be null)
+  float* dx; float* dWr; float* dbr; float* dW1; float* db1; float* dW2; float* db2;
+  // workspace
+  float* dye; float* dh; float* dxe; float* dg; float* dz;
+};
+int launch_backward(const BackwardArgs& a, cudaStream_t s);
+
 // Blocks of the cross-tile scan (one per 32 experts); scan_partial holds G * this many floats.
 __host__ __device__ inline int route_scan_blocks(int E) { return (E + 31) / 32; }
 
