@@ -215,6 +215,68 @@ def config_of(shape, args):
             "l2": "flushed (256 MB write) before every timed step; expert weights (>1 GB) exceed L2 anyway"}
 
 
+
+# ---------------------------------------------------------------- training step (--train)
+FP32_ALU_TFLOPS = 148 * 128 * 2 * 2.032 / 1e3  # SMs x FP32 lanes x FMA x max SM clock (GHz) -> TFLOP/s
+
+
+def run_train(args, shape):
+    """One step = switch_forward in training mode + switch_backward (fixed dy, w_aux = 1,
+    w_z = 1e-3).  The backward's products run on CUDA cores: its roofline is the float32
+    ALU peak (unit counts x clock)."""
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from sparse_mixture_experts_slots_b300 import SwitchMoE
+    inp = make_inputs(shape, workload_seed(args.workload), dev)
+    dt = torch.float32 if shape.dtype == "f32" else torch.bfloat16
+    layer = SwitchMoE(shape.G, shape.T, shape.d_model, shape.d_ff, shape.E, shape.capacity_factor, dtype=dt,
+                      training=True, device=dev)
+    r = layer.alloc_route()
+    y = torch.empty(shape.N, shape.d_model, dtype=dt, device=dev)
+    dy = (torch.randn(shape.N, shape.d_model, generator=torch.Generator().manual_seed(3)) * 0.5).to(dt).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    bw = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1.0)
+        k = i - args.warmup
+        if k >= 0:
+            fw[k][0].record(stream)
+        layer.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], r=r, y=y,
+                      stream=stream)
+        if k >= 0:
+            bw[k].record(stream)
+        layer.backward(inp["x"], inp["Wr"], inp["W1"], inp["W2"], r, dy, 1.0, 1e-3, stream=stream)
+        if k >= 0:
+            fw[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    layer.sync_status(stream)
+    step_ms = sum(a.elapsed_time(b) for a, b in fw) / args.steps
+    fwd_ms = sum(a.elapsed_time(b) for (a, _), b in zip(fw, bw)) / args.steps
+    bwd_ms = step_ms - fwd_ms
+    K = int(r.expert_rows.sum().item())
+    bwd_flops = 4 * 2.0 * K * shape.d_model * shape.d_ff + 2 * 2.0 * shape.N * shape.E * shape.d_model
+    tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    hbm, tc_burst, tc_sust, peak_src = peaks()
+    print(json.dumps({
+        "metric": METRIC + " (training step: forward + backward)", "value": shape.N / (step_ms * 1e-3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if shape.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": config_of(shape, argparse.Namespace(gpus=1, top_k=1)) | {"mode": "train"},
+        "forward_ms": fwd_ms, "backward_ms": bwd_ms, "kept_rows": K,
+        "roofline": {"bound": "alu", "kernel": "bgemm_kernel (backward products)", "achieved": tf,
+                     "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS,
+                     "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 (FMA) x 2.032 GHz",
+                     "frac_of_bf16_tensor_burst": tf / tc_burst,
+                     "algorithmic_flops": bwd_flops, "traffic": None},
+    }), flush=True)
+    return 0
+
 # ---------------------------------------------------------------- GPU arm
 def run_gpu(args, shape):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -398,6 +460,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--ref-ffn-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step (forward in training mode + switch_backward)")
     ap.add_argument("--top-k", type=int, default=1, choices=[1, 2],
                     help="2: the top-2 variant (weights = softmax over the two highest scores)")
     args = ap.parse_args()
@@ -405,6 +469,8 @@ def main():
     shape = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, shape)
+    if args.train:
+        return run_train(args, shape)
     return run_gpu(args, shape)
 
 
