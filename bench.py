@@ -403,7 +403,8 @@ def run_gpu(args, shape):
     # The binding roof is the one whose floor time is longer: algorithmic bytes at the copy
     # bandwidth, or the kept rows' FLOPs at the bf16 burst rate.
     tensor_bound = tc_path and work["ffn_flops"] / (tc_burst * 1e12) > work["ffn_bytes"] / (hbm * 1e9)
-    traffic = traffic_from_profiles(f"{kern}:{shape.name}")
+    # the recorded captures are of the top-1 layer; a top-2 run has no matching record
+    traffic = traffic_from_profiles(f"{kern}:{shape.name}") if args.top_k == 1 else None
     value = shape.N * world * args.steps / (total_ms * 1e-3)
     names = ["route", "dispatch", "ffn", "ffn_layer2", "combine"]
     line = {
