@@ -31,59 +31,88 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return _
 // C_b(i, j) = sum_k A_b(i, k) B_b(j, k) for i < M_b, j < N_b, k < K_b, where X_b(u, v) =
 // X[b sXb + u sXu + v sXv] and M_b = min(M, limM[b]) (likewise N, K) when a limit array is
 // given.  EPI 1: C *= (mask_b(i, j) > 0), the mask in float32 or bfloat16.  ACC: C += .
-constexpr int BG_T = 64, BG_K = 16;
+constexpr int BG_N = 128, BG_K = 16, BG_THREADS = 256;
 
-template <typename TA, typename TB, typename TM, int EPI, bool ACC>
-__global__ void __launch_bounds__(256) bgemm_kernel(const TA* __restrict__ A, const TB* __restrict__ B,
-                                                    float* __restrict__ C, const TM* __restrict__ mask,
-                                                    BgemmArgs g) {
+// Loads one BK-deep slice of an operand tile (rows u < ROWS of the tile, k < BG_K) into
+// registers: consecutive threads walk the operand's contiguous axis (k when its k stride
+// is 1, else the row axis), so a warp reads whole runs of memory.
+template <typename T, int ROWS>
+__device__ __forceinline__ void bg_load(const T* __restrict__ X, long long su, long long sk, int u0, int k0, int lim_u,
+                                        int lim_k, bool kfast, float (&r)[ROWS * BG_K / BG_THREADS]) {
+#pragma unroll
+  for (int q = 0; q < ROWS * BG_K / BG_THREADS; ++q) {
+    const int idx = threadIdx.x + BG_THREADS * q;
+    const int kk = kfast ? idx % BG_K : idx / ROWS;
+    const int u = kfast ? idx / BG_K : idx % ROWS;
+    const int gu = u0 + u, gk = k0 + kk;
+    r[q] = (gu < lim_u && gk < lim_k) ? to_f<T>(X[(long long)gu * su + (long long)gk * sk]) : 0.f;
+  }
+}
+template <int ROWS>
+__device__ __forceinline__ void bg_store(float (*S)[ROWS + 4], bool kfast, const float (&r)[ROWS * BG_K / BG_THREADS]) {
+#pragma unroll
+  for (int q = 0; q < ROWS * BG_K / BG_THREADS; ++q) {
+    const int idx = threadIdx.x + BG_THREADS * q;
+    const int kk = kfast ? idx % BG_K : idx / ROWS;
+    const int u = kfast ? idx / BG_K : idx % ROWS;
+    S[kk][u] = r[q];
+  }
+}
+
+// Tile BM x 128 (BM = 64 or 128), 256 threads in a 16 x 16 grid, each BM/16 rows x 8 columns
+// (rows ty + 16 p, columns tx + 16 q); the next K slice is loaded into registers while the
+// current one is multiplied.
+template <typename TA, typename TB, typename TM, int EPI, bool ACC, int BM>
+__global__ void __launch_bounds__(BG_THREADS) bgemm_kernel(const TA* __restrict__ A, const TB* __restrict__ B,
+                                                           float* __restrict__ C, const TM* __restrict__ mask,
+                                                           BgemmArgs g) {
   griddep_wait();
   griddep_launch_dependents();
-  __shared__ float As[BG_K][BG_T + 4], Bs[BG_K][BG_T + 4];
+  constexpr int RA = BM * BG_K / BG_THREADS, RB = BG_N * BG_K / BG_THREADS, PM = BM / 16;
+  __shared__ float As[BG_K][BM + 4], Bs[BG_K][BG_N + 4];
   const int b = blockIdx.z;
   const int Mb = g.limM ? min(g.M, g.limM[b]) : g.M;
   const int Nb = g.limN ? min(g.N, g.limN[b]) : g.N;
   const int Kb = g.limK ? min(g.K, g.limK[b]) : g.K;
-  const int i0 = blockIdx.y * BG_T, j0 = blockIdx.x * BG_T;
+  const int i0 = blockIdx.y * BM, j0 = blockIdx.x * BG_N;
   if (i0 >= Mb || j0 >= Nb) return;
   const TA* Ab = A + (long long)b * g.sAb;
   const TB* Bb = B + (long long)b * g.sBb;
+  const bool akf = g.sAk == 1, bkf = g.sBk == 1;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4] = {};
+  float acc[PM][8] = {};
+  float ra[RA], rb[RB];
+  bg_load<TA, BM>(Ab, g.sAi, g.sAk, i0, 0, Mb, Kb, akf, ra);
+  bg_load<TB, BG_N>(Bb, g.sBj, g.sBk, j0, 0, Nb, Kb, bkf, rb);
   for (int k0 = 0; k0 < Kb; k0 += BG_K) {
-    // 64 x 16 elements of each operand per step: 4 per thread
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int idx = threadIdx.x + 256 * q;
-      const int kk = idx / BG_T, u = idx % BG_T;
-      const int k = k0 + kk;
-      const int i = i0 + u, j = j0 + u;
-      As[kk][u] = (i < Mb && k < Kb) ? to_f<TA>(Ab[(long long)i * g.sAi + (long long)k * g.sAk]) : 0.f;
-      Bs[kk][u] = (j < Nb && k < Kb) ? to_f<TB>(Bb[(long long)j * g.sBj + (long long)k * g.sBk]) : 0.f;
-    }
+    bg_store<BM>(As, akf, ra);
+    bg_store<BG_N>(Bs, bkf, rb);
     __syncthreads();
+    if (k0 + BG_K < Kb) {  // next slice in flight during the products below
+      bg_load<TA, BM>(Ab, g.sAi, g.sAk, i0, k0 + BG_K, Mb, Kb, akf, ra);
+      bg_load<TB, BG_N>(Bb, g.sBj, g.sBk, j0, k0 + BG_K, Nb, Kb, bkf, rb);
+    }
 #pragma unroll
     for (int kk = 0; kk < BG_K; ++kk) {
-      float a[4], bv[4];
+      float a[PM], bv[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        a[q] = As[kk][ty + 16 * q];
-        bv[q] = Bs[kk][tx + 16 * q];
-      }
+      for (int p = 0; p < PM; ++p) a[p] = As[kk][ty + 16 * p];
 #pragma unroll
-      for (int p = 0; p < 4; ++p)
+      for (int q = 0; q < 8; ++q) bv[q] = Bs[kk][tx + 16 * q];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(a[p], bv[q], acc[p][q]);
+      for (int p = 0; p < PM; ++p)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[p][q] = fmaf(a[p], bv[q], acc[p][q]);
     }
     __syncthreads();
   }
   float* Cb = C + (long long)b * g.sCb;
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
+  for (int p = 0; p < PM; ++p) {
     const int i = i0 + ty + 16 * p;
     if (i >= Mb) continue;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const int j = j0 + tx + 16 * q;
       if (j >= Nb) continue;
       float v = acc[p][q];
@@ -101,11 +130,13 @@ template <typename TA, typename TB, typename TM, int EPI, bool ACC>
 static int launch_bg(const TA* A, const TB* B, float* C, const TM* mask, const BgemmArgs& g, int batches,
                      cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0 || batches <= 0) return 0;
-  const dim3 grid((unsigned)((g.N + BG_T - 1) / BG_T), (unsigned)((g.M + BG_T - 1) / BG_T), (unsigned)batches);
-  return launch_k(bgemm_kernel<TA, TB, TM, EPI, ACC>, grid, dim3(256), 0, s, false, 1, A, B, C, mask, g) ==
-                 cudaSuccess
-             ? 1
-             : -1;
+  const bool big = g.M >= 128;
+  const int BM = big ? 128 : 64;
+  const dim3 grid((unsigned)((g.N + BG_N - 1) / BG_N), (unsigned)((g.M + BM - 1) / BM), (unsigned)batches);
+  const cudaError_t e =
+      big ? launch_k(bgemm_kernel<TA, TB, TM, EPI, ACC, 128>, grid, dim3(BG_THREADS), 0, s, false, 1, A, B, C, mask, g)
+          : launch_k(bgemm_kernel<TA, TB, TM, EPI, ACC, 64>, grid, dim3(BG_THREADS), 0, s, false, 1, A, B, C, mask, g);
+  return e == cudaSuccess ? 1 : -1;
 }
 
 // ---------------------------------------------------------------- combine backward
