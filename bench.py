@@ -37,6 +37,27 @@ DEFAULT_WORKLOAD = "switch-base-e128"
 L2_FLUSH_BYTES = 256 << 20  # > 126 MB L2
 
 
+# ---------------------------------------------------------------- across ranks
+def rank_batch_seed(seed: int, rank: int, world: int) -> int:
+    """Seed of a rank's token batch: routing groups are independent, so each rank routes its
+    own batch (weak scaling) while the expert weights, drawn from `seed`, are replicated."""
+    return seed if world == 1 else seed + 7919 * rank
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time (the job is done when every rank is)."""
+    if not dist:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_step: int, world: int, steps: int, ms: float) -> float:
+    """Whole-job tokens/s: the tokens every rank processed over the slowest rank's time."""
+    return tokens_per_step * world * steps / (ms * 1e-3)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -297,7 +318,7 @@ def run_gpu(args, shape):
     seed = workload_seed(args.workload)
     inp = make_inputs(shape, seed, dev)
     if world > 1:  # each rank routes its own batch; the expert weights are replicated
-        inp["x"] = make_inputs(shape, seed + 7919 * rank, dev, with_experts=False)["x"]
+        inp["x"] = make_inputs(shape, rank_batch_seed(seed, rank, world), dev, with_experts=False)["x"]
     dt = torch.float32 if shape.dtype == "f32" else torch.bfloat16
     mk = lambda prof: SwitchMoE(shape.G, shape.T, shape.d_model, shape.d_ff, shape.E, shape.capacity_factor,
                                 dtype=dt, profile=prof, top_k=args.top_k, device=dev)
@@ -334,11 +355,7 @@ def run_gpu(args, shape):
         dist.barrier()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
     layer.sync_status(stream)
 
     # ---------------- per-stage times: a profiled pass of the same workload (CUDA events
@@ -380,11 +397,7 @@ def run_gpu(args, shape):
     for i in range(args.steps):
         e2e_step(i)
     torch.cuda.synchronize(dev)
-    e2e_ms = (time.perf_counter() - t0) * 1e3
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, dist, dev)
 
     if rank != 0:
         if dist:
@@ -405,7 +418,7 @@ def run_gpu(args, shape):
     tensor_bound = tc_path and work["ffn_flops"] / (tc_burst * 1e12) > work["ffn_bytes"] / (hbm * 1e9)
     # the recorded captures are of the top-1 layer; a top-2 run has no matching record
     traffic = traffic_from_profiles(f"{kern}:{shape.name}") if args.top_k == 1 else None
-    value = shape.N * world * args.steps / (total_ms * 1e-3)
+    value = job_throughput(shape.N, world, args.steps, total_ms)
     names = ["route", "dispatch", "ffn", "ffn_layer2", "combine"]
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -433,7 +446,7 @@ def run_gpu(args, shape):
         "ffn_hbm_frac": achieved / hbm,
         "dispatch_hbm_gbs": float(work["dispatch_bytes"] / (stage_avg[1] * 1e-3) / 1e9),
         "kept_rows": work["kept_rows"], "dropped": int(shape.N - work["kept_rows"]),
-        "e2e": {"value": shape.N * world * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(shape.N, world, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                 "d2h_bytes_per_step": int(y_host.numel() * y_host.element_size() + 4),
                 "ms_per_step": e2e_ms / args.steps,

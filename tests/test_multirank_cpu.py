@@ -1,0 +1,74 @@
+"""The N > 1 path of bench.py on CPU: two gloo ranks (no GPU).
+
+Checks the pieces the GPU arm uses across ranks: each rank routes its own batch while the
+expert weights are replicated, the timed region's barrier, the max over ranks, and the
+whole-job throughput; and that the reference arm runs on rank 0 only.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_path):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    sys.path.insert(0, ROOT)
+    import bench
+    from gen import WORKLOADS, make_inputs, workload_seed
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        shape = WORKLOADS["tiny-e16-fp32"]
+        seed = workload_seed(shape.name)
+        inp = make_inputs(shape, seed, "cpu")
+        x = make_inputs(shape, bench.rank_batch_seed(seed, rank, world), "cpu", with_experts=False)["x"]
+        # replicated weights, distinct batches
+        w_sum = torch.tensor([float(inp["W1"].double().sum())], dtype=torch.float64)
+        x_sum = torch.tensor([float(x.double().sum())], dtype=torch.float64)
+        ws = [torch.zeros(1, dtype=torch.float64) for _ in range(world)]
+        xs = [torch.zeros(1, dtype=torch.float64) for _ in range(world)]
+        dist.all_gather(ws, w_sum)
+        dist.all_gather(xs, x_sum)
+        dist.barrier()
+        local_ms = 10.0 + 2.5 * rank
+        total = bench.max_over_ranks(local_ms, dist, "cpu")
+        value = bench.job_throughput(shape.N, world, 7, total)
+        with open(out_path + f".{rank}", "w") as fh:
+            json.dump({"w": [float(t) for t in ws], "x": [float(t) for t in xs], "total": total, "value": value}, fh)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks(tmp_path):
+    world, port = 2, _free_port()
+    out = str(tmp_path / "rank")
+    mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, join=True, start_method="spawn")
+    res = [json.load(open(out + f".{r}")) for r in range(world)]
+    for r in res:
+        assert r["w"][0] == r["w"][1], "expert weights must be the same on every rank"
+        assert r["x"][0] != r["x"][1], "each rank routes its own batch"
+        assert r["total"] == 12.5, "the slowest rank's time"
+        assert abs(r["value"] - 32 * 2 * 7 / 12.5e-3) < 1e-6
+    assert res[0] == res[1]
+
+
+def test_reference_arm_runs_on_rank0_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    p = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny-e16-fp32", "--steps",
+                        "1", "--warmup", "1", "--gpus", "2"], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert p.returncode == 0 and p.stdout.strip() == ""
