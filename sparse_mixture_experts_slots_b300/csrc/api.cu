@@ -57,6 +57,12 @@ struct switch_layer {
   float* bw_dxe;  // [E, R, d]
   float* bw_dg;   // [N]
   float* bw_dz;   // [N, E]
+  // tensor-core backward (bf16 with tensor-core FFN shapes): transposed weights, bf16 copies
+  void* bw_W1T;   // [E, d, F]
+  void* bw_W2T;   // [E, F, d]
+  void* bw_dye16; // [E, R, d]
+  void* bw_dh16;  // [E, R, F]
+  void* bw_dxe16; // [E, R, d]
   cudaEvent_t ev[6];
   bool have_events;
   int last_launches;
@@ -195,6 +201,12 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_bdxe = take(train ? E * R * d * sizeof(float) : 0);
   const size_t o_bdg = take(train ? N * sizeof(float) : 0);
   const size_t o_bdz = take(train ? N * E * sizeof(float) : 0);
+  const bool train_tc = train && cfg->dtype == SWITCH_BF16 && tc_shape_ok((int)F, (int)d) && tc_shape_ok((int)d, (int)F);
+  const size_t o_w1t = take(train_tc ? E * F * d * 2 : 0);
+  const size_t o_w2t = take(train_tc ? E * F * d * 2 : 0);
+  const size_t o_dye16 = take(train_tc ? E * R * d * 2 : 0);
+  const size_t o_dh16 = take(train_tc ? E * R * F * 2 : 0);
+  const size_t o_dxe16 = take(train_tc ? E * R * d * 2 : 0);
   h->ws_bytes = off;
   if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -224,6 +236,11 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->bw_dxe = reinterpret_cast<float*>(h->ws + o_bdxe);
   h->bw_dg = reinterpret_cast<float*>(h->ws + o_bdg);
   h->bw_dz = reinterpret_cast<float*>(h->ws + o_bdz);
+  h->bw_W1T = train_tc ? h->ws + o_w1t : nullptr;
+  h->bw_W2T = train_tc ? h->ws + o_w2t : nullptr;
+  h->bw_dye16 = train_tc ? h->ws + o_dye16 : nullptr;
+  h->bw_dh16 = train_tc ? h->ws + o_dh16 : nullptr;
+  h->bw_dxe16 = train_tc ? h->ws + o_dxe16 : nullptr;
   if (cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess) {
     cudaFree(h->ws);
     delete h;
@@ -352,7 +369,7 @@ static switch_status run_ffn_tc(switch_handle h, const void* xe, const void* W1,
                                 const void* b2, const int32_t* rows, void* out, bool combine,
                                 const switch_route_out* r, const void* resid, cudaStream_t s, bool pdl) {
   const switch_config& c = h->cfg;
-  FfnLaunch L;
+  FfnLaunch L{};
   L.xe = xe;
   L.W1 = W1;
   L.b1 = b1;
@@ -622,6 +639,14 @@ switch_status switch_backward(switch_handle h, const void* x, const float* Wr, c
   a.dxe = h->bw_dxe;
   a.dg = h->bw_dg;
   a.dz = h->bw_dz;
+  a.W1T = h->bw_W1T;
+  a.W2T = h->bw_W2T;
+  a.dye16 = h->bw_dye16;
+  a.dh16 = h->bw_dh16;
+  a.dxe16 = h->bw_dxe16;
+  a.counters = h->ffn_counters;
+  a.counter_words = h->ffn_counter_words;
+  a.err = h->err;
   h->last_launches = 0;
   return launched(launch_backward(a, (cudaStream_t)stream), h);
 }

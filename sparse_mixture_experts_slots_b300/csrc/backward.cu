@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const T* __restrict__ 
                                                           const int32_t* __restrict__ expert,
                                                           const int32_t* __restrict__ row,
                                                           const float* __restrict__ gate, float* __restrict__ dye,
+                                                          __nv_bfloat16* __restrict__ dye16,
                                                           float* __restrict__ dg, long long N, int d, int R) {
   griddep_wait();
   griddep_launch_dependents();
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const T* __restrict__ 
   for (int c = lane; c < d; c += 32) {
     const float v = to_f<T>(dy[t * d + c]);
     dye[base + c] = g * v;
+    if (dye16) dye16[base + c] = __float2bfloat16_rn(g * v);
     s = fmaf(v, to_f<T>(ye[base + c]), s);
   }
   s = warp_sum(s);
@@ -171,7 +173,8 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const T* __restrict__ 
 
 // ---------------------------------------------------------------- column sums over an expert's rows
 // out[e, c] = sum_{r < rows[e]} in[e, r, c] (fixed order), thread per (e, c).
-__global__ void __launch_bounds__(256) colsum_rows_kernel(const float* __restrict__ in, const int32_t* __restrict__ rows,
+template <typename TI>
+__global__ void __launch_bounds__(256) colsum_rows_kernel(const TI* __restrict__ in, const int32_t* __restrict__ rows,
                                                           float* __restrict__ out, int E, int R, int W) {
   griddep_wait();
   griddep_launch_dependents();
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(256) colsum_rows_kernel(const float* __restric
   const int e = (int)(k / W), c = (int)(k % W);
   const int n = rows ? min(R, rows[e]) : R;
   float s = 0.f;
-  for (int r = 0; r < n; ++r) s += in[((long long)e * R + r) * W + c];
+  for (int r = 0; r < n; ++r) s += to_f<TI>(in[((long long)e * R + r) * W + c]);
   out[k] = s;
 }
 
@@ -226,8 +229,8 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float* __restrict
 
 // ---------------------------------------------------------------- dx assembly
 // dx_t += dxe[e*_t, row_t] (kept tokens) (+ dy_t with the residual)
-template <typename T>
-__global__ void __launch_bounds__(256) dx_assemble_kernel(float* __restrict__ dx, const float* __restrict__ dxe,
+template <typename T, typename TX>
+__global__ void __launch_bounds__(256) dx_assemble_kernel(float* __restrict__ dx, const TX* __restrict__ dxe,
                                                           const T* __restrict__ dy, const int32_t* __restrict__ expert,
                                                           const int32_t* __restrict__ row, long long N, int d, int R,
                                                           int residual) {
@@ -237,13 +240,41 @@ __global__ void __launch_bounds__(256) dx_assemble_kernel(float* __restrict__ dx
   const int lane = threadIdx.x % 32;
   if (t >= N) return;
   const int r = row[t];
-  const float* src = r >= 0 ? dxe + ((long long)expert[t] * R + r) * d : nullptr;
+  const TX* src = r >= 0 ? dxe + ((long long)expert[t] * R + r) * d : nullptr;
   for (int c = lane; c < d; c += 32) {
     float v = dx[t * d + c];
-    if (src) v += src[c];
+    if (src) v += to_f<TX>(src[c]);
     if (residual) v += to_f<T>(dy[t * d + c]);
     dx[t * d + c] = v;
   }
+}
+
+// ---------------------------------------------------------------- transpose
+// out[b][q][p] = in[b][p][q] (bfloat16), 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in,
+                                                             __nv_bfloat16* __restrict__ out, int P, int Q) {
+  __shared__ __nv_bfloat16 t[32][33];
+  const long long b = blockIdx.z;
+  const int p0 = blockIdx.y * 32, q0 = blockIdx.x * 32;
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 8 rows of 32 per pass
+  const __nv_bfloat16* src = in + b * (long long)P * Q;
+  __nv_bfloat16* dst = out + b * (long long)P * Q;
+  for (int k = ty; k < 32; k += 8) {
+    const int p = p0 + k, q = q0 + tx;
+    if (p < P && q < Q) t[k][tx] = src[(long long)p * Q + q];
+  }
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    const int q = q0 + k, p = p0 + tx;
+    if (p < P && q < Q) dst[(long long)q * P + p] = t[tx][k];
+  }
+}
+
+static int launch_transpose(const void* in, void* out, int B, int P, int Q, cudaStream_t s) {
+  const dim3 grid((unsigned)((Q + 31) / 32), (unsigned)((P + 31) / 32), (unsigned)B);
+  transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out),
+                                             P, Q);
+  return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
 // ---------------------------------------------------------------- launcher
@@ -267,9 +298,33 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
   } while (0)
   if (N > 0)
     BW_STEP(launch_k(combine_bwd_kernel<T>, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1, dy, ye,
-                     a.expert, a.row, a.gate, a.dye, a.dg, N, d, R) == cudaSuccess ? 1 : -1);
+                     a.expert, a.row, a.gate, a.dye, (__nv_bfloat16*)a.dye16, a.dg, N, d, R) == cudaSuccess ? 1 : -1);
+  const bool tc = a.W1T != nullptr;
+  if (tc) {
+    // dh = (dye W2_e) * [h > 0] and dxe = dh W1_e are the forward's two layers with the
+    // transposed weights: W2^T [F, d] in the first, W1^T [d, F] in the second
+    BW_STEP(launch_transpose(a.W2, a.W2T, E, d, F, s));
+    BW_STEP(launch_transpose(a.W1, a.W1T, E, F, d, s));
+    if (cudaMemsetAsync(a.counters, 0, (size_t)a.counter_words * sizeof(uint32_t), s) != cudaSuccess) return -1;
+    FfnLaunch L{};
+    L.xe = a.dye16;
+    L.W1 = a.W2T;
+    L.W2 = a.W1T;
+    L.h = a.dh16;
+    L.out = a.dxe16;
+    L.expert_rows = a.expert_rows;
+    L.combine = false;
+    L.hmask = a.h;
+    L.counters = a.counters;
+    L.err = a.err;
+    L.E = E;
+    L.R = R;
+    L.d = d;
+    L.F = F;
+    if (R > 0) BW_STEP(launch_ffn_tc(L, s, false));
+  }
   // dh = (dye W2_e) * [h > 0]: i = row (<= rows_e), j = f, k = c
-  {
+  if (!tc) {
     BgemmArgs g{};
     g.M = R; g.N = F; g.K = d; g.limM = a.expert_rows;
     g.sAb = (long long)R * d; g.sAi = d; g.sAk = 1;                // dye [E, R, d]
@@ -285,10 +340,13 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     g.sAb = (long long)R * d; g.sAi = 1; g.sAk = d;
     g.sBb = (long long)R * F; g.sBj = 1; g.sBk = F;
     g.sCb = (long long)d * F; g.sCi = F; g.sCj = 1;
-    BW_STEP((launch_bg<float, T, float, 0, false>(a.dye, hb, a.dW2, nullptr, g, E, s)));
+    if (tc)
+      BW_STEP((launch_bg<__nv_bfloat16, T, float, 0, false>((const __nv_bfloat16*)a.dye16, hb, a.dW2, nullptr, g, E, s)));
+    else
+      BW_STEP((launch_bg<float, T, float, 0, false>(a.dye, hb, a.dW2, nullptr, g, E, s)));
   }
   // dxe = dh W1_e: i = row, j = c, k = f
-  {
+  if (!tc) {
     BgemmArgs g{};
     g.M = R; g.N = d; g.K = F; g.limM = a.expert_rows;
     g.sAb = (long long)R * F; g.sAi = F; g.sAk = 1;
@@ -303,15 +361,24 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     g.sAb = (long long)R * F; g.sAi = 1; g.sAk = F;
     g.sBb = (long long)R * d; g.sBj = 1; g.sBk = d;
     g.sCb = (long long)F * d; g.sCi = d; g.sCj = 1;
-    BW_STEP((launch_bg<float, T, float, 0, false>(a.dh, xe, a.dW1, nullptr, g, E, s)));
+    if (tc)
+      BW_STEP((launch_bg<__nv_bfloat16, T, float, 0, false>((const __nv_bfloat16*)a.dh16, xe, a.dW1, nullptr, g, E, s)));
+    else
+      BW_STEP((launch_bg<float, T, float, 0, false>(a.dh, xe, a.dW1, nullptr, g, E, s)));
   }
   // bias gradients
   if (a.db2)
-    BW_STEP(launch_k(colsum_rows_kernel, dim3((unsigned)(((long long)E * d + 255) / 256)), dim3(256), 0, s, false, 1,
-                     (const float*)a.dye, a.expert_rows, a.db2, E, R, d) == cudaSuccess ? 1 : -1);
-  if (a.db1)
-    BW_STEP(launch_k(colsum_rows_kernel, dim3((unsigned)(((long long)E * F + 255) / 256)), dim3(256), 0, s, false, 1,
-                     (const float*)a.dh, a.expert_rows, a.db1, E, R, F) == cudaSuccess ? 1 : -1);
+    BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)(((long long)E * d + 255) / 256)), dim3(256), 0, s,
+                     false, 1, (const float*)a.dye, a.expert_rows, a.db2, E, R, d) == cudaSuccess ? 1 : -1);
+  if (a.db1) {
+    if (tc)
+      BW_STEP(launch_k(colsum_rows_kernel<__nv_bfloat16>, dim3((unsigned)(((long long)E * F + 255) / 256)), dim3(256),
+                       0, s, false, 1, (const __nv_bfloat16*)a.dh16, a.expert_rows, a.db1, E, R, F) == cudaSuccess
+                  ? 1 : -1);
+    else
+      BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)(((long long)E * F + 255) / 256)), dim3(256), 0, s,
+                       false, 1, (const float*)a.dh, a.expert_rows, a.db1, E, R, F) == cudaSuccess ? 1 : -1);
+  }
   if (N > 0) {
     const float aux_coef = a.w_aux * a.alpha * (float)E / ((float)a.G * (float)a.T * (float)a.T);  // f = raw / T
     const float z_coef = a.w_z * 2.f / ((float)a.G * (float)a.T);
@@ -327,7 +394,7 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
       BW_STEP((launch_bg<float, T, float, 0, false>(a.dz, x, a.dWr, nullptr, g, 1, s)));
     }
     if (a.dbr)
-      BW_STEP(launch_k(colsum_rows_kernel, dim3((unsigned)((E + 255) / 256)), dim3(256), 0, s, false, 1,
+      BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)((E + 255) / 256)), dim3(256), 0, s, false, 1,
                        (const float*)a.dz, (const int32_t*)nullptr, a.dbr, 1, (int)N, E) == cudaSuccess ? 1 : -1);
     // dx = dz Wr: i = t, j = c, k = e
     {
@@ -338,8 +405,13 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
       g.sCi = d; g.sCj = 1;
       BW_STEP((launch_bg<float, float, float, 0, false>(a.dz, a.Wr, a.dx, nullptr, g, 1, s)));
     }
-    BW_STEP(launch_k(dx_assemble_kernel<T>, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1, a.dx,
-                     (const float*)a.dxe, dy, a.expert, a.row, N, d, R, a.residual ? 1 : 0) == cudaSuccess ? 1 : -1);
+    if (tc)
+      BW_STEP(launch_k(dx_assemble_kernel<T, __nv_bfloat16>, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1,
+                       a.dx, (const __nv_bfloat16*)a.dxe16, dy, a.expert, a.row, N, d, R, a.residual ? 1 : 0) ==
+                      cudaSuccess ? 1 : -1);
+    else
+      BW_STEP(launch_k(dx_assemble_kernel<T, float>, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1, a.dx,
+                       (const float*)a.dxe, dy, a.expert, a.row, N, d, R, a.residual ? 1 : 0) == cudaSuccess ? 1 : -1);
   }
 #undef BW_STEP
   return n;

@@ -57,6 +57,7 @@ struct FfnParams {
   const int32_t* tok_of_row;     // [E * R] (combine)
   const float* gate;             // [N] (combine)
   const __nv_bfloat16* resid;    // [N, d] or null (combine)
+  const __nv_bfloat16* hmask;    // [E * R, F]: with MASK, layer 1 keeps its sum where this is > 0
   uint32_t* next_tile;           // zero at launch
   uint32_t* done1;               // [E * NCH], zero at launch
   uint32_t* err;
@@ -144,7 +145,9 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // MB: 128-row weight blocks per tile, all reading one activation tile (compile-time, so the
 // MMA issue loop stays fully unrolled).  NBUF: TMEM accumulator sets (2: the epilogue of
 // a tile overlaps the next tile's MMAs; 1 when two sets do not fit in 512 columns).
-template <int MB, int NBUF>
+// MASK (the backward's dh = (dye W2) * [h > 0]): layer 1's epilogue keeps the sum where the
+// saved forward activation hmask is positive instead of applying ReLU.
+template <int MB, int NBUF, bool MASK>
 __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     ffn_persistent_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
@@ -419,8 +422,17 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
           for (int i = 0; i < 8; ++i) {
             float v0 = __uint_as_float(r[q][2 * i]) + bv, v1 = __uint_as_float(r[q][2 * i + 1]) + bv;
             if (l1) {
-              v0 = fmaxf(v0, 0.f);
-              v1 = fmaxf(v1, 0.f);
+              if (MASK) {  // tokens cb + 2i, + 1 of the chunk (rows past nv are not read)
+                const int j0 = cb + 2 * i;
+                const size_t mr = (size_t)e * p.R + n0 + j0;
+                const float k0 = j0 < nv ? __bfloat162float(p.hmask[mr * p.F + m]) : 0.f;
+                const float k1 = j0 + 1 < nv ? __bfloat162float(p.hmask[(mr + 1) * p.F + m]) : 0.f;
+                v0 = k0 > 0.f ? v0 : 0.f;
+                v1 = k1 > 0.f ? v1 : 0.f;
+              } else {
+                v0 = fmaxf(v0, 0.f);
+                v1 = fmaxf(v1, 0.f);
+              }
             }
             const __nv_bfloat162 pr = __floats2bfloat162_rn(v0, v1);  // h, or ye rounded to bf16
             xw[i * 32 + lane] = *reinterpret_cast<const uint32_t*>(&pr);
@@ -627,6 +639,7 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.STAGES = t.STAGES;
   p.stage_bytes = t.stage_bytes;
   p.combine = L.combine ? 1 : 0;
+  p.hmask = (const __nv_bfloat16*)L.hmask;
   p.w_evict_first = t.NCH == 1 ? 1 : 0;  // several chunks re-read a weight tile
   const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
   const long long tiles = (long long)L.E * t.NCH * (L.F / (FF_BM * t.MB) + L.d / (FF_BM * t.MB));
@@ -635,19 +648,21 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
     return -1;  // tickets and TMA row coordinates are 32-bit
   const int ctas = (int)(tiles < device_sm_count() ? tiles : device_sm_count());
   cudaError_t e;
-#define SMOE_FFN(MBV, NBV)                                                                                         \
+#define SMOE_FFN(MBV, NBV, MK)                                                                                     \
   do {                                                                                                             \
-    auto kern = ffn_persistent_kernel<MBV, NBV>;                                                                   \
+    auto kern = ffn_persistent_kernel<MBV, NBV, MK>;                                                               \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1; \
     e = launch_k(kern, dim3((unsigned)ctas), dim3(ff_threads<MBV>()), (size_t)smem, s, pdl, 1, tmW1, tmX, tmW2, tmH, \
                  tmXp, tmHp, p);                                                                                               \
   } while (0)
-  if (t.MB == 1)
-    SMOE_FFN(1, 2);
-  else if (t.NBUF == 2)
-    SMOE_FFN(2, 2);
-  else
-    SMOE_FFN(2, 1);
+  const bool mk = L.hmask != nullptr;
+  if (t.MB == 1) {
+    if (mk) SMOE_FFN(1, 2, true); else SMOE_FFN(1, 2, false);
+  } else if (t.NBUF == 2) {
+    if (mk) SMOE_FFN(2, 2, true); else SMOE_FFN(2, 2, false);
+  } else {
+    if (mk) SMOE_FFN(2, 1, true); else SMOE_FFN(2, 1, false);
+  }
 #undef SMOE_FFN
   return e == cudaSuccess ? 1 : -1;
 }

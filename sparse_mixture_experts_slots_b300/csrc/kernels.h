@@ -102,6 +102,11 @@ struct BackwardArgs {
   float* dx; float* dWr; float* dbr; float* dW1; float* db1; float* dW2; float* db2;
   // workspace
   float* dye; float* dh; float* dxe; float* dg; float* dz;
+  // tensor-core path (bf16, tc_shape_ok): dh and dxe by the persistent FFN kernel (mask
+  // epilogue) on transposed weights; null otherwise
+  void* W1T; void* W2T;               // [E, d, F], [E, F, d] bf16
+  void* dye16; void* dh16; void* dxe16;  // [E, R, d], [E, R, F], [E, R, d] bf16
+  uint32_t* counters; int counter_words; uint32_t* err;
 };
 int launch_backward(const BackwardArgs& a, cudaStream_t s);
 
@@ -184,6 +189,7 @@ struct FfnLaunch {
   const int32_t* tok_of_row; // [E * R] (combine)
   const float* gate;         // [N] (combine)
   const void* resid;         // [N, d] or null (combine)
+  const void* hmask;         // [E * R, F] or null: layer 1 keeps its sum where hmask > 0 (no ReLU)
   uint32_t* counters;        // ffn_counter_words(E, R) words, zero at launch
   uint32_t* err;
   int E, R, d, F;
