@@ -63,6 +63,11 @@ struct switch_layer {
   void* bw_dye16; // [E, R, d]
   void* bw_dh16;  // [E, R, F]
   void* bw_dxe16; // [E, R, d]
+  int bw_Rpad;
+  void* bw_hT; void* bw_dhT;   // [E, F, Rpad]
+  void* bw_dyeT; void* bw_xeT; // [E, d, Rpad]
+  int32_t* bw_rows_d; int32_t* bw_rows_F;
+  uint32_t* bw_counters; int bw_counter_words;
   cudaEvent_t ev[6];
   bool have_events;
   int last_launches;
@@ -207,6 +212,14 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_dye16 = take(train_tc ? E * R * d * 2 : 0);
   const size_t o_dh16 = take(train_tc ? E * R * F * 2 : 0);
   const size_t o_dxe16 = take(train_tc ? E * R * d * 2 : 0);
+  const size_t Rpad = (R + 63) / 64 * 64;
+  const size_t o_hT = take(train_tc ? E * F * Rpad * 2 : 0);
+  const size_t o_dhT = take(train_tc ? E * F * Rpad * 2 : 0);
+  const size_t o_dyeT = take(train_tc ? E * d * Rpad * 2 : 0);
+  const size_t o_xeT = take(train_tc ? E * d * Rpad * 2 : 0);
+  const size_t o_rows2 = take(train_tc ? 2 * E * sizeof(int32_t) : 0);
+  const size_t cw2 = 1 + E * ((std::max(d, F) + 255) / 256);
+  const size_t o_cnt2 = take(train_tc ? cw2 * sizeof(uint32_t) : 0);
   h->ws_bytes = off;
   if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -241,6 +254,15 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->bw_dye16 = train_tc ? h->ws + o_dye16 : nullptr;
   h->bw_dh16 = train_tc ? h->ws + o_dh16 : nullptr;
   h->bw_dxe16 = train_tc ? h->ws + o_dxe16 : nullptr;
+  h->bw_Rpad = (int)Rpad;
+  h->bw_hT = h->ws + o_hT;
+  h->bw_dhT = h->ws + o_dhT;
+  h->bw_dyeT = h->ws + o_dyeT;
+  h->bw_xeT = h->ws + o_xeT;
+  h->bw_rows_d = reinterpret_cast<int32_t*>(h->ws + o_rows2);
+  h->bw_rows_F = h->bw_rows_d + E;
+  h->bw_counters = reinterpret_cast<uint32_t*>(h->ws + o_cnt2);
+  h->bw_counter_words = (int)cw2;
   if (cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess) {
     cudaFree(h->ws);
     delete h;
@@ -647,6 +669,15 @@ switch_status switch_backward(switch_handle h, const void* x, const float* Wr, c
   a.counters = h->ffn_counters;
   a.counter_words = h->ffn_counter_words;
   a.err = h->err;
+  a.Rpad = h->bw_Rpad;
+  a.hT = h->bw_hT;
+  a.dhT = h->bw_dhT;
+  a.dyeT = h->bw_dyeT;
+  a.xeT = h->bw_xeT;
+  a.rows_d = h->bw_rows_d;
+  a.rows_F = h->bw_rows_F;
+  a.counters2 = h->bw_counters;
+  a.counter2_words = h->bw_counter_words;
   h->last_launches = 0;
   return launched(launch_backward(a, (cudaStream_t)stream), h);
 }

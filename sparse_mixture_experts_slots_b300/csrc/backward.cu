@@ -270,6 +270,41 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16
   }
 }
 
+// out[b][q][p] = (p < lim[b] ? in[b][p][q] : 0) for p < Ppad: an expert block's rows become
+// the contraction axis of a weight gradient, zero past its row count and up to Ppad.
+__global__ void __launch_bounds__(256) transpose_rows_bf16_kernel(const __nv_bfloat16* __restrict__ in,
+                                                                  __nv_bfloat16* __restrict__ out,
+                                                                  const int32_t* __restrict__ lim, int P, int Q,
+                                                                  int Ppad) {
+  __shared__ __nv_bfloat16 t[32][33];
+  const long long b = blockIdx.z;
+  const int p0 = blockIdx.y * 32, q0 = blockIdx.x * 32;
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+  const int np = min(P, lim[b]);
+  const __nv_bfloat16* src = in + b * (long long)P * Q;
+  __nv_bfloat16* dst = out + b * (long long)Ppad * Q;
+  for (int k = ty; k < 32; k += 8) {
+    const int p = p0 + k, q = q0 + tx;
+    t[k][tx] = (p < np && q < Q) ? src[(long long)p * Q + q] : __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    const int q = q0 + k, p = p0 + tx;
+    if (p < Ppad && q < Q) dst[(long long)q * Ppad + p] = t[tx][k];
+  }
+}
+
+__global__ void fill_i32_kernel(int32_t* __restrict__ a, int n, int v) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) a[i] = v;
+}
+
+__global__ void __launch_bounds__(256) bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* __restrict__ out,
+                                                          long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    out[i] = __bfloat162float(in[i]);
+}
+
 static int launch_transpose(const void* in, void* out, int B, int P, int Q, cudaStream_t s) {
   const dim3 grid((unsigned)((Q + 31) / 32), (unsigned)((P + 31) / 32), (unsigned)B);
   transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out),
@@ -315,6 +350,7 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     L.expert_rows = a.expert_rows;
     L.combine = false;
     L.hmask = a.h;
+    L.mode = 1;
     L.counters = a.counters;
     L.err = a.err;
     L.E = E;
@@ -322,6 +358,50 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     L.d = d;
     L.F = F;
     if (R > 0) BW_STEP(launch_ffn_tc(L, s, false));
+    // dW2_e = dye^T h and dW1_e = dh^T xe: an expert's rows become the contraction axis
+    // (transposed, zero past its row count); the kernel's layer 1 with the plain sum, in
+    // bfloat16 into the (now free) transposed-weight buffers, then widened to float32
+    if (R > 0) {
+      const int Rp = a.Rpad;
+      const dim3 gF((unsigned)((F + 31) / 32), (unsigned)(Rp / 32), (unsigned)E);
+      const dim3 gd((unsigned)((d + 31) / 32), (unsigned)(Rp / 32), (unsigned)E);
+      transpose_rows_bf16_kernel<<<gF, 256, 0, s>>>((const __nv_bfloat16*)a.h, (__nv_bfloat16*)a.hT, a.expert_rows, R, F, Rp);
+      transpose_rows_bf16_kernel<<<gF, 256, 0, s>>>((const __nv_bfloat16*)a.dh16, (__nv_bfloat16*)a.dhT, a.expert_rows, R, F,
+                                                    Rp);
+      transpose_rows_bf16_kernel<<<gd, 256, 0, s>>>((const __nv_bfloat16*)a.dye16, (__nv_bfloat16*)a.dyeT, a.expert_rows, R,
+                                                    d, Rp);
+      transpose_rows_bf16_kernel<<<gd, 256, 0, s>>>((const __nv_bfloat16*)a.xe, (__nv_bfloat16*)a.xeT, a.expert_rows, R, d,
+                                                    Rp);
+      fill_i32_kernel<<<(E + 255) / 256, 256, 0, s>>>(a.rows_d, E, d);
+      fill_i32_kernel<<<(E + 255) / 256, 256, 0, s>>>(a.rows_F, E, F);
+      if (cudaGetLastError() != cudaSuccess) return -1;
+      n += 6;
+      for (int wgt = 0; wgt < 2; ++wgt) {
+        // wgt 0: dW2[e, c, f] = sum_r dye[r, c] h[r, f]   (tokens c < d, weight rows f < F)
+        // wgt 1: dW1[e, f, c] = sum_r dh[r, f] xe[r, c]   (tokens f < F, weight rows c < d)
+        if (cudaMemsetAsync(a.counters2, 0, (size_t)a.counter2_words * sizeof(uint32_t), s) != cudaSuccess) return -1;
+        FfnLaunch M{};
+        M.xe = wgt == 0 ? a.dyeT : a.dhT;
+        M.W1 = wgt == 0 ? a.hT : a.xeT;
+        M.W2 = M.W1;
+        M.h = wgt == 0 ? a.W2T : a.W1T;  // output [E * tokens, weight rows] bfloat16
+        M.out = M.h;
+        M.expert_rows = wgt == 0 ? a.rows_d : a.rows_F;
+        M.combine = false;
+        M.mode = 2;
+        M.counters = a.counters2;
+        M.err = a.err;
+        M.E = E;
+        M.R = wgt == 0 ? d : F;
+        M.d = Rp;
+        M.F = wgt == 0 ? F : d;
+        BW_STEP(launch_ffn_tc(M, s, false));
+        const long long cnt = (long long)E * d * F;
+        bf16_to_f32_kernel<<<1184, 256, 0, s>>>((const __nv_bfloat16*)M.h, wgt == 0 ? a.dW2 : a.dW1, cnt);
+        if (cudaGetLastError() != cudaSuccess) return -1;
+        ++n;
+      }
+    }
   }
   // dh = (dye W2_e) * [h > 0]: i = row (<= rows_e), j = f, k = c
   if (!tc) {
@@ -340,10 +420,7 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     g.sAb = (long long)R * d; g.sAi = 1; g.sAk = d;
     g.sBb = (long long)R * F; g.sBj = 1; g.sBk = F;
     g.sCb = (long long)d * F; g.sCi = F; g.sCj = 1;
-    if (tc)
-      BW_STEP((launch_bg<__nv_bfloat16, T, float, 0, false>((const __nv_bfloat16*)a.dye16, hb, a.dW2, nullptr, g, E, s)));
-    else
-      BW_STEP((launch_bg<float, T, float, 0, false>(a.dye, hb, a.dW2, nullptr, g, E, s)));
+    if (!tc) BW_STEP((launch_bg<float, T, float, 0, false>(a.dye, hb, a.dW2, nullptr, g, E, s)));
   }
   // dxe = dh W1_e: i = row, j = c, k = f
   if (!tc) {
@@ -361,10 +438,7 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     g.sAb = (long long)R * F; g.sAi = 1; g.sAk = F;
     g.sBb = (long long)R * d; g.sBj = 1; g.sBk = d;
     g.sCb = (long long)F * d; g.sCi = d; g.sCj = 1;
-    if (tc)
-      BW_STEP((launch_bg<__nv_bfloat16, T, float, 0, false>((const __nv_bfloat16*)a.dh16, xe, a.dW1, nullptr, g, E, s)));
-    else
-      BW_STEP((launch_bg<float, T, float, 0, false>(a.dh, xe, a.dW1, nullptr, g, E, s)));
+    if (!tc) BW_STEP((launch_bg<float, T, float, 0, false>(a.dh, xe, a.dW1, nullptr, g, E, s)));
   }
   // bias gradients
   if (a.db2)

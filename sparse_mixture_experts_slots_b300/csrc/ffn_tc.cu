@@ -63,6 +63,7 @@ struct FfnParams {
   uint32_t* err;
   int E, R, d, F, BN, NCH, LOOK, NA, STAGES, stage_bytes, combine, w_evict_first;
   int MB;                        // 128-row weight blocks per tile (the kernel's template value)
+  int layer2;                    // 0: layer-1 tiles only (a weight gradient)
 };
 
 struct FfTile {
@@ -75,7 +76,7 @@ struct FfTile {
 // Returns false past the last tile.
 __device__ __forceinline__ bool ff_decode(uint32_t t, const FfnParams& p, FfTile& tl) {
   const uint32_t S1 = (uint32_t)p.NCH * (uint32_t)(p.F / (FF_BM * p.MB));
-  const uint32_t S2 = (uint32_t)p.NCH * (uint32_t)(p.d / (FF_BM * p.MB));
+  const uint32_t S2 = p.layer2 ? (uint32_t)p.NCH * (uint32_t)(p.d / (FF_BM * p.MB)) : 0u;
   const uint32_t L = (uint32_t)min(p.LOOK, p.E);
   const uint32_t E = (uint32_t)p.E;
   uint32_t r;
@@ -145,9 +146,11 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // MB: 128-row weight blocks per tile, all reading one activation tile (compile-time, so the
 // MMA issue loop stays fully unrolled).  NBUF: TMEM accumulator sets (2: the epilogue of
 // a tile overlaps the next tile's MMAs; 1 when two sets do not fit in 512 columns).
-// MASK (the backward's dh = (dye W2) * [h > 0]): layer 1's epilogue keeps the sum where the
-// saved forward activation hmask is positive instead of applying ReLU.
-template <int MB, int NBUF, bool MASK>
+// MODE 0: the forward (layer 1: + bias, ReLU).  MODE 1, the backward's dh = (dye W2) *
+// [h > 0]: layer 1 keeps the sum where the saved forward activation hmask is positive.
+// MODE 2, a weight gradient (sum over an expert's rows): layer 1 stores the plain sum, and
+// no layer-2 tile is handed out (p.layer2 = 0).
+template <int MB, int NBUF, int MODE>
 __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     ffn_persistent_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
@@ -422,14 +425,14 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
           for (int i = 0; i < 8; ++i) {
             float v0 = __uint_as_float(r[q][2 * i]) + bv, v1 = __uint_as_float(r[q][2 * i + 1]) + bv;
             if (l1) {
-              if (MASK) {  // tokens cb + 2i, + 1 of the chunk (rows past nv are not read)
+              if (MODE == 1) {  // tokens cb + 2i, + 1 of the chunk (rows past nv are not read)
                 const int j0 = cb + 2 * i;
                 const size_t mr = (size_t)e * p.R + n0 + j0;
                 const float k0 = j0 < nv ? __bfloat162float(p.hmask[mr * p.F + m]) : 0.f;
                 const float k1 = j0 + 1 < nv ? __bfloat162float(p.hmask[(mr + 1) * p.F + m]) : 0.f;
                 v0 = k0 > 0.f ? v0 : 0.f;
                 v1 = k1 > 0.f ? v1 : 0.f;
-              } else {
+              } else if (MODE == 0) {
                 v0 = fmaxf(v0, 0.f);
                 v1 = fmaxf(v1, 0.f);
               }
@@ -593,22 +596,36 @@ size_t ffn_counter_words(int E, int R, int d, int F) { return 1 + (size_t)E * ff
 
 int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   if (L.E == 0 || L.R == 0) return 0;
-  if (!tc_shape_ok(L.F, L.d) || !tc_shape_ok(L.d, L.F)) return -1;
-  const FfnTiling t = ffn_tiling(L.R, L.d, L.F);
+  if (!tc_shape_ok(L.F, L.d) || (L.mode != 2 && !tc_shape_ok(L.d, L.F))) return -1;
+  if (L.mode == 1 && !L.hmask) return -1;
+  FfnTiling t = ffn_tiling(L.R, L.d, L.F);
+  if (L.mode == 2 && t.NA == 2) {  // the contraction is one 64-column atom: one atom per box
+    t.NA = 1;
+    t.stage_bytes = t.MB * FF_ATOM_A + t.BN * FF_BK * 2;
+    t.STAGES = FF_RING / t.stage_bytes < FF_MAX_STAGES ? FF_RING / t.stage_bytes : FF_MAX_STAGES;
+  }
   if (t.STAGES < 2 || t.BN > 256) return -1;
   CUtensorMap tmW1, tmX, tmW2, tmH, tmXp, tmHp;
   if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
   if (!encode_bf16_3d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
-  if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
-  if (!encode_bf16_3d(&tmH, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
+  if (L.mode == 2) {  // no layer 2: its maps are never read
+    tmW2 = tmW1;
+    tmH = tmX;
+  } else {
+    if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
+    if (!encode_bf16_3d(&tmH, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
+  }
   if (t.BN > FF_PB) {  // one atom per box: the boxes of a partly filled chunk
     if (!encode_bf16_3d(&tmXp, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)FF_PB, 1u)) return -1;
-    if (!encode_bf16_3d(&tmHp, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)FF_PB, 1u)) return -1;
+    if (L.mode == 2)
+      tmHp = tmXp;
+    else if (!encode_bf16_3d(&tmHp, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)FF_PB, 1u))
+      return -1;
   } else {
     tmXp = tmX;
     tmHp = tmH;
   }
-  FfnParams p;
+  FfnParams p{};
   p.b1 = (const __nv_bfloat16*)L.b1;
   p.b2 = (const __nv_bfloat16*)L.b2;
   p.h = (__nv_bfloat16*)L.h;
@@ -630,7 +647,8 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   // Layer-2 tiles of an expert are handed out LOOK experts after its layer-1 tiles: a
   // lead of about 8 tiles per CTA, so a layer-1 tile (up to ~3 tiles of queue latency
   // behind a CTA's earlier tiles) is normally stored before anyone needs it.
-  const int per_expert = t.NCH * (L.F / (FF_BM * t.MB) + L.d / (FF_BM * t.MB));
+  const int l2_blocks = L.mode == 2 ? 0 : L.d / (FF_BM * t.MB);
+  const int per_expert = t.NCH * (L.F / (FF_BM * t.MB) + l2_blocks);
   const int ctas_max = device_sm_count();
   p.LOOK = (8 * ctas_max + per_expert - 1) / per_expert;
   if (p.LOOK > L.E) p.LOOK = L.E;
@@ -640,9 +658,10 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.stage_bytes = t.stage_bytes;
   p.combine = L.combine ? 1 : 0;
   p.hmask = (const __nv_bfloat16*)L.hmask;
+  p.layer2 = L.mode == 2 ? 0 : 1;
   p.w_evict_first = t.NCH == 1 ? 1 : 0;  // several chunks re-read a weight tile
   const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
-  const long long tiles = (long long)L.E * t.NCH * (L.F / (FF_BM * t.MB) + L.d / (FF_BM * t.MB));
+  const long long tiles = (long long)L.E * t.NCH * (L.F / (FF_BM * t.MB) + l2_blocks);
   if (tiles >= (1ll << 31) || (long long)L.E * L.R >= (1ll << 31) || (long long)L.E * L.F >= (1ll << 31) ||
       (long long)L.E * L.d >= (1ll << 31))
     return -1;  // tickets and TMA row coordinates are 32-bit
@@ -655,13 +674,15 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
     e = launch_k(kern, dim3((unsigned)ctas), dim3(ff_threads<MBV>()), (size_t)smem, s, pdl, 1, tmW1, tmX, tmW2, tmH, \
                  tmXp, tmHp, p);                                                                                               \
   } while (0)
-  const bool mk = L.hmask != nullptr;
-  if (t.MB == 1) {
-    if (mk) SMOE_FFN(1, 2, true); else SMOE_FFN(1, 2, false);
+  if (L.mode == 2) {  // d < 128: one weight block per tile, two accumulator sets
+    if (t.MB != 1 || t.NBUF != 2) return -1;
+    SMOE_FFN(1, 2, 2);
+  } else if (t.MB == 1) {
+    if (L.mode == 1) SMOE_FFN(1, 2, 1); else SMOE_FFN(1, 2, 0);
   } else if (t.NBUF == 2) {
-    if (mk) SMOE_FFN(2, 2, true); else SMOE_FFN(2, 2, false);
+    if (L.mode == 1) SMOE_FFN(2, 2, 1); else SMOE_FFN(2, 2, 0);
   } else {
-    if (mk) SMOE_FFN(2, 1, true); else SMOE_FFN(2, 1, false);
+    if (L.mode == 1) SMOE_FFN(2, 1, 1); else SMOE_FFN(2, 1, 0);
   }
 #undef SMOE_FFN
   return e == cudaSuccess ? 1 : -1;

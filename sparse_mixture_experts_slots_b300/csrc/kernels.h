@@ -107,6 +107,11 @@ struct BackwardArgs {
   void* W1T; void* W2T;               // [E, d, F], [E, F, d] bf16
   void* dye16; void* dh16; void* dxe16;  // [E, R, d], [E, R, F], [E, R, d] bf16
   uint32_t* counters; int counter_words; uint32_t* err;
+  // weight gradients on the same kernel (mode 2): expert rows as the contraction axis
+  int Rpad;                                   // R rounded up to 64
+  void* hT; void* dhT; void* dyeT; void* xeT;   // [E, F, Rpad], [E, F, Rpad], [E, d, Rpad], [E, d, Rpad]
+  int32_t* rows_d; int32_t* rows_F;            // [E] filled with d, F
+  uint32_t* counters2; int counter2_words;      // 1 + E * ceil(max(d, F) / 256)
 };
 int launch_backward(const BackwardArgs& a, cudaStream_t s);
 
@@ -189,7 +194,9 @@ struct FfnLaunch {
   const int32_t* tok_of_row; // [E * R] (combine)
   const float* gate;         // [N] (combine)
   const void* resid;         // [N, d] or null (combine)
-  const void* hmask;         // [E * R, F] or null: layer 1 keeps its sum where hmask > 0 (no ReLU)
+  const void* hmask;         // [E * R, F] (mode 1): layer 1 keeps its sum where hmask > 0
+  int mode;                  // 0 forward; 1 backward dh (mask, no bias/ReLU); 2 weight gradient
+                             // (layer 1 only, plain sum; d = the padded row count)
   uint32_t* counters;        // ffn_counter_words(E, R) words, zero at launch
   uint32_t* err;
   int E, R, d, F;
