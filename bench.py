@@ -243,8 +243,9 @@ FP32_ALU_TFLOPS = 148 * 128 * 2 * 2.032 / 1e3  # SMs x FP32 lanes x FMA x max SM
 
 def run_train(args, shape):
     """One step = switch_forward in training mode + switch_backward (fixed dy, w_aux = 1,
-    w_z = 1e-3).  The backward's products run on CUDA cores: its roofline is the float32
-    ALU peak (unit counts x clock)."""
+    w_z = 1e-3).  With bf16 tensor-core shapes the backward's expert products run on the
+    tensor cores (roofline: the bf16 peak); otherwise on CUDA cores (the float32 ALU peak,
+    unit counts x clock)."""
     if not torch.cuda.is_available():
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
         return 1
@@ -283,6 +284,7 @@ def run_train(args, shape):
     bwd_flops = 4 * 2.0 * K * shape.d_model * shape.d_ff + 2 * 2.0 * shape.N * shape.E * shape.d_model
     tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
     hbm, tc_burst, tc_sust, peak_src = peaks()
+    tc_shapes = shape.dtype == "bf16" and shape.d_model % 128 == 0 and shape.d_ff % 128 == 0
     print(json.dumps({
         "metric": METRIC + " (training step: forward + backward)", "value": shape.N / (step_ms * 1e-3),
         "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -290,11 +292,16 @@ def run_train(args, shape):
         "dtype": "bf16" if shape.dtype == "bf16" else "f32", "data": "synthetic",
         "config": config_of(shape, argparse.Namespace(gpus=1, top_k=1)) | {"mode": "train"},
         "forward_ms": fwd_ms, "backward_ms": bwd_ms, "kept_rows": K,
-        "roofline": {"bound": "alu", "kernel": "bgemm_kernel (backward products)", "achieved": tf,
-                     "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS,
-                     "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 (FMA) x 2.032 GHz",
-                     "frac_of_bf16_tensor_burst": tf / tc_burst,
-                     "algorithmic_flops": bwd_flops, "traffic": None},
+        "roofline": ({"bound": "tensor", "kernel": "switch_backward (expert products: ffn_persistent_kernel modes 1-2)",
+                      "achieved": tf, "peak": tc_burst, "unit": "TFLOP/s", "frac": tf / tc_burst,
+                      "peak_source": f"{peak_src} bf16_tflops (cuBLAS bf16 GEMM, burst)",
+                      "algorithmic_flops": bwd_flops, "traffic": None,
+                      "note": "whole backward time, transposes and float32 widening included"}
+                     if tc_shapes else
+                     {"bound": "alu", "kernel": "bgemm_kernel (backward products)", "achieved": tf,
+                      "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS,
+                      "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 (FMA) x 2.032 GHz",
+                      "algorithmic_flops": bwd_flops, "traffic": None}),
     }), flush=True)
     return 0
 

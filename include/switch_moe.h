@@ -238,7 +238,9 @@ SWITCH_API switch_status switch_forward_host(switch_handle h, const void* x_host
  *   x [N, d] act, Wr [E, d] f32, W1 [E, d_ff, d], W2 [E, d, d_ff] act, dy [N, d] act.
  *   Outputs (float32, caller-owned): dx [N, d], dWr [E, d], dbr [E], dW1 [E, d_ff, d],
  *   db1 [E, d_ff], dW2 [E, d, d_ff], db2 [E, d]; dbr, db1, db2 may be NULL.
- * The matrix products run on CUDA cores (float32 accumulation).
+ * With bfloat16 and d, d_ff multiples of 128 the expert products run on the tensor cores
+ * (dye, dh, dxe and the weight gradients pass through bfloat16; float32 accumulation);
+ * otherwise, and for the router's products, on CUDA cores in float32.
  */
 SWITCH_API switch_status switch_backward(switch_handle h, const void* x, const float* Wr, const void* W1,
                               const void* W2, const switch_route_out* r, const void* dy, float w_aux,
