@@ -119,3 +119,13 @@ def test_top2_capacity_and_config(lib):
         assert lib.switch_capacity(ctypes.byref(cfg)) == so.capacity(2 * c, T, E)
     one = SwitchConfig(1, 64, 128, 256, 1, 1.0, 0, 0.01, 1, FLAG_TOP2)  # top-2 needs two experts
     assert lib.switch_capacity(ctypes.byref(one)) == -1
+
+
+def test_flag_constants_match_the_header():
+    from sparse_mixture_experts_slots_b300 import _lib
+    text = open(HEADER, encoding="utf-8").read()
+    flags = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define SWITCH_FLAG_(\w+)\s+0x([0-9a-fA-F]+)u", text)}
+    assert flags, "no SWITCH_FLAG_ definitions found"
+    for name, value in flags.items():
+        assert getattr(_lib, "FLAG_" + name) == value, name
+    assert len(set(flags.values())) == len(flags), "flag bits overlap"
