@@ -57,6 +57,8 @@ struct switch_layer {
   float* bw_dxe;  // [E, R, d]
   float* bw_dg;   // [N]
   float* bw_dz;   // [N, E]
+  float* bw_part; // [nsplit, E, d]: per-token-chunk partial sums of dWr and dbr
+  int bw_nsplit;
   // tensor-core backward (bf16 with tensor-core FFN shapes): transposed weights, bf16 copies
   void* bw_W1T;   // [E, d, F]
   void* bw_W2T;   // [E, F, d]
@@ -206,6 +208,12 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_bdxe = take(train ? E * R * d * sizeof(float) : 0);
   const size_t o_bdg = take(train ? N * sizeof(float) : 0);
   const size_t o_bdz = take(train ? N * E * sizeof(float) : 0);
+  // token chunks of the router's weight-gradient sums: ~256 tokens each, the partials
+  // [nsplit, E, d] kept under 64 M floats
+  size_t nsplit = N > 0 ? (N + 255) / 256 : 1;
+  const size_t cap = std::max<size_t>(1, ((size_t)64 << 20) / std::max<size_t>(1, E * d));
+  if (nsplit > cap) nsplit = cap;
+  const size_t o_bpart = take(train ? nsplit * E * d * sizeof(float) : 0);
   const bool train_tc = train && cfg->dtype == SWITCH_BF16 && tc_shape_ok((int)F, (int)d) && tc_shape_ok((int)d, (int)F);
   const size_t o_w1t = take(train_tc ? E * F * d * 2 : 0);
   const size_t o_w2t = take(train_tc ? E * F * d * 2 : 0);
@@ -249,6 +257,8 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->bw_dxe = reinterpret_cast<float*>(h->ws + o_bdxe);
   h->bw_dg = reinterpret_cast<float*>(h->ws + o_bdg);
   h->bw_dz = reinterpret_cast<float*>(h->ws + o_bdz);
+  h->bw_part = reinterpret_cast<float*>(h->ws + o_bpart);
+  h->bw_nsplit = (int)nsplit;
   h->bw_W1T = train_tc ? h->ws + o_w1t : nullptr;
   h->bw_W2T = train_tc ? h->ws + o_w2t : nullptr;
   h->bw_dye16 = train_tc ? h->ws + o_dye16 : nullptr;
@@ -678,6 +688,8 @@ switch_status switch_backward(switch_handle h, const void* x, const float* Wr, c
   a.rows_F = h->bw_rows_F;
   a.counters2 = h->bw_counters;
   a.counter2_words = h->bw_counter_words;
+  a.part = h->bw_part;
+  a.nsplit = h->bw_nsplit;
   h->last_launches = 0;
   return launched(launch_backward(a, (cudaStream_t)stream), h);
 }

@@ -73,7 +73,8 @@ __global__ void __launch_bounds__(BG_THREADS) bgemm_kernel(const TA* __restrict_
   const int b = blockIdx.z;
   const int Mb = g.limM ? min(g.M, g.limM[b]) : g.M;
   const int Nb = g.limN ? min(g.N, g.limN[b]) : g.N;
-  const int Kb = g.limK ? min(g.K, g.limK[b]) : g.K;
+  int Kb = g.limK ? min(g.K, g.limK[b]) : g.K;
+  if (g.Ktot > 0) Kb = (int)min((long long)Kb, g.Ktot - (long long)b * g.K);
   const int i0 = blockIdx.y * BM, j0 = blockIdx.x * BG_N;
   if (i0 >= Mb || j0 >= Nb) return;
   const TA* Ab = A + (long long)b * g.sAb;
@@ -294,6 +295,50 @@ __global__ void __launch_bounds__(256) transpose_rows_bf16_kernel(const __nv_bfl
   }
 }
 
+// 64 x 64 tiles with 16-byte loads and stores (P, Q multiples of 64): out[b][q][p] = in[b][p][q].
+__global__ void __launch_bounds__(256) transpose64_bf16_kernel(const __nv_bfloat16* __restrict__ in,
+                                                               __nv_bfloat16* __restrict__ out, int P, int Q) {
+  __shared__ __nv_bfloat16 t[64][64 + 8];
+  const long long b = blockIdx.z;
+  const int p0 = blockIdx.y * 64, q0 = blockIdx.x * 64;
+  const __nv_bfloat16* src = in + b * (long long)P * Q;
+  __nv_bfloat16* dst = out + b * (long long)P * Q;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {  // 512 vectors of 8 along q
+    const int v = threadIdx.x + 256 * i;
+    const int r = v / 8, cg = v % 8;
+    const uint4 val = *reinterpret_cast<const uint4*>(src + (long long)(p0 + r) * Q + q0 + 8 * cg);
+    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[r][8 * cg + k] = e[k];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {  // 512 vectors of 8 along p
+    const int v = threadIdx.x + 256 * i;
+    const int q = v / 8, pg = v % 8;
+    uint4 val;
+    __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&val);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) e[k] = t[8 * pg + k][q];
+    *reinterpret_cast<uint4*>(dst + (long long)(q0 + q) * P + p0 + 8 * pg) = val;
+  }
+}
+
+// part[s][c] = sum of in[t][c] over the tokens t of chunk s (kc tokens each, the last one
+// shorter): thread per (chunk, column).
+__global__ void __launch_bounds__(256) colsum_split_kernel(const float* __restrict__ in, float* __restrict__ part,
+                                                           long long N, int W, int kc) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int sidx = blockIdx.y;
+  if (c >= W) return;
+  const long long t0 = (long long)sidx * kc;
+  const long long t1 = min(N, t0 + kc);
+  float acc = 0.f;
+  for (long long t = t0; t < t1; ++t) acc += in[t * W + c];
+  part[(long long)sidx * W + c] = acc;
+}
+
 __global__ void fill_i32_kernel(int32_t* __restrict__ a, int n, int v) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) a[i] = v;
@@ -306,6 +351,11 @@ __global__ void __launch_bounds__(256) bf16_to_f32_kernel(const __nv_bfloat16* _
 }
 
 static int launch_transpose(const void* in, void* out, int B, int P, int Q, cudaStream_t s) {
+  if (P % 64 == 0 && Q % 64 == 0) {
+    transpose64_bf16_kernel<<<dim3((unsigned)(Q / 64), (unsigned)(P / 64), (unsigned)B), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out), P, Q);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+  }
   const dim3 grid((unsigned)((Q + 31) / 32), (unsigned)((P + 31) / 32), (unsigned)B);
   transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out),
                                              P, Q);
@@ -458,18 +508,28 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     const float z_coef = a.w_z * 2.f / ((float)a.G * (float)a.T);
     BW_STEP(launch_k(router_bwd_kernel, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1, a.logits, a.expert,
                      (const float*)a.dg, a.raw, a.dz, N, a.T, E, a.G, aux_coef, z_coef) == cudaSuccess ? 1 : -1);
-    // dWr = dz^T x: i = e, j = c, k = t
+    // dWr = dz^T x (i = e, j = c, k = t) and dbr = sum_t dz_t, split over nsplit token chunks:
+    // partial results per chunk, then their sum in chunk order
+    const int ns = a.nsplit;
+    const int kc = (int)((N + ns - 1) / ns);
     {
       BgemmArgs g{};
-      g.M = E; g.N = d; g.K = (int)N;
-      g.sAi = 1; g.sAk = E;
-      g.sBj = 1; g.sBk = d;
-      g.sCi = d; g.sCj = 1;
-      BW_STEP((launch_bg<float, T, float, 0, false>(a.dz, x, a.dWr, nullptr, g, 1, s)));
+      g.M = E; g.N = d; g.K = kc; g.Ktot = N;
+      g.sAb = (long long)kc * E; g.sAi = 1; g.sAk = E;
+      g.sBb = (long long)kc * d; g.sBj = 1; g.sBk = d;
+      g.sCb = (long long)E * d; g.sCi = d; g.sCj = 1;
+      BW_STEP((launch_bg<float, T, float, 0, false>(a.dz, x, a.part, nullptr, g, ns, s)));
+      BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)(((long long)E * d + 255) / 256)), dim3(256), 0, s,
+                       false, 1, (const float*)a.part, (const int32_t*)nullptr, a.dWr, 1, ns, E * d) == cudaSuccess
+                  ? 1 : -1);
     }
-    if (a.dbr)
+    if (a.dbr) {
+      colsum_split_kernel<<<dim3((unsigned)((E + 255) / 256), (unsigned)ns), 256, 0, s>>>(a.dz, a.part, N, E, kc);
+      if (cudaGetLastError() != cudaSuccess) return -1;
+      ++n;
       BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)((E + 255) / 256)), dim3(256), 0, s, false, 1,
-                       (const float*)a.dz, (const int32_t*)nullptr, a.dbr, 1, (int)N, E) == cudaSuccess ? 1 : -1);
+                       (const float*)a.part, (const int32_t*)nullptr, a.dbr, 1, ns, E) == cudaSuccess ? 1 : -1);
+    }
     // dx = dz Wr: i = t, j = c, k = e
     {
       BgemmArgs g{};

@@ -82,6 +82,7 @@ struct RouteArgs {
 struct BgemmArgs {
   int M, N, K;
   const int32_t* limM; const int32_t* limN; const int32_t* limK;  // per-batch limits or null
+  long long Ktot;      // > 0: batch b covers k in [b K, min((b + 1) K, Ktot)) (a split of one K)
   long long sAb, sAi, sAk, sBb, sBj, sBk, sCb, sCi, sCj, sMb, sMi, sMj;
 };
 
@@ -112,6 +113,8 @@ struct BackwardArgs {
   void* hT; void* dhT; void* dyeT; void* xeT;   // [E, F, Rpad], [E, F, Rpad], [E, d, Rpad], [E, d, Rpad]
   int32_t* rows_d; int32_t* rows_F;            // [E] filled with d, F
   uint32_t* counters2; int counter2_words;      // 1 + E * ceil(max(d, F) / 256)
+  // split sums over tokens (dWr, dbr): partial products / sums, nsplit of them
+  float* part; int nsplit;                      // [nsplit, E, d] floats (>= nsplit * E)
 };
 int launch_backward(const BackwardArgs& a, cudaStream_t s);
 
