@@ -12,9 +12,12 @@
 // the aux loss's gradient flows through P and not through the hard counts f, and the z-loss
 // through the log-sum-exp (070 page, section 核心思想与公式).
 //
-// The matrix products run in one batched kernel with arbitrary strides on both operands
-// and per-batch limits on M, N or K (an expert's row count), float32 accumulation on CUDA
-// cores.
+// With bfloat16 and tensor-core shapes the four expert products run on the persistent
+// tcgen05 FFN kernel (ffn_tc.cu): dh -> dxe as its two layers over transposed W2, W1 (mode 1,
+// a mask epilogue), dW2 and dW1 as layer-1-only launches whose contraction axis is an
+// expert's rows (mode 2).  The router's products, and every product for float32 or other
+// widths, run in one batched float32 kernel on CUDA cores with arbitrary strides and
+// per-batch limits on M, N or K.
 #include "common.cuh"
 #include "kernels.h"
 
