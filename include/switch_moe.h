@@ -78,8 +78,10 @@ typedef enum { SWITCH_F32 = 0, SWITCH_BF16 = 1 } switch_dtype;
 #define SWITCH_FLAG_TOP2          0x10u
 /* Training: switch_forward keeps the dispatched rows, the hidden activations, the
  * expert outputs and the router logits in the workspace (unfused FFN and combine) for
- * switch_backward; the workspace grows by float32 gradient scratch (2 E G C d + E G C d_ff
- * + N + N E floats). */
+ * switch_backward.  The workspace grows by float32 gradient scratch (2 E R d + E R d_ff +
+ * N + N E floats, R = G min(C, T), plus the router's per-chunk partials, at most 64 M
+ * floats) and, with bfloat16 and d, d_ff multiples of 128, by two transposed copies of the
+ * expert weights (2 E d d_ff bfloat16) and bfloat16 copies of the backward's activations. */
 #define SWITCH_FLAG_TRAINING      0x20u
 
 typedef struct {
