@@ -1,8 +1,9 @@
-"""The N > 1 path of bench.py on CPU: two gloo ranks (no GPU).
+"""Host-side logic of bench.py on CPU (no GPU).
 
-Checks the pieces the GPU arm uses across ranks: each rank routes its own batch while the
-expert weights are replicated, the timed region's barrier, the max over ranks, and the
-whole-job throughput; and that the reference arm runs on rank 0 only.
+The N > 1 path as two gloo ranks: each rank routes its own batch while the expert weights
+are replicated, the timed region's barrier, the max over ranks and the whole-job
+throughput; the reference arm runs on rank 0 only.  And the roofline's algorithmic byte /
+FLOP counts against a hand count.
 """
 import json
 import os
@@ -72,3 +73,21 @@ def test_reference_arm_runs_on_rank0_only():
                         "1", "--warmup", "1", "--gpus", "2"], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=300)
     assert p.returncode == 0 and p.stdout.strip() == ""
+
+
+def test_roofline_arithmetic_matches_the_hand_count():
+    # switch-base with every expert used and 7484 kept rows: the FFN streams both weight
+    # matrices of 128 experts (2 * 128 * 3072 * 768 * 2 B) and moves each kept row in and out
+    # (2 * 7484 * 768 * 2 B); FLOPs 4 K d d_ff
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from gen import WORKLOADS
+    shape = WORKLOADS["switch-base-e128"]
+    rows = np.full(shape.E, 7484 // shape.E, dtype=np.int64)
+    rows[: 7484 - rows.sum()] += 1
+    w = bench.algorithmic(shape, rows, shape.N)
+    assert w["kept_rows"] == 7484 and w["experts_used"] == 128
+    assert w["ffn_bytes"] == 2 * 128 * 3072 * 768 * 2 + 2 * 7484 * 768 * 2 == 1230950400
+    assert w["ffn_flops"] == 4.0 * 7484 * 768 * 3072
+    assert bench.FP32_ALU_TFLOPS == 148 * 128 * 2 * 2.032 / 1e3
