@@ -410,7 +410,13 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     L.R = R;
     L.d = d;
     L.F = F;
-    if (R > 0) BW_STEP(launch_ffn_tc(L, s, false));
+    if (R > 0) {
+      BW_STEP(launch_ffn_tc(L, s, false));
+    } else {  // no expert rows: the weight gradients are zero
+      if (cudaMemsetAsync(a.dW1, 0, (size_t)E * F * d * sizeof(float), s) != cudaSuccess ||
+          cudaMemsetAsync(a.dW2, 0, (size_t)E * F * d * sizeof(float), s) != cudaSuccess)
+        return -1;
+    }
     // dW2_e = dye^T h and dW1_e = dh^T xe: an expert's rows become the contraction axis
     // (transposed, zero past its row count); the kernel's layer 1 with the plain sum, in
     // bfloat16 into the (now free) transposed-weight buffers, then widened to float32
@@ -505,6 +511,10 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     else
       BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)(((long long)E * F + 255) / 256)), dim3(256), 0, s,
                        false, 1, (const float*)a.dh, a.expert_rows, a.db1, E, R, F) == cudaSuccess ? 1 : -1);
+  }
+  if (N == 0) {  // no tokens: the router's gradients are zero
+    if (cudaMemsetAsync(a.dWr, 0, (size_t)E * d * sizeof(float), s) != cudaSuccess) return -1;
+    if (a.dbr && cudaMemsetAsync(a.dbr, 0, (size_t)E * sizeof(float), s) != cudaSuccess) return -1;
   }
   if (N > 0) {
     const float aux_coef = a.w_aux * a.alpha * (float)E / ((float)a.G * (float)a.T * (float)a.T);  // f = raw / T
