@@ -15,7 +15,7 @@ Pages cited (title, then the section / equation / table):
   [070]  "开源 AI 论文复现实验与代码解读 · 070" on MoE routing load collapse
          (zffjzz.top)
 
-Readings taken where the pages leave a step open (each is listed in the design doc):
+Readings taken where the pages leave a step open:
   * argmax is taken over the logits z (softmax is monotone); ties go to the
     lowest expert index, the NumPy rule [070, 核心思想与公式].
   * capacity C = ceil(c*T/E), with c*T/E snapped to an integer when it is within
@@ -174,27 +174,41 @@ class Route:
         return int((~self.keep).sum())
 
 
+def _choice_scores(z: np.ndarray, choice_logits: Optional[dict], T: int) -> np.ndarray:
+    """The scores the choice step ranks: z, with the given groups' rows replaced."""
+    if not choice_logits:
+        return z
+    zc = z.copy()
+    for g, zg in choice_logits.items():
+        zc[g * T:(g + 1) * T] = np.asarray(zg, dtype=np.float64)
+    return zc
+
+
 def route(x, Wr, br, G: int, T: int, E: int, capacity_factor: float, alpha: float = 1e-2,
-          capacity_override: int = 0, logits_override: Optional[dict] = None) -> Route:
+          capacity_override: int = 0, choice_logits: Optional[dict] = None) -> Route:
     """Router, top-1 choice, slots, capacity mask and load statistics per group.
 
     Steps in the order of the pipeline in [042, §三]: router probabilities in
     float (here float64), one expert per token, load statistics and aux loss,
-    then capacity truncation.  `logits_override` maps a group index to a [T, E]
-    array of logits to use for that group instead of the float64 ones (used
-    when the GPU's float32 logits sit within 1e-6 of a tie).
+    then capacity truncation.
+
+    `choice_logits` maps a group index to a [T, E] array of logits from which
+    that group's expert choices are taken instead of from the float64 logits.
+    Only the choice step reads it: it decides which expert each token goes to,
+    hence slots, capacity mask and the counts f, while the probabilities, the
+    gate values p_{t, e*} of the chosen experts, P and the z-loss stay float64.
+    It is used where another implementation's float32 logits of a token sit
+    within 1e-6 of a tie, so that rounding, not the method, picked between the
+    two experts ([070, 核心思想与公式]: the tie rule decides the choice only).
     """
     x = np.asarray(x)
     N = G * T
     assert x.shape[0] == N
     C = capacity(capacity_factor, T, E, capacity_override)
     z = router_logits(x, Wr, br)
-    if logits_override:
-        z = z.copy()
-        for g, zg in logits_override.items():
-            z[g * T:(g + 1) * T] = np.asarray(zg, dtype=np.float64)
+    zc = _choice_scores(z, choice_logits, T)
     p = softmax(z) if N > 0 else np.zeros((0, E))
-    a = top1(z) if N > 0 else np.zeros(0, dtype=np.int64)
+    a = top1(zc) if N > 0 else np.zeros(0, dtype=np.int64)
     gate = p[np.arange(N), a] if N > 0 else np.zeros(0)
 
     slot = np.empty(N, dtype=np.int64)
@@ -296,12 +310,12 @@ def combine(r: Route, outputs: dict, tokens: Sequence[int], d: int) -> np.ndarra
 
 def forward(x, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor: float,
             alpha: float = 1e-2, capacity_override: int = 0,
-            tokens: Optional[Sequence[int]] = None, logits_override: Optional[dict] = None):
+            tokens: Optional[Sequence[int]] = None, choice_logits: Optional[dict] = None):
     """The whole layer: route, then expert FFN and combine on `tokens` (default: all).
 
     Returns (route, y[tokens], ungated expert outputs by token).
     """
-    r = route(x, Wr, br, G, T, E, capacity_factor, alpha, capacity_override, logits_override)
+    r = route(x, Wr, br, G, T, E, capacity_factor, alpha, capacity_override, choice_logits)
     N = G * T
     toks = np.arange(N) if tokens is None else np.asarray(tokens, dtype=np.int64)
     outs = expert_outputs(x, r, W1, b1, W2, b2, toks)
@@ -370,25 +384,24 @@ def top2(z: np.ndarray):
 
 
 def route_top2(x, Wr, br, G: int, T: int, E: int, capacity_factor: float, alpha: float = 1e-2,
-               capacity_override: int = 0, logits_override: Optional[dict] = None) -> Route2:
+               capacity_override: int = 0, choice_logits: Optional[dict] = None) -> Route2:
     """Top-2 routing per group: choices, gates, slots, capacity mask and statistics.
 
     Gates: softmax over the two kept scores, so they add to 1 [moe, 路由器只开两条线].
     Capacity: ceil(2 c T / E), twice the top-1 capacity [card, 方法适配].  Slots: the
     first choices of the group in sequence order, then its second choices in sequence
     order, each expert's second choices numbered after its kept first choices.
+    `choice_logits` (as in `route`) decides the two choices of the given groups; the
+    gates are then the softmax over the two chosen experts' float64 scores.
     """
     assert E >= 2
     x = np.asarray(x)
     N = G * T
     C = capacity(2.0 * capacity_factor, T, E, capacity_override)
     z = router_logits(x, Wr, br)
-    if logits_override:
-        z = z.copy()
-        for g, zg in logits_override.items():
-            z[g * T:(g + 1) * T] = np.asarray(zg, dtype=np.float64)
+    zc = _choice_scores(z, choice_logits, T)
     p = softmax(z) if N > 0 else np.zeros((0, E))
-    a1, a2 = top2(z) if N > 0 else (np.zeros(0, np.int64), np.zeros(0, np.int64))
+    a1, a2 = top2(zc) if N > 0 else (np.zeros(0, np.int64), np.zeros(0, np.int64))
     z1 = z[np.arange(N), a1] if N > 0 else np.zeros(0)
     z2 = z[np.arange(N), a2] if N > 0 else np.zeros(0)
     gate = 1.0 / (1.0 + np.exp(z2 - z1))       # exp(z1) / (exp(z1) + exp(z2))
@@ -477,7 +490,7 @@ def expert_outputs_top2(x, r: Route2, W1, b1, W2, b2, tokens: Optional[Sequence[
 
 def backward(x, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor: float, dy,
              w_aux: float = 0.0, w_z: float = 0.0, alpha: float = 1e-2, capacity_override: int = 0,
-             residual: bool = False, logits_override: Optional[dict] = None) -> dict:
+             residual: bool = False, choice_logits: Optional[dict] = None) -> dict:
     """Gradients of L = sum(dy * y) + w_aux * aux_loss + w_z * z_loss for the top-1 layer.
 
     The choice, the slots and the capacity mask are held fixed (they are piecewise
@@ -495,7 +508,7 @@ def backward(x, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor:
     W2 = np.asarray(W2, dtype=np.float64)
     N, d = x.shape
     F = W1.shape[1]
-    r = route(x, Wr, br, G, T, E, capacity_factor, alpha, capacity_override, logits_override)
+    r = route(x, Wr, br, G, T, E, capacity_factor, alpha, capacity_override, choice_logits)
     p = r.probs
     dx = dy.copy() if residual else np.zeros_like(x)
     dW1 = np.zeros_like(W1)

@@ -8,10 +8,14 @@ Comparison rules:
     ||y_t - y_ref,t|| <= 1e-2 ||y_ref,t|| (the elementwise bound alone would pass an
     all-zero output at these init scales), and y_t == 0 exactly for dropped tokens;
   * ungated expert output rows: ||ye_row - o_ref|| <= 1e-2 ||o_ref||.
+  * router logits (when written): |z - z_ref| <= 1e-5 on every logit, compared with the
+    float64 oracle before anything else.
 Near ties: where any token's top-two float32 logits (GPU) or float64 logits
-(oracle) lie within 1e-6, that token's whole group is routed by the oracle from
-the GPU's own float32 logits, because one flipped choice shifts every later slot
-of that expert in the group.
+(oracle) lie within 1e-6, the choices of that token's whole group are taken by
+the oracle from the GPU's own float32 logits (the oracle's dispatch stage: one
+flipped choice shifts every later slot of that expert in the group).  Only the
+choices move: probabilities, gates, P, balance, aux and z-loss are still the
+float64 oracle's values for every token.
 """
 from __future__ import annotations
 
@@ -24,6 +28,7 @@ REL_FLOAT = 1e-5
 Y_ATOL, Y_RTOL = 1e-2, 1e-2
 ROW_REL_L2 = 1e-2
 TIE_EPS = 1e-6
+LOGIT_ABS = 1e-5
 
 
 def to_np(t):
@@ -39,7 +44,9 @@ def make_layer(shape, **kw):
 
 
 def oracle_route(inp, shape, gpu_logits: np.ndarray | None = None):
-    """Oracle routing; groups with near ties are routed from the GPU's logits."""
+    """Oracle routing; in groups with near ties the GPU's logits decide the choices.
+
+    Returns (route, substituted group indices)."""
     x = to_np(inp["x"])
     Wr = to_np(inp["Wr"])
     br = to_np(inp["br"]) if inp["br"] is not None else None
@@ -51,8 +58,21 @@ def oracle_route(inp, shape, gpu_logits: np.ndarray | None = None):
         if subst:
             over = {g: gpu_logits[g * shape.T:(g + 1) * shape.T] for g in subst}
             r = so.route(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor,
-                         capacity_override=shape.capacity_override, logits_override=over)
+                         capacity_override=shape.capacity_override, choice_logits=over)
     return r, subst
+
+
+def near_tie_tokens(gpu_logits: np.ndarray, ref_logits: np.ndarray) -> int:
+    """Tokens whose top-two logits (GPU float32 or oracle float64) lie within TIE_EPS."""
+    return int((so.ties_within(gpu_logits, TIE_EPS) | so.ties_within(ref_logits, TIE_EPS)).sum())
+
+
+def check_logits(gpu_logits: np.ndarray, ref: so.Route, what: str = "logits"):
+    """Every float32 logit within LOGIT_ABS of the float64 oracle's (never substituted)."""
+    err = np.abs(np.asarray(gpu_logits, dtype=np.float64) - ref.logits)
+    worst = float(err.max()) if err.size else 0.0
+    assert worst <= LOGIT_ABS, f"{what}: max |z - z_ref| = {worst:.3e} > {LOGIT_ABS}"
+    return worst
 
 
 def rel_close(a, b, rel=REL_FLOAT, what=""):
@@ -116,6 +136,36 @@ def sample_tokens(ref: so.Route, n: int, seed: int = 0) -> np.ndarray:
     return np.sort(np.array(pick, dtype=np.int64))
 
 
+def structured_tokens(ref: so.Route, chunk: int = 256, max_experts: int | None = None, seed: int = 0) -> np.ndarray:
+    """Tokens at the edges of each expert block: the rows the FFN's tiling treats apart.
+
+    Per expert (all of them, or `max_experts` of them: a random draw plus the fullest and the
+    emptiest non-empty expert), the tokens dispatched to its first and last kept row and to
+    the rows on both sides of every `chunk`-row boundary of its block."""
+    kept = np.flatnonzero(ref.keep)
+    E = ref.expert_rows.size
+    experts = np.flatnonzero(ref.expert_rows > 0)
+    if max_experts is not None and experts.size > max_experts:
+        rng = np.random.default_rng(seed)
+        fullest = experts[np.argmax(ref.expert_rows[experts])]
+        emptiest = experts[np.argmin(ref.expert_rows[experts])]
+        experts = np.unique(np.concatenate([rng.choice(experts, size=max_experts - 2, replace=False),
+                                            [fullest, emptiest]]))
+    tok_of = {}
+    for t in kept:
+        e = int(ref.expert[t])
+        tok_of.setdefault(e, {})[int(ref.row[t])] = int(t)
+    pick = []
+    for e in experts:
+        n = int(ref.expert_rows[e])
+        rows = {0, n - 1}
+        for c in range(chunk, n, chunk):
+            rows.update((c - 1, c))
+        pick += [tok_of[int(e)][r] for r in rows if r in tok_of.get(int(e), {})]
+    assert E == 0 or experts.size == 0 or pick, "no kept token found at an expert block edge"
+    return np.unique(np.asarray(pick, dtype=np.int64))
+
+
 def oracle_outputs(inp, ref: so.Route, tokens: np.ndarray) -> dict:
     """Ungated fp64 expert outputs for the kept tokens among `tokens` (weights copied per expert)."""
     x = inp["x"]
@@ -174,8 +224,8 @@ def top3_near_ties(z: np.ndarray, eps: float) -> np.ndarray:
 
 
 def oracle_route_top2(inp, shape, gpu_logits: np.ndarray):
-    """Oracle top-2 routing; groups with a near tie among a token's top three logits (GPU or
-    oracle) are routed from the GPU's own float32 logits."""
+    """Oracle top-2 routing; in groups with a near tie among a token's top three logits (GPU
+    or oracle) the GPU's own float32 logits decide the two choices."""
     x = to_np(inp["x"])
     Wr = to_np(inp["Wr"])
     br = to_np(inp["br"]) if inp["br"] is not None else None
@@ -188,7 +238,7 @@ def oracle_route_top2(inp, shape, gpu_logits: np.ndarray):
         if subst:
             over = {g: gpu_logits[g * shape.T:(g + 1) * shape.T] for g in subst}
             r = so.route_top2(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor,
-                              capacity_override=shape.capacity_override, logits_override=over)
+                              capacity_override=shape.capacity_override, choice_logits=over)
     return r, subst
 
 

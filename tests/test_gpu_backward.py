@@ -60,7 +60,7 @@ def test_backward_against_oracle(name):
     f = lambda k: None if inp[k] is None else P.to_np(inp[k])
     ref = so.backward(f("x"), f("Wr"), f("br"), f("W1"), f("b1"), f("W2"), f("b2"), shape.G, shape.T, shape.E,
                       shape.capacity_factor, P.to_np(dy), w_aux, w_z, residual=residual,
-                      logits_override=over or None)
+                      choice_logits=over or None)
     tol = 1e-4 if shape.dtype == "f32" else 2e-2
     for k in ("dx", "dWr", "dbr", "dW1", "db1", "dW2", "db2"):
         _close(k, g[k], ref[k], tol)

@@ -56,6 +56,7 @@ def test_top2_against_oracle(name):
     layer, r, xe, y, y2, r2 = _run(shape, inp)
     assert layer.C == P.so.capacity(2 * shape.capacity_factor, shape.T, shape.E)
     ref, subst = P.oracle_route_top2(inp, shape, P.to_np(r.logits))
+    P.check_logits(P.to_np(r.logits), ref)
     P.compare_route_top2(r, ref, shape)
     P.compare_route_top2(r2, ref, shape)
     P.check_dispatch_top2(xe, inp["x"], ref)
@@ -82,6 +83,7 @@ def test_top2_switch_base_full_size():
     y, r = layer.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"])
     layer.sync_status()
     ref, _ = P.oracle_route_top2(inp, shape, P.to_np(r.logits))
+    P.check_logits(P.to_np(r.logits), ref)
     P.compare_route_top2(r, ref, shape)
     tokens = np.sort(np.random.default_rng(1).choice(shape.N, 192, replace=False))
     P.check_y_top2(y, ref, inp, tokens)

@@ -353,17 +353,34 @@ def test_near_tie_detection():
     assert so.groups_with_near_ties([z], G=2, T=1) == [0]
 
 
-def test_logits_override_reroutes_group():
+def test_choice_logits_decide_only_the_choices():
+    # Substituted scores move group 1's tokens to expert 2; probabilities, gates and P stay
+    # the float64 ones, and f (hence the balance term) follows the new choices.
     rng = np.random.default_rng(8)
     G, T, E, d = 2, 6, 3, 4
     x = rng.standard_normal((G * T, d))
     Wr = rng.standard_normal((E, d))
     z_alt = np.zeros((T, E))
     z_alt[:, 2] = 1.0
-    r = so.route(x, Wr, None, G, T, E, 1.0, logits_override={1: z_alt})
-    assert (r.expert[T:] == 2).all()
+    r = so.route(x, Wr, None, G, T, E, 1.0, choice_logits={1: z_alt})
     r0 = so.route(x, Wr, None, G, T, E, 1.0)
+    assert (r.expert[T:] == 2).all()
     np.testing.assert_array_equal(r.expert[:T], r0.expert[:T])
+    np.testing.assert_array_equal(r.logits, r0.logits)
+    np.testing.assert_array_equal(r.probs, r0.probs)
+    np.testing.assert_array_equal(r.P, r0.P)
+    assert r.z_loss == r0.z_loss
+    np.testing.assert_array_equal(r.gate, r0.probs[np.arange(G * T), r.expert])
+    np.testing.assert_array_equal(r.raw[1], [0, 0, T])
+    assert r.balance[1] == E * r0.P[1][2]  # f = (0, 0, 1)
+    np.testing.assert_array_equal(r.balance[0], r0.balance[0])
+    # top-2: the substituted scores pick the pair; the gates come from the float64 scores
+    z_alt2 = np.zeros((T, E))
+    z_alt2[:, 2], z_alt2[:, 0] = 2.0, 1.0
+    r2 = so.route_top2(x, Wr, None, G, T, E, 1.0, choice_logits={1: z_alt2})
+    assert (r2.expert[T:] == 2).all() and (r2.expert2[T:] == 0).all()
+    z = r0.logits[T:]
+    np.testing.assert_allclose(r2.gate[T:], np.exp(z[:, 2]) / (np.exp(z[:, 2]) + np.exp(z[:, 0])), rtol=1e-14)
 
 
 # ----------------------------------------------------------------------------- router z-loss
