@@ -3,4 +3,4 @@
 Holds no arithmetic of the layer itself; see gen.inputs.
 """
 from .inputs import (LayerShape, WORKLOADS, WORKLOAD_ORDER, WORKLOAD_SEEDS, SKEW_GAMMA,
-                     act_dtype, make_inputs, skewed_router_bias, workload, workload_seed)
+                     act_dtype, expert_weights, make_inputs, skewed_router_bias, workload, workload_seed)

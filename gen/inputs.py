@@ -162,6 +162,20 @@ def make_inputs(shape: LayerShape, seed: int, device="cpu", *, with_experts: boo
     return out
 
 
+def expert_weights(shape: LayerShape, seed: int, expert: int, device="cpu") -> tuple:
+    """W1[e] [d_ff, d] and W2[e] [d, d_ff] of one expert, drawn from a generator of its own
+    (seed, expert), with make_inputs' distributions but not its values.  For a host-side
+    sample that needs a few experts of a layer too large to draw whole on the host."""
+    gen = torch.Generator(device=torch.device(device))
+    gen.manual_seed(int(seed) * 65537 + 1 + int(expert))
+    dt = act_dtype(shape)
+    W1 = torch.empty(shape.d_ff, shape.d_model, dtype=dt, device=device)
+    _trunc_normal_(W1, math.sqrt(0.1 / shape.d_model), gen)
+    W2 = torch.empty(shape.d_model, shape.d_ff, dtype=dt, device=device)
+    _trunc_normal_(W2, math.sqrt(0.1 / shape.d_ff), gen)
+    return W1, W2
+
+
 def workload(name: str) -> LayerShape:
     return WORKLOADS[name]
 
