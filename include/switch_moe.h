@@ -83,6 +83,15 @@ typedef enum { SWITCH_F32 = 0, SWITCH_BF16 = 1 } switch_dtype;
  * floats) and, with bfloat16 and d, d_ff multiples of 128, by two transposed copies of the
  * expert weights (2 E d d_ff bfloat16) and bfloat16 copies of the backward's activations. */
 #define SWITCH_FLAG_TRAINING      0x20u
+/* Test only (fault injection on the host's request, no GPU fault): in the tensor-core
+ * expert FFN, the first layer-1 tile of expert 0's first token chunk stores its part of h
+ * but never publishes it, so the layer-2 tiles of that chunk wait on a count that nothing
+ * completes.  Their bounded wait gives up after about a second of SM clock, sets the
+ * device error word and carries on; switch_sync_status / switch_get_stats then return
+ * SWITCH_ERR_DEVICE_TIMEOUT (and clear the word).  The outputs of such a call are
+ * unspecified; the handle stays usable.  Has no effect where expert 0 receives no token
+ * or the FFN runs on CUDA cores. */
+#define SWITCH_FLAG_TEST_STALL    0x40u
 
 typedef struct {
   int G;                   /* routing groups; capacity and statistics are per group */
@@ -284,8 +293,10 @@ SWITCH_API int switch_last_launch_count(switch_handle h);
  * loads the library holds until the process exits.  Nothing is allocated: no cudaMalloc,
  * no cudaFree, no allocating library call; the call enqueues one cudaMemsetAsync of 16
  * bytes (clearing the error word and a counter) and the routing kernels on `stream`.
- *   - The first call on a device looks up the array's device address on that device
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call looks up the array's device address in the current device's context
+ *     (cudaGetSymbolAddress), so a call after a context reset (cudaDeviceReset) uses the
+ *     new address.  The first call on a device also loads the library's device code there;
+ *     make that first call before any stream capture.
  *   - Every call on a device shares the array and leaves its contents behind: two calls
  *     whose kernels overlap on the GPU (different streams, or concurrent graphs) race and
  *     give wrong results.  Serialise them.

@@ -28,6 +28,7 @@ FLAG_DEBUG_BOUNDS = 0x4
 FLAG_PROFILE = 0x8
 FLAG_TOP2 = 0x10
 FLAG_TRAINING = 0x20
+FLAG_TEST_STALL = 0x40
 
 
 class SwitchConfig(ctypes.Structure):

@@ -4,7 +4,6 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include <mutex>
 #include <new>
 
 #include "../../include/switch_moe.h"
@@ -420,6 +419,7 @@ static switch_status run_ffn_tc(switch_handle h, const void* xe, const void* W1,
   L.R = h->R;
   L.d = c.d_model;
   L.F = c.d_ff;
+  L.stall = (c.flags & SWITCH_FLAG_TEST_STALL) != 0;
   const int n = launch_ffn_tc(L, s, pdl);
   if (n < 0) return SWITCH_ERR_CUDA;
   h->last_launches += n;
@@ -765,24 +765,18 @@ namespace {
 constexpr size_t STATIC_ROUTE_SCRATCH_BYTES = (size_t)32 << 20;  // 32 MiB
 __device__ __align__(256) uint8_t g_static_route_scratch[STATIC_ROUTE_SCRATCH_BYTES];
 
-constexpr int STATIC_MAX_DEVICES = 64;
-std::mutex g_static_mu;
-void* g_static_addr[STATIC_MAX_DEVICES];  // device address of the array, per device
-
-// Device address of the array on the current device (looked up once per device; the
-// name is only a host-side stand-in and must never be handed to a kernel).
-void* static_route_scratch(int dev) {
-  if (dev < 0 || dev >= STATIC_MAX_DEVICES) return nullptr;
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_route_scratch) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    g_static_addr[dev] = p;
+// Device address of the array in the current device's context.  Looked up on every call:
+// the name is only a host-side stand-in and must never be handed to a kernel, and after a
+// context reset (cudaDeviceReset) the array lives at a new address, so a cached one could
+// go stale.  Once the library's device code is loaded on the device the lookup is a host
+// table read.
+void* static_route_scratch() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_route_scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
   }
-  return g_static_addr[dev];
+  return p;
 }
 
 }  // namespace
@@ -820,9 +814,7 @@ extern "C" switch_status switch_route_static(const switch_config* cfg, const voi
   const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
   if (off > STATIC_ROUTE_SCRATCH_BYTES) return SWITCH_ERR_UNSUPPORTED;  // needs more than 32 MiB
   (void)d;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SWITCH_ERR_CUDA;
-  uint8_t* ws = static_cast<uint8_t*>(static_route_scratch(dev));
+  uint8_t* ws = static_cast<uint8_t*>(static_route_scratch());
   if (!ws) return SWITCH_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   // the error word and the scan's block counter must start at zero; everything else is

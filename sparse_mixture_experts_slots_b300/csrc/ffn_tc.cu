@@ -64,6 +64,7 @@ struct FfnParams {
   int E, R, d, F, BN, NCH, LOOK, NA, STAGES, stage_bytes, combine, w_evict_first;
   int MB;                        // 128-row weight blocks per tile (the kernel's template value)
   int layer2;                    // 0: layer-1 tiles only (a weight gradient)
+  int stall;                     // test only: tile (layer 1, expert 0, block 0, chunk 0) never publishes
 };
 
 struct FfTile {
@@ -496,7 +497,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       epi_sync<MB>();  // every thread's TMEM reads and stores of this tile are done
       if (leader) {
         mbar_arrive(&sh.aempty[buf]);
-        if (l1) {
+        if (l1 && !(p.stall && e == 0 && mt == 0 && nc == 0)) {
           __threadfence();  // the chunk's h stores (ordered by the barrier) before the count
           atomicAdd(p.done1 + (size_t)e * p.NCH + nc, 1u);
         }
@@ -659,6 +660,7 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.combine = L.combine ? 1 : 0;
   p.hmask = (const __nv_bfloat16*)L.hmask;
   p.layer2 = L.mode == 2 ? 0 : 1;
+  p.stall = L.stall ? 1 : 0;
   p.w_evict_first = t.NCH == 1 ? 1 : 0;  // several chunks re-read a weight tile
   const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
   const long long tiles = (long long)L.E * t.NCH * (L.F / (FF_BM * t.MB) + l2_blocks);

@@ -203,6 +203,7 @@ struct FfnLaunch {
   uint32_t* counters;        // ffn_counter_words(E, R) words, zero at launch
   uint32_t* err;
   int E, R, d, F;
+  bool stall;                // test only: layer-1 tile (expert 0, chunk 0, block 0) never publishes
 };
 // Needs d % 128 == 0 and F % 128 == 0 (tc_shape_ok both ways).  Returns launches or -1.
 bool tc_shape_ok(int M, int K);

@@ -63,7 +63,8 @@ class SwitchMoE:
     def __init__(self, G: int, T: int, d_model: int, d_ff: int, E: int, capacity_factor: float = 1.0, *,
                  dtype: torch.dtype = torch.bfloat16, alpha: float = 0.01, capacity_override: int = 0,
                  write_probs: bool = False, write_logits: bool = False, debug_bounds: bool = False,
-                 profile: bool = False, top_k: int = 1, training: bool = False, device=None):
+                 profile: bool = False, top_k: int = 1, training: bool = False, test_stall: bool = False,
+                 device=None):
         self.lib = _lib.load()
         if dtype not in (torch.bfloat16, torch.float32):
             raise ValueError("dtype must be torch.bfloat16 or torch.float32")
@@ -71,7 +72,8 @@ class SwitchMoE:
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         flags = ((_lib.FLAG_WRITE_PROBS if write_probs else 0) | (_lib.FLAG_WRITE_LOGITS if write_logits else 0)
                  | (_lib.FLAG_DEBUG_BOUNDS if debug_bounds else 0) | (_lib.FLAG_PROFILE if profile else 0)
-                 | (_lib.FLAG_TOP2 if top_k == 2 else 0) | (_lib.FLAG_TRAINING if training else 0))
+                 | (_lib.FLAG_TOP2 if top_k == 2 else 0) | (_lib.FLAG_TRAINING if training else 0)
+                 | (_lib.FLAG_TEST_STALL if test_stall else 0))
         if top_k not in (1, 2):
             raise ValueError("top_k must be 1 or 2")
         self.top_k = top_k
@@ -190,15 +192,17 @@ class SwitchMoE:
         return r
 
     def backward(self, x, Wr, W1, W2, r: RouteResult, dy, w_aux: float = 0.0, w_z: float = 0.0,
-                 residual: bool = False, stream=None) -> dict:
+                 residual: bool = False, out: Optional[dict] = None, stream=None) -> dict:
         """Float32 gradients of sum(dy * y) + w_aux * aux_loss + w_z * z_loss for the last
-        forward on this layer (constructed with training=True): dx, dWr, dbr, dW1, db1, dW2, db2."""
+        forward on this layer (constructed with training=True): dx, dWr, dbr, dW1, db1, dW2, db2.
+        out: float32 tensors of those names to write into (allocated when None)."""
         dev, f32 = self.device, torch.float32
         E, d, F, N = self.E, self.d_model, self.d_ff, self.N
-        g = dict(dx=torch.empty(N, d, dtype=f32, device=dev), dWr=torch.empty(E, d, dtype=f32, device=dev),
-                 dbr=torch.empty(E, dtype=f32, device=dev), dW1=torch.empty(E, F, d, dtype=f32, device=dev),
-                 db1=torch.empty(E, F, dtype=f32, device=dev), dW2=torch.empty(E, d, F, dtype=f32, device=dev),
-                 db2=torch.empty(E, d, dtype=f32, device=dev))
+        g = out if out is not None else dict(
+            dx=torch.empty(N, d, dtype=f32, device=dev), dWr=torch.empty(E, d, dtype=f32, device=dev),
+            dbr=torch.empty(E, dtype=f32, device=dev), dW1=torch.empty(E, F, d, dtype=f32, device=dev),
+            db1=torch.empty(E, F, dtype=f32, device=dev), dW2=torch.empty(E, d, F, dtype=f32, device=dev),
+            db2=torch.empty(E, d, dtype=f32, device=dev))
         cs = r.c_struct()
         check(self.lib.switch_backward(self._h, _ptr(x), _ptr(Wr), _ptr(W1), _ptr(W2), ctypes.byref(cs), _ptr(dy),
                                        float(w_aux), float(w_z), 1 if residual else 0, _ptr(g["dx"]), _ptr(g["dWr"]),

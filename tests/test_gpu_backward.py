@@ -68,6 +68,29 @@ def test_backward_against_oracle(name):
         assert (~ref["route"].keep).sum() > 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_backward_without_tokens_writes_zero_gradients(dtype):
+    # T = 0: no tokens and no expert rows.  Every weight and bias gradient must come out
+    # exactly zero (the outputs start as NaN, so an untouched one fails), on the tensor-core
+    # path (bf16, widths multiples of 128) and on the CUDA-core path (float32).
+    shape = (LayerShape("bwd-empty", 2, 0, 128, 256, 4, 1.0) if dtype == "bf16"
+             else LayerShape("bwd-empty-f32", 2, 0, 48, 32, 16, 1.0, dtype="f32"))
+    inp = make_inputs(shape, 5, "cuda", expert_bias_std=0.05)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    layer = P.make_layer(shape, training=True)
+    y, r = layer.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"])
+    E, d, F = shape.E, shape.d_model, shape.d_ff
+    nan = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device="cuda")
+    out = dict(dx=nan(0, d), dWr=nan(E, d), dbr=nan(E), dW1=nan(E, F, d), db1=nan(E, F), dW2=nan(E, d, F),
+               db2=nan(E, d))
+    dy = torch.empty(0, d, dtype=dt, device="cuda")
+    g = layer.backward(inp["x"], inp["Wr"], inp["W1"], inp["W2"], r, dy, 0.7, 0.3, out=out)
+    layer.sync_status()
+    torch.cuda.synchronize()
+    for k in ("dWr", "dbr", "dW1", "db1", "dW2", "db2"):
+        assert torch.equal(g[k], torch.zeros_like(g[k])), f"{k} is not exactly zero"
+
+
 def test_backward_needs_training_flag():
     shape, kw, _ = CASES["bwd-tc"]
     inp = make_inputs(shape, 5, "cuda", **kw)
