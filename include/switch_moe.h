@@ -301,7 +301,8 @@ SWITCH_API int switch_last_launch_count(switch_handle h);
  *     whose kernels overlap on the GPU (different streams, or concurrent graphs) race and
  *     give wrong results.  Serialise them.
  *   - A configuration whose scratch needs more than 32 MiB returns SWITCH_ERR_UNSUPPORTED.
- *     The scratch is about (12 E + 4) G ceil(T/128) + 6 E d + 4 E G C bytes with bfloat16
+ *     The scratch is about (12 E + 4) G ceil(T/128) + 6 E d + 4 E G C bytes (d rounded up to a
+ *     multiple of 64, E up to the next multiple of the router's experts per CTA) with bfloat16
  *     activations (all five named workloads fit; 65536 tokens x 2048 experts needs 22 MiB),
  *     plus 4 G T E bytes of logits with float32 activations.  Invalid arguments return
  *     SWITCH_ERR_INVALID_ARG.

@@ -1,7 +1,7 @@
-// Dispatch gather and combine scatter (sm_103a), 16-byte vectors, one warp per row.
+// Dispatch gather and combine scatter (sm_103a), 16-byte vectors.
 //
-// Dispatch: kept tokens are copied into their expert's block of xe; the rest of
-// the block is zero, as the one-hot dispatch tensor of the Switch Transformers
+// Dispatch: kept tokens are copied into their expert's block of xe; switch_dispatch also
+// zeroes the rest of the block, as the one-hot dispatch tensor of the Switch Transformers
 // card (ai-papers.xuzou.cn, 方法适配) would give.
 // Combine: y_t = p_{e*}(x_t) * f_{e*}(x_t) for kept tokens and 0 for dropped ones
 // ("042 · Switch Transformer：每个词只选一个专家", section 一; the gate is not
@@ -63,104 +63,104 @@ int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_
 }
 
 // Forward path: the slots of the routing step and the dispatch copy in one pass.
-// Warp w < N takes token w: every lane first loads its part of the row (that read does not
-// depend on routing), while lane 0 turns the token's in-tile rank (held in slot[]) into its
-// slot, keep flag and row (as route_slots_kernel does); then the row goes to its expert
-// block, or, for a dropped token with the combine fused into the FFN, y gets the residual
-// (or zero).  Warps past N zero the rows past each expert's count.
-constexpr int DS_VMAX = 4;  // 16-byte vectors per lane held in registers (rows <= 2 KB)
+// Warp w takes tokens DS_TPW w .. DS_TPW w + DS_TPW - 1: every lane first loads its part of
+// all of their rows (those reads do not depend on routing), while lane j < DS_TPW turns
+// token j's in-tile rank (held in slot[]) into its slot, keep flag and row (as
+// route_slots_kernel does); then each row goes to its expert block, or, for a dropped token
+// with the combine fused into the FFN, y gets the residual (or zero).  Rows of an expert
+// block past its count are left as they are: the forward's expert FFN never uses them (its
+// MMA columns past a chunk's filled rows are discarded), unlike switch_dispatch's output.
+constexpr int DS_VMAX = 4;  // 16-byte vectors per lane and row held in registers (rows <= 2 KB)
+constexpr int DS_TPW = 4;   // tokens per warp
 
 __global__ void __launch_bounds__(DC_WARPS * 32) dispatch_slots_kernel(
     const uint4* __restrict__ x, uint4* __restrict__ xe, const int32_t* __restrict__ expert,
     const int32_t* __restrict__ tile_base, const int32_t* __restrict__ group_off,
-    const int32_t* __restrict__ expert_rows, int32_t* __restrict__ slot, uint8_t* __restrict__ keep,
-    int32_t* __restrict__ row, int32_t* __restrict__ tok_of_row, long long N, int T, int E, int nT, int C, int R,
-    int vecs, bool debug, uint32_t* err, uint4* __restrict__ y, const uint4* __restrict__ resid,
-    uint32_t* __restrict__ zero_ptr, int zero_words) {
+    int32_t* __restrict__ slot, uint8_t* __restrict__ keep, int32_t* __restrict__ row,
+    int32_t* __restrict__ tok_of_row, long long N, int T, int E, int nT, int C, int R, int vecs, bool debug,
+    uint32_t* err, uint4* __restrict__ y, const uint4* __restrict__ resid, uint32_t* __restrict__ zero_ptr,
+    int zero_words) {
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const long long w = (long long)blockIdx.x * DC_WARPS + warp;
+  const long long w0 = ((long long)blockIdx.x * DC_WARPS + warp) * DS_TPW;
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero_ptr[i] = 0u;
-  if (w < N) {
-    const uint4* src = x + w * vecs;
-    const bool in_regs = vecs <= 32 * DS_VMAX;
-    uint4 v[DS_VMAX];
-    if (in_regs) {
+  if (w0 >= N) return;
+  const bool in_regs = vecs <= 32 * DS_VMAX;
+  uint4 v[DS_TPW][DS_VMAX];
+  if (in_regs) {
+#pragma unroll
+    for (int j = 0; j < DS_TPW; ++j)
 #pragma unroll
       for (int k = 0; k < DS_VMAX; ++k)
-        if (lane + 32 * k < vecs) v[k] = __ldg(src + lane + 32 * k);
-    }
-    int r = -1, e = 0;
-    if (lane == 0) {
-      const int g = (int)(w / T);
-      const int ti = (int)(w - (long long)g * T);
-      const int rank = slot[w];
-      e = expert[w];
-      if (e < 0 || e >= E) {
-        raise_error(err, ERR_BOUNDS);
-        e = 0;
-        slot[w] = 0;
-        keep[w] = 0;
-      } else {
-        const int s = tile_base[((size_t)g * nT + ti / ROUTE_TILE) * E + e] + rank;
-        const int goff = group_off[(size_t)g * E + e];
-        slot[w] = s;
-        if (s < C) {
-          r = goff + s;
-          if (r < 0 || r >= R) {
-            if (debug) raise_error(err, ERR_BOUNDS);
-            r = -1;
-          } else {
-            tok_of_row[(size_t)e * R + r] = (int32_t)w;
-          }
+        if (w0 + j < N && lane + 32 * k < vecs) v[j][k] = __ldg(x + (w0 + j) * vecs + lane + 32 * k);
+  }
+  int r = -1, e = 0;
+  if (lane < DS_TPW && w0 + lane < N) {
+    const long long w = w0 + lane;
+    const int g = (int)(w / T);
+    const int ti = (int)(w - (long long)g * T);
+    const int rank = slot[w];
+    e = expert[w];
+    if (e < 0 || e >= E) {
+      raise_error(err, ERR_BOUNDS);
+      e = 0;
+      slot[w] = 0;
+      keep[w] = 0;
+    } else {
+      const int s = tile_base[((size_t)g * nT + ti / ROUTE_TILE) * E + e] + rank;
+      const int goff = group_off[(size_t)g * E + e];
+      slot[w] = s;
+      if (s < C) {
+        r = goff + s;
+        if (r < 0 || r >= R) {
+          if (debug) raise_error(err, ERR_BOUNDS);
+          r = -1;
+        } else {
+          tok_of_row[(size_t)e * R + r] = (int32_t)w;
         }
-        keep[w] = r >= 0 ? 1 : 0;
       }
-      row[w] = r;
+      keep[w] = r >= 0 ? 1 : 0;
     }
-    r = __shfl_sync(0xffffffffu, r, 0);
-    e = __shfl_sync(0xffffffffu, e, 0);
-    if (r < 0) {
+    row[w] = r;
+  }
+#pragma unroll
+  for (int j = 0; j < DS_TPW; ++j) {
+    const int rj = __shfl_sync(0xffffffffu, r, j);
+    const int ej = __shfl_sync(0xffffffffu, e, j);
+    const long long w = w0 + j;
+    if (w >= N) break;
+    if (rj < 0) {
       if (y) {  // a dropped token skips the expert: y is the residual alone, or zero
         const uint4 zero = make_uint4(0, 0, 0, 0);
         for (int k = lane; k < vecs; k += 32) y[w * vecs + k] = resid ? __ldg(resid + w * vecs + k) : zero;
       }
-      return;
+      continue;
     }
-    uint4* dst = xe + ((long long)e * R + r) * vecs;
+    uint4* dst = xe + ((long long)ej * R + rj) * vecs;
     if (in_regs) {
 #pragma unroll
       for (int k = 0; k < DS_VMAX; ++k)
-        if (lane + 32 * k < vecs) dst[lane + 32 * k] = v[k];
+        if (lane + 32 * k < vecs) dst[lane + 32 * k] = v[j][k];
     } else {
-      for (int k = lane; k < vecs; k += 32) dst[k] = __ldg(src + k);
+      for (int k = lane; k < vecs; k += 32) dst[k] = __ldg(x + w * vecs + k);
     }
-    return;
   }
-  const long long dr = w - N;
-  if (dr >= (long long)E * R) return;
-  const int e = (int)(dr / R), r = (int)(dr % R);
-  if (r < expert_rows[e]) return;
-  uint4* dst = xe + dr * vecs;
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int k = lane; k < vecs; k += 32) dst[k] = zero;
 }
 
 int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, void* y, const void* resid,
                           uint32_t* zero_ptr, int zero_words, cudaStream_t s, bool pdl) {
   const long long N = (long long)a.G * a.T;
-  long long warps = N + (long long)a.E * a.R;
+  long long warps = (N + DS_TPW - 1) / DS_TPW;
   if (warps == 0 && zero_words == 0) return 0;
   if (warps == 0) warps = 1;  // one block still clears the words
   const int nT = (a.T + ROUTE_TILE - 1) / ROUTE_TILE;
   const int vecs = a.d * (a.x_bf16 ? 2 : 4) / 16;
   const unsigned blocks = (unsigned)((warps + DC_WARPS - 1) / DC_WARPS);
   return launch_k(dispatch_slots_kernel, dim3(blocks), dim3(DC_WARPS * 32), 0, s, pdl, 1, (const uint4*)x, (uint4*)xe,
-                  a.expert, a.tile_base, a.group_off, a.expert_rows, a.slot, a.keep, a.row, a.tok_of_row, N, a.T, a.E,
-                  nT, a.C, a.R, vecs, a.debug, a.err, (uint4*)y, (const uint4*)resid, zero_ptr, zero_words) ==
-                 cudaSuccess
+                  a.expert, a.tile_base, a.group_off, a.slot, a.keep, a.row, a.tok_of_row, N, a.T, a.E, nT, a.C, a.R,
+                  vecs, a.debug, a.err, (uint4*)y, (const uint4*)resid, zero_ptr, zero_words) == cudaSuccess
              ? 1
              : -1;
 }

@@ -128,9 +128,6 @@ struct FfShared {
 };
 static_assert(offsetof(FfShared, xpose) % 16 == 0, "16-byte vector reads of the transpose buffer");
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 template <int MB>
 __device__ __forceinline__ void epi_sync() {  // named barrier over the epilogue warps
   asm volatile("bar.sync 1, %0;" ::"n"(128 * FF_EPW * MB) : "memory");

@@ -53,7 +53,7 @@ struct RouteArgs {
   // workspace
   float* logits;       // [N, E] float32 logits of the CUDA-core router (workspace or the caller's)
   float* logits_out;   // [N, E] or null: logits the caller asked for
-  void* wsplit;        // [3, E, d] bf16: W_r split into hi, mid, lo (tensor-core router)
+  void* wsplit;        // W_r split into hi, mid, lo bf16 pieces (tensor-core router; layout in route_tc.cu)
   int32_t* tile_hist;  // [G, nT, E]
   float* tile_P;       // [G, nT, E]
   float* tile_Z;       // [G, nT]: sum over the tile's tokens of (log sum_e exp z)^2
@@ -132,7 +132,7 @@ int launch_route(const RouteArgs& a, cudaStream_t s);
 int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s);
 int router_tc_experts_per_cta(int E);
 int router_tc_mma_n(int EC);
-// Bytes of the split W_r workspace ([Q][hi, mid, lo][EC][d] bf16) for E experts of width d.
+// Bytes of the split W_r workspace ([Q][d / 64 atoms][hi, mid, lo][EC][64] bf16) for E experts of width d.
 size_t router_tc_wsplit_bytes(int E, int d);
 
 // 3-D view [cols / 64 atoms][rows][64] of a row-major bf16 matrix (cols % 64 == 0); a box of

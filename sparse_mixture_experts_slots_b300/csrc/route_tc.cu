@@ -8,23 +8,29 @@
 // next 8 bits of the significand).  Then
 //     z = x . hi + (x . mid + x . lo)
 // with every bf16 x bf16 product exact and accumulated in float32 by the tensor
-// cores, each piece in its own TMEM accumulator so the small terms never share an
+// cores, the hi piece in its own TMEM accumulator so the small terms never share an
 // accumulator with the large ones; the pieces are added in the epilogue.
 //
-// One CTA (or a cluster of Q CTAs, each with EC experts) takes a tile of 128
-// tokens of one routing group:
-//   warp 0, one lane : TMA producer; one stage = the x tile and the slice's three
-//                      W pieces for 64 or 128 columns of K, behind one barrier
-//   warp 1, one lane : MMA issuer (M = 128 tokens, N = 3 EC rows of pieces, K = 16)
-//   16 warps         : epilogue; warp w reads TMEM lane quadrant w % 4 (32 tokens)
-//                      and column group w / 4 (a quarter of the CTA's experts):
-//     pass 1  logits z (+ bias) into registers, max / argmax (ties -> lowest index),
-//             combined over the column groups through shared memory
+// One persistent kernel.  A cluster of Q CTAs (CTA q holds experts q EC .. q EC + EC - 1)
+// walks the token tiles (128 tokens of one routing group); clusters take tiles in turn.
+// Per CTA:
+//   warp 0, one lane : TMA producer.  Per 64-column atom of K the x tile (an x stage holds
+//                      NAX atoms) and the slice's W box(es) (hi, mid, lo rows), each in a
+//                      ring slot of its own behind one barrier.
+//   warp 1, one lane : MMA issuer (M = 128 tokens, N = MMA_N rows of pieces, K = 16) into
+//                      one of NBUF TMEM accumulator sets; the next tile's MMAs start as soon
+//                      as the epilogue has read the previous accumulator out of TMEM.
+//   warps 2 .. 17    : epilogue; warp w reads TMEM lane quadrant w % 4 (32 tokens) and
+//                      column group (w - 2) / 4 (a quarter of the CTA's experts):
+//     pass 1  logits z (+ bias) into registers, then the accumulator is released;
+//             max / argmax (ties -> lowest index), combined over the column groups
 //     pass 1b exp(z - max) in registers (ex2 of the log2e-scaled difference), sums
-//     exchange of (max, sum, argmax) between the Q CTAs through distributed shared memory
-//     pass 2  p = exp(z - max) * exp(max - Max) / Sum; column sums over the tile's
-//             tokens (warp reduce-scatter), expert histogram of the tile, rank of
-//             each token among the tile's earlier tokens with the same expert.
+//     exchange of (max, sum, argmax) between the Q CTAs: each CTA writes its values into
+//             every peer's receive buffer with asynchronous remote stores that count their
+//             bytes on the peer's barrier; everyone reads the Q slices from its own memory
+//     pass 2  p = exp(z - max) * exp(max - Max) / Sum; column sums over the tile's tokens
+//             (warp reduce-scatter), expert histogram of the tile, rank of each token
+//             among the tile's earlier tokens with the same expert.
 // Outputs per token: expert (raw choice), gate = p_{expert}, rank in tile; per
 // (group, tile, expert): token count and probability sum.  The cross-tile scan
 // that turns ranks into slots runs in route.cu.
@@ -37,88 +43,94 @@ namespace smoe {
 
 constexpr int RT_BM = ROUTE_TILE;  // 128 tokens per tile
 constexpr int RT_BK = 64;          // 64 bf16 = one 128-byte swizzle row
-constexpr int RT_THREADS = 512;    // 16 warps: 4 TMEM lane quadrants x 4 column groups
+constexpr int RT_EPI_WARPS = 16;   // 4 TMEM lane quadrants x 4 column groups
+constexpr int RT_THREADS = 64 + 32 * RT_EPI_WARPS;
+constexpr int RT_RING = 192 * 1024;
+constexpr int RT_MAX_WS = 8;
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- W_r -> hi, mid, lo
-// Layout of the pieces: [Q slices][hi, mid, lo][EC experts][d], experts past E zero, so
-// one TMA box (and one MMA) covers all three pieces of a slice's experts.
+// Layout of the pieces: [Q slices][NK atoms][hi, mid, lo][EC experts][64 columns] (experts
+// past E and columns past d zero), so the W box of one MMA (MMA_N rows of one atom) is one
+// contiguous block of MMA_N * 128 bytes.
 __global__ void router_split_kernel(const float* __restrict__ Wr, __nv_bfloat16* __restrict__ ws, int E, int d,
-                                    int EC, long long n /* Q * EC * d */) {
+                                    int EC, int NK, long long n /* Q * EC * NK * 64 */) {
   griddep_wait();
   griddep_launch_dependents();
+  const int dp = NK * 64;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
-    const long long row = i / d;  // q * EC + el = expert index
-    const int k = (int)(i - row * d);
+    const long long row = i / dp;  // q * EC + el = expert index
+    const int kd = (int)(i - row * dp);
     const int q = (int)(row / EC), el = (int)(row - (long long)q * EC);
-    const float w = row < E ? Wr[row * d + k] : 0.f;
+    const int k = kd >> 6, kc = kd & 63;
+    const float w = (row < E && kd < d) ? Wr[row * d + kd] : 0.f;
     const __nv_bfloat16 hi = __float2bfloat16_rn(w);
     const float r1 = w - __bfloat162float(hi);  // exact: fits in the 24-bit significand
     const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
     const float r2 = r1 - __bfloat162float(mid);  // exact
-    const size_t base = ((size_t)q * 3 * EC + el) * d + k;
+    const size_t base = (((size_t)q * NK + k) * 3 * EC + el) * 64 + kc;
     ws[base] = hi;
-    ws[base + (size_t)EC * d] = mid;
-    ws[base + (size_t)2 * EC * d] = __float2bfloat16_rn(r2);
+    ws[base + (size_t)EC * 64] = mid;
+    ws[base + (size_t)2 * EC * 64] = __float2bfloat16_rn(r2);
   }
 }
 
 // ---------------------------------------------------------------- tiling
-// Per 64-column atom of K, a stage holds the x tile (128 tokens) and the 3 * EC rows of
-// W pieces of the CTA's slice, in WBOXES boxes of MMA_N rows; MMA m takes box m.
-// Accumulators in TMEM: one block of EC columns per piece (hi, mid, lo); with EC = 256
-// the 512 columns hold hi and (mid + lo).
+// A W box holds MMA_N rows of the slice's pieces for one 64-column atom; MMA b takes box b.
+// Accumulators in TMEM per tile: one block of EC columns per piece (hi, mid, lo); with
+// EC = 256 the 512 columns hold hi and (mid + lo), one tile at a time.
 template <int EC>
 struct RtGeom {
   static constexpr int WROWS = 3 * EC;
   static constexpr int MMA_N = EC == 256 ? 256 : (WROWS <= 256 ? WROWS : 192);
   static constexpr int WBOXES = WROWS / MMA_N;
   static constexpr int ACC_BLOCKS = EC == 256 ? 2 : 3;
-  static constexpr uint32_t TMEM_COLS = ACC_BLOCKS * EC <= 32 ? 32 : ACC_BLOCKS * EC <= 64 ? 64
-                                       : ACC_BLOCKS * EC <= 128 ? 128 : ACC_BLOCKS * EC <= 256 ? 256 : 512;
-  // first TMEM column written by MMA m
-  static __device__ __forceinline__ uint32_t dcol(int m) { return EC == 256 ? (m == 0 ? 0u : 256u) : (uint32_t)(m * MMA_N); }
+  static constexpr int TILE_COLS = ACC_BLOCKS * EC;
+  static constexpr int NBUF = 2 * TILE_COLS <= 512 ? 2 : 1;
+  static constexpr int COLS = NBUF * TILE_COLS;
+  static constexpr uint32_t TMEM_COLS = COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : COLS <= 256 ? 256 : 512;
+  static constexpr int W_BOX = MMA_N * RT_BK * 2;
+  // first TMEM column (within a tile's set) written by MMA b
+  static __device__ __forceinline__ uint32_t dcol(int b) { return EC == 256 ? (b == 0 ? 0u : 256u) : (uint32_t)(b * MMA_N); }
   static_assert(WROWS % MMA_N == 0 && MMA_N % 16 == 0 && MMA_N <= 256, "tcgen05 M=128 takes N = 16..256, step 16");
-  static_assert((MMA_N * 128) % 1024 == 0, "every W box starts on a swizzle atom");
+  static_assert(W_BOX % 1024 == 0, "every W box starts on a swizzle atom");
+  static_assert(TILE_COLS <= 512, "a tile's accumulators fit in TMEM");
 };
 
-// DEEP: one CTA per SM with ~170-220 KB of loads in flight (a grid that fits in one
-// wave); !DEEP: two CTAs per SM (each <= 113 KB, <= 256 TMEM columns), so one CTA's
-// epilogue overlaps the other's main loop on larger grids.  Each stage is one barrier
-// phase: per-phase cost, not bytes, limits a CTA's TMA stream, so stages are large.
-template <int EC, bool DEEP>
+// NAX: 64-column atoms per x stage (2 when d % 128 == 0: one 3-D box of 256 bytes per row).
+template <int EC, int NAX>
 struct RtCfg {
   using G = RtGeom<EC>;
-  static constexpr int NA = (EC <= 16 || (EC <= 64 && DEEP)) ? 2 : 1;  // 64-column atoms per stage
-  static constexpr int X_ATOM = RT_BM * RT_BK * 2;                    // 16 KB
-  static constexpr int W_ATOM = G::WROWS * RT_BK * 2;
-  static constexpr int STAGE_BYTES = NA * (X_ATOM + W_ATOM);
-  static constexpr int RING_BUDGET = DEEP ? 224 * 1024 : 110 * 1024;
-  static constexpr int STAGES = RING_BUDGET / STAGE_BYTES < 4 ? RING_BUDGET / STAGE_BYTES : 4;
-  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-  static_assert(STAGES >= 2, "double buffering at least");
-  static_assert(DEEP || G::TMEM_COLS <= 256, "two CTAs per SM share the 512 TMEM columns");
-  static_assert(NA == 1 || G::WBOXES == 1, "a 3-D W box spans atoms only when one box covers the pieces");
+  static constexpr int X_ATOM = RT_BM * RT_BK * 2;  // 16 KB
+  static constexpr int X_STAGE = NAX * X_ATOM;
+  static constexpr int XS = NAX == 2 ? 2 : 3;        // x stages
+  static constexpr int WS_FIT = (RT_RING - XS * X_STAGE) / G::W_BOX;
+  static constexpr int WS = WS_FIT < RT_MAX_WS ? WS_FIT : RT_MAX_WS;  // W stages
+  static constexpr int X_BYTES = XS * X_STAGE;
+  static constexpr int RING_BYTES = X_BYTES + WS * G::W_BOX;
+  static_assert(WS >= 3, "at least three W boxes in flight");
 };
 
-template <int EC, bool DEEP>
+template <int XS, int WS>
 struct RtBars {
-  uint64_t full[RtCfg<EC, DEEP>::STAGES], empty[RtCfg<EC, DEEP>::STAGES];
-  uint64_t accb;
+  uint64_t xfull[XS], xempty[XS], wfull[WS], wempty[WS];
+  uint64_t afull[2], aempty[2];    // accumulator sets: MMAs done / read out of TMEM
+  uint64_t rfull, rfree;           // cluster exchange: receive buffer filled by all Q / read by all Q
+  uint64_t drain;
   uint32_t tmem_slot;
   volatile int abort_flag;
+  int ep_ok;                       // broadcast by the epilogue leader
 };
 
-// Epilogue scratch; it reuses the ring's shared memory once every MMA has completed.
+// Epilogue scratch (outside the rings: the next tile's copies land while it is in use).
 template <int EC>
 struct RtScratch {
   float red_m[4][RT_BM];  // per column group: max logit of each token
   int red_a[4][RT_BM];    // per column group: argmax
   float red_s[4][RT_BM];  // per column group: sum of exp(z - m)
-  float m[RT_BM];         // this CTA's experts: max logit per token (read by cluster peers)
-  float s[RT_BM];         // this CTA's experts: sum of exp(z - m)
-  int a[RT_BM];           // this CTA's experts: argmax
+  float2 rms[8][RT_BM];   // receive buffer, per cluster rank: that slice's (max logit, sum of exp(z - max))
+  int ra[8][RT_BM];       // and its argmax, per token
   float Mall[RT_BM];      // all experts: max logit per token
   float Sall[RT_BM];      // all experts: sum of exp(z - Mall)
   int texp[RT_BM];        // final expert per token (-1 past the group's end)
@@ -128,80 +140,86 @@ struct RtScratch {
   float bias[EC];
 };
 
-template <int EC, bool DEEP>
+template <int EC, int NAX>
 constexpr int rt_smem_bytes() {
-  return RtCfg<EC, DEEP>::RING_BYTES + (int)sizeof(RtBars<EC, DEEP>) + 1024;
+  using Cf = RtCfg<EC, NAX>;
+  return Cf::RING_BYTES + (int)sizeof(RtScratch<EC>) + (int)sizeof(RtBars<Cf::XS, Cf::WS>) + 1024;
 }
-static_assert(sizeof(RtScratch<256>) <= RtCfg<256, true>::RING_BYTES, "scratch fits in the ring");
-static_assert(sizeof(RtScratch<16>) <= RtCfg<16, false>::RING_BYTES, "scratch fits in the ring");
-static_assert(rt_smem_bytes<256, true>() <= 227 * 1024 && rt_smem_bytes<128, true>() <= 227 * 1024 &&
-                  rt_smem_bytes<64, true>() <= 227 * 1024 && rt_smem_bytes<32, true>() <= 227 * 1024 &&
-                  rt_smem_bytes<16, true>() <= 227 * 1024,
-              "deep ring fits in one SM's shared memory");
-static_assert(rt_smem_bytes<64, false>() <= 113 * 1024 && rt_smem_bytes<32, false>() <= 113 * 1024 &&
-                  rt_smem_bytes<16, false>() <= 113 * 1024,
-              "shallow ring lets two CTAs share an SM");
+static_assert(rt_smem_bytes<256, 1>() <= 227 * 1024 && rt_smem_bytes<256, 2>() <= 227 * 1024 &&
+                  rt_smem_bytes<128, 1>() <= 227 * 1024 && rt_smem_bytes<128, 2>() <= 227 * 1024 &&
+                  rt_smem_bytes<64, 2>() <= 227 * 1024 && rt_smem_bytes<16, 1>() <= 227 * 1024,
+              "rings and scratch fit in one SM's shared memory");
 
-// Sum of v over the 32 lanes for 16 columns at once (reduce-scatter).  On return,
-// lane L holds the warp's total of column (L >> 1) & 15 (lanes L and L^1 agree).
-__device__ __forceinline__ float warp_colsum16(const float (&p)[16], int lane) {
-  float v8[8], v4[4], v2[2];
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float send = b4 ? p[j] : p[j + 8];
-    const float keep = b4 ? p[j + 8] : p[j];
-    v8[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
+// Sum of p over the 32 lanes for 8 columns at once (reduce-scatter).  On return, lane L
+// holds the warp's total of column (L >> 2) & 7 (lanes 4c .. 4c + 3 agree).
+__device__ __forceinline__ float warp_colsum8(const float* p, int lane) {
+  float v4[4], v2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float send = b3 ? v8[j] : v8[j + 4];
-    const float keep = b3 ? v8[j + 4] : v8[j];
-    v4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    const float send = b4 ? p[j] : p[j + 4];
+    const float keep = b4 ? p[j + 4] : p[j];
+    v4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
   }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const float send = b2 ? v4[j] : v4[j + 2];
-    const float keep = b2 ? v4[j + 2] : v4[j];
-    v2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    const float send = b3 ? v4[j] : v4[j + 2];
+    const float keep = b3 ? v4[j + 2] : v4[j];
+    v2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
   }
-  const float send = b1 ? v2[0] : v2[1];
-  const float keep = b1 ? v2[1] : v2[0];
-  const float v1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  const float send = b2 ? v2[0] : v2[1];
+  const float keep = b2 ? v2[1] : v2[0];
+  float v1 = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
   return v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
 }
 
+// Named barrier over the 16 epilogue warps (the producer and MMA warps do not take part).
+__device__ __forceinline__ void rt_epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * RT_EPI_WARPS) : "memory"); }
+
 // ---------------------------------------------------------------- the router kernel
-// grid (Q * nT, G); clusters of Q CTAs along x when Q > 1.
-template <int EC, bool DEEP>
-__global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
+// grid Q * (clusters); clusters of Q CTAs along x when Q > 1.  Cluster c takes the tiles
+// c, c + clusters, ... of the G * nT tiles (tile id = group * nT + tile in group).
+template <int EC, int NAX>
+__global__ void __launch_bounds__(RT_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                     const float* __restrict__ br, int T, int E, int d, int nT, int Q, int use3d,
+                     const float* __restrict__ br, int T, int E, int d, int nT, int Q, int total_tiles,
                      int32_t* __restrict__ expert, float* __restrict__ gate, int32_t* __restrict__ rank,
                      int32_t* __restrict__ tile_hist, float* __restrict__ tile_P, float* __restrict__ tile_Z,
                      float* __restrict__ logits, float* __restrict__ probs, uint32_t* err) {
-  using Cf = RtCfg<EC, DEEP>;
+  using Cf = RtCfg<EC, NAX>;
   using Gm = RtGeom<EC>;
+  constexpr int XS = Cf::XS, WS = Cf::WS, NBUF = Gm::NBUF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  RtBars<EC, DEEP>& bar = *reinterpret_cast<RtBars<EC, DEEP>*>(smem + Cf::RING_BYTES);
-  RtScratch<EC>& sh = *reinterpret_cast<RtScratch<EC>*>(smem);  // valid after the main loop
+  uint8_t* xring = smem;
+  uint8_t* wring = smem + Cf::X_BYTES;
+  RtScratch<EC>& sh = *reinterpret_cast<RtScratch<EC>*>(smem + Cf::RING_BYTES);
+  RtBars<XS, WS>& bar = *reinterpret_cast<RtBars<XS, WS>*>(smem + Cf::RING_BYTES + sizeof(RtScratch<EC>));
 
   const int q = Q > 1 ? (int)cluster_ctarank() : 0;
-  const int tile = blockIdx.x / Q;
-  const int g = blockIdx.y;
+  const int cl = (int)blockIdx.x / Q, ncl = (int)gridDim.x / Q;
   const int e0 = q * EC;
-  const int t0 = tile * RT_BM;
-  const long long tok0 = (long long)g * T + t0;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int NST = (d + Cf::NA * RT_BK - 1) / (Cf::NA * RT_BK);  // stages along K
+  const int NK = (d + RT_BK - 1) / RT_BK;  // atoms along K
+  const int NXS = (NK + NAX - 1) / NAX;    // x stages per tile
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Cf::STAGES; ++i) {
-      mbar_init(&bar.full[i], 1);
-      mbar_init(&bar.empty[i], 1);
+    for (int i = 0; i < XS; ++i) {
+      mbar_init(&bar.xfull[i], 1);
+      mbar_init(&bar.xempty[i], 1);
     }
-    mbar_init(&bar.accb, 1);
+    for (int i = 0; i < WS; ++i) {
+      mbar_init(&bar.wfull[i], 1);
+      mbar_init(&bar.wempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.afull[i], 1);
+      mbar_init(&bar.aempty[i], RT_EPI_WARPS);
+    }
+    mbar_init(&bar.rfull, 1);  // the leader's expect_tx; the peers' stores complete its bytes
+    mbar_init(&bar.rfree, (uint32_t)Q);
+    mbar_init(&bar.drain, 1);
     bar.abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
@@ -211,286 +229,399 @@ __global__ void __launch_bounds__(RT_THREADS, DEEP ? 1 : 2)
     tmem_alloc(&bar.tmem_slot, Gm::TMEM_COLS);
     tmem_relinquish();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bar.tmem_slot;
-  griddep_launch_dependents();  // after the TMEM allocation: a dependent grid cannot starve it
-
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
-    int issued = 0;
-    bool ok = true;
-    griddep_wait();  // the W_r pieces come from the previous kernel
-    for (int st = 0; st < NST; ++st) {
-      const int slot = st % Cf::STAGES;
-      if (st >= Cf::STAGES && !mbar_wait(&bar.empty[slot], ((st / Cf::STAGES) - 1) & 1)) { ok = false; break; }
-      if (bar.abort_flag) { ok = false; break; }
-      uint8_t* stage = smem + slot * Cf::STAGE_BYTES;
-      if (use3d) {
-        // one 3-D box per operand covers the stage's NA atoms (past d: zeros, not used)
-        mbar_arrive_expect_tx(&bar.full[slot], (uint32_t)Cf::STAGE_BYTES);
-        tma_load_3d(stage, &tmX, &bar.full[slot], 0, (int)tok0, st * Cf::NA);
-        for (int b = 0; b < Gm::WBOXES; ++b)  // WBOXES > 1 only with NA = 1
-          tma_load_3d(stage + Cf::NA * Cf::X_ATOM + b * Gm::MMA_N * 128, &tmW, &bar.full[slot], 0,
-                      q * Gm::WROWS + b * Gm::MMA_N, st * Cf::NA);
-      } else {
-        const int na = min(Cf::NA, (d - st * Cf::NA * RT_BK + RT_BK - 1) / RT_BK);  // atoms inside d
-        mbar_arrive_expect_tx(&bar.full[slot], (uint32_t)(na * (Cf::X_ATOM + Cf::W_ATOM)));
-        for (int at = 0; at < na; ++at) {
-          const int kx = (st * Cf::NA + at) * RT_BK;
-          tma_load_2d(stage + at * Cf::X_ATOM, &tmX, &bar.full[slot], kx, (int)tok0);
-          for (int b = 0; b < Gm::WBOXES; ++b)
-            tma_load_2d(stage + Cf::NA * Cf::X_ATOM + at * Cf::W_ATOM + b * Gm::MMA_N * 128, &tmW, &bar.full[slot],
-                        kx, q * Gm::WROWS + b * Gm::MMA_N);
-        }
-      }
-      issued = st + 1;
-    }
-    if (!ok) {
-      raise_error(err, ERR_TIMEOUT);
-      bar.abort_flag = 1;
-    }
-    // Drain: every copy started here has landed before the CTA can leave.
-    for (int i = issued > Cf::STAGES ? issued - Cf::STAGES : 0; i < issued; ++i)
-      if (!mbar_wait(&bar.full[i % Cf::STAGES], (i / Cf::STAGES) & 1)) raise_error(err, ERR_TIMEOUT);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(RT_BM, Gm::MMA_N);
-    bool ok = true;
-    for (int st = 0; st < NST && ok; ++st) {
-      const int slot = st % Cf::STAGES;
-      if (!mbar_wait(&bar.full[slot], (st / Cf::STAGES) & 1)) { ok = false; break; }
-      if (bar.abort_flag) { ok = false; break; }
-      tc_fence_after();
-      const int na = min(Cf::NA, (d - st * Cf::NA * RT_BK + RT_BK - 1) / RT_BK);
-      const uint32_t stage = smem_u32(smem + slot * Cf::STAGE_BYTES);
-      for (int at = 0; at < na; ++at) {
-        const uint32_t xa = stage + at * Cf::X_ATOM;
-        const uint32_t wa = stage + Cf::NA * Cf::X_ATOM + at * Cf::W_ATOM;
-#pragma unroll
-        for (int kk = 0; kk < RT_BK / 16; ++kk)
-#pragma unroll
-          for (int mm = 0; mm < Gm::WBOXES; ++mm) {
-            const bool first = st == 0 && at == 0 && kk == 0 && !(EC == 256 && mm == 2);
-            tc_mma_bf16(tmem + Gm::dcol(mm), sw128_kmajor_desc(xa + kk * 32),
-                        sw128_kmajor_desc(wa + mm * Gm::MMA_N * 128 + kk * 32), idesc, first ? 0u : 1u);
-          }
-      }
-      tc_commit(&bar.empty[slot]);
-    }
-    if (!ok) {
-      raise_error(err, ERR_TIMEOUT);
-      bar.abort_flag = 1;
-    }
-    tc_commit(&bar.accb);  // arrives once every MMA issued above has completed
-  }
-  __syncwarp();
-
-  // ---------------- epilogue
-  if (!mbar_wait(&bar.accb, 0)) {
-    raise_error(err, ERR_TIMEOUT);
-    bar.abort_flag = 1;
-  }
-  tc_fence_after();
-  __syncthreads();  // every MMA has read its operands: the ring is scratch from here on
-  const bool run = bar.abort_flag == 0;
-  for (int c = threadIdx.x; c < EC; c += blockDim.x) {
+  for (int c = threadIdx.x; c < EC; c += blockDim.x) {  // br comes from the caller, not a prior kernel
     const int e = e0 + c;
     sh.bias[c] = (br && e < E) ? br[e] : 0.f;
     sh.hist[c] = 0;
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  if (Q > 1) cluster_sync();  // every peer's barriers are initialised before any remote arrival
+  const uint32_t tmem = bar.tmem_slot;
+  griddep_launch_dependents();  // after the TMEM allocation: a dependent grid cannot starve it
 
-  // Warp w reads TMEM lane quadrant lq = w % 4 (tokens 32 lq .. 32 lq + 31) and column
-  // group cg = w / 4 (CPW consecutive experts); NCG groups cover the CTA's EC experts.
-  constexpr int NCG = EC >= 64 ? 4 : EC / 16;
-  constexpr int CPW = EC / NCG;
-  const int lq = warp & 3, cg = warp >> 2;
-  const bool has_cols = cg < NCG;
-  const int cbeg = cg * CPW;
-  const int i = lq * 32 + lane;
-  const bool valid = t0 + i < T;
-  const long long tok = tok0 + i;
-  const uint32_t trow = tmem + ((uint32_t)(lq * 32) << 16);
-
-  // pass 1: logits z (+ bias) into registers; max / argmax over this warp's columns
-  // (increasing e with strict >, so the lowest index wins a tie)
-  float v[CPW];
-  float m = -INFINITY;
-  int a = INT_MAX;
-  if (run && has_cols) {
-#pragma unroll
-    for (int ch = 0; ch < CPW / 16; ++ch) {
-      const uint32_t col = (uint32_t)(cbeg + ch * 16);
-      uint32_t h[16], r1[16], r2[16];
-      tmem_ld16(trow + col, h);
-      tmem_ld16(trow + EC + col, r1);
-      if (Gm::ACC_BLOCKS == 3) tmem_ld16(trow + 2 * EC + col, r2);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int c = cbeg + ch * 16 + j;
-        const float corr = Gm::ACC_BLOCKS == 3 ? __uint_as_float(r1[j]) + __uint_as_float(r2[j])
-                                                : __uint_as_float(r1[j]);
-        const float z = (__uint_as_float(h[j]) + corr) + sh.bias[c];
-        v[ch * 16 + j] = z;
-        if (e0 + c < E) {
-          if (z > m) { m = z; a = e0 + c; }
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      griddep_wait();  // the W_r pieces come from the previous kernel
+      uint32_t xi = 0, wi = 0;
+      bool ok = true;
+      for (int tid = cl; tid < total_tiles && ok; tid += ncl) {
+        const int g = tid / nT, tile = tid - g * nT;
+        const int row0 = g * T + tile * RT_BM;
+        for (int xs = 0; xs < NXS && ok; ++xs) {
+          if (bar.abort_flag) { ok = false; break; }
+          const int slot = (int)(xi % XS);
+          if (xi >= (uint32_t)XS && !mbar_wait(&bar.xempty[slot], ((xi / XS) - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bar.xfull[slot], (uint32_t)Cf::X_STAGE);
+          if (NAX == 2)  // one 3-D box: two atoms of 128 rows (past d: zeros, never used)
+            tma_load_3d(xring + slot * Cf::X_STAGE, &tmX, &bar.xfull[slot], 0, row0, xs * 2);
+          else
+            tma_load_2d(xring + slot * Cf::X_STAGE, &tmX, &bar.xfull[slot], xs * RT_BK, row0);
+          ++xi;
+          for (int at = 0; at < NAX && ok; ++at) {
+            const int k = xs * NAX + at;
+            if (k >= NK) break;
+            for (int b = 0; b < Gm::WBOXES; ++b) {
+              const int ws = (int)(wi % WS);
+              if (wi >= (uint32_t)WS && !mbar_wait(&bar.wempty[ws], ((wi / WS) - 1) & 1)) { ok = false; break; }
+              mbar_arrive_expect_tx(&bar.wfull[ws], (uint32_t)Gm::W_BOX);
+              tma_load_2d(wring + ws * Gm::W_BOX, &tmW, &bar.wfull[ws], 0, (q * NK + k) * Gm::WROWS + b * Gm::MMA_N);
+              ++wi;
+            }
+          }
         }
       }
-      if (logits && valid) {  // the chunk's 16 logits of this token: 16-byte stores when aligned
-        const int c0 = e0 + cbeg + ch * 16;
-        float* dst = logits + tok * E + c0;
-        if ((E & 3) == 0 && c0 + 16 <= E) {
+      if (!ok) {
+        raise_error(err, ERR_TIMEOUT);
+        bar.abort_flag = 1;
+      }
+      // Drain: every copy started here has landed before the CTA can leave.
+      for (uint32_t i = xi > (uint32_t)XS ? xi - XS : 0; i < xi; ++i)
+        if (!mbar_wait(&bar.xfull[i % XS], (i / XS) & 1)) raise_error(err, ERR_TIMEOUT);
+      for (uint32_t i = wi > (uint32_t)WS ? wi - WS : 0; i < wi; ++i)
+        if (!mbar_wait(&bar.wfull[i % WS], (i / WS) & 1)) raise_error(err, ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(RT_BM, Gm::MMA_N);
+      uint32_t xi = 0, wi = 0;
+      int lt = 0;
+      bool ok = true;
+      for (int tid = cl; tid < total_tiles && ok; tid += ncl, ++lt) {
+        if (bar.abort_flag) { ok = false; break; }
+        const int buf = lt % NBUF;
+        if (lt >= NBUF && !mbar_wait(&bar.aempty[buf], ((lt / NBUF) - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)(buf * Gm::TILE_COLS);
+        for (int xs = 0; xs < NXS && ok; ++xs) {
+          const int slot = (int)(xi % XS);
+          if (!mbar_wait(&bar.xfull[slot], (xi / XS) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t xa0 = smem_u32(xring + slot * Cf::X_STAGE);
+          for (int at = 0; at < NAX && ok; ++at) {
+            const int k = xs * NAX + at;
+            if (k >= NK) break;
+            const uint32_t xa = xa0 + at * Cf::X_ATOM;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<float4*>(dst + 4 * q4) =
-                make_float4(v[ch * 16 + 4 * q4], v[ch * 16 + 4 * q4 + 1], v[ch * 16 + 4 * q4 + 2],
-                            v[ch * 16 + 4 * q4 + 3]);
+            for (int b = 0; b < Gm::WBOXES; ++b) {
+              const int ws = (int)(wi % WS);
+              if (!mbar_wait(&bar.wfull[ws], (wi / WS) & 1)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t wa = smem_u32(wring + ws * Gm::W_BOX);
+#pragma unroll
+              for (int kk = 0; kk < RT_BK / 16; ++kk) {
+                const bool first = k == 0 && kk == 0 && !(EC == 256 && b == 2);
+                tc_mma_bf16(acc + Gm::dcol(b), sw128_kmajor_desc(xa + kk * 32), sw128_kmajor_desc(wa + kk * 32),
+                            idesc, first ? 0u : 1u);
+              }
+              tc_commit(&bar.wempty[ws]);
+              ++wi;
+            }
+          }
+          tc_commit(&bar.xempty[slot]);
+          ++xi;
+        }
+        tc_commit(&bar.afull[buf]);  // arrives once every MMA of the tile has completed
+      }
+      if (!ok) {
+        raise_error(err, ERR_TIMEOUT);
+        bar.abort_flag = 1;
+      }
+      // every MMA issued above has completed before TMEM can be freed
+      tc_commit(&bar.drain);
+      if (!mbar_wait(&bar.drain, 0)) raise_error(err, ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2 .. 17)
+    // Warp w reads TMEM lane quadrant lq = w % 4 (tokens 32 lq .. 32 lq + 31) and column
+    // group cg = (w - 2) / 4 (CPW consecutive experts); NCG groups cover the CTA's EC experts.
+    constexpr int NCG = EC >= 64 ? 4 : EC / 16;
+    constexpr int CPW = EC / NCG;
+    const int lq = warp & 3, cg = (warp - 2) >> 2;
+    const bool has_cols = cg < NCG;
+    const int cbeg = cg * CPW;
+    const int i = lq * 32 + lane;
+    const int et = threadIdx.x - 64;  // 0 .. 511
+    const bool leader = et == 0;
+    int lt = 0;
+    for (int tid = cl; tid < total_tiles; tid += ncl, ++lt) {
+      const int buf = lt % NBUF;
+      const int g = tid / nT, tile = tid - g * nT;
+      const int t0 = tile * RT_BM;
+      const long long tok0 = (long long)g * T + t0;
+      const bool valid = t0 + i < T;
+      const long long tok = tok0 + i;
+      const uint32_t trow = tmem + (uint32_t)(buf * Gm::TILE_COLS) + ((uint32_t)(lq * 32) << 16);
+
+      if (leader) {  // the tile's accumulator is complete (or the kernel is giving up)
+        int ok = bar.abort_flag ? 0 : 1;
+        if (ok && !mbar_wait(&bar.afull[buf], (lt / NBUF) & 1)) {
+          raise_error(err, ERR_TIMEOUT);
+          ok = 0;
+        }
+        if (!ok) bar.abort_flag = 1;
+        bar.ep_ok = ok;
+      }
+      rt_epi_sync();
+      if (!bar.ep_ok) break;
+      tc_fence_after();
+
+      // pass 1: logits z (+ bias) into registers; max / argmax over this warp's columns
+      // (increasing e with strict >, so the lowest index wins a tie)
+      float v[CPW];
+      float m = -INFINITY;
+      int a = INT_MAX;
+      if (has_cols) {
+#pragma unroll
+        for (int ch = 0; ch < CPW / 8; ++ch) {
+          const uint32_t col = (uint32_t)(cbeg + ch * 8);
+          uint32_t h[8], r1[8], r2[8];
+          tmem_ld8(trow + col, h);
+          tmem_ld8(trow + EC + col, r1);
+          if (Gm::ACC_BLOCKS == 3) tmem_ld8(trow + 2 * EC + col, r2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int c = cbeg + ch * 8 + j;
+            const float corr = Gm::ACC_BLOCKS == 3 ? __uint_as_float(r1[j]) + __uint_as_float(r2[j])
+                                                    : __uint_as_float(r1[j]);
+            const float z = (__uint_as_float(h[j]) + corr) + sh.bias[c];
+            v[ch * 8 + j] = z;
+            if (e0 + c < E) {
+              if (z > m) { m = z; a = e0 + c; }
+            }
+          }
+          if (logits && valid) {  // the chunk's 8 logits of this token: 16-byte stores when aligned
+            const int c0 = e0 + cbeg + ch * 8;
+            float* dst = logits + tok * E + c0;
+            if ((E & 3) == 0 && c0 + 8 <= E) {
+#pragma unroll
+              for (int q4 = 0; q4 < 2; ++q4)
+                *reinterpret_cast<float4*>(dst + 4 * q4) =
+                    make_float4(v[ch * 8 + 4 * q4], v[ch * 8 + 4 * q4 + 1], v[ch * 8 + 4 * q4 + 2],
+                                v[ch * 8 + 4 * q4 + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (c0 + j < E) dst[j] = v[ch * 8 + j];
+            }
+          }
+        }
+      }
+      // the accumulator set is read: the next tile's MMAs may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.aempty[buf]);
+
+      if (has_cols) {
+        sh.red_m[cg][i] = m;
+        sh.red_a[cg][i] = a;
+      }
+      rt_epi_sync();
+      float mc = -INFINITY;  // max over this CTA's experts
+      int ac = INT_MAX;
+#pragma unroll
+      for (int k = 0; k < NCG; ++k)
+        if (sh.red_m[k][i] > mc) { mc = sh.red_m[k][i]; ac = sh.red_a[k][i]; }
+
+      // pass 1b: exp(z - mc) in registers, partial sums
+      float ps = 0.f;
+      if (has_cols) {
+        const float mcs = mc * LOG2E;
+#pragma unroll
+        for (int k = 0; k < CPW; ++k) {
+          const float ex = (e0 + cbeg + k < E) ? ex2_approx(fmaf(v[k], LOG2E, -mcs)) : 0.f;
+          v[k] = ex;
+          ps += ex;
+        }
+        sh.red_s[cg][i] = ps;
+      }
+      if (Q > 1 && leader) {
+        int ok = 1;
+        // every peer has read its receive buffer of the previous tile
+        if (lt >= 1 && !mbar_wait_cluster(&bar.rfree, (lt - 1) & 1)) {
+          raise_error(err, ERR_TIMEOUT);
+          bar.abort_flag = 1;
+          ok = 0;
+        }
+        // arm this CTA's receive barrier for the tile: Q slices of 12 bytes per token
+        mbar_arrive_expect_tx(&bar.rfull, (uint32_t)(Q * RT_BM * 12));
+        bar.ep_ok = ok;
+      }
+      rt_epi_sync();
+      if (cg == 0) {
+        float sc = 0.f;
+#pragma unroll
+        for (int k = 0; k < NCG; ++k) sc += sh.red_s[k][i];
+        if (Q > 1) {  // into slot q of every peer's receive buffer
+          for (int rk = 0; rk < Q; ++rk) {
+            st_async_v2_f32(&sh.rms[q][i], mc, sc, &bar.rfull, (uint32_t)rk);
+            st_async_s32(&sh.ra[q][i], ac, &bar.rfull, (uint32_t)rk);
+          }
         } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < E) dst[j] = v[ch * 16 + j];
+          sh.rms[0][i] = make_float2(mc, sc);
+          sh.ra[0][i] = ac;
         }
       }
-    }
-  }
-  if (has_cols) {
-    sh.red_m[cg][i] = m;
-    sh.red_a[cg][i] = a;
-  }
-  __syncthreads();
-  float mc = -INFINITY;  // max over this CTA's experts
-  int ac = INT_MAX;
-#pragma unroll
-  for (int k = 0; k < NCG; ++k)
-    if (sh.red_m[k][i] > mc) { mc = sh.red_m[k][i]; ac = sh.red_a[k][i]; }
+      bool xok = true;
+      if (Q > 1) {
+        if (leader) {
+          int ok = bar.ep_ok;
+          if (ok && !mbar_wait_cluster(&bar.rfull, lt & 1)) {
+            raise_error(err, ERR_TIMEOUT);
+            bar.abort_flag = 1;
+            ok = 0;
+          }
+          bar.ep_ok = ok;
+        }
+        rt_epi_sync();
+        xok = bar.ep_ok != 0;
+      } else {
+        rt_epi_sync();
+      }
+      if (cg == 0) {
+        float M = -INFINITY, S = 0.f;
+        int A = INT_MAX;
+        if (xok) {  // expert slices in rank order: the lowest index wins a tie
+          for (int rk = 0; rk < Q; ++rk) {
+            const float mr = sh.rms[rk][i].x;
+            if (mr > M) {
+              M = mr;
+              A = sh.ra[rk][i];
+            }
+          }
+          for (int rk = 0; rk < Q; ++rk) {
+            const float2 ms = sh.rms[rk][i];
+            if (ms.y > 0.f) S += ms.y * expf(ms.x - M);
+          }
+        }
+        if (A < 0 || A >= E) {  // only non-finite logits (or a failed exchange) get here
+          if (valid) raise_error(err, ERR_BOUNDS);
+          A = 0;
+        }
+        sh.Mall[i] = M;
+        sh.Sall[i] = S;
+        sh.texp[i] = valid ? A : -1;
+        const float lse = M + logf(S);  // log sum_e exp z_e over all E experts (router z-loss)
+        sh.zz[i] = valid ? lse * lse : 0.f;
+      }
+      rt_epi_sync();
+      // this CTA has read its receive buffer: peers may fill it with the next tile
+      if (Q > 1 && leader)
+        for (int rk = 0; rk < Q; ++rk) mbar_arrive_remote(&bar.rfree, (uint32_t)rk);
 
-  // pass 1b: exp(z - mc) in registers, partial sums
-  float ps = 0.f;
-  if (run && has_cols) {
-    const float mcs = mc * LOG2E;
+      // pass 2: p = exp(z - mc) * exp(mc - M) / S; column sums over the tile's tokens
+      const float scale = valid ? expf(mc - sh.Mall[i]) / sh.Sall[i] : 0.f;
+      if (has_cols) {
 #pragma unroll
-    for (int k = 0; k < CPW; ++k) {
-      const float ex = (e0 + cbeg + k < E) ? ex2_approx(fmaf(v[k], LOG2E, -mcs)) : 0.f;
-      v[k] = ex;
-      ps += ex;
-    }
-  }
-  if (has_cols) sh.red_s[cg][i] = ps;
-  __syncthreads();
-  if (cg == 0) {
-    float sc = 0.f;
+        for (int ch = 0; ch < CPW / 8; ++ch) {
+          float* p = v + ch * 8;  // scaled in place: exp(z - mc) is not needed afterwards
 #pragma unroll
-    for (int k = 0; k < NCG; ++k) sc += sh.red_s[k][i];
-    sh.m[i] = mc;
-    sh.s[i] = sc;
-    sh.a[i] = ac;
-  }
-
-  // exchange between the cluster's CTAs (expert slices in rank order)
-  if (Q > 1) cluster_sync();
-  else __syncthreads();
-  if (cg == 0) {
-    float M = sh.m[i], S = sh.s[i];
-    int A = sh.a[i];
-    if (Q > 1) {
-      M = -INFINITY;
-      A = INT_MAX;
-      for (int rk = 0; rk < Q; ++rk) {
-        const float mr = dsmem_ld_f32(dsmem_addr(&sh.m[i], rk));
-        if (mr > M) {
-          M = mr;
-          A = dsmem_ld_s32(dsmem_addr(&sh.a[i], rk));
+          for (int j = 0; j < 8; ++j) {
+            const int c = cbeg + ch * 8 + j;
+            p[j] *= scale;  // 0 past E (v = 0) and for invalid tokens (scale = 0)
+            if (probs && valid && e0 + c < E) probs[tok * E + e0 + c] = p[j];
+          }
+          const float cs = warp_colsum8(p, lane);
+          if ((lane & 3) == 0) sh.colsum[lq][cbeg + ch * 8 + (lane >> 2)] = cs;
         }
       }
-      S = 0.f;
-      for (int rk = 0; rk < Q; ++rk) {
-        const float mr = dsmem_ld_f32(dsmem_addr(&sh.m[i], rk));
-        const float sr = dsmem_ld_f32(dsmem_addr(&sh.s[i], rk));
-        if (sr > 0.f) S += sr * expf(mr - M);
-      }
-    }
-    if (A < 0 || A >= E) {  // only non-finite logits (or an aborted tile) get here
-      if (run && valid) raise_error(err, ERR_BOUNDS);
-      A = 0;
-    }
-    sh.Mall[i] = M;
-    sh.Sall[i] = S;
-    sh.texp[i] = valid ? A : -1;
-    const float lse = M + logf(S);  // log sum_e exp z_e over all E experts (router z-loss)
-    sh.zz[i] = (run && valid) ? lse * lse : 0.f;
-  }
-  __syncthreads();
+      const int A = sh.texp[i];
+      if (cg == 0 && A >= e0 && A < e0 + EC) atomicAdd(&sh.hist[A - e0], 1);
+      rt_epi_sync();
 
-  // pass 2: p = exp(z - mc) * exp(mc - M) / S; column sums over the tile's tokens
-  const float scale = (run && valid) ? expf(mc - sh.Mall[i]) / sh.Sall[i] : 0.f;
-  if (has_cols) {
-#pragma unroll
-    for (int ch = 0; ch < CPW / 16; ++ch) {
-      float p[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int c = cbeg + ch * 16 + j;
-        p[j] = v[ch * 16 + j] * scale;  // 0 past E (v = 0) and for invalid tokens (scale = 0)
-        if (probs && valid && run && e0 + c < E) probs[tok * E + e0 + c] = p[j];
+      const size_t tbase = ((size_t)g * nT + tile) * E;
+      if (q == 0 && warp == 2) {  // the tile's sum of (log sum exp z)^2, fixed order
+        float zs = (sh.zz[lane] + sh.zz[lane + 32]) + (sh.zz[lane + 64] + sh.zz[lane + 96]);
+        zs = warp_sum(zs);
+        if (lane == 0) tile_Z[(size_t)g * nT + tile] = zs;
       }
-      const float cs = warp_colsum16(p, lane);
-      if ((lane & 1) == 0) sh.colsum[lq][cbeg + ch * 16 + (lane >> 1)] = cs;
-    }
-  }
-  const int A = sh.texp[i];
-  if (cg == 0 && A >= e0 && A < e0 + EC) atomicAdd(&sh.hist[A - e0], 1);
-  __syncthreads();
-
-  const size_t tbase = ((size_t)g * nT + tile) * E;
-  if (q == 0 && warp == 0) {  // the tile's sum of (log sum exp z)^2, fixed order
-    float zs = (sh.zz[lane] + sh.zz[lane + 32]) + (sh.zz[lane + 64] + sh.zz[lane + 96]);
-    zs = warp_sum(zs);
-    if (lane == 0) tile_Z[(size_t)g * nT + tile] = zs;
-  }
-  for (int c = threadIdx.x; c < EC; c += blockDim.x) {
-    const int e = e0 + c;
-    if (e < E) {
-      tile_P[tbase + e] = ((sh.colsum[0][c] + sh.colsum[1][c]) + sh.colsum[2][c]) + sh.colsum[3][c];
-      tile_hist[tbase + e] = sh.hist[c];
-    }
-  }
-  if (q == 0 && cg == 0) {
-    // rank among the tile's earlier tokens with the same expert
-    const int key = valid ? A : -1 - lane;
-    const unsigned same = __match_any_sync(0xffffffffu, key);
-    int rk = __popc(same & ((1u << lane) - 1u));
-    for (int j = 0; j < lq * 32; ++j) rk += sh.texp[j] == A;
-    if (valid) {
-      expert[tok] = A;
-      gate[tok] = 1.0f / sh.Sall[i];  // exp(z_A - M) / S with z_A = M; never renormalised
-      rank[tok] = rk;
+      for (int c = et; c < EC; c += 32 * RT_EPI_WARPS) {
+        const int e = e0 + c;
+        if (e < E) {
+          tile_P[tbase + e] = ((sh.colsum[0][c] + sh.colsum[1][c]) + sh.colsum[2][c]) + sh.colsum[3][c];
+          tile_hist[tbase + e] = sh.hist[c];
+        }
+        sh.hist[c] = 0;  // for the next tile
+      }
+      if (q == 0 && cg == 0) {
+        // rank among the tile's earlier tokens with the same expert
+        const int key = valid ? A : -1 - lane;
+        const unsigned same = __match_any_sync(0xffffffffu, key);
+        int rk = __popc(same & ((1u << lane) - 1u));
+        for (int j = 0; j < lq * 32; ++j) rk += sh.texp[j] == A;
+        if (valid) {
+          expert[tok] = A;
+          gate[tok] = 1.0f / sh.Sall[i];  // exp(z_A - M) / S with z_A = M; never renormalised
+          rank[tok] = rk;
+        }
+      }
+      rt_epi_sync();  // the tile's scratch is read before the next tile writes it
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (Q > 1) cluster_sync();  // no peer reads this CTA's shared memory or arrives on its barriers any more
   if (warp == 1) tmem_dealloc(tmem, Gm::TMEM_COLS);
-  if (Q > 1) cluster_sync();  // peers are done reading this CTA's m / s / a
 }
 
 // ---------------------------------------------------------------- host side
-template <int EC, bool DEEP>
-static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteArgs& a, int nT, int Q, int use3d,
+// Clusters of Q CTAs that fit on the device at once (cached per device and kernel).
+template <typename K>
+static int rt_clusters(K kern, int smem, int Q) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (Q > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)Q, 1, 1);
+    cfg.blockDim = dim3(RT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)Q;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = device_sm_count() / Q;
+    }
+  } else {
+    n = device_sm_count();
+  }
+  if (n < 1) n = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+template <int EC, int NAX>
+static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteArgs& a, int nT, int Q,
                      int32_t* rank, cudaStream_t s) {
-  auto kern = router_tc_kernel<EC, DEEP>;
-  constexpr int smem = rt_smem_bytes<EC, DEEP>();
+  auto kern = router_tc_kernel<EC, NAX>;
+  constexpr int smem = rt_smem_bytes<EC, NAX>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-  const cudaError_t e = launch_k(kern, dim3((unsigned)(Q * nT), (unsigned)a.G, 1), dim3(RT_THREADS, 1, 1), smem, s,
-                                 /*pdl=*/true, (unsigned)Q, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, use3d, a.expert,
+  const long long total = (long long)a.G * nT;
+  if (total >= (1ll << 31)) return -1;
+  const int fit = rt_clusters(kern, smem, Q);
+  const int ncl = (int)(total < fit ? total : fit);
+  const cudaError_t e = launch_k(kern, dim3((unsigned)(Q * ncl), 1, 1), dim3(RT_THREADS, 1, 1), smem, s,
+                                 /*pdl=*/true, (unsigned)Q, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, (int)total, a.expert,
                                  a.gate, rank, a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs, a.err);
   return e == cudaSuccess ? 1 : -1;
 }
 
 // Experts per CTA: the smallest power of two >= 16 that keeps the cluster at <= 8
-// CTAs, raised to 64 when E allows (more parallel CTAs for few-token batches).
+// CTAs, raised to 64 when E allows (fewer CTAs re-reading each token tile).
 int router_tc_experts_per_cta(int E) {
   int ec = 16;
   while ((E + ec - 1) / ec > 8) ec *= 2;
@@ -504,7 +635,8 @@ int router_tc_mma_n(int EC) { return EC == 256 ? 256 : (3 * EC <= 256 ? 3 * EC :
 size_t router_tc_wsplit_bytes(int E, int d) {
   const int EC = router_tc_experts_per_cta(E);
   const size_t Q = (size_t)((E + EC - 1) / EC);
-  return Q * EC * 3 * (size_t)d * 2;
+  const size_t NK = (size_t)((d + RT_BK - 1) / RT_BK);
+  return Q * EC * 3 * NK * RT_BK * 2;
 }
 
 int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
@@ -514,37 +646,30 @@ int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
   const int EC = router_tc_experts_per_cta(a.E);
   const int Q = (a.E + EC - 1) / EC;
   if (EC > 256 || Q > 8) return -1;
-  const long long n = (long long)Q * EC * a.d;
+  const int NK = (a.d + RT_BK - 1) / RT_BK;
+  const long long n = (long long)Q * EC * NK * RT_BK;
   const unsigned sb = (unsigned)((n + 255) / 256 < 148 * 16 ? (n + 255) / 256 : 148 * 16);
   if (launch_k(router_split_kernel, dim3(sb), dim3(256), 0, s, false, 1, a.Wr, (__nv_bfloat16*)a.wsplit, a.E, a.d, EC,
-               n) != cudaSuccess)
+               NK, n) != cudaSuccess)
     return -1;
-  // One wave on this device's SMs -> the deep ring; EC >= 128 always takes it (512 TMEM columns).
-  const long long ctas = (long long)Q * nT * a.G;
-  const bool deep = EC >= 128 || ctas <= (long long)device_sm_count();
-  const int NA = (EC <= 16 || (EC <= 64 && deep)) ? 2 : 1;  // RtCfg<EC, deep>::NA
-  const int use3d = a.d % RT_BK == 0 ? 1 : 0;
+  if ((long long)Q * NK * 3 * EC >= (1ll << 31)) return -1;  // TMA row coordinates are 32-bit
+  const int nax = a.d % (2 * RT_BK) == 0 ? 2 : 1;  // x stages of two atoms (256 B per row) when d allows
   CUtensorMap tmX, tmW;
-  if (use3d) {
-    if (!encode_bf16_3d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM, (uint32_t)NA)) return -1;
-    if (!encode_bf16_3d(&tmW, a.wsplit, (uint64_t)3 * Q * EC, (uint64_t)a.d, (uint32_t)router_tc_mma_n(EC),
-                        (uint32_t)NA))
-      return -1;
-  } else {
-    if (!encode_bf16_2d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM)) return -1;
-    if (!encode_bf16_2d(&tmW, a.wsplit, (uint64_t)3 * Q * EC, (uint64_t)a.d, (uint32_t)router_tc_mma_n(EC)))
-      return -1;
+  if (nax == 2) {
+    if (!encode_bf16_3d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM, 2u)) return -1;
+  } else if (!encode_bf16_2d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM)) {
+    return -1;
   }
+  if (!encode_bf16_2d(&tmW, a.wsplit, (uint64_t)3 * Q * EC * NK, (uint64_t)RT_BK, (uint32_t)router_tc_mma_n(EC)))
+    return -1;
   int n2;
-#define SMOE_RT(ECV)                                                                                        \
-  n2 = deep ? launch_rt<ECV, true>(tmX, tmW, a, nT, Q, use3d, rank, s)                                      \
-            : launch_rt<ECV, false>(tmX, tmW, a, nT, Q, use3d, rank, s)
+#define SMOE_RT(ECV) n2 = nax == 2 ? launch_rt<ECV, 2>(tmX, tmW, a, nT, Q, rank, s) : launch_rt<ECV, 1>(tmX, tmW, a, nT, Q, rank, s)
   switch (EC) {
     case 16: SMOE_RT(16); break;
     case 32: SMOE_RT(32); break;
     case 64: SMOE_RT(64); break;
-    case 128: n2 = launch_rt<128, true>(tmX, tmW, a, nT, Q, use3d, rank, s); break;
-    default: n2 = launch_rt<256, true>(tmX, tmW, a, nT, Q, use3d, rank, s); break;
+    case 128: SMOE_RT(128); break;
+    default: SMOE_RT(256); break;
   }
 #undef SMOE_RT
   return n2 < 0 ? -1 : 2;
