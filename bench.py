@@ -264,7 +264,9 @@ def config_of(shape, args):
             "E": shape.E, "capacity_factor": shape.capacity_factor, "top_k": getattr(args, "top_k", 1),
             "global_batch_tokens": shape.N * args.gpus, "parallelism": f"replicas{args.gpus}",
             "l2": "flushed (256 MB write) before every device-timed step, outside its events; expert "
-                  "weights (>= 0.6 GB) exceed L2 anyway"}
+                  "weights (>= 0.6 GB) exceed L2 anyway",
+            "router_weights": "bf16 split prepared once at load (switch_prepare_router); every step runs "
+                              "the router GEMM, softmax, top-1, statistics, slots, dispatch, FFN, combine"}
 
 
 
@@ -365,9 +367,14 @@ def run_gpu(args, shape):
     y = torch.empty(shape.N, shape.d_model, dtype=dt, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # inference: the router weights are split into their bf16 pieces once, at load time
+    prepared = shape.dtype == "bf16"
+    if prepared:
+        layer.prepare_router(inp["Wr"], stream=stream)
+    Wr_step = None if prepared else inp["Wr"]
 
     def step(lay):
-        lay.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], r=r, y=y,
+        lay.forward(inp["x"], Wr_step, inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], r=r, y=y,
                     stream=stream)
 
     for _ in range(args.warmup):
@@ -399,6 +406,8 @@ def run_gpu(args, shape):
     # ---------------- per-stage times: a profiled pass of the same workload (CUDA events
     # recorded on this stream between the stages; no programmatic overlap across them)
     prof_layer = mk(True)
+    if prepared:
+        prof_layer.prepare_router(inp["Wr"], stream=stream)
     n_prof = max(3, min(args.steps, 50))
     stage_sum = np.zeros(5)
     for i in range(args.warmup + n_prof):
@@ -422,7 +431,7 @@ def run_gpu(args, shape):
     done = [torch.cuda.Event() for _ in range(2)]
 
     def e2e_step(i):  # no L2 flush here: x comes from the host every step
-        layer.forward_host(x_host, inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"],
+        layer.forward_host(x_host, Wr_step, inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"],
                            y_host=y_host, aux_host=aux_host, r=r, done=done[i % 2], stream=stream)
 
     for i in range(args.warmup):

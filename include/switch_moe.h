@@ -160,9 +160,27 @@ SWITCH_API switch_status switch_destroy(switch_handle h);
  * except probs/logits, which need their flags.  All fields other than
  * probs, logits and the z-loss are required, and with SWITCH_FLAG_TOP2 the
  * second-choice fields too.
+ * With bfloat16 activations Wr may be NULL after switch_prepare_router on this handle:
+ * the call then uses the prepared copy of the router weights (see there).  A non-NULL Wr
+ * is read by this call, and the prepared copy is replaced by its split.
  */
 SWITCH_API switch_status switch_route(switch_handle h, const void* x, const float* Wr, const float* br,
                            const switch_route_out* out, void* stream);
+
+/*
+ * Prepare the router weights once for calls that do not change them (inference).
+ *   Wr [E, d] float32, read on `stream` by this call.
+ * With bfloat16 activations the router multiplies on the tensor cores with W_r split into
+ * three bfloat16 pieces (hi + mid + lo = w to within 2^-24 |w|).  Every switch_route,
+ * switch_forward and switch_forward_host with a non-NULL Wr splits it again first (one
+ * small kernel: 6 E d bytes written); after this call, passing Wr = NULL skips that step
+ * and uses this split, until the next call with a non-NULL Wr replaces it.  The caller
+ * must not change the weights in between without preparing again.
+ * Returns SWITCH_ERR_UNSUPPORTED with float32 activations (the CUDA-core router reads Wr
+ * itself), SWITCH_ERR_INVALID_ARG for a NULL handle or Wr.  Asynchronous on `stream`.
+ * Not an operation of the method: a re-layout of the router weights kept on the handle.
+ */
+SWITCH_API switch_status switch_prepare_router(switch_handle h, const float* Wr, void* stream);
 
 /*
  * Dispatch gather: xe[e, row_t, :] = x_t for every kept token t with expert e

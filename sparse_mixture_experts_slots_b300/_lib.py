@@ -54,6 +54,7 @@ SIGNATURES = {
     "switch_create": (c_int, [POINTER(SwitchConfig), POINTER(c_void_p)]),
     "switch_destroy": (c_int, [c_void_p]),
     "switch_route": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, POINTER(SwitchRouteOut), c_void_p]),
+    "switch_prepare_router": (c_int, [c_void_p, c_void_p, c_void_p]),
     "switch_dispatch": (c_int, [c_void_p, c_void_p, POINTER(SwitchRouteOut), c_void_p, c_void_p]),
     "switch_expert_ffn": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p]),

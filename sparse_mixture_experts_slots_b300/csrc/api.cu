@@ -69,6 +69,7 @@ struct switch_layer {
   void* bw_dyeT; void* bw_xeT; // [E, d, Rpad]
   int32_t* bw_rows_d; int32_t* bw_rows_F;
   uint32_t* bw_counters; int bw_counter_words;
+  bool wsplit_ready;  // wsplit holds the pieces of the last router weights split on this handle
   cudaEvent_t ev[6];
   bool have_events;
   int last_launches;
@@ -308,7 +309,10 @@ switch_status switch_destroy(switch_handle h) {
 
 static switch_status route_args(switch_handle h, const void* x, const float* Wr, const float* br,
                                 const switch_route_out* out, RouteArgs* a) {
-  if (!h || !Wr || !route_out_ok(out, h ? h->N : 0, h && top2_of(&h->cfg))) return SWITCH_ERR_INVALID_ARG;
+  if (!h || !route_out_ok(out, h ? h->N : 0, h && top2_of(&h->cfg))) return SWITCH_ERR_INVALID_ARG;
+  // Wr may be NULL only for the tensor-core router with prepared weights
+  if (!Wr && !(h->cfg.dtype == SWITCH_BF16 && h->wsplit_ready)) return SWITCH_ERR_INVALID_ARG;
+  if (Wr && h->cfg.dtype == SWITCH_BF16 && h->N > 0) h->wsplit_ready = true;  // this call splits Wr
   if (h->N > 0 && !x) return SWITCH_ERR_INVALID_ARG;
   if (x && !aligned16(x)) return SWITCH_ERR_INVALID_ARG;
   const switch_config& c = h->cfg;
@@ -376,6 +380,14 @@ switch_status switch_route(switch_handle h, const void* x, const float* Wr, cons
   const switch_status st = route_args(h, x, Wr, br, out, &a);
   if (st != SWITCH_OK) return st;
   return launched(launch_route(a, (cudaStream_t)stream), h);
+}
+
+switch_status switch_prepare_router(switch_handle h, const float* Wr, void* stream) {
+  if (!h || !Wr) return SWITCH_ERR_INVALID_ARG;
+  if (h->cfg.dtype != SWITCH_BF16) return SWITCH_ERR_UNSUPPORTED;
+  if (launch_router_split(Wr, h->wsplit, h->cfg.E, h->cfg.d_model, (cudaStream_t)stream) < 0) return SWITCH_ERR_CUDA;
+  h->wsplit_ready = true;
+  return SWITCH_OK;
 }
 
 switch_status switch_dispatch(switch_handle h, const void* x, const switch_route_out* r, void* xe, void* stream) {

@@ -297,6 +297,13 @@ __device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t rank)
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(dsmem_addr(bar, rank))
                : "memory");
 }
+// The same without release semantics (no implied cluster-scope fence): for a signal that
+// orders nothing but work already completed, e.g. "the values read from this buffer are
+// consumed", where the reads finished before a barrier that precedes the arrival.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint64_t* bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(dsmem_addr(bar, rank))
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -53,7 +53,8 @@ struct RouteArgs {
   // workspace
   float* logits;       // [N, E] float32 logits of the CUDA-core router (workspace or the caller's)
   float* logits_out;   // [N, E] or null: logits the caller asked for
-  void* wsplit;        // W_r split into hi, mid, lo bf16 pieces (tensor-core router; layout in route_tc.cu)
+  void* wsplit;        // W_r split into hi, mid, lo bf16 pieces (tensor-core router; layout in route_tc.cu);
+                       // with Wr null the router uses it as it is (prepared by an earlier split)
   int32_t* tile_hist;  // [G, nT, E]
   float* tile_P;       // [G, nT, E]
   float* tile_Z;       // [G, nT]: sum over the tile's tokens of (log sum_e exp z)^2
@@ -130,6 +131,8 @@ int launch_route(const RouteArgs& a, cudaStream_t s);
 // Writes expert, gate, the in-tile rank (into `rank`), tile_hist, tile_P and, when
 // asked, logits_out / probs.  Returns launches or -1.
 int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s);
+// W_r -> its bf16 pieces in wsplit (the first kernel of launch_router_tc when a.Wr is set).
+int launch_router_split(const float* Wr, void* wsplit, int E, int d, cudaStream_t s);
 int router_tc_experts_per_cta(int E);
 int router_tc_mma_n(int EC);
 // Bytes of the split W_r workspace ([Q][d / 64 atoms][hi, mid, lo][EC][64] bf16) for E experts of width d.

@@ -229,22 +229,25 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     tmem_alloc(&bar.tmem_slot, Gm::TMEM_COLS);
     tmem_relinquish();
   }
-  for (int c = threadIdx.x; c < EC; c += blockDim.x) {  // br comes from the caller, not a prior kernel
-    const int e = e0 + c;
-    sh.bias[c] = (br && e < E) ? br[e] : 0.f;
-    sh.hist[c] = 0;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (Q > 1) cluster_sync();  // every peer's barriers are initialised before any remote arrival
   const uint32_t tmem = bar.tmem_slot;
   griddep_launch_dependents();  // after the TMEM allocation: a dependent grid cannot starve it
+  // This grid may start while the previous kernel of the stream still runs: everything it
+  // reads from memory (x, the W_r pieces, br) is read after this wait.
+  griddep_wait();
+  for (int c = threadIdx.x; c < EC; c += blockDim.x) {
+    const int e = e0 + c;
+    sh.bias[c] = (br && e < E) ? br[e] : 0.f;
+    sh.hist[c] = 0;
+  }
+  __syncthreads();
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      griddep_wait();  // the W_r pieces come from the previous kernel
       uint32_t xi = 0, wi = 0;
       bool ok = true;
       for (int tid = cl; tid < total_tiles && ok; tid += ncl) {
@@ -511,9 +514,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         sh.zz[i] = valid ? lse * lse : 0.f;
       }
       rt_epi_sync();
-      // this CTA has read its receive buffer: peers may fill it with the next tile
+      // this CTA has read its receive buffer (every read value was consumed before the
+      // barrier above): peers may fill it with the next tile
       if (Q > 1 && leader)
-        for (int rk = 0; rk < Q; ++rk) mbar_arrive_remote(&bar.rfree, (uint32_t)rk);
+        for (int rk = 0; rk < Q; ++rk) mbar_arrive_remote_relaxed(&bar.rfree, (uint32_t)rk);
 
       // pass 2: p = exp(z - mc) * exp(mc - M) / S; column sums over the tile's tokens
       const float scale = valid ? expf(mc - sh.Mall[i]) / sh.Sall[i] : 0.f;
@@ -639,6 +643,18 @@ size_t router_tc_wsplit_bytes(int E, int d) {
   return Q * EC * 3 * NK * RT_BK * 2;
 }
 
+int launch_router_split(const float* Wr, void* wsplit, int E, int d, cudaStream_t s) {
+  const int EC = router_tc_experts_per_cta(E);
+  const int Q = (E + EC - 1) / EC;
+  const int NK = (d + RT_BK - 1) / RT_BK;
+  const long long n = (long long)Q * EC * NK * RT_BK;
+  const unsigned sb = (unsigned)((n + 255) / 256 < 148 * 16 ? (n + 255) / 256 : 148 * 16);
+  return launch_k(router_split_kernel, dim3(sb), dim3(256), 0, s, false, 1, Wr, (__nv_bfloat16*)wsplit, E, d, EC, NK,
+                  n) == cudaSuccess
+             ? 1
+             : -1;
+}
+
 int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
   const long long N = (long long)a.G * a.T;
   if (N == 0) return 0;
@@ -647,12 +663,12 @@ int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
   const int Q = (a.E + EC - 1) / EC;
   if (EC > 256 || Q > 8) return -1;
   const int NK = (a.d + RT_BK - 1) / RT_BK;
-  const long long n = (long long)Q * EC * NK * RT_BK;
-  const unsigned sb = (unsigned)((n + 255) / 256 < 148 * 16 ? (n + 255) / 256 : 148 * 16);
-  if (launch_k(router_split_kernel, dim3(sb), dim3(256), 0, s, false, 1, a.Wr, (__nv_bfloat16*)a.wsplit, a.E, a.d, EC,
-               NK, n) != cudaSuccess)
-    return -1;
   if ((long long)Q * NK * 3 * EC >= (1ll << 31)) return -1;  // TMA row coordinates are 32-bit
+  int launches = 0;
+  if (a.Wr) {  // else: the pieces prepared by an earlier split are used as they are
+    if (launch_router_split(a.Wr, a.wsplit, a.E, a.d, s) < 0) return -1;
+    ++launches;
+  }
   const int nax = a.d % (2 * RT_BK) == 0 ? 2 : 1;  // x stages of two atoms (256 B per row) when d allows
   CUtensorMap tmX, tmW;
   if (nax == 2) {
@@ -672,7 +688,7 @@ int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
     default: SMOE_RT(256); break;
   }
 #undef SMOE_RT
-  return n2 < 0 ? -1 : 2;
+  return n2 < 0 ? -1 : launches + 1;
 }
 
 }  // namespace smoe

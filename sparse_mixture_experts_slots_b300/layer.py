@@ -128,6 +128,10 @@ class SwitchMoE:
         return torch.empty(self.E, self.block_rows, width or self.d_model, dtype=self.dtype, device=self.device)
 
     # ------------------------------------------------------------------ stages
+    def prepare_router(self, Wr, stream=None) -> None:
+        """Split the router weights once (bfloat16 activations); later calls may pass Wr=None."""
+        check(self.lib.switch_prepare_router(self._h, _ptr(Wr), _stream(stream)), "switch_prepare_router")
+
     def route(self, x, Wr, br=None, out: Optional[RouteResult] = None, stream=None) -> RouteResult:
         r = out or self.alloc_route()
         cs = r.c_struct()
