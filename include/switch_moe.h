@@ -296,6 +296,28 @@ SWITCH_API switch_status switch_sync_status(switch_handle h, void* stream);
  */
 SWITCH_API switch_status switch_stage_ms(switch_handle h, float* ms, int n);
 
+/*
+ * Expert parallelism: regroup the rows an expert-owning rank receives.  The Switch
+ * Transformers card (ai-papers.xuzou.cn, 方法适配) shards the experts over the cores and
+ * moves tokens with an all-to-all before the expert FFN and another after it.  With W ranks,
+ * this rank owning El experts, every source rank s sends the blocks [El][R][row] of its
+ * dispatched buffer for those experts (R = the source's expert block rows, G*C); counts
+ * [W][El] int32 (device) holds the valid rows of each block (the source's expert_rows).
+ *   inverse = 0: src = chunks [W][El][R][row] (as received), dst = packed [El][W*R][row]:
+ *                dst[e][off(s, e) + i] = src[s][e][i] for i < counts[s][e], with
+ *                off(s, e) = counts[0][e] + ... + counts[s-1][e] (sources in rank order);
+ *                rows_out (device [El] int32, may be NULL) gets sum_s counts[s][e], the row
+ *                counts for switch_expert_ffn on the packed buffer.
+ *   inverse = 1: src = packed, dst = chunks: dst[s][e][i] = src[e][off(s, e) + i] (the
+ *                expert outputs back into per-source chunks for the return all-to-all);
+ *                rows_out must be NULL.
+ * Rows past the counts are not written.  row bytes: a multiple of 16; src and dst 16-byte
+ * aligned, not overlapping; a count outside 0 .. R counts as zero.  Asynchronous on
+ * `stream`; argument errors return SWITCH_ERR_INVALID_ARG.
+ */
+SWITCH_API switch_status switch_ep_regroup(const void* src, void* dst, const int32_t* counts, int32_t* rows_out,
+                                           int W, int El, int R, int row_bytes, int inverse, void* stream);
+
 /* Number of kernels the last switch_forward on this handle launched. */
 SWITCH_API int switch_last_launch_count(switch_handle h);
 

@@ -486,6 +486,56 @@ def expert_outputs_top2(x, r: Route2, W1, b1, W2, b2, tokens: Optional[Sequence[
     return out
 
 
+# ----------------------------------------------------------------------------- expert parallelism
+
+def ep_forward(x_ranks, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor: float, world: int,
+               alpha: float = 1e-2, capacity_override: int = 0):
+    """The top-1 layer with its experts sharded over `world` ranks, step by step.
+
+    [card, 方法适配]: the input is laid out per core, every core routes its own tokens, an
+    all-to-all sends each token to the core holding its expert, the experts run there, and a
+    second all-to-all returns the outputs for the combine.  Reading: rank r holds the experts
+    floor(rE/world) .. floor((r+1)E/world) - 1 and routes its own G groups of T tokens
+    (x_ranks[r] is [G*T, d]); what travels is each rank's per-expert block of the dispatched
+    buffer with its valid row count.  Written with explicit per-rank send and receive lists
+    (no communication library).  Returns (routes per rank, y per rank).
+    """
+    begin = [(r * E) // world for r in range(world + 1)]
+    routes, xe = [], []
+    for r in range(world):
+        rt = route(x_ranks[r], Wr, br, G, T, E, capacity_factor, alpha, capacity_override)
+        routes.append(rt)
+        xe.append(dispatch(x_ranks[r], rt, E, G))  # [E, G*C, d]
+    # first all-to-all: owner o receives from every source s the blocks of its experts
+    recv = [[xe[s][begin[o]:begin[o + 1]] for s in range(world)] for o in range(world)]
+    rows = [[routes[s].expert_rows[begin[o]:begin[o + 1]] for s in range(world)] for o in range(world)]
+    # each owner runs its experts on the rows received from all sources
+    out = [[np.zeros_like(recv[o][s]) for s in range(world)] for o in range(world)]
+    for o in range(world):
+        for j, e in enumerate(range(begin[o], begin[o + 1])):
+            parts = [recv[o][s][j, :int(rows[o][s][j])] for s in range(world)]
+            stacked = np.concatenate(parts, axis=0)
+            if stacked.shape[0] == 0:
+                continue
+            ye = expert_ffn(stacked, W1[e], None if b1 is None else b1[e], W2[e], None if b2 is None else b2[e])
+            at = 0
+            for s in range(world):
+                n = int(rows[o][s][j])
+                out[o][s][j, :n] = ye[at:at + n]
+                at += n
+    # second all-to-all: source s gets back the output blocks of every owner, in expert order
+    ye_back = [np.concatenate([out[o][s] for o in range(world)], axis=0) for s in range(world)]
+    ys = []
+    for s in range(world):
+        rt = routes[s]
+        y = np.zeros((G * T, np.asarray(x_ranks[s]).shape[1]))
+        for t in range(G * T):
+            if rt.keep[t]:
+                y[t] = rt.gate[t] * ye_back[s][rt.expert[t], rt.row[t]]
+        ys.append(y)
+    return routes, ys
+
+
 # ----------------------------------------------------------------------------- backward (top-1)
 
 def backward(x, Wr, br, W1, b1, W2, b2, G: int, T: int, E: int, capacity_factor: float, dy,

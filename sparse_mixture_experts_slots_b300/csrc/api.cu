@@ -765,6 +765,17 @@ switch_status switch_stage_ms(switch_handle h, float* ms, int n) {
 
 int switch_last_launch_count(switch_handle h) { return h ? h->last_launches : -1; }
 
+switch_status switch_ep_regroup(const void* src, void* dst, const int32_t* counts, int32_t* rows_out, int W, int El,
+                                int R, int row_bytes, int inverse, void* stream) {
+  if (W < 1 || El < 1 || R < 0 || row_bytes <= 0 || row_bytes % 16 != 0 || !counts) return SWITCH_ERR_INVALID_ARG;
+  if ((long long)W * El * R >= (1ll << 31)) return SWITCH_ERR_INVALID_ARG;
+  if ((long long)W * El * R > 0 && (!src || !dst || !aligned16(src) || !aligned16(dst))) return SWITCH_ERR_INVALID_ARG;
+  if (inverse && rows_out) return SWITCH_ERR_INVALID_ARG;
+  return launch_ep_regroup(src, dst, counts, rows_out, W, El, R, row_bytes, inverse != 0, (cudaStream_t)stream) < 0
+             ? SWITCH_ERR_CUDA
+             : SWITCH_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------- routing without a handle

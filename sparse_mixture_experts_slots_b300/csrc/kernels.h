@@ -212,4 +212,9 @@ struct FfnLaunch {
 bool tc_shape_ok(int M, int K);
 int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl);
 
+// Expert parallelism (ep.cu): chunk[W][El][R] rows <-> packed[El][W R] rows, per-(source,
+// expert) counts [W][El]; forward also writes the packed row count per expert (rows_out).
+int launch_ep_regroup(const void* src, void* dst, const int32_t* counts, int32_t* rows_out, int W, int El, int R,
+                      int row_bytes, bool inverse, cudaStream_t s);
+
 }  // namespace smoe

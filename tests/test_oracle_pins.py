@@ -618,3 +618,32 @@ def test_backward_gate_path_only_reaches_the_chosen_expert():
     for e in range(E):
         if not (r.keep & (r.expert == e)).any():
             assert (g["dW1"][e] == 0).all() and (g["dW2"][e] == 0).all()
+
+
+# ----------------------------------------------------------------------------- expert parallelism
+
+@pytest.mark.parametrize("world,E", [(2, 8), (3, 7), (4, 4)])
+def test_sharded_experts_equal_the_single_rank_layer(world, E):
+    # [card, 方法适配]: experts sharded over cores with two all-to-alls compute the same layer
+    # as one core holding every expert over all the cores' routing groups: routing is per
+    # group and each expert output depends on its own token only.  Uneven expert ranges
+    # (E = 7 over 3 ranks) and one expert per rank are included.
+    rng = np.random.default_rng(41 + world)
+    G, T, d, F = 2, 24, 12, 10
+    xs = [rng.standard_normal((G * T, d)) for _ in range(world)]
+    Wr = rng.standard_normal((E, d)) * 0.4
+    br = rng.standard_normal(E) * 0.2
+    W1 = rng.standard_normal((E, F, d)) * 0.3
+    b1 = rng.standard_normal((E, F)) * 0.1
+    W2 = rng.standard_normal((E, d, F)) * 0.3
+    b2 = rng.standard_normal((E, d)) * 0.1
+    routes, ys = so.ep_forward(xs, Wr, br, W1, b1, W2, b2, G, T, E, 0.75, world)
+    ref, y_ref, _ = so.forward(np.concatenate(xs), Wr, br, W1, b1, W2, b2, world * G, T, E, 0.75)
+    N = G * T
+    for r in range(world):
+        sl = slice(r * N, (r + 1) * N)
+        for f in ("expert", "slot", "keep", "gate"):
+            np.testing.assert_array_equal(getattr(routes[r], f), getattr(ref, f)[sl], err_msg=f)
+        np.testing.assert_allclose(routes[r].raw, ref.raw[r * G:(r + 1) * G])
+        np.testing.assert_allclose(ys[r], y_ref[sl], rtol=1e-12, atol=1e-14)
+    assert (~ref.keep).any() and ref.keep.any()  # c = 0.75 drops tokens
