@@ -80,8 +80,8 @@ typedef enum { SWITCH_F32 = 0, SWITCH_BF16 = 1 } switch_dtype;
  * expert outputs and the router logits in the workspace (unfused FFN and combine) for
  * switch_backward.  The workspace grows by float32 gradient scratch (2 E R d + E R d_ff +
  * N + N E floats, R = G min(C, T), plus the router's per-chunk partials, at most 64 M
- * floats) and, with bfloat16 and d, d_ff multiples of 128, by two transposed copies of the
- * expert weights (2 E d d_ff bfloat16) and bfloat16 copies of the backward's activations. */
+ * floats) and, with bfloat16 and d, d_ff multiples of 128, by bfloat16 copies of the
+ * backward's activations (E R (2 d + d_ff) bfloat16). */
 #define SWITCH_FLAG_TRAINING      0x20u
 /* Test only (fault injection on the host's request, no GPU fault): in the tensor-core
  * expert FFN, the first layer-1 tile of expert 0's first token chunk stores its part of h

@@ -58,15 +58,12 @@ struct switch_layer {
   float* bw_dz;   // [N, E]
   float* bw_part; // [nsplit, E, d]: per-token-chunk partial sums of dWr and dbr
   int bw_nsplit;
-  // tensor-core backward (bf16 with tensor-core FFN shapes): transposed weights, bf16 copies
-  void* bw_W1T;   // [E, d, F]
-  void* bw_W2T;   // [E, F, d]
+  // tensor-core backward (bf16 with tensor-core FFN shapes): bf16 copies of the gradients
+  bool bw_tc;
   void* bw_dye16; // [E, R, d]
   void* bw_dh16;  // [E, R, F]
   void* bw_dxe16; // [E, R, d]
   int bw_Rpad;
-  void* bw_hT; void* bw_dhT;   // [E, F, Rpad]
-  void* bw_dyeT; void* bw_xeT; // [E, d, Rpad]
   int32_t* bw_rows_d; int32_t* bw_rows_F;
   uint32_t* bw_counters; int bw_counter_words;
   bool wsplit_ready;  // wsplit holds the pieces of the last router weights split on this handle
@@ -215,16 +212,10 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   if (nsplit > cap) nsplit = cap;
   const size_t o_bpart = take(train ? nsplit * E * d * sizeof(float) : 0);
   const bool train_tc = train && cfg->dtype == SWITCH_BF16 && tc_shape_ok((int)F, (int)d) && tc_shape_ok((int)d, (int)F);
-  const size_t o_w1t = take(train_tc ? E * F * d * 2 : 0);
-  const size_t o_w2t = take(train_tc ? E * F * d * 2 : 0);
   const size_t o_dye16 = take(train_tc ? E * R * d * 2 : 0);
   const size_t o_dh16 = take(train_tc ? E * R * F * 2 : 0);
   const size_t o_dxe16 = take(train_tc ? E * R * d * 2 : 0);
   const size_t Rpad = (R + 63) / 64 * 64;
-  const size_t o_hT = take(train_tc ? E * F * Rpad * 2 : 0);
-  const size_t o_dhT = take(train_tc ? E * F * Rpad * 2 : 0);
-  const size_t o_dyeT = take(train_tc ? E * d * Rpad * 2 : 0);
-  const size_t o_xeT = take(train_tc ? E * d * Rpad * 2 : 0);
   const size_t o_rows2 = take(train_tc ? 2 * E * sizeof(int32_t) : 0);
   const size_t cw2 = 1 + E * ((std::max(d, F) + 255) / 256);
   const size_t o_cnt2 = take(train_tc ? cw2 * sizeof(uint32_t) : 0);
@@ -259,16 +250,11 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->bw_dz = reinterpret_cast<float*>(h->ws + o_bdz);
   h->bw_part = reinterpret_cast<float*>(h->ws + o_bpart);
   h->bw_nsplit = (int)nsplit;
-  h->bw_W1T = train_tc ? h->ws + o_w1t : nullptr;
-  h->bw_W2T = train_tc ? h->ws + o_w2t : nullptr;
+  h->bw_tc = train_tc;
   h->bw_dye16 = train_tc ? h->ws + o_dye16 : nullptr;
   h->bw_dh16 = train_tc ? h->ws + o_dh16 : nullptr;
   h->bw_dxe16 = train_tc ? h->ws + o_dxe16 : nullptr;
   h->bw_Rpad = (int)Rpad;
-  h->bw_hT = h->ws + o_hT;
-  h->bw_dhT = h->ws + o_dhT;
-  h->bw_dyeT = h->ws + o_dyeT;
-  h->bw_xeT = h->ws + o_xeT;
   h->bw_rows_d = reinterpret_cast<int32_t*>(h->ws + o_rows2);
   h->bw_rows_F = h->bw_rows_d + E;
   h->bw_counters = reinterpret_cast<uint32_t*>(h->ws + o_cnt2);
@@ -683,8 +669,7 @@ switch_status switch_backward(switch_handle h, const void* x, const float* Wr, c
   a.dxe = h->bw_dxe;
   a.dg = h->bw_dg;
   a.dz = h->bw_dz;
-  a.W1T = h->bw_W1T;
-  a.W2T = h->bw_W2T;
+  a.tc = h->bw_tc;
   a.dye16 = h->bw_dye16;
   a.dh16 = h->bw_dh16;
   a.dxe16 = h->bw_dxe16;
@@ -692,10 +677,6 @@ switch_status switch_backward(switch_handle h, const void* x, const float* Wr, c
   a.counter_words = h->ffn_counter_words;
   a.err = h->err;
   a.Rpad = h->bw_Rpad;
-  a.hT = h->bw_hT;
-  a.dhT = h->bw_dhT;
-  a.dyeT = h->bw_dyeT;
-  a.xeT = h->bw_xeT;
   a.rows_d = h->bw_rows_d;
   a.rows_F = h->bw_rows_F;
   a.counters2 = h->bw_counters;

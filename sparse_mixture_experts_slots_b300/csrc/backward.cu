@@ -13,11 +13,13 @@
 // through the log-sum-exp (070 page, section 核心思想与公式).
 //
 // With bfloat16 and tensor-core shapes the four expert products run on the persistent
-// tcgen05 FFN kernel (ffn_tc.cu): dh -> dxe as its two layers over transposed W2, W1 (mode 1,
-// a mask epilogue), dW2 and dW1 as layer-1-only launches whose contraction axis is an
-// expert's rows (mode 2).  The router's products, and every product for float32 or other
-// widths, run in one batched float32 kernel on CUDA cores with arbitrary strides and
-// per-batch limits on M, N or K.
+// tcgen05 FFN kernel (ffn_tc.cu) with no copy of any operand: dh -> dxe as its two layers
+// reading W2 and W1 as stored (MN-major operands; mode 1, a mask epilogue), dW2 and dW1 as
+// layer-1-only launches whose contraction axis is an expert's rows, read MN-major from the
+// saved activations (mode 2), with float32 results stored directly.  The rows past each
+// expert's count are zeroed first, so they add nothing to those sums.  The router's
+// products, and every product for float32 or other widths, run in one batched float32
+// kernel on CUDA cores with arbitrary strides and per-batch limits on M, N or K.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -253,81 +255,6 @@ __global__ void __launch_bounds__(256) dx_assemble_kernel(float* __restrict__ dx
   }
 }
 
-// ---------------------------------------------------------------- transpose
-// out[b][q][p] = in[b][p][q] (bfloat16), 32 x 32 tiles through shared memory.
-__global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in,
-                                                             __nv_bfloat16* __restrict__ out, int P, int Q) {
-  __shared__ __nv_bfloat16 t[32][33];
-  const long long b = blockIdx.z;
-  const int p0 = blockIdx.y * 32, q0 = blockIdx.x * 32;
-  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 8 rows of 32 per pass
-  const __nv_bfloat16* src = in + b * (long long)P * Q;
-  __nv_bfloat16* dst = out + b * (long long)P * Q;
-  for (int k = ty; k < 32; k += 8) {
-    const int p = p0 + k, q = q0 + tx;
-    if (p < P && q < Q) t[k][tx] = src[(long long)p * Q + q];
-  }
-  __syncthreads();
-  for (int k = ty; k < 32; k += 8) {
-    const int q = q0 + k, p = p0 + tx;
-    if (p < P && q < Q) dst[(long long)q * P + p] = t[tx][k];
-  }
-}
-
-// out[b][q][p] = (p < lim[b] ? in[b][p][q] : 0) for p < Ppad: an expert block's rows become
-// the contraction axis of a weight gradient, zero past its row count and up to Ppad.
-__global__ void __launch_bounds__(256) transpose_rows_bf16_kernel(const __nv_bfloat16* __restrict__ in,
-                                                                  __nv_bfloat16* __restrict__ out,
-                                                                  const int32_t* __restrict__ lim, int P, int Q,
-                                                                  int Ppad) {
-  __shared__ __nv_bfloat16 t[32][33];
-  const long long b = blockIdx.z;
-  const int p0 = blockIdx.y * 32, q0 = blockIdx.x * 32;
-  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
-  const int np = min(P, lim[b]);
-  const __nv_bfloat16* src = in + b * (long long)P * Q;
-  __nv_bfloat16* dst = out + b * (long long)Ppad * Q;
-  for (int k = ty; k < 32; k += 8) {
-    const int p = p0 + k, q = q0 + tx;
-    t[k][tx] = (p < np && q < Q) ? src[(long long)p * Q + q] : __float2bfloat16_rn(0.f);
-  }
-  __syncthreads();
-  for (int k = ty; k < 32; k += 8) {
-    const int q = q0 + k, p = p0 + tx;
-    if (p < Ppad && q < Q) dst[(long long)q * Ppad + p] = t[tx][k];
-  }
-}
-
-// 64 x 64 tiles with 16-byte loads and stores (P, Q multiples of 64): out[b][q][p] = in[b][p][q].
-__global__ void __launch_bounds__(256) transpose64_bf16_kernel(const __nv_bfloat16* __restrict__ in,
-                                                               __nv_bfloat16* __restrict__ out, int P, int Q) {
-  __shared__ __nv_bfloat16 t[64][64 + 8];
-  const long long b = blockIdx.z;
-  const int p0 = blockIdx.y * 64, q0 = blockIdx.x * 64;
-  const __nv_bfloat16* src = in + b * (long long)P * Q;
-  __nv_bfloat16* dst = out + b * (long long)P * Q;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {  // 512 vectors of 8 along q
-    const int v = threadIdx.x + 256 * i;
-    const int r = v / 8, cg = v % 8;
-    const uint4 val = *reinterpret_cast<const uint4*>(src + (long long)(p0 + r) * Q + q0 + 8 * cg);
-    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) t[r][8 * cg + k] = e[k];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {  // 512 vectors of 8 along p
-    const int v = threadIdx.x + 256 * i;
-    const int q = v / 8, pg = v % 8;
-    uint4 val;
-    __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&val);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) e[k] = t[8 * pg + k][q];
-    *reinterpret_cast<uint4*>(dst + (long long)(q0 + q) * P + p0 + 8 * pg) = val;
-  }
-}
-
 // part[s][c] = sum of in[t][c] over the tokens t of chunk s (kc tokens each, the last one
 // shorter): thread per (chunk, column).
 __global__ void __launch_bounds__(256) colsum_split_kernel(const float* __restrict__ in, float* __restrict__ part,
@@ -342,27 +269,30 @@ __global__ void __launch_bounds__(256) colsum_split_kernel(const float* __restri
   part[(long long)sidx * W + c] = acc;
 }
 
+// Rows r >= rows[e] of every expert block of up to three bfloat16 buffers [E, R, w_k] are
+// set to zero: warp per (expert, row), 16-byte stores (w_k % 8 == 0).
+__global__ void __launch_bounds__(256) zero_tail_rows_kernel(const int32_t* __restrict__ rows, int E, int R,
+                                                             __nv_bfloat16* a, int wa, __nv_bfloat16* b, int wb,
+                                                             __nv_bfloat16* c, int wc) {
+  const long long w = (long long)blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (w >= (long long)E * R) return;
+  const int e = (int)(w / R), r = (int)(w % R);
+  if (r < rows[e]) return;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  __nv_bfloat16* bufs[3] = {a, b, c};
+  const int widths[3] = {wa, wb, wc};
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    if (!bufs[k]) continue;
+    uint4* row = reinterpret_cast<uint4*>(bufs[k] + (size_t)w * widths[k]);
+    for (int v = lane; v < widths[k] / 8; v += 32) row[v] = zero;
+  }
+}
+
 __global__ void fill_i32_kernel(int32_t* __restrict__ a, int n, int v) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) a[i] = v;
-}
-
-__global__ void __launch_bounds__(256) bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* __restrict__ out,
-                                                          long long n) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-    out[i] = __bfloat162float(in[i]);
-}
-
-static int launch_transpose(const void* in, void* out, int B, int P, int Q, cudaStream_t s) {
-  if (P % 64 == 0 && Q % 64 == 0) {
-    transpose64_bf16_kernel<<<dim3((unsigned)(Q / 64), (unsigned)(P / 64), (unsigned)B), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out), P, Q);
-    return cudaGetLastError() == cudaSuccess ? 1 : -1;
-  }
-  const dim3 grid((unsigned)((Q + 31) / 32), (unsigned)((P + 31) / 32), (unsigned)B);
-  transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out),
-                                             P, Q);
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
 // ---------------------------------------------------------------- launcher
@@ -387,17 +317,24 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
   if (N > 0)
     BW_STEP(launch_k(combine_bwd_kernel<T>, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1, dy, ye,
                      a.expert, a.row, a.gate, a.dye, (__nv_bfloat16*)a.dye16, a.dg, N, d, R) == cudaSuccess ? 1 : -1);
-  const bool tc = a.W1T != nullptr;
+  const bool tc = a.tc;
   if (tc) {
-    // dh = (dye W2_e) * [h > 0] and dxe = dh W1_e are the forward's two layers with the
-    // transposed weights: W2^T [F, d] in the first, W1^T [d, F] in the second
-    BW_STEP(launch_transpose(a.W2, a.W2T, E, d, F, s));
-    BW_STEP(launch_transpose(a.W1, a.W1T, E, F, d, s));
+    // rows past each expert's count hold stale values in h, dye and dh: zero them, so the
+    // weight gradients (sums over an expert's rows) read zeros there
+    if ((long long)E * R > 0) {
+      zero_tail_rows_kernel<<<(unsigned)(((long long)E * R + 7) / 8), 256, 0, s>>>(
+          a.expert_rows, E, R, (__nv_bfloat16*)const_cast<void*>(a.h), F, (__nv_bfloat16*)a.dye16, d,
+          (__nv_bfloat16*)a.dh16, F);
+      if (cudaGetLastError() != cudaSuccess) return -1;
+      ++n;
+    }
+    // dh = (dye W2_e) * [h > 0] and dxe = dh W1_e: the forward's two layers with W2 [E, d, F]
+    // and W1 [E, F, d] read as they are stored (MN-major A operands)
     if (cudaMemsetAsync(a.counters, 0, (size_t)a.counter_words * sizeof(uint32_t), s) != cudaSuccess) return -1;
     FfnLaunch L{};
     L.xe = a.dye16;
-    L.W1 = a.W2T;
-    L.W2 = a.W1T;
+    L.W1 = a.W2;
+    L.W2 = a.W1;
     L.h = a.dh16;
     L.out = a.dxe16;
     L.expert_rows = a.expert_rows;
@@ -412,54 +349,38 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     L.F = F;
     if (R > 0) {
       BW_STEP(launch_ffn_tc(L, s, false));
-    } else {  // no expert rows: the weight gradients are zero
-      if (cudaMemsetAsync(a.dW1, 0, (size_t)E * F * d * sizeof(float), s) != cudaSuccess ||
-          cudaMemsetAsync(a.dW2, 0, (size_t)E * F * d * sizeof(float), s) != cudaSuccess)
-        return -1;
-    }
-    // dW2_e = dye^T h and dW1_e = dh^T xe: an expert's rows become the contraction axis
-    // (transposed, zero past its row count); the kernel's layer 1 with the plain sum, in
-    // bfloat16 into the (now free) transposed-weight buffers, then widened to float32
-    if (R > 0) {
-      const int Rp = a.Rpad;
-      const dim3 gF((unsigned)((F + 31) / 32), (unsigned)(Rp / 32), (unsigned)E);
-      const dim3 gd((unsigned)((d + 31) / 32), (unsigned)(Rp / 32), (unsigned)E);
-      transpose_rows_bf16_kernel<<<gF, 256, 0, s>>>((const __nv_bfloat16*)a.h, (__nv_bfloat16*)a.hT, a.expert_rows, R, F, Rp);
-      transpose_rows_bf16_kernel<<<gF, 256, 0, s>>>((const __nv_bfloat16*)a.dh16, (__nv_bfloat16*)a.dhT, a.expert_rows, R, F,
-                                                    Rp);
-      transpose_rows_bf16_kernel<<<gd, 256, 0, s>>>((const __nv_bfloat16*)a.dye16, (__nv_bfloat16*)a.dyeT, a.expert_rows, R,
-                                                    d, Rp);
-      transpose_rows_bf16_kernel<<<gd, 256, 0, s>>>((const __nv_bfloat16*)a.xe, (__nv_bfloat16*)a.xeT, a.expert_rows, R, d,
-                                                    Rp);
+      // dW2_e = dye^T h and dW1_e = dh^T xe: the contraction axis is an expert's rows, read
+      // MN-major from [E, R, .] (rows past R read as zero, past the count zeroed above);
+      // float32 results straight into dW2 [E, d, F] and dW1 [E, F, d]
       fill_i32_kernel<<<(E + 255) / 256, 256, 0, s>>>(a.rows_d, E, d);
       fill_i32_kernel<<<(E + 255) / 256, 256, 0, s>>>(a.rows_F, E, F);
       if (cudaGetLastError() != cudaSuccess) return -1;
-      n += 6;
+      n += 2;
       for (int wgt = 0; wgt < 2; ++wgt) {
-        // wgt 0: dW2[e, c, f] = sum_r dye[r, c] h[r, f]   (tokens c < d, weight rows f < F)
-        // wgt 1: dW1[e, f, c] = sum_r dh[r, f] xe[r, c]   (tokens f < F, weight rows c < d)
+        // wgt 0: dW2[e, c, f] = sum_r h[r, f] dye[r, c]  (tokens c < d, features f < F)
+        // wgt 1: dW1[e, f, c] = sum_r xe[r, c] dh[r, f]  (tokens f < F, features c < d)
         if (cudaMemsetAsync(a.counters2, 0, (size_t)a.counter2_words * sizeof(uint32_t), s) != cudaSuccess) return -1;
         FfnLaunch M{};
-        M.xe = wgt == 0 ? a.dyeT : a.dhT;
-        M.W1 = wgt == 0 ? a.hT : a.xeT;
+        M.W1 = wgt == 0 ? a.h : a.xe;        // A: features
         M.W2 = M.W1;
-        M.h = wgt == 0 ? a.W2T : a.W1T;  // output [E * tokens, weight rows] bfloat16
-        M.out = M.h;
+        M.xe = wgt == 0 ? (const void*)a.dye16 : (const void*)a.dh16;  // B: tokens
         M.expert_rows = wgt == 0 ? a.rows_d : a.rows_F;
         M.combine = false;
         M.mode = 2;
         M.counters = a.counters2;
         M.err = a.err;
         M.E = E;
-        M.R = wgt == 0 ? d : F;
-        M.d = Rp;
-        M.F = wgt == 0 ? F : d;
+        M.R = wgt == 0 ? d : F;              // tokens per expert
+        M.F = wgt == 0 ? F : d;              // features
+        M.d = a.Rpad;                        // contraction: the expert's rows, rounded up to 64
+        M.krows = R;
+        M.out_f32 = wgt == 0 ? a.dW2 : a.dW1;
         BW_STEP(launch_ffn_tc(M, s, false));
-        const long long cnt = (long long)E * d * F;
-        bf16_to_f32_kernel<<<1184, 256, 0, s>>>((const __nv_bfloat16*)M.h, wgt == 0 ? a.dW2 : a.dW1, cnt);
-        if (cudaGetLastError() != cudaSuccess) return -1;
-        ++n;
       }
+    } else {  // no expert rows: the weight gradients are zero
+      if (cudaMemsetAsync(a.dW1, 0, (size_t)E * F * d * sizeof(float), s) != cudaSuccess ||
+          cudaMemsetAsync(a.dW2, 0, (size_t)E * F * d * sizeof(float), s) != cudaSuccess)
+        return -1;
     }
   }
   // dh = (dye W2_e) * [h > 0]: i = row (<= rows_e), j = f, k = c

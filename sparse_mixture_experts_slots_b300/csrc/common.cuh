@@ -140,6 +140,15 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                                                  int z, uint64_t policy) {
   asm volatile(
@@ -240,6 +249,20 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address, 16-byte units
   d |= (uint64_t)1 << 16;                    // leading byte offset (unused when swizzled, K-major)
   d |= (uint64_t)(1024u >> 4) << 32;         // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;                    // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Shared-memory matrix descriptor: MN-major operand, 128-byte swizzle.  Each 128-byte row
+// holds 64 consecutive bf16 of M (or N) for one k; rows of consecutive k are 128 B apart in
+// 8-row swizzle atoms (1024 B, the stride between groups of 8 k); the next 64 elements of
+// M (or N) start `lbo` bytes further (a TMA box {64, k rows, chunks} lands in this order).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address, 16-byte units
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;  // leading byte offset: next 64 elements of M / N
+  d |= (uint64_t)(1024u >> 4) << 32;         // stride byte offset: next 8 k-rows
   d |= (uint64_t)1 << 46;                    // descriptor version for tcgen05
   d |= (uint64_t)2 << 61;                    // 128-byte swizzle
   return d;

@@ -65,6 +65,7 @@ struct FfnParams {
   int MB;                        // 128-row weight blocks per tile (the kernel's template value)
   int layer2;                    // 0: layer-1 tiles only (a weight gradient)
   int stall;                     // test only: tile (layer 1, expert 0, block 0, chunk 0) never publishes
+  float* out_f32;                // MODE 2: the float32 result [E * R, F] (R: tokens, F: features)
 };
 
 struct FfTile {
@@ -127,6 +128,8 @@ struct FfShared {
   int ep_acc_ok;
 };
 static_assert(offsetof(FfShared, xpose) % 16 == 0, "16-byte vector reads of the transpose buffer");
+static_assert(sizeof(FfShared::xpose) >= 8 * FF_EPW * 16 * 32 * sizeof(float) / 2,
+              "the float32 staging of one weight block's epilogue warps fits in the transpose buffer");
 
 template <int MB>
 __device__ __forceinline__ void epi_sync() {  // named barrier over the epilogue warps
@@ -144,10 +147,15 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // MB: 128-row weight blocks per tile, all reading one activation tile (compile-time, so the
 // MMA issue loop stays fully unrolled).  NBUF: TMEM accumulator sets (2: the epilogue of
 // a tile overlaps the next tile's MMAs; 1 when two sets do not fit in 512 columns).
-// MODE 0: the forward (layer 1: + bias, ReLU).  MODE 1, the backward's dh = (dye W2) *
-// [h > 0]: layer 1 keeps the sum where the saved forward activation hmask is positive.
-// MODE 2, a weight gradient (sum over an expert's rows): layer 1 stores the plain sum, and
-// no layer-2 tile is handed out (p.layer2 = 0).
+// MODE 0: the forward (layer 1: + bias, ReLU); both operands K-major.
+// MODE 1, the backward's dh = (dye W2) * [h > 0] and dxe = dh W1: the weights are read as
+// they are stored (W2 [E, d, F] as layer 1's A with K = d, W1 [E, F, d] as layer 2's with
+// K = F), i.e. MN-major A operands; layer 1 keeps the sum where the saved forward activation
+// hmask is positive.
+// MODE 2, a weight gradient (sum over an expert's rows): both operands MN-major with the
+// expert's rows as the contraction axis, read through 4-D tensor maps [E][rows][..] so rows
+// past an expert's block read as zero; layer 1 only (p.layer2 = 0), float32 results stored
+// straight to out_f32.
 template <int MB, int NBUF, int MODE>
 __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     ffn_persistent_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
@@ -241,7 +249,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       // A chunk filled to at most BN - 64 rows loads its activations as 64-row boxes, only
       // as many as cover its rows (nbox = 0: one box of BN rows)
       const int nt = (nv + 15) & ~15;
-      const int nbox = (BN > FF_PB && nt <= BN - FF_PB) ? (nt + FF_PB - 1) / FF_PB : 0;
+      const int nbox = (MODE != 2 && BN > FF_PB && nt <= BN - FF_PB) ? (nt + FF_PB - 1) / FF_PB : 0;
       const uint32_t tx = nbox ? (uint32_t)(NA * MB * FF_ATOM_A + NA * nbox * FF_PB * FF_BK * 2) : (uint32_t)p.stage_bytes;
       const int K = l1 ? p.d : p.F;
       const int M = l1 ? p.F : p.d;
@@ -256,12 +264,20 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         // atom a swizzled [rows x 128 B] block; atoms past K read as zero (never used).
         mbar_arrive_expect_tx(&sh.full[slot], tx);
         uint8_t* stage = ring + (size_t)slot * p.stage_bytes;
-        if (p.w_evict_first)
+        if (MODE == 2)  // activations, MN-major: K rows a0 .. of expert e, 2 MB chunks of 64 features
+          tma_load_4d(stage, tmA, &sh.full[slot], 0, a0 * FF_BK, tl.mt * MB * 2, tl.e);
+        else if (MODE == 1 && p.w_evict_first)  // weights as stored, MN-major: K rows of expert e
+          tma_load_3d_hint(stage, tmA, &sh.full[slot], 0, tl.e * K + a0 * FF_BK, tl.mt * MB * 2, w_policy);
+        else if (MODE == 1)
+          tma_load_3d(stage, tmA, &sh.full[slot], 0, tl.e * K + a0 * FF_BK, tl.mt * MB * 2);
+        else if (p.w_evict_first)
           tma_load_3d_hint(stage, tmA, &sh.full[slot], 0, arow, a0, w_policy);
         else
           tma_load_3d(stage, tmA, &sh.full[slot], 0, arow, a0);
         uint8_t* sb = stage + NA * MB * FF_ATOM_A;
-        if (nbox == 0) {
+        if (MODE == 2) {  // expert rows as K, BN / 64 chunks of 64 output rows (past the end: zeros)
+          tma_load_4d(sb, tmB, &sh.full[slot], 0, a0 * FF_BK, tl.nc * (BN / 64), tl.e);
+        } else if (nbox == 0) {
           tma_load_3d(sb, tmB, &sh.full[slot], 0, brow, a0);
         } else {
           for (int at = 0; at < NA; ++at)  // atom at keeps its [BN x 128 B] place in the stage
@@ -293,8 +309,10 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       }
       const int4 tv = sh.sched[qs];
       if (tv.x < 0) break;
-      // N = the chunk's filled rows rounded up to 16: MMA time and operand reads scale with N
-      const uint32_t idesc = idesc_bf16_f32(FF_BM, (sh.sched_nv[qs] + 15) & ~15);
+      // N = the chunk's filled rows rounded up to 16: MMA time and operand reads scale with N.
+      // Bits 15 / 16: A / B read MN-major.
+      const uint32_t idesc = idesc_bf16_f32(FF_BM, MODE == 2 ? BN : (sh.sched_nv[qs] + 15) & ~15) |
+                             (MODE >= 1 ? (1u << 15) : 0u) | (MODE == 2 ? (1u << 16) : 0u);
       const int buf = lt % NBUF;
       if (lt >= NBUF && !mbar_wait(&sh.aempty[buf], ((lt / NBUF) - 1) & 1)) {
         raise_error(p.err, ERR_TIMEOUT);
@@ -313,8 +331,11 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         // offset (16-byte units) to the start-address field, which cannot carry out of its
         // 14 bits inside the 227 KB shared window.
         const uint32_t st = smem_u32(ring + (size_t)slot * p.stage_bytes);
-        const uint64_t da = sw128_kmajor_desc(st);
-        const uint64_t db = sw128_kmajor_desc(st + NA * MB * FF_ATOM_A);
+        // MN-major boxes hold 64 * NA k-rows per 64-element chunk: chunk stride (LBO) in bytes
+        const uint32_t mn_lbo = (uint32_t)(NA * FF_BK * 128);
+        const uint64_t da = MODE == 0 ? sw128_kmajor_desc(st) : sw128_mnmajor_desc(st, mn_lbo);
+        const uint64_t db = MODE == 2 ? sw128_mnmajor_desc(st + NA * MB * FF_ATOM_A, mn_lbo)
+                                      : sw128_kmajor_desc(st + NA * MB * FF_ATOM_A);
         const uint32_t b_atom16 = (uint32_t)(BN * FF_BK * 2) >> 4;
 #pragma unroll
         for (int at = 0; at < 2; ++at) {
@@ -322,11 +343,15 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
 #pragma unroll
           for (int kk = 0; kk < FF_BK / 16; ++kk)
 #pragma unroll
-            for (int hb = 0; hb < MB; ++hb)  // weight block hb: rows 128 hb .. of the atom
-              tc_mma_bf16(acc + (uint32_t)(hb * BN),
-                          da + (uint64_t)(((at * MB + hb) * FF_ATOM_A + kk * 32) >> 4),
-                          db + (uint64_t)(at * b_atom16 + ((kk * 32) >> 4)), idesc,
+            for (int hb = 0; hb < MB; ++hb) {  // weight block hb: rows 128 hb .. of the atom
+              // A: K-major atoms of 128 rows; MN-major: chunks 2 hb, 2 hb + 1, k-row 64 at + 16 kk
+              const uint32_t aoff = MODE == 0 ? (uint32_t)((at * MB + hb) * FF_ATOM_A + kk * 32)
+                                              : (uint32_t)(2 * hb) * mn_lbo + (uint32_t)((at * FF_BK + kk * 16) * 128);
+              const uint32_t boff16 = MODE == 2 ? (uint32_t)(((at * FF_BK + kk * 16) * 128) >> 4)
+                                                : at * b_atom16 + (uint32_t)((kk * 32) >> 4);
+              tc_mma_bf16(acc + (uint32_t)(hb * BN), da + (uint64_t)(aoff >> 4), db + (uint64_t)boff16, idesc,
                           (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
+            }
         }
         tc_commit(&sh.empty[slot]);
         ++gst;
@@ -398,8 +423,40 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       tc_fence_after();
       // The two warps of a quadrant take alternate 32-column slices; both TMEM loads of a
       // slice are in flight before one wait.
+      if (MODE == 2) {
+        // float32 results, token-major.  Each 16-column chunk goes through shared memory as
+        // [16 tokens][32 features] (lane = feature); lane L then stores features 4 (L % 8) ..
+        // + 3 of tokens L / 8 + 4 i, i < 4, as 16-byte vectors (8 lanes per 128-byte row).
+        float* xf = reinterpret_cast<float*>(&sh.xpose[0][0][0]) + (warp - 2) * (16 * 32);
+        const int mb0 = (mt * MB + hb) * FF_BM + quad * 32;  // first feature of this warp
 #pragma unroll 1
-      for (int c0 = 32 * part; c0 < nv; c0 += 64) {
+        for (int c0 = 32 * part; c0 < nv; c0 += 64) {
+          uint32_t r[2][16];
+          const int nch = min(2, (nv - c0 + 15) / 16);
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            if (q < nch) tmem_ld16(taddr + (uint32_t)(c0 + 16 * q), r[q]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            if (q >= nch) break;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xf[j * 32 + lane] = __uint_as_float(r[q][j]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int j = (lane >> 3) + 4 * i;
+              const int col = c0 + 16 * q + j;
+              const float4 v = *reinterpret_cast<const float4*>(xf + j * 32 + 4 * (lane & 7));
+              if (col < nv)
+                *reinterpret_cast<float4*>(p.out_f32 + ((size_t)e * p.R + n0 + col) * p.F + mb0 + 4 * (lane & 7)) = v;
+            }
+            __syncwarp();  // the chunk's reads of xf are done before the next chunk writes it
+          }
+        }
+      }
+#pragma unroll 1
+      for (int c0 = 32 * part; MODE != 2 && c0 < nv; c0 += 64) {
         uint32_t r[2][16];
         const int nch = min(2, (nv - c0 + 15) / 16);
 #pragma unroll
@@ -565,6 +622,22 @@ bool encode_bf16_3d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D view [E][rows][cols / 64 chunks][64] of a bf16 buffer [E, rows, cols] (cols % 64 == 0):
+// a box {64, box_rows, box_chunks, 1} at (0, r, c, e) holds rows r .. of expert e only (rows
+// past `rows` read as zero), chunk by chunk: the MN-major layout with the rows as K.
+bool encode_bf16_4d(CUtensorMap* map, const void* base, uint64_t E, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t box_chunks) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn || cols % FF_BK != 0) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)FF_BK, rows, cols / FF_BK, E};
+  cuuint64_t strides[3] = {cols * 2, (cuuint64_t)FF_BK * 2, rows * cols * 2};
+  cuuint32_t box[4] = {(cuuint32_t)FF_BK, box_rows, box_chunks, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_shape_ok(int M, int K) { return M > 0 && K > 0 && M % FF_BM == 0 && K % FF_BK == 0; }
 
 FfnTiling ffn_tiling(int R, int d, int F) {
@@ -604,16 +677,34 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   }
   if (t.STAGES < 2 || t.BN > 256) return -1;
   CUtensorMap tmW1, tmX, tmW2, tmH, tmXp, tmHp;
-  if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
-  if (!encode_bf16_3d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
+  if (L.mode == 0) {  // K-major weights [E, M, K]
+    if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
+  } else if (L.mode == 1) {  // weights as stored [E, K, M], MN-major: boxes of 64 NA k-rows x 2 MB chunks
+    if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.d, (uint64_t)L.F, (uint32_t)(FF_BK * t.NA), 2u * t.MB))
+      return -1;
+  } else {  // activations [E, krows, F] with the rows as K, MN-major
+    if (L.krows <= 0 || !encode_bf16_4d(&tmW1, L.W1, (uint64_t)L.E, (uint64_t)L.krows, (uint64_t)L.F, FF_BK, 2u * t.MB))
+      return -1;
+  }
+  if (L.mode == 2) {  // tokens [E, krows, R]: the rows as K, BN / 64 chunks of 64 tokens
+    if (!encode_bf16_4d(&tmX, L.xe, (uint64_t)L.E, (uint64_t)L.krows, (uint64_t)L.R, FF_BK, (uint32_t)(t.BN / 64)))
+      return -1;
+  } else if (!encode_bf16_3d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)t.BN, (uint32_t)t.NA)) {
+    return -1;
+  }
   if (L.mode == 2) {  // no layer 2: its maps are never read
     tmW2 = tmW1;
     tmH = tmX;
   } else {
-    if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
+    if (L.mode == 1) {
+      if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.F, (uint64_t)L.d, (uint32_t)(FF_BK * t.NA), 2u * t.MB))
+        return -1;
+    } else if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM * t.MB, (uint32_t)t.NA)) {
+      return -1;
+    }
     if (!encode_bf16_3d(&tmH, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
   }
-  if (t.BN > FF_PB) {  // one atom per box: the boxes of a partly filled chunk
+  if (L.mode != 2 && t.BN > FF_PB) {  // one atom per box: the boxes of a partly filled chunk
     if (!encode_bf16_3d(&tmXp, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)FF_PB, 1u)) return -1;
     if (L.mode == 2)
       tmHp = tmXp;
@@ -658,6 +749,8 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.hmask = (const __nv_bfloat16*)L.hmask;
   p.layer2 = L.mode == 2 ? 0 : 1;
   p.stall = L.stall ? 1 : 0;
+  p.out_f32 = L.out_f32;
+  if (L.mode == 2 && (!L.out_f32 || t.BN % 64 != 0)) return -1;
   p.w_evict_first = t.NCH == 1 ? 1 : 0;  // several chunks re-read a weight tile
   const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
   const long long tiles = (long long)L.E * t.NCH * (L.F / (FF_BM * t.MB) + l2_blocks);

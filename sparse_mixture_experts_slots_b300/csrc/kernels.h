@@ -104,14 +104,13 @@ struct BackwardArgs {
   float* dx; float* dWr; float* dbr; float* dW1; float* db1; float* dW2; float* db2;
   // workspace
   float* dye; float* dh; float* dxe; float* dg; float* dz;
-  // tensor-core path (bf16, tc_shape_ok): dh and dxe by the persistent FFN kernel (mask
-  // epilogue) on transposed weights; null otherwise
-  void* W1T; void* W2T;               // [E, d, F], [E, F, d] bf16
+  // tensor-core path (bf16, tc_shape_ok): the four expert products on the persistent FFN
+  // kernel, reading the weights and the saved activations in place (MN-major operands)
+  bool tc;
   void* dye16; void* dh16; void* dxe16;  // [E, R, d], [E, R, F], [E, R, d] bf16
   uint32_t* counters; int counter_words; uint32_t* err;
   // weight gradients on the same kernel (mode 2): expert rows as the contraction axis
   int Rpad;                                   // R rounded up to 64
-  void* hT; void* dhT; void* dyeT; void* xeT;   // [E, F, Rpad], [E, F, Rpad], [E, d, Rpad], [E, d, Rpad]
   int32_t* rows_d; int32_t* rows_F;            // [E] filled with d, F
   uint32_t* counters2; int counter2_words;      // 1 + E * ceil(max(d, F) / 256)
   // split sums over tokens (dWr, dbr): partial products / sums, nsplit of them
@@ -201,8 +200,12 @@ struct FfnLaunch {
   const float* gate;         // [N] (combine)
   const void* resid;         // [N, d] or null (combine)
   const void* hmask;         // [E * R, F] (mode 1): layer 1 keeps its sum where hmask > 0
-  int mode;                  // 0 forward; 1 backward dh (mask, no bias/ReLU); 2 weight gradient
-                             // (layer 1 only, plain sum; d = the padded row count)
+  int mode;                  // 0 forward; 1 backward dh -> dxe (W1 = W2 [E, d, F] and W2 = W1 [E, F, d]
+                             // as stored, mask, no bias/ReLU); 2 weight gradient (layer 1 only,
+                             // plain sum: W1 = activations [E, krows, F], xe = [E, krows, R],
+                             // d = krows rounded up to 64, float32 result in out_f32 [E * R, F])
+  int krows;                 // mode 2: rows per expert of W1 / xe (the contraction axis)
+  float* out_f32;            // mode 2 output
   uint32_t* counters;        // ffn_counter_words(E, R) words, zero at launch
   uint32_t* err;
   int E, R, d, F;
