@@ -56,8 +56,12 @@ struct switch_layer {
   float* bw_dxe;  // [E, R, d]
   float* bw_dg;   // [N]
   float* bw_dz;   // [N, E]
-  float* bw_part; // [nsplit, E, d]: per-token-chunk partial sums of dWr and dbr
+  float* bw_part; // [nsplit, E, d]: per-token-chunk partial sums of dWr and dbr (or [ntc, 2E, d])
   int bw_nsplit;
+  int bw_ntc, bw_kc;          // tensor-core router products: token chunks and their rows (ntc 0: off)
+  void* bw_dzp;               // [N, 3E] bf16
+  void* bw_Wp;                // [3E, d] bf16
+  int32_t* bw_rows_k;         // [ntc + 1]
   // tensor-core backward (bf16 with tensor-core FFN shapes): bf16 copies of the gradients
   bool bw_tc;
   void* bw_dye16; // [E, R, d]
@@ -200,24 +204,45 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const size_t o_xe = take(E * R * d * h->es);
   const size_t o_h = take(E * R * F * h->es);
   const size_t o_ye = take(E * R * d * h->es);
+  const bool train_tc = train && cfg->dtype == SWITCH_BF16 && tc_shape_ok((int)F, (int)d) && tc_shape_ok((int)d, (int)F);
   const size_t o_bdye = take(train ? E * R * d * sizeof(float) : 0);
-  const size_t o_bdh = take(train ? E * R * F * sizeof(float) : 0);
-  const size_t o_bdxe = take(train ? E * R * d * sizeof(float) : 0);
+  const size_t o_bdh = take(train && !train_tc ? E * R * F * sizeof(float) : 0);   // CUDA-core path only
+  const size_t o_bdxe = take(train && !train_tc ? E * R * d * sizeof(float) : 0);
   const size_t o_bdg = take(train ? N * sizeof(float) : 0);
   const size_t o_bdz = take(train ? N * E * sizeof(float) : 0);
   // token chunks of the router's weight-gradient sums: ~256 tokens each, the partials
   // [nsplit, E, d] kept under 64 M floats
+  const size_t part_cap = (size_t)64 << 20;
   size_t nsplit = N > 0 ? (N + 255) / 256 : 1;
-  const size_t cap = std::max<size_t>(1, ((size_t)64 << 20) / std::max<size_t>(1, E * d));
+  const size_t cap = std::max<size_t>(1, part_cap / std::max<size_t>(1, E * d));
   if (nsplit > cap) nsplit = cap;
-  const size_t o_bpart = take(train ? nsplit * E * d * sizeof(float) : 0);
-  const bool train_tc = train && cfg->dtype == SWITCH_BF16 && tc_shape_ok((int)F, (int)d) && tc_shape_ok((int)d, (int)F);
+  // tensor-core router products: E % 64 == 0 and kc-row token chunks (kc a multiple of 64
+  // dividing N) with at most 64 chunks and partials [ntc, 2E, d] under the same cap
+  size_t kc = 0, ntc = 0;
+  if (train_tc && E % 64 == 0 && N > 0) {
+    const size_t cands[] = {256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072, 128, 64};
+    for (size_t k : cands) {
+      if (k > N || N % k != 0) continue;
+      const size_t ns = N / k;
+      if (ns <= 64 && ns * 2 * E * d <= part_cap) {
+        kc = k;
+        ntc = ns;
+        break;
+      }
+    }
+  }
+  const size_t part_floats = std::max(nsplit * E * d, ntc * 2 * E * d);
+  const size_t o_bpart = take(train ? part_floats * sizeof(float) : 0);
+  const size_t o_dzp = take(ntc ? N * 3 * E * 2 : 0);
+  const size_t o_wp = take(ntc ? 3 * E * d * 2 : 0);
+  const size_t o_rowsk = take(ntc ? (ntc + 1) * sizeof(int32_t) : 0);
   const size_t o_dye16 = take(train_tc ? E * R * d * 2 : 0);
   const size_t o_dh16 = take(train_tc ? E * R * F * 2 : 0);
   const size_t o_dxe16 = take(train_tc ? E * R * d * 2 : 0);
   const size_t Rpad = (R + 63) / 64 * 64;
   const size_t o_rows2 = take(train_tc ? 2 * E * sizeof(int32_t) : 0);
-  const size_t cw2 = 1 + E * ((std::max(d, F) + 255) / 256);
+  const size_t cw2 = std::max(1 + E * ((std::max(d, F) + 255) / 256),
+                              std::max(1 + ntc * ((2 * E + 255) / 256), 1 + (N + 255) / 256));
   const size_t o_cnt2 = take(train_tc ? cw2 * sizeof(uint32_t) : 0);
   h->ws_bytes = off;
   if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
@@ -250,6 +275,11 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->bw_dz = reinterpret_cast<float*>(h->ws + o_bdz);
   h->bw_part = reinterpret_cast<float*>(h->ws + o_bpart);
   h->bw_nsplit = (int)nsplit;
+  h->bw_ntc = (int)ntc;
+  h->bw_kc = (int)kc;
+  h->bw_dzp = ntc ? h->ws + o_dzp : nullptr;
+  h->bw_Wp = ntc ? h->ws + o_wp : nullptr;
+  h->bw_rows_k = ntc ? reinterpret_cast<int32_t*>(h->ws + o_rowsk) : nullptr;
   h->bw_tc = train_tc;
   h->bw_dye16 = train_tc ? h->ws + o_dye16 : nullptr;
   h->bw_dh16 = train_tc ? h->ws + o_dh16 : nullptr;
@@ -683,6 +713,11 @@ switch_status switch_backward(switch_handle h, const void* x, const float* Wr, c
   a.counter2_words = h->bw_counter_words;
   a.part = h->bw_part;
   a.nsplit = h->bw_nsplit;
+  a.ntc = h->bw_ntc;
+  a.kc = h->bw_kc;
+  a.dzp = h->bw_dzp;
+  a.Wp = h->bw_Wp;
+  a.rows_k = h->bw_rows_k;
   h->last_launches = 0;
   return launched(launch_backward(a, (cudaStream_t)stream), h);
 }

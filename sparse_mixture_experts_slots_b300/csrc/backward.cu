@@ -196,10 +196,12 @@ __global__ void __launch_bounds__(256) colsum_rows_kernel(const TI* __restrict__
 // ---------------------------------------------------------------- router backward
 // Warp per token: p from the logits, dp = onehot(e*) dg + w_aux alpha E f / (G T), the
 // softmax Jacobian, plus the z-loss term; writes dz [N, E].
+// dzp (or null): dz also as bfloat16 pieces [N, 3E] = [hi | lo | hi] (hi = bf16(dz), lo =
+// bf16(dz - hi)) for the tensor-core products dWr and dx.
 __global__ void __launch_bounds__(256) router_bwd_kernel(const float* __restrict__ z, const int32_t* __restrict__ expert,
                                                          const float* __restrict__ dg, const int32_t* __restrict__ raw,
-                                                         float* __restrict__ dz, long long N, int T, int E, int G,
-                                                         float aux_coef, float z_coef) {
+                                                         float* __restrict__ dz, __nv_bfloat16* __restrict__ dzp,
+                                                         long long N, int T, int E, int G, float aux_coef, float z_coef) {
   griddep_wait();
   griddep_launch_dependents();
   const long long t = (long long)blockIdx.x * 8 + threadIdx.x / 32;
@@ -229,7 +231,29 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float* __restrict
   for (int e = lane; e < E; e += 32) {
     const float p = expf(zr[e] - m) / s;
     const float dp = (e == a ? dgt : 0.f) + aux_coef * (float)rg[e];
-    dz[t * E + e] = p * (dp - pdp) + z_coef * lse * p;
+    const float v = p * (dp - pdp) + z_coef * lse * p;
+    dz[t * E + e] = v;
+    if (dzp) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      __nv_bfloat16* row = dzp + t * 3 * E;
+      row[e] = hi;
+      row[E + e] = lo;
+      row[2 * E + e] = hi;
+    }
+  }
+}
+
+// W_r [E, d] float32 -> Wp [3E, d] bfloat16 = [hi; hi; lo]: with dzp's [hi | lo | hi] the
+// product over 3E sums dz_hi W_hi + dz_lo W_hi + dz_hi W_lo (dx = dz W_r to ~2^-16).
+__global__ void __launch_bounds__(256) split_wr3_kernel(const float* __restrict__ Wr, __nv_bfloat16* __restrict__ Wp,
+                                                        long long n /* E * d */) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const float w = Wr[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    Wp[i] = hi;
+    Wp[n + i] = hi;
+    Wp[2 * n + i] = __float2bfloat16_rn(w - __bfloat162float(hi));
   }
 }
 
@@ -440,13 +464,61 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
   if (N > 0) {
     const float aux_coef = a.w_aux * a.alpha * (float)E / ((float)a.G * (float)a.T * (float)a.T);  // f = raw / T
     const float z_coef = a.w_z * 2.f / ((float)a.G * (float)a.T);
+    const bool tc_router = tc && a.ntc > 0;
     BW_STEP(launch_k(router_bwd_kernel, dim3((unsigned)((N + 7) / 8)), dim3(256), 0, s, false, 1, a.logits, a.expert,
-                     (const float*)a.dg, a.raw, a.dz, N, a.T, E, a.G, aux_coef, z_coef) == cudaSuccess ? 1 : -1);
-    // dWr = dz^T x (i = e, j = c, k = t) and dbr = sum_t dz_t, split over nsplit token chunks:
-    // partial results per chunk, then their sum in chunk order
-    const int ns = a.nsplit;
-    const int kc = (int)((N + ns - 1) / ns);
-    {
+                     (const float*)a.dg, a.raw, a.dz, tc_router ? (__nv_bfloat16*)a.dzp : (__nv_bfloat16*)nullptr, N, a.T, E, a.G,
+                     aux_coef, z_coef) == cudaSuccess ? 1 : -1);
+    if (tc_router) {
+      // dWr = dz^T x on the tensor cores: token chunks of kc rows as the contraction axis,
+      // dz as [hi | lo] pieces (2E output rows per chunk, x exact in bfloat16), float32
+      // partials [ntc, 2E, d] summed in chunk and piece order
+      split_wr3_kernel<<<592, 256, 0, s>>>(a.Wr, (__nv_bfloat16*)a.Wp, (long long)E * d);
+      fill_i32_kernel<<<(a.ntc + 255) / 256, 256, 0, s>>>(a.rows_k, a.ntc, 2 * E);
+      fill_i32_kernel<<<1, 32, 0, s>>>(a.rows_k + a.ntc, 1, (int)N);
+      if (cudaGetLastError() != cudaSuccess) return -1;
+      n += 3;
+      if (cudaMemsetAsync(a.counters2, 0, (size_t)a.counter2_words * sizeof(uint32_t), s) != cudaSuccess) return -1;
+      FfnLaunch M{};
+      M.W1 = a.x;   // A: features c < d, rows = the chunk's tokens
+      M.W2 = M.W1;
+      M.xe = a.dzp; // B: the first 2E of 3E columns, rows = the chunk's tokens
+      M.expert_rows = a.rows_k;
+      M.mode = 2;
+      M.counters = a.counters2;
+      M.err = a.err;
+      M.E = a.ntc;
+      M.R = 2 * E;
+      M.bcols = 3 * E;
+      M.F = d;
+      M.d = a.kc;
+      M.krows = a.kc;
+      M.out_f32 = a.part;
+      BW_STEP(launch_ffn_tc(M, s, false));
+      BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)(((long long)E * d + 255) / 256)), dim3(256), 0, s,
+                       false, 1, (const float*)a.part, (const int32_t*)nullptr, a.dWr, 1, 2 * a.ntc, E * d) ==
+                      cudaSuccess ? 1 : -1);
+      // dx = dz W_r: the product over 3E of dzp [N, 3E] (K-major rows) and Wp [3E, d] (as
+      // stored, MN-major), float32 results straight into dx
+      if (cudaMemsetAsync(a.counters2, 0, (size_t)a.counter2_words * sizeof(uint32_t), s) != cudaSuccess) return -1;
+      FfnLaunch X{};
+      X.W1 = a.Wp;
+      X.W2 = X.W1;
+      X.xe = a.dzp;
+      X.expert_rows = a.rows_k + a.ntc;
+      X.mode = 3;
+      X.counters = a.counters2;
+      X.err = a.err;
+      X.E = 1;
+      X.R = (int)N;
+      X.d = 3 * E;
+      X.F = d;
+      X.out_f32 = a.dx;
+      BW_STEP(launch_ffn_tc(X, s, false));
+    } else {
+      // dWr = dz^T x (i = e, j = c, k = t), split over nsplit token chunks: partial results
+      // per chunk, then their sum in chunk order
+      const int ns = a.nsplit;
+      const int kc = (int)((N + ns - 1) / ns);
       BgemmArgs g{};
       g.M = E; g.N = d; g.K = kc; g.Ktot = N;
       g.sAb = (long long)kc * E; g.sAi = 1; g.sAk = E;
@@ -457,15 +529,16 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
                        false, 1, (const float*)a.part, (const int32_t*)nullptr, a.dWr, 1, ns, E * d) == cudaSuccess
                   ? 1 : -1);
     }
-    if (a.dbr) {
+    if (a.dbr) {  // dbr = sum_t dz_t, split over token chunks, then the chunks' sum in order
+      const int ns = a.nsplit;
+      const int kc = (int)((N + ns - 1) / ns);
       colsum_split_kernel<<<dim3((unsigned)((E + 255) / 256), (unsigned)ns), 256, 0, s>>>(a.dz, a.part, N, E, kc);
       if (cudaGetLastError() != cudaSuccess) return -1;
       ++n;
       BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)((E + 255) / 256)), dim3(256), 0, s, false, 1,
                        (const float*)a.part, (const int32_t*)nullptr, a.dbr, 1, ns, E) == cudaSuccess ? 1 : -1);
     }
-    // dx = dz Wr: i = t, j = c, k = e
-    {
+    if (!tc_router) {  // dx = dz Wr: i = t, j = c, k = e
       BgemmArgs g{};
       g.M = (int)N; g.N = d; g.K = E;
       g.sAi = E; g.sAk = 1;

@@ -156,6 +156,9 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // expert's rows as the contraction axis, read through 4-D tensor maps [E][rows][..] so rows
 // past an expert's block read as zero; layer 1 only (p.layer2 = 0), float32 results stored
 // straight to out_f32.
+// MODE 3, a plain product out[n, m] = sum_k A[k, m] B[n, k]: A MN-major as stored (3-D map,
+// like MODE 1's weights), B K-major rows (like the forward's tokens); layer 1 only, float32
+// results as in MODE 2.
 template <int MB, int NBUF, int MODE>
 __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     ffn_persistent_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
@@ -266,9 +269,9 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         uint8_t* stage = ring + (size_t)slot * p.stage_bytes;
         if (MODE == 2)  // activations, MN-major: K rows a0 .. of expert e, 2 MB chunks of 64 features
           tma_load_4d(stage, tmA, &sh.full[slot], 0, a0 * FF_BK, tl.mt * MB * 2, tl.e);
-        else if (MODE == 1 && p.w_evict_first)  // weights as stored, MN-major: K rows of expert e
+        else if ((MODE == 1 || MODE == 3) && p.w_evict_first)  // as stored, MN-major: K rows of expert e
           tma_load_3d_hint(stage, tmA, &sh.full[slot], 0, tl.e * K + a0 * FF_BK, tl.mt * MB * 2, w_policy);
-        else if (MODE == 1)
+        else if (MODE == 1 || MODE == 3)
           tma_load_3d(stage, tmA, &sh.full[slot], 0, tl.e * K + a0 * FF_BK, tl.mt * MB * 2);
         else if (p.w_evict_first)
           tma_load_3d_hint(stage, tmA, &sh.full[slot], 0, arow, a0, w_policy);
@@ -423,7 +426,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       tc_fence_after();
       // The two warps of a quadrant take alternate 32-column slices; both TMEM loads of a
       // slice are in flight before one wait.
-      if (MODE == 2) {
+      if (MODE >= 2) {
         // float32 results, token-major.  Each 16-column chunk goes through shared memory as
         // [16 tokens][32 features] (lane = feature); lane L then stores features 4 (L % 8) ..
         // + 3 of tokens L / 8 + 4 i, i < 4, as 16-byte vectors (8 lanes per 128-byte row).
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         }
       }
 #pragma unroll 1
-      for (int c0 = 32 * part; MODE != 2 && c0 < nv; c0 += 64) {
+      for (int c0 = 32 * part; MODE < 2 && c0 < nv; c0 += 64) {
         uint32_t r[2][16];
         const int nch = min(2, (nv - c0 + 15) / 16);
 #pragma unroll
@@ -479,18 +482,9 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float v0 = __uint_as_float(r[q][2 * i]) + bv, v1 = __uint_as_float(r[q][2 * i + 1]) + bv;
-            if (l1) {
-              if (MODE == 1) {  // tokens cb + 2i, + 1 of the chunk (rows past nv are not read)
-                const int j0 = cb + 2 * i;
-                const size_t mr = (size_t)e * p.R + n0 + j0;
-                const float k0 = j0 < nv ? __bfloat162float(p.hmask[mr * p.F + m]) : 0.f;
-                const float k1 = j0 + 1 < nv ? __bfloat162float(p.hmask[(mr + 1) * p.F + m]) : 0.f;
-                v0 = k0 > 0.f ? v0 : 0.f;
-                v1 = k1 > 0.f ? v1 : 0.f;
-              } else if (MODE == 0) {
-                v0 = fmaxf(v0, 0.f);
-                v1 = fmaxf(v1, 0.f);
-              }
+            if (l1 && MODE == 0) {
+              v0 = fmaxf(v0, 0.f);
+              v1 = fmaxf(v1, 0.f);
             }
             const __nv_bfloat162 pr = __floats2bfloat162_rn(v0, v1);  // h, or ye rounded to bf16
             xw[i * 32 + lane] = *reinterpret_cast<const uint32_t*>(&pr);
@@ -508,8 +502,22 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
           for (int t2 = 0; t2 < 2; ++t2) {
             const int j = 2 * ip + t2;
             if (cb + j < nv) {
-              const uint4 val = tv2[t2];
+              uint4 val = tv2[t2];
               const size_t row = (size_t)e * p.R + n0 + cb + j;
+              if (MODE == 1 && l1) {
+                // dh keeps its value where the saved forward activation h is > 0: the same 8
+                // features of h as one 16-byte load, each bf16 kept when its sign is clear and it
+                // is not zero
+                const uint4 hm = __ldg(reinterpret_cast<const uint4*>(p.hmask + row * p.F + mb + f8));
+                const uint32_t hw[4] = {hm.x, hm.y, hm.z, hm.w};
+                uint32_t* vw = reinterpret_cast<uint32_t*>(&val);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint32_t lo_keep = ((hw[k] & 0x8000u) == 0u && (hw[k] & 0x7fffu) != 0u) ? 0x0000ffffu : 0u;
+                  const uint32_t hi_keep = ((hw[k] & 0x80000000u) == 0u && (hw[k] & 0x7fff0000u) != 0u) ? 0xffff0000u : 0u;
+                  vw[k] &= lo_keep | hi_keep;
+                }
+              }
               if (l1) {
                 *reinterpret_cast<uint4*>(p.h + row * p.F + mb + f8) = val;
               } else if (!p.combine) {
@@ -667,9 +675,17 @@ size_t ffn_counter_words(int E, int R, int d, int F) { return 1 + (size_t)E * ff
 
 int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   if (L.E == 0 || L.R == 0) return 0;
-  if (!tc_shape_ok(L.F, L.d) || (L.mode != 2 && !tc_shape_ok(L.d, L.F))) return -1;
+  if (!tc_shape_ok(L.F, L.d) || (L.mode < 2 && !tc_shape_ok(L.d, L.F))) return -1;
   if (L.mode == 1 && !L.hmask) return -1;
   FfnTiling t = ffn_tiling(L.R, L.d, L.F);
+  if (L.mode >= 2 && t.MB == 2) {  // one weight block per tile (one compiled variant each)
+    t.MB = 1;
+    t.NBUF = 2;
+    const int stage_atom = FF_ATOM_A + t.BN * FF_BK * 2;
+    t.NA = stage_atom <= 48 * 1024 ? 2 : 1;
+    t.stage_bytes = t.NA * stage_atom;
+    t.STAGES = FF_RING / t.stage_bytes < FF_MAX_STAGES ? FF_RING / t.stage_bytes : FF_MAX_STAGES;
+  }
   if (L.mode == 2 && t.NA == 2) {  // the contraction is one 64-column atom: one atom per box
     t.NA = 1;
     t.stage_bytes = t.MB * FF_ATOM_A + t.BN * FF_BK * 2;
@@ -679,20 +695,22 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   CUtensorMap tmW1, tmX, tmW2, tmH, tmXp, tmHp;
   if (L.mode == 0) {  // K-major weights [E, M, K]
     if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
-  } else if (L.mode == 1) {  // weights as stored [E, K, M], MN-major: boxes of 64 NA k-rows x 2 MB chunks
+  } else if (L.mode == 1 || L.mode == 3) {  // as stored [E, K, M], MN-major: boxes of 64 NA k-rows x 2 MB chunks
     if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.d, (uint64_t)L.F, (uint32_t)(FF_BK * t.NA), 2u * t.MB))
       return -1;
   } else {  // activations [E, krows, F] with the rows as K, MN-major
     if (L.krows <= 0 || !encode_bf16_4d(&tmW1, L.W1, (uint64_t)L.E, (uint64_t)L.krows, (uint64_t)L.F, FF_BK, 2u * t.MB))
       return -1;
   }
-  if (L.mode == 2) {  // tokens [E, krows, R]: the rows as K, BN / 64 chunks of 64 tokens
-    if (!encode_bf16_4d(&tmX, L.xe, (uint64_t)L.E, (uint64_t)L.krows, (uint64_t)L.R, FF_BK, (uint32_t)(t.BN / 64)))
+  if (L.mode == 2) {  // tokens [E, krows, bcols]: the rows as K, BN / 64 chunks of 64 tokens
+    const uint64_t bcols = L.bcols > 0 ? (uint64_t)L.bcols : (uint64_t)L.R;
+    if (bcols < (uint64_t)L.R || !encode_bf16_4d(&tmX, L.xe, (uint64_t)L.E, (uint64_t)L.krows, bcols, FF_BK,
+                                                 (uint32_t)(t.BN / 64)))
       return -1;
   } else if (!encode_bf16_3d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)t.BN, (uint32_t)t.NA)) {
     return -1;
   }
-  if (L.mode == 2) {  // no layer 2: its maps are never read
+  if (L.mode >= 2) {  // no layer 2: its maps are never read
     tmW2 = tmW1;
     tmH = tmX;
   } else {
@@ -706,7 +724,7 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   }
   if (L.mode != 2 && t.BN > FF_PB) {  // one atom per box: the boxes of a partly filled chunk
     if (!encode_bf16_3d(&tmXp, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)FF_PB, 1u)) return -1;
-    if (L.mode == 2)
+    if (L.mode == 3)
       tmHp = tmXp;
     else if (!encode_bf16_3d(&tmHp, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)FF_PB, 1u))
       return -1;
@@ -736,7 +754,7 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   // Layer-2 tiles of an expert are handed out LOOK experts after its layer-1 tiles: a
   // lead of about 8 tiles per CTA, so a layer-1 tile (up to ~3 tiles of queue latency
   // behind a CTA's earlier tiles) is normally stored before anyone needs it.
-  const int l2_blocks = L.mode == 2 ? 0 : L.d / (FF_BM * t.MB);
+  const int l2_blocks = L.mode >= 2 ? 0 : L.d / (FF_BM * t.MB);
   const int per_expert = t.NCH * (L.F / (FF_BM * t.MB) + l2_blocks);
   const int ctas_max = device_sm_count();
   p.LOOK = (8 * ctas_max + per_expert - 1) / per_expert;
@@ -747,10 +765,11 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.stage_bytes = t.stage_bytes;
   p.combine = L.combine ? 1 : 0;
   p.hmask = (const __nv_bfloat16*)L.hmask;
-  p.layer2 = L.mode == 2 ? 0 : 1;
+  p.layer2 = L.mode >= 2 ? 0 : 1;
   p.stall = L.stall ? 1 : 0;
   p.out_f32 = L.out_f32;
-  if (L.mode == 2 && (!L.out_f32 || t.BN % 64 != 0)) return -1;
+  if (L.mode >= 2 && !L.out_f32) return -1;
+  if (L.mode == 2 && t.BN % 64 != 0) return -1;
   p.w_evict_first = t.NCH == 1 ? 1 : 0;  // several chunks re-read a weight tile
   const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
   const long long tiles = (long long)L.E * t.NCH * (L.F / (FF_BM * t.MB) + l2_blocks);
@@ -769,6 +788,9 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   if (L.mode == 2) {  // d < 128: one weight block per tile, two accumulator sets
     if (t.MB != 1 || t.NBUF != 2) return -1;
     SMOE_FFN(1, 2, 2);
+  } else if (L.mode == 3) {
+    if (t.MB != 1 || t.NBUF != 2) return -1;
+    SMOE_FFN(1, 2, 3);
   } else if (t.MB == 1) {
     if (L.mode == 1) SMOE_FFN(1, 2, 1); else SMOE_FFN(1, 2, 0);
   } else if (t.NBUF == 2) {

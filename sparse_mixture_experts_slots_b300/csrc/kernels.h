@@ -115,6 +115,11 @@ struct BackwardArgs {
   uint32_t* counters2; int counter2_words;      // 1 + E * ceil(max(d, F) / 256)
   // split sums over tokens (dWr, dbr): partial products / sums, nsplit of them
   float* part; int nsplit;                      // [nsplit, E, d] floats (>= nsplit * E)
+  // router products on the tensor cores (tc, E % 64 == 0): ntc > 0 token chunks of kc rows
+  int ntc, kc;
+  void* dzp;                                    // [N, 3E] bf16: dz as [hi | lo | hi]
+  void* Wp;                                     // [3E, d] bf16: W_r as [hi; hi; lo]
+  int32_t* rows_k;                              // [ntc + 1] ints (filled in the backward)
 };
 int launch_backward(const BackwardArgs& a, cudaStream_t s);
 
@@ -205,7 +210,10 @@ struct FfnLaunch {
                              // plain sum: W1 = activations [E, krows, F], xe = [E, krows, R],
                              // d = krows rounded up to 64, float32 result in out_f32 [E * R, F])
   int krows;                 // mode 2: rows per expert of W1 / xe (the contraction axis)
-  float* out_f32;            // mode 2 output
+  int bcols;                 // mode 2: row length of xe in elements when it is wider than R (else 0)
+  float* out_f32;            // modes 2 and 3 output
+                             // mode 3: out_f32[E * R, F] = sum_k W1[e, k, f] xe[e * R + n, k] (W1 as
+                             // stored [E, d, F], xe K-major rows [E * R, d]; layer 1 only)
   uint32_t* counters;        // ffn_counter_words(E, R) words, zero at launch
   uint32_t* err;
   int E, R, d, F;

@@ -30,6 +30,9 @@ CASES = {
     "bwd-fp32": (dataclasses.replace(WORKLOADS["tiny-e16-fp32"], name="bwd-fp32", T=200, G=2),
                  dict(expert_bias_std=0.05), False),
     "bwd-dropped-residual": (LayerShape("bwd-dropped", 1, 400, 128, 256, 6, 0.5), dict(router_bias_std=0.5), True),
+    # 64 experts and 1024 tokens: the router's products dWr and dx on the tensor cores too
+    # (token chunks of 256 rows, dz in bf16 hi/lo pieces)
+    "bwd-tc-router": (LayerShape("bwd-tc-router", 2, 512, 256, 384, 64, 1.0), dict(router_bias_std=0.1), False),
 }
 
 
