@@ -314,22 +314,34 @@ def run_train(args, shape):
     fwd_ms = sum(a.elapsed_time(b) for (a, _), b in zip(fw, bw)) / args.steps
     bwd_ms = step_ms - fwd_ms
     K = int(r.expert_rows.sum().item())
-    bwd_flops = 4 * 2.0 * K * shape.d_model * shape.d_ff + 2 * 2.0 * shape.N * shape.E * shape.d_model
+    N, E, d, F = shape.N, shape.E, shape.d_model, shape.d_ff
+    es = 4 if shape.dtype == "f32" else 2
+    used = int((r.expert_rows > 0).sum().item())
+    R = layer.block_rows
+    bwd_flops = 4 * 2.0 * K * d * F + 2 * 2.0 * N * E * d
+    # algorithmic bytes of the backward: the used experts' W1 and W2 read once, their float32
+    # weight gradients written once (every expert's, unused ones as zeros), the saved
+    # activations xe and h and the incoming dy read once, the float32 dx, dWr and the router
+    # logits [N, E] read / written once
+    bwd_bytes = (2 * used * d * F * es + 2 * E * d * F * 4 + K * (d + F) * es + N * d * es + N * d * 4
+                 + E * d * 4 + N * E * 4)
     tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    gbs = bwd_bytes / (bwd_ms * 1e-3) / 1e9
     hbm, tc_burst, tc_sust, peak_src = peaks()
-    tc_shapes = shape.dtype == "bf16" and shape.d_model % 128 == 0 and shape.d_ff % 128 == 0
+    tc_shapes = shape.dtype == "bf16" and d % 128 == 0 and F % 128 == 0
     print(json.dumps({
-        "metric": METRIC + " (training step: forward + backward)", "value": shape.N / (step_ms * 1e-3),
+        "metric": METRIC + " (training step: forward + backward)", "value": N / (step_ms * 1e-3),
         "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if shape.dtype == "bf16" else "f32", "data": "synthetic",
         "config": config_of(shape, argparse.Namespace(gpus=1, top_k=1)) | {"mode": "train"},
-        "forward_ms": fwd_ms, "backward_ms": bwd_ms, "kept_rows": K,
-        "roofline": ({"bound": "tensor", "kernel": "switch_backward (expert products: ffn_persistent_kernel modes 1-2)",
-                      "achieved": tf, "peak": tc_burst, "unit": "TFLOP/s", "frac": tf / tc_burst,
-                      "peak_source": f"{peak_src} bf16_tflops (cuBLAS bf16 GEMM, burst)",
-                      "algorithmic_flops": bwd_flops, "traffic": None,
-                      "note": "whole backward time, transposes and float32 widening included"}
+        "forward_ms": fwd_ms, "backward_ms": bwd_ms, "kept_rows": K, "expert_block_rows": R,
+        "roofline": ({"bound": "hbm", "kernel": "switch_backward (whole backward)", "achieved": gbs, "peak": hbm,
+                      "unit": "GB/s", "frac": gbs / hbm, "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
+                      "algorithmic_bytes": bwd_bytes, "traffic": None,
+                      "tensor": {"achieved_tflops": tf, "peak_tflops": tc_burst, "frac": tf / tc_burst},
+                      "note": "the backward moves ~3.6 GB at switch-base (weights in, float32 weight gradients "
+                              "out) for 0.07 TFLOP: bytes bind it; all its products run on the tensor cores"}
                      if tc_shapes else
                      {"bound": "alu", "kernel": "bgemm_kernel (backward products)", "achieved": tf,
                       "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS,
@@ -337,6 +349,59 @@ def run_train(args, shape):
                       "algorithmic_flops": bwd_flops, "traffic": None}),
     }), flush=True)
     return 0
+
+# ---------------------------------------------------------------- routing step alone (--stage route)
+def run_route(args, shape):
+    """One step = switch_route (router GEMM, softmax, top-1, statistics, aux and z-loss, slots
+    and capacity mask) over the workload's tokens with W_r prepared once; no expert weights
+    are allocated.  Roofline of the router kernel: its three bf16 pieces' MMA FLOPs (2 N d E
+    each) at the bf16 tensor peak."""
+    if not torch.cuda.is_available() or shape.dtype != "bf16":
+        print(json.dumps({"metric": METRIC + " (routing step)", "error": "needs a CUDA device and bf16"}))
+        return 1
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from sparse_mixture_experts_slots_b300 import SwitchMoE
+    inp = make_inputs(shape, workload_seed(args.workload), dev, with_experts=False)
+    layer = SwitchMoE(shape.G, shape.T, shape.d_model, shape.d_ff, shape.E, shape.capacity_factor,
+                      dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    layer.prepare_router(inp["Wr"], stream=stream)
+    r = layer.alloc_route()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        layer.route(inp["x"], None, inp["br"], out=r, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        layer.route(inp["x"], None, inp["br"], out=r, stream=stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    layer.sync_status(stream)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    flops = 3 * 2.0 * shape.N * shape.d_model * shape.E  # hi, mid and lo pieces
+    hbm, tc_burst, tc_sust, peak_src = peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": METRIC + " (routing step)", "value": shape.N / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(shape, argparse.Namespace(gpus=1, top_k=1)) | {"mode": "route"},
+        "roofline": {"bound": "tensor", "kernel": "router_tc_kernel + split-free route (scan, slots)",
+                     "achieved": tf, "peak": tc_burst, "unit": "TFLOP/s", "frac": tf / tc_burst,
+                     "peak_source": f"{peak_src} bf16_tflops (cuBLAS bf16 GEMM, burst)",
+                     "algorithmic_flops": flops, "traffic": None,
+                     "note": "the router multiplies three bf16 pieces of the float32 W_r; the stage also "
+                             "runs the cross-tile scan and the slots kernel"},
+        "clocks": clk,
+    }), flush=True)
+    return 0
+
 
 # ---------------------------------------------------------------- GPU arm
 def run_gpu(args, shape):
@@ -531,6 +596,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--train", action="store_true",
                     help="time a training step (forward in training mode + switch_backward)")
+    ap.add_argument("--stage", default="layer", choices=["layer", "route"],
+                    help="route: time the routing step alone (no expert weights)")
     ap.add_argument("--top-k", type=int, default=1, choices=[1, 2],
                     help="2: the top-2 variant (weights = softmax over the two highest scores)")
     args = ap.parse_args()
@@ -538,6 +605,8 @@ def main():
     shape = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, shape)
+    if args.stage == "route":
+        return run_route(args, shape)
     if args.train:
         return run_train(args, shape)
     return run_gpu(args, shape)
