@@ -43,6 +43,7 @@ struct switch_layer {
   int32_t* group_off;
   int32_t* tok_of_row;
   void* wsplit;
+  void* xchg;  // the router's global exchange rows, or null
   uint32_t* ffn_counters;
   int ffn_counter_words;
   float* scan_partial;
@@ -190,6 +191,8 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const bool train = training_of(cfg);
   const size_t o_logits = take(cfg->dtype == SWITCH_F32 || two || train ? N * E * sizeof(float) : 0);
   const size_t o_wsplit = take(cfg->dtype == SWITCH_BF16 ? router_tc_wsplit_bytes(cfg->E, cfg->d_model) : 0);
+  const size_t xchg_bytes = cfg->dtype == SWITCH_BF16 ? router_tc_exchange_bytes((long long)(G * nT), cfg->E) : 0;
+  const size_t o_xchg = take(xchg_bytes);
   const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
   const size_t ffn_words = ffn_counter_words(cfg->E, (int)R, cfg->d_model, cfg->d_ff);
   const size_t o_fcnt = take(ffn_words * sizeof(uint32_t));
@@ -261,6 +264,7 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   h->group_off = reinterpret_cast<int32_t*>(h->ws + o_goff);
   h->tok_of_row = reinterpret_cast<int32_t*>(h->ws + o_tor);
   h->wsplit = h->ws + o_wsplit;
+  h->xchg = xchg_bytes ? h->ws + o_xchg : nullptr;
   h->scan_partial = reinterpret_cast<float*>(h->ws + o_part);
   h->ffn_counters = reinterpret_cast<uint32_t*>(h->ws + o_fcnt);
   h->ffn_counter_words = (int)ffn_words;
@@ -351,6 +355,7 @@ static switch_status route_args(switch_handle h, const void* x, const float* Wr,
   // training: the backward needs the logits, so the tensor-core router writes them too
   a->logits_out = want_logits ? out->logits : (training_of(&c) ? h->logits : nullptr);
   a->wsplit = h->wsplit;
+  a->xchg = h->xchg;
   a->tile_hist = h->tile_hist;
   a->tile_P = h->tile_P;
   a->tile_Z = h->tile_Z;
@@ -412,7 +417,7 @@ switch_status switch_dispatch(switch_handle h, const void* x, const switch_route
   if (h->N > 0 && (!x || !aligned16(x))) return SWITCH_ERR_INVALID_ARG;
   const bool two = top2_of(&h->cfg);
   return launched(launch_dispatch(x, xe, r->expert, r->row, two ? r->expert2 : nullptr, two ? r->row2 : nullptr,
-                                  r->expert_rows, h->N, h->cfg.E, h->R, h->cfg.d_model * h->es,
+                                  r->expert_rows, h->N, h->cfg.E, h->R, h->cfg.d_model * h->es, h->err,
                                   (cudaStream_t)stream),
                   h);
 }
@@ -495,7 +500,7 @@ static switch_status combine_impl(switch_handle h, const void* ye, const switch_
   if (x_residual && !aligned16(x_residual)) return SWITCH_ERR_INVALID_ARG;
   return launched(launch_combine(ye, r->expert, r->row, r->gate, two ? r->expert2 : nullptr,
                                  two ? r->row2 : nullptr, two ? r->gate2 : nullptr, x_residual, y, h->N,
-                                 h->cfg.d_model, h->R, h->cfg.dtype == SWITCH_BF16, s, pdl),
+                                 h->cfg.d_model, h->cfg.E, h->R, h->cfg.dtype == SWITCH_BF16, h->err, s, pdl),
                   h);
 }
 
@@ -530,7 +535,7 @@ switch_status switch_forward(switch_handle h, const void* x, const float* Wr, co
     if (prof) cudaEventRecord(h->ev[1], s);
     st = launched(launch_dispatch(x, h->xe, r->expert, r->row, a.top2 ? r->expert2 : nullptr,
                                   a.top2 ? r->row2 : nullptr, r->expert_rows, h->N, h->cfg.E, h->R,
-                                  h->cfg.d_model * h->es, s),
+                                  h->cfg.d_model * h->es, h->err, s),
                   h);
     if (st != SWITCH_OK) return st;
     if (prof) cudaEventRecord(h->ev[2], s);

@@ -135,11 +135,6 @@ template <int MB>
 __device__ __forceinline__ void epi_sync() {  // named barrier over the epilogue warps
   asm volatile("bar.sync 1, %0;" ::"n"(128 * FF_EPW * MB) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }

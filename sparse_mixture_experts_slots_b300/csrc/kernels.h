@@ -55,6 +55,8 @@ struct RouteArgs {
   float* logits_out;   // [N, E] or null: logits the caller asked for
   void* wsplit;        // W_r split into hi, mid, lo bf16 pieces (tensor-core router; layout in route_tc.cu);
                        // with Wr null the router uses it as it is (prepared by an earlier split)
+  void* xchg;          // router_tc_exchange_bytes of zeroed memory (tensor-core router over more than
+                       // two expert slices: the slices meet in global memory), or null: clusters
   int32_t* tile_hist;  // [G, nT, E]
   float* tile_P;       // [G, nT, E]
   float* tile_Z;       // [G, nT]: sum over the tile's tokens of (log sum_e exp z)^2
@@ -141,6 +143,9 @@ int router_tc_experts_per_cta(int E);
 int router_tc_mma_n(int EC);
 // Bytes of the split W_r workspace ([Q][d / 64 atoms][hi, mid, lo][EC][64] bf16) for E experts of width d.
 size_t router_tc_wsplit_bytes(int E, int d);
+// Bytes of the global exchange rows of the tensor-core router for `tiles` 128-token tiles
+// (0 when E's slices meet in a cluster).  Zeroed once when allocated.
+size_t router_tc_exchange_bytes(long long tiles, int E);
 
 // 3-D view [cols / 64 atoms][rows][64] of a row-major bf16 matrix (cols % 64 == 0); a box of
 // box_atoms consecutive 64-column atoms of box_rows rows lands as box_atoms swizzled
@@ -154,24 +159,25 @@ int device_sm_count();
 // 2-D bf16 tensor map [rows, cols] (cols contiguous), box box_rows x 64 columns, 128-byte swizzle.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
-// Slots from in-tile ranks, then the dispatch copy: one warp per token.  When y is
-// not null (combine fused into the FFN), dropped tokens' rows of y get their final
-// value here (x_residual or zero), and `zero` words at zero_ptr are cleared.
+// Slots from in-tile ranks, then the dispatch copy (rows staged through shared memory by
+// bulk copies).  When y is not null (combine fused into the FFN), dropped tokens' rows of y
+// get their final value here (x_residual or zero), and `zero` words at zero_ptr are cleared.
 int launch_dispatch_slots(const void* x, void* xe, const RouteArgs& a, void* y, const void* resid,
                           uint32_t* zero_ptr, int zero_words, cudaStream_t s, bool pdl);
 
 // xe[expert[t]*R + row[t]] = x[t] for kept tokens (row[t] >= 0), and likewise for the
 // second choice (expert2/row2, top-2 routing; null otherwise); rows r >= expert_rows[e] of
 // every expert block are zeroed.
+// err: the device error word (a staging wait that runs out sets ERR_TIMEOUT).
 int launch_dispatch(const void* x, void* xe, const int32_t* expert, const int32_t* row, const int32_t* expert2,
                     const int32_t* row2, const int32_t* expert_rows, int N, int E, int R, int row_bytes,
-                    cudaStream_t s);
+                    uint32_t* err, cudaStream_t s);
 
 // y[t] = (row[t] >= 0 ? gate[t] * ye[expert[t]*R + row[t]] : 0)
 //        (+ row2[t] >= 0 ? gate2[t] * ye[expert2[t]*R + row2[t]] : 0, top-2) (+ resid[t]).
 int launch_combine(const void* ye, const int32_t* expert, const int32_t* row, const float* gate,
                    const int32_t* expert2, const int32_t* row2, const float* gate2, const void* resid,
-                   void* y, int N, int d, int R, bool bf16, cudaStream_t s, bool pdl);
+                   void* y, int N, int d, int E, int R, bool bf16, uint32_t* err, cudaStream_t s, bool pdl);
 
 // out[e*R + n, m] = act(sum_k in[e*R + n, k] * W[e, m, k] + bias[e, m]) for n < expert_rows[e].
 // CUDA-core kernel for float32 and for shapes the tensor-core kernel does not take.

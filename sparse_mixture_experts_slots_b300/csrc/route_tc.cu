@@ -11,8 +11,21 @@
 // cores, the hi piece in its own TMEM accumulator so the small terms never share an
 // accumulator with the large ones; the pieces are added in the epilogue.
 //
-// One persistent kernel.  A cluster of Q CTAs (CTA q holds experts q EC .. q EC + EC - 1)
-// walks the token tiles (128 tokens of one routing group); clusters take tiles in turn.
+// One persistent kernel; a work item is one token tile (128 tokens of one routing group)
+// times one slice of EC experts (slice q: experts q EC .. q EC + EC - 1), Q slices per tile.
+// Two ways to put the slices of a tile together:
+//   clusters  a cluster of Q CTAs (CTA q holds slice q) walks the tiles; clusters take tiles
+//             in turn; the per-token partials move through distributed shared memory.
+//             Clusters of 4 or 8 CTAs fit on fewer SMs (8: 120 of 148), so this is used for
+//             Q <= 2 (and where no exchange buffer is given);
+//   global    every SM runs one CTA of a cooperative grid; CTA c takes items c, c + grid, ...
+//             (item = tile Q + slice); the partials go through global memory, each slice's
+//             flag set to the launch's epoch when they are written.  An item waits only on the
+//             other slices of its tile, items a CTA owns come in increasing order, and the
+//             slices of a tile are items within Q - 1 of each other, so every wait is on work
+//             that is running or done.  The epoch lives in device memory: every CTA reads it
+//             at the start, and the last CTA to finish advances it (a ticket), so a replayed
+//             CUDA graph of the call still sees a fresh epoch.
 // Per CTA:
 //   warp 0, one lane : TMA producer.  Per 64-column atom of K the x tile (an x stage holds
 //                      NAX atoms) and the slice's W box(es) (hi, mid, lo rows), each in a
@@ -25,9 +38,11 @@
 //     pass 1  logits z (+ bias) into registers, then the accumulator is released;
 //             max / argmax (ties -> lowest index), combined over the column groups
 //     pass 1b exp(z - max) in registers (ex2 of the log2e-scaled difference), sums
-//     exchange of (max, sum, argmax) between the Q CTAs: each CTA writes its values into
-//             every peer's receive buffer with asynchronous remote stores that count their
-//             bytes on the peer's barrier; everyone reads the Q slices from its own memory
+//     exchange of (max, sum, argmax) between the Q slices: (clusters) each CTA writes its
+//             values into every peer's receive buffer with asynchronous remote stores that
+//             count their bytes on the peer's barrier, everyone reads the Q slices from its
+//             own memory; (global) each CTA writes them to the tile's exchange rows and
+//             releases its flag, then reads all Q slices once every flag carries the epoch
 //     pass 2  p = exp(z - max) * exp(max - Max) / Sum; column sums over the tile's tokens
 //             (warp reduce-scatter), expert histogram of the tile, rank of each token
 //             among the tile's earlier tokens with the same expert.
@@ -178,15 +193,20 @@ __device__ __forceinline__ float warp_colsum8(const float* p, int lane) {
 __device__ __forceinline__ void rt_epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * RT_EPI_WARPS) : "memory"); }
 
 // ---------------------------------------------------------------- the router kernel
-// grid Q * (clusters); clusters of Q CTAs along x when Q > 1.  Cluster c takes the tiles
-// c, c + clusters, ... of the G * nT tiles (tile id = group * nT + tile in group).
-template <int EC, int NAX>
+// GX false: grid Q * (clusters); clusters of Q CTAs along x when Q > 1.  Cluster c takes the
+// tiles c, c + clusters, ... of the G * nT tiles (tile id = group * nT + tile in group).
+// GX true: a cooperative grid of one CTA per SM; CTA c takes the items c, c + grid, ... of
+// the G * nT * Q items (item = tile id * Q + slice).  Exchange rows (GX): xms / xam
+// [tile id][Q][128], xflag [tile id][Q]; xctl[0] the epoch of the last launch, xctl[1] the
+// finish ticket (zero between launches).
+template <int EC, int NAX, bool GX>
 __global__ void __launch_bounds__(RT_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const float* __restrict__ br, int T, int E, int d, int nT, int Q, int total_tiles,
                      int32_t* __restrict__ expert, float* __restrict__ gate, int32_t* __restrict__ rank,
                      int32_t* __restrict__ tile_hist, float* __restrict__ tile_P, float* __restrict__ tile_Z,
-                     float* __restrict__ logits, float* __restrict__ probs, uint32_t* err) {
+                     float* __restrict__ logits, float* __restrict__ probs, uint32_t* err, float2* __restrict__ xms,
+                     int* __restrict__ xam, uint32_t* __restrict__ xflag, uint32_t* __restrict__ xctl) {
   using Cf = RtCfg<EC, NAX>;
   using Gm = RtGeom<EC>;
   constexpr int XS = Cf::XS, WS = Cf::WS, NBUF = Gm::NBUF;
@@ -197,9 +217,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   RtScratch<EC>& sh = *reinterpret_cast<RtScratch<EC>*>(smem + Cf::RING_BYTES);
   RtBars<XS, WS>& bar = *reinterpret_cast<RtBars<XS, WS>*>(smem + Cf::RING_BYTES + sizeof(RtScratch<EC>));
 
-  const int q = Q > 1 ? (int)cluster_ctarank() : 0;
-  const int cl = (int)blockIdx.x / Q, ncl = (int)gridDim.x / Q;
-  const int e0 = q * EC;
+  // work items: (clusters) the tiles of this cluster, slice fixed by the cluster rank;
+  // (global) tile it / Q, slice it % Q
+  const int qc = (!GX && Q > 1) ? (int)cluster_ctarank() : 0;
+  const int it0 = GX ? (int)blockIdx.x : (int)blockIdx.x / Q;
+  const int istep = GX ? (int)gridDim.x : (int)gridDim.x / Q;
+  const int n_items = GX ? total_tiles * Q : total_tiles;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int NK = (d + RT_BK - 1) / RT_BK;  // atoms along K
   const int NXS = (NK + NAX - 1) / NAX;    // x stages per tile
@@ -232,15 +255,17 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (Q > 1) cluster_sync();  // every peer's barriers are initialised before any remote arrival
+  if (!GX && Q > 1) cluster_sync();  // every peer's barriers are initialised before any remote arrival
   const uint32_t tmem = bar.tmem_slot;
+  // (global) this launch's flag value; no CTA advances xctl[0] before every CTA has read it
+  const uint32_t epoch = GX ? __ldcg(xctl) + 1u : 0u;
   griddep_launch_dependents();  // after the TMEM allocation: a dependent grid cannot starve it
   // This grid may start while the previous kernel of the stream still runs: everything it
   // reads from memory (x, the W_r pieces, br) is read after this wait.
   griddep_wait();
   for (int c = threadIdx.x; c < EC; c += blockDim.x) {
-    const int e = e0 + c;
-    sh.bias[c] = (br && e < E) ? br[e] : 0.f;
+    const int e = qc * EC + c;  // (global: reloaded per item)
+    sh.bias[c] = e < E ? (br ? br[e] : 0.f) : -INFINITY;  // padding experts never win and weigh 0
     sh.hist[c] = 0;
   }
   __syncthreads();
@@ -250,7 +275,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       // ---------------- TMA producer
       uint32_t xi = 0, wi = 0;
       bool ok = true;
-      for (int tid = cl; tid < total_tiles && ok; tid += ncl) {
+      for (int it = it0; it < n_items && ok; it += istep) {
+        const int tid = GX ? it / Q : it, q = GX ? it - tid * Q : qc;
         const int g = tid / nT, tile = tid - g * nT;
         const int row0 = g * T + tile * RT_BM;
         for (int xs = 0; xs < NXS && ok; ++xs) {
@@ -294,7 +320,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       uint32_t xi = 0, wi = 0;
       int lt = 0;
       bool ok = true;
-      for (int tid = cl; tid < total_tiles && ok; tid += ncl, ++lt) {
+      for (int it = it0; it < n_items && ok; it += istep, ++lt) {
         if (bar.abort_flag) { ok = false; break; }
         const int buf = lt % NBUF;
         if (lt >= NBUF && !mbar_wait(&bar.aempty[buf], ((lt / NBUF) - 1) & 1)) { ok = false; break; }
@@ -352,14 +378,19 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     const int et = threadIdx.x - 64;  // 0 .. 511
     const bool leader = et == 0;
     int lt = 0;
-    for (int tid = cl; tid < total_tiles; tid += ncl, ++lt) {
+    for (int it = it0; it < n_items; it += istep, ++lt) {
       const int buf = lt % NBUF;
+      const int tid = GX ? it / Q : it, q = GX ? it - tid * Q : qc;
+      const int e0 = q * EC;
       const int g = tid / nT, tile = tid - g * nT;
       const int t0 = tile * RT_BM;
       const long long tok0 = (long long)g * T + t0;
       const bool valid = t0 + i < T;
       const long long tok = tok0 + i;
       const uint32_t trow = tmem + (uint32_t)(buf * Gm::TILE_COLS) + ((uint32_t)(lq * 32) << 16);
+      if (GX)  // this item's slice of the bias (the previous item's epilogue is done with it)
+        for (int c = et; c < EC; c += 32 * RT_EPI_WARPS)
+          sh.bias[c] = e0 + c < E ? (br ? br[e0 + c] : 0.f) : -INFINITY;
 
       if (leader) {  // the tile's accumulator is complete (or the kernel is giving up)
         int ok = bar.abort_flag ? 0 : 1;
@@ -395,9 +426,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
                                                     : __uint_as_float(r1[j]);
             const float z = (__uint_as_float(h[j]) + corr) + sh.bias[c];
             v[ch * 8 + j] = z;
-            if (e0 + c < E) {
-              if (z > m) { m = z; a = e0 + c; }
-            }
+            if (z > m) { m = z; a = e0 + c; }  // padding experts: z = -inf
           }
           if (logits && valid) {  // the chunk's 8 logits of this token: 16-byte stores when aligned
             const int c0 = e0 + cbeg + ch * 8;
@@ -438,13 +467,13 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         const float mcs = mc * LOG2E;
 #pragma unroll
         for (int k = 0; k < CPW; ++k) {
-          const float ex = (e0 + cbeg + k < E) ? ex2_approx(fmaf(v[k], LOG2E, -mcs)) : 0.f;
+          const float ex = ex2_approx(fmaf(v[k], LOG2E, -mcs));  // 0 for padding experts (z = -inf)
           v[k] = ex;
           ps += ex;
         }
         sh.red_s[cg][i] = ps;
       }
-      if (Q > 1 && leader) {
+      if (!GX && Q > 1 && leader) {
         int ok = 1;
         // every peer has read its receive buffer of the previous tile
         if (lt >= 1 && !mbar_wait_cluster(&bar.rfree, (lt - 1) & 1)) {
@@ -457,11 +486,15 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         bar.ep_ok = ok;
       }
       rt_epi_sync();
+      const size_t xrow = (size_t)tid * Q;  // (global) the tile's exchange rows
       if (cg == 0) {
         float sc = 0.f;
 #pragma unroll
         for (int k = 0; k < NCG; ++k) sc += sh.red_s[k][i];
-        if (Q > 1) {  // into slot q of every peer's receive buffer
+        if (GX) {
+          xms[(xrow + q) * RT_BM + i] = make_float2(mc, sc);
+          xam[(xrow + q) * RT_BM + i] = ac;
+        } else if (Q > 1) {  // into slot q of every peer's receive buffer
           for (int rk = 0; rk < Q; ++rk) {
             st_async_v2_f32(&sh.rms[q][i], mc, sc, &bar.rfull, (uint32_t)rk);
             st_async_s32(&sh.ra[q][i], ac, &bar.rfull, (uint32_t)rk);
@@ -472,7 +505,26 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         }
       }
       bool xok = true;
-      if (Q > 1) {
+      if (GX) {
+        rt_epi_sync();  // this slice's 128 rows are written
+        if (leader) {
+          int ok = bar.abort_flag ? 0 : 1;
+          __threadfence();
+          st_release_gpu(xflag + xrow + q, epoch);
+          const long long t0 = clock64();
+          for (int k = 0; k < Q && ok; ++k)
+            while (ld_acquire_gpu(xflag + xrow + k) != epoch)
+              if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+                raise_error(err, ERR_TIMEOUT);
+                bar.abort_flag = 1;
+                ok = 0;
+                break;
+              }
+          bar.ep_ok = ok;
+        }
+        rt_epi_sync();
+        xok = bar.ep_ok != 0;
+      } else if (Q > 1) {
         if (leader) {
           int ok = bar.ep_ok;
           if (ok && !mbar_wait_cluster(&bar.rfull, lt & 1)) {
@@ -490,7 +542,19 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       if (cg == 0) {
         float M = -INFINITY, S = 0.f;
         int A = INT_MAX;
-        if (xok) {  // expert slices in rank order: the lowest index wins a tie
+        if (xok && GX) {  // expert slices in order: the lowest index wins a tie
+          for (int rk = 0; rk < Q; ++rk) {
+            const float mr = __ldcg(&xms[(xrow + rk) * RT_BM + i].x);
+            if (mr > M) {
+              M = mr;
+              A = __ldcg(xam + (xrow + rk) * RT_BM + i);
+            }
+          }
+          for (int rk = 0; rk < Q; ++rk) {
+            const float2 ms = __ldcg(xms + (xrow + rk) * RT_BM + i);
+            if (ms.y > 0.f) S += ms.y * expf(ms.x - M);
+          }
+        } else if (xok) {  // expert slices in rank order: the lowest index wins a tie
           for (int rk = 0; rk < Q; ++rk) {
             const float mr = sh.rms[rk][i].x;
             if (mr > M) {
@@ -516,7 +580,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       rt_epi_sync();
       // this CTA has read its receive buffer (every read value was consumed before the
       // barrier above): peers may fill it with the next tile
-      if (Q > 1 && leader)
+      if (!GX && Q > 1 && leader)
         for (int rk = 0; rk < Q; ++rk) mbar_arrive_remote_relaxed(&bar.rfree, (uint32_t)rk);
 
       // pass 2: p = exp(z - mc) * exp(mc - M) / S; column sums over the tile's tokens
@@ -571,7 +635,15 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (Q > 1) cluster_sync();  // no peer reads this CTA's shared memory or arrives on its barriers any more
+  if (!GX && Q > 1) cluster_sync();  // no peer reads this CTA's shared memory or arrives on its barriers any more
+  if (GX && threadIdx.x == 0) {  // the last CTA to finish advances the epoch for the next launch
+    __threadfence();
+    if (atomicAdd(xctl + 1, 1u) == gridDim.x - 1) {
+      xctl[1] = 0u;
+      __threadfence();
+      st_release_gpu(xctl, epoch);
+    }
+  }
   if (warp == 1) tmem_dealloc(tmem, Gm::TMEM_COLS);
 }
 
@@ -608,19 +680,96 @@ static int rt_clusters(K kern, int smem, int Q) {
   return n;
 }
 
+// Exchange rows of the global variant for `tiles` token tiles: (max, sum) float2 and argmax
+// int per (tile, slice, token), a flag per (tile, slice), then the epoch and ticket words.
+struct RtXchg {
+  float2* ms;
+  int* am;
+  uint32_t* flag;
+  uint32_t* ctl;
+};
+static size_t rt_round256(size_t b) { return (b + 255) / 256 * 256; }
+static bool rt_global(int E) {
+  const int EC = router_tc_experts_per_cta(E);
+  return (E + EC - 1) / EC > 2;
+}
+size_t router_tc_exchange_bytes(long long tiles, int E) {
+  if (!rt_global(E) || tiles <= 0) return 0;
+  const int EC = router_tc_experts_per_cta(E);
+  const size_t n = (size_t)tiles * (size_t)((E + EC - 1) / EC);
+  return rt_round256(n * RT_BM * sizeof(float2)) + rt_round256(n * RT_BM * sizeof(int)) +
+         rt_round256(n * sizeof(uint32_t)) + 256;
+}
+static RtXchg rt_xchg(void* base, long long tiles, int Q) {
+  uint8_t* p = static_cast<uint8_t*>(base);
+  const size_t n = (size_t)tiles * Q;
+  RtXchg x;
+  x.ms = reinterpret_cast<float2*>(p);
+  p += rt_round256(n * RT_BM * sizeof(float2));
+  x.am = reinterpret_cast<int*>(p);
+  p += rt_round256(n * RT_BM * sizeof(int));
+  x.flag = reinterpret_cast<uint32_t*>(p);
+  p += rt_round256(n * sizeof(uint32_t));
+  x.ctl = reinterpret_cast<uint32_t*>(p);
+  return x;
+}
+
+// CTAs of the global variant that are resident at once (one per SM with this shared memory).
+template <typename K>
+static int rt_coop_ctas(K kern, int smem) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RT_THREADS, (size_t)smem) != cudaSuccess ||
+      per_sm <= 0) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int n = per_sm * device_sm_count();
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
 template <int EC, int NAX>
 static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteArgs& a, int nT, int Q,
                      int32_t* rank, cudaStream_t s) {
-  auto kern = router_tc_kernel<EC, NAX>;
+  const long long total = (long long)a.G * nT;
+  if (total * Q >= (1ll << 31)) return -1;
+  if (a.xchg && rt_global(a.E)) {
+    // cooperative grid: the CTAs wait on one another's exchange flags, so all must be resident
+    auto kern = router_tc_kernel<EC, NAX, true>;
+    constexpr int smem = rt_smem_bytes<EC, NAX>();
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+    const int fit = rt_coop_ctas(kern, smem);
+    const long long items = total * Q;
+    const int grid = (int)(items < fit ? items : fit);
+    const RtXchg x = rt_xchg(a.xchg, total, Q);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(RT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeCooperative;
+    attr.val.cooperative = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, (int)total, a.expert,
+                                             a.gate, rank, a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs,
+                                             a.err, x.ms, x.am, x.flag, x.ctl);
+    return e == cudaSuccess ? 1 : -1;
+  }
+  auto kern = router_tc_kernel<EC, NAX, false>;
   constexpr int smem = rt_smem_bytes<EC, NAX>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-  const long long total = (long long)a.G * nT;
-  if (total >= (1ll << 31)) return -1;
   const int fit = rt_clusters(kern, smem, Q);
   const int ncl = (int)(total < fit ? total : fit);
   const cudaError_t e = launch_k(kern, dim3((unsigned)(Q * ncl), 1, 1), dim3(RT_THREADS, 1, 1), smem, s,
                                  /*pdl=*/true, (unsigned)Q, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, (int)total, a.expert,
-                                 a.gate, rank, a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs, a.err);
+                                 a.gate, rank, a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs, a.err,
+                                 (float2*)nullptr, (int*)nullptr, (uint32_t*)nullptr, (uint32_t*)nullptr);
   return e == cudaSuccess ? 1 : -1;
 }
 

@@ -66,6 +66,12 @@ SMALL = {
                       dict(expert_bias_std=0.05, router_bias_std=0.3)),
     # d = 192: three 64-column atoms, so the router's last two-atom stage has a zero-filled half
     "odd-atoms": (LayerShape("odd-atoms", 2, 260, 192, 256, 12, 1.0), dict(router_bias_std=0.1)),
+    # 512 experts over 8 slices of 64 (34 tiles x 8 = 272 router items, more than one per SM):
+    # the slices of a tile meet in global memory, some tiles straddle two rounds of the grid
+    "gx-rounds": (LayerShape("gx-rounds", 2, 2100, 128, 128, 512, 1.0), dict(router_bias_std=0.1)),
+    # float32 rows of 49,408 bytes: too wide for the shared-memory row slots of the bulk-copy
+    # dispatch and combine, so their register kernels run
+    "wide-rows": (LayerShape("wide-rows", 1, 40, 12352, 32, 4, 1.0, dtype="f32"), dict(expert_bias_std=0.05)),
 }
 
 
