@@ -507,20 +507,27 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       bool xok = true;
       if (GX) {
         rt_epi_sync();  // this slice's 128 rows are written
-        if (leader) {
-          int ok = bar.abort_flag ? 0 : 1;
-          __threadfence();
-          st_release_gpu(xflag + xrow + q, epoch);
+        if (warp == 2) {  // the leader's warp: publish, then lane k watches slice k's flag
+          bool ok = bar.abort_flag == 0;
+          if (leader) {
+            __threadfence();
+            st_release_gpu(xflag + xrow + q, epoch);
+          }
+          __syncwarp();
           const long long t0 = clock64();
-          for (int k = 0; k < Q && ok; ++k)
-            while (ld_acquire_gpu(xflag + xrow + k) != epoch)
-              if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+          bool seen = lane >= Q;
+          while (ok) {
+            if (!seen) seen = ld_acquire_gpu(xflag + xrow + lane) == epoch;
+            if (__all_sync(0xffffffffu, seen)) break;
+            if (__shfl_sync(0xffffffffu, clock64() - t0 > WAIT_LIMIT_CYCLES ? 1 : 0, 0)) {
+              if (leader) {
                 raise_error(err, ERR_TIMEOUT);
                 bar.abort_flag = 1;
-                ok = 0;
-                break;
               }
-          bar.ep_ok = ok;
+              ok = false;
+            }
+          }
+          if (leader) bar.ep_ok = ok ? 1 : 0;
         }
         rt_epi_sync();
         xok = bar.ep_ok != 0;
@@ -543,17 +550,21 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         float M = -INFINITY, S = 0.f;
         int A = INT_MAX;
         if (xok && GX) {  // expert slices in order: the lowest index wins a tie
-          for (int rk = 0; rk < Q; ++rk) {
-            const float mr = __ldcg(&xms[(xrow + rk) * RT_BM + i].x);
-            if (mr > M) {
-              M = mr;
-              A = __ldcg(xam + (xrow + rk) * RT_BM + i);
+          float2 ms[8];  // every slice's pair in flight at once (Q <= 8)
+#pragma unroll
+          for (int rk = 0; rk < 8; ++rk)
+            if (rk < Q) ms[rk] = __ldcg(xms + (xrow + rk) * RT_BM + i);
+          int kb = 0;
+#pragma unroll
+          for (int rk = 0; rk < 8; ++rk)
+            if (rk < Q && ms[rk].x > M) {
+              M = ms[rk].x;
+              kb = rk;
             }
-          }
-          for (int rk = 0; rk < Q; ++rk) {
-            const float2 ms = __ldcg(xms + (xrow + rk) * RT_BM + i);
-            if (ms.y > 0.f) S += ms.y * expf(ms.x - M);
-          }
+          if (M > -INFINITY) A = __ldcg(xam + (xrow + kb) * RT_BM + i);
+#pragma unroll
+          for (int rk = 0; rk < 8; ++rk)
+            if (rk < Q && ms[rk].y > 0.f) S += ms[rk].y * expf(ms[rk].x - M);
         } else if (xok) {  // expert slices in rank order: the lowest index wins a tie
           for (int rk = 0; rk < Q; ++rk) {
             const float mr = sh.rms[rk][i].x;
@@ -648,35 +659,44 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
-// Clusters of Q CTAs that fit on the device at once (cached per device and kernel).
-template <typename K>
-static int rt_clusters(K kern, int smem, int Q) {
-  static int cache[64] = {0};
+// CTAs of router_tc_kernel<EC, NAX, GX> resident at once in clusters of cl CTAs (cached per
+// kernel, device and cluster size).
+template <int EC, int NAX, bool GX>
+static int rt_fit(int cl) {
+  static int cache[64][9] = {};
+  auto kern = router_tc_kernel<EC, NAX, GX>;
+  constexpr int smem = rt_smem_bytes<EC, NAX>();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  const bool cached = dev >= 0 && dev < 64 && cl >= 1 && cl <= 8;
+  if (cached && cache[dev][cl] > 0) return cache[dev][cl];
   int n = 0;
-  if (Q > 1) {
+  if (cl > 1) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)Q, 1, 1);
+    cfg.gridDim = dim3((unsigned)cl, 1, 1);
     cfg.blockDim = dim3(RT_THREADS, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = (unsigned)Q;
+    attr.val.clusterDim.x = (unsigned)cl;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
-      n = device_sm_count() / Q;
+      n = device_sm_count() / cl;
     }
+    n *= cl;
   } else {
-    n = device_sm_count();
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, RT_THREADS, (size_t)smem) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 1;
+    }
+    n *= device_sm_count();
   }
-  if (n < 1) n = 1;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (n < cl) n = cl;
+  if (cached) cache[dev][cl] = n;
   return n;
 }
 
@@ -714,24 +734,6 @@ static RtXchg rt_xchg(void* base, long long tiles, int Q) {
   return x;
 }
 
-// CTAs of the global variant that are resident at once (one per SM with this shared memory).
-template <typename K>
-static int rt_coop_ctas(K kern, int smem) {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RT_THREADS, (size_t)smem) != cudaSuccess ||
-      per_sm <= 0) {
-    cudaGetLastError();
-    per_sm = 1;
-  }
-  const int n = per_sm * device_sm_count();
-  if (dev >= 0 && dev < 64) cache[dev] = n;
-  return n;
-}
-
 template <int EC, int NAX>
 static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteArgs& a, int nT, int Q,
                      int32_t* rank, cudaStream_t s) {
@@ -742,7 +744,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const Route
     auto kern = router_tc_kernel<EC, NAX, true>;
     constexpr int smem = rt_smem_bytes<EC, NAX>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-    const int fit = rt_coop_ctas(kern, smem);
+    const int fit = rt_fit<EC, NAX, true>(1);
     const long long items = total * Q;
     const int grid = (int)(items < fit ? items : fit);
     const RtXchg x = rt_xchg(a.xchg, total, Q);
@@ -764,7 +766,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const Route
   auto kern = router_tc_kernel<EC, NAX, false>;
   constexpr int smem = rt_smem_bytes<EC, NAX>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-  const int fit = rt_clusters(kern, smem, Q);
+  const int fit = rt_fit<EC, NAX, false>(Q) / Q;
   const int ncl = (int)(total < fit ? total : fit);
   const cudaError_t e = launch_k(kern, dim3((unsigned)(Q * ncl), 1, 1), dim3(RT_THREADS, 1, 1), smem, s,
                                  /*pdl=*/true, (unsigned)Q, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, (int)total, a.expert,

@@ -69,6 +69,8 @@ SMALL = {
     # 512 experts over 8 slices of 64 (34 tiles x 8 = 272 router items, more than one per SM):
     # the slices of a tile meet in global memory, some tiles straddle two rounds of the grid
     "gx-rounds": (LayerShape("gx-rounds", 2, 2100, 128, 128, 512, 1.0), dict(router_bias_std=0.1)),
+    # an odd number of tiles (5) over 5 slices of 128 experts, fewer items than SMs
+    "gx-odd-tiles": (LayerShape("gx-odd-tiles", 1, 600, 128, 128, 640, 1.0), {}),
     # float32 rows of 49,408 bytes: too wide for the shared-memory row slots of the bulk-copy
     # dispatch and combine, so their register kernels run
     "wide-rows": (LayerShape("wide-rows", 1, 40, 12352, 32, 4, 1.0, dtype="f32"), dict(expert_bias_std=0.05)),
