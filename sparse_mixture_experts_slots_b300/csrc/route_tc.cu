@@ -114,17 +114,20 @@ struct RtGeom {
 };
 
 // NAX: 64-column atoms per x stage (2 when d % 128 == 0: one 3-D box of 256 bytes per row).
-template <int EC, int NAX>
+// PAIR: a CTA pair shares every W box, each CTA holding half of its rows.
+template <int EC, int NAX, bool PAIR = false>
 struct RtCfg {
   using G = RtGeom<EC>;
   static constexpr int X_ATOM = RT_BM * RT_BK * 2;  // 16 KB
   static constexpr int X_STAGE = NAX * X_ATOM;
   static constexpr int XS = NAX == 2 ? 2 : 3;        // x stages
-  static constexpr int WS_FIT = (RT_RING - XS * X_STAGE) / G::W_BOX;
+  static constexpr int WB = PAIR ? G::W_BOX / 2 : G::W_BOX;  // bytes of one W slot
+  static constexpr int WS_FIT = (RT_RING - XS * X_STAGE) / WB;
   static constexpr int WS = WS_FIT < RT_MAX_WS ? WS_FIT : RT_MAX_WS;  // W stages
   static constexpr int X_BYTES = XS * X_STAGE;
-  static constexpr int RING_BYTES = X_BYTES + WS * G::W_BOX;
+  static constexpr int RING_BYTES = X_BYTES + WS * WB;
   static_assert(WS >= 3, "at least three W boxes in flight");
+  static_assert(WB % 1024 == 0, "every W slot starts on a swizzle atom");
 };
 
 template <int XS, int WS>
@@ -155,14 +158,15 @@ struct RtScratch {
   float bias[EC];
 };
 
-template <int EC, int NAX>
+template <int EC, int NAX, bool PAIR = false>
 constexpr int rt_smem_bytes() {
-  using Cf = RtCfg<EC, NAX>;
+  using Cf = RtCfg<EC, NAX, PAIR>;
   return Cf::RING_BYTES + (int)sizeof(RtScratch<EC>) + (int)sizeof(RtBars<Cf::XS, Cf::WS>) + 1024;
 }
 static_assert(rt_smem_bytes<256, 1>() <= 227 * 1024 && rt_smem_bytes<256, 2>() <= 227 * 1024 &&
                   rt_smem_bytes<128, 1>() <= 227 * 1024 && rt_smem_bytes<128, 2>() <= 227 * 1024 &&
-                  rt_smem_bytes<64, 2>() <= 227 * 1024 && rt_smem_bytes<16, 1>() <= 227 * 1024,
+                  rt_smem_bytes<64, 2>() <= 227 * 1024 && rt_smem_bytes<16, 1>() <= 227 * 1024 &&
+                  rt_smem_bytes<256, 1, true>() <= 227 * 1024 && rt_smem_bytes<256, 2, true>() <= 227 * 1024,
               "rings and scratch fit in one SM's shared memory");
 
 // Sum of p over the 32 lanes for 8 columns at once (reduce-scatter).  On return, lane L
@@ -195,19 +199,28 @@ __device__ __forceinline__ void rt_epi_sync() { asm volatile("bar.sync 1, %0;" :
 // ---------------------------------------------------------------- the router kernel
 // GX false: grid Q * (clusters); clusters of Q CTAs along x when Q > 1.  Cluster c takes the
 // tiles c, c + clusters, ... of the G * nT tiles (tile id = group * nT + tile in group).
-// GX true: a cooperative grid of one CTA per SM; CTA c takes the items c, c + grid, ... of
-// the G * nT * Q items (item = tile id * Q + slice).  Exchange rows (GX): xms / xam
-// [tile id][Q][128], xflag [tile id][Q]; xctl[0] the epoch of the last launch, xctl[1] the
-// finish ticket (zero between launches).
-template <int EC, int NAX, bool GX>
+// XM 1 (global): a cooperative grid of one CTA per SM; CTA c takes the items c, c + grid,
+// ... of the G * nT * Q items (item = tile id * Q + slice).
+// XM 2 (global, CTA pairs; EC = 256): clusters of 2 on a cooperative grid; pair p takes the
+// pair items p, p + pairs, ... of the ceil(G nT / 2) * Q pair items (pair item = tile pair *
+// Q + slice), cluster rank r the tile 2 (tile pair) + r (a tile id past the last one reads
+// zeros and writes nothing).  The even CTA issues the MMAs of both (tcgen05 cta_group::2,
+// M = 256: each CTA's 128 token rows against the slice's 256 W rows, 128 of them in each
+// CTA's shared memory, tmWh's boxes), so every CTA streams half of the W bytes; both CTAs'
+// copies count on the even CTA's barriers, the MMAs' completions arrive on both CTAs'.
+// Exchange rows (XM >= 1): xms / xam [tile id][Q][128], xflag [tile id][Q]; xctl[0] the
+// epoch of the last launch, xctl[1] the finish ticket (zero between launches).
+template <int EC, int NAX, int XM>
 __global__ void __launch_bounds__(RT_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                     const float* __restrict__ br, int T, int E, int d, int nT, int Q, int total_tiles,
+                     const __grid_constant__ CUtensorMap tmWh, const float* __restrict__ br, int T, int E, int d, int nT, int Q, int total_tiles,
                      int32_t* __restrict__ expert, float* __restrict__ gate, int32_t* __restrict__ rank,
                      int32_t* __restrict__ tile_hist, float* __restrict__ tile_P, float* __restrict__ tile_Z,
                      float* __restrict__ logits, float* __restrict__ probs, uint32_t* err, float2* __restrict__ xms,
                      int* __restrict__ xam, uint32_t* __restrict__ xflag, uint32_t* __restrict__ xctl) {
-  using Cf = RtCfg<EC, NAX>;
+  constexpr bool GX = XM >= 1, P2 = XM == 2;
+  static_assert(!P2 || EC == 256, "CTA pairs split 256-row W boxes");
+  using Cf = RtCfg<EC, NAX, P2>;
   using Gm = RtGeom<EC>;
   constexpr int XS = Cf::XS, WS = Cf::WS, NBUF = Gm::NBUF;
   extern __shared__ uint8_t smem_raw[];
@@ -219,10 +232,13 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 
   // work items: (clusters) the tiles of this cluster, slice fixed by the cluster rank;
   // (global) tile it / Q, slice it % Q
+  // (pairs) tile 2 (it / Q) + rank, slice it % Q
   const int qc = (!GX && Q > 1) ? (int)cluster_ctarank() : 0;
-  const int it0 = GX ? (int)blockIdx.x : (int)blockIdx.x / Q;
-  const int istep = GX ? (int)gridDim.x : (int)gridDim.x / Q;
-  const int n_items = GX ? total_tiles * Q : total_tiles;
+  const int prk = P2 ? (int)cluster_ctarank() : 0;
+  const bool issuer = prk == 0;  // (pairs) the even CTA issues the MMAs and arms the full barriers
+  const int it0 = P2 ? (int)blockIdx.x / 2 : GX ? (int)blockIdx.x : (int)blockIdx.x / Q;
+  const int istep = P2 ? (int)gridDim.x / 2 : GX ? (int)gridDim.x : (int)gridDim.x / Q;
+  const int n_items = P2 ? (total_tiles + 1) / 2 * Q : GX ? total_tiles * Q : total_tiles;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int NK = (d + RT_BK - 1) / RT_BK;  // atoms along K
   const int NXS = (NK + NAX - 1) / NAX;    // x stages per tile
@@ -238,7 +254,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.afull[i], 1);
-      mbar_init(&bar.aempty[i], RT_EPI_WARPS);
+      mbar_init(&bar.aempty[i], P2 ? 2 * RT_EPI_WARPS : RT_EPI_WARPS);  // (pairs) both CTAs' epilogues
     }
     mbar_init(&bar.rfull, 1);  // the leader's expect_tx; the peers' stores complete its bytes
     mbar_init(&bar.rfree, (uint32_t)Q);
@@ -246,16 +262,21 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     bar.abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
-    prefetch_tmap(&tmW);
+    prefetch_tmap(P2 ? &tmWh : &tmW);
   }
   if (warp == 1) {
-    tmem_alloc(&bar.tmem_slot, Gm::TMEM_COLS);
-    tmem_relinquish();
+    if (P2) {
+      tmem_alloc_pair(&bar.tmem_slot, Gm::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bar.tmem_slot, Gm::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (!GX && Q > 1) cluster_sync();  // every peer's barriers are initialised before any remote arrival
+  if ((!GX && Q > 1) || P2) cluster_sync();  // every peer's barriers are initialised before any remote arrival
   const uint32_t tmem = bar.tmem_slot;
   // (global) this launch's flag value; no CTA advances xctl[0] before every CTA has read it
   const uint32_t epoch = GX ? __ldcg(xctl) + 1u : 0u;
@@ -276,18 +297,26 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       uint32_t xi = 0, wi = 0;
       bool ok = true;
       for (int it = it0; it < n_items && ok; it += istep) {
-        const int tid = GX ? it / Q : it, q = GX ? it - tid * Q : qc;
+        const int q = GX ? it % Q : qc;
+        const int tid = P2 ? 2 * (it / Q) + prk : GX ? it / Q : it;
         const int g = tid / nT, tile = tid - g * nT;
-        const int row0 = g * T + tile * RT_BM;
+        const int row0 = g * T + tile * RT_BM;  // past the last tile: rows past N, read as zeros
         for (int xs = 0; xs < NXS && ok; ++xs) {
           if (bar.abort_flag) { ok = false; break; }
           const int slot = (int)(xi % XS);
           if (xi >= (uint32_t)XS && !mbar_wait(&bar.xempty[slot], ((xi / XS) - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bar.xfull[slot], (uint32_t)Cf::X_STAGE);
-          if (NAX == 2)  // one 3-D box: two atoms of 128 rows (past d: zeros, never used)
+          if (issuer) mbar_arrive_expect_tx(&bar.xfull[slot], (uint32_t)(P2 ? 2 * Cf::X_STAGE : Cf::X_STAGE));
+          if (P2) {  // counted on the even CTA's barrier
+            const uint32_t xb = dsmem_addr(&bar.xfull[slot], 0);
+            if (NAX == 2)
+              tma_load_3d_pair(xring + slot * Cf::X_STAGE, &tmX, xb, 0, row0, xs * 2);
+            else
+              tma_load_2d_pair(xring + slot * Cf::X_STAGE, &tmX, xb, xs * RT_BK, row0);
+          } else if (NAX == 2) {  // one 3-D box: two atoms of 128 rows (past d: zeros, never used)
             tma_load_3d(xring + slot * Cf::X_STAGE, &tmX, &bar.xfull[slot], 0, row0, xs * 2);
-          else
+          } else {
             tma_load_2d(xring + slot * Cf::X_STAGE, &tmX, &bar.xfull[slot], xs * RT_BK, row0);
+          }
           ++xi;
           for (int at = 0; at < NAX && ok; ++at) {
             const int k = xs * NAX + at;
@@ -295,8 +324,13 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
             for (int b = 0; b < Gm::WBOXES; ++b) {
               const int ws = (int)(wi % WS);
               if (wi >= (uint32_t)WS && !mbar_wait(&bar.wempty[ws], ((wi / WS) - 1) & 1)) { ok = false; break; }
-              mbar_arrive_expect_tx(&bar.wfull[ws], (uint32_t)Gm::W_BOX);
-              tma_load_2d(wring + ws * Gm::W_BOX, &tmW, &bar.wfull[ws], 0, (q * NK + k) * Gm::WROWS + b * Gm::MMA_N);
+              const int wrow = (q * NK + k) * Gm::WROWS + b * Gm::MMA_N;
+              if (issuer) mbar_arrive_expect_tx(&bar.wfull[ws], (uint32_t)Gm::W_BOX);  // (pairs) both halves
+              if (P2)  // this CTA's half of the box's rows
+                tma_load_2d_pair(wring + ws * Cf::WB, &tmWh, dsmem_addr(&bar.wfull[ws], 0), 0,
+                                 wrow + prk * (Gm::MMA_N / 2));
+              else
+                tma_load_2d(wring + ws * Cf::WB, &tmW, &bar.wfull[ws], 0, wrow);
               ++wi;
             }
           }
@@ -306,17 +340,19 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         raise_error(err, ERR_TIMEOUT);
         bar.abort_flag = 1;
       }
-      // Drain: every copy started here has landed before the CTA can leave.
+      // Drain: every copy started here has landed before the CTA can leave.  (Pairs: the
+      // copies count on the even CTA's barriers; the MMAs' release of each slot, which
+      // arrives on this CTA's barriers, follows them, and no arrival is left in flight.)
       for (uint32_t i = xi > (uint32_t)XS ? xi - XS : 0; i < xi; ++i)
-        if (!mbar_wait(&bar.xfull[i % XS], (i / XS) & 1)) raise_error(err, ERR_TIMEOUT);
+        if (!mbar_wait(P2 ? &bar.xempty[i % XS] : &bar.xfull[i % XS], (i / XS) & 1)) raise_error(err, ERR_TIMEOUT);
       for (uint32_t i = wi > (uint32_t)WS ? wi - WS : 0; i < wi; ++i)
-        if (!mbar_wait(&bar.wfull[i % WS], (i / WS) & 1)) raise_error(err, ERR_TIMEOUT);
+        if (!mbar_wait(P2 ? &bar.wempty[i % WS] : &bar.wfull[i % WS], (i / WS) & 1)) raise_error(err, ERR_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(RT_BM, Gm::MMA_N);
+    if (lane == 0 && issuer) {
+      // ---------------- MMA issuer (pairs: the even CTA, M = 256 over both CTAs' tokens)
+      constexpr uint32_t idesc = idesc_bf16_f32(P2 ? 2 * RT_BM : RT_BM, Gm::MMA_N);
       uint32_t xi = 0, wi = 0;
       int lt = 0;
       bool ok = true;
@@ -340,29 +376,48 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
               const int ws = (int)(wi % WS);
               if (!mbar_wait(&bar.wfull[ws], (wi / WS) & 1)) { ok = false; break; }
               tc_fence_after();
-              const uint32_t wa = smem_u32(wring + ws * Gm::W_BOX);
+              const uint32_t wa = smem_u32(wring + ws * Cf::WB);
 #pragma unroll
               for (int kk = 0; kk < RT_BK / 16; ++kk) {
                 const bool first = k == 0 && kk == 0 && !(EC == 256 && b == 2);
-                tc_mma_bf16(acc + Gm::dcol(b), sw128_kmajor_desc(xa + kk * 32), sw128_kmajor_desc(wa + kk * 32),
-                            idesc, first ? 0u : 1u);
+                if (P2)
+                  tc_mma_bf16_pair(acc + Gm::dcol(b), sw128_kmajor_desc(xa + kk * 32),
+                                   sw128_kmajor_desc(wa + kk * 32), idesc, first ? 0u : 1u);
+                else
+                  tc_mma_bf16(acc + Gm::dcol(b), sw128_kmajor_desc(xa + kk * 32), sw128_kmajor_desc(wa + kk * 32),
+                              idesc, first ? 0u : 1u);
               }
-              tc_commit(&bar.wempty[ws]);
+              if (P2)
+                tc_commit_pair(&bar.wempty[ws], (uint16_t)3u);
+              else
+                tc_commit(&bar.wempty[ws]);
               ++wi;
             }
           }
-          tc_commit(&bar.xempty[slot]);
+          if (P2)
+            tc_commit_pair(&bar.xempty[slot], (uint16_t)3u);
+          else
+            tc_commit(&bar.xempty[slot]);
           ++xi;
         }
-        tc_commit(&bar.afull[buf]);  // arrives once every MMA of the tile has completed
+        if (P2)
+          tc_commit_pair(&bar.afull[buf], (uint16_t)3u);
+        else
+          tc_commit(&bar.afull[buf]);  // arrives once every MMA of the tile has completed
       }
       if (!ok) {
         raise_error(err, ERR_TIMEOUT);
         bar.abort_flag = 1;
       }
       // every MMA issued above has completed before TMEM can be freed
-      tc_commit(&bar.drain);
+      if (P2)
+        tc_commit_pair(&bar.drain, (uint16_t)1u);
+      else
+        tc_commit(&bar.drain);
       if (!mbar_wait(&bar.drain, 0)) raise_error(err, ERR_TIMEOUT);
+      // (pairs) the last item's releases from the odd CTA have arrived before this CTA leaves
+      if (P2 && ok && lt >= 1 && !mbar_wait(&bar.aempty[(lt - 1) % NBUF], ((lt - 1) / NBUF) & 1))
+        raise_error(err, ERR_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -380,7 +435,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     int lt = 0;
     for (int it = it0; it < n_items; it += istep, ++lt) {
       const int buf = lt % NBUF;
-      const int tid = GX ? it / Q : it, q = GX ? it - tid * Q : qc;
+      const int q = GX ? it % Q : qc;
+      const int tid = P2 ? 2 * (it / Q) + prk : GX ? it / Q : it;
       const int e0 = q * EC;
       const int g = tid / nT, tile = tid - g * nT;
       const int t0 = tile * RT_BM;
@@ -404,6 +460,13 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       rt_epi_sync();
       if (!bar.ep_ok) break;
       tc_fence_after();
+      if (P2 && tid >= total_tiles) {  // the pair's second tile past the last one: release only
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(&bar.aempty[buf], 0u);
+        rt_epi_sync();  // every thread has read ep_ok before the leader writes it again
+        continue;
+      }
 
       // pass 1: logits z (+ bias) into registers; max / argmax over this warp's columns
       // (increasing e with strict >, so the lowest index wins a tie)
@@ -448,7 +511,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       // the accumulator set is read: the next tile's MMAs may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.aempty[buf]);
+      if (lane == 0) {
+        if (P2)  // on the even CTA's barrier (its own arrival is local)
+          mbar_arrive_remote(&bar.aempty[buf], 0u);
+        else
+          mbar_arrive(&bar.aempty[buf]);
+      }
 
       if (has_cols) {
         sh.red_m[cg][i] = m;
@@ -646,7 +714,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (!GX && Q > 1) cluster_sync();  // no peer reads this CTA's shared memory or arrives on its barriers any more
+  if ((!GX && Q > 1) || P2) cluster_sync();  // no peer reads this CTA's shared memory or arrives on its barriers any more
   if (GX && threadIdx.x == 0) {  // the last CTA to finish advances the epoch for the next launch
     __threadfence();
     if (atomicAdd(xctl + 1, 1u) == gridDim.x - 1) {
@@ -655,17 +723,22 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       st_release_gpu(xctl, epoch);
     }
   }
-  if (warp == 1) tmem_dealloc(tmem, Gm::TMEM_COLS);
+  if (warp == 1) {
+    if (P2)
+      tmem_dealloc_pair(tmem, Gm::TMEM_COLS);
+    else
+      tmem_dealloc(tmem, Gm::TMEM_COLS);
+  }
 }
 
 // ---------------------------------------------------------------- host side
-// CTAs of router_tc_kernel<EC, NAX, GX> resident at once in clusters of cl CTAs (cached per
+// CTAs of router_tc_kernel<EC, NAX, XM> resident at once in clusters of cl CTAs (cached per
 // kernel, device and cluster size).
-template <int EC, int NAX, bool GX>
+template <int EC, int NAX, int XM>
 static int rt_fit(int cl) {
   static int cache[64][9] = {};
-  auto kern = router_tc_kernel<EC, NAX, GX>;
-  constexpr int smem = rt_smem_bytes<EC, NAX>();
+  auto kern = router_tc_kernel<EC, NAX, XM>;
+  constexpr int smem = rt_smem_bytes<EC, NAX, XM == 2>();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
   const bool cached = dev >= 0 && dev < 64 && cl >= 1 && cl <= 8;
@@ -734,45 +807,83 @@ static RtXchg rt_xchg(void* base, long long tiles, int Q) {
   return x;
 }
 
+template <int EC, int NAX, int XM>
+static cudaError_t rt_launch(int grid, int cluster, bool coop, bool pdl, cudaStream_t s, const CUtensorMap& tmX,
+                             const CUtensorMap& tmW, const CUtensorMap& tmWh, const RouteArgs& a, int nT, int Q,
+                             int total, int32_t* rank, const RtXchg& x) {
+  auto kern = router_tc_kernel<EC, NAX, XM>;
+  constexpr int smem = rt_smem_bytes<EC, NAX, XM == 2>();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(RT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[3];
+  unsigned n = 0;
+  if (coop) {  // the CTAs wait on one another's exchange flags: all must be resident
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, tmWh, a.br, a.T, a.E, a.d, nT, Q, total, a.expert, a.gate, rank,
+                            a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs, a.err, x.ms, x.am, x.flag, x.ctl);
+}
+
+// CTA pairs need a cooperative launch of 2-CTA clusters; a device that refuses it gets the
+// one-CTA global variant from then on.
+static bool g_rt_pair_refused[64] = {};
+
 template <int EC, int NAX>
-static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const RouteArgs& a, int nT, int Q,
-                     int32_t* rank, cudaStream_t s) {
+static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmWh, const RouteArgs& a,
+                     int nT, int Q, int32_t* rank, cudaStream_t s) {
   const long long total = (long long)a.G * nT;
   if (total * Q >= (1ll << 31)) return -1;
   if (a.xchg && rt_global(a.E)) {
-    // cooperative grid: the CTAs wait on one another's exchange flags, so all must be resident
-    auto kern = router_tc_kernel<EC, NAX, true>;
-    constexpr int smem = rt_smem_bytes<EC, NAX>();
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-    const int fit = rt_fit<EC, NAX, true>(1);
-    const long long items = total * Q;
-    const int grid = (int)(items < fit ? items : fit);
     const RtXchg x = rt_xchg(a.xchg, total, Q);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(RT_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeCooperative;
-    attr.val.cooperative = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, (int)total, a.expert,
-                                             a.gate, rank, a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs,
-                                             a.err, x.ms, x.am, x.flag, x.ctl);
-    return e == cudaSuccess ? 1 : -1;
+    if constexpr (EC == 256) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+      if (total >= 2 && !(dev >= 0 && dev < 64 && g_rt_pair_refused[dev])) {
+        const long long pitems = (total + 1) / 2 * Q;
+        const int fit = rt_fit<EC, NAX, 2>(2) / 2;
+        const int pairs = (int)(pitems < fit ? pitems : fit);
+        if (rt_launch<EC, NAX, 2>(2 * pairs, 2, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank, x) ==
+            cudaSuccess)
+          return 1;
+        cudaGetLastError();
+        if (dev >= 0 && dev < 64) g_rt_pair_refused[dev] = true;
+      }
+    }
+    const long long items = total * Q;
+    const int fit = rt_fit<EC, NAX, 1>(1);
+    const int grid = (int)(items < fit ? items : fit);
+    return rt_launch<EC, NAX, 1>(grid, 1, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank, x) ==
+                   cudaSuccess
+               ? 1
+               : -1;
   }
-  auto kern = router_tc_kernel<EC, NAX, false>;
-  constexpr int smem = rt_smem_bytes<EC, NAX>();
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-  const int fit = rt_fit<EC, NAX, false>(Q) / Q;
+  const int fit = rt_fit<EC, NAX, 0>(Q) / Q;
   const int ncl = (int)(total < fit ? total : fit);
-  const cudaError_t e = launch_k(kern, dim3((unsigned)(Q * ncl), 1, 1), dim3(RT_THREADS, 1, 1), smem, s,
-                                 /*pdl=*/true, (unsigned)Q, tmX, tmW, a.br, a.T, a.E, a.d, nT, Q, (int)total, a.expert,
-                                 a.gate, rank, a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs, a.err,
-                                 (float2*)nullptr, (int*)nullptr, (uint32_t*)nullptr, (uint32_t*)nullptr);
-  return e == cudaSuccess ? 1 : -1;
+  return rt_launch<EC, NAX, 0>(Q * ncl, Q, false, true, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank, RtXchg{}) ==
+                 cudaSuccess
+             ? 1
+             : -1;
 }
 
 // Experts per CTA: the smallest power of two >= 16 that keeps the cluster at <= 8
@@ -821,7 +932,7 @@ int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
     ++launches;
   }
   const int nax = a.d % (2 * RT_BK) == 0 ? 2 : 1;  // x stages of two atoms (256 B per row) when d allows
-  CUtensorMap tmX, tmW;
+  CUtensorMap tmX, tmW, tmWh;
   if (nax == 2) {
     if (!encode_bf16_3d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM, 2u)) return -1;
   } else if (!encode_bf16_2d(&tmX, a.x, (uint64_t)N, (uint64_t)a.d, RT_BM)) {
@@ -829,8 +940,11 @@ int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s) {
   }
   if (!encode_bf16_2d(&tmW, a.wsplit, (uint64_t)3 * Q * EC * NK, (uint64_t)RT_BK, (uint32_t)router_tc_mma_n(EC)))
     return -1;
+  tmWh = tmW;  // half boxes (CTA pairs split each W box's rows)
+  if (EC == 256 && !encode_bf16_2d(&tmWh, a.wsplit, (uint64_t)3 * Q * EC * NK, (uint64_t)RT_BK, 128u)) return -1;
   int n2;
-#define SMOE_RT(ECV) n2 = nax == 2 ? launch_rt<ECV, 2>(tmX, tmW, a, nT, Q, rank, s) : launch_rt<ECV, 1>(tmX, tmW, a, nT, Q, rank, s)
+#define SMOE_RT(ECV) \
+  n2 = nax == 2 ? launch_rt<ECV, 2>(tmX, tmW, tmWh, a, nT, Q, rank, s) : launch_rt<ECV, 1>(tmX, tmW, tmWh, a, nT, Q, rank, s)
   switch (EC) {
     case 16: SMOE_RT(16); break;
     case 32: SMOE_RT(32); break;

@@ -66,11 +66,17 @@ SMALL = {
                       dict(expert_bias_std=0.05, router_bias_std=0.3)),
     # d = 192: three 64-column atoms, so the router's last two-atom stage has a zero-filled half
     "odd-atoms": (LayerShape("odd-atoms", 2, 260, 192, 256, 12, 1.0), dict(router_bias_std=0.1)),
-    # 512 experts over 8 slices of 64 (34 tiles x 8 = 272 router items, more than one per SM):
-    # the slices of a tile meet in global memory, some tiles straddle two rounds of the grid
+    # router slices meeting in global memory.  200 experts: 4 slices of 64
+    "gx-e200": (LayerShape("gx-e200", 1, 900, 128, 128, 200, 1.0), dict(router_bias_std=0.1)),
+    # 512 experts: 8 slices of 64 over 34 tiles (272 items, more than one per SM; some tiles'
+    # slices straddle two rounds of the grid)
     "gx-rounds": (LayerShape("gx-rounds", 2, 2100, 128, 128, 512, 1.0), dict(router_bias_std=0.1)),
-    # an odd number of tiles (5) over 5 slices of 128 experts, fewer items than SMs
+    # an odd number of tiles (5) over 5 slices of 128 experts
     "gx-odd-tiles": (LayerShape("gx-odd-tiles", 1, 600, 128, 128, 640, 1.0), {}),
+    # 1536 experts (6 slices of 256) over 42 tiles: CTA pairs, 126 pair items
+    "gx-e1536": (LayerShape("gx-e1536", 1, 5300, 128, 128, 1536, 1.0), dict(router_bias_std=0.1)),
+    # 1100 experts (5 slices of 256) over 5 tiles: the last pair's second tile is past the end
+    "gx-pair-odd": (LayerShape("gx-pair-odd", 1, 600, 128, 128, 1100, 1.0), {}),
     # float32 rows of 49,408 bytes: too wide for the shared-memory row slots of the bulk-copy
     # dispatch and combine, so their register kernels run
     "wide-rows": (LayerShape("wide-rows", 1, 40, 12352, 32, 4, 1.0, dtype="f32"), dict(expert_bias_std=0.05)),
