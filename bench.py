@@ -340,8 +340,9 @@ def run_train(args, shape):
                       "unit": "GB/s", "frac": gbs / hbm, "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
                       "algorithmic_bytes": bwd_bytes, "traffic": None,
                       "tensor": {"achieved_tflops": tf, "peak_tflops": tc_burst, "frac": tf / tc_burst},
-                      "note": "the backward moves ~3.6 GB at switch-base (weights in, float32 weight gradients "
-                              "out) for 0.07 TFLOP: bytes bind it; all its products run on the tensor cores"}
+                      "note": f"the backward moves {bwd_bytes / 1e9:.2f} GB (weights in, float32 weight "
+                              f"gradients out) for {bwd_flops / 1e12:.2f} TFLOP; all its products run on the "
+                              "tensor cores"}
                      if tc_shapes else
                      {"bound": "alu", "kernel": "bgemm_kernel (backward products)", "achieved": tf,
                       "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS,
