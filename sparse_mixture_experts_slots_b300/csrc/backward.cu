@@ -193,6 +193,60 @@ __global__ void __launch_bounds__(256) colsum_rows_kernel(const TI* __restrict__
   out[k] = s;
 }
 
+// The same sums with 8 row groups per block and 16-byte column vectors: thread (g, v) of a
+// block adds rows g, g + 8, ... of V consecutive columns; the 8 groups' partials are then
+// added in group order (fixed order).  Needs W % V == 0 and 16-byte aligned rows.
+template <typename TI>
+__global__ void __launch_bounds__(256) colsum_rows_vec_kernel(const TI* __restrict__ in, const int32_t* __restrict__ rows,
+                                                              float* __restrict__ out, int E, int R, int W) {
+  constexpr int V = 16 / sizeof(TI);
+  __shared__ float part[8][32 * V];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int e = blockIdx.y;
+  const int v = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const long long c0 = ((long long)blockIdx.x * 32 + v) * V;
+  const int n = rows ? min(R, rows[e]) : R;
+  float acc[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) acc[j] = 0.f;
+  if (c0 < W) {
+    const TI* src = in + (long long)e * R * W + c0;
+#pragma unroll 4
+    for (int r = g; r < n; r += 8) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * W));
+      const TI* t = reinterpret_cast<const TI*>(&q);
+#pragma unroll
+      for (int j = 0; j < V; ++j) acc[j] += to_f<TI>(t[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < V; ++j) part[g][v * V + j] = acc[j];
+  __syncthreads();
+  for (int k = threadIdx.x; k < 32 * V; k += blockDim.x) {
+    const long long c = (long long)blockIdx.x * 32 * V + k;
+    if (c >= W) continue;
+    float t = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) t += part[q][k];
+    out[(long long)e * W + c] = t;
+  }
+}
+
+// out[e, c] = sum_{r < rows[e]} in[e, r, c]: the vector kernel when the rows allow it.
+template <typename TI>
+static cudaError_t launch_colsum_rows(const TI* in, const int32_t* rows, float* out, int E, int R, int W,
+                                      cudaStream_t s) {
+  constexpr int V = 16 / sizeof(TI);
+  if (W % V == 0 && (reinterpret_cast<uintptr_t>(in) & 15u) == 0) {
+    const long long bx = ((long long)W + 32 * V - 1) / (32 * V);
+    return launch_k(colsum_rows_vec_kernel<TI>, dim3((unsigned)bx, (unsigned)E), dim3(256), 0, s, false, 1, in, rows,
+                    out, E, R, W);
+  }
+  return launch_k(colsum_rows_kernel<TI>, dim3((unsigned)(((long long)E * W + 255) / 256)), dim3(256), 0, s, false, 1,
+                  in, rows, out, E, R, W);
+}
+
 // ---------------------------------------------------------------- router backward
 // Warp per token: p from the logits, dp = onehot(e*) dg + w_aux alpha E f / (G T), the
 // softmax Jacobian, plus the z-loss term; writes dz [N, E].
@@ -293,8 +347,10 @@ __global__ void __launch_bounds__(256) colsum_split_kernel(const float* __restri
   part[(long long)sidx * W + c] = acc;
 }
 
-// Rows r >= rows[e] of every expert block of up to three bfloat16 buffers [E, R, w_k] are
-// set to zero: warp per (expert, row), 16-byte stores (w_k % 8 == 0).
+// Rows from rows[e] to the end of its last 64-row atom (rows 0 .. 63 when rows[e] = 0) of
+// every expert block of up to three bfloat16 buffers [E, R, w_k] are set to zero: the
+// weight-gradient products read whole atoms up to there.  Warp per (expert, row), 16-byte
+// stores (w_k % 8 == 0).
 __global__ void __launch_bounds__(256) zero_tail_rows_kernel(const int32_t* __restrict__ rows, int E, int R,
                                                              __nv_bfloat16* a, int wa, __nv_bfloat16* b, int wb,
                                                              __nv_bfloat16* c, int wc) {
@@ -302,7 +358,8 @@ __global__ void __launch_bounds__(256) zero_tail_rows_kernel(const int32_t* __re
   const int lane = threadIdx.x % 32;
   if (w >= (long long)E * R) return;
   const int e = (int)(w / R), r = (int)(w % R);
-  if (r < rows[e]) return;
+  const int n = rows[e];
+  if (r < n || r >= 64 * max(1, (n + 63) / 64)) return;  // only the rest of the last 64-row atom
   const uint4 zero = make_uint4(0, 0, 0, 0);
   __nv_bfloat16* bufs[3] = {a, b, c};
   const int widths[3] = {wa, wb, wc};
@@ -374,7 +431,8 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
     if (R > 0) {
       BW_STEP(launch_ffn_tc(L, s, false));
       // dW2_e = dye^T h and dW1_e = dh^T xe: the contraction axis is an expert's rows, read
-      // MN-major from [E, R, .] (rows past R read as zero, past the count zeroed above);
+      // MN-major from [E, R, .] (only the atoms holding the expert's rows; the rest of the
+      // last one zeroed above);
       // float32 results straight into dW2 [E, d, F] and dW1 [E, F, d]
       fill_i32_kernel<<<(E + 255) / 256, 256, 0, s>>>(a.rows_d, E, d);
       fill_i32_kernel<<<(E + 255) / 256, 256, 0, s>>>(a.rows_F, E, F);
@@ -389,6 +447,7 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
         M.W2 = M.W1;
         M.xe = wgt == 0 ? (const void*)a.dye16 : (const void*)a.dh16;  // B: tokens
         M.expert_rows = wgt == 0 ? a.rows_d : a.rows_F;
+        M.kcount = a.expert_rows;            // contraction: only the atoms holding the expert's rows
         M.combine = false;
         M.mode = 2;
         M.counters = a.counters2;
@@ -446,16 +505,13 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
   }
   // bias gradients
   if (a.db2)
-    BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)(((long long)E * d + 255) / 256)), dim3(256), 0, s,
-                     false, 1, (const float*)a.dye, a.expert_rows, a.db2, E, R, d) == cudaSuccess ? 1 : -1);
+    BW_STEP(launch_colsum_rows<float>((const float*)a.dye, a.expert_rows, a.db2, E, R, d, s) == cudaSuccess ? 1 : -1);
   if (a.db1) {
     if (tc)
-      BW_STEP(launch_k(colsum_rows_kernel<__nv_bfloat16>, dim3((unsigned)(((long long)E * F + 255) / 256)), dim3(256),
-                       0, s, false, 1, (const __nv_bfloat16*)a.dh16, a.expert_rows, a.db1, E, R, F) == cudaSuccess
+      BW_STEP(launch_colsum_rows<__nv_bfloat16>((const __nv_bfloat16*)a.dh16, a.expert_rows, a.db1, E, R, F, s) == cudaSuccess
                   ? 1 : -1);
     else
-      BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)(((long long)E * F + 255) / 256)), dim3(256), 0, s,
-                       false, 1, (const float*)a.dh, a.expert_rows, a.db1, E, R, F) == cudaSuccess ? 1 : -1);
+      BW_STEP(launch_colsum_rows<float>((const float*)a.dh, a.expert_rows, a.db1, E, R, F, s) == cudaSuccess ? 1 : -1);
   }
   if (N == 0) {  // no tokens: the router's gradients are zero
     if (cudaMemsetAsync(a.dWr, 0, (size_t)E * d * sizeof(float), s) != cudaSuccess) return -1;
@@ -494,8 +550,7 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
       M.krows = a.kc;
       M.out_f32 = a.part;
       BW_STEP(launch_ffn_tc(M, s, false));
-      BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)(((long long)E * d + 255) / 256)), dim3(256), 0, s,
-                       false, 1, (const float*)a.part, (const int32_t*)nullptr, a.dWr, 1, 2 * a.ntc, E * d) ==
+      BW_STEP(launch_colsum_rows<float>((const float*)a.part, (const int32_t*)nullptr, a.dWr, 1, 2 * a.ntc, E * d, s) ==
                       cudaSuccess ? 1 : -1);
       // dx = dz W_r: the product over 3E of dzp [N, 3E] (K-major rows) and Wp [3E, d] (as
       // stored, MN-major), float32 results straight into dx
@@ -525,8 +580,7 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
       g.sBb = (long long)kc * d; g.sBj = 1; g.sBk = d;
       g.sCb = (long long)E * d; g.sCi = d; g.sCj = 1;
       BW_STEP((launch_bg<float, T, float, 0, false>(a.dz, x, a.part, nullptr, g, ns, s)));
-      BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)(((long long)E * d + 255) / 256)), dim3(256), 0, s,
-                       false, 1, (const float*)a.part, (const int32_t*)nullptr, a.dWr, 1, ns, E * d) == cudaSuccess
+      BW_STEP(launch_colsum_rows<float>((const float*)a.part, (const int32_t*)nullptr, a.dWr, 1, ns, E * d, s) == cudaSuccess
                   ? 1 : -1);
     }
     if (a.dbr) {  // dbr = sum_t dz_t, split over token chunks, then the chunks' sum in order
@@ -535,8 +589,7 @@ static int run_backward(const BackwardArgs& a, cudaStream_t s) {
       colsum_split_kernel<<<dim3((unsigned)((E + 255) / 256), (unsigned)ns), 256, 0, s>>>(a.dz, a.part, N, E, kc);
       if (cudaGetLastError() != cudaSuccess) return -1;
       ++n;
-      BW_STEP(launch_k(colsum_rows_kernel<float>, dim3((unsigned)((E + 255) / 256)), dim3(256), 0, s, false, 1,
-                       (const float*)a.part, (const int32_t*)nullptr, a.dbr, 1, ns, E) == cudaSuccess ? 1 : -1);
+      BW_STEP(launch_colsum_rows<float>((const float*)a.part, (const int32_t*)nullptr, a.dbr, 1, ns, E, s) == cudaSuccess ? 1 : -1);
     }
     if (!tc_router) {  // dx = dz Wr: i = t, j = c, k = e
       BgemmArgs g{};

@@ -66,6 +66,8 @@ struct FfnParams {
   int layer2;                    // 0: layer-1 tiles only (a weight gradient)
   int stall;                     // test only: tile (layer 1, expert 0, block 0, chunk 0) never publishes
   float* out_f32;                // MODE 2: the float32 result [E * R, F] (R: tokens, F: features)
+  const int32_t* kcount;         // MODE 2 (or null): rows of expert e on the contraction axis; only
+                                 // their 64-row atoms are read (at least one, zero past the count)
 };
 
 struct FfTile {
@@ -130,6 +132,15 @@ struct FfShared {
 static_assert(offsetof(FfShared, xpose) % 16 == 0, "16-byte vector reads of the transpose buffer");
 static_assert(sizeof(FfShared::xpose) >= 8 * FF_EPW * 16 * 32 * sizeof(float) / 2,
               "the float32 staging of one weight block's epilogue warps fits in the transpose buffer");
+
+// 64-column atoms of the contraction axis a tile of expert e reads: all of K, or (MODE 2
+// with per-expert row counts) the atoms that hold the expert's rows, at least one.
+template <int MODE>
+__device__ __forceinline__ int ff_atoms(const FfnParams& p, int e, int K) {
+  if (MODE != 2 || !p.kcount) return K / FF_BK;
+  const int n = min(max(p.kcount[e], 0), K);
+  return max(1, (n + FF_BK - 1) / FF_BK);
+}
 
 template <int MB>
 __device__ __forceinline__ void epi_sync() {  // named barrier over the epilogue warps
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       const int M = l1 ? p.F : p.d;
       const int arow = tl.e * M + tl.mt * FF_BM * MB;
       const int brow = tl.e * p.R + tl.nc * BN;
-      const int atoms = K / FF_BK;
+      const int atoms = ff_atoms<MODE>(p, tl.e, K);
       bool ok = true;
       for (int a0 = 0; a0 < atoms; a0 += NA) {
         const int slot = (int)(gst % (uint32_t)STAGES);
@@ -318,7 +329,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         break;
       }
       tc_fence_after();
-      const int atoms = (tv.x == 0 ? p.d : p.F) / FF_BK;
+      const int atoms = ff_atoms<MODE>(p, tv.y, tv.x == 0 ? p.d : p.F);
       const uint32_t acc = tmem + (uint32_t)(buf * ACC);
       bool ok = true;
       for (int a0 = 0; a0 < atoms; a0 += NA) {
@@ -763,6 +774,7 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.layer2 = L.mode >= 2 ? 0 : 1;
   p.stall = L.stall ? 1 : 0;
   p.out_f32 = L.out_f32;
+  p.kcount = L.mode == 2 ? L.kcount : nullptr;
   if (L.mode >= 2 && !L.out_f32) return -1;
   if (L.mode == 2 && t.BN % 64 != 0) return -1;
   p.w_evict_first = t.NCH == 1 ? 1 : 0;  // several chunks re-read a weight tile

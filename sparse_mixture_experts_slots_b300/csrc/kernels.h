@@ -218,6 +218,9 @@ struct FfnLaunch {
   int krows;                 // mode 2: rows per expert of W1 / xe (the contraction axis)
   int bcols;                 // mode 2: row length of xe in elements when it is wider than R (else 0)
   float* out_f32;            // modes 2 and 3 output
+  const int32_t* kcount;     // mode 2 (or null): rows of each expert on the contraction axis; only the
+                             // 64-row atoms holding them are read (rows past the count in the last
+                             // one must be zero; an expert with none reads one atom of zeros)
                              // mode 3: out_f32[E * R, F] = sum_k W1[e, k, f] xe[e * R + n, k] (W1 as
                              // stored [E, d, F], xe K-major rows [E * R, d]; layer 1 only)
   uint32_t* counters;        // ffn_counter_words(E, R) words, zero at launch
