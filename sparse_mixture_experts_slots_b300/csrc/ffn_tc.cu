@@ -165,7 +165,16 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // MODE 3, a plain product out[n, m] = sum_k A[k, m] B[n, k]: A MN-major as stored (3-D map,
 // like MODE 1's weights), B K-major rows (like the forward's tokens); layer 1 only, float32
 // results as in MODE 2.
-template <int MB, int NBUF, int MODE>
+// PAIR (MODE 0; clusters of 2): a tile is 2 MB 128-row weight blocks (p.MB = 2 MB for the
+// ticket order) against one token chunk, MB blocks per CTA.  The even CTA takes the tickets
+// and publishes every tile to both CTAs' queues; each CTA loads its weight blocks and half
+// of the chunk's token rows; the even CTA issues tcgen05 cta_group::2 MMAs (M = 256: a
+// block of each CTA against all N tokens, N / 2 token rows from each CTA's shared memory),
+// whose completions arrive on both CTAs' barriers; each CTA's epilogue writes its blocks'
+// features, the odd CTA releasing the accumulator and the queue entry on the even CTA's
+// barriers.  Per SM the token rows a tile streams are halved.  The library runs MB = 2,
+// NBUF = 1 (four blocks per tile); MB = 1, NBUF = 2 measured no faster.
+template <int MB, int NBUF, int MODE, bool PAIR = false>
 __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     ffn_persistent_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
@@ -175,7 +184,12 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   FfShared& sh = *reinterpret_cast<FfShared*>(ring + FF_RING);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  static_assert(!PAIR || (MODE == 0 && ((MB == 1 && NBUF == 2) || (MB == 2 && NBUF == 1))),
+                "CTA pairs: the forward, one or two blocks per CTA");
   const int BN = p.BN, NA = p.NA, STAGES = p.STAGES;
+  const int BNC = PAIR ? BN / 2 : BN;  // token rows of a stage in this CTA's shared memory
+  const int prk = PAIR ? (int)cluster_ctarank() : 0;
+  const bool issuer = prk == 0;  // (pairs) the even CTA takes tickets and issues the MMAs
   const int ACC = MB * BN;  // TMEM columns of one accumulator set
   const int cols = NBUF * ACC;
   const uint32_t TMEM_COLS = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
@@ -187,11 +201,11 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     }
     for (int i = 0; i < FF_SCHED; ++i) {
       mbar_init(&sh.sfull[i], 1);
-      mbar_init(&sh.sempty[i], 2);  // the MMA issuer and the epilogue
+      mbar_init(&sh.sempty[i], PAIR ? 3 : 2);  // the MMA issuer and the epilogue (pairs: both epilogues)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.afull[i], 1);
-      mbar_init(&sh.aempty[i], 1);
+      mbar_init(&sh.aempty[i], PAIR ? 2 : 1);
     }
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -203,13 +217,20 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     prefetch_tmap(&tmHp);
   }
   if (warp == 1) {
-    tmem_alloc(&sh.tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(&sh.tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&sh.tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (PAIR) cluster_sync();  // both CTAs' barriers are initialised before any remote arrival or copy
   const uint32_t tmem = sh.tmem_slot;
+  // layer-1 tiles of an (expert, chunk); pairs count one per CTA and block
   const int MT1 = p.F / (FF_BM * MB);
   griddep_launch_dependents();  // after the TMEM allocation: a dependent grid cannot starve it
   griddep_wait();               // the dispatched rows, row counts and cleared counters
@@ -218,23 +239,51 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
     // ---------------- scheduler + TMA producer
     const uint64_t w_policy = policy_evict_first();  // used when a weight tile is read once
     uint32_t gst = 0;  // stages issued
-    int sidx = 0;      // queue entries published
+    int sidx = 0;      // queue entries published (pairs, odd CTA: received)
     while (true) {
       if (sh.abort_flag) break;
       FfTile tl;
-      const uint32_t t = atomicAdd(p.next_tile, 1u);
-      const bool has = ff_decode(t, p, tl);
-      const int nv = has ? min(BN, p.expert_rows[tl.e] - tl.nc * BN) : 0;
-      if (has && nv <= 0) continue;  // empty chunk
-      const int qs = sidx % FF_SCHED;
-      if (sidx >= FF_SCHED && !mbar_wait(&sh.sempty[qs], ((sidx / FF_SCHED) - 1) & 1)) {
-        raise_error(p.err, ERR_TIMEOUT);
-        sh.abort_flag = 1;
-        break;
+      bool has;
+      int nv;
+      if (issuer) {
+        const uint32_t t = atomicAdd(p.next_tile, 1u);
+        has = ff_decode(t, p, tl);
+        nv = has ? min(BN, p.expert_rows[tl.e] - tl.nc * BN) : 0;
+        if (has && nv <= 0) continue;  // empty chunk
+        const int qs = sidx % FF_SCHED;
+        if (sidx >= FF_SCHED && !mbar_wait(&sh.sempty[qs], ((sidx / FF_SCHED) - 1) & 1)) {
+          raise_error(p.err, ERR_TIMEOUT);
+          sh.abort_flag = 1;
+          break;
+        }
+        const int4 ent = has ? make_int4(tl.layer, tl.e, tl.mt, tl.nc) : make_int4(-1, 0, 0, 0);
+        sh.sched[qs] = ent;
+        sh.sched_nv[qs] = nv;
+        mbar_arrive(&sh.sfull[qs]);
+        if (PAIR) {  // the same entry in the odd CTA's queue, released with the arrival
+          const uint32_t q4 = dsmem_addr(&sh.sched[qs], 1u);
+          dsmem_st_s32(q4, ent.x);
+          dsmem_st_s32(q4 + 4, ent.y);
+          dsmem_st_s32(q4 + 8, ent.z);
+          dsmem_st_s32(q4 + 12, ent.w);
+          dsmem_st_s32(dsmem_addr(&sh.sched_nv[qs], 1u), nv);
+          mbar_arrive_remote(&sh.sfull[qs], 1u);
+        }
+      } else {  // (pairs, odd CTA) the even CTA's entry
+        const int qs = sidx % FF_SCHED;
+        if (!mbar_wait_cluster(&sh.sfull[qs], (sidx / FF_SCHED) & 1)) {
+          raise_error(p.err, ERR_TIMEOUT);
+          sh.abort_flag = 1;
+          break;
+        }
+        const int4 ent = sh.sched[qs];
+        has = ent.x >= 0;
+        tl.layer = ent.x;
+        tl.e = ent.y;
+        tl.mt = ent.z;
+        tl.nc = ent.w;
+        nv = sh.sched_nv[qs];
       }
-      sh.sched[qs] = has ? make_int4(tl.layer, tl.e, tl.mt, tl.nc) : make_int4(-1, 0, 0, 0);
-      sh.sched_nv[qs] = nv;
-      mbar_arrive(&sh.sfull[qs]);
       ++sidx;
       if (!has) break;
       const bool l1 = tl.layer == 0;
@@ -258,12 +307,15 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       // A chunk filled to at most BN - 64 rows loads its activations as 64-row boxes, only
       // as many as cover its rows (nbox = 0: one box of BN rows)
       const int nt = (nv + 15) & ~15;
-      const int nbox = (MODE != 2 && BN > FF_PB && nt <= BN - FF_PB) ? (nt + FF_PB - 1) / FF_PB : 0;
-      const uint32_t tx = nbox ? (uint32_t)(NA * MB * FF_ATOM_A + NA * nbox * FF_PB * FF_BK * 2) : (uint32_t)p.stage_bytes;
+      const int nbox = (!PAIR && MODE != 2 && BN > FF_PB && nt <= BN - FF_PB) ? (nt + FF_PB - 1) / FF_PB : 0;
+      // (pairs) the even CTA's barrier counts both CTAs' bytes
+      const uint32_t tx = nbox ? (uint32_t)(NA * MB * FF_ATOM_A + NA * nbox * FF_PB * FF_BK * 2)
+                               : (uint32_t)(PAIR ? 2 * p.stage_bytes : p.stage_bytes);
       const int K = l1 ? p.d : p.F;
       const int M = l1 ? p.F : p.d;
-      const int arow = tl.e * M + tl.mt * FF_BM * MB;
-      const int brow = tl.e * p.R + tl.nc * BN;
+      // (pairs) this CTA's weight block of the tile's two, and its half of the chunk's rows
+      const int arow = tl.e * M + (PAIR ? (tl.mt * 2 + prk) * MB : tl.mt * MB) * FF_BM;
+      const int brow = tl.e * p.R + tl.nc * BN + (PAIR ? prk * (nt / 2) : 0);
       const int atoms = ff_atoms<MODE>(p, tl.e, K);
       bool ok = true;
       for (int a0 = 0; a0 < atoms; a0 += NA) {
@@ -271,8 +323,15 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         if (gst >= (uint32_t)STAGES && !mbar_wait(&sh.empty[slot], ((gst / STAGES) - 1) & 1)) { ok = false; break; }
         // One 3-D box per operand: NA consecutive 64-column atoms of 128 (or BN) rows, each
         // atom a swizzled [rows x 128 B] block; atoms past K read as zero (never used).
-        mbar_arrive_expect_tx(&sh.full[slot], tx);
+        if (issuer) mbar_arrive_expect_tx(&sh.full[slot], tx);
         uint8_t* stage = ring + (size_t)slot * p.stage_bytes;
+        if (PAIR) {  // counted on the even CTA's barrier
+          const uint32_t fb = dsmem_addr(&sh.full[slot], 0u);
+          tma_load_3d_pair(stage, tmA, fb, 0, arow, a0);
+          tma_load_3d_pair(stage + NA * MB * FF_ATOM_A, tmB, fb, 0, brow, a0);
+          ++gst;
+          continue;
+        }
         if (MODE == 2)  // activations, MN-major: K rows a0 .. of expert e, 2 MB chunks of 64 features
           tma_load_4d(stage, tmA, &sh.full[slot], 0, a0 * FF_BK, tl.mt * MB * 2, tl.e);
         else if ((MODE == 1 || MODE == 3) && p.w_evict_first)  // as stored, MN-major: K rows of expert e
@@ -302,11 +361,18 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         break;
       }
     }
-    // Drain: every copy started here has landed before the CTA can leave.
+    // Drain: every copy started here has landed before the CTA can leave.  (Pairs: the
+    // copies count on the even CTA's barriers; the MMAs' release of each stage, which
+    // arrives on this CTA's barriers, follows them, and no arrival is left in flight.  The
+    // even CTA also waits for the odd CTA's releases of the last queue entries.)
     for (uint32_t i = gst > (uint32_t)STAGES ? gst - STAGES : 0; i < gst; ++i)
-      if (!mbar_wait(&sh.full[i % STAGES], (i / STAGES) & 1)) raise_error(p.err, ERR_TIMEOUT);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+      if (!mbar_wait(PAIR ? &sh.empty[i % STAGES] : &sh.full[i % STAGES], (i / STAGES) & 1))
+        raise_error(p.err, ERR_TIMEOUT);
+    if (PAIR && issuer && !sh.abort_flag)
+      for (int i = sidx > FF_SCHED ? sidx - FF_SCHED : 0; i < sidx - 1; ++i)  // the last entry stops
+        if (!mbar_wait(&sh.sempty[i % FF_SCHED], (i / FF_SCHED) & 1)) raise_error(p.err, ERR_TIMEOUT);
+  } else if (warp == 1 && lane == 0 && issuer) {
+    // ---------------- MMA issuer (pairs: the even CTA, M = 256 over both CTAs' blocks)
     uint32_t gst = 0;
     int sidx = 0, lt = 0;
     while (true) {
@@ -320,7 +386,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       if (tv.x < 0) break;
       // N = the chunk's filled rows rounded up to 16: MMA time and operand reads scale with N.
       // Bits 15 / 16: A / B read MN-major.
-      const uint32_t idesc = idesc_bf16_f32(FF_BM, MODE == 2 ? BN : (sh.sched_nv[qs] + 15) & ~15) |
+      const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * FF_BM : FF_BM, MODE == 2 ? BN : (sh.sched_nv[qs] + 15) & ~15) |
                              (MODE >= 1 ? (1u << 15) : 0u) | (MODE == 2 ? (1u << 16) : 0u);
       const int buf = lt % NBUF;
       if (lt >= NBUF && !mbar_wait(&sh.aempty[buf], ((lt / NBUF) - 1) & 1)) {
@@ -345,7 +411,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         const uint64_t da = MODE == 0 ? sw128_kmajor_desc(st) : sw128_mnmajor_desc(st, mn_lbo);
         const uint64_t db = MODE == 2 ? sw128_mnmajor_desc(st + NA * MB * FF_ATOM_A, mn_lbo)
                                       : sw128_kmajor_desc(st + NA * MB * FF_ATOM_A);
-        const uint32_t b_atom16 = (uint32_t)(BN * FF_BK * 2) >> 4;
+        const uint32_t b_atom16 = (uint32_t)(BNC * FF_BK * 2) >> 4;
 #pragma unroll
         for (int at = 0; at < 2; ++at) {
           if (at >= NA || a0 + at >= atoms) break;
@@ -358,14 +424,24 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
                                               : (uint32_t)(2 * hb) * mn_lbo + (uint32_t)((at * FF_BK + kk * 16) * 128);
               const uint32_t boff16 = MODE == 2 ? (uint32_t)(((at * FF_BK + kk * 16) * 128) >> 4)
                                                 : at * b_atom16 + (uint32_t)((kk * 32) >> 4);
-              tc_mma_bf16(acc + (uint32_t)(hb * BN), da + (uint64_t)(aoff >> 4), db + (uint64_t)boff16, idesc,
-                          (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
+              if (PAIR)
+                tc_mma_bf16_pair(acc + (uint32_t)(hb * BN), da + (uint64_t)(aoff >> 4), db + (uint64_t)boff16,
+                                 idesc, (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
+              else
+                tc_mma_bf16(acc + (uint32_t)(hb * BN), da + (uint64_t)(aoff >> 4), db + (uint64_t)boff16, idesc,
+                            (a0 > 0 || at > 0 || kk > 0) ? 1u : 0u);
             }
         }
-        tc_commit(&sh.empty[slot]);
+        if (PAIR)
+          tc_commit_pair(&sh.empty[slot], (uint16_t)3u);
+        else
+          tc_commit(&sh.empty[slot]);
         ++gst;
       }
-      tc_commit(&sh.afull[buf]);  // the accumulator is complete once these MMAs are
+      if (PAIR)
+        tc_commit_pair(&sh.afull[buf], (uint16_t)3u);
+      else
+        tc_commit(&sh.afull[buf]);  // the accumulator is complete once these MMAs are
       if (!ok) {
         raise_error(p.err, ERR_TIMEOUT);
         sh.abort_flag = 1;
@@ -375,6 +451,11 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       ++lt;
       ++sidx;
     }
+    // (pairs) both epilogues' releases of the last accumulator sets have arrived before
+    // this CTA can leave
+    if (PAIR && !sh.abort_flag)
+      for (int i = lt > NBUF ? lt - NBUF : 0; i < lt; ++i)
+        if (!mbar_wait(&sh.aempty[i % NBUF], (i / NBUF) & 1)) raise_error(p.err, ERR_TIMEOUT);
   } else if (warp >= 2) {
     // ---------------- epilogue (warps 2 .. 1 + 8 MB; TMEM lane quadrant = warp % 4,
     // weight block hb = (warp - 2) / 8, column slice part = ((warp - 2) / 4) % 2)
@@ -391,7 +472,9 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       // leader waits for the accumulator.  Readers of a broadcast are done with it before
       // the end-of-tile barrier, so the leader never overwrites it early.
       if (leader) {
-        const int ok = mbar_wait(&sh.sfull[qs], (sidx / FF_SCHED) & 1) ? 1 : 0;
+        // (pairs, odd CTA) the entry was stored by the even CTA: a cluster-scope acquire
+        const int ok = (PAIR ? mbar_wait_cluster(&sh.sfull[qs], (sidx / FF_SCHED) & 1)
+                             : mbar_wait(&sh.sfull[qs], (sidx / FF_SCHED) & 1)) ? 1 : 0;
         if (!ok) {
           raise_error(p.err, ERR_TIMEOUT);
           sh.abort_flag = 1;
@@ -408,7 +491,8 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       const int e = tv.y, mt = tv.z, nc = tv.w;
       const int n0 = nc * BN;
       const int M = l1 ? p.F : p.d;
-      const int m = (mt * MB + hb) * FF_BM + quad * 32 + lane;
+      const int blk = PAIR ? (mt * 2 + prk) * MB + hb : mt * MB + hb;  // this warp's 128-row weight block
+      const int m = blk * FF_BM + quad * 32 + lane;
       const __nv_bfloat16* bias = l1 ? p.b1 : p.b2;
       const float bv = bias ? __bfloat162float(bias[(size_t)e * M + m]) : 0.f;
       const uint32_t taddr = tmem + (uint32_t)(buf * ACC + hb * BN) + ((uint32_t)(quad * 32) << 16);
@@ -437,7 +521,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         // [16 tokens][32 features] (lane = feature); lane L then stores features 4 (L % 8) ..
         // + 3 of tokens L / 8 + 4 i, i < 4, as 16-byte vectors (8 lanes per 128-byte row).
         float* xf = reinterpret_cast<float*>(&sh.xpose[0][0][0]) + (warp - 2) * (16 * 32);
-        const int mb0 = (mt * MB + hb) * FF_BM + quad * 32;  // first feature of this warp
+        const int mb0 = blk * FF_BM + quad * 32;  // first feature of this warp
 #pragma unroll 1
         for (int c0 = 32 * part; c0 < nv; c0 += 64) {
           uint32_t r[2][16];
@@ -480,7 +564,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
         uint32_t* xw = reinterpret_cast<uint32_t*>(&sh.xpose[warp - 2][0][0]);
         const int ip = lane >> 2, f8 = (lane & 3) * 8;
         const int sw = (ip & 1) * 4;
-        const int mb = (mt * MB + hb) * FF_BM + quad * 32;  // first feature of this warp
+        const int mb = blk * FF_BM + quad * 32;  // first feature of this warp
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           if (q >= nch) break;
@@ -564,12 +648,18 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       tc_fence_before();
       epi_sync<MB>();  // every thread's TMEM reads and stores of this tile are done
       if (leader) {
-        mbar_arrive(&sh.aempty[buf]);
+        if (PAIR && !issuer)  // the even CTA's barriers
+          mbar_arrive_remote(&sh.aempty[buf], 0u);
+        else
+          mbar_arrive(&sh.aempty[buf]);
         if (l1 && !(p.stall && e == 0 && mt == 0 && nc == 0)) {
           __threadfence();  // the chunk's h stores (ordered by the barrier) before the count
           atomicAdd(p.done1 + (size_t)e * p.NCH + nc, 1u);
         }
-        mbar_arrive(&sh.sempty[qs]);
+        if (PAIR && !issuer)
+          mbar_arrive_remote(&sh.sempty[qs], 0u);
+        else
+          mbar_arrive(&sh.sempty[qs]);
       }
       ++lt;
       ++sidx;
@@ -578,7 +668,13 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+  if (PAIR) cluster_sync();  // no peer copies into this CTA or arrives on its barriers any more
+  if (warp == 1) {
+    if (PAIR)
+      tmem_dealloc_pair(tmem, TMEM_COLS);
+    else
+      tmem_dealloc(tmem, TMEM_COLS);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -679,6 +775,32 @@ FfnTiling ffn_tiling(int R, int d, int F) {
 
 size_t ffn_counter_words(int E, int R, int d, int F) { return 1 + (size_t)E * ffn_tiling(R, d, F).NCH; }
 
+// Clusters of 2 of the pair kernel resident at once (cached per device).
+static int ffn_pair_clusters(int smem) {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(ff_threads<2>(), 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, ffn_persistent_kernel<2, 1, 0, true>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = device_sm_count() / 2;
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
 int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   if (L.E == 0 || L.R == 0) return 0;
   if (!tc_shape_ok(L.F, L.d) || (L.mode < 2 && !tc_shape_ok(L.d, L.F))) return -1;
@@ -697,10 +819,28 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
     t.stage_bytes = t.MB * FF_ATOM_A + t.BN * FF_BK * 2;
     t.STAGES = FF_RING / t.stage_bytes < FF_MAX_STAGES ? FF_RING / t.stage_bytes : FF_MAX_STAGES;
   }
+  // Forward tiles of two weight blocks become tiles of four on CTA pairs: two blocks per
+  // CTA, half of the chunk's token rows in each CTA's stages (t.MB = 4 for the ticket order).
+  const bool pair = L.mode == 0 && t.MB == 2 && t.BN % 32 == 0 && L.F % 512 == 0 && L.d % 512 == 0;
+  if (pair) {
+    t.MB = 4;
+    t.NBUF = 1;
+    const int stage_atom = 2 * FF_ATOM_A + (t.BN / 2) * FF_BK * 2;
+    t.NA = stage_atom <= 48 * 1024 ? 2 : 1;
+    t.stage_bytes = t.NA * stage_atom;
+    t.STAGES = FF_RING / t.stage_bytes < FF_MAX_STAGES ? FF_RING / t.stage_bytes : FF_MAX_STAGES;
+    if (t.STAGES < 3 && t.NA == 2) {
+      t.NA = 1;
+      t.stage_bytes = stage_atom;
+      t.STAGES = FF_RING / t.stage_bytes < FF_MAX_STAGES ? FF_RING / t.stage_bytes : FF_MAX_STAGES;
+    }
+  }
+  const int mb_box = pair ? 2 : t.MB;          // weight blocks of a CTA's A boxes
+  const int bn_box = pair ? t.BN / 2 : t.BN;   // token rows of a CTA's B boxes
   if (t.STAGES < 2 || t.BN > 256) return -1;
   CUtensorMap tmW1, tmX, tmW2, tmH, tmXp, tmHp;
   if (L.mode == 0) {  // K-major weights [E, M, K]
-    if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM * t.MB, (uint32_t)t.NA)) return -1;
+    if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.F, (uint64_t)L.d, FF_BM * mb_box, (uint32_t)t.NA)) return -1;
   } else if (L.mode == 1 || L.mode == 3) {  // as stored [E, K, M], MN-major: boxes of 64 NA k-rows x 2 MB chunks
     if (!encode_bf16_3d(&tmW1, L.W1, (uint64_t)L.E * L.d, (uint64_t)L.F, (uint32_t)(FF_BK * t.NA), 2u * t.MB))
       return -1;
@@ -713,7 +853,7 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
     if (bcols < (uint64_t)L.R || !encode_bf16_4d(&tmX, L.xe, (uint64_t)L.E, (uint64_t)L.krows, bcols, FF_BK,
                                                  (uint32_t)(t.BN / 64)))
       return -1;
-  } else if (!encode_bf16_3d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)t.BN, (uint32_t)t.NA)) {
+  } else if (!encode_bf16_3d(&tmX, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)bn_box, (uint32_t)t.NA)) {
     return -1;
   }
   if (L.mode >= 2) {  // no layer 2: its maps are never read
@@ -723,10 +863,10 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
     if (L.mode == 1) {
       if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.F, (uint64_t)L.d, (uint32_t)(FF_BK * t.NA), 2u * t.MB))
         return -1;
-    } else if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM * t.MB, (uint32_t)t.NA)) {
+    } else if (!encode_bf16_3d(&tmW2, L.W2, (uint64_t)L.E * L.d, (uint64_t)L.F, FF_BM * mb_box, (uint32_t)t.NA)) {
       return -1;
     }
-    if (!encode_bf16_3d(&tmH, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)t.BN, (uint32_t)t.NA)) return -1;
+    if (!encode_bf16_3d(&tmH, L.h, (uint64_t)L.E * L.R, (uint64_t)L.F, (uint32_t)bn_box, (uint32_t)t.NA)) return -1;
   }
   if (L.mode != 2 && t.BN > FF_PB) {  // one atom per box: the boxes of a partly filled chunk
     if (!encode_bf16_3d(&tmXp, L.xe, (uint64_t)L.E * L.R, (uint64_t)L.d, (uint32_t)FF_PB, 1u)) return -1;
@@ -783,8 +923,17 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   if (tiles >= (1ll << 31) || (long long)L.E * L.R >= (1ll << 31) || (long long)L.E * L.F >= (1ll << 31) ||
       (long long)L.E * L.d >= (1ll << 31))
     return -1;  // tickets and TMA row coordinates are 32-bit
-  const int ctas = (int)(tiles < device_sm_count() ? tiles : device_sm_count());
   cudaError_t e;
+  if (pair) {
+    auto kern = ffn_persistent_kernel<2, 1, 0, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+    const int fit = ffn_pair_clusters(smem);
+    const int pairs = (int)(tiles < fit ? tiles : fit);
+    e = launch_k(kern, dim3((unsigned)(2 * pairs)), dim3(ff_threads<2>()), (size_t)smem, s, pdl, 2, tmW1, tmX, tmW2,
+                 tmH, tmXp, tmHp, p);
+    return e == cudaSuccess ? 1 : -1;
+  }
+  const int ctas = (int)(tiles < device_sm_count() ? tiles : device_sm_count());
 #define SMOE_FFN(MBV, NBV, MK)                                                                                     \
   do {                                                                                                             \
     auto kern = ffn_persistent_kernel<MBV, NBV, MK>;                                                               \

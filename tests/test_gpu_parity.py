@@ -62,6 +62,11 @@ SMALL = {
     "tc-two-blocks-db": (LayerShape("tc-two-blocks-db", 1, 512, 256, 512, 4, 1.0), dict(router_bias_std=0.1)),
     # 350-row expert blocks with two weight blocks per tile and uneven loads: experts that fit
     # one 256-row chunk, and second chunks of one or two 64-row boxes
+    # d, d_ff multiples of 512: tiles of four weight blocks on CTA pairs (two blocks per CTA,
+    # half of each token chunk in each CTA); 150-row blocks, then 350-row blocks in two chunks
+    "tc-pairs": (LayerShape("tc-pairs", 1, 600, 512, 1024, 4, 1.0), dict(expert_bias_std=0.05)),
+    "tc-pairs-chunks": (LayerShape("tc-pairs-chunks", 2, 700, 512, 1024, 4, 1.0),
+                        dict(expert_bias_std=0.05, router_bias_std=0.3)),
     "tc-chunks-256": (LayerShape("tc-chunks-256", 2, 700, 256, 512, 4, 1.0),
                       dict(expert_bias_std=0.05, router_bias_std=0.3)),
     # d = 192: three 64-column atoms, so the router's last two-atom stage has a zero-filled half
