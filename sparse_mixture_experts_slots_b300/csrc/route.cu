@@ -167,10 +167,12 @@ __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
     const float* __restrict__ z, int T, int E, int nT, int32_t* __restrict__ expert, int32_t* __restrict__ expert2,
     float* __restrict__ gate, float* __restrict__ gate2, int32_t* __restrict__ rank, int32_t* __restrict__ rank2,
     int32_t* __restrict__ tile_hist, int32_t* __restrict__ tile_hist2, float* __restrict__ tile_P,
-    float* __restrict__ tile_Z, float* __restrict__ probs, uint32_t* err) {
+    float* __restrict__ tile_Z, float* __restrict__ probs, uint32_t* err, int staged) {
   griddep_wait();
   griddep_launch_dependents();
-  extern __shared__ int32_t hist[];  // [2E]: first choices, then second choices
+  // [2E] ints: first choices, then second choices; [nch E] floats: column partials; with
+  // `staged`, the tile's logits [ROUTE_TILE][E] (each token's row becomes its probabilities)
+  extern __shared__ int32_t hist[];
   int32_t* hist2 = hist + E;
   __shared__ float m_s[ROUTE_TILE], s_s[ROUTE_TILE], zz_s[ROUTE_TILE];
   __shared__ int a_s[ROUTE_TILE], a2_s[ROUTE_TILE];
@@ -179,11 +181,21 @@ __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
   const int len = min(ROUTE_TILE, T - t0);
   const size_t tok0 = (size_t)g * T + t0;
   for (int e = threadIdx.x; e < 2 * E; e += blockDim.x) hist[e] = 0;
+  const int nch = E >= (int)blockDim.x ? 1 : (int)blockDim.x / E;
+  float* zt = reinterpret_cast<float*>(hist + 2 * E) + (size_t)nch * E;  // staged logits
+  if (staged) {  // the tile's rows are contiguous: 16-byte loads when E allows
+    if ((E & 3) == 0) {
+      const float4* src = reinterpret_cast<const float4*>(z + tok0 * E);
+      for (int k = threadIdx.x; k < len * E / 4; k += blockDim.x) reinterpret_cast<float4*>(zt)[k] = src[k];
+    } else {
+      for (int k = threadIdx.x; k < len * E; k += blockDim.x) zt[k] = z[tok0 * E + k];
+    }
+  }
   __syncthreads();
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
   for (int i = warp; i < len; i += nwarps) {
-    const float* zr = z + (tok0 + i) * E;
+    const float* zr = staged ? zt + (size_t)i * E : z + (tok0 + i) * E;
     float m1 = -INFINITY, m2 = -INFINITY;
     int i1 = 0x7fffffff, i2 = 0x7fffffff;
     for (int e = lane; e < E; e += 32) {  // increasing e: strict > keeps the lower index
@@ -215,6 +227,14 @@ __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
     float s = 0.f;
     for (int e = lane; e < E; e += 32) s += expf(zr[e] - m1);
     s = warp_sum(s);
+    if (staged) {  // the row's probabilities in place (each lane rewrites only what it read)
+      float* pr = zt + (size_t)i * E;
+      for (int e = lane; e < E; e += 32) {
+        const float pv = expf(pr[e] - m1) / s;
+        pr[e] = pv;
+        if (probs) probs[(tok0 + i) * E + e] = pv;
+      }
+    }
     if (lane == 0) {
       m_s[i] = m1;
       s_s[i] = s;
@@ -251,16 +271,19 @@ __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
   // Column pass: (expert, token chunk) per thread, chunk sums combined in a fixed order.
   const size_t tbase = ((size_t)g * nT + tile) * E;
   float* part = reinterpret_cast<float*>(hist + 2 * E);
-  const int nch = E >= (int)blockDim.x ? 1 : (int)blockDim.x / E;
   const int clen = (len + nch - 1) / nch;
   for (int k = threadIdx.x; k < E * nch; k += blockDim.x) {
     const int e = k % E, c = k / E;
     float acc = 0.f;
     const int i1 = min(len, (c + 1) * clen);
-    for (int i = c * clen; i < i1; ++i) {
-      const float p = expf(z[(tok0 + i) * E + e] - m_s[i]) / s_s[i];
-      acc += p;
-      if (probs) probs[(tok0 + i) * E + e] = p;
+    if (staged) {
+      for (int i = c * clen; i < i1; ++i) acc += zt[(size_t)i * E + e];
+    } else {
+      for (int i = c * clen; i < i1; ++i) {
+        const float p = expf(z[(tok0 + i) * E + e] - m_s[i]) / s_s[i];
+        acc += p;
+        if (probs) probs[(tok0 + i) * E + e] = p;
+      }
     }
     part[c * E + e] = acc;
   }
@@ -517,10 +540,17 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
       ++launches;
     }
     const int nch = a.E >= TOP2_THREADS ? 1 : TOP2_THREADS / a.E;
-    if (launch_k(route_top2_kernel, dim3(nT, a.G), dim3(TOP2_THREADS),
-                 2 * a.E * sizeof(int32_t) + (size_t)nch * a.E * sizeof(float), s, true, 1,
-                 (const float*)a.logits, a.T, a.E, nT, a.expert, a.expert2, a.gate, a.gate2, a.slot, a.slot2,
-                 a.tile_hist, a.tile_hist2, a.tile_P, a.tile_Z, a.probs, a.err) != cudaSuccess)
+    // the tile's logits staged in shared memory when they fit (E up to about 390)
+    const size_t base_smem = 2 * a.E * sizeof(int32_t) + (size_t)nch * a.E * sizeof(float);
+    const size_t stage_smem = (size_t)ROUTE_TILE * a.E * sizeof(float);
+    const int staged = base_smem + stage_smem <= 200 * 1024 ? 1 : 0;
+    const size_t smem = base_smem + (staged ? stage_smem : 0);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(route_top2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return -1;
+    if (launch_k(route_top2_kernel, dim3(nT, a.G), dim3(TOP2_THREADS), smem, s, true, 1, (const float*)a.logits, a.T,
+                 a.E, nT, a.expert, a.expert2, a.gate, a.gate2, a.slot, a.slot2, a.tile_hist, a.tile_hist2, a.tile_P,
+                 a.tile_Z, a.probs, a.err, staged) != cudaSuccess)
       return -1;
     ++launches;
   } else if (N > 0) {
