@@ -82,6 +82,9 @@ SMALL = {
     "gx-e1536": (LayerShape("gx-e1536", 1, 5300, 128, 128, 1536, 1.0), dict(router_bias_std=0.1)),
     # 1100 experts (5 slices of 256) over 5 tiles: the last pair's second tile is past the end
     "gx-pair-odd": (LayerShape("gx-pair-odd", 1, 600, 128, 128, 1100, 1.0), {}),
+    # two routing groups of 5 tiles: the pair (4, 5) takes the last tile of group 0 and the
+    # first of group 1
+    "gx-pair-groups": (LayerShape("gx-pair-groups", 2, 600, 128, 128, 1100, 1.0), dict(router_bias_std=0.1)),
     # float32 rows of 49,408 bytes: too wide for the shared-memory row slots of the bulk-copy
     # dispatch and combine, so their register kernels run
     "wide-rows": (LayerShape("wide-rows", 1, 40, 12352, 32, 4, 1.0, dtype="f32"), dict(expert_bias_std=0.05)),
