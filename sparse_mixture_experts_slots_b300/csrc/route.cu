@@ -298,9 +298,12 @@ __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
 }
 
 // ---------------------------------------------------------------- 3. cross-tile scan + finalize
-// One block per 32 experts (lane <-> expert); the warps split each group's tiles.  When the
-// router z-loss is asked for, one more block reduces the tiles' sums of (log sum exp z)^2
-// per group, alongside the scan (nothing later in the layer waits for it).
+// One block per (32 experts, routing group), lane <-> expert; the warps split the group's
+// tiles.  Each block writes its group's tile prefixes, raw / accepted counts and P; the last
+// block to finish (atomic ticket) adds the groups' row counts in group order (group row
+// offsets, expert block rows) and the per-block balance partials in a fixed order.  When the
+// router z-loss is asked for, one more block reduces the tiles' sums of (log sum exp z)^2 per
+// group, alongside the scan (nothing later in the layer waits for it).
 constexpr int SCAN_WARPS = 16;
 
 __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
@@ -321,6 +324,7 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nblk = route_scan_blocks(E);
   if ((int)blockIdx.x >= nblk) {  // router z-loss: a warp per group, then the mean over groups
+    if (blockIdx.y != 0) return;
     double wsum = 0.0;
     for (int g = warp; g < G; g += SCAN_WARPS) {
       double zs = 0.0;
@@ -339,24 +343,21 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
     }
     return;
   }
+  const int g = blockIdx.y;
   const int e = blockIdx.x * 32 + lane;
   const bool ev = e < E;
   const int chunk = (nT + SCAN_WARPS - 1) / SCAN_WARPS;
   const int j0 = min(nT, warp * chunk), j1 = min(nT, j0 + chunk);
-  int rows_run = 0;
-  for (int g = 0; g < G; ++g) {
-    int hs = 0;
+  {
+    int hs = 0, hs2 = 0;
     float ps = 0.f;
     if (ev)
       for (int j = j0; j < j1; ++j) {
         const size_t idx = ((size_t)g * nT + j) * E + e;
         hs += tile_hist[idx];
         ps += tile_P[idx];
+        if (tile_hist2) hs2 += tile_hist2[idx];  // top-2: second choices, counted the same way
       }
-    // top-2: second choices, counted and prefixed the same way
-    int hs2 = 0;
-    if (tile_hist2 && ev)
-      for (int j = j0; j < j1; ++j) hs2 += tile_hist2[((size_t)g * nT + j) * E + e];
     sh_h[warp][lane] = hs;
     sh_h2[warp][lane] = hs2;
     sh_p[warp][lane] = ps;
@@ -392,42 +393,47 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) route_scan_kernel(
         raw[ge] = tot;
         accepted[ge] = acc;
         P[ge] = Pv;
-        group_off[ge] = rows_run;
-        rows_run += acc;
         if (tile_hist2) {  // second choices fill what the kept first choices leave
-          const int acc2 = min(tot2, max(C - acc, 0));
           raw2[ge] = tot2;
-          accepted2[ge] = acc2;
-          rows_run += acc2;
+          accepted2[ge] = min(tot2, max(C - acc, 0));
         }
         contrib = (float)tot * Pv;
       }
       contrib = warp_sum(contrib);
       if (lane == 0) partial[(size_t)g * nblk + blockIdx.x] = contrib;
     }
-    __syncthreads();
   }
-  if (warp == 0 && ev) expert_rows[e] = rows_run;
 
-  // The last block to finish sums the per-block partials (fixed order) per group.
+  // The last block to finish: group row offsets and expert rows (groups in order), then the
+  // per-block partials (fixed order) per group.
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == (unsigned)nblk - 1;
+  if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == (unsigned)(nblk * G) - 1;
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+  for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
+    int rows_run = 0;
+    for (int gg = 0; gg < G; ++gg) {
+      const size_t ge = (size_t)gg * E + ee;
+      group_off[ge] = rows_run;
+      rows_run += __ldcg(&accepted[ge]);
+      if (tile_hist2) rows_run += __ldcg(&accepted2[ge]);
+    }
+    expert_rows[ee] = rows_run;
+  }
+  for (int gg = threadIdx.x; gg < G; gg += blockDim.x) {
     float sum = 0.f;
-    for (int b = 0; b < nblk; ++b) sum += __ldcg(&partial[(size_t)g * nblk + b]);
+    for (int b = 0; b < nblk; ++b) sum += __ldcg(&partial[(size_t)gg * nblk + b]);
     // E * sum_e f_e P_e with f_e = raw_e / T
     const float bal = T > 0 ? (float)E * (sum / (float)T) : 0.f;
-    balance[g] = bal;
-    aux_g[g] = alpha * bal;
+    balance[gg] = bal;
+    aux_g[gg] = alpha * bal;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     float total = 0.f;
-    for (int g = 0; g < G; ++g) total += aux_g[g];
+    for (int gg = 0; gg < G; ++gg) total += aux_g[gg];
     aux[0] = G > 0 ? total / (float)G : 0.f;
     *counter = 0u;
   }
@@ -571,7 +577,8 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   // The scan follows the router kernel of this call (programmatic launch); with no
   // tokens it is the first kernel of the call.
   const int scan_grid = route_scan_blocks(a.E) + ((a.z_g || a.z) ? 1 : 0);
-  if (launch_k(route_scan_kernel, dim3(scan_grid), dim3(SCAN_WARPS * 32), 0, s, N > 0, 1, a.tile_hist,
+  if (a.G > 65535) return -1;
+  if (launch_k(route_scan_kernel, dim3(scan_grid, a.G), dim3(SCAN_WARPS * 32), 0, s, N > 0, 1, a.tile_hist,
                a.tile_P, (const float*)a.tile_Z, a.top2 ? (const int32_t*)a.tile_hist2 : nullptr, a.G, a.T, a.E, nT,
                a.C, a.alpha, a.tile_base, a.top2 ? a.tile_base2 : nullptr, a.raw, a.accepted,
                a.top2 ? a.raw2 : nullptr, a.top2 ? a.accepted2 : nullptr, a.P, a.group_off, a.expert_rows,
