@@ -71,7 +71,9 @@ SMALL = {
                       dict(expert_bias_std=0.05, router_bias_std=0.3)),
     # d = 192: three 64-column atoms, so the router's last two-atom stage has a zero-filled half
     "odd-atoms": (LayerShape("odd-atoms", 2, 260, 192, 256, 12, 1.0), dict(router_bias_std=0.1)),
-    # router slices meeting in global memory.  200 experts: 4 slices of 64
+    # router slices meeting in global memory.  One tile of 300 experts (5 slices of 64)
+    "gx-single-tile": (LayerShape("gx-single-tile", 1, 100, 128, 128, 300, 1.0), dict(router_bias_std=0.1)),
+    # 200 experts: 4 slices of 64
     "gx-e200": (LayerShape("gx-e200", 1, 900, 128, 128, 200, 1.0), dict(router_bias_std=0.1)),
     # 512 experts: 8 slices of 64 over 34 tiles (272 items, more than one per SM; some tiles'
     # slices straddle two rounds of the grid)
