@@ -24,7 +24,12 @@
  *   - Execution: all calls except switch_get_stats, switch_sync_status and
  *     switch_stage_ms are asynchronous on the given stream.  Calls on one handle
  *     share its workspace: calls on one handle that overlap on the GPU race, so
- *     issue them on one stream (or serialise the streams).
+ *     issue them on one stream (or serialise the streams).  The stream-ordered calls
+ *     enqueue work only (no host synchronisation), so a CUDA graph may capture them
+ *     and replay them on new contents of the same buffers (make one call before the
+ *     capture).  With bfloat16 activations and more than two 64..256-expert router
+ *     slices the router is a cooperative launch of one CTA per SM (two-CTA clusters
+ *     for 256-expert slices): it starts once every SM can take one of its CTAs.
  *   - Errors: argument errors return at once (nothing is enqueued).  A kernel
  *     that finds an impossible state (a bounded wait that ran out, a debug bounds
  *     hit) sets a flag in the workspace; switch_get_stats / switch_sync_status
