@@ -478,10 +478,29 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         for (int ch = 0; ch < CPW / 8; ++ch) {
           const uint32_t col = (uint32_t)(cbeg + ch * 8);
           uint32_t h[8], r1[8], r2[8];
-          tmem_ld8(trow + col, h);
-          tmem_ld8(trow + EC + col, r1);
-          if (Gm::ACC_BLOCKS == 3) tmem_ld8(trow + 2 * EC + col, r2);
-          tmem_ld_wait();
+          if (Gm::ACC_BLOCKS == 2 && (ch & 1) == 0) {  // two chunks' loads before one wait
+            uint32_t h2[8], q2[8];
+            tmem_ld8(trow + col, h);
+            tmem_ld8(trow + EC + col, r1);
+            tmem_ld8(trow + col + 8, h2);
+            tmem_ld8(trow + EC + col + 8, q2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              v[ch * 8 + 8 + j] = __uint_as_float(h2[j]) + __uint_as_float(q2[j]);
+            }
+          } else if (Gm::ACC_BLOCKS == 2) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              h[j] = __float_as_uint(v[ch * 8 + j]);
+              r1[j] = 0u;
+            }
+          } else {
+            tmem_ld8(trow + col, h);
+            tmem_ld8(trow + EC + col, r1);
+            if (Gm::ACC_BLOCKS == 3) tmem_ld8(trow + 2 * EC + col, r2);
+            tmem_ld_wait();
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int c = cbeg + ch * 8 + j;
