@@ -170,8 +170,8 @@ __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const CUtensorM
 
 // 1-D bulk copies (cp.async.bulk, no tensor map): `bytes` a multiple of 16, both addresses
 // 16-byte aligned.  A load's bytes are counted on the mbarrier `bar`; stores are tracked in
-// the issuing thread's bulk groups (commit, then wait for the reads of shared memory or for
-// completion).
+// the issuing thread's bulk groups (commit, then wait for the reads of shared memory; the
+// writes to global memory complete by the end of the grid).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_u32(smem_dst)),
@@ -186,8 +186,6 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uin
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // This thread's committed stores have read their shared-memory sources.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// This thread's committed stores are complete.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Order this thread's generic-proxy writes of shared memory before later async-proxy reads.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
