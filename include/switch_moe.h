@@ -97,6 +97,12 @@ typedef enum { SWITCH_F32 = 0, SWITCH_BF16 = 1 } switch_dtype;
  * unspecified; the handle stays usable.  Has no effect where expert 0 receives no token
  * or the FFN runs on CUDA cores. */
 #define SWITCH_FLAG_TEST_STALL    0x40u
+/* Test only.  Outside training the tensor-core FFN drops each token chunk's hidden
+ * activations from L2 once the chunk's last layer-2 tile has read them (no write-back
+ * of scratch to DRAM), but only where they outgrow half of L2 and its tiles keep two
+ * accumulator sets; this flag makes it do so for every shape, so small layers exercise
+ * that path.  Results are unchanged. */
+#define SWITCH_FLAG_TEST_DISCARD  0x80u
 
 typedef struct {
   int G;                   /* routing groups; capacity and statistics are per group */
@@ -248,6 +254,8 @@ SWITCH_API switch_status switch_forward(switch_handle h, const void* x, const fl
  *   done_event != NULL (a cudaEvent_t the caller created): it is recorded after
  *     the copy out and `stream` does not wait; the results are in place once
  *     the event has completed.
+ * The copy in is issued in pieces of at most 16 MiB (one large host-to-device copy
+ * was measured slower than its pieces on the PCIe hosts of B300 machines).
  * The first call allocates the staging buffers (4 * N * d act elements) and
  * creates the copy streams, so it is not for use under stream capture.
  * Returns SWITCH_ERR_INVALID_ARG for NULL x_host / y_host with N > 0, else as
@@ -273,8 +281,9 @@ SWITCH_API switch_status switch_forward_host(switch_handle h, const void* x_host
  *   Outputs (float32, caller-owned): dx [N, d], dWr [E, d], dbr [E], dW1 [E, d_ff, d],
  *   db1 [E, d_ff], dW2 [E, d, d_ff], db2 [E, d]; dbr, db1, db2 may be NULL.
  * With bfloat16 and d, d_ff multiples of 128 the expert products run on the tensor cores
- * (dye, dh, dxe and the weight gradients pass through bfloat16; float32 accumulation);
- * otherwise, and for the router's products, on CUDA cores in float32.
+ * (dye, dh, dxe and the weight gradients pass through bfloat16; float32 accumulation), and
+ * so do the router's products dW_r = dz^T x and dz W_r when E is a multiple of 64 (dz and
+ * W_r as bfloat16 hi + lo pieces, ~2^-16 relative); otherwise on CUDA cores in float32.
  */
 SWITCH_API switch_status switch_backward(switch_handle h, const void* x, const float* Wr, const void* W1,
                               const void* W2, const switch_route_out* r, const void* dy, float w_aux,

@@ -29,6 +29,7 @@ FLAG_PROFILE = 0x8
 FLAG_TOP2 = 0x10
 FLAG_TRAINING = 0x20
 FLAG_TEST_STALL = 0x40
+FLAG_TEST_DISCARD = 0x80
 
 
 class SwitchConfig(ctypes.Structure):

@@ -4,6 +4,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 
 #include "../../include/switch_moe.h"
@@ -453,6 +454,8 @@ static switch_status run_ffn_tc(switch_handle h, const void* xe, const void* W1,
   L.d = c.d_model;
   L.F = c.d_ff;
   L.stall = (c.flags & SWITCH_FLAG_TEST_STALL) != 0;
+  // training keeps h for the backward
+  L.discard_h = training_of(&c) ? 0 : (c.flags & SWITCH_FLAG_TEST_DISCARD) ? 2 : 1;
   const int n = launch_ffn_tc(L, s, pdl);
   if (n < 0) return SWITCH_ERR_CUDA;
   h->last_launches += n;
@@ -629,8 +632,13 @@ switch_status switch_forward_host(switch_handle h, const void* x_host, const flo
   const bool reuse = p->calls >= 2;  // slot k was used by the call before the previous one
   // copy in: after the layer of that call has read x from slot k
   if (reuse && cudaStreamWaitEvent(p->cin, p->fwd_done[k], 0) != cudaSuccess) return SWITCH_ERR_CUDA;
-  if (p->act_bytes && cudaMemcpyAsync(xs, x_host, p->act_bytes, cudaMemcpyHostToDevice, p->cin) != cudaSuccess)
-    return SWITCH_ERR_CUDA;
+  // In pieces of at most 16 MiB: a single copy of 100 MB from page-locked memory ran at
+  // 36-42 GB/s where the same bytes in 16 MiB pieces reached 54 GB/s (B300 hosts, PCIe).
+  constexpr size_t kCopyPiece = (size_t)16 << 20;
+  for (size_t off = 0; off < p->act_bytes; off += kCopyPiece)
+    if (cudaMemcpyAsync(xs + off, static_cast<const uint8_t*>(x_host) + off, std::min(kCopyPiece, p->act_bytes - off),
+                        cudaMemcpyHostToDevice, p->cin) != cudaSuccess)
+      return SWITCH_ERR_CUDA;
   if (cudaEventRecord(p->in_done[k], p->cin) != cudaSuccess) return SWITCH_ERR_CUDA;
   // the layer: after its input has landed and the copy out of that call has read y
   if (cudaStreamWaitEvent(s, p->in_done[k], 0) != cudaSuccess) return SWITCH_ERR_CUDA;

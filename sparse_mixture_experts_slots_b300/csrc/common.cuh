@@ -234,6 +234,12 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// Drops one 128-byte line (address 128-byte aligned) from L2 without writing it back: a
+// weak write of undefined contents, for scratch that nothing reads again.
+__device__ __forceinline__ void l2_discard_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

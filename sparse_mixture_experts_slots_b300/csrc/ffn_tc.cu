@@ -60,11 +60,13 @@ struct FfnParams {
   const __nv_bfloat16* hmask;    // [E * R, F]: with MASK, layer 1 keeps its sum where this is > 0
   uint32_t* next_tile;           // zero at launch
   uint32_t* done1;               // [E * NCH], zero at launch
+  uint32_t* done2;               // [E * NCH], zero at launch: layer-2 tiles of (expert, chunk) done
   uint32_t* err;
   int E, R, d, F, BN, NCH, LOOK, NA, STAGES, stage_bytes, combine, w_evict_first;
   int MB;                        // 128-row weight blocks per tile (the kernel's template value)
   int layer2;                    // 0: layer-1 tiles only (a weight gradient)
   int stall;                     // test only: tile (layer 1, expert 0, block 0, chunk 0) never publishes
+  int discard_h;                 // h is scratch: the last layer-2 tile of a chunk drops its lines from L2
   float* out_f32;                // MODE 2: the float32 result [E * R, F] (R: tokens, F: features)
   const int32_t* kcount;         // MODE 2 (or null): rows of expert e on the contraction axis; only
                                  // their 64-row atoms are read (at least one, zero past the count)
@@ -128,6 +130,8 @@ struct FfShared {
   volatile int abort_flag;
   int ep_ok;
   int ep_acc_ok;
+  int4 ep_disc;       // (flag, expert, first row, rows): the previous tile was the last reader of
+                      // that chunk's h
 };
 static_assert(offsetof(FfShared, xpose) % 16 == 0, "16-byte vector reads of the transpose buffer");
 static_assert(sizeof(FfShared::xpose) >= 8 * FF_EPW * 16 * 32 * sizeof(float) / 2,
@@ -208,6 +212,7 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       mbar_init(&sh.aempty[i], PAIR ? 2 : 1);
     }
     sh.abort_flag = 0;
+    sh.ep_disc = make_int4(0, 0, 0, 0);
     fence_mbar_init();
     prefetch_tmap(&tmW1);
     prefetch_tmap(&tmX);
@@ -486,6 +491,15 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
       epi_sync<MB>();
       const int4 tv = sh.ep_tile;
       const int nv = sh.ep_nv;
+      const int4 dc = sh.ep_disc;  // the leader writes it again only after the next barrier
+      if (dc.x) {
+        // Nothing reads that chunk's h again: drop its 128-byte lines from L2 without writing
+        // them back to DRAM (the rows' contents become undefined).
+        const int lines_per_row = p.F * 2 / 128;
+        const __nv_bfloat16* h0 = p.h + ((size_t)dc.y * p.R + dc.z) * p.F;
+        for (int i = threadIdx.x - 64; i < dc.w * lines_per_row; i += 128 * FF_EPW * MB)
+          l2_discard_line(h0 + (size_t)(i / lines_per_row) * p.F + (size_t)(i % lines_per_row) * 64);
+      }
       if (!sh.ep_ok || tv.x < 0) break;
       const bool l1 = tv.x == 0;
       const int e = tv.y, mt = tv.z, nc = tv.w;
@@ -656,6 +670,17 @@ __global__ void __launch_bounds__(ff_threads<MB>(), 1)
           __threadfence();  // the chunk's h stores (ordered by the barrier) before the count
           atomicAdd(p.done1 + (size_t)e * p.NCH + nc, 1u);
         }
+        // Every copy of h this layer-2 tile made had landed before its accumulator was
+        // complete; the tile that completes its chunk's count is the chunk's last reader
+        // (pairs: the even CTA counts for both).  Off the accumulator's path: counted after
+        // the release, the lines dropped while the next tile's MMAs run.
+        int last = 0;
+        if (!l1 && p.discard_h && issuer) {
+          __threadfence();
+          last = atomicAdd(p.done2 + (size_t)e * p.NCH + nc, 1u) == (uint32_t)(p.d / (FF_BM * p.MB)) - 1u ? 1 : 0;
+          if (last) __threadfence();
+        }
+        sh.ep_disc = make_int4(last, e, n0, nv);
         if (PAIR && !issuer)
           mbar_arrive_remote(&sh.sempty[qs], 0u);
         else
@@ -773,7 +798,7 @@ FfnTiling ffn_tiling(int R, int d, int F) {
   return t;
 }
 
-size_t ffn_counter_words(int E, int R, int d, int F) { return 1 + (size_t)E * ffn_tiling(R, d, F).NCH; }
+size_t ffn_counter_words(int E, int R, int d, int F) { return 1 + 2 * (size_t)E * ffn_tiling(R, d, F).NCH; }
 
 // Clusters of 2 of the pair kernel resident at once (cached per device).
 static int ffn_pair_clusters(int smem) {
@@ -889,6 +914,7 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.resid = (const __nv_bfloat16*)L.resid;
   p.next_tile = L.counters;
   p.done1 = L.counters + 1;
+  p.done2 = L.counters + 1 + (size_t)L.E * t.NCH;
   p.err = L.err;
   p.E = L.E;
   p.R = L.R;
@@ -913,6 +939,13 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   p.hmask = (const __nv_bfloat16*)L.hmask;
   p.layer2 = L.mode >= 2 ? 0 : 1;
   p.stall = L.stall ? 1 : 0;
+  // Dropping h's lines pays where h does not stay in L2 until the next launch overwrites it
+  // (its dirty lines would be written back to DRAM: more than half of the 126 MB L2) and the
+  // epilogue has slack (two accumulator sets).  Measured: 2048 experts (268 MB of h, two
+  // sets) FFN 1942 -> 1905 us, DRAM writes 290 -> 82 MB; with one accumulator set
+  // (skewed-e64-g8, switch-large-e128) 228 -> 238 and 533 -> 547 us, so not there.
+  const bool big_h = (size_t)L.E * L.R * L.F * 2 > ((size_t)64 << 20);
+  p.discard_h = L.mode == 0 && (L.discard_h == 2 || (L.discard_h == 1 && big_h && t.NBUF == 2 && !pair)) ? 1 : 0;
   p.out_f32 = L.out_f32;
   p.kcount = L.mode == 2 ? L.kcount : nullptr;
   if (L.mode >= 2 && !L.out_f32) return -1;

@@ -227,6 +227,10 @@ struct FfnLaunch {
   uint32_t* err;
   int E, R, d, F;
   bool stall;                // test only: layer-1 tile (expert 0, chunk 0, block 0) never publishes
+  int discard_h;             // mode 0, h not read after this launch (no training): 1 drop its lines
+                             // from L2 once the last layer-2 tile of a chunk read them, where h
+                             // outgrows half of L2 and the tiles keep two accumulator sets;
+                             // 2 for every shape (tests)
 };
 // Needs d % 128 == 0 and F % 128 == 0 (tc_shape_ok both ways).  Returns launches or -1.
 bool tc_shape_ok(int M, int K);

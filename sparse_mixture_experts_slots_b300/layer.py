@@ -64,7 +64,7 @@ class SwitchMoE:
                  dtype: torch.dtype = torch.bfloat16, alpha: float = 0.01, capacity_override: int = 0,
                  write_probs: bool = False, write_logits: bool = False, debug_bounds: bool = False,
                  profile: bool = False, top_k: int = 1, training: bool = False, test_stall: bool = False,
-                 device=None):
+                 test_discard: bool = False, device=None):
         self.lib = _lib.load()
         if dtype not in (torch.bfloat16, torch.float32):
             raise ValueError("dtype must be torch.bfloat16 or torch.float32")
@@ -73,7 +73,7 @@ class SwitchMoE:
         flags = ((_lib.FLAG_WRITE_PROBS if write_probs else 0) | (_lib.FLAG_WRITE_LOGITS if write_logits else 0)
                  | (_lib.FLAG_DEBUG_BOUNDS if debug_bounds else 0) | (_lib.FLAG_PROFILE if profile else 0)
                  | (_lib.FLAG_TOP2 if top_k == 2 else 0) | (_lib.FLAG_TRAINING if training else 0)
-                 | (_lib.FLAG_TEST_STALL if test_stall else 0))
+                 | (_lib.FLAG_TEST_STALL if test_stall else 0) | (_lib.FLAG_TEST_DISCARD if test_discard else 0))
         if top_k not in (1, 2):
             raise ValueError("top_k must be 1 or 2")
         self.top_k = top_k
