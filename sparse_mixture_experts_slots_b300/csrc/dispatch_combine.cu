@@ -635,7 +635,9 @@ __global__ void __launch_bounds__(BULK_MAX_WARPS * 32) combine_bulk_kernel(
 
 template <typename K, typename... Args>
 static int launch_bulk(K kern, const BulkPlan& p, cudaStream_t s, bool pdl, Args&&... args) {
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess) return -1;
+  // the plans' bound, not this plan's size: one value whatever the shape, so calls from
+  // several host threads never lower it under one another's launch
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BULK_SMEM_MAX) != cudaSuccess) return -1;
   return launch_k(kern, dim3((unsigned)p.ctas), dim3((unsigned)p.warps * 32), p.smem, s, pdl, 1,
                   std::forward<Args>(args)...) == cudaSuccess
              ? 1

@@ -30,6 +30,7 @@
 //                      layer-2 tiles.
 // Every wait is bounded; on timeout the CTA sets the error flag, stops taking tiles,
 // drains its own copies and MMAs, frees TMEM and returns.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -722,13 +723,16 @@ static EncodeTiledFn get_encode_fn() {
 }
 
 int device_sm_count() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // per device; handles on several host threads may fill it
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -802,10 +806,13 @@ size_t ffn_counter_words(int E, int R, int d, int F) { return 1 + 2 * (size_t)E 
 
 // Clusters of 2 of the pair kernel resident at once (cached per device).
 static int ffn_pair_clusters(int smem) {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(ff_threads<2>(), 1, 1);
@@ -822,7 +829,7 @@ static int ffn_pair_clusters(int smem) {
     cudaGetLastError();
     n = device_sm_count() / 2;
   }
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -551,8 +551,10 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
     const size_t stage_smem = (size_t)ROUTE_TILE * a.E * sizeof(float);
     const int staged = base_smem + stage_smem <= 200 * 1024 ? 1 : 0;
     const size_t smem = base_smem + (staged ? stage_smem : 0);
+    // the attribute is the bound every call stays under (one value whatever the shape, so
+    // calls from several host threads never lower it under one another's launch)
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(route_top2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        cudaFuncSetAttribute(route_top2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
       return -1;
     if (launch_k(route_top2_kernel, dim3(nT, a.G), dim3(TOP2_THREADS), smem, s, true, 1, (const float*)a.logits, a.T,
                  a.E, nT, a.expert, a.expert2, a.gate, a.gate2, a.slot, a.slot2, a.tile_hist, a.tile_hist2, a.tile_P,

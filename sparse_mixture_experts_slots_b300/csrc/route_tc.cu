@@ -51,6 +51,8 @@
 // that turns ranks into slots runs in route.cu.
 #include <limits.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -755,13 +757,16 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 // kernel, device and cluster size).
 template <int EC, int NAX, int XM>
 static int rt_fit(int cl) {
-  static int cache[64][9] = {};
+  static std::atomic<int> cache[64][9];  // handles on several host threads may fill it
   auto kern = router_tc_kernel<EC, NAX, XM>;
   constexpr int smem = rt_smem_bytes<EC, NAX, XM == 2>();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
   const bool cached = dev >= 0 && dev < 64 && cl >= 1 && cl <= 8;
-  if (cached && cache[dev][cl] > 0) return cache[dev][cl];
+  if (cached) {
+    const int c = cache[dev][cl].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cl > 1) {
     cudaLaunchConfig_t cfg = {};
@@ -788,7 +793,7 @@ static int rt_fit(int cl) {
     n *= device_sm_count();
   }
   if (n < cl) n = cl;
-  if (cached) cache[dev][cl] = n;
+  if (cached) cache[dev][cl].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -866,7 +871,7 @@ static cudaError_t rt_launch(int grid, int cluster, bool coop, bool pdl, cudaStr
 
 // CTA pairs need a cooperative launch of 2-CTA clusters; a device that refuses it gets the
 // one-CTA global variant from then on.
-static bool g_rt_pair_refused[64] = {};
+static std::atomic<bool> g_rt_pair_refused[64];
 
 template <int EC, int NAX>
 static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmWh, const RouteArgs& a,
@@ -878,7 +883,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
     if constexpr (EC == 256) {
       int dev = 0;
       if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-      if (total >= 2 && !(dev >= 0 && dev < 64 && g_rt_pair_refused[dev])) {
+      if (total >= 2 && !(dev >= 0 && dev < 64 && g_rt_pair_refused[dev].load(std::memory_order_relaxed))) {
         const long long pitems = (total + 1) / 2 * Q;
         const int fit = rt_fit<EC, NAX, 2>(2) / 2;
         const int pairs = (int)(pitems < fit ? pitems : fit);
@@ -886,7 +891,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
             cudaSuccess)
           return 1;
         cudaGetLastError();
-        if (dev >= 0 && dev < 64) g_rt_pair_refused[dev] = true;
+        if (dev >= 0 && dev < 64) g_rt_pair_refused[dev].store(true, std::memory_order_relaxed);
       }
     }
     const long long items = total * Q;
