@@ -632,9 +632,10 @@ switch_status switch_forward_host(switch_handle h, const void* x_host, const flo
   const bool reuse = p->calls >= 2;  // slot k was used by the call before the previous one
   // copy in: after the layer of that call has read x from slot k
   if (reuse && cudaStreamWaitEvent(p->cin, p->fwd_done[k], 0) != cudaSuccess) return SWITCH_ERR_CUDA;
-  // In pieces of at most 16 MiB: a single copy of 100 MB from page-locked memory ran at
-  // 36-42 GB/s where the same bytes in 16 MiB pieces reached 54 GB/s (B300 hosts, PCIe).
-  constexpr size_t kCopyPiece = (size_t)16 << 20;
+  // In pieces of at most 4 MiB: single host-to-device copies from page-locked memory ran at
+  // 10-30 GB/s (12.6 MB) and 36-42 GB/s (100 MB) on some B300 hosts, where pieces of a few
+  // MiB reached 50-54 GB/s; on the others the pieces cost nothing.
+  constexpr size_t kCopyPiece = (size_t)4 << 20;
   for (size_t off = 0; off < p->act_bytes; off += kCopyPiece)
     if (cudaMemcpyAsync(xs + off, static_cast<const uint8_t*>(x_host) + off, std::min(kCopyPiece, p->act_bytes - off),
                         cudaMemcpyHostToDevice, p->cin) != cudaSuccess)
