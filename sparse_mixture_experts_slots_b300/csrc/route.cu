@@ -162,6 +162,7 @@ __device__ __forceinline__ bool top_before(float v, int i, float w, int j) {
 }
 
 constexpr int TOP2_THREADS = 512;
+constexpr float ROUTE_LOG2E = 1.4426950408889634f;
 
 __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
     const float* __restrict__ z, int T, int E, int nT, int32_t* __restrict__ expert, int32_t* __restrict__ expert2,
@@ -172,10 +173,12 @@ __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
   griddep_launch_dependents();
   // [2E] ints: first choices, then second choices; [nch E] floats: column partials; with
   // `staged`, the tile's logits [ROUTE_TILE][E] (each token's row becomes its probabilities)
-  extern __shared__ int32_t hist[];
+  extern __shared__ __align__(16) int32_t hist[];
   int32_t* hist2 = hist + E;
-  __shared__ float m_s[ROUTE_TILE], s_s[ROUTE_TILE], zz_s[ROUTE_TILE];
+  __shared__ float m_s[ROUTE_TILE], r_s[ROUTE_TILE], zz_s[ROUTE_TILE];  // max, 1 / sum exp, lse^2
   __shared__ int a_s[ROUTE_TILE], a2_s[ROUTE_TILE];
+  __shared__ uint64_t stage_bar;
+  __shared__ int stage_ok;
   const int g = blockIdx.y, tile = blockIdx.x;
   const int t0 = tile * ROUTE_TILE;
   const int len = min(ROUTE_TILE, T - t0);
@@ -183,15 +186,29 @@ __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
   for (int e = threadIdx.x; e < 2 * E; e += blockDim.x) hist[e] = 0;
   const int nch = E >= (int)blockDim.x ? 1 : (int)blockDim.x / E;
   float* zt = reinterpret_cast<float*>(hist + 2 * E) + (size_t)nch * E;  // staged logits
-  if (staged) {  // the tile's rows are contiguous: 16-byte loads when E allows
-    if ((E & 3) == 0) {
-      const float4* src = reinterpret_cast<const float4*>(z + tok0 * E);
-      for (int k = threadIdx.x; k < len * E / 4; k += blockDim.x) reinterpret_cast<float4*>(zt)[k] = src[k];
-    } else {
-      for (int k = threadIdx.x; k < len * E; k += blockDim.x) zt[k] = z[tok0 * E + k];
-    }
+  // The tile's rows are contiguous: one bulk copy into shared memory when E allows 16-byte
+  // alignment (E % 4 == 0; at most 200 KB, under an mbarrier's transaction limit).
+  const bool bulk = staged && (E & 3) == 0;
+  if (bulk && threadIdx.x == 0) {
+    mbar_init(&stage_bar, 1);
+    fence_mbar_init();
   }
   __syncthreads();
+  if (bulk) {
+    if (threadIdx.x == 0) {
+      const uint32_t bytes = (uint32_t)((size_t)len * E * sizeof(float));
+      mbar_arrive_expect_tx(&stage_bar, bytes);
+      bulk_load(zt, z + tok0 * E, bytes, &stage_bar);
+      stage_ok = mbar_wait(&stage_bar, 0) ? 1 : 0;
+    }
+  } else if (staged) {
+    for (int k = threadIdx.x; k < len * E; k += blockDim.x) zt[k] = z[tok0 * E + k];
+  }
+  __syncthreads();
+  if (bulk && !stage_ok) {  // the copy never landed (bounded wait): report, leave the tile
+    if (threadIdx.x == 0) raise_error(err, ERR_TIMEOUT);
+    return;
+  }
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
   for (int i = warp; i < len; i += nwarps) {
@@ -224,23 +241,26 @@ __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
       m1 = zr[0];
       m2 = zr[1];
     }
+    // exp(z - m1) as 2^(z log2 e - m1 log2 e) on the special-function unit
+    const float m1s = m1 * ROUTE_LOG2E;
     float s = 0.f;
-    for (int e = lane; e < E; e += 32) s += expf(zr[e] - m1);
+    for (int e = lane; e < E; e += 32) s += ex2_approx(fmaf(zr[e], ROUTE_LOG2E, -m1s));
     s = warp_sum(s);
+    const float rs = 1.0f / s;
     if (staged) {  // the row's probabilities in place (each lane rewrites only what it read)
       float* pr = zt + (size_t)i * E;
       for (int e = lane; e < E; e += 32) {
-        const float pv = expf(pr[e] - m1) / s;
+        const float pv = ex2_approx(fmaf(pr[e], ROUTE_LOG2E, -m1s)) * rs;
         pr[e] = pv;
         if (probs) probs[(tok0 + i) * E + e] = pv;
       }
     }
     if (lane == 0) {
       m_s[i] = m1;
-      s_s[i] = s;
+      r_s[i] = rs;
       a_s[i] = i1;
       a2_s[i] = i2;
-      const float u = expf(m2 - m1);  // the pair's softmax: 1 / (1 + u) and u / (1 + u)
+      const float u = ex2_approx((m2 - m1) * ROUTE_LOG2E);  // the pair's softmax: 1 / (1 + u), u / (1 + u)
       expert[tok0 + i] = i1;
       expert2[tok0 + i] = i2;
       gate[tok0 + i] = 1.0f / (1.0f + u);
@@ -280,7 +300,7 @@ __global__ void __launch_bounds__(TOP2_THREADS) route_top2_kernel(
       for (int i = c * clen; i < i1; ++i) acc += zt[(size_t)i * E + e];
     } else {
       for (int i = c * clen; i < i1; ++i) {
-        const float p = expf(z[(tok0 + i) * E + e] - m_s[i]) / s_s[i];
+        const float p = ex2_approx(fmaf(z[(tok0 + i) * E + e], ROUTE_LOG2E, -m_s[i] * ROUTE_LOG2E)) * r_s[i];
         acc += p;
         if (probs) probs[(tok0 + i) * E + e] = p;
       }
