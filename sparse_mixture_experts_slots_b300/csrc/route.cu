@@ -549,12 +549,18 @@ int launch_route(const RouteArgs& a, cudaStream_t s) {
   const long long N = (long long)a.G * a.T;
   const int nT = (a.T + ROUTE_TILE - 1) / ROUTE_TILE;
   int launches = 0;
-  if (N > 0 && a.top2) {
+  if (N > 0 && a.top2 && a.x_bf16 && router_tc_top2_fused(a.E, a.d)) {
+    // top-2 in the tensor-core router's own pass (no float32 logits round trip)
+    const int n = launch_router_tc(a, a.slot, s);
+    if (n < 0) return -1;
+    launches += n;
+  } else if (N > 0 && a.top2) {
     // top-2: float32 logits from the router (tensor cores for bf16 x: its own top-1
     // outputs are overwritten below), then the per-tile top-2 pass
     if (a.x_bf16) {
       RouteArgs b = a;
       b.logits_out = a.logits;
+      b.top2 = false;
       const int n = launch_router_tc(b, a.slot, s);
       if (n < 0) return -1;
       launches += n;

@@ -144,7 +144,8 @@ struct RtBars {
 };
 
 // Epilogue scratch (outside the rings: the next tile's copies land while it is in use).
-template <int EC>
+// T2 (top-2 routing): the second choices' partials, receive buffers and counts as well.
+template <int EC, bool T2 = false>
 struct RtScratch {
   float red_m[4][RT_BM];  // per column group: max logit of each token
   int red_a[4][RT_BM];    // per column group: argmax
@@ -158,18 +159,27 @@ struct RtScratch {
   float colsum[4][EC];    // per lane quadrant: probability sums of the columns
   int hist[EC];
   float bias[EC];
+  float red_m2[T2 ? 4 : 1][RT_BM];  // (T2) per column group: second-highest logit and its expert
+  int red_a2[T2 ? 4 : 1][RT_BM];
+  int rm2[T2 ? 8 : 1][RT_BM];       // (T2) receive buffer: each slice's second logit (bits) and expert
+  int ra2[T2 ? 8 : 1][RT_BM];
+  float M2all[T2 ? RT_BM : 1];      // (T2) second-highest logit over all experts
+  int texp2[T2 ? RT_BM : 1];        // (T2) second choice per token (-1 past the group's end)
+  int hist2[T2 ? EC : 1];
 };
 
-template <int EC, int NAX, bool PAIR = false>
+template <int EC, int NAX, bool PAIR = false, bool T2 = false>
 constexpr int rt_smem_bytes() {
   using Cf = RtCfg<EC, NAX, PAIR>;
-  return Cf::RING_BYTES + (int)sizeof(RtScratch<EC>) + (int)sizeof(RtBars<Cf::XS, Cf::WS>) + 1024;
+  return Cf::RING_BYTES + (int)sizeof(RtScratch<EC, T2>) + (int)sizeof(RtBars<Cf::XS, Cf::WS>) + 1024;
 }
 static_assert(rt_smem_bytes<256, 1>() <= 227 * 1024 && rt_smem_bytes<256, 2>() <= 227 * 1024 &&
                   rt_smem_bytes<128, 1>() <= 227 * 1024 && rt_smem_bytes<128, 2>() <= 227 * 1024 &&
                   rt_smem_bytes<64, 2>() <= 227 * 1024 && rt_smem_bytes<16, 1>() <= 227 * 1024 &&
                   rt_smem_bytes<256, 1, true>() <= 227 * 1024 && rt_smem_bytes<256, 2, true>() <= 227 * 1024,
               "rings and scratch fit in one SM's shared memory");
+static_assert(rt_smem_bytes<64, 2, false, true>() <= 227 * 1024,
+              "the top-2 scratch fits too (with two-atom x stages; d % 128 != 0 keeps the separate top-2 pass)");
 
 // Sum of p over the 32 lanes for 8 columns at once (reduce-scatter).  On return, lane L
 // holds the warp's total of column (L >> 2) & 7 (lanes 4c .. 4c + 3 agree).
@@ -195,6 +205,27 @@ __device__ __forceinline__ float warp_colsum8(const float* p, int lane) {
   return v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
 }
 
+// (m1, a1, m2, a2) <- the two highest of (m1, a1, m2, a2) and (n1, b1, n2, b2), where every
+// expert of the second pair ranks after every expert of the first (a later column group or
+// slice): ties go to the first pair, i.e. to the lower expert index.
+__device__ __forceinline__ void top2_merge(float& m1, int& a1, float& m2, int& a2, float n1, int b1, float n2,
+                                           int b2) {
+  if (n1 > m1) {
+    if (m1 >= n2) {
+      m2 = m1;
+      a2 = a1;
+    } else {
+      m2 = n2;
+      a2 = b2;
+    }
+    m1 = n1;
+    a1 = b1;
+  } else if (n1 > m2) {
+    m2 = n1;
+    a2 = b1;
+  }
+}
+
 // Named barrier over the 16 epilogue warps (the producer and MMA warps do not take part).
 __device__ __forceinline__ void rt_epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * RT_EPI_WARPS) : "memory"); }
 
@@ -212,16 +243,21 @@ __device__ __forceinline__ void rt_epi_sync() { asm volatile("bar.sync 1, %0;" :
 // copies count on the even CTA's barriers, the MMAs' completions arrive on both CTAs'.
 // Exchange rows (XM >= 1): xms / xam [tile id][Q][128], xflag [tile id][Q]; xctl[0] the
 // epoch of the last launch, xctl[1] the finish ticket (zero between launches).
-template <int EC, int NAX, int XM>
+// T2 (clusters only): top-2 routing in the same pass; expert2 / gate2 / rank2 / tile_hist2
+// take the second choices, gate / gate2 the softmax over the two chosen logits.
+template <int EC, int NAX, int XM, bool T2 = false>
 __global__ void __launch_bounds__(RT_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmWh, const float* __restrict__ br, int T, int E, int d, int nT, int Q, int total_tiles,
                      int32_t* __restrict__ expert, float* __restrict__ gate, int32_t* __restrict__ rank,
                      int32_t* __restrict__ tile_hist, float* __restrict__ tile_P, float* __restrict__ tile_Z,
                      float* __restrict__ logits, float* __restrict__ probs, uint32_t* err, float2* __restrict__ xms,
-                     int* __restrict__ xam, uint32_t* __restrict__ xflag, uint32_t* __restrict__ xctl) {
+                     int* __restrict__ xam, uint32_t* __restrict__ xflag, uint32_t* __restrict__ xctl,
+                     int32_t* __restrict__ expert2, float* __restrict__ gate2, int32_t* __restrict__ rank2,
+                     int32_t* __restrict__ tile_hist2) {
   constexpr bool GX = XM >= 1, P2 = XM == 2;
   static_assert(!P2 || EC == 256, "CTA pairs split 256-row W boxes");
+  static_assert(!T2 || XM == 0, "top-2 routing in the router: the slices meet in a cluster");
   using Cf = RtCfg<EC, NAX, P2>;
   using Gm = RtGeom<EC>;
   constexpr int XS = Cf::XS, WS = Cf::WS, NBUF = Gm::NBUF;
@@ -229,8 +265,9 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* xring = smem;
   uint8_t* wring = smem + Cf::X_BYTES;
-  RtScratch<EC>& sh = *reinterpret_cast<RtScratch<EC>*>(smem + Cf::RING_BYTES);
-  RtBars<XS, WS>& bar = *reinterpret_cast<RtBars<XS, WS>*>(smem + Cf::RING_BYTES + sizeof(RtScratch<EC>));
+  using Scr = RtScratch<EC, T2>;
+  Scr& sh = *reinterpret_cast<Scr*>(smem + Cf::RING_BYTES);
+  RtBars<XS, WS>& bar = *reinterpret_cast<RtBars<XS, WS>*>(smem + Cf::RING_BYTES + sizeof(Scr));
 
   // work items: (clusters) the tiles of this cluster, slice fixed by the cluster rank;
   // (global) tile it / Q, slice it % Q
@@ -290,6 +327,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     const int e = qc * EC + c;  // (global: reloaded per item)
     sh.bias[c] = e < E ? (br ? br[e] : 0.f) : -INFINITY;  // padding experts never win and weigh 0
     sh.hist[c] = 0;
+    if (T2) sh.hist2[c] = 0;
   }
   __syncthreads();
 
@@ -473,8 +511,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       // pass 1: logits z (+ bias) into registers; max / argmax over this warp's columns
       // (increasing e with strict >, so the lowest index wins a tie)
       float v[CPW];
-      float m = -INFINITY;
-      int a = INT_MAX;
+      float m = -INFINITY, m2 = -INFINITY;  // (T2) m2, a2: the second-highest logit and its expert
+      int a = INT_MAX, a2 = INT_MAX;
       if (has_cols) {
 #pragma unroll
         for (int ch = 0; ch < CPW / 8; ++ch) {
@@ -510,7 +548,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
                                                     : __uint_as_float(r1[j]);
             const float z = (__uint_as_float(h[j]) + corr) + sh.bias[c];
             v[ch * 8 + j] = z;
-            if (z > m) { m = z; a = e0 + c; }  // padding experts: z = -inf
+            if (z > m) {  // padding experts: z = -inf
+              if (T2) { m2 = m; a2 = a; }
+              m = z;
+              a = e0 + c;
+            } else if (T2 && z > m2) {
+              m2 = z;
+              a2 = e0 + c;
+            }
           }
           if (logits && valid) {  // the chunk's 8 logits of this token: 16-byte stores when aligned
             const int c0 = e0 + cbeg + ch * 8;
@@ -542,13 +587,23 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       if (has_cols) {
         sh.red_m[cg][i] = m;
         sh.red_a[cg][i] = a;
+        if (T2) {
+          sh.red_m2[cg][i] = m2;
+          sh.red_a2[cg][i] = a2;
+        }
       }
       rt_epi_sync();
-      float mc = -INFINITY;  // max over this CTA's experts
-      int ac = INT_MAX;
+      float mc = -INFINITY, mc2 = -INFINITY;  // max (and, T2, second) over this CTA's experts
+      int ac = INT_MAX, ac2 = INT_MAX;
 #pragma unroll
-      for (int k = 0; k < NCG; ++k)
-        if (sh.red_m[k][i] > mc) { mc = sh.red_m[k][i]; ac = sh.red_a[k][i]; }
+      for (int k = 0; k < NCG; ++k) {
+        if (T2)
+          top2_merge(mc, ac, mc2, ac2, sh.red_m[k][i], sh.red_a[k][i], sh.red_m2[k][i], sh.red_a2[k][i]);
+        else if (sh.red_m[k][i] > mc) {
+          mc = sh.red_m[k][i];
+          ac = sh.red_a[k][i];
+        }
+      }
 
       // pass 1b: exp(z - mc) in registers, partial sums
       float ps = 0.f;
@@ -570,8 +625,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
           bar.abort_flag = 1;
           ok = 0;
         }
-        // arm this CTA's receive barrier for the tile: Q slices of 12 bytes per token
-        mbar_arrive_expect_tx(&bar.rfull, (uint32_t)(Q * RT_BM * 12));
+        // arm this CTA's receive barrier for the tile: Q slices of 12 (T2: 20) bytes per token
+        mbar_arrive_expect_tx(&bar.rfull, (uint32_t)(Q * RT_BM * (T2 ? 20 : 12)));
         bar.ep_ok = ok;
       }
       rt_epi_sync();
@@ -587,10 +642,18 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
           for (int rk = 0; rk < Q; ++rk) {
             st_async_v2_f32(&sh.rms[q][i], mc, sc, &bar.rfull, (uint32_t)rk);
             st_async_s32(&sh.ra[q][i], ac, &bar.rfull, (uint32_t)rk);
+            if (T2) {
+              st_async_s32(&sh.rm2[q][i], __float_as_int(mc2), &bar.rfull, (uint32_t)rk);
+              st_async_s32(&sh.ra2[q][i], ac2, &bar.rfull, (uint32_t)rk);
+            }
           }
         } else {
           sh.rms[0][i] = make_float2(mc, sc);
           sh.ra[0][i] = ac;
+          if (T2) {
+            sh.rm2[0][i] = __float_as_int(mc2);
+            sh.ra2[0][i] = ac2;
+          }
         }
       }
       bool xok = true;
@@ -636,8 +699,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         rt_epi_sync();
       }
       if (cg == 0) {
-        float M = -INFINITY, S = 0.f;
-        int A = INT_MAX;
+        float M = -INFINITY, S = 0.f, M2 = -INFINITY;
+        int A = INT_MAX, A2 = INT_MAX;
         if (xok && GX) {  // expert slices in order: the lowest index wins a tie
           float2 ms[8];  // every slice's pair in flight at once (Q <= 8)
 #pragma unroll
@@ -657,7 +720,9 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         } else if (xok) {  // expert slices in rank order: the lowest index wins a tie
           for (int rk = 0; rk < Q; ++rk) {
             const float mr = sh.rms[rk][i].x;
-            if (mr > M) {
+            if (T2) {
+              top2_merge(M, A, M2, A2, mr, sh.ra[rk][i], __int_as_float(sh.rm2[rk][i]), sh.ra2[rk][i]);
+            } else if (mr > M) {
               M = mr;
               A = sh.ra[rk][i];
             }
@@ -670,6 +735,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         if (A < 0 || A >= E) {  // only non-finite logits (or a failed exchange) get here
           if (valid) raise_error(err, ERR_BOUNDS);
           A = 0;
+        }
+        if (T2) {
+          if (A2 < 0 || A2 >= E || A2 == A) {  // the same (E >= 2)
+            if (valid) raise_error(err, ERR_BOUNDS);
+            A2 = A == 0 ? 1 : 0;
+          }
+          sh.M2all[i] = M2;
+          sh.texp2[i] = valid ? A2 : -1;
         }
         sh.Mall[i] = M;
         sh.Sall[i] = S;
@@ -701,6 +774,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       }
       const int A = sh.texp[i];
       if (cg == 0 && A >= e0 && A < e0 + EC) atomicAdd(&sh.hist[A - e0], 1);
+      if (T2) {
+        const int A2 = sh.texp2[i];
+        if (cg == 0 && A2 >= e0 && A2 < e0 + EC) atomicAdd(&sh.hist2[A2 - e0], 1);
+      }
       rt_epi_sync();
 
       const size_t tbase = ((size_t)g * nT + tile) * E;
@@ -714,8 +791,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         if (e < E) {
           tile_P[tbase + e] = ((sh.colsum[0][c] + sh.colsum[1][c]) + sh.colsum[2][c]) + sh.colsum[3][c];
           tile_hist[tbase + e] = sh.hist[c];
+          if (T2) tile_hist2[tbase + e] = sh.hist2[c];
         }
         sh.hist[c] = 0;  // for the next tile
+        if (T2) sh.hist2[c] = 0;
       }
       if (q == 0 && cg == 0) {
         // rank among the tile's earlier tokens with the same expert
@@ -727,6 +806,20 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
           expert[tok] = A;
           gate[tok] = 1.0f / sh.Sall[i];  // exp(z_A - M) / S with z_A = M; never renormalised
           rank[tok] = rk;
+        }
+        if (T2) {  // the second choice: its rank among the tile's second choices; the pair's softmax
+          const int A2 = sh.texp2[i];
+          const int key2 = valid ? A2 : -1 - lane;
+          const unsigned same2 = __match_any_sync(0xffffffffu, key2);
+          int rk2 = __popc(same2 & ((1u << lane) - 1u));
+          for (int j = 0; j < lq * 32; ++j) rk2 += sh.texp2[j] == A2;
+          if (valid) {
+            const float u = expf(sh.M2all[i] - sh.Mall[i]);
+            gate[tok] = 1.0f / (1.0f + u);
+            gate2[tok] = u / (1.0f + u);
+            expert2[tok] = A2;
+            rank2[tok] = rk2;
+          }
         }
       }
       rt_epi_sync();  // the tile's scratch is read before the next tile writes it
@@ -755,11 +848,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 // ---------------------------------------------------------------- host side
 // CTAs of router_tc_kernel<EC, NAX, XM> resident at once in clusters of cl CTAs (cached per
 // kernel, device and cluster size).
-template <int EC, int NAX, int XM>
+template <int EC, int NAX, int XM, bool T2 = false>
 static int rt_fit(int cl) {
   static std::atomic<int> cache[64][9];  // handles on several host threads may fill it
-  auto kern = router_tc_kernel<EC, NAX, XM>;
-  constexpr int smem = rt_smem_bytes<EC, NAX, XM == 2>();
+  auto kern = router_tc_kernel<EC, NAX, XM, T2>;
+  constexpr int smem = rt_smem_bytes<EC, NAX, XM == 2, T2>();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
   const bool cached = dev >= 0 && dev < 64 && cl >= 1 && cl <= 8;
@@ -810,6 +903,10 @@ static bool rt_global(int E) {
   const int EC = router_tc_experts_per_cta(E);
   return (E + EC - 1) / EC > 2;
 }
+bool router_tc_top2_fused(int E, int d) {
+  return E >= 2 && d % (2 * RT_BK) == 0 && !rt_global(E) && router_tc_experts_per_cta(E) <= 64;
+}
+
 size_t router_tc_exchange_bytes(long long tiles, int E) {
   if (!rt_global(E) || tiles <= 0) return 0;
   const int EC = router_tc_experts_per_cta(E);
@@ -831,12 +928,12 @@ static RtXchg rt_xchg(void* base, long long tiles, int Q) {
   return x;
 }
 
-template <int EC, int NAX, int XM>
+template <int EC, int NAX, int XM, bool T2 = false>
 static cudaError_t rt_launch(int grid, int cluster, bool coop, bool pdl, cudaStream_t s, const CUtensorMap& tmX,
                              const CUtensorMap& tmW, const CUtensorMap& tmWh, const RouteArgs& a, int nT, int Q,
                              int total, int32_t* rank, const RtXchg& x) {
-  auto kern = router_tc_kernel<EC, NAX, XM>;
-  constexpr int smem = rt_smem_bytes<EC, NAX, XM == 2>();
+  auto kern = router_tc_kernel<EC, NAX, XM, T2>;
+  constexpr int smem = rt_smem_bytes<EC, NAX, XM == 2, T2>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -866,7 +963,9 @@ static cudaError_t rt_launch(int grid, int cluster, bool coop, bool pdl, cudaStr
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, tmWh, a.br, a.T, a.E, a.d, nT, Q, total, a.expert, a.gate, rank,
-                            a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs, a.err, x.ms, x.am, x.flag, x.ctl);
+                            a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs, a.err, x.ms, x.am, x.flag, x.ctl,
+                            T2 ? a.expert2 : nullptr, T2 ? a.gate2 : nullptr, T2 ? a.slot2 : nullptr,
+                            T2 ? a.tile_hist2 : nullptr);
 }
 
 // CTA pairs need a cooperative launch of 2-CTA clusters; a device that refuses it gets the
@@ -878,6 +977,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
                      int nT, int Q, int32_t* rank, cudaStream_t s) {
   const long long total = (long long)a.G * nT;
   if (total * Q >= (1ll << 31)) return -1;
+  if (a.top2 && rt_global(a.E)) return -1;  // top-2 in the router: clusters only
   if (a.xchg && rt_global(a.E)) {
     const RtXchg x = rt_xchg(a.xchg, total, Q);
     if constexpr (EC == 256) {
@@ -901,6 +1001,17 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
                    cudaSuccess
                ? 1
                : -1;
+  }
+  if (a.top2) {  // top-2 routing in the router (slices of at most 64 experts, in one cluster)
+    if constexpr (EC <= 64 && NAX == 2) {
+      const int fit = rt_fit<EC, NAX, 0, true>(Q) / Q;
+      const int ncl = (int)(total < fit ? total : fit);
+      return rt_launch<EC, NAX, 0, true>(Q * ncl, Q, false, true, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank,
+                                         RtXchg{}) == cudaSuccess
+                 ? 1
+                 : -1;
+    }
+    return -1;
   }
   const int fit = rt_fit<EC, NAX, 0>(Q) / Q;
   const int ncl = (int)(total < fit ? total : fit);
