@@ -254,8 +254,8 @@ SWITCH_API switch_status switch_forward(switch_handle h, const void* x, const fl
  *   done_event != NULL (a cudaEvent_t the caller created): it is recorded after
  *     the copy out and `stream` does not wait; the results are in place once
  *     the event has completed.
- * The copy in is issued in pieces of at most 4 MiB (one large host-to-device copy
- * was measured slower than its pieces on some PCIe hosts of B300 machines).
+ * The copy in is issued in four pieces of at least 1 MiB (one large host-to-device copy
+ * was measured slower than a few pieces on some PCIe hosts of B300 machines).
  * The first call allocates the staging buffers (4 * N * d act elements) and
  * creates the copy streams, so it is not for use under stream capture.
  * Returns SWITCH_ERR_INVALID_ARG for NULL x_host / y_host with N > 0, else as

@@ -632,12 +632,13 @@ switch_status switch_forward_host(switch_handle h, const void* x_host, const flo
   const bool reuse = p->calls >= 2;  // slot k was used by the call before the previous one
   // copy in: after the layer of that call has read x from slot k
   if (reuse && cudaStreamWaitEvent(p->cin, p->fwd_done[k], 0) != cudaSuccess) return SWITCH_ERR_CUDA;
-  // In pieces of at most 4 MiB: single host-to-device copies from page-locked memory ran at
-  // 10-30 GB/s (12.6 MB) and 36-42 GB/s (100 MB) on some B300 hosts, where pieces of a few
-  // MiB reached 50-54 GB/s; on the others the pieces cost nothing.
-  constexpr size_t kCopyPiece = (size_t)4 << 20;
-  for (size_t off = 0; off < p->act_bytes; off += kCopyPiece)
-    if (cudaMemcpyAsync(xs + off, static_cast<const uint8_t*>(x_host) + off, std::min(kCopyPiece, p->act_bytes - off),
+  // In four pieces (of at least 1 MiB): single host-to-device copies from page-locked memory
+  // ran at 10-30 GB/s (12.6 MB) and 36-42 GB/s (100 MB) on some B300 hosts, where two to eight
+  // pieces reached 53-55 GB/s; many small pieces (<= 4 MiB) slowed the copies down when the
+  // copy out ran at the same time.
+  const size_t piece = std::max<size_t>((size_t)1 << 20, ((p->act_bytes + 3) / 4 + 4095) / 4096 * 4096);
+  for (size_t off = 0; off < p->act_bytes; off += piece)
+    if (cudaMemcpyAsync(xs + off, static_cast<const uint8_t*>(x_host) + off, std::min(piece, p->act_bytes - off),
                         cudaMemcpyHostToDevice, p->cin) != cudaSuccess)
       return SWITCH_ERR_CUDA;
   if (cudaEventRecord(p->in_done[k], p->cin) != cudaSuccess) return SWITCH_ERR_CUDA;

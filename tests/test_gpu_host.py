@@ -25,7 +25,7 @@ def _need_cuda():
 CASES = {
     # tensor-core FFN with the combine fused in, ragged routing tiles
     "host-tc": (LayerShape("host-tc", 2, 300, 256, 384, 8, 1.0), dict(expert_bias_std=0.05, router_bias_std=0.1)),
-    # x over several 4 MiB copy pieces, with a ragged last piece (11000 x 768 bf16)
+    # x in four copy pieces with a ragged last one (11000 x 768 bf16)
     "host-pieces": (LayerShape("host-pieces", 1, 11000, 768, 256, 8, 1.0), dict(router_bias_std=0.1)),
     # float32 activations: CUDA-core FFN and a separate combine
     "host-fp32": (dataclasses.replace(WORKLOADS["tiny-e16-fp32"], name="host-fp32", T=200, G=2),
