@@ -296,9 +296,13 @@ def run_train(args, shape):
     stream = torch.cuda.current_stream(dev)
     fw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     bw = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = None
     for i in range(args.warmup + args.steps):
         flush.fill_(1.0)
         k = i - args.warmup
+        if k == 0:
+            torch.cuda.synchronize(dev)
+            clocks = ClockSampler(dev.index)  # sampled over the timed steps
         if k >= 0:
             fw[k][0].record(stream)
         layer.forward(inp["x"], inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"], r=r, y=y,
@@ -309,6 +313,7 @@ def run_train(args, shape):
         if k >= 0:
             fw[k][1].record(stream)
     torch.cuda.synchronize(dev)
+    clk = clocks.stop() if clocks is not None else None
     layer.sync_status(stream)
     step_ms = sum(a.elapsed_time(b) for a, b in fw) / args.steps
     fwd_ms = sum(a.elapsed_time(b) for (a, _), b in zip(fw, bw)) / args.steps
@@ -348,6 +353,7 @@ def run_train(args, shape):
                       "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS,
                       "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 (FMA) x 2.032 GHz",
                       "algorithmic_flops": bwd_flops, "traffic": None}),
+        "clocks": clk,
     }), flush=True)
     return 0
 
