@@ -4,9 +4,11 @@ switch_forward launches only stream-ordered work, and the router's global exchan
 its epoch in device memory (advanced by the last CTA of each launch), so a replayed graph
 sees a fresh epoch every time.  Three expert counts cover the router's exchange modes:
 one 2-CTA cluster per tile (128 experts), one CTA per SM with the slices meeting in global
-memory (200 experts), and CTA pairs sharing each W box (1100 experts).  Replays alternate
-between two inputs; every output is compared bit for bit with an eager call on the same
-inputs (the same kernels in the same order).
+memory (200 experts), and CTA pairs sharing each W box (1100 experts); the top-2 layer runs
+with both choices taken in the router's own pass (128 experts) and in a pass of its own over
+the float32 logits (200 experts).  Replays alternate between two inputs; every output is
+compared bit for bit with an eager call on the same inputs (the same kernels in the same
+order).
 """
 import pytest
 import torch
@@ -24,24 +26,26 @@ def _need_cuda():
 
 
 FIELDS = ("expert", "slot", "keep", "gate", "row", "raw_count", "accepted_count", "P", "aux_loss", "expert_rows")
+FIELDS_TOP2 = FIELDS + ("expert2", "slot2", "keep2", "gate2", "row2")
 
 
-def _snapshot(y, r):
-    return y.clone(), {f: getattr(r, f).clone() for f in FIELDS}
+def _snapshot(y, r, fields):
+    return y.clone(), {f: getattr(r, f).clone() for f in fields}
 
 
-@pytest.mark.parametrize("E", [128, 200, 1100])
-def test_graph_replay_equals_eager(E):
-    shape = LayerShape(f"graph-e{E}", 1, 900, 128, 128, E, 1.0)
+@pytest.mark.parametrize("E,k", [(128, 1), (200, 1), (1100, 1), (128, 2), (200, 2)])
+def test_graph_replay_equals_eager(E, k):
+    fields = FIELDS_TOP2 if k == 2 else FIELDS
+    shape = LayerShape(f"graph-e{E}-top{k}", 1, 900, 128, 128, E, 1.0)
     a = make_inputs(shape, 3, "cuda", router_bias_std=0.1)
     b = make_inputs(shape, 4, "cuda", router_bias_std=0.1)
-    layer = P.make_layer(shape)
+    layer = P.make_layer(shape, top_k=k)
     w = (a["Wr"], a["br"], a["W1"], a["b1"], a["W2"], a["b2"])
     ref = []
     for inp in (a, b):  # eager calls (the first one also warms the library's caches)
         y, r = layer.forward(inp["x"], *w)
         torch.cuda.synchronize()
-        ref.append(_snapshot(y, r))
+        ref.append(_snapshot(y, r, fields))
     xs = a["x"].clone()
     rs = layer.alloc_route()
     ys = torch.empty_like(xs)
@@ -50,12 +54,12 @@ def test_graph_replay_equals_eager(E):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, capture_error_mode="relaxed"):
         layer.forward(xs, *w, r=rs, y=ys)
-    for k in (0, 1, 0, 1):
-        xs.copy_((a, b)[k]["x"])
+    for i in (0, 1, 0, 1):
+        xs.copy_((a, b)[i]["x"])
         g.replay()
         torch.cuda.synchronize()
-        y_ref, r_ref = ref[k]
-        assert torch.equal(ys, y_ref), f"replay on input {k}: y differs from the eager call"
-        for f in FIELDS:
-            assert torch.equal(getattr(rs, f), r_ref[f]), f"replay on input {k}: {f} differs"
+        y_ref, r_ref = ref[i]
+        assert torch.equal(ys, y_ref), f"replay on input {i}: y differs from the eager call"
+        for f in fields:
+            assert torch.equal(getattr(rs, f), r_ref[f]), f"replay on input {i}: {f} differs"
     layer.sync_status()
