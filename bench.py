@@ -172,10 +172,12 @@ class ExpertCache:
         return self.cache[e]
 
 
-def oracle_sample(shape, x, Wr, br, experts, n_ffn_tokens: int, top_k: int = 1):
-    """Time the fp64 oracle: routing of the whole batch + the expert FFN of a
-    sample of kept tokens (kept (token, choice) requests with top-2), scaled to the
-    batch.  x, Wr, br: float64 arrays; experts(e) -> float64 (W1[e], W2[e]).
+def oracle_sample(shape, x, Wr, br, experts, n_ffn_tokens: int, top_k: int = 1, n_route_tokens: int = 8192):
+    """Time the fp64 oracle on a bounded sample of the workload: routing of the first T'
+    tokens of every group (T' = min(T, n_route_tokens / G): a layer of the same shape on
+    those tokens, the whole batch when it is small) + the expert FFN of a sample of its kept
+    tokens (kept (token, choice) requests with top-2), the FFN time scaled to all its kept
+    tokens.  x, Wr, br: float64 arrays; experts(e) -> float64 (W1[e], W2[e]).
     Returns (tokens/s, detail)."""
     from oracle import switch_oracle as so
     try:
@@ -183,14 +185,18 @@ def oracle_sample(shape, x, Wr, br, experts, n_ffn_tokens: int, top_k: int = 1):
         threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
     except Exception:
         threads = os.cpu_count()
+    Ts = max(1, min(shape.T, n_route_tokens // shape.G))
+    if Ts < shape.T:  # the first Ts tokens of every group (groups are contiguous in x)
+        x = np.ascontiguousarray(x.reshape(shape.G, shape.T, -1)[:, :Ts].reshape(shape.G * Ts, -1))
+    Ns = shape.G * Ts
     t0 = time.perf_counter()
     if top_k == 2:
-        r = so.route_top2(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor)
+        r = so.route_top2(x, Wr, br, shape.G, Ts, shape.E, shape.capacity_factor)
         req_e = np.concatenate([r.expert[r.keep], r.expert2[r.keep2]])  # kept (token, choice) requests
         req_t = np.concatenate([np.flatnonzero(r.keep), np.flatnonzero(r.keep2)])
         req_g = np.concatenate([r.gate[r.keep], r.gate2[r.keep2]])
     else:
-        r = so.route(x, Wr, br, shape.G, shape.T, shape.E, shape.capacity_factor)
+        r = so.route(x, Wr, br, shape.G, Ts, shape.E, shape.capacity_factor)
         req_t = np.flatnonzero(r.keep)
         req_e = r.expert[req_t]
         req_g = r.gate[req_t]
@@ -207,9 +213,11 @@ def oracle_sample(shape, x, Wr, br, experts, n_ffn_tokens: int, top_k: int = 1):
         _ = req_g[sel, None] * o
     t_ffn = time.perf_counter() - t0
     t_total = t_route + t_ffn * req_t.size / max(1, pick.size)
-    return shape.N / t_total, {
+    what = f"all {shape.N} tokens" if Ts == shape.T else \
+        f"the first {Ts} of {shape.T} tokens of each of the {shape.G} group(s) ({Ns} tokens, as a layer of its own)"
+    return Ns / t_total, {
         "cores": threads,
-        "sample": (f"routing of all {shape.N} tokens + expert FFN/combine of {pick.size} of {req_t.size} kept "
+        "sample": (f"routing of {what} + expert FFN/combine of {pick.size} of its {req_t.size} kept "
                    f"{'requests' if top_k == 2 else 'tokens'}, FFN time scaled by {req_t.size}/{pick.size}"),
         "t_route_s": t_route, "t_ffn_sample_s": t_ffn}
 
@@ -242,7 +250,7 @@ def run_reference(args, shape):
     vals = []
     detail = {}
     for i in range(args.warmup + args.steps):
-        v, detail = oracle_sample(shape, x, Wr, br, experts, args.ref_ffn_tokens, args.top_k)
+        v, detail = oracle_sample(shape, x, Wr, br, experts, args.ref_ffn_tokens, args.top_k, args.ref_route_tokens)
         if i >= args.warmup:
             vals.append(v)
     value = float(np.mean(vals))
@@ -583,7 +591,7 @@ def run_gpu(args, shape):
     if not args.no_cpu_baseline and world == 1:
         x64, Wr64, br64 = host_f64(inp)
         v, det = oracle_sample(shape, x64, Wr64, br64, ExpertCache(lambda e: (inp["W1"][e], inp["W2"][e])),
-                               args.ref_ffn_tokens, args.top_k)
+                               args.ref_ffn_tokens, args.top_k, args.ref_route_tokens)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": det["cores"], "kind": "oracle",
                                 "sample": det["sample"]}
     print(json.dumps(line), flush=True)
@@ -600,6 +608,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--ref-ffn-tokens", type=int, default=256)
+    ap.add_argument("--ref-route-tokens", type=int, default=8192,
+                    help="tokens the fp64 oracle routes per timed sample (the first ones of each group)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--train", action="store_true",
                     help="time a training step (forward in training mode + switch_backward)")

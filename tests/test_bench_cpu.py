@@ -91,3 +91,23 @@ def test_roofline_arithmetic_matches_the_hand_count():
     assert w["ffn_bytes"] == 2 * 128 * 3072 * 768 * 2 + 2 * 7484 * 768 * 2 == 1230950400
     assert w["ffn_flops"] == 4.0 * 7484 * 768 * 3072
     assert bench.FP32_ALU_TFLOPS == 148 * 128 * 2 * 2.032 / 1e3
+
+
+def test_oracle_sample_bounds_its_routing():
+    # the timed oracle routes the first T' = n_route_tokens / G tokens of every group as a
+    # layer of its own when the batch is larger, and the whole batch otherwise
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from gen import LayerShape, make_inputs
+    shape = LayerShape("sample", 2, 300, 16, 8, 4, 1.0, dtype="f32")
+    inp = make_inputs(shape, 5, "cpu")
+    x, Wr, br = bench.host_f64(inp)
+    experts = bench.ExpertCache(lambda e: (inp["W1"][e], inp["W2"][e]))
+    v, det = bench.oracle_sample(shape, x, Wr, br, experts, 16, 1, n_route_tokens=200)
+    assert v > 0 and "the first 100 of 300 tokens of each of the 2 group(s) (200 tokens" in det["sample"]
+    v, det = bench.oracle_sample(shape, x, Wr, br, experts, 16, 1, n_route_tokens=8192)
+    assert v > 0 and det["sample"].startswith("routing of all 600 tokens")
+    v, det = bench.oracle_sample(shape, x, Wr, br, experts, 16, 2, n_route_tokens=200)
+    assert v > 0 and "requests" in det["sample"]
+    assert np.isfinite(det["t_route_s"])
