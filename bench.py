@@ -590,8 +590,10 @@ def run_gpu(args, shape):
     }
     if not args.no_cpu_baseline and world == 1:
         x64, Wr64, br64 = host_f64(inp)
-        v, det = oracle_sample(shape, x64, Wr64, br64, ExpertCache(lambda e: (inp["W1"][e], inp["W2"][e])),
-                               args.ref_ffn_tokens, args.top_k, args.ref_route_tokens)
+        cache = ExpertCache(lambda e: (inp["W1"][e], inp["W2"][e]))
+        for _ in range(2):  # one untimed warm-up sample (BLAS threads, page faults), then the timed one
+            v, det = oracle_sample(shape, x64, Wr64, br64, cache, args.ref_ffn_tokens, args.top_k,
+                                   args.ref_route_tokens)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": det["cores"], "kind": "oracle",
                                 "sample": det["sample"]}
     print(json.dumps(line), flush=True)
