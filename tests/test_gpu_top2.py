@@ -33,6 +33,9 @@ CASES = {
     "top2-many-experts": (LayerShape("top2-many-experts", 1, 700, 128, 128, 300, 1.0), {}),
     # two 128-row weight blocks per FFN tile, 256-row token chunks
     "top2-two-blocks": (LayerShape("top2-two-blocks", 1, 600, 256, 512, 4, 1.0), dict(expert_bias_std=0.05)),
+    # both choices in the router's pass with two 64-expert slices per cluster (100 experts,
+    # the second slice partly padding), two groups with ragged tiles
+    "top2-cluster": (LayerShape("top2-cluster", 2, 300, 256, 384, 100, 1.0), dict(router_bias_std=0.2)),
 }
 
 
