@@ -192,7 +192,8 @@ switch_status switch_create(const switch_config* cfg, switch_handle* out) {
   const bool train = training_of(cfg);
   const size_t o_logits = take(cfg->dtype == SWITCH_F32 || two || train ? N * E * sizeof(float) : 0);
   const size_t o_wsplit = take(cfg->dtype == SWITCH_BF16 ? router_tc_wsplit_bytes(cfg->E, cfg->d_model) : 0);
-  const size_t xchg_bytes = cfg->dtype == SWITCH_BF16 ? router_tc_exchange_bytes((long long)(G * nT), cfg->E) : 0;
+  const size_t xchg_bytes =
+      cfg->dtype == SWITCH_BF16 ? router_tc_exchange_bytes((long long)(G * nT), cfg->E, two) : 0;
   const size_t o_xchg = take(xchg_bytes);
   const size_t o_part = take(G * (size_t)route_scan_blocks(cfg->E) * sizeof(float));
   const size_t ffn_words = ffn_counter_words(cfg->E, (int)R, cfg->d_model, cfg->d_ff);

@@ -243,8 +243,9 @@ __device__ __forceinline__ void rt_epi_sync() { asm volatile("bar.sync 1, %0;" :
 // copies count on the even CTA's barriers, the MMAs' completions arrive on both CTAs'.
 // Exchange rows (XM >= 1): xms / xam [tile id][Q][128], xflag [tile id][Q]; xctl[0] the
 // epoch of the last launch, xctl[1] the finish ticket (zero between launches).
-// T2 (clusters only): top-2 routing in the same pass; expert2 / gate2 / rank2 / tile_hist2
-// take the second choices, gate / gate2 the softmax over the two chosen logits.
+// T2 (not with CTA pairs): top-2 routing in the same pass; expert2 / gate2 / rank2 / tile_hist2
+// take the second choices, gate / gate2 the softmax over the two chosen logits; with the
+// slices meeting in global memory each slice's second logit and expert go through xm2 / xa2.
 template <int EC, int NAX, int XM, bool T2 = false>
 __global__ void __launch_bounds__(RT_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -254,10 +255,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
                      float* __restrict__ logits, float* __restrict__ probs, uint32_t* err, float2* __restrict__ xms,
                      int* __restrict__ xam, uint32_t* __restrict__ xflag, uint32_t* __restrict__ xctl,
                      int32_t* __restrict__ expert2, float* __restrict__ gate2, int32_t* __restrict__ rank2,
-                     int32_t* __restrict__ tile_hist2) {
+                     int32_t* __restrict__ tile_hist2, float* __restrict__ xm2, int* __restrict__ xa2) {
   constexpr bool GX = XM >= 1, P2 = XM == 2;
   static_assert(!P2 || EC == 256, "CTA pairs split 256-row W boxes");
-  static_assert(!T2 || XM == 0, "top-2 routing in the router: the slices meet in a cluster");
+  static_assert(!T2 || XM <= 1, "top-2 routing in the router: slices meeting in a cluster or in global memory");
   using Cf = RtCfg<EC, NAX, P2>;
   using Gm = RtGeom<EC>;
   constexpr int XS = Cf::XS, WS = Cf::WS, NBUF = Gm::NBUF;
@@ -638,6 +639,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         if (GX) {
           xms[(xrow + q) * RT_BM + i] = make_float2(mc, sc);
           xam[(xrow + q) * RT_BM + i] = ac;
+          if (T2) {
+            xm2[(xrow + q) * RT_BM + i] = mc2;
+            xa2[(xrow + q) * RT_BM + i] = ac2;
+          }
         } else if (Q > 1) {  // into slot q of every peer's receive buffer
           for (int rk = 0; rk < Q; ++rk) {
             st_async_v2_f32(&sh.rms[q][i], mc, sc, &bar.rfull, (uint32_t)rk);
@@ -717,6 +722,21 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 #pragma unroll
           for (int rk = 0; rk < 8; ++rk)
             if (rk < Q && ms[rk].y > 0.f) S += ms[rk].y * expf(ms[rk].x - M);
+          if (T2) {  // second: the best slice's own second, or the best first of another slice
+            float Mo = -INFINITY;
+            int ko = -1;
+#pragma unroll
+            for (int rk = 0; rk < 8; ++rk)
+              if (rk < Q && rk != kb && ms[rk].x > Mo) {
+                Mo = ms[rk].x;
+                ko = rk;
+              }
+            const float mk2 = __ldcg(xm2 + (xrow + kb) * RT_BM + i);
+            // on a tie the lower expert index wins: slice ko's experts rank before kb's when ko < kb
+            const bool other = ko >= 0 && (Mo > mk2 || (Mo == mk2 && ko < kb));
+            M2 = other ? Mo : mk2;
+            A2 = other ? __ldcg(xam + (xrow + ko) * RT_BM + i) : __ldcg(xa2 + (xrow + kb) * RT_BM + i);
+          }
         } else if (xok) {  // expert slices in rank order: the lowest index wins a tie
           for (int rk = 0; rk < Q; ++rk) {
             const float mr = sh.rms[rk][i].x;
@@ -897,6 +917,8 @@ struct RtXchg {
   int* am;
   uint32_t* flag;
   uint32_t* ctl;
+  float* m2;  // (top-2) each slice's second logit and expert per token
+  int* a2;
 };
 static size_t rt_round256(size_t b) { return (b + 255) / 256 * 256; }
 static bool rt_global(int E) {
@@ -904,15 +926,16 @@ static bool rt_global(int E) {
   return (E + EC - 1) / EC > 2;
 }
 bool router_tc_top2_fused(int E, int d) {
-  return E >= 2 && d % (2 * RT_BK) == 0 && !rt_global(E) && router_tc_experts_per_cta(E) <= 64;
+  return E >= 2 && d % (2 * RT_BK) == 0 && router_tc_experts_per_cta(E) <= 64;
 }
 
-size_t router_tc_exchange_bytes(long long tiles, int E) {
+size_t router_tc_exchange_bytes(long long tiles, int E, bool top2) {
   if (!rt_global(E) || tiles <= 0) return 0;
   const int EC = router_tc_experts_per_cta(E);
   const size_t n = (size_t)tiles * (size_t)((E + EC - 1) / EC);
   return rt_round256(n * RT_BM * sizeof(float2)) + rt_round256(n * RT_BM * sizeof(int)) +
-         rt_round256(n * sizeof(uint32_t)) + 256;
+         rt_round256(n * sizeof(uint32_t)) + 256 +
+         (top2 ? rt_round256(n * RT_BM * sizeof(float)) + rt_round256(n * RT_BM * sizeof(int)) : 0);
 }
 static RtXchg rt_xchg(void* base, long long tiles, int Q) {
   uint8_t* p = static_cast<uint8_t*>(base);
@@ -925,6 +948,10 @@ static RtXchg rt_xchg(void* base, long long tiles, int Q) {
   x.flag = reinterpret_cast<uint32_t*>(p);
   p += rt_round256(n * sizeof(uint32_t));
   x.ctl = reinterpret_cast<uint32_t*>(p);
+  p += 256;
+  x.m2 = reinterpret_cast<float*>(p);  // present only in buffers sized for top-2
+  p += rt_round256(n * RT_BM * sizeof(float));
+  x.a2 = reinterpret_cast<int*>(p);
   return x;
 }
 
@@ -965,7 +992,8 @@ static cudaError_t rt_launch(int grid, int cluster, bool coop, bool pdl, cudaStr
   return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, tmWh, a.br, a.T, a.E, a.d, nT, Q, total, a.expert, a.gate, rank,
                             a.tile_hist, a.tile_P, a.tile_Z, a.logits_out, a.probs, a.err, x.ms, x.am, x.flag, x.ctl,
                             T2 ? a.expert2 : nullptr, T2 ? a.gate2 : nullptr, T2 ? a.slot2 : nullptr,
-                            T2 ? a.tile_hist2 : nullptr);
+                            T2 ? a.tile_hist2 : nullptr, T2 && XM >= 1 ? x.m2 : nullptr,
+                            T2 && XM >= 1 ? x.a2 : nullptr);
 }
 
 // CTA pairs need a cooperative launch of 2-CTA clusters; a device that refuses it gets the
@@ -977,9 +1005,20 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
                      int nT, int Q, int32_t* rank, cudaStream_t s) {
   const long long total = (long long)a.G * nT;
   if (total * Q >= (1ll << 31)) return -1;
-  if (a.top2 && rt_global(a.E)) return -1;  // top-2 in the router: clusters only
   if (a.xchg && rt_global(a.E)) {
     const RtXchg x = rt_xchg(a.xchg, total, Q);
+    if (a.top2) {  // top-2 in the router: one CTA per SM (no CTA pairs), slices of 64 experts
+      if constexpr (EC == 64 && NAX == 2) {
+        const long long items = total * Q;
+        const int fit = rt_fit<EC, NAX, 1, true>(1);
+        const int grid = (int)(items < fit ? items : fit);
+        return rt_launch<EC, NAX, 1, true>(grid, 1, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank,
+                                           x) == cudaSuccess
+                   ? 1
+                   : -1;
+      }
+      return -1;
+    }
     if constexpr (EC == 256) {
       int dev = 0;
       if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -1002,7 +1041,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
                ? 1
                : -1;
   }
-  if (a.top2) {  // top-2 routing in the router (slices of at most 64 experts, in one cluster)
+  if (a.top2) {  // top-2 routing in the router (slices of at most 64 experts meeting in a cluster)
     if constexpr (EC <= 64 && NAX == 2) {
       const int fit = rt_fit<EC, NAX, 0, true>(Q) / Q;
       const int ncl = (int)(total < fit ? total : fit);

@@ -36,6 +36,9 @@ CASES = {
     # both choices in the router's pass with two 64-expert slices per cluster (100 experts,
     # the second slice partly padding), two groups with ragged tiles
     "top2-cluster": (LayerShape("top2-cluster", 2, 300, 256, 384, 100, 1.0), dict(router_bias_std=0.2)),
+    # both choices in the router's pass with 8 slices meeting in global memory (512 experts),
+    # two groups with ragged tiles
+    "top2-global": (LayerShape("top2-global", 2, 700, 256, 256, 512, 1.0), dict(router_bias_std=0.2)),
 }
 
 
