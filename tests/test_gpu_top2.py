@@ -93,3 +93,29 @@ def test_top2_switch_base_full_size():
     P.compare_route_top2(r, ref, shape)
     tokens = np.sort(np.random.default_rng(1).choice(shape.N, 192, replace=False))
     P.check_y_top2(y, ref, inp, tokens)
+
+
+@pytest.mark.parametrize("E", [100, 200])
+def test_top2_exact_ties_across_slices(E):
+    # Router rows duplicated within one 64-expert slice (5 -> 6) and across slices (3 -> 70
+    # -> 140 where they exist): identical logits, so both choices follow the lowest-index rule
+    # through the column-group and slice merges (100 experts: a 2-CTA cluster; 200: slices
+    # meeting in global memory).  A shift on expert 3 makes it the usual winner.
+    shape = LayerShape(f"top2-ties-e{E}", 2, 300, 128, 128, E, 1.0)
+    inp = make_inputs(shape, 21, "cuda")
+    Wr = inp["Wr"]
+    for dst in (70, 140):
+        if dst < E:
+            Wr[dst].copy_(Wr[3])
+    Wr[6].copy_(Wr[5])
+    br = torch.zeros(E, dtype=torch.float32, device="cuda")
+    for e in (3, 70, 140):
+        if e < E:
+            br[e] = 0.5
+    inp["br"] = br
+    layer, r, xe, y, y2, r2 = _run(shape, inp)
+    ref, subst = P.oracle_route_top2(inp, shape, P.to_np(r.logits))
+    P.compare_route_top2(r, ref, shape)
+    P.check_y_top2(y, ref, inp, np.arange(shape.N))
+    e1, e2 = P.to_np(r.expert), P.to_np(r.expert2)
+    assert ((e1 == 3) & (e2 == 70)).sum() > 0, "the tie between experts 3 and 70 never decided both choices"
