@@ -1,4 +1,4 @@
-// Router of the top-1 Switch layer on 5th-generation tensor cores (tcgen05, sm_103a).
+// Router of the Switch layer on 5th-generation tensor cores (tcgen05, sm_103a).
 //
 // The router runs in float32 (selective precision: Switch Transformers card on
 // ai-papers.xuzou.cn, 方法适配; "042 · Switch Transformer：每个词只选一个专家",
@@ -49,6 +49,11 @@
 // Outputs per token: expert (raw choice), gate = p_{expert}, rank in tile; per
 // (group, tile, expert): token count and probability sum.  The cross-tile scan
 // that turns ranks into slots runs in route.cu.
+// Top-2 variant (T2, slices of up to 64 experts, clusters or the global exchange): the
+// second-highest logit and its expert ride along through pass 1, the column-group merge and
+// the exchange ("混合专家", world.lapla.si/zh/moe, 路由器只开两条线: the two highest
+// scores, weighted by the softmax over those two); the outputs add the second choice, its
+// gate and in-tile rank and the per-tile counts of second choices.
 #include <limits.h>
 
 #include <atomic>
