@@ -141,8 +141,8 @@ int launch_router_tc(const RouteArgs& a, int32_t* rank, cudaStream_t s);
 int launch_router_split(const float* Wr, void* wsplit, int E, int d, cudaStream_t s);
 int router_tc_experts_per_cta(int E);
 // With a.top2 the tensor-core router also takes the second choices (expert2, gate2, the
-// in-tile rank of second choices into slot2, tile_hist2) in its own pass: true for up to 512
-// experts (slices of at most 64) and d % 128 == 0.
+// in-tile rank of second choices into slot2, tile_hist2) in its own pass: true for up to 1024
+// experts (slices of at most 128) and d % 128 == 0.
 bool router_tc_top2_fused(int E, int d);
 int router_tc_mma_n(int EC);
 // Bytes of the split W_r workspace ([Q][d / 64 atoms][hi, mid, lo][EC][64] bf16) for E experts of width d.

@@ -49,7 +49,7 @@
 // Outputs per token: expert (raw choice), gate = p_{expert}, rank in tile; per
 // (group, tile, expert): token count and probability sum.  The cross-tile scan
 // that turns ranks into slots runs in route.cu.
-// Top-2 variant (T2, slices of up to 64 experts, clusters or the global exchange): the
+// Top-2 variant (T2, slices of up to 128 experts, clusters or the global exchange): the
 // second-highest logit and its expert ride along through pass 1, the column-group merge and
 // the exchange ("混合专家", world.lapla.si/zh/moe, 路由器只开两条线: the two highest
 // scores, weighted by the softmax over those two); the outputs add the second choice, its
@@ -183,7 +183,7 @@ static_assert(rt_smem_bytes<256, 1>() <= 227 * 1024 && rt_smem_bytes<256, 2>() <
                   rt_smem_bytes<64, 2>() <= 227 * 1024 && rt_smem_bytes<16, 1>() <= 227 * 1024 &&
                   rt_smem_bytes<256, 1, true>() <= 227 * 1024 && rt_smem_bytes<256, 2, true>() <= 227 * 1024,
               "rings and scratch fit in one SM's shared memory");
-static_assert(rt_smem_bytes<64, 2, false, true>() <= 227 * 1024,
+static_assert(rt_smem_bytes<64, 2, false, true>() <= 227 * 1024 && rt_smem_bytes<128, 2, false, true>() <= 227 * 1024,
               "the top-2 scratch fits too (with two-atom x stages; d % 128 != 0 keeps the separate top-2 pass)");
 
 // Sum of p over the 32 lanes for 8 columns at once (reduce-scatter).  On return, lane L
@@ -931,7 +931,7 @@ static bool rt_global(int E) {
   return (E + EC - 1) / EC > 2;
 }
 bool router_tc_top2_fused(int E, int d) {
-  return E >= 2 && d % (2 * RT_BK) == 0 && router_tc_experts_per_cta(E) <= 64;
+  return E >= 2 && d % (2 * RT_BK) == 0 && router_tc_experts_per_cta(E) <= 128;
 }
 
 size_t router_tc_exchange_bytes(long long tiles, int E, bool top2) {
@@ -1012,8 +1012,8 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
   if (total * Q >= (1ll << 31)) return -1;
   if (a.xchg && rt_global(a.E)) {
     const RtXchg x = rt_xchg(a.xchg, total, Q);
-    if (a.top2) {  // top-2 in the router: one CTA per SM (no CTA pairs), slices of 64 experts
-      if constexpr (EC == 64 && NAX == 2) {
+    if (a.top2) {  // top-2 in the router: one CTA per SM (no CTA pairs), slices of 64 or 128
+      if constexpr ((EC == 64 || EC == 128) && NAX == 2) {
         const long long items = total * Q;
         const int fit = rt_fit<EC, NAX, 1, true>(1);
         const int grid = (int)(items < fit ? items : fit);

@@ -39,6 +39,8 @@ CASES = {
     # both choices in the router's pass with 8 slices meeting in global memory (512 experts),
     # two groups with ragged tiles
     "top2-global": (LayerShape("top2-global", 2, 700, 256, 256, 512, 1.0), dict(router_bias_std=0.2)),
+    # the same with 128-expert slices (700 experts: 6 slices, the last partly padding)
+    "top2-global-128": (LayerShape("top2-global-128", 1, 900, 256, 256, 700, 1.0), dict(router_bias_std=0.2)),
 }
 
 
