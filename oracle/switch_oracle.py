@@ -297,7 +297,7 @@ def combine(r: Route, outputs: dict, tokens: Sequence[int], d: int) -> np.ndarra
     """y_t = p_{e*}(x_t) * f_{e*}(x_t) for kept tokens, 0 for dropped ones.
 
     [042, §一]: y = p_{e*(x)}(x) f_{e*(x)}(x); the selected gate multiplies the
-    expert output un-renormalised ([042] "只执行一个专家时检查路由是否被错误归一化":
+    expert output un-renormalised ([042], section 只执行一个专家时检查路由是否被错误归一化:
     a gate of 0.7 stays 0.7).  Dropped tokens get zero expert output and carry
     on through the residual, which is outside y [042, §一].
     """
