@@ -525,6 +525,70 @@ def run_gpu(args, shape):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, dist, dev)
 
+    # ---------------- (--sm-budget R,F) two batches in flight: two handles on two streams,
+    # each handle's router capped at R CTAs and its FFN at F, so the router of one batch (bound
+    # by the tensor cores) runs beside the FFN of the other (bound by the weights' bytes)
+    two = None
+    if args.sm_budget:
+        rc, fc = (int(v) for v in args.sm_budget.split(","))
+        x_b = make_inputs(shape, seed + 7919, dev, with_experts=False)["x"]
+        lays = [mk(False), mk(False)]
+        rr = [lays[0].alloc_route(), lays[1].alloc_route()]
+        yy = [torch.empty_like(y), torch.empty_like(y)]
+        sts = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        for lay in lays:
+            if prepared:
+                lay.prepare_router(inp["Wr"], stream=stream)
+            lay.set_sm_budget(rc, fc)
+        torch.cuda.synchronize(dev)
+
+        def two_step(i):
+            j = i % 2
+            lays[j].forward((inp["x"], x_b)[j], Wr_step, inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"],
+                            r=rr[j], y=yy[j], stream=sts[j])
+
+        for i in range(max(args.warmup, 4)):
+            two_step(i)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ta.record(stream)
+        for st in sts:
+            st.wait_event(ta)
+        for i in range(args.steps):
+            two_step(i)
+        for st in sts:
+            ev_end = torch.cuda.Event()
+            ev_end.record(st)
+            stream.wait_event(ev_end)
+        tb.record(stream)
+        torch.cuda.synchronize(dev)
+        two_ms = max_over_ranks(ta.elapsed_time(tb), dist, dev)
+        # the same alternating batches on one stream with no budgets and no L2 flush: the
+        # like-for-like single-stream time
+        for lay in lays:
+            lay.set_sm_budget(0, 0)
+        sts = [stream, stream]
+        for i in range(4):
+            two_step(i)
+        torch.cuda.synchronize(dev)
+        ta.record(stream)
+        for i in range(args.steps):
+            two_step(i)
+        tb.record(stream)
+        torch.cuda.synchronize(dev)
+        one_ms = max_over_ranks(ta.elapsed_time(tb), dist, dev)
+        for lay in lays:
+            lay.sync_status(stream)
+        two = {"value": job_throughput(shape.N, world, args.steps, two_ms), "unit": "tokens/s",
+               "ms_per_step": two_ms / args.steps, "route_ctas": rc, "ffn_ctas": fc,
+               "one_stream_ms_per_step": one_ms / args.steps,
+               "how": "two handles on two streams, batches alternating between them (two in flight); "
+                      "router and FFN CTA budgets from switch_set_sm_budget; no L2 flush (weights > L2); "
+                      "CUDA events around all steps"}
+        del lays, rr, yy
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -588,6 +652,8 @@ def run_gpu(args, shape):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if two is not None:
+        line["two_streams"] = two
     if not args.no_cpu_baseline and world == 1:
         x64, Wr64, br64 = host_f64(inp)
         cache = ExpertCache(lambda e: (inp["W1"][e], inp["W2"][e]))
@@ -613,6 +679,8 @@ def main():
     ap.add_argument("--ref-route-tokens", type=int, default=8192,
                     help="tokens the fp64 oracle routes per timed sample (the first ones of each group)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sm-budget", default="",
+                    help="R,F: also time two batches in flight on two streams, router CTAs <= R, FFN CTAs <= F")
     ap.add_argument("--train", action="store_true",
                     help="time a training step (forward in training mode + switch_backward)")
     ap.add_argument("--stage", default="layer", choices=["layer", "route"],

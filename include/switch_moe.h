@@ -194,6 +194,26 @@ SWITCH_API switch_status switch_route(switch_handle h, const void* x, const floa
 SWITCH_API switch_status switch_prepare_router(switch_handle h, const float* Wr, void* stream);
 
 /*
+ * Cap the CTAs of this handle's two persistent kernels, so that two handles working on two
+ * batches on two streams run side by side on disjoint SMs: the router (bound by the
+ * tensor cores) of one batch next to the expert FFN (bound by the weights' HBM bytes) of
+ * the other.  Both kernels hold about 200 KB of shared memory, so each CTA takes an SM of
+ * its own.
+ *   route_ctas: CTAs of the tensor-core router; raised to the fewest that keep its expert
+ *               slices waiting only on running CTAs (one cluster; one CTA per slice, or a
+ *               CTA pair per slice where pairs share the weight boxes).
+ *   ffn_ctas:   CTAs of the tensor-core expert FFN, at least 1 (2 where it runs on CTA pairs;
+ *               rounded down to an even count there).
+ * 0 restores the default (as many as the device holds).  Results do not depend on the caps:
+ * only which CTA computes which tile changes.  Applies to later forward calls on the handle
+ * (switch_route, switch_expert_ffn, switch_forward, switch_forward_host); the backward's
+ * kernels are not capped.
+ * Returns SWITCH_ERR_INVALID_ARG for a NULL handle or a negative cap.  Not an operation of the
+ * method: a scheduling knob of this library.
+ */
+SWITCH_API switch_status switch_set_sm_budget(switch_handle h, int route_ctas, int ffn_ctas);
+
+/*
  * Dispatch gather: xe[e, row_t, :] = x_t for every kept token t with expert e
  * (with SWITCH_FLAG_TOP2 also xe[expert2_t, row2_t, :] = x_t for kept second
  * choices); every other row of xe is zero.  xe is [E, G*C, d] act: expert e's block holds

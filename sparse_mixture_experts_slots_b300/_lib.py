@@ -73,6 +73,7 @@ SIGNATURES = {
     "switch_sync_status": (c_int, [c_void_p, c_void_p]),
     "switch_stage_ms": (c_int, [c_void_p, POINTER(c_float), c_int]),
     "switch_last_launch_count": (c_int, [c_void_p]),
+    "switch_set_sm_budget": (c_int, [c_void_p, c_int, c_int]),
     "switch_ep_regroup": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "switch_route_static": (c_int, [POINTER(SwitchConfig), c_void_p, c_void_p, c_void_p, POINTER(SwitchRouteOut),
                                     c_void_p]),

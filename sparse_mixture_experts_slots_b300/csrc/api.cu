@@ -73,6 +73,7 @@ struct switch_layer {
   int32_t* bw_rows_d; int32_t* bw_rows_F;
   uint32_t* bw_counters; int bw_counter_words;
   bool wsplit_ready;  // wsplit holds the pieces of the last router weights split on this handle
+  int route_ctas, ffn_ctas;  // CTA caps of the persistent router and FFN kernels (0: none)
   cudaEvent_t ev[6];
   bool have_events;
   int last_launches;
@@ -367,6 +368,7 @@ static switch_status route_args(switch_handle h, const void* x, const float* Wr,
   a->scan_partial = h->scan_partial;
   a->scan_counter = h->scan_counter;
   a->err = h->err;
+  a->max_ctas = h->route_ctas;
   a->expert = out->expert;
   a->slot = out->slot;
   a->keep = out->keep;
@@ -455,6 +457,7 @@ static switch_status run_ffn_tc(switch_handle h, const void* xe, const void* W1,
   L.d = c.d_model;
   L.F = c.d_ff;
   L.stall = (c.flags & SWITCH_FLAG_TEST_STALL) != 0;
+  L.max_ctas = h->ffn_ctas;
   // training keeps h for the backward
   L.discard_h = training_of(&c) ? 0 : (c.flags & SWITCH_FLAG_TEST_DISCARD) ? 2 : 1;
   const int n = launch_ffn_tc(L, s, pdl);
@@ -796,6 +799,13 @@ switch_status switch_stage_ms(switch_handle h, float* ms, int n) {
 }
 
 int switch_last_launch_count(switch_handle h) { return h ? h->last_launches : -1; }
+
+switch_status switch_set_sm_budget(switch_handle h, int route_ctas, int ffn_ctas) {
+  if (!h || route_ctas < 0 || ffn_ctas < 0) return SWITCH_ERR_INVALID_ARG;
+  h->route_ctas = route_ctas;
+  h->ffn_ctas = ffn_ctas;
+  return SWITCH_OK;
+}
 
 switch_status switch_ep_regroup(const void* src, void* dst, const int32_t* counts, int32_t* rows_out, int W, int El,
                                 int R, int row_bytes, int inverse, void* stream) {

@@ -935,7 +935,19 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   // behind a CTA's earlier tiles) is normally stored before anyone needs it.
   const int l2_blocks = L.mode >= 2 ? 0 : L.d / (FF_BM * t.MB);
   const int per_expert = t.NCH * (L.F / (FF_BM * t.MB) + l2_blocks);
-  const int ctas_max = device_sm_count();
+  // CTAs of the launch: one per SM (pairs: as many clusters as fit), or the caller's budget
+  const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
+  int ctas_max = device_sm_count();
+  if (pair) {
+    // the occupancy query sees the kernel's shared-memory limit, so it is set first
+    if (cudaFuncSetAttribute(ffn_persistent_kernel<2, 1, 0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return -1;
+    const int fit = 2 * ffn_pair_clusters(smem);
+    ctas_max = L.max_ctas > 0 && L.max_ctas < fit ? (L.max_ctas >= 2 ? L.max_ctas / 2 * 2 : 2) : fit;
+  } else if (L.max_ctas > 0 && L.max_ctas < ctas_max) {
+    ctas_max = L.max_ctas;
+  }
   p.LOOK = (8 * ctas_max + per_expert - 1) / per_expert;
   if (p.LOOK > L.E) p.LOOK = L.E;
   if (p.LOOK < 1) p.LOOK = 1;
@@ -958,7 +970,6 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   if (L.mode >= 2 && !L.out_f32) return -1;
   if (L.mode == 2 && t.BN % 64 != 0) return -1;
   p.w_evict_first = t.NCH == 1 ? 1 : 0;  // several chunks re-read a weight tile
-  const int smem = FF_RING + (int)sizeof(FfShared) + 1024;
   const long long tiles = (long long)L.E * t.NCH * (L.F / (FF_BM * t.MB) + l2_blocks);
   if (tiles >= (1ll << 31) || (long long)L.E * L.R >= (1ll << 31) || (long long)L.E * L.F >= (1ll << 31) ||
       (long long)L.E * L.d >= (1ll << 31))
@@ -966,14 +977,13 @@ int launch_ffn_tc(const FfnLaunch& L, cudaStream_t s, bool pdl) {
   cudaError_t e;
   if (pair) {
     auto kern = ffn_persistent_kernel<2, 1, 0, true>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-    const int fit = ffn_pair_clusters(smem);
+    const int fit = ctas_max / 2;
     const int pairs = (int)(tiles < fit ? tiles : fit);
     e = launch_k(kern, dim3((unsigned)(2 * pairs)), dim3(ff_threads<2>()), (size_t)smem, s, pdl, 2, tmW1, tmX, tmW2,
                  tmH, tmXp, tmHp, p);
     return e == cudaSuccess ? 1 : -1;
   }
-  const int ctas = (int)(tiles < device_sm_count() ? tiles : device_sm_count());
+  const int ctas = (int)(tiles < ctas_max ? tiles : ctas_max);
 #define SMOE_FFN(MBV, NBV, MK)                                                                                     \
   do {                                                                                                             \
     auto kern = ffn_persistent_kernel<MBV, NBV, MK>;                                                               \

@@ -79,6 +79,8 @@ struct RouteArgs {
   int32_t* raw2; int32_t* accepted2;
   int32_t* tile_hist2; // [G, nT, E]
   int32_t* tile_base2; // [G, nT, E]
+  int max_ctas;        // > 0: at most this many CTAs for the persistent tensor-core router (raised
+                       // to the fewest its slices need); 0: as many as fit on the device
 };
 
 // Batched strided product C_b(i, j) = sum_k A_b(i, k) B_b(j, k) (see backward.cu).
@@ -231,6 +233,7 @@ struct FfnLaunch {
   uint32_t* err;
   int E, R, d, F;
   bool stall;                // test only: layer-1 tile (expert 0, chunk 0, block 0) never publishes
+  int max_ctas;              // > 0: at most this many CTAs (at least one, or one pair); 0: one per SM
   int discard_h;             // mode 0, h not read after this launch (no training): 1 drop its lines
                              // from L2 once the last layer-2 tile of a chunk read them, where h
                              // outgrows half of L2 and the tiles keep two accumulator sets;

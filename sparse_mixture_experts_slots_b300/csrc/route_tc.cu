@@ -1005,6 +1005,14 @@ static cudaError_t rt_launch(int grid, int cluster, bool coop, bool pdl, cudaStr
 // one-CTA global variant from then on.
 static std::atomic<bool> g_rt_pair_refused[64];
 
+// CTAs resident at once, lowered to the caller's budget (> 0) but never below the fewest
+// that keep every wait of the kernel on running work (need: one cluster of Q; one CTA per
+// slice of a tile for the global exchange; a pair per slice for CTA pairs).
+static int rt_budget(int fit, int max_ctas, int need) {
+  if (max_ctas <= 0 || max_ctas >= fit) return fit;
+  return max_ctas > need ? max_ctas : (need < fit ? need : fit);
+}
+
 template <int EC, int NAX>
 static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmWh, const RouteArgs& a,
                      int nT, int Q, int32_t* rank, cudaStream_t s) {
@@ -1015,7 +1023,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
     if (a.top2) {  // top-2 in the router: one CTA per SM (no CTA pairs), slices of 64 or 128
       if constexpr ((EC == 64 || EC == 128) && NAX == 2) {
         const long long items = total * Q;
-        const int fit = rt_fit<EC, NAX, 1, true>(1);
+        const int fit = rt_budget(rt_fit<EC, NAX, 1, true>(1), a.max_ctas, Q);
         const int grid = (int)(items < fit ? items : fit);
         return rt_launch<EC, NAX, 1, true>(grid, 1, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank,
                                            x) == cudaSuccess
@@ -1029,7 +1037,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
       if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
       if (total >= 2 && !(dev >= 0 && dev < 64 && g_rt_pair_refused[dev].load(std::memory_order_relaxed))) {
         const long long pitems = (total + 1) / 2 * Q;
-        const int fit = rt_fit<EC, NAX, 2>(2) / 2;
+        const int fit = rt_budget(rt_fit<EC, NAX, 2>(2), a.max_ctas, 2 * Q) / 2;
         const int pairs = (int)(pitems < fit ? pitems : fit);
         if (rt_launch<EC, NAX, 2>(2 * pairs, 2, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank, x) ==
             cudaSuccess)
@@ -1039,7 +1047,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
       }
     }
     const long long items = total * Q;
-    const int fit = rt_fit<EC, NAX, 1>(1);
+    const int fit = rt_budget(rt_fit<EC, NAX, 1>(1), a.max_ctas, Q);
     const int grid = (int)(items < fit ? items : fit);
     return rt_launch<EC, NAX, 1>(grid, 1, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank, x) ==
                    cudaSuccess
@@ -1048,7 +1056,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
   }
   if (a.top2) {  // top-2 routing in the router (slices of at most 64 experts meeting in a cluster)
     if constexpr (EC <= 64 && NAX == 2) {
-      const int fit = rt_fit<EC, NAX, 0, true>(Q) / Q;
+      const int fit = rt_budget(rt_fit<EC, NAX, 0, true>(Q), a.max_ctas, Q) / Q;
       const int ncl = (int)(total < fit ? total : fit);
       return rt_launch<EC, NAX, 0, true>(Q * ncl, Q, false, true, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank,
                                          RtXchg{}) == cudaSuccess
@@ -1057,7 +1065,7 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
     }
     return -1;
   }
-  const int fit = rt_fit<EC, NAX, 0>(Q) / Q;
+  const int fit = rt_budget(rt_fit<EC, NAX, 0>(Q), a.max_ctas, Q) / Q;
   const int ncl = (int)(total < fit ? total : fit);
   return rt_launch<EC, NAX, 0>(Q * ncl, Q, false, true, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank, RtXchg{}) ==
                  cudaSuccess

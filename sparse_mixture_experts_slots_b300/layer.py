@@ -132,6 +132,11 @@ class SwitchMoE:
         """Split the router weights once (bfloat16 activations); later calls may pass Wr=None."""
         check(self.lib.switch_prepare_router(self._h, _ptr(Wr), _stream(stream)), "switch_prepare_router")
 
+    def set_sm_budget(self, route_ctas: int = 0, ffn_ctas: int = 0) -> None:
+        """Cap the CTAs of the persistent router and FFN kernels (0: as many as fit), so two
+        layers on two streams can run their router and FFN side by side on disjoint SMs."""
+        check(self.lib.switch_set_sm_budget(self._h, int(route_ctas), int(ffn_ctas)), "switch_set_sm_budget")
+
     def route(self, x, Wr, br=None, out: Optional[RouteResult] = None, stream=None) -> RouteResult:
         r = out or self.alloc_route()
         cs = r.c_struct()
