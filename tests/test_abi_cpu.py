@@ -103,6 +103,7 @@ def test_null_arguments_rejected(lib):
     assert lib.switch_forward(None, None, None, None, None, None, None, None, None, None, None, None) == 1
     assert lib.switch_create(None, None) == 1
     assert lib.switch_prepare_router(None, None, None) == 1
+    assert lib.switch_set_sm_budget(None, 0, 0) == 1
 
 
 def test_status_strings(lib):
