@@ -200,8 +200,10 @@ SWITCH_API switch_status switch_prepare_router(switch_handle h, const float* Wr,
  * the other.  Both kernels hold about 200 KB of shared memory, so each CTA takes an SM of
  * its own.
  *   route_ctas: CTAs of the tensor-core router; raised to the fewest that keep its expert
- *               slices waiting only on running CTAs (one cluster; one CTA per slice, or a
- *               CTA pair per slice where pairs share the weight boxes).
+ *               slices waiting only on running CTAs (one cluster, or one CTA per slice).
+ *               Routers whose slices meet in global memory then run as single CTAs, not
+ *               CTA pairs: a pair needs two free SMs at once, while the other stream's
+ *               kernels free them one at a time.
  *   ffn_ctas:   CTAs of the tensor-core expert FFN, at least 1 (2 where it runs on CTA pairs;
  *               rounded down to an even count there).
  * 0 restores the default (as many as the device holds).  Results do not depend on the caps:

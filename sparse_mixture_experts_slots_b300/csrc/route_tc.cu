@@ -1035,7 +1035,9 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
     if constexpr (EC == 256) {
       int dev = 0;
       if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-      if (total >= 2 && !(dev >= 0 && dev < 64 && g_rt_pair_refused[dev].load(std::memory_order_relaxed))) {
+      // (with a CTA budget: single CTAs, which fit on SMs that another kernel frees one at a time)
+      if (a.max_ctas == 0 && total >= 2 &&
+          !(dev >= 0 && dev < 64 && g_rt_pair_refused[dev].load(std::memory_order_relaxed))) {
         const long long pitems = (total + 1) / 2 * Q;
         const int fit = rt_budget(rt_fit<EC, NAX, 2>(2), a.max_ctas, 2 * Q) / 2;
         const int pairs = (int)(pitems < fit ? pitems : fit);

@@ -2,12 +2,13 @@
 
 A budget only changes which CTA computes which router item or FFN tile, so every output must
 equal the uncapped call's bit for bit.  The shapes cover each router exchange (one 2-CTA
-cluster per tile: 128 experts; slices meeting in global memory: 200 experts; CTA pairs
-sharing the W boxes: 1100 experts; top-2 in the router's pass) and both FFN tilings (one CTA
-per SM; CTA pairs of four weight blocks).  The smallest budgets are raised to what the
-kernels need (a CTA per router slice, a pair per slice, one FFN pair).  Then two handles
-with budgets run on two streams at once, as a caller overlapping two batches would, and
-each output must equal its own handle's uncapped result.
+cluster per tile: 128 experts; slices meeting in global memory: 200 experts; 1100 experts,
+whose uncapped router runs on CTA pairs sharing the W boxes and whose budgeted one runs as
+single CTAs; top-2 in the router's pass) and both FFN tilings (one CTA per SM; CTA pairs of
+four weight blocks).  The smallest budgets are raised to what the kernels need (a CTA per
+router slice, one FFN pair).  Then two handles with budgets run on two streams at once, as a
+caller overlapping two batches would, and each output must equal its own handle's uncapped
+result.
 """
 import pytest
 import torch
