@@ -7,7 +7,8 @@ cluster, CTAs meeting in global memory, CTA pairs above 1024 experts), 1 to 3 ro
 token tiles, capacity factors from 0.3 to 2.5 and capacity overrides, biases on and off, the
 residual on and off.  Each case runs the stages one by one and fused, and compares routing
 bit for bit (near ties as in parity.py), every logit, the dispatched rows, every expert's
-ungated rows and every token's output with the oracle.  Further draws run the top-2 layer
+ungated rows and every token's output with the oracle; the fused call then runs again under
+a randomly drawn CTA budget (switch_set_sm_budget) and must give the same bits.  Further draws run the top-2 layer
 (routing, dispatch and output of both choices) and the training backward (every gradient)
 against the oracle on smaller shapes.
 """
@@ -56,6 +57,24 @@ def draw_case(k: int, max_tokens: int = 2100, max_experts: int = 2048, max_width
     return shape, kw, resid
 
 
+ROUTE_FIELDS = ("expert", "slot", "keep", "gate", "row", "raw_count", "accepted_count", "P", "aux_loss",
+                "expert_rows", "logits")
+
+
+def _same_under_budget(layer, k, args, y_ref, r_ref, fields):
+    """The fused forward again under a CTA budget drawn for case k: bit-identical results."""
+    rs = np.random.RandomState(9300 + k)
+    rc, fc = int(rs.randint(1, 41)), int(rs.randint(1, 41))
+    layer.set_sm_budget(rc, fc)
+    y3, r3 = layer.forward(*args)
+    layer.sync_status()
+    torch.cuda.synchronize()
+    layer.set_sm_budget(0, 0)
+    assert torch.equal(y3, y_ref), f"budget ({rc}, {fc}): y differs"
+    for f in fields:
+        assert torch.equal(getattr(r3, f), getattr(r_ref, f)), f"budget ({rc}, {fc}): {f} differs"
+
+
 @pytest.mark.parametrize("k", range(N_CASES))
 def test_random_shape_against_oracle(k):
     shape, kw, resid = draw_case(k)
@@ -81,6 +100,7 @@ def test_random_shape_against_oracle(k):
     P.check_expert_rows(ye, ref, outs)
     P.check_y(y, ref, outs, tokens, resid=x if resid else None)
     assert torch.equal(y, y2), f"{shape}: forward differs from the stage-by-stage calls"
+    _same_under_budget(layer, k, (x, inp["Wr"], inp["br"], *w, x if resid else None), y2, r2, ROUTE_FIELDS)
 
 
 def test_draws_cover_the_paths():
@@ -120,6 +140,8 @@ def test_random_shape_top2_against_oracle(k):
     P.check_dispatch_top2(xe, x, ref)
     P.check_y_top2(y, ref, inp, np.arange(shape.N), resid=x if resid else None)
     assert torch.equal(y, y2), f"{shape}: forward differs from the stage-by-stage calls"
+    _same_under_budget(layer, 100 + k, (x, inp["Wr"], inp["br"], *w, x if resid else None), y2, r2,
+                       ROUTE_FIELDS + ("expert2", "slot2", "keep2", "gate2", "row2"))
 
 
 @pytest.mark.parametrize("k", range(N_BACKWARD))
