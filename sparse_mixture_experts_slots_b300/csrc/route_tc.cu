@@ -101,20 +101,29 @@ __global__ void router_split_kernel(const float* __restrict__ Wr, __nv_bfloat16*
 // ---------------------------------------------------------------- tiling
 // A W box holds MMA_N rows of the slice's pieces for one 64-column atom; MMA b takes box b.
 // Accumulators in TMEM per tile: one block of EC columns per piece (hi, mid, lo); with
-// EC = 256 the 512 columns hold hi and (mid + lo), one tile at a time.
-template <int EC>
+// EC = 256 the 512 columns hold hi and (mid + lo), one tile at a time, or (ONE) all three
+// pieces go into one block of 256 columns, so two tiles' sets fit and the MMAs of the next
+// tile need not wait for the epilogue.  ONE trades precision for that: the tensor cores'
+// float32 sums then take the small pieces' terms at the size of the whole logit, and the
+// largest logit error grows with d about 2.5 times (measured against float64: 8.0e-6 at
+// d = 1024, 6.5e-6 at d = 768, against 2.5e-6 at d = 768 with hi apart), so it is used only
+// where d <= 1024.
+template <int EC, bool ONE = false>
 struct RtGeom {
+  static_assert(!ONE || EC == 256, "one accumulator block: 256-expert slices");
   static constexpr int WROWS = 3 * EC;
   static constexpr int MMA_N = EC == 256 ? 256 : (WROWS <= 256 ? WROWS : 192);
   static constexpr int WBOXES = WROWS / MMA_N;
-  static constexpr int ACC_BLOCKS = EC == 256 ? 2 : 3;
+  static constexpr int ACC_BLOCKS = ONE ? 1 : EC == 256 ? 2 : 3;
   static constexpr int TILE_COLS = ACC_BLOCKS * EC;
   static constexpr int NBUF = 2 * TILE_COLS <= 512 ? 2 : 1;
   static constexpr int COLS = NBUF * TILE_COLS;
   static constexpr uint32_t TMEM_COLS = COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : COLS <= 256 ? 256 : 512;
   static constexpr int W_BOX = MMA_N * RT_BK * 2;
   // first TMEM column (within a tile's set) written by MMA b
-  static __device__ __forceinline__ uint32_t dcol(int b) { return EC == 256 ? (b == 0 ? 0u : 256u) : (uint32_t)(b * MMA_N); }
+  static __device__ __forceinline__ uint32_t dcol(int b) {
+    return ONE ? 0u : EC == 256 ? (b == 0 ? 0u : 256u) : (uint32_t)(b * MMA_N);
+  }
   static_assert(WROWS % MMA_N == 0 && MMA_N % 16 == 0 && MMA_N <= 256, "tcgen05 M=128 takes N = 16..256, step 16");
   static_assert(W_BOX % 1024 == 0, "every W box starts on a swizzle atom");
   static_assert(TILE_COLS <= 512, "a tile's accumulators fit in TMEM");
@@ -251,7 +260,8 @@ __device__ __forceinline__ void rt_epi_sync() { asm volatile("bar.sync 1, %0;" :
 // T2 (not with CTA pairs): top-2 routing in the same pass; expert2 / gate2 / rank2 / tile_hist2
 // take the second choices, gate / gate2 the softmax over the two chosen logits; with the
 // slices meeting in global memory each slice's second logit and expert go through xm2 / xa2.
-template <int EC, int NAX, int XM, bool T2 = false>
+// ONE (256-expert slices): the three pieces in one accumulator block (see RtGeom).
+template <int EC, int NAX, int XM, bool T2 = false, bool ONE = false>
 __global__ void __launch_bounds__(RT_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmWh, const float* __restrict__ br, int T, int E, int d, int nT, int Q, int total_tiles,
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   static_assert(!P2 || EC == 256, "CTA pairs split 256-row W boxes");
   static_assert(!T2 || XM <= 1, "top-2 routing in the router: slices meeting in a cluster or in global memory");
   using Cf = RtCfg<EC, NAX, P2>;
-  using Gm = RtGeom<EC>;
+  using Gm = RtGeom<EC, ONE>;
   constexpr int XS = Cf::XS, WS = Cf::WS, NBUF = Gm::NBUF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -425,7 +435,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
               const uint32_t wa = smem_u32(wring + ws * Cf::WB);
 #pragma unroll
               for (int kk = 0; kk < RT_BK / 16; ++kk) {
-                const bool first = k == 0 && kk == 0 && !(EC == 256 && b == 2);
+                const bool first = k == 0 && kk == 0 && !(EC == 256 && (ONE ? b > 0 : b == 2));
                 if (P2)
                   tc_mma_bf16_pair(acc + Gm::dcol(b), sw128_kmajor_desc(xa + kk * 32),
                                    sw128_kmajor_desc(wa + kk * 32), idesc, first ? 0u : 1u);
@@ -461,9 +471,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       else
         tc_commit(&bar.drain);
       if (!mbar_wait(&bar.drain, 0)) raise_error(err, ERR_TIMEOUT);
-      // (pairs) the last item's releases from the odd CTA have arrived before this CTA leaves
-      if (P2 && ok && lt >= 1 && !mbar_wait(&bar.aempty[(lt - 1) % NBUF], ((lt - 1) / NBUF) & 1))
-        raise_error(err, ERR_TIMEOUT);
+      // (pairs) the last items' releases from the odd CTA have arrived before this CTA leaves
+      if (P2 && ok)
+        for (int i = lt > NBUF ? lt - NBUF : 0; i < lt; ++i)
+          if (!mbar_wait(&bar.aempty[i % NBUF], (i / NBUF) & 1)) raise_error(err, ERR_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -524,7 +535,27 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         for (int ch = 0; ch < CPW / 8; ++ch) {
           const uint32_t col = (uint32_t)(cbeg + ch * 8);
           uint32_t h[8], r1[8], r2[8];
-          if (Gm::ACC_BLOCKS == 2 && (ch & 1) == 0) {  // two chunks' loads before one wait
+          if (Gm::ACC_BLOCKS == 1 && (ch & 3) == 0) {  // four chunks' loads before one wait
+            uint32_t h1[8], h2[8], h3[8];
+            tmem_ld8(trow + col, h);
+            tmem_ld8(trow + col + 8, h1);
+            tmem_ld8(trow + col + 16, h2);
+            tmem_ld8(trow + col + 24, h3);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              v[ch * 8 + 8 + j] = __uint_as_float(h1[j]);
+              v[ch * 8 + 16 + j] = __uint_as_float(h2[j]);
+              v[ch * 8 + 24 + j] = __uint_as_float(h3[j]);
+              r1[j] = 0u;
+            }
+          } else if (Gm::ACC_BLOCKS == 1) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              h[j] = __float_as_uint(v[ch * 8 + j]);
+              r1[j] = 0u;
+            }
+          } else if (Gm::ACC_BLOCKS == 2 && (ch & 1) == 0) {  // two chunks' loads before one wait
             uint32_t h2[8], q2[8];
             tmem_ld8(trow + col, h);
             tmem_ld8(trow + EC + col, r1);
@@ -550,8 +581,9 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int c = cbeg + ch * 8 + j;
-            const float corr = Gm::ACC_BLOCKS == 3 ? __uint_as_float(r1[j]) + __uint_as_float(r2[j])
-                                                    : __uint_as_float(r1[j]);
+            const float corr = Gm::ACC_BLOCKS == 3   ? __uint_as_float(r1[j]) + __uint_as_float(r2[j])
+                               : Gm::ACC_BLOCKS == 2 ? __uint_as_float(r1[j])
+                                                     : 0.f;
             const float z = (__uint_as_float(h[j]) + corr) + sh.bias[c];
             v[ch * 8 + j] = z;
             if (z > m) {  // padding experts: z = -inf
@@ -873,10 +905,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 // ---------------------------------------------------------------- host side
 // CTAs of router_tc_kernel<EC, NAX, XM> resident at once in clusters of cl CTAs (cached per
 // kernel, device and cluster size).
-template <int EC, int NAX, int XM, bool T2 = false>
+template <int EC, int NAX, int XM, bool T2 = false, bool ONE = false>
 static int rt_fit(int cl) {
   static std::atomic<int> cache[64][9];  // handles on several host threads may fill it
-  auto kern = router_tc_kernel<EC, NAX, XM, T2>;
+  auto kern = router_tc_kernel<EC, NAX, XM, T2, ONE>;
   constexpr int smem = rt_smem_bytes<EC, NAX, XM == 2, T2>();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -960,11 +992,11 @@ static RtXchg rt_xchg(void* base, long long tiles, int Q) {
   return x;
 }
 
-template <int EC, int NAX, int XM, bool T2 = false>
+template <int EC, int NAX, int XM, bool T2 = false, bool ONE = false>
 static cudaError_t rt_launch(int grid, int cluster, bool coop, bool pdl, cudaStream_t s, const CUtensorMap& tmX,
                              const CUtensorMap& tmW, const CUtensorMap& tmWh, const RouteArgs& a, int nT, int Q,
                              int total, int32_t* rank, const RtXchg& x) {
-  auto kern = router_tc_kernel<EC, NAX, XM, T2>;
+  auto kern = router_tc_kernel<EC, NAX, XM, T2, ONE>;
   constexpr int smem = rt_smem_bytes<EC, NAX, XM == 2, T2>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return cudaErrorInvalidValue;
@@ -1000,6 +1032,9 @@ static cudaError_t rt_launch(int grid, int cluster, bool coop, bool pdl, cudaStr
                             T2 ? a.tile_hist2 : nullptr, T2 && XM >= 1 ? x.m2 : nullptr,
                             T2 && XM >= 1 ? x.a2 : nullptr);
 }
+
+// Widest d for which 256-expert slices sum all three pieces in one accumulator block (RtGeom).
+constexpr int RT_ONE_ACC_MAX_D = 1024;
 
 // CTA pairs need a cooperative launch of 2-CTA clusters; a device that refuses it gets the
 // one-CTA global variant from then on.
@@ -1039,16 +1074,31 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
       if (a.max_ctas == 0 && total >= 2 &&
           !(dev >= 0 && dev < 64 && g_rt_pair_refused[dev].load(std::memory_order_relaxed))) {
         const long long pitems = (total + 1) / 2 * Q;
-        const int fit = rt_budget(rt_fit<EC, NAX, 2>(2), a.max_ctas, 2 * Q) / 2;
+        const int fit = rt_budget(a.d <= RT_ONE_ACC_MAX_D ? rt_fit<EC, NAX, 2, false, true>(2) : rt_fit<EC, NAX, 2>(2),
+                                  a.max_ctas, 2 * Q) /
+                        2;
         const int pairs = (int)(pitems < fit ? pitems : fit);
-        if (rt_launch<EC, NAX, 2>(2 * pairs, 2, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank, x) ==
-            cudaSuccess)
+        if ((a.d <= RT_ONE_ACC_MAX_D
+                 ? rt_launch<EC, NAX, 2, false, true>(2 * pairs, 2, true, false, s, tmX, tmW, tmWh, a, nT, Q,
+                                                      (int)total, rank, x)
+                 : rt_launch<EC, NAX, 2>(2 * pairs, 2, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank,
+                                         x)) == cudaSuccess)
           return 1;
         cudaGetLastError();
         if (dev >= 0 && dev < 64) g_rt_pair_refused[dev].store(true, std::memory_order_relaxed);
       }
     }
     const long long items = total * Q;
+    if constexpr (EC == 256) {
+      if (a.d <= RT_ONE_ACC_MAX_D) {
+        const int fit = rt_budget(rt_fit<EC, NAX, 1, false, true>(1), a.max_ctas, Q);
+        const int grid = (int)(items < fit ? items : fit);
+        return rt_launch<EC, NAX, 1, false, true>(grid, 1, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total,
+                                                  rank, x) == cudaSuccess
+                   ? 1
+                   : -1;
+      }
+    }
     const int fit = rt_budget(rt_fit<EC, NAX, 1>(1), a.max_ctas, Q);
     const int grid = (int)(items < fit ? items : fit);
     return rt_launch<EC, NAX, 1>(grid, 1, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank, x) ==
