@@ -167,7 +167,11 @@ SWITCH_API switch_status switch_destroy(switch_handle h);
  * Router + top-1 + slots + capacity mask + load statistics + aux loss.
  *   x   [N, d] act;  Wr [E, d] float32;  br [E] float32 or NULL (zero).
  * Logits are float32 (x cast up, then dot products with float32 accumulation);
- * ties go to the lowest expert index.  Writes every non-NULL field of *out
+ * ties go to the lowest expert index.  Measured against float64 dot products, the largest
+ * logit error is ~1.5e-7 with float32 activations (CUDA cores) and grows with d on the
+ * tensor-core path of bfloat16 activations: ~3.3e-9 d, or ~7.8e-9 d where more than 1024
+ * experts and d <= 1024 let the three weight pieces share one accumulator (6.5e-6 at d = 768).
+ * Writes every non-NULL field of *out
  * except probs/logits, which need their flags.  All fields other than
  * probs, logits and the z-loss are required, and with SWITCH_FLAG_TOP2 the
  * second-choice fields too.
