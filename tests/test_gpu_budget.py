@@ -98,3 +98,28 @@ def test_negative_budget_is_rejected():
         layer.set_sm_budget(-1, 0)
     with pytest.raises(Exception):
         layer.set_sm_budget(0, -2)
+
+
+def test_budgeted_forward_in_a_cuda_graph():
+    """A budgeted layer captured in a CUDA graph and replayed equals its eager calls."""
+    shape = LayerShape("budget-graph", 1, 1300, 128, 256, 1100, 1.0)
+    inp = make_inputs(shape, 52, "cuda", router_bias_std=0.1)
+    layer = P.make_layer(shape)
+    layer.set_sm_budget(24, 40)
+    ref = _run(layer, inp)
+    torch.cuda.synchronize()
+    rs = layer.alloc_route()
+    ys = torch.empty_like(inp["x"])
+    w = (inp["Wr"], inp["br"], inp["W1"], inp["b1"], inp["W2"], inp["b2"])
+    layer.forward(inp["x"], *w, r=rs, y=ys)  # warm the library's caches outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        layer.forward(inp["x"], *w, r=rs, y=ys)
+    for _ in range(3):
+        ys.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        _same((ys, rs), ref, FIELDS, "graph replay under a budget")
+    layer.sync_status()
+

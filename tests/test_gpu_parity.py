@@ -88,8 +88,9 @@ SMALL = {
     # first of group 1
     "gx-pair-groups": (LayerShape("gx-pair-groups", 2, 600, 128, 128, 1100, 1.0), dict(router_bias_std=0.1)),
     # d > 1024 with 256-expert slices: the hi piece in an accumulator of its own (up to
-    # d = 1024 all three pieces share one, two tiles' sets in TMEM)
+    # d = 1024 all three pieces share one, two tiles' sets in TMEM: the widest such case next)
     "gx-pair-wide": (LayerShape("gx-pair-wide", 1, 400, 1152, 128, 1100, 1.0), dict(router_bias_std=0.1)),
+    "gx-pair-1024": (LayerShape("gx-pair-1024", 1, 400, 1024, 128, 1100, 1.0), dict(router_bias_std=0.1)),
     # float32 rows of 49,408 bytes: too wide for the shared-memory row slots of the bulk-copy
     # dispatch and combine, so their register kernels run
     "wide-rows": (LayerShape("wide-rows", 1, 40, 12352, 32, 4, 1.0, dtype="f32"), dict(expert_bias_std=0.05)),
