@@ -49,7 +49,7 @@
 // Outputs per token: expert (raw choice), gate = p_{expert}, rank in tile; per
 // (group, tile, expert): token count and probability sum.  The cross-tile scan
 // that turns ranks into slots runs in route.cu.
-// Top-2 variant (T2, slices of up to 128 experts, clusters or the global exchange): the
+// Top-2 variant (T2, clusters or the global exchange; 256-expert slices as single CTAs): the
 // second-highest logit and its expert ride along through pass 1, the column-group merge and
 // the exchange ("混合专家", world.lapla.si/zh/moe, 路由器只开两条线: the two highest
 // scores, weighted by the softmax over those two); the outputs add the second choice, its
@@ -131,14 +131,15 @@ struct RtGeom {
 
 // NAX: 64-column atoms per x stage (2 when d % 128 == 0: one 3-D box of 256 bytes per row).
 // PAIR: a CTA pair shares every W box, each CTA holding half of its rows.
-template <int EC, int NAX, bool PAIR = false>
+// T2: with 256-expert slices the top-2 scratch takes the place of one W stage.
+template <int EC, int NAX, bool PAIR = false, bool T2 = false>
 struct RtCfg {
   using G = RtGeom<EC>;
   static constexpr int X_ATOM = RT_BM * RT_BK * 2;  // 16 KB
   static constexpr int X_STAGE = NAX * X_ATOM;
   static constexpr int XS = NAX == 2 ? 2 : 3;        // x stages
   static constexpr int WB = PAIR ? G::W_BOX / 2 : G::W_BOX;  // bytes of one W slot
-  static constexpr int WS_FIT = (RT_RING - XS * X_STAGE) / WB;
+  static constexpr int WS_FIT = (RT_RING - XS * X_STAGE) / WB - (T2 && EC == 256 ? 1 : 0);
   static constexpr int WS = WS_FIT < RT_MAX_WS ? WS_FIT : RT_MAX_WS;  // W stages
   static constexpr int X_BYTES = XS * X_STAGE;
   static constexpr int RING_BYTES = X_BYTES + WS * WB;
@@ -184,7 +185,7 @@ struct RtScratch {
 
 template <int EC, int NAX, bool PAIR = false, bool T2 = false>
 constexpr int rt_smem_bytes() {
-  using Cf = RtCfg<EC, NAX, PAIR>;
+  using Cf = RtCfg<EC, NAX, PAIR, T2>;
   return Cf::RING_BYTES + (int)sizeof(RtScratch<EC, T2>) + (int)sizeof(RtBars<Cf::XS, Cf::WS>) + 1024;
 }
 static_assert(rt_smem_bytes<256, 1>() <= 227 * 1024 && rt_smem_bytes<256, 2>() <= 227 * 1024 &&
@@ -192,7 +193,8 @@ static_assert(rt_smem_bytes<256, 1>() <= 227 * 1024 && rt_smem_bytes<256, 2>() <
                   rt_smem_bytes<64, 2>() <= 227 * 1024 && rt_smem_bytes<16, 1>() <= 227 * 1024 &&
                   rt_smem_bytes<256, 1, true>() <= 227 * 1024 && rt_smem_bytes<256, 2, true>() <= 227 * 1024,
               "rings and scratch fit in one SM's shared memory");
-static_assert(rt_smem_bytes<64, 2, false, true>() <= 227 * 1024 && rt_smem_bytes<128, 2, false, true>() <= 227 * 1024,
+static_assert(rt_smem_bytes<64, 2, false, true>() <= 227 * 1024 && rt_smem_bytes<128, 2, false, true>() <= 227 * 1024 &&
+                  rt_smem_bytes<256, 2, false, true>() <= 227 * 1024,
               "the top-2 scratch fits too (with two-atom x stages; d % 128 != 0 keeps the separate top-2 pass)");
 
 // Sum of p over the 32 lanes for 8 columns at once (reduce-scatter).  On return, lane L
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   constexpr bool GX = XM >= 1, P2 = XM == 2;
   static_assert(!P2 || EC == 256, "CTA pairs split 256-row W boxes");
   static_assert(!T2 || XM <= 1, "top-2 routing in the router: slices meeting in a cluster or in global memory");
-  using Cf = RtCfg<EC, NAX, P2>;
+  using Cf = RtCfg<EC, NAX, P2, T2>;
   using Gm = RtGeom<EC, ONE>;
   constexpr int XS = Cf::XS, WS = Cf::WS, NBUF = Gm::NBUF;
   extern __shared__ uint8_t smem_raw[];
@@ -963,7 +965,7 @@ static bool rt_global(int E) {
   return (E + EC - 1) / EC > 2;
 }
 bool router_tc_top2_fused(int E, int d) {
-  return E >= 2 && d % (2 * RT_BK) == 0 && router_tc_experts_per_cta(E) <= 128;
+  return E >= 2 && d % (2 * RT_BK) == 0;
 }
 
 size_t router_tc_exchange_bytes(long long tiles, int E, bool top2) {
@@ -1055,9 +1057,19 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
   if (total * Q >= (1ll << 31)) return -1;
   if (a.xchg && rt_global(a.E)) {
     const RtXchg x = rt_xchg(a.xchg, total, Q);
-    if (a.top2) {  // top-2 in the router: one CTA per SM (no CTA pairs), slices of 64 or 128
-      if constexpr ((EC == 64 || EC == 128) && NAX == 2) {
+    if (a.top2) {  // top-2 in the router: one CTA per SM (no CTA pairs), slices of 64 to 256
+      if constexpr ((EC == 64 || EC == 128 || EC == 256) && NAX == 2) {
         const long long items = total * Q;
+        if constexpr (EC == 256) {
+          if (a.d <= RT_ONE_ACC_MAX_D) {
+            const int fit = rt_budget(rt_fit<EC, NAX, 1, true, true>(1), a.max_ctas, Q);
+            const int grid = (int)(items < fit ? items : fit);
+            return rt_launch<EC, NAX, 1, true, true>(grid, 1, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total,
+                                                     rank, x) == cudaSuccess
+                       ? 1
+                       : -1;
+          }
+        }
         const int fit = rt_budget(rt_fit<EC, NAX, 1, true>(1), a.max_ctas, Q);
         const int grid = (int)(items < fit ? items : fit);
         return rt_launch<EC, NAX, 1, true>(grid, 1, true, false, s, tmX, tmW, tmWh, a, nT, Q, (int)total, rank,

@@ -5,8 +5,9 @@ its epoch in device memory (advanced by the last CTA of each launch), so a repla
 sees a fresh epoch every time.  Three expert counts cover the router's exchange modes:
 one 2-CTA cluster per tile (128 experts), one CTA per SM with the slices meeting in global
 memory (200 experts), and CTA pairs sharing each W box (1100 experts); the top-2 layer runs
-with both choices taken in the router's own pass (128 experts: one cluster per tile; 200: the
-slices meeting in global memory) and in a pass of its own over the float32 logits (1100).
+with both choices taken in the router's own pass (128 experts: one cluster per tile; 200 and
+1100: the slices meeting in global memory) and, with d = 192 (not a multiple of 128), in a
+pass of its own over the router's float32 logits.
 Replays alternate between two inputs; every output is compared bit for bit with an eager
 call on the same inputs (the same kernels in the same order).
 """
@@ -33,10 +34,11 @@ def _snapshot(y, r, fields):
     return y.clone(), {f: getattr(r, f).clone() for f in fields}
 
 
-@pytest.mark.parametrize("E,k", [(128, 1), (200, 1), (1100, 1), (128, 2), (200, 2), (1100, 2)])
-def test_graph_replay_equals_eager(E, k):
+@pytest.mark.parametrize("E,k,d", [(128, 1, 128), (200, 1, 128), (1100, 1, 128), (128, 2, 128), (200, 2, 128),
+                                   (1100, 2, 128), (300, 2, 192)])
+def test_graph_replay_equals_eager(E, k, d):
     fields = FIELDS_TOP2 if k == 2 else FIELDS
-    shape = LayerShape(f"graph-e{E}-top{k}", 1, 900, 128, 128, E, 1.0)
+    shape = LayerShape(f"graph-e{E}-top{k}-d{d}", 1, 900, d, 128, E, 1.0)
     a = make_inputs(shape, 3, "cuda", router_bias_std=0.1)
     b = make_inputs(shape, 4, "cuda", router_bias_std=0.1)
     layer = P.make_layer(shape, top_k=k)

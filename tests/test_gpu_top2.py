@@ -41,6 +41,11 @@ CASES = {
     "top2-global": (LayerShape("top2-global", 2, 700, 256, 256, 512, 1.0), dict(router_bias_std=0.2)),
     # the same with 128-expert slices (700 experts: 6 slices, the last partly padding)
     "top2-global-128": (LayerShape("top2-global-128", 1, 900, 256, 256, 700, 1.0), dict(router_bias_std=0.2)),
+    # 256-expert slices (1100 experts: 5 slices, the last partly padding): the three weight
+    # pieces in one accumulator block (d <= 1024), and with d > 1024 the hi piece apart
+    "top2-global-256": (LayerShape("top2-global-256", 2, 700, 256, 256, 1100, 1.0), dict(router_bias_std=0.2)),
+    "top2-global-256-wide": (LayerShape("top2-global-256-wide", 1, 400, 1152, 128, 1100, 1.0),
+                             dict(router_bias_std=0.2)),
 }
 
 
@@ -97,21 +102,22 @@ def test_top2_switch_base_full_size():
     P.check_y_top2(y, ref, inp, tokens)
 
 
-@pytest.mark.parametrize("E", [100, 200])
+@pytest.mark.parametrize("E", [100, 200, 1100])
 def test_top2_exact_ties_across_slices(E):
     # Router rows duplicated within one 64-expert slice (5 -> 6) and across slices (3 -> 70
-    # -> 140 where they exist): identical logits, so both choices follow the lowest-index rule
-    # through the column-group and slice merges (100 experts: a 2-CTA cluster; 200: slices
-    # meeting in global memory).  A shift on expert 3 makes it the usual winner.
+    # -> 140 -> 300 where they exist): identical logits, so both choices follow the
+    # lowest-index rule through the column-group and slice merges (100 experts: a 2-CTA
+    # cluster; 200: slices of 64 meeting in global memory; 1100: slices of 256, expert 300 in
+    # the second).  A shift on expert 3 makes it the usual winner.
     shape = LayerShape(f"top2-ties-e{E}", 2, 300, 128, 128, E, 1.0)
     inp = make_inputs(shape, 21, "cuda")
     Wr = inp["Wr"]
-    for dst in (70, 140):
+    for dst in (70, 140, 300):
         if dst < E:
             Wr[dst].copy_(Wr[3])
     Wr[6].copy_(Wr[5])
     br = torch.zeros(E, dtype=torch.float32, device="cuda")
-    for e in (3, 70, 140):
+    for e in (3, 70, 140, 300):
         if e < E:
             br[e] = 0.5
     inp["br"] = br
