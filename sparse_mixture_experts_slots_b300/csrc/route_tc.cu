@@ -49,7 +49,7 @@
 // Outputs per token: expert (raw choice), gate = p_{expert}, rank in tile; per
 // (group, tile, expert): token count and probability sum.  The cross-tile scan
 // that turns ranks into slots runs in route.cu.
-// Top-2 variant (T2, clusters or the global exchange; 256-expert slices as single CTAs): the
+// Top-2 variant (T2, clusters or the global exchange, CTA pairs for 256-expert slices): the
 // second-highest logit and its expert ride along through pass 1, the column-group merge and
 // the exchange ("混合专家", world.lapla.si/zh/moe, 路由器只开两条线: the two highest
 // scores, weighted by the softmax over those two); the outputs add the second choice, its
@@ -194,7 +194,7 @@ static_assert(rt_smem_bytes<256, 1>() <= 227 * 1024 && rt_smem_bytes<256, 2>() <
                   rt_smem_bytes<256, 1, true>() <= 227 * 1024 && rt_smem_bytes<256, 2, true>() <= 227 * 1024,
               "rings and scratch fit in one SM's shared memory");
 static_assert(rt_smem_bytes<64, 2, false, true>() <= 227 * 1024 && rt_smem_bytes<128, 2, false, true>() <= 227 * 1024 &&
-                  rt_smem_bytes<256, 2, false, true>() <= 227 * 1024,
+                  rt_smem_bytes<256, 2, false, true>() <= 227 * 1024 && rt_smem_bytes<256, 2, true, true>() <= 227 * 1024,
               "the top-2 scratch fits too (with two-atom x stages; d % 128 != 0 keeps the separate top-2 pass)");
 
 // Sum of p over the 32 lanes for 8 columns at once (reduce-scatter).  On return, lane L
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
                      int32_t* __restrict__ tile_hist2, float* __restrict__ xm2, int* __restrict__ xa2) {
   constexpr bool GX = XM >= 1, P2 = XM == 2;
   static_assert(!P2 || EC == 256, "CTA pairs split 256-row W boxes");
-  static_assert(!T2 || XM <= 1, "top-2 routing in the router: slices meeting in a cluster or in global memory");
+  static_assert(!T2 || XM <= 1 || EC == 256, "top-2 routing on CTA pairs: 256-expert slices");
   using Cf = RtCfg<EC, NAX, P2, T2>;
   using Gm = RtGeom<EC, ONE>;
   constexpr int XS = Cf::XS, WS = Cf::WS, NBUF = Gm::NBUF;
@@ -1057,10 +1057,26 @@ static int launch_rt(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUten
   if (total * Q >= (1ll << 31)) return -1;
   if (a.xchg && rt_global(a.E)) {
     const RtXchg x = rt_xchg(a.xchg, total, Q);
-    if (a.top2) {  // top-2 in the router: one CTA per SM (no CTA pairs), slices of 64 to 256
+    if (a.top2) {  // top-2 in the router: slices of 64 to 256 (256: CTA pairs when they run)
       if constexpr ((EC == 64 || EC == 128 || EC == 256) && NAX == 2) {
         const long long items = total * Q;
         if constexpr (EC == 256) {
+          int dev = 0;
+          if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+          if (a.max_ctas == 0 && total >= 2 &&
+              !(dev >= 0 && dev < 64 && g_rt_pair_refused[dev].load(std::memory_order_relaxed))) {
+            const bool one = a.d <= RT_ONE_ACC_MAX_D;
+            const long long pitems = (total + 1) / 2 * Q;
+            const int pfit = (one ? rt_fit<EC, NAX, 2, true, true>(2) : rt_fit<EC, NAX, 2, true>(2)) / 2;
+            const int pairs = (int)(pitems < pfit ? pitems : pfit);
+            if ((one ? rt_launch<EC, NAX, 2, true, true>(2 * pairs, 2, true, false, s, tmX, tmW, tmWh, a, nT, Q,
+                                                         (int)total, rank, x)
+                     : rt_launch<EC, NAX, 2, true>(2 * pairs, 2, true, false, s, tmX, tmW, tmWh, a, nT, Q,
+                                                   (int)total, rank, x)) == cudaSuccess)
+              return 1;
+            cudaGetLastError();
+            if (dev >= 0 && dev < 64) g_rt_pair_refused[dev].store(true, std::memory_order_relaxed);
+          }
           if (a.d <= RT_ONE_ACC_MAX_D) {
             const int fit = rt_budget(rt_fit<EC, NAX, 1, true, true>(1), a.max_ctas, Q);
             const int grid = (int)(items < fit ? items : fit);
